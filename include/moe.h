@@ -1,0 +1,152 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) single-GPU Mixture-of-Experts layer.
+ *
+ * The layer: router logits -> top-k expert selection -> token dispatch ->
+ * per-expert SwiGLU FFN -> weighted combine, its backward pass, and a
+ * small-batch decode path.
+ *
+ * What it follows. "Cursor открыл код ядра Mixture of Experts: обучение MoE
+ * ускоряется до 2,37 раза" (dzen.guru), section "Что именно тормозило обучение
+ * MoE-моделей?": every MoE layer routes each token to experts, runs the
+ * experts, and gathers the results back; section "Три решения, которые дали
+ * результат": receivers pull the tokens they need (pull dispatch), results are
+ * pushed back (push combine), no CPU in the loop, no dropped tokens, a fixed
+ * ring buffer walked in reverse in the backward pass, one deterministic GPU
+ * call, BF16 and MXFP8. "Cursor a réécrit le décodage de MoE" (toolnavs.com),
+ * sections "Cursor a réécrit le décodage de MoE" and "1.84x plus de vitesse
+ * ...": small-batch decode where each warp owns one output value, the whole
+ * layer in two kernels, output closer to an FP32 reference.
+ * The pages give no formulas. The layer computed here:
+ *   l = x Wr^T (fp32)                       key = l + b (fp32, selection only)
+ *   idx[t, 0..k-1] = the k largest keys, largest first, ties to the lower expert
+ *   gate: softmax of the selected logits (renorm) or of all E (taken at idx),
+ *         or route_scale * sigmoid(l) / sum over selected (renorm) or without /sum
+ *   y_t = shared(x_t) + sum_{j=0}^{k-1} gate[t, j] * FFN_{idx[t, j]}(x_t)
+ *   FFN_e(x) = (silu(x Wg[e]^T) * (x Wu[e]^T)) Wd[e]^T, shared expert = slot E.
+ *
+ * Conventions for every call:
+ *  - Pointers named "device" must be device memory; the caller owns all of it.
+ *    The library never allocates device memory except the small status word in
+ *    moe_create. Scratch comes from the caller's `workspace` (sizes from
+ *    moe_workspace_size), 256-byte aligned.
+ *  - Every compute call only enqueues work on `stream` (a cudaStream_t passed
+ *    as void*; NULL = legacy default stream) and never synchronises the host.
+ *  - Arguments are validated on the host first; a bad argument returns an
+ *    error code and launches nothing. Launch failures return MOE_ERR_CUDA.
+ *    Errors detected on the device (an index out of range, a pipeline wait
+ *    that timed out) are written to the handle's device status word; read it
+ *    with moe_get_status (the only call that synchronises).
+ *  - Row-major layouts. "bf16" storage means IEEE bfloat16 (uint16 bit
+ *    patterns); fp32 storage for the MOE_FP32 precision.
+ *  - A handle may be used from one stream at a time.
+ *  - Results are bit-identical between runs for identical inputs (no floating
+ *    point atomics; every sum has a fixed order).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moe_handle_s* moe_handle;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null pointer, size out of range, k > E, ... */
+  MOE_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement (shape multiple, precision) */
+  MOE_ERR_WORKSPACE = 3,     /* workspace or context smaller than required / misaligned */
+  MOE_ERR_CUDA = 4,          /* a CUDA runtime call failed */
+  MOE_ERR_TIMEOUT = 5,       /* device status: a pipeline wait exceeded its limit */
+  MOE_ERR_DEVICE_INDEX = 6,  /* device status: an index read on the device was out of range */
+  MOE_ERR_NO_WEIGHTS = 7     /* compute call before moe_set_weights */
+} moe_status;
+
+typedef enum { MOE_ROUTER_SOFTMAX = 0, MOE_ROUTER_SIGMOID = 1 } moe_router_kind;
+typedef enum { MOE_FP32 = 0, MOE_BF16 = 1, MOE_MXFP8 = 2 } moe_precision;
+
+typedef struct {
+  int T_max;          /* largest token count any call will pass */
+  int d;              /* hidden size */
+  int E;              /* routed experts, 1..256 */
+  int n_shared;       /* shared experts: 0 or 1 (stored as expert slot E) */
+  int f;              /* SwiGLU intermediate width */
+  int k;              /* experts per token, 1..min(E, 8) */
+  int router;         /* moe_router_kind */
+  int renorm;         /* 1: renormalise gates over the k selected experts */
+  float route_scale;  /* multiplies the routed gates (1 for a plain softmax router) */
+  int prec;           /* moe_precision of activations, weights and outputs */
+  int chunk_tokens;   /* tokens per chunk of moe_train_chunked (0: whole batch) */
+  size_t ring_bytes;  /* bytes of saved activations moe_train_chunked may keep */
+} moe_config;
+
+/* Create a handle for one layer shape on the current CUDA device. Validates
+ * the config (MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED) and allocates the
+ * device status word (the library's only allocation). */
+moe_status moe_create(const moe_config* cfg, moe_handle* out);
+moe_status moe_destroy(moe_handle h);
+
+/* Bytes the caller must provide, for T tokens (T <= T_max):
+ *   fwd_ws:   workspace of moe_forward / moe_route / moe_decode
+ *   ctx:      activations saved by a training forward for moe_backward
+ *   bwd_ws:   workspace of moe_backward
+ *   packed:   packed weight buffer of moe_set_weights (independent of T)
+ * Any output pointer may be NULL. */
+moe_status moe_workspace_size(moe_handle h, int T, size_t* fwd_ws, size_t* ctx, size_t* bwd_ws,
+                              size_t* packed);
+
+/* Pack the layer's weights (device pointers, storage type of cfg.prec; bf16
+ * for MXFP8) into the caller-owned device buffer `packed`:
+ *   Wr [E, d]   router weight           bias [E] fp32 selection bias (NULL: zeros)
+ *   Wg [E+S, f, d], Wu [E+S, f, d]      gate / up projections, rows = outputs
+ *   Wd [E+S, d, f]                      down projection
+ * Enqueued on `stream`; the source buffers may be freed once it has run. The
+ * handle keeps `packed` and uses it in every later call: it must stay
+ * allocated and unmodified. */
+moe_status moe_set_weights(moe_handle h, const void* Wr, const float* bias, const void* Wg,
+                           const void* Wu, const void* Wd, void* packed, void* stream);
+
+/* Route T tokens x [T, d] (device). Writes (device, caller-owned):
+ *   idx [T, k] int32, gate [T, k] fp32, cnt [E] int32, off [E+1] int32 (exclusive
+ *   prefix of cnt), perm [T*k] int32 (sorted position -> assignment t*k+j, sorted
+ *   by (expert, assignment)), inv [T*k] int32 (perm^-1), logits [T, E] fp32.
+ * logits_override (nullable, device [T, E] fp32): route these logits instead of
+ * computing x Wr^T (x may then be NULL). Any output may be NULL except logits
+ * when logits_override is NULL. Uses `workspace` (fwd_ws bytes). */
+moe_status moe_route(moe_handle h, const void* x, int T, const float* logits_override,
+                     float* logits, int32_t* idx, float* gate, int32_t* cnt, int32_t* off,
+                     int32_t* perm, int32_t* inv, void* workspace, void* stream);
+
+/* Forward: y [T, d] = layer(x [T, d]) (device, storage type of cfg.prec; bf16
+ * for MXFP8). ctx (nullable): when given (ctx bytes), the routing and the
+ * expert pre-activations are saved there for moe_backward (training); NULL for
+ * inference. */
+moe_status moe_forward(moe_handle h, const void* x, int T, void* y, void* ctx, void* workspace,
+                       void* stream);
+
+/* Backward of the forward that filled ctx with the same x and T. dy [T, d] is
+ * dL/dy. Writes (not accumulates) dx [T, d], dWr [E, d] fp32, and dWg, dWu
+ * [E+S, f, d], dWd [E+S, d, f] in the storage type (fp32 for MOE_FP32, else
+ * bf16). The selection bias gets no gradient. */
+moe_status moe_backward(moe_handle h, const void* x, const void* dy, int T, const void* ctx,
+                        void* dx, float* dWr, void* dWg, void* dWu, void* dWd, void* workspace,
+                        void* stream);
+
+/* Small-batch decode: y [B, d] bf16 = layer(x [B, d] bf16), 1 <= B <= 64,
+ * cfg.prec == MOE_BF16. Warp-per-output kernels with fp32 intermediates. */
+moe_status moe_decode(moe_handle h, const void* x, int B, void* y, void* workspace, void* stream);
+
+/* Wait for the handle's queued work on `stream`, then read and clear the
+ * device status word into *device_status (MOE_OK if no device error). */
+moe_status moe_get_status(moe_handle h, void* stream, int* device_status);
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,329 @@
+// Host side of the C ABI declared in include/moe.h: validation, workspace
+// carving and the launch sequence of each call. Every call only enqueues work
+// on the caller's stream; nothing here waits for the device except
+// moe_get_status.
+#include <cmath>
+#include <cstring>
+#include <new>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace moe;
+
+struct moe_handle_s {
+  moe_config cfg;
+  Layer L;
+  int device;
+  bool tc;   // bf16 tensor-core path available for this shape
+};
+
+namespace {
+
+inline size_t al(size_t v) { return (v + 255) & ~size_t(255); }
+
+struct Sizes {
+  size_t route, uv, fwd_scratch, ctx, fwd_ws, bwd_ws, packed;
+};
+
+Sizes sizes_for(const Layer& L, int T) {
+  const size_t A = (size_t)T * L.k, nseg = L.E + L.S, R = A + (size_t)L.S * T;
+  const size_t eb = elem_bytes(L.prec);
+  const size_t nch = (A + kChunk - 1) / kChunk;
+  Sizes z;
+  z.route = al(4 * T * (size_t)L.E) + 2 * al(4 * A) + 3 * al(4 * (nseg + 1)) + 2 * al(4 * A) + 2 * al(4 * R);
+  z.uv = al(eb * R * 2 * L.f);
+  z.fwd_scratch = 2 * al(4 * nch * L.E) + al(eb * R * L.f) + al(eb * R * L.d);
+  z.ctx = z.route + z.uv;
+  z.fwd_ws = z.route + z.fwd_scratch;
+  if (L.prec == MOE_BF16) {
+    const size_t dec = decode_workspace_bytes(L, T < kMaxDecodeB ? T : kMaxDecodeB);
+    if (dec > z.fwd_ws) z.fwd_ws = dec;
+  }
+  z.bwd_ws = al(eb * R * 2 * L.f) + al(eb * R * L.f) + al(4 * A * (L.f / 64)) + al(eb * R * L.d) +
+             al(4 * T * (size_t)L.E) + al(4 * A);
+  z.packed = al(eb * nseg * 2 * L.f * L.d) + al(eb * nseg * L.d * L.f) + al(eb * L.E * L.d) + al(4 * L.E);
+  return z;
+}
+
+// Routing arrays at p (in context or workspace order); returns the end.
+char* carve_route(Bufs& B, const Layer& L, char* p) {
+  const size_t nseg = L.E + L.S;
+  B.logits = (float*)p; p += al(4 * (size_t)B.T * L.E);
+  B.idx = (int*)p; p += al(4 * (size_t)B.A);
+  B.gate = (float*)p; p += al(4 * (size_t)B.A);
+  B.cnt = (int*)p; p += al(4 * (nseg + 1));
+  B.off = (int*)p; p += al(4 * (nseg + 1));
+  B.mt_off = (int*)p; p += al(4 * (nseg + 1));
+  B.perm = (int*)p; p += al(4 * (size_t)B.A);
+  B.inv = (int*)p; p += al(4 * (size_t)B.A);
+  B.row_token = (int*)p; p += al(4 * (size_t)B.R);
+  B.row_gate = (float*)p; p += al(4 * (size_t)B.R);
+  return p;
+}
+
+Bufs carve(const Layer& L, int T, void* ws, const void* ctx, void* bws) {
+  Bufs B;
+  std::memset(&B, 0, sizeof(B));
+  B.T = T;
+  B.A = T * L.k;
+  B.R = B.A + L.S * T;
+  B.nch = (B.A + kChunk - 1) / kChunk;
+  const size_t eb = elem_bytes(L.prec);
+  char* w = (char*)ws;
+  if (ctx) {
+    char* c = carve_route(B, L, (char*)ctx);
+    B.uv = c;
+  } else if (w) {
+    w = carve_route(B, L, w);
+  }
+  if (w) {
+    B.chunk_hist = (int*)w; w += al(4 * (size_t)B.nch * L.E);
+    B.chunk_base = (int*)w; w += al(4 * (size_t)B.nch * L.E);
+    B.h = w; w += al(eb * B.R * L.f);
+    B.o = w; w += al(eb * B.R * L.d);
+  }
+  if (bws) {
+    char* b = (char*)bws;
+    B.dudv = b; b += al(eb * B.R * 2 * L.f);
+    B.hg = b; b += al(eb * B.R * L.f);
+    B.dg_part = (float*)b; b += al(4 * (size_t)B.A * (L.f / 64));
+    B.dx_rows = b; b += al(eb * B.R * L.d);
+    B.dl = (float*)b; b += al(4 * (size_t)B.T * L.E);
+    B.dgate = (float*)b; b += al(4 * (size_t)B.A);
+  }
+  return B;
+}
+
+inline bool aligned256(const void* p) { return ((uintptr_t)p & 255) == 0; }
+inline bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+#define CK(expr)                                  \
+  do {                                            \
+    if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+
+moe_status check_T(const moe_handle_s* h, int T) {
+  if (T < 0 || T > h->cfg.T_max) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+// router logits, top-k, counts, offsets, permutation
+moe_status run_route(const moe_handle_s* h, const Bufs& B, const void* x, const float* logits_override,
+                     cudaStream_t s) {
+  const Layer& L = h->L;
+  const float* lg = B.logits;
+  if (logits_override) {
+    lg = logits_override;
+  } else if (h->tc) {
+    CK(launch_tc_router_logits(L, x, B.T, B.logits, s));
+  } else {
+    CK(launch_router_logits(L, x, B.T, B.logits, s));
+  }
+  CK(launch_topk(L, lg, B.T, B.idx, B.gate, s));
+  CK(launch_scan_permute(L, B, s));
+  if (logits_override && lg != B.logits)
+    CK(cudaMemcpyAsync(B.logits, lg, sizeof(float) * (size_t)B.T * L.E, cudaMemcpyDeviceToDevice, s));
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(int st) {
+  switch (st) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape or precision";
+    case MOE_ERR_WORKSPACE: return "workspace or context too small or misaligned";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_DEVICE_INDEX: return "device index out of range";
+    case MOE_ERR_NO_WEIGHTS: return "weights not set";
+    default: return "unknown status";
+  }
+}
+
+moe_status moe_create(const moe_config* cfg, moe_handle* out) {
+  if (!cfg || !out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  const moe_config& c = *cfg;
+  if (c.T_max < 1 || c.d < 1 || c.E < 1 || c.f < 1 || c.k < 1 || c.k > c.E || c.k > kMaxK ||
+      (c.n_shared != 0 && c.n_shared != 1) || (c.router != MOE_ROUTER_SOFTMAX && c.router != MOE_ROUTER_SIGMOID) ||
+      (c.prec != MOE_FP32 && c.prec != MOE_BF16 && c.prec != MOE_MXFP8) || !std::isfinite(c.route_scale) ||
+      c.route_scale <= 0.f || c.chunk_tokens < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c.E > kMaxE || c.f % 64 != 0 || c.d % 8 != 0 || c.prec == MOE_MXFP8 ||
+      (long)c.T_max * c.k >= (1L << 30))
+    return MOE_ERR_UNSUPPORTED;
+  moe_handle_s* h = new (std::nothrow) moe_handle_s();
+  if (!h) return MOE_ERR_INVALID_ARG;
+  h->cfg = c;
+  Layer& L = h->L;
+  L.d = c.d; L.E = c.E; L.S = c.n_shared; L.f = c.f; L.k = c.k;
+  L.router = c.router; L.renorm = c.renorm ? 1 : 0; L.prec = c.prec; L.scale = c.route_scale;
+  L.G = (c.f % kGate == 0) ? kGate : 64;
+  L.has_weights = false;
+  if (cudaGetDevice(&h->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&L.num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
+    delete h;
+    return MOE_ERR_CUDA;
+  }
+  int* words = nullptr;
+  if (cudaMalloc(&words, 256) != cudaSuccess || cudaMemset(words, 0, 256) != cudaSuccess) {
+    if (words) cudaFree(words);
+    delete h;
+    return MOE_ERR_CUDA;
+  }
+  L.status = words;
+  L.decode_counter = words + 32;
+  h->tc = (c.prec == MOE_BF16) && tc_supported(L);
+  *out = h;
+  return MOE_OK;
+}
+
+moe_status moe_destroy(moe_handle h) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  cudaFree(h->L.status);
+  delete h;
+  return MOE_OK;
+}
+
+moe_status moe_workspace_size(moe_handle h, int T, size_t* fwd_ws, size_t* ctx, size_t* bwd_ws, size_t* packed) {
+  if (!h || T < 0) return MOE_ERR_INVALID_ARG;
+  const Sizes z = sizes_for(h->L, T);
+  if (fwd_ws) *fwd_ws = z.fwd_ws;
+  if (ctx) *ctx = z.ctx;
+  if (bwd_ws) *bwd_ws = z.bwd_ws;
+  if (packed) *packed = z.packed;
+  return MOE_OK;
+}
+
+moe_status moe_set_weights(moe_handle h, const void* Wr, const float* bias, const void* Wg, const void* Wu,
+                           const void* Wd, void* packed, void* stream) {
+  if (!h || !Wr || !Wg || !Wu || !Wd || !packed) return MOE_ERR_INVALID_ARG;
+  if (!aligned256(packed)) return MOE_ERR_WORKSPACE;
+  if (!aligned16(Wr) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd)) return MOE_ERR_INVALID_ARG;
+  Layer& L = h->L;
+  const size_t eb = elem_bytes(L.prec);
+  const size_t nseg = L.E + L.S;
+  char* p = (char*)packed;
+  L.W13 = p; p += al(eb * nseg * 2 * L.f * L.d);
+  L.Wd = p; p += al(eb * nseg * L.d * L.f);
+  L.Wr = p; p += al(eb * L.E * L.d);
+  L.bias = (float*)p;
+  cudaStream_t s = (cudaStream_t)stream;
+  CK(launch_pack_weights(L, Wr, bias, Wg, Wu, Wd, s));
+  if (h->tc) CK(tc_init(L));
+  L.has_weights = true;
+  return MOE_OK;
+}
+
+moe_status moe_route(moe_handle h, const void* x, int T, const float* logits_override, float* logits, int32_t* idx,
+                     float* gate, int32_t* cnt, int32_t* off, int32_t* perm, int32_t* inv, void* workspace,
+                     void* stream) {
+  if (!h || !workspace) return MOE_ERR_INVALID_ARG;
+  if (check_T(h, T) != MOE_OK) return MOE_ERR_INVALID_ARG;
+  if (!logits_override && (!x || !logits)) return MOE_ERR_INVALID_ARG;
+  if (!h->L.has_weights) return MOE_ERR_NO_WEIGHTS;
+  if (!aligned256(workspace)) return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+  const Layer& L = h->L;
+  cudaStream_t s = (cudaStream_t)stream;
+  Bufs B = carve(L, T, workspace, nullptr, nullptr);
+  moe_status st = run_route(h, B, x, logits_override, s);
+  if (st != MOE_OK) return st;
+  const size_t A = (size_t)T * L.k;
+  if (logits) CK(cudaMemcpyAsync(logits, B.logits, 4 * (size_t)T * L.E, cudaMemcpyDeviceToDevice, s));
+  if (idx) CK(cudaMemcpyAsync(idx, B.idx, 4 * A, cudaMemcpyDeviceToDevice, s));
+  if (gate) CK(cudaMemcpyAsync(gate, B.gate, 4 * A, cudaMemcpyDeviceToDevice, s));
+  if (cnt) CK(cudaMemcpyAsync(cnt, B.cnt, 4 * (size_t)L.E, cudaMemcpyDeviceToDevice, s));
+  if (off) CK(cudaMemcpyAsync(off, B.off, 4 * (size_t)(L.E + 1), cudaMemcpyDeviceToDevice, s));
+  if (perm) CK(cudaMemcpyAsync(perm, B.perm, 4 * A, cudaMemcpyDeviceToDevice, s));
+  if (inv) CK(cudaMemcpyAsync(inv, B.inv, 4 * A, cudaMemcpyDeviceToDevice, s));
+  return MOE_OK;
+}
+
+moe_status moe_forward(moe_handle h, const void* x, int T, void* y, void* ctx, void* workspace, void* stream) {
+  if (!h || !x || !y || !workspace) return MOE_ERR_INVALID_ARG;
+  if (check_T(h, T) != MOE_OK) return MOE_ERR_INVALID_ARG;
+  if (!h->L.has_weights) return MOE_ERR_NO_WEIGHTS;
+  if (!aligned256(workspace) || (ctx && !aligned256(ctx))) return MOE_ERR_WORKSPACE;
+  if (!aligned16(x) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  const Layer& L = h->L;
+  cudaStream_t s = (cudaStream_t)stream;
+  Bufs B = carve(L, T, workspace, ctx, nullptr);
+  moe_status st = run_route(h, B, x, nullptr, s);
+  if (st != MOE_OK) return st;
+  if (h->tc) {
+    CK(launch_tc_gateup(L, B, x, s));
+    CK(launch_tc_down(L, B, s));
+  } else {
+    CK(launch_simt_gateup(L, B, x, s));
+    CK(launch_simt_down(L, B, s));
+  }
+  CK(launch_combine(L, B, y, s));
+  return MOE_OK;
+}
+
+moe_status moe_backward(moe_handle h, const void* x, const void* dy, int T, const void* ctx, void* dx, float* dWr,
+                        void* dWg, void* dWu, void* dWd, void* workspace, void* stream) {
+  if (!h || !x || !dy || !ctx || !dx || !dWr || !dWg || !dWu || !dWd || !workspace) return MOE_ERR_INVALID_ARG;
+  if (check_T(h, T) != MOE_OK) return MOE_ERR_INVALID_ARG;
+  if (!h->L.has_weights) return MOE_ERR_NO_WEIGHTS;
+  if (!aligned256(workspace) || !aligned256(ctx)) return MOE_ERR_WORKSPACE;
+  if (!aligned16(x) || !aligned16(dy) || !aligned16(dx)) return MOE_ERR_INVALID_ARG;
+  const Layer& L = h->L;
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t eb = elem_bytes(L.prec);
+  const size_t nseg = L.E + L.S;
+  if (T == 0) {
+    CK(cudaMemsetAsync(dWr, 0, 4 * (size_t)L.E * L.d, s));
+    CK(cudaMemsetAsync(dWg, 0, eb * nseg * L.f * L.d, s));
+    CK(cudaMemsetAsync(dWu, 0, eb * nseg * L.f * L.d, s));
+    CK(cudaMemsetAsync(dWd, 0, eb * nseg * L.d * L.f, s));
+    return MOE_OK;
+  }
+  Bufs B = carve(L, T, nullptr, ctx, workspace);
+  if (h->tc) {
+    CK(launch_tc_bwd_dh(L, B, dy, s));
+    CK(launch_tc_bwd_dx(L, B, s));
+  } else {
+    CK(launch_simt_bwd_dh(L, B, dy, s));
+    CK(launch_simt_bwd_dx(L, B, s));
+  }
+  CK(launch_router_bwd(L, B, x, dWr, s));
+  CK(launch_dx_gather(L, B, dx, s));
+  if (h->tc) {
+    CK(launch_tc_bwd_dw(L, B, x, dy, dWg, dWu, dWd, s));
+  } else {
+    CK(launch_simt_bwd_dw(L, B, x, dy, dWg, dWu, dWd, s));
+  }
+  return MOE_OK;
+}
+
+moe_status moe_decode(moe_handle h, const void* x, int B, void* y, void* workspace, void* stream) {
+  if (!h || !x || !y || !workspace) return MOE_ERR_INVALID_ARG;
+  if (B < 1 || B > kMaxDecodeB || B > h->cfg.T_max) return MOE_ERR_INVALID_ARG;
+  if (h->L.prec != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (!h->L.has_weights) return MOE_ERR_NO_WEIGHTS;
+  if (!aligned256(workspace)) return MOE_ERR_WORKSPACE;
+  if (!aligned16(x) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+  CK(launch_decode(h->L, x, B, y, workspace, (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+moe_status moe_get_status(moe_handle h, void* stream, int* device_status) {
+  if (!h || !device_status) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  int v = 0;
+  CK(cudaStreamSynchronize(s));
+  CK(cudaMemcpy(&v, h->L.status, sizeof(int), cudaMemcpyDeviceToHost));
+  CK(cudaMemset(h->L.status, 0, sizeof(int)));
+  *device_status = v;
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,104 @@
+// Internal interface between the host API (api.cu) and the kernel translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kMaxE = 256;        // routed experts supported by the routing kernels
+constexpr int kMaxK = 8;          // experts per token
+constexpr int kChunk = 1024;      // assignments per block of the histogram / permutation kernels
+constexpr int kBM = 128;          // rows per M-tile of the grouped GEMMs (segment padding unit)
+constexpr int kGate = 128;        // gate/up interleave block of the packed W13 (rows)
+constexpr int kMaxDecodeB = 64;
+
+// Shape of one layer and the pointers that stay fixed after moe_set_weights.
+struct Layer {
+  int d, E, S, f, k, router, renorm, prec;
+  float scale;
+  int G;                 // gate/up interleave block actually used (kGate, or f when f < kGate)
+  // packed weights (device)
+  void* W13;             // [E+S][2f][d] gate/up rows interleaved in blocks of G
+  void* Wd;              // [E+S][d][f]
+  void* Wr;              // [E][d]
+  float* bias;           // [E]
+  int* status;           // device status word
+  int* decode_counter;   // device counter of the decode router's last-block election
+  int num_sms;
+  bool has_weights;
+  // tensor maps of the packed weights (bf16 tcgen05 path)
+  alignas(64) CUtensorMap tm_W13;       // K-major rows of W13 (box 64 x 256)
+  alignas(64) CUtensorMap tm_Wd;        // K-major rows of Wd (box 64 x 256)
+  alignas(64) CUtensorMap tm_W13_mn;    // W13 as [K=2f rows][N=d] for dx (box 64 x 64)
+  alignas(64) CUtensorMap tm_Wd_mn;     // Wd as [K=d rows][N=f] for the dY.Wd product (box 64 x 64)
+};
+
+// Device buffers of one forward / backward, carved from the caller's workspace and context.
+struct Bufs {
+  int T, A, R;           // tokens, assignments (T*k), sorted rows (A + S*T)
+  int nch;               // histogram chunks
+  // routing (context when training, else workspace)
+  float* logits;         // [T, E]
+  int* idx;              // [T, k]
+  float* gate;           // [T, k]
+  int* cnt;              // [E+S]
+  int* off;              // [E+S+1]
+  int* mt_off;           // [E+S+1] prefix of ceil(cnt / kBM)
+  int* perm;             // [A]
+  int* inv;              // [A]
+  int* row_token;        // [R]
+  float* row_gate;       // [R]
+  void* uv;              // [R, 2f] saved pre-activations (interleaved like W13), may be null
+  // forward scratch
+  int* chunk_hist;       // [nch, E]
+  int* chunk_base;       // [nch, E]
+  void* h;               // [R, f]
+  void* o;               // [R, d]
+  // backward scratch
+  void* dudv;            // [R, 2f]
+  void* hg;              // [R, f]  gate * h
+  float* dg_part;        // [A, f / kGate]
+  void* dx_rows;         // [R, d]
+  float* dl;             // [T, E]
+  float* dgate;          // [T, k]
+};
+
+// ----------------------------------------------------------- launchers
+// route.cu
+cudaError_t launch_router_logits(const Layer& L, const void* x, int T, float* logits, cudaStream_t s);
+cudaError_t launch_topk(const Layer& L, const float* logits, int T, int* idx, float* gate, cudaStream_t s);
+cudaError_t launch_scan_permute(const Layer& L, const Bufs& B, cudaStream_t s);
+// simt.cu (fp32 path and reference-grade kernels)
+cudaError_t launch_simt_gateup(const Layer& L, const Bufs& B, const void* x, cudaStream_t s);
+cudaError_t launch_simt_down(const Layer& L, const Bufs& B, cudaStream_t s);
+cudaError_t launch_simt_bwd_dh(const Layer& L, const Bufs& B, const void* dy, cudaStream_t s);
+cudaError_t launch_simt_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s);
+cudaError_t launch_simt_bwd_dw(const Layer& L, const Bufs& B, const void* x, const void* dy,
+                               void* dWg, void* dWu, void* dWd, cudaStream_t s);
+// combine.cu
+cudaError_t launch_combine(const Layer& L, const Bufs& B, void* y, cudaStream_t s);
+cudaError_t launch_router_bwd(const Layer& L, const Bufs& B, const void* x, float* dWr, cudaStream_t s);
+cudaError_t launch_dx_gather(const Layer& L, const Bufs& B, void* dx, cudaStream_t s);
+cudaError_t launch_pack_weights(const Layer& L, const void* Wr, const float* bias, const void* Wg,
+                                const void* Wu, const void* Wd, cudaStream_t s);
+// decode.cu
+size_t decode_workspace_bytes(const Layer& L, int B);
+cudaError_t launch_decode(const Layer& L, const void* x, int B, void* y, void* ws, cudaStream_t s);
+// tc_gemm.cu (bf16 tcgen05 path)
+bool tc_supported(const Layer& L);
+cudaError_t tc_init(Layer& L);   // encodes the weight tensor maps, sets kernel attributes
+cudaError_t launch_tc_router_logits(const Layer& L, const void* x, int T, float* logits, cudaStream_t s);
+cudaError_t launch_tc_gateup(const Layer& L, const Bufs& B, const void* x, cudaStream_t s);
+cudaError_t launch_tc_down(const Layer& L, const Bufs& B, cudaStream_t s);
+cudaError_t launch_tc_bwd_dh(const Layer& L, const Bufs& B, const void* dy, cudaStream_t s);
+cudaError_t launch_tc_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s);
+cudaError_t launch_tc_bwd_dw(const Layer& L, const Bufs& B, const void* x, const void* dy,
+                             void* dWg, void* dWu, void* dWd, cudaStream_t s);
+
+inline size_t elem_bytes(int prec) { return prec == MOE_FP32 ? 4 : 2; }
+
+}  // namespace moe
