@@ -1,0 +1,453 @@
+#!/usr/bin/env python
+"""MoE-layer throughput on GB300: tokens/s and fraction of roofline.
+
+Default workload (one step = forward + backward of one MoE layer):
+  bf16, T=2048 tokens, d=2048, E=64 experts, f=1408, top-6 softmax router
+  renormalised over the top-6, router bias giving a Zipf(s=1.0) expert load.
+Extra workloads in the same JSON line (key "extra"): the DeepSeek-V3-shaped
+bf16 forward (T=8192, d=7168, 256 routed + 1 shared expert, f=2048, top-8
+sigmoid x 2.5; uniform and Zipf s=1.2 routing) and small-batch decode B=1/4/16.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line on rank 0. Inputs are synthetic (moe_synth), resident in
+HBM before the timed region; the expert weights (1.1 GB) exceed L2 and stream
+from HBM every step, so no L2 flush is inserted. "e2e" repeats the step
+through the C ABI with host-resident x and dy copied in and y and dx copied out
+every step. "roofline" is for the kernel group with the largest time share.
+The reference arm (--impl reference) times the CPU oracle on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s fwd, fwd+bwd, decode on 1×GB300; % of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------- helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ------------------------------------------------- algorithmic work per group
+
+def work_per_group(spec, cnt, training=True):
+    """Algorithmic (flops, bytes) of one launch of each kernel group for the realised expert loads.
+
+    Bytes count what each step must move at least once: weights of experts that
+    received tokens, activations read and written once.
+    """
+    T, d, E, S, f, k = spec.T, spec.d, spec.E, spec.S, spec.f, spec.k
+    A = T * k
+    R = A + S * T
+    active = int(np.count_nonzero(cnt)) + S
+    w13 = active * 2 * f * d * 2
+    wd = active * d * f * 2
+    g = {}
+    g["router_logits"] = (2 * T * E * d, T * d * 2 + E * d * 2 + T * E * 4)
+    g["gateup"] = (2 * R * 2 * f * d, w13 + T * d * 2 + R * f * 2 + (R * 2 * f * 2 if training else 0))
+    g["down"] = (2 * R * d * f, wd + R * f * 2 + R * d * 2)
+    g["combine"] = (R * d, R * d * 2 + T * d * 2)
+    g["bwd_dh"] = (2 * R * f * d, wd + T * d * 2 + R * 2 * f * 2 * 2 + R * f * 2)
+    g["bwd_dx"] = (2 * R * d * 2 * f, w13 + R * 2 * f * 2 + R * d * 2)
+    g["bwd_dw"] = (2 * R * 2 * f * d + 2 * R * d * f,
+                   (E + S) * 3 * f * d * 2 + R * 2 * f * 2 + T * d * 2 * 2 + R * f * 2)
+    g["dx_gather"] = (R * d, R * d * 2 + T * d * 2)
+    g["decode_gateup"] = (2 * R * 2 * f * d, w13 + T * d * 2)
+    g["decode_down"] = (2 * R * d * f, wd + R * f * 4 + T * d * 2)
+    return g
+
+
+def roofline_entry(group, ms_per_launch, flops, nbytes, pk, traffic=None):
+    t_tensor = flops / (pk["bf16_tflops"] * 1e12)
+    t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
+    if t_tensor >= t_hbm:
+        achieved = flops / (ms_per_launch * 1e-3) / 1e12
+        return {"kernel": group, "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": traffic,
+                "peak_source": pk["source"] + " (burst)"}
+    achieved = nbytes / (ms_per_launch * 1e-3) / 1e9
+    return {"kernel": group, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / pk["hbm_gbs"], "traffic": traffic, "peak_source": pk["source"]}
+
+
+def stored_traffic(group):
+    """dram bytes per launch from the committed ncu summary, if its kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as fh:
+            tab = json.load(fh)
+        ent = tab.get(group)
+        if not ent:
+            return None
+        src = os.path.join(ROOT, ent["source"])
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if digest != ent["source_sha256_16"]:
+            return None
+        return ent["dram_bytes_per_launch"]
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------ our GPU path
+
+class TrainStep:
+    """Preallocated buffers for forward (saving ctx) + backward through the C ABI."""
+
+    def __init__(self, spec, dev):
+        from mixture_experts_layer_routing_gb300 import MoeLayer, moe_backward, moe_forward
+        self._fwd, self._bwd = moe_forward, moe_backward
+        self.spec = spec
+        inp = moe_synth.make_inputs(spec, dev, grad=True)
+        self.inp = inp
+        self.layer = MoeLayer.from_spec(spec, device=dev)
+        self.layer.set_weights(inp["Wr"], inp["b"], inp["Wg"], inp["Wu"], inp["Wd"])
+        del inp["Wg"], inp["Wu"], inp["Wd"]
+        T, d, E, S, f = spec.T, spec.d, spec.E, spec.S, spec.f
+        sz = self.layer.sizes(T)
+        self.ctx = self.layer.new_ctx(T)
+        self.ws = self.layer.buffer("fwd", sz["fwd_ws"])
+        self.bws = self.layer.buffer("bwd", sz["bwd_ws"])
+        bf = torch.bfloat16
+        self.y = torch.empty((T, d), dtype=bf, device=dev)
+        self.dx = torch.empty((T, d), dtype=bf, device=dev)
+        self.dWr = torch.empty((E, d), dtype=torch.float32, device=dev)
+        self.dWg = torch.empty((E + S, f, d), dtype=bf, device=dev)
+        self.dWu = torch.empty((E + S, f, d), dtype=bf, device=dev)
+        self.dWd = torch.empty((E + S, d, f), dtype=bf, device=dev)
+
+    def __call__(self, x=None, dy=None):
+        x = self.inp["x"] if x is None else x
+        dy = self.inp["dy"] if dy is None else dy
+        h, T = self.layer.h, self.spec.T
+        self._fwd(h, x, T, self.y, self.ctx, self.ws)
+        self._bwd(h, x, dy, T, self.ctx, self.dx, self.dWr, self.dWg, self.dWu, self.dWd, self.bws)
+
+
+def time_steps(fn, steps, warmup, world):
+    for _ in range(warmup):
+        fn()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = a.elapsed_time(b) / steps
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms
+
+
+def profile_groups(layer_h, fn, steps):
+    from mixture_experts_layer_routing_gb300 import moe_profile_enable, moe_profile_read
+    moe_profile_read(layer_h)
+    moe_profile_enable(layer_h, True)
+    for _ in range(steps):
+        fn()
+    torch.cuda.synchronize()
+    moe_profile_enable(layer_h, False)
+    return moe_profile_read(layer_h)
+
+
+def oracle_inputs(inp_cpu):
+    """Host float32 copies of the inputs (bf16 values widened exactly); prepared outside any timer."""
+    return {k: v.float().numpy() for k, v in inp_cpu.items()}
+
+
+def cpu_baseline(spec, n, n_tokens, training=True):
+    """Seconds the oracle, as it stands, takes for the first n_tokens tokens of the workload (host cores)."""
+    from oracle import moe_oracle as oracle
+    x = n["x"][:n_tokens]
+    kw = dict(k=spec.k, router=spec.router, renorm=spec.renorm, scale=spec.route_scale, n_shared=spec.S)
+    t0 = time.perf_counter()
+    oracle.forward(x, n["Wr"], n["b"], n["Wg"], n["Wu"], n["Wd"], **kw)
+    if training:
+        oracle.backward(x, n["Wr"], n["b"], n["Wg"], n["Wu"], n["Wd"], n["dy"][:n_tokens], **kw)
+    return time.perf_counter() - t0
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        if info:
+            return int(max(i.get("num_threads", 1) for i in info))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def run_ours(args):
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+    from mixture_experts_layer_routing_gb300 import moe_launch_count
+    pk = peaks()
+    spec = moe_synth.BF16_T2048
+    step = TrainStep(spec, dev)
+    r = step.layer.route(step.inp["x"])
+    cnt = r["cnt"].cpu().numpy()
+    n0 = moe_launch_count(step.layer.h)
+    with ClockSampler(local) as clk:
+        ms = time_steps(step, args.steps, args.warmup, world)
+    launches = (moe_launch_count(step.layer.h) - n0) // (args.steps + args.warmup) * args.steps
+    value = world * spec.T / (ms * 1e-3)
+
+    # end to end through the C ABI: host x, dy in; host y, dx out; every step
+    x_h = step.inp["x"].cpu().pin_memory()
+    dy_h = step.inp["dy"].cpu().pin_memory()
+    y_h = torch.empty_like(x_h).pin_memory()
+    dx_h = torch.empty_like(x_h).pin_memory()
+    x_d = torch.empty_like(step.inp["x"])
+    dy_d = torch.empty_like(step.inp["dy"])
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        dy_d.copy_(dy_h, non_blocking=True)
+        step(x_d, dy_d)
+        y_h.copy_(step.y, non_blocking=True)
+        dx_h.copy_(step.dx, non_blocking=True)
+
+    ms_e2e = time_steps(e2e_step, args.steps, args.warmup, world)
+    e2e = {"value": world * spec.T / (ms_e2e * 1e-3), "unit": "tokens/s",
+           "h2d_bytes_per_step": x_h.numel() * 2 + dy_h.numel() * 2,
+           "d2h_bytes_per_step": y_h.numel() * 2 + dx_h.numel() * 2}
+
+    # per-kernel-group times (events on the launching stream), dominant group's roofline
+    prof = profile_groups(step.layer.h, step, args.steps)
+    work = work_per_group(spec, cnt, training=True)
+    tot = sum(v[1] for v in prof.values())
+    groups = {}
+    for g, (nk, gms) in prof.items():
+        per_launch = gms / args.steps
+        ent = {"ms_per_step": per_launch, "share": gms / tot if tot else None}
+        if g in work:
+            fl, by = work[g]
+            ent.update(tflops=fl / (per_launch * 1e-3) / 1e12, gbs=by / (per_launch * 1e-3) / 1e9)
+        groups[g] = ent
+    dom = max((g for g in prof if g in work), key=lambda g: prof[g][1])
+    dom_ms = prof[dom][1] / args.steps
+    roof = roofline_entry(dom, dom_ms, *work[dom], pk, stored_traffic(dom))
+
+    out = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, moe_synth)",
+           "config": {"workload": spec.name + " fwd+bwd", "T": spec.T, "d": spec.d, "E": spec.E, "f": spec.f,
+                      "k": spec.k, "router": "softmax top-6 renorm, Zipf(1.0) load bias", "global_batch": spec.T * world,
+                      "parallelism": f"replicas x{world}",
+                      "l2": "no flush: expert weights (1.11 GB) exceed L2 and stream from HBM every step",
+                      "active_experts": int(np.count_nonzero(cnt)), "max_expert_load": int(cnt.max())},
+           "e2e": e2e, "gpu_launches": int(launches), "roofline": roof, "kernel_groups": groups}
+    out["clocks"] = clk.summary()
+
+    if rank == 0 and not args.no_extra:
+        out["extra"] = run_extra(args, dev, pk)
+    if rank == 0 and not args.no_cpu_baseline:
+        n = oracle_inputs(moe_synth.make_inputs(spec, "cpu", grad=True))
+        ntok = args.cpu_tokens
+        dt = cpu_baseline(spec, n, ntok)
+        out["cpu_baseline"] = {"value": ntok / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                               "sample": f"fwd+bwd of the first {ntok} of {spec.T} tokens (all experts' weights), "
+                                         f"{dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_extra(args, dev, pk):
+    """DeepSeek-V3-shaped forward (uniform, Zipf 1.2) and decode B=1/4/16."""
+    from mixture_experts_layer_routing_gb300 import MoeLayer, moe_decode, moe_forward
+    extra = {}
+    steps, warm = max(3, args.steps // 2), 3
+    for spec in (moe_synth.DSV3_UNIFORM, moe_synth.DSV3_ZIPF):
+        inp = moe_synth.make_inputs(spec, dev)
+        layer = MoeLayer.from_spec(spec, device=dev)
+        layer.set_weights(inp["Wr"], inp["b"], inp["Wg"], inp["Wu"], inp["Wd"])
+        del inp["Wg"], inp["Wu"], inp["Wd"]
+        torch.cuda.empty_cache()
+        cnt = layer.route(inp["x"])["cnt"].cpu().numpy()
+        y = torch.empty_like(inp["x"])
+        ws = layer.buffer("fwd", layer.sizes(spec.T)["fwd_ws"])
+        fn = lambda: moe_forward(layer.h, inp["x"], spec.T, y, None, ws)  # noqa: E731
+        ms = time_steps(fn, steps, warm, 1)
+        prof = profile_groups(layer.h, fn, steps)
+        work = work_per_group(spec, cnt, training=False)
+        fl = sum(work[g][0] for g in ("router_logits", "gateup", "down", "combine"))
+        by = sum(work[g][1] for g in ("router_logits", "gateup", "down", "combine"))
+        t_roof = max(fl / (pk["bf16_tflops"] * 1e12), by / (pk["hbm_gbs"] * 1e9))
+        extra[spec.name + " fwd"] = {
+            "tokens_per_s": spec.T / (ms * 1e-3), "ms": ms, "roofline_ms": t_roof * 1e3,
+            "frac_of_roofline": t_roof * 1e3 / ms, "active_experts": int(np.count_nonzero(cnt)) + spec.S,
+            "groups_ms": {g: v[1] / steps for g, v in prof.items()}}
+        # decode on the same weights
+        if spec is moe_synth.DSV3_UNIFORM:
+            for B in (1, 4, 16):
+                xb = moe_synth.make_tokens(spec.with_(T=B), 1, dev)[0]
+                yb = torch.empty_like(xb)
+                wsb = layer.buffer("fwd", layer.sizes(B)["fwd_ws"])
+                fnb = lambda: moe_decode(layer.h, xb, B, yb, wsb)  # noqa: E731
+                msb = time_steps(fnb, 50, 5, 1)
+                profb = profile_groups(layer.h, fnb, 20)
+                rb = layer.route(xb)
+                cb = rb["cnt"].cpu().numpy()
+                nact = int(np.count_nonzero(cb)) + spec.S
+                nbytes = nact * 3 * spec.f * spec.d * 2 + spec.E * spec.d * 2
+                t_roof = nbytes / (pk["hbm_gbs"] * 1e9)
+                extra[f"dsv3_bf16_decode_B{B}"] = {
+                    "tokens_per_s": B / (msb * 1e-3), "ms": msb, "weight_gbs": nbytes / (msb * 1e-3) / 1e9,
+                    "roofline_ms": t_roof * 1e3, "frac_of_roofline": t_roof * 1e3 / msb, "experts_read": nact,
+                    "groups_ms": {g: v[1] / 20 for g, v in profb.items()}}
+        layer.close()
+        del layer, inp
+        torch.cuda.empty_cache()
+    return extra
+
+
+# -------------------------------------------------------- reference arm
+
+def run_reference(args):
+    world, rank, local = dist_env()
+    if rank != 0:
+        return
+    spec = moe_synth.BF16_T2048
+    n = oracle_inputs(moe_synth.make_inputs(spec, "cpu", grad=True))
+    ntok = args.ref_tokens
+    for _ in range(args.warmup):
+        cpu_baseline(spec, n, ntok)
+    times = [cpu_baseline(spec, n, ntok) for _ in range(args.steps)]
+    ms = 1e3 * float(np.mean(times))
+    value = ntok / (ms * 1e-3)
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, moe_synth)",
+           "config": {"workload": spec.name + " fwd+bwd", "T": spec.T, "d": spec.d, "E": spec.E, "f": spec.f,
+                      "k": spec.k, "sample_tokens_per_step": ntok},
+           "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                            "sample": f"fwd+bwd of the first {ntok} of {spec.T} tokens per step"},
+           "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=128, help="oracle sample for cpu_baseline")
+    ap.add_argument("--ref-tokens", type=int, default=16, help="oracle sample per reference-arm step")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

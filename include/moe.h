@@ -143,6 +143,20 @@ moe_status moe_decode(moe_handle h, const void* x, int B, void* y, void* workspa
  * device status word into *device_status (MOE_OK if no device error). */
 moe_status moe_get_status(moe_handle h, void* stream, int* device_status);
 
+/* Tracing. When enabled, every kernel launch of later calls on this handle is
+ * bracketed by two CUDA events recorded on the call's stream (no extra device
+ * memory). moe_profile_read waits for the recorded events and returns, for
+ * each kernel group that ran (at most max_groups), its name (NUL-terminated,
+ * at most 31 characters, in names[32*i]), its kernel launches and the summed
+ * milliseconds between its events; then it forgets the records. *n_groups
+ * receives the number of groups written. */
+moe_status moe_profile_enable(moe_handle h, int enable);
+moe_status moe_profile_read(moe_handle h, int max_groups, char* names, long long* launches, double* total_ms,
+                            int* n_groups);
+
+/* Number of kernels the handle has launched since moe_create (host counter). */
+moe_status moe_launch_count(moe_handle h, long long* launches);
+
 /* Human-readable name of a status code (static string). */
 const char* moe_status_string(int status);
 

@@ -22,7 +22,8 @@ MOE_ROUTER_SOFTMAX, MOE_ROUTER_SIGMOID = 0, 1
 MOE_FP32, MOE_BF16, MOE_MXFP8 = 0, 1, 2
 
 EXPORTED = ("moe_create", "moe_destroy", "moe_workspace_size", "moe_set_weights", "moe_route", "moe_forward",
-            "moe_backward", "moe_decode", "moe_get_status", "moe_status_string")
+            "moe_backward", "moe_decode", "moe_get_status", "moe_profile_enable", "moe_profile_read",
+            "moe_launch_count", "moe_status_string")
 
 
 class MoeError(RuntimeError):
@@ -60,6 +61,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_backward.argtypes = [vp, vp, vp, i32] + [vp] * 8
     lib.moe_decode.argtypes = [vp, vp, i32, vp, vp, vp]
     lib.moe_get_status.argtypes = [vp, vp, P(i32)]
+    lib.moe_profile_enable.argtypes = [vp, i32]
+    lib.moe_profile_read.argtypes = [vp, i32, ctypes.c_char_p, P(ctypes.c_longlong), P(ctypes.c_double), P(i32)]
+    lib.moe_launch_count.argtypes = [vp, P(ctypes.c_longlong)]
     lib.moe_status_string.argtypes = [i32]
     lib.moe_status_string.restype = ctypes.c_char_p
     for name in EXPORTED[:-1]:
@@ -142,6 +146,30 @@ def moe_decode(h, x, B, y, workspace, stream=None):
 def moe_get_status(h, stream=None) -> int:
     v = ctypes.c_int()
     _check(load_library().moe_get_status(h, _stream(stream), ctypes.byref(v)), "moe_get_status")
+    return v.value
+
+
+def moe_profile_enable(h, enable: bool = True):
+    _check(load_library().moe_profile_enable(h, int(bool(enable))), "moe_profile_enable")
+
+
+def moe_profile_read(h, max_groups: int = 32) -> dict:
+    """{group name: (kernel launches, total ms)} of the launches recorded since the last read."""
+    names = ctypes.create_string_buffer(32 * max_groups)
+    launches = (ctypes.c_longlong * max_groups)()
+    ms = (ctypes.c_double * max_groups)()
+    n = ctypes.c_int()
+    _check(load_library().moe_profile_read(h, max_groups, names, launches, ms, ctypes.byref(n)), "moe_profile_read")
+    out = {}
+    for i in range(n.value):
+        name = names.raw[32 * i:32 * i + 32].split(b"\0", 1)[0].decode()
+        out[name] = (launches[i], ms[i])
+    return out
+
+
+def moe_launch_count(h) -> int:
+    v = ctypes.c_longlong()
+    _check(load_library().moe_launch_count(h, ctypes.byref(v)), "moe_launch_count")
     return v.value
 
 

@@ -5,17 +5,36 @@
 #include <cmath>
 #include <cstring>
 #include <new>
+#include <vector>
 
 #include "common.cuh"
 #include "kernels.h"
 
 using namespace moe;
 
+// Kernel groups reported by moe_profile_read.
+enum Group {
+  G_ROUTER_LOGITS, G_TOPK, G_SCAN_PERMUTE, G_GATEUP, G_DOWN, G_COMBINE, G_BWD_DH, G_BWD_DX, G_ROUTER_BWD,
+  G_DX_GATHER, G_BWD_DW, G_DECODE_ROUTE, G_DECODE_GATEUP, G_DECODE_DOWN, G_PACK, G_COUNT
+};
+static const char* kGroupNames[G_COUNT] = {
+    "router_logits", "topk", "scan_permute", "gateup", "down", "combine", "bwd_dh", "bwd_dx", "router_bwd",
+    "dx_gather", "bwd_dw", "decode_route", "decode_gateup", "decode_down", "pack_weights"};
+
+struct ProfRec {
+  int group, kernels;
+  cudaEvent_t a, b;
+};
+
 struct moe_handle_s {
   moe_config cfg;
   Layer L;
   int device;
   bool tc;   // bf16 tensor-core path available for this shape
+  bool prof = false;
+  long long launches = 0;
+  std::vector<ProfRec> recs;
+  std::vector<cudaEvent_t> pool;
 };
 
 namespace {
@@ -103,25 +122,54 @@ inline bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
     if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
   } while (0)
 
+cudaEvent_t take_event(moe_handle_s* h) {
+  if (!h->pool.empty()) {
+    cudaEvent_t e = h->pool.back();
+    h->pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Launches one kernel group (nk kernels) and, when profiling, brackets it with events on s.
+template <class F>
+cudaError_t run(moe_handle_s* h, cudaStream_t s, int group, int nk, F&& f) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (h->prof) {
+    a = take_event(h);
+    b = take_event(h);
+    if (a && b) cudaEventRecord(a, s);
+  }
+  const cudaError_t e = f();
+  if (a && b) {
+    cudaEventRecord(b, s);
+    h->recs.push_back({group, nk, a, b});
+  }
+  h->launches += nk;
+  return e;
+}
+
 moe_status check_T(const moe_handle_s* h, int T) {
   if (T < 0 || T > h->cfg.T_max) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
 // router logits, top-k, counts, offsets, permutation
-moe_status run_route(const moe_handle_s* h, const Bufs& B, const void* x, const float* logits_override,
+moe_status run_route(moe_handle_s* h, const Bufs& B, const void* x, const float* logits_override,
                      cudaStream_t s) {
   const Layer& L = h->L;
   const float* lg = B.logits;
   if (logits_override) {
     lg = logits_override;
   } else if (h->tc) {
-    CK(launch_tc_router_logits(L, x, B.T, B.logits, s));
+    CK(run(h, s, G_ROUTER_LOGITS, 1, [&] { return launch_tc_router_logits(L, x, B.T, B.logits, s); }));
   } else {
-    CK(launch_router_logits(L, x, B.T, B.logits, s));
+    CK(run(h, s, G_ROUTER_LOGITS, 1, [&] { return launch_router_logits(L, x, B.T, B.logits, s); }));
   }
-  CK(launch_topk(L, lg, B.T, B.idx, B.gate, s));
-  CK(launch_scan_permute(L, B, s));
+  CK(run(h, s, G_TOPK, 1, [&] { return launch_topk(L, lg, B.T, B.idx, B.gate, s); }));
+  CK(run(h, s, G_SCAN_PERMUTE, L.S ? 4 : 3, [&] { return launch_scan_permute(L, B, s); }));
   if (logits_override && lg != B.logits)
     CK(cudaMemcpyAsync(B.logits, lg, sizeof(float) * (size_t)B.T * L.E, cudaMemcpyDeviceToDevice, s));
   return MOE_OK;
@@ -185,6 +233,11 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
 
 moe_status moe_destroy(moe_handle h) {
   if (!h) return MOE_ERR_INVALID_ARG;
+  for (auto& r : h->recs) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (auto e : h->pool) cudaEventDestroy(e);
   cudaFree(h->L.status);
   delete h;
   return MOE_OK;
@@ -214,7 +267,7 @@ moe_status moe_set_weights(moe_handle h, const void* Wr, const float* bias, cons
   L.Wr = p; p += al(eb * L.E * L.d);
   L.bias = (float*)p;
   cudaStream_t s = (cudaStream_t)stream;
-  CK(launch_pack_weights(L, Wr, bias, Wg, Wu, Wd, s));
+  CK(run(h, s, G_PACK, 1, [&] { return launch_pack_weights(L, Wr, bias, Wg, Wu, Wd, s); }));
   if (h->tc) CK(tc_init(L));
   L.has_weights = true;
   return MOE_OK;
@@ -258,13 +311,13 @@ moe_status moe_forward(moe_handle h, const void* x, int T, void* y, void* ctx, v
   moe_status st = run_route(h, B, x, nullptr, s);
   if (st != MOE_OK) return st;
   if (h->tc) {
-    CK(launch_tc_gateup(L, B, x, s));
-    CK(launch_tc_down(L, B, s));
+    CK(run(h, s, G_GATEUP, 1, [&] { return launch_tc_gateup(L, B, x, s); }));
+    CK(run(h, s, G_DOWN, 1, [&] { return launch_tc_down(L, B, s); }));
   } else {
-    CK(launch_simt_gateup(L, B, x, s));
-    CK(launch_simt_down(L, B, s));
+    CK(run(h, s, G_GATEUP, 1, [&] { return launch_simt_gateup(L, B, x, s); }));
+    CK(run(h, s, G_DOWN, 1, [&] { return launch_simt_down(L, B, s); }));
   }
-  CK(launch_combine(L, B, y, s));
+  CK(run(h, s, G_COMBINE, 1, [&] { return launch_combine(L, B, y, s); }));
   return MOE_OK;
 }
 
@@ -288,18 +341,18 @@ moe_status moe_backward(moe_handle h, const void* x, const void* dy, int T, cons
   }
   Bufs B = carve(L, T, nullptr, ctx, workspace);
   if (h->tc) {
-    CK(launch_tc_bwd_dh(L, B, dy, s));
-    CK(launch_tc_bwd_dx(L, B, s));
+    CK(run(h, s, G_BWD_DH, 1, [&] { return launch_tc_bwd_dh(L, B, dy, s); }));
+    CK(run(h, s, G_BWD_DX, 1, [&] { return launch_tc_bwd_dx(L, B, s); }));
   } else {
-    CK(launch_simt_bwd_dh(L, B, dy, s));
-    CK(launch_simt_bwd_dx(L, B, s));
+    CK(run(h, s, G_BWD_DH, 1, [&] { return launch_simt_bwd_dh(L, B, dy, s); }));
+    CK(run(h, s, G_BWD_DX, 1, [&] { return launch_simt_bwd_dx(L, B, s); }));
   }
-  CK(launch_router_bwd(L, B, x, dWr, s));
-  CK(launch_dx_gather(L, B, dx, s));
+  CK(run(h, s, G_ROUTER_BWD, 2, [&] { return launch_router_bwd(L, B, x, dWr, s); }));
+  CK(run(h, s, G_DX_GATHER, 1, [&] { return launch_dx_gather(L, B, dx, s); }));
   if (h->tc) {
-    CK(launch_tc_bwd_dw(L, B, x, dy, dWg, dWu, dWd, s));
+    CK(run(h, s, G_BWD_DW, 2, [&] { return launch_tc_bwd_dw(L, B, x, dy, dWg, dWu, dWd, s); }));
   } else {
-    CK(launch_simt_bwd_dw(L, B, x, dy, dWg, dWu, dWd, s));
+    CK(run(h, s, G_BWD_DW, 2, [&] { return launch_simt_bwd_dw(L, B, x, dy, dWg, dWu, dWd, s); }));
   }
   return MOE_OK;
 }
@@ -311,7 +364,55 @@ moe_status moe_decode(moe_handle h, const void* x, int B, void* y, void* workspa
   if (!h->L.has_weights) return MOE_ERR_NO_WEIGHTS;
   if (!aligned256(workspace)) return MOE_ERR_WORKSPACE;
   if (!aligned16(x) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
-  CK(launch_decode(h->L, x, B, y, workspace, (cudaStream_t)stream));
+  cudaStream_t s = (cudaStream_t)stream;
+  const Layer& L = h->L;
+  CK(run(h, s, G_DECODE_ROUTE, 1, [&] { return launch_decode_route(L, x, B, workspace, s); }));
+  CK(run(h, s, G_DECODE_GATEUP, 1, [&] { return launch_decode_gateup(L, x, B, workspace, s); }));
+  CK(run(h, s, G_DECODE_DOWN, 1, [&] { return launch_decode_down(L, B, y, workspace, s); }));
+  return MOE_OK;
+}
+
+moe_status moe_profile_enable(moe_handle h, int enable) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  h->prof = enable != 0;
+  return MOE_OK;
+}
+
+moe_status moe_profile_read(moe_handle h, int max_groups, char* names, long long* launches, double* total_ms,
+                            int* n_groups) {
+  if (!h || max_groups < 0 || !n_groups || (max_groups > 0 && (!names || !launches || !total_ms)))
+    return MOE_ERR_INVALID_ARG;
+  double ms[G_COUNT] = {};
+  long long nk[G_COUNT] = {};
+  bool seen[G_COUNT] = {};
+  moe_status st = MOE_OK;
+  for (auto& r : h->recs) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess)
+      st = MOE_ERR_CUDA;
+    ms[r.group] += t;
+    nk[r.group] += r.kernels;
+    seen[r.group] = true;
+    h->pool.push_back(r.a);
+    h->pool.push_back(r.b);
+  }
+  h->recs.clear();
+  int n = 0;
+  for (int g = 0; g < G_COUNT && n < max_groups; ++g) {
+    if (!seen[g]) continue;
+    std::strncpy(names + 32 * n, kGroupNames[g], 31);
+    names[32 * n + 31] = 0;
+    launches[n] = nk[g];
+    total_ms[n] = ms[g];
+    ++n;
+  }
+  *n_groups = n;
+  return st;
+}
+
+moe_status moe_launch_count(moe_handle h, long long* launches) {
+  if (!h || !launches) return MOE_ERR_INVALID_ARG;
+  *launches = h->launches;
   return MOE_OK;
 }
 

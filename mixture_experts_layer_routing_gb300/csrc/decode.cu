@@ -250,13 +250,23 @@ size_t decode_workspace_bytes(const Layer& L, int B) {
          al(sizeof(float) * na) + al(sizeof(float) * B * (L.k + 1) * L.f);
 }
 
-cudaError_t launch_decode(const Layer& L, const void* x, int B, void* y, void* ws, cudaStream_t s) {
+cudaError_t launch_decode_route(const Layer& L, const void* x, int B, void* ws, cudaStream_t s) {
   DecodeWs w = carve(L, B, ws);
   const int route_blocks = (B * L.E + kRouteWarps - 1) / kRouteWarps;
   decode_route_kernel<<<route_blocks, kRouteWarps * 32, 0, s>>>((const bf16*)x, (const bf16*)L.Wr, L.bias, B, L.d,
                                                                 L.E, L.k, L.S, L.router, L.renorm, L.scale, w,
                                                                 L.decode_counter);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_gateup(const Layer& L, const void* x, int B, void* ws, cudaStream_t s) {
+  DecodeWs w = carve(L, B, ws);
   decode_gateup_kernel<<<L.num_sms * 8, 256, 0, s>>>((const bf16*)x, (const bf16*)L.W13, L.d, L.f, L.G, L.k, w);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_down(const Layer& L, int B, void* y, void* ws, cudaStream_t s) {
+  DecodeWs w = carve(L, B, ws);
   const int down_blocks = (L.d + kDownWarps * kCols - 1) / (kDownWarps * kCols);
   const size_t smem = sizeof(float) * kDownWarps * B * kCols;
   decode_down_kernel<<<down_blocks, kDownWarps * 32, smem, s>>>((const bf16*)L.Wd, B, L.d, L.f, L.k, w, (bf16*)y);

@@ -31,10 +31,10 @@ struct Layer {
   int num_sms;
   bool has_weights;
   // tensor maps of the packed weights (bf16 tcgen05 path)
-  alignas(64) CUtensorMap tm_W13;       // K-major rows of W13 (box 64 x 256)
-  alignas(64) CUtensorMap tm_Wd;        // K-major rows of Wd (box 64 x 256)
-  alignas(64) CUtensorMap tm_W13_mn;    // W13 as [K=2f rows][N=d] for dx (box 64 x 64)
-  alignas(64) CUtensorMap tm_Wd_mn;     // Wd as [K=d rows][N=f] for the dY.Wd product (box 64 x 64)
+  CUtensorMap tm_W13;       // K-major rows of W13 (box 64 x 256)
+  CUtensorMap tm_Wd;        // K-major rows of Wd (box 64 x 256)
+  CUtensorMap tm_W13_mn;    // W13 as [K=2f rows][N=d] for dx (box 64 x 64)
+  CUtensorMap tm_Wd_mn;     // Wd as [K=d rows][N=f] for the dY.Wd product (box 64 x 64)
 };
 
 // Device buffers of one forward / backward, carved from the caller's workspace and context.
@@ -61,7 +61,7 @@ struct Bufs {
   // backward scratch
   void* dudv;            // [R, 2f]
   void* hg;              // [R, f]  gate * h
-  float* dg_part;        // [A, f / kGate]
+  float* dg_part;        // [A, f / 64] gate-gradient partials, one per 64 features
   void* dx_rows;         // [R, d]
   float* dl;             // [T, E]
   float* dgate;          // [T, k]
@@ -87,7 +87,9 @@ cudaError_t launch_pack_weights(const Layer& L, const void* Wr, const float* bia
                                 const void* Wu, const void* Wd, cudaStream_t s);
 // decode.cu
 size_t decode_workspace_bytes(const Layer& L, int B);
-cudaError_t launch_decode(const Layer& L, const void* x, int B, void* y, void* ws, cudaStream_t s);
+cudaError_t launch_decode_route(const Layer& L, const void* x, int B, void* ws, cudaStream_t s);
+cudaError_t launch_decode_gateup(const Layer& L, const void* x, int B, void* ws, cudaStream_t s);
+cudaError_t launch_decode_down(const Layer& L, int B, void* y, void* ws, cudaStream_t s);
 // tc_gemm.cu (bf16 tcgen05 path)
 bool tc_supported(const Layer& L);
 cudaError_t tc_init(Layer& L);   // encodes the weight tensor maps, sets kernel attributes

@@ -1,16 +1,552 @@
-// tcgen05 grouped GEMMs (bf16). Not yet enabled: tc_supported() reports false
-// and the bf16 path runs on the CUDA-core kernels.
+// bf16 grouped GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// One persistent kernel template serves the router logits and both expert
+// projections of the forward pass. Per CTA (one per SM):
+//   warps 0-3  producers: A rows pulled by token index with 16-byte cp.async
+//              into the 128-byte-swizzled K-major layout (the dispatch never
+//              materialises a permuted copy of x), or A by TMA when its rows are
+//              contiguous; B (weights) by TMA. STAGES-deep smem ring.
+//   warp 8     MMA issuer: tcgen05.mma kind::f16, M=128, N=BN, K=16, fp32
+//              accumulators in TMEM, double buffered (2 x BN columns).
+//   warps 4-7  epilogue: tcgen05.ld of the accumulator, fused epilogue
+//              (SwiGLU, gate scale, fp32 store), direct global stores.
+// Tiles are (segment, n-tile, m-tile) with m fastest, so CTAs running at the
+// same time share an expert's weight tile through L2.
+//
+// Pull dispatch and the fused, deterministic single call follow "Cursor
+// открыл код ядра Mixture of Experts ..." (dzen.guru), section "Три решения,
+// которые дали результат". Every accumulation runs in a fixed order
+// (K ascending inside one CTA), so results are bit-identical between runs.
+// Every wait on an mbarrier is bounded: past the limit the kernel records
+// MOE_ERR_TIMEOUT, drains its copies and MMAs, frees TMEM and returns.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
 #include "kernels.h"
 
 namespace moe {
-bool tc_supported(const Layer&) { return false; }
-cudaError_t tc_init(Layer&) { return cudaErrorNotSupported; }
-cudaError_t launch_tc_router_logits(const Layer&, const void*, int, float*, cudaStream_t) { return cudaErrorNotSupported; }
-cudaError_t launch_tc_gateup(const Layer&, const Bufs&, const void*, cudaStream_t) { return cudaErrorNotSupported; }
-cudaError_t launch_tc_down(const Layer&, const Bufs&, cudaStream_t) { return cudaErrorNotSupported; }
-cudaError_t launch_tc_bwd_dh(const Layer&, const Bufs&, const void*, cudaStream_t) { return cudaErrorNotSupported; }
-cudaError_t launch_tc_bwd_dx(const Layer&, const Bufs&, cudaStream_t) { return cudaErrorNotSupported; }
-cudaError_t launch_tc_bwd_dw(const Layer&, const Bufs&, const void*, const void*, void*, void*, void*, cudaStream_t) {
-  return cudaErrorNotSupported;
+
+namespace {
+
+constexpr int BM = 128, BK = 64, STAGES = 4, LAG = 2;
+constexpr int kProducerWarps = 4, kEpiWarps = 4;
+constexpr int kThreads = (kProducerWarps + kEpiWarps + 1) * 32;   // 288
+constexpr int kMmaWarp = kProducerWarps + kEpiWarps;               // warp 8
+
+enum { A_GATHER = 0, A_TMA = 1 };
+enum { EPI_SWIGLU = 0, EPI_GATE = 1, EPI_F32 = 2 };
+
+struct TcParams {
+  const bf16* A;          // gather source rows [*, K] (A_GATHER)
+  const int* row_token;   // sorted row -> source row (A_GATHER)
+  const int* off;         // [nseg+1] segment row offsets (null: dense)
+  const int* mt_off;      // [nseg+1] prefix of 128-row tiles
+  int nseg;
+  int dense_rows;         // dense mode: rows of the single segment
+  int K;                  // reduction length (multiple of 64)
+  int n_tiles;            // N / BN
+  int b_rows_per_seg;     // rows of B per segment in tmB
+  void* out;              // EPI_SWIGLU: h [R, ldo] bf16; EPI_GATE: o [R, ldo] bf16; EPI_F32: [rows, ldo] fp32
+  int ldo;
+  int n_valid;            // EPI_F32: columns to store
+  const float* row_gate;  // EPI_GATE
+  bf16* uv;               // EPI_SWIGLU: saved pre-activations [R, 2f] (nullable)
+  int ld_uv;
+  int* status;
+};
+
+// ------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false on timeout (recorded) or when another role aborted.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > kWaitLimitNs) {
+        set_error(status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor, kind::f16: bf16 A and B (K-major), fp32 accumulator, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
+          tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------- schedule
+struct Tile {
+  int e, m, n, row0, row_end;
+};
+
+__device__ __forceinline__ int total_tiles(const TcParams& p) {
+  if (!p.off) return ((p.dense_rows + BM - 1) / BM) * p.n_tiles;
+  return p.mt_off[p.nseg] * p.n_tiles;
+}
+
+__device__ __forceinline__ Tile map_tile(const TcParams& p, int L) {
+  Tile t;
+  if (!p.off) {
+    t.e = 0;
+    t.n = L % p.n_tiles;
+    t.m = L / p.n_tiles;
+    t.row0 = t.m * BM;
+    t.row_end = p.dense_rows;
+    return t;
+  }
+  int lo = 0, hi = p.nseg;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (p.mt_off[mid] * p.n_tiles <= L) lo = mid; else hi = mid;
+  }
+  const int Me = p.mt_off[lo + 1] - p.mt_off[lo];
+  const int local = L - p.mt_off[lo] * p.n_tiles;
+  t.e = lo;
+  t.n = local / Me;
+  t.m = local % Me;
+  t.row0 = p.off[lo] + t.m * BM;
+  t.row_end = p.off[lo + 1];
+  return t;
+}
+
+template <int BN>
+struct Smem {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int TOTAL = STAGES * STAGE + 1024 /*align*/ + 256 /*barriers*/;
+};
+
+// ------------------------------------------------------------------ kernel
+template <int BN, int AMODE, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcParams p) {
+  static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
+  constexpr uint32_t TMEM_COLS = 2 * BN <= 32 ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
+  constexpr uint32_t IDESC = idesc_bf16(BM, BN);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* stage_base = smem;
+  uint64_t* bars = (uint64_t*)(smem + STAGES * Smem<BN>::STAGE);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
+  const uint32_t tfull0 = smem_u32(bars + 2 * STAGES), tempty0 = smem_u32(bars + 2 * STAGES + 2);
+  const uint32_t drain = smem_u32(bars + 2 * STAGES + 4);
+  volatile int* abort_flag = (volatile int*)(bars + 2 * STAGES + 5);
+  uint32_t* tmem_slot = (uint32_t*)(bars + 2 * STAGES + 6);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, AMODE == A_GATHER ? kProducerWarps * 32 : 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, kEpiWarps * 32);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int ntiles = total_tiles(p);
+  const int nkb = p.K / BK;
+
+  if (warp < kProducerWarps) {
+    // ------------------------------------------------------------ producers
+    const int ptid = threadIdx.x;             // 0..127
+    int it = 0;
+    bool ok = true;
+    for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
+      const Tile t = map_tile(p, L);
+      const bf16* src[8];
+      uint32_t nbytes[8];
+      if (AMODE == A_GATHER) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int r = warp * 32 + j * 4 + (lane >> 3);   // tile row of this thread's j-th copy
+          const int row = t.row0 + r;
+          const bool v = row < t.row_end;
+          const int tok = v ? p.row_token[row] : 0;
+          src[j] = p.A + (size_t)tok * p.K + (lane & 7) * 8;
+          nbytes[j] = v ? 16u : 0u;
+        }
+      }
+      const int b_row = t.e * p.b_rows_per_seg + t.n * BN;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        if (!mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sa = smem_u32(stage_base + s * Smem<BN>::STAGE);
+        const uint32_t sb = sa + Smem<BN>::A_BYTES;
+        if (AMODE == A_GATHER) {
+          if (ptid == 0) {
+            mbar_expect_tx(full0 + 8 * s, Smem<BN>::B_BYTES);
+            tma_load_2d(sb, &tmB, kb * BK, b_row, full0 + 8 * s);
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int r = warp * 32 + j * 4 + (lane >> 3);
+            const int c = lane & 7;
+            const uint32_t dst = sa + r * 128 + ((c ^ (r & 7)) << 4);
+            cp_async16(dst, src[j] + kb * BK, nbytes[j]);
+          }
+          cp_async_commit();
+          if (it >= LAG) {
+            cp_async_wait<LAG>();
+            fence_proxy_async();
+            mbar_arrive(full0 + 8 * ((it - LAG) % STAGES));
+          }
+        } else if (ptid == 0) {
+          mbar_arrive_expect_tx(full0 + 8 * s, Smem<BN>::A_BYTES + Smem<BN>::B_BYTES);
+          tma_load_2d(sa, &tmA, kb * BK, t.row0, full0 + 8 * s);
+          tma_load_2d(sb, &tmB, kb * BK, b_row, full0 + 8 * s);
+        }
+      }
+    }
+    if (AMODE == A_GATHER) {
+      // complete the last LAG stages (the MMA waits for them even after an abort is seen)
+      cp_async_wait<0>();
+      fence_proxy_async();
+      for (int q = (it > LAG ? it - LAG : 0); q < it; ++q) mbar_arrive(full0 + 8 * (q % STAGES));
+    }
+  } else if (warp == kMmaWarp) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      int it = 0, tcount = 0;
+      bool ok = true;
+      for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x, ++tcount) {
+        const int acc = tcount & 1;
+        const uint32_t aph = (tcount >> 1) & 1;
+        if (!mbar_wait(tempty0 + 8 * acc, aph ^ 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t dcol = tmem_base + acc * BN;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait(full0 + 8 * s, ph, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(stage_base + s * Smem<BN>::STAGE);
+          const uint32_t sb = sa + Smem<BN>::A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_bf16(dcol, desc_kmajor_sw128(sa + k * 32), desc_kmajor_sw128(sb + k * 32), IDESC,
+                     (kb > 0 || k > 0) ? 1u : 0u);
+          mma_commit(empty0 + 8 * s);
+        }
+        if (!ok) break;
+        mma_commit(tfull0 + 8 * acc);
+      }
+      // drain: wait until every issued MMA has completed before TMEM is freed
+      mma_commit(drain);
+      const uint64_t t0 = global_ns();
+      while (!mbar_try_wait(drain, 0)) {
+        if (global_ns() - t0 > kWaitLimitNs) {
+          set_error(p.status, MOE_ERR_TIMEOUT);
+          break;
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - kProducerWarps;     // 0..3 == warp % 4: TMEM lanes 32*ew..
+    const int r = ew * 32 + lane;             // tile row
+    int tcount = 0;
+    for (int L = blockIdx.x; L < ntiles; L += gridDim.x, ++tcount) {
+      const Tile t = map_tile(p, L);
+      const int acc = tcount & 1;
+      const uint32_t aph = (tcount >> 1) & 1;
+      if (!mbar_wait(tfull0 + 8 * acc, aph, abort_flag, p.status)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(ew * 32) << 16);
+      const int row = t.row0 + r;
+      const bool valid = row < t.row_end;
+      if (EPI == EPI_SWIGLU) {
+        bf16* hrow = (bf16*)p.out + (size_t)row * p.ldo + t.n * (BN / 2);
+        bf16* uvrow = p.uv ? p.uv + (size_t)row * p.ld_uv + t.n * BN : nullptr;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN / 2; c0 += 32) {
+          uint32_t u[32], v[32];
+          tmem_ld32(tbase + c0, u);
+          tmem_ld32(tbase + BN / 2 + c0, v);
+          tmem_ld_wait();
+          if (valid) {
+            float hf[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float uf = __uint_as_float(u[i]);
+              hf[i] = silu_f(uf) * __uint_as_float(v[i]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(hrow + c0 + q * 8) = pack8(hf + q * 8);
+            if (uvrow) {
+              float uf[32], vf[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                uf[i] = __uint_as_float(u[i]);
+                vf[i] = __uint_as_float(v[i]);
+              }
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                *reinterpret_cast<uint4*>(uvrow + c0 + q * 8) = pack8(uf + q * 8);
+                *reinterpret_cast<uint4*>(uvrow + BN / 2 + c0 + q * 8) = pack8(vf + q * 8);
+              }
+            }
+          }
+        }
+      } else if (EPI == EPI_GATE) {
+        const float g = valid ? p.row_gate[row] : 0.f;
+        bf16* orow = (bf16*)p.out + (size_t)row * p.ldo + t.n * BN;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t a[32];
+          tmem_ld32(tbase + c0, a);
+          tmem_ld_wait();
+          if (valid) {
+            float of[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) of[i] = g * __uint_as_float(a[i]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(orow + c0 + q * 8) = pack8(of + q * 8);
+          }
+        }
+      } else {
+        float* orow = (float*)p.out + (size_t)row * p.ldo + t.n * BN;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t a[32];
+          tmem_ld32(tbase + c0, a);
+          tmem_ld_wait();
+          if (valid) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (t.n * BN + c0 + i < p.n_valid) orow[c0 + i] = __uint_as_float(a[i]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty0 + 8 * acc);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// -------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor map over [rows][cols] (cols contiguous), box box_cols x box_rows, 128-byte swizzle.
+bool make_tmap(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+               uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int AMODE, int EPI>
+cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcParams& p, int grid, cudaStream_t s) {
+  auto kern = tc_gemm_kernel<BN, AMODE, EPI>;
+  const int smem = Smem<BN>::TOTAL;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  kern<<<grid, kThreads, smem, s>>>(tmA, tmB, p);
+  return cudaGetLastError();
+}
+
+constexpr int kBNup = 256;     // gate/up: 128 gate + 128 up columns
+constexpr int kBNdown = 256;
+constexpr int kBNrouter = 256;
+
+}  // namespace
+
+bool tc_supported(const Layer& L) {
+  return L.prec == MOE_BF16 && L.d % 256 == 0 && L.f % kGate == 0 && L.G == kGate && L.E <= kBNrouter &&
+         encode_fn() != nullptr;
+}
+
+cudaError_t tc_init(Layer& L) {
+  const uint64_t nseg = L.E + L.S;
+  if (!make_tmap(&L.tm_W13, L.W13, L.d, nseg * 2 * L.f, BK, kBNup)) return cudaErrorInvalidValue;
+  if (!make_tmap(&L.tm_Wd, L.Wd, L.f, nseg * L.d, BK, kBNdown)) return cudaErrorInvalidValue;
+  return cudaSuccess;
+}
+
+cudaError_t launch_tc_router_logits(const Layer& L, const void* x, int T, float* logits, cudaStream_t s) {
+  CUtensorMap tx, tw;
+  if (!make_tmap(&tx, x, L.d, T, BK, BM) || !make_tmap(&tw, L.Wr, L.d, L.E, BK, kBNrouter))
+    return cudaErrorInvalidValue;
+  TcParams p = {};
+  p.dense_rows = T;
+  p.K = L.d;
+  p.n_tiles = 1;
+  p.b_rows_per_seg = 0;
+  p.out = logits;
+  p.ldo = L.E;
+  p.n_valid = L.E;
+  p.status = L.status;
+  const int tiles = (T + BM - 1) / BM;
+  return launch<kBNrouter, A_TMA, EPI_F32>(tx, tw, p, tiles < L.num_sms ? tiles : L.num_sms, s);
+}
+
+cudaError_t launch_tc_gateup(const Layer& L, const Bufs& B, const void* x, cudaStream_t s) {
+  TcParams p = {};
+  p.A = (const bf16*)x;
+  p.row_token = B.row_token;
+  p.off = B.off;
+  p.mt_off = B.mt_off;
+  p.nseg = L.E + L.S;
+  p.K = L.d;
+  p.n_tiles = 2 * L.f / kBNup;
+  p.b_rows_per_seg = 2 * L.f;
+  p.out = B.h;
+  p.ldo = L.f;
+  p.uv = (bf16*)B.uv;
+  p.ld_uv = 2 * L.f;
+  p.status = L.status;
+  return launch<kBNup, A_GATHER, EPI_SWIGLU>(L.tm_W13 /*unused*/, L.tm_W13, p, L.num_sms, s);
+}
+
+cudaError_t launch_tc_down(const Layer& L, const Bufs& B, cudaStream_t s) {
+  CUtensorMap th;
+  if (!make_tmap(&th, B.h, L.f, B.R, BK, BM)) return cudaErrorInvalidValue;
+  TcParams p = {};
+  p.off = B.off;
+  p.mt_off = B.mt_off;
+  p.nseg = L.E + L.S;
+  p.K = L.f;
+  p.n_tiles = L.d / kBNdown;
+  p.b_rows_per_seg = L.d;
+  p.out = B.o;
+  p.ldo = L.d;
+  p.row_gate = B.row_gate;
+  p.status = L.status;
+  return launch<kBNdown, A_TMA, EPI_GATE>(th, L.tm_Wd, p, L.num_sms, s);
+}
+
+// The backward GEMMs run on the CUDA-core kernels for now.
+cudaError_t launch_tc_bwd_dh(const Layer& L, const Bufs& B, const void* dy, cudaStream_t s) {
+  return launch_simt_bwd_dh(L, B, dy, s);
+}
+cudaError_t launch_tc_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s) { return launch_simt_bwd_dx(L, B, s); }
+cudaError_t launch_tc_bwd_dw(const Layer& L, const Bufs& B, const void* x, const void* dy, void* dWg, void* dWu,
+                             void* dWd, cudaStream_t s) {
+  return launch_simt_bwd_dw(L, B, x, dy, dWg, dWu, dWd, s);
+}
+
 }  // namespace moe

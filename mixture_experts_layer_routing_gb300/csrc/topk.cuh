@@ -20,7 +20,7 @@ __device__ __forceinline__ void warp_topk_gates(const float* lr, const float* __
 #pragma unroll
   for (int q = 0; q < PER; ++q) {
     const int e = lane + 32 * q;
-    lg[q] = e < E ? lr[e] : 0.f;
+    lg[q] = e < E ? __ldcg(lr + e) : 0.f;   // L2 read: logits may come from other blocks
     key[q] = e < E ? lg[q] + bias[e] : -INFINITY;
   }
   unsigned taken = 0;                       // bit q: expert lane + 32q already selected
