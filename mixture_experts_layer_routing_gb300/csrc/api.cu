@@ -8,6 +8,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "handle.h"
 #include "kernels.h"
 
 using namespace moe;
@@ -20,22 +21,6 @@ enum Group {
 static const char* kGroupNames[G_COUNT] = {
     "router_logits", "topk", "scan_permute", "gateup", "down", "combine", "bwd_dh", "bwd_dx", "router_bwd",
     "dx_gather", "bwd_dw", "decode_route", "decode_gateup", "decode_down", "pack_weights"};
-
-struct ProfRec {
-  int group, kernels;
-  cudaEvent_t a, b;
-};
-
-struct moe_handle_s {
-  moe_config cfg;
-  Layer L;
-  int device;
-  bool tc;   // bf16 tensor-core path available for this shape
-  bool prof = false;
-  long long launches = 0;
-  std::vector<ProfRec> recs;
-  std::vector<cudaEvent_t> pool;
-};
 
 namespace {
 

@@ -1,0 +1,21 @@
+// The opaque handle behind moe_handle (internal to the library).
+#pragma once
+#include <vector>
+
+#include "kernels.h"
+
+struct ProfRec {
+  int group, kernels;
+  cudaEvent_t a, b;
+};
+
+struct moe_handle_s {
+  moe_config cfg;
+  moe::Layer L;
+  int device;
+  bool tc;   // bf16 tensor-core path available for this shape
+  bool prof = false;
+  long long launches = 0;
+  std::vector<ProfRec> recs;
+  std::vector<cudaEvent_t> pool;
+};
