@@ -143,6 +143,27 @@ moe_status moe_decode(moe_handle h, const void* x, int B, void* y, void* workspa
  * device status word into *device_status (MOE_OK if no device error). */
 moe_status moe_get_status(moe_handle h, void* stream, int* device_status);
 
+/* Routing for callers that cannot allocate device memory: the same outputs
+ * as moe_route with logits computed from x (logits, idx, gate, cnt, off, perm,
+ * inv; all required, device, caller-owned), without a workspace argument. The
+ * pages describe no such call; it exists for callers that may not allocate,
+ * such as a plugin inside a host program that owns all device memory, or a
+ * serving loop that bans cudaMalloc/cudaFree after start-up because they can
+ * block and synchronise the device.
+ * Its scratch is one fixed 4 MiB array inside the library (held on every GPU
+ * that loads the library until the process exits). A call needs
+ *   2*pad(4*ceil(T*k/1024)*E) + 3*pad(4*(E+S+1)) + 2*pad(4*T*(k+S)) bytes,
+ * pad() rounding up to 256; larger T returns MOE_ERR_WORKSPACE before any
+ * launch (E = 256, k = 8, S = 1 allows T up to 47,616 tokens).
+ * The first call on a device looks up the array's address there; make that
+ * first call before any stream capture. Every call on a device shares the one
+ * array and it keeps the last call's contents (each call writes every entry
+ * it reads, so none needs clearing); calls whose GPU work overlaps (other
+ * streams, other handles) race and must be serialised by the caller. The
+ * handle's device must be current. Calls no CUDA allocation routine. */
+moe_status moe_route_noalloc(moe_handle h, const void* x, int T, float* logits, int32_t* idx, float* gate,
+                             int32_t* cnt, int32_t* off, int32_t* perm, int32_t* inv, void* stream);
+
 /* Tracing. When enabled, every kernel launch of later calls on this handle is
  * bracketed by two CUDA events recorded on the call's stream (no extra device
  * memory). moe_profile_read waits for the recorded events and returns, for

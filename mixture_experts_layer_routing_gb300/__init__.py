@@ -23,7 +23,7 @@ MOE_FP32, MOE_BF16, MOE_MXFP8 = 0, 1, 2
 
 EXPORTED = ("moe_create", "moe_destroy", "moe_workspace_size", "moe_set_weights", "moe_route", "moe_forward",
             "moe_backward", "moe_decode", "moe_get_status", "moe_profile_enable", "moe_profile_read",
-            "moe_launch_count", "moe_status_string")
+            "moe_launch_count", "moe_route_noalloc", "moe_status_string")
 
 
 class MoeError(RuntimeError):
@@ -64,6 +64,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_profile_enable.argtypes = [vp, i32]
     lib.moe_profile_read.argtypes = [vp, i32, ctypes.c_char_p, P(ctypes.c_longlong), P(ctypes.c_double), P(i32)]
     lib.moe_launch_count.argtypes = [vp, P(ctypes.c_longlong)]
+    lib.moe_route_noalloc.argtypes = [vp, vp, i32] + [vp] * 8
     lib.moe_status_string.argtypes = [i32]
     lib.moe_status_string.restype = ctypes.c_char_p
     for name in EXPORTED[:-1]:
@@ -127,6 +128,12 @@ def moe_route(h, x, T, logits_override, logits, idx, gate, cnt, off, perm, inv, 
     _check(load_library().moe_route(h, _ptr(x), T, _ptr(logits_override), _ptr(logits), _ptr(idx), _ptr(gate),
                                     _ptr(cnt), _ptr(off), _ptr(perm), _ptr(inv), _ptr(workspace), _stream(stream)),
            "moe_route")
+
+
+def moe_route_noalloc(h, x, T, logits, idx, gate, cnt, off, perm, inv, stream=None):
+    """Routing without a workspace (scratch in a fixed array inside the library); see include/moe.h."""
+    _check(load_library().moe_route_noalloc(h, _ptr(x), T, _ptr(logits), _ptr(idx), _ptr(gate), _ptr(cnt),
+                                            _ptr(off), _ptr(perm), _ptr(inv), _stream(stream)), "moe_route_noalloc")
 
 
 def moe_forward(h, x, T, y, ctx, workspace, stream=None):
