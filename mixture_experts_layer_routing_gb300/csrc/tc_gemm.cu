@@ -1,24 +1,31 @@
 // bf16 grouped GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
 //
-// One persistent kernel template serves the router logits and both expert
-// projections of the forward pass. Per CTA (one per SM):
-//   warps 0-3  producers: A rows pulled by token index with 16-byte cp.async
-//              into the 128-byte-swizzled K-major layout (the dispatch never
-//              materialises a permuted copy of x), or A by TMA when its rows are
-//              contiguous; B (weights) by TMA. STAGES-deep smem ring.
+// One persistent kernel template serves every GEMM of the layer: the router
+// logits, both expert projections of the forward pass, and the four grouped
+// products of the backward pass. Per CTA (one per SM):
+//   warps 0-3  producers: operands pulled by token index with 16-byte cp.async
+//              into the 128-byte-swizzled layout the MMA reads (the dispatch
+//              never materialises a permuted copy of x or dy), or loaded by TMA
+//              when their rows are contiguous. STAGES-deep smem ring.
 //   warp 8     MMA issuer: tcgen05.mma kind::f16, M=128, N=BN, K=16, fp32
 //              accumulators in TMEM, double buffered (2 x BN columns).
-//   warps 4-7  epilogue: tcgen05.ld of the accumulator, fused epilogue
-//              (SwiGLU, gate scale, fp32 store), direct global stores.
-// Tiles are (segment, n-tile, m-tile) with m fastest, so CTAs running at the
-// same time share an expert's weight tile through L2.
+//   warps 4-7  epilogue: tcgen05.ld of the accumulator and a fused epilogue
+//              (SwiGLU, gate scale, SwiGLU backward + gate gradient, stores).
+// Operands are K-major (rows contiguous along K) or MN-major (rows contiguous
+// along M or N, K the row index): the backward reads the weights transposed
+// and reduces the weight gradients over each expert's token segment without
+// any transposed copy.
+// Schedules: SEG_M, tiles (segment, n-tile, m-tile) over the sorted rows of
+// each expert with m fastest, so CTAs running together share an expert's
+// weight tile through L2; DENSE, one segment; SEG_K, tiles (segment, n, m) of
+// a per-expert weight gradient whose K runs over that expert's sorted rows.
 //
-// Pull dispatch and the fused, deterministic single call follow "Cursor
+// Pull dispatch and one fused, deterministic call per step follow "Cursor
 // открыл код ядра Mixture of Experts ..." (dzen.guru), section "Три решения,
-// которые дали результат". Every accumulation runs in a fixed order
-// (K ascending inside one CTA), so results are bit-identical between runs.
-// Every wait on an mbarrier is bounded: past the limit the kernel records
-// MOE_ERR_TIMEOUT, drains its copies and MMAs, frees TMEM and returns.
+// которые дали результат". Each output element is accumulated in one CTA in
+// ascending K order, so results are bit-identical between runs. Every wait on
+// an mbarrier is bounded: past the limit the kernel records MOE_ERR_TIMEOUT,
+// drains its copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -32,26 +39,37 @@ constexpr int BM = 128, BK = 64, STAGES = 4, LAG = 2;
 constexpr int kProducerWarps = 4, kEpiWarps = 4;
 constexpr int kThreads = (kProducerWarps + kEpiWarps + 1) * 32;   // 288
 constexpr int kMmaWarp = kProducerWarps + kEpiWarps;               // warp 8
+constexpr int kChunkBytes = 64 * 128;                              // 64 rows of 128 bytes (one MN-major column chunk)
 
-enum { A_GATHER = 0, A_TMA = 1 };
-enum { EPI_SWIGLU = 0, EPI_GATE = 1, EPI_F32 = 2 };
+enum { A_GATHER_K = 0, A_TMA_K = 1, A_TMA_MN = 2, A_GATHER_MN = 3 };
+enum { B_TMA_K = 0, B_TMA_MN = 1, B_GATHER_MN = 2 };
+enum { SCHED_SEG_M = 0, SCHED_DENSE = 1, SCHED_SEG_K = 2 };
+enum { EPI_SWIGLU = 0, EPI_GATE = 1, EPI_F32 = 2, EPI_DH = 3, EPI_STORE = 4, EPI_DW13 = 5, EPI_DWD = 6 };
 
 struct TcParams {
-  const bf16* A;          // gather source rows [*, K] (A_GATHER)
-  const int* row_token;   // sorted row -> source row (A_GATHER)
-  const int* off;         // [nseg+1] segment row offsets (null: dense)
-  const int* mt_off;      // [nseg+1] prefix of 128-row tiles
+  const bf16* A;          // gathered A rows [*, lda]     (A_GATHER_*)
+  int lda;
+  const bf16* Bsrc;       // gathered B rows [*, ldb]     (B_GATHER_MN)
+  int ldb;
+  const int* row_token;   // sorted row -> token
+  const int* off;         // [nseg+1] segment row offsets
+  const int* mt_off;      // [nseg+1] prefix of 128-row tiles (SEG_M)
   int nseg;
-  int dense_rows;         // dense mode: rows of the single segment
-  int K;                  // reduction length (multiple of 64)
+  int dense_rows;         // DENSE: rows of the single segment
+  int K;                  // reduction length for SEG_M / DENSE (multiple of 64)
+  int m_tiles;            // SEG_K: M / 128
   int n_tiles;            // N / BN
-  int b_rows_per_seg;     // rows of B per segment in tmB
-  void* out;              // EPI_SWIGLU: h [R, ldo] bf16; EPI_GATE: o [R, ldo] bf16; EPI_F32: [rows, ldo] fp32
+  int b_rows_per_seg;     // B by TMA: first row of segment e is e * b_rows_per_seg (SEG_M / DENSE)
+  void* out;              // primary output (see the epilogues)
   int ldo;
   int n_valid;            // EPI_F32: columns to store
-  const float* row_gate;  // EPI_GATE
-  bf16* uv;               // EPI_SWIGLU: saved pre-activations [R, 2f] (nullable)
+  void* out2;             // EPI_DH: g*h [R, f]; EPI_DW13: dWu
+  const float* row_gate;  // EPI_GATE, EPI_DH
+  bf16* uv;               // EPI_SWIGLU: saved pre-activations (nullable); EPI_DH: read
   int ld_uv;
+  float* dg_part;         // EPI_DH: gate-gradient partials [A_rows, dg_slots]
+  int dg_slots;
+  int A_rows;             // routed rows (rows >= A_rows are the shared expert)
   int* status;
 };
 
@@ -116,14 +134,22 @@ __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t addr) {
+// Shared-memory matrix descriptors (128-byte swizzle, version 1).
+// K-major: rows of 128 bytes along K, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t addr) {
   return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
-// Instruction descriptor, kind::f16: bf16 A and B (K-major), fp32 accumulator, M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// MN-major: 64 M/N elements (128 bytes) per row, one row per K index; 8-row K
+// groups 1024 bytes apart; 64-element M/N chunks kChunkBytes apart.
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)(kChunkBytes >> 4) << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, M x N, operand majors.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
@@ -147,24 +173,43 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+__device__ __forceinline__ void unpack8_to(const bf16* p, float* f) { unpack8(*reinterpret_cast<const uint4*>(p), f); }
+
 // ---------------------------------------------------------------- schedule
 struct Tile {
-  int e, m, n, row0, row_end;
+  int e, m, n;
+  int row0, row_end;   // SEG_M / DENSE: output rows; SEG_K: the segment's sorted rows (the K range)
+  int nkb;             // K blocks of 64
 };
 
+template <int SCHED>
 __device__ __forceinline__ int total_tiles(const TcParams& p) {
-  if (!p.off) return ((p.dense_rows + BM - 1) / BM) * p.n_tiles;
+  if (SCHED == SCHED_DENSE) return ((p.dense_rows + BM - 1) / BM) * p.n_tiles;
+  if (SCHED == SCHED_SEG_K) return p.nseg * p.m_tiles * p.n_tiles;
   return p.mt_off[p.nseg] * p.n_tiles;
 }
 
+template <int SCHED>
 __device__ __forceinline__ Tile map_tile(const TcParams& p, int L) {
   Tile t;
-  if (!p.off) {
+  if (SCHED == SCHED_DENSE) {
     t.e = 0;
     t.n = L % p.n_tiles;
     t.m = L / p.n_tiles;
     t.row0 = t.m * BM;
     t.row_end = p.dense_rows;
+    t.nkb = p.K / BK;
+    return t;
+  }
+  if (SCHED == SCHED_SEG_K) {
+    const int per = p.m_tiles * p.n_tiles;
+    t.e = L / per;
+    const int rem = L % per;
+    t.n = rem / p.m_tiles;
+    t.m = rem % p.m_tiles;
+    t.row0 = p.off[t.e];
+    t.row_end = p.off[t.e + 1];
+    t.nkb = (t.row_end - t.row0 + BK - 1) / BK;
     return t;
   }
   int lo = 0, hi = p.nseg;
@@ -179,6 +224,7 @@ __device__ __forceinline__ Tile map_tile(const TcParams& p, int L) {
   t.m = local % Me;
   t.row0 = p.off[lo] + t.m * BM;
   t.row_end = p.off[lo + 1];
+  t.nkb = p.K / BK;
   return t;
 }
 
@@ -190,13 +236,80 @@ struct Smem {
   static constexpr int TOTAL = STAGES * STAGE + 1024 /*align*/ + 256 /*barriers*/;
 };
 
+template <int AMODE, int BMODE>
+struct Modes {
+  static constexpr bool kCpAsync = AMODE == A_GATHER_K || AMODE == A_GATHER_MN || BMODE == B_GATHER_MN;
+  static constexpr int kAMn = (AMODE == A_TMA_MN || AMODE == A_GATHER_MN) ? 1 : 0;
+  static constexpr int kBMn = (BMODE == B_TMA_MN || BMODE == B_GATHER_MN) ? 1 : 0;
+};
+
+// Issues one stage: A and B of K block kb of tile t.
+template <int BN, int AMODE, int BMODE, int SCHED>
+__device__ __forceinline__ void load_stage(const TcParams& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                           const Tile& t, int kb, uint32_t sa, uint32_t sb, uint32_t full_bar,
+                                           const bf16* const (&gsrc)[8], const uint32_t (&gbytes)[8]) {
+  constexpr uint32_t tma_bytes = (AMODE == A_TMA_K || AMODE == A_TMA_MN ? Smem<BN>::A_BYTES : 0) +
+                                 (BMODE == B_TMA_K || BMODE == B_TMA_MN ? Smem<BN>::B_BYTES : 0);
+  const int ptid = threadIdx.x;
+  if (ptid == 0 && tma_bytes) {
+    if (Modes<AMODE, BMODE>::kCpAsync) mbar_expect_tx(full_bar, tma_bytes);
+    else mbar_arrive_expect_tx(full_bar, tma_bytes);
+    if (AMODE == A_TMA_K) tma_load_2d(sa, tmA, kb * BK, t.row0, full_bar);
+    if (AMODE == A_TMA_MN) {
+#pragma unroll
+      for (int j = 0; j < BM / 64; ++j) tma_load_2d(sa + j * kChunkBytes, tmA, t.m * BM + j * 64, t.row0 + kb * BK, full_bar);
+    }
+    if (BMODE == B_TMA_K) tma_load_2d(sb, tmB, kb * BK, t.e * p.b_rows_per_seg + t.n * BN, full_bar);
+    if (BMODE == B_TMA_MN) {
+      const int krow = (SCHED == SCHED_SEG_K ? t.row0 : t.e * p.b_rows_per_seg) + kb * BK;
+#pragma unroll
+      for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * kChunkBytes, tmB, t.n * BN + j * 64, krow, full_bar);
+    }
+  }
+  if (AMODE == A_GATHER_K) {
+    const int warp = ptid >> 5, lane = ptid & 31;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int r = warp * 32 + j * 4 + (lane >> 3);
+      const int c = lane & 7;
+      cp_async16(sa + r * 128 + ((c ^ (r & 7)) << 4), gsrc[j] + kb * BK, gbytes[j]);
+    }
+  }
+  if (AMODE == A_GATHER_MN || BMODE == B_GATHER_MN) {
+    // one K row (sorted row of the segment) per thread pair
+    const int kk = ptid >> 1, half = ptid & 1;
+    const int row = t.row0 + kb * BK + kk;
+    const bool v = row < t.row_end;
+    const int tok = v ? p.row_token[row] : 0;
+    const uint32_t nb = v ? 16u : 0u;
+    const uint32_t swz = (uint32_t)(kk & 7);
+    if (AMODE == A_GATHER_MN) {
+      const bf16* src = p.A + (size_t)tok * p.lda + t.m * BM + half * 64;
+      const uint32_t dst = sa + half * kChunkBytes + kk * 128;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) cp_async16(dst + ((q ^ swz) << 4), src + q * 8, nb);
+    }
+    if (BMODE == B_GATHER_MN) {
+#pragma unroll
+      for (int jj = 0; jj < BN / 128; ++jj) {
+        const int j = half * (BN / 128) + jj;
+        const bf16* src = p.Bsrc + (size_t)tok * p.ldb + t.n * BN + j * 64;
+        const uint32_t dst = sb + j * kChunkBytes + kk * 128;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) cp_async16(dst + ((q ^ swz) << 4), src + q * 8, nb);
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ kernel
-template <int BN, int AMODE, int EPI>
+template <int BN, int AMODE, int BMODE, int SCHED, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcParams p) {
-  static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
-  constexpr uint32_t TMEM_COLS = 2 * BN <= 32 ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
-  constexpr uint32_t IDESC = idesc_bf16(BM, BN);
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
+  using MD = Modes<AMODE, BMODE>;
+  constexpr uint32_t TMEM_COLS = 2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512);
+  constexpr uint32_t IDESC = idesc_bf16(BM, BN, MD::kAMn, MD::kBMn);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* stage_base = smem;
@@ -211,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full0 + 8 * s, AMODE == A_GATHER ? kProducerWarps * 32 : 1);
+      mbar_init(full0 + 8 * s, MD::kCpAsync ? kProducerWarps * 32 : 1);
       mbar_init(empty0 + 8 * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -232,31 +345,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int ntiles = total_tiles(p);
-  const int nkb = p.K / BK;
+  const int ntiles = total_tiles<SCHED>(p);
 
   if (warp < kProducerWarps) {
     // ------------------------------------------------------------ producers
-    const int ptid = threadIdx.x;             // 0..127
     int it = 0;
     bool ok = true;
     for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
-      const Tile t = map_tile(p, L);
-      const bf16* src[8];
-      uint32_t nbytes[8];
-      if (AMODE == A_GATHER) {
+      const Tile t = map_tile<SCHED>(p, L);
+      const bf16* gsrc[8];
+      uint32_t gbytes[8];
+      if (AMODE == A_GATHER_K) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const int r = warp * 32 + j * 4 + (lane >> 3);   // tile row of this thread's j-th copy
+          const int r = warp * 32 + j * 4 + (lane >> 3);
           const int row = t.row0 + r;
           const bool v = row < t.row_end;
           const int tok = v ? p.row_token[row] : 0;
-          src[j] = p.A + (size_t)tok * p.K + (lane & 7) * 8;
-          nbytes[j] = v ? 16u : 0u;
+          gsrc[j] = p.A + (size_t)tok * p.lda + (lane & 7) * 8;
+          gbytes[j] = v ? 16u : 0u;
         }
       }
-      const int b_row = t.e * p.b_rows_per_seg + t.n * BN;
-      for (int kb = 0; kb < nkb; ++kb, ++it) {
+      for (int kb = 0; kb < t.nkb; ++kb, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
         if (!mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, p.status)) {
@@ -265,32 +375,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t sa = smem_u32(stage_base + s * Smem<BN>::STAGE);
         const uint32_t sb = sa + Smem<BN>::A_BYTES;
-        if (AMODE == A_GATHER) {
-          if (ptid == 0) {
-            mbar_expect_tx(full0 + 8 * s, Smem<BN>::B_BYTES);
-            tma_load_2d(sb, &tmB, kb * BK, b_row, full0 + 8 * s);
-          }
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int r = warp * 32 + j * 4 + (lane >> 3);
-            const int c = lane & 7;
-            const uint32_t dst = sa + r * 128 + ((c ^ (r & 7)) << 4);
-            cp_async16(dst, src[j] + kb * BK, nbytes[j]);
-          }
+        load_stage<BN, AMODE, BMODE, SCHED>(p, &tmA, &tmB, t, kb, sa, sb, full0 + 8 * s, gsrc, gbytes);
+        if (MD::kCpAsync) {
           cp_async_commit();
           if (it >= LAG) {
             cp_async_wait<LAG>();
             fence_proxy_async();
             mbar_arrive(full0 + 8 * ((it - LAG) % STAGES));
           }
-        } else if (ptid == 0) {
-          mbar_arrive_expect_tx(full0 + 8 * s, Smem<BN>::A_BYTES + Smem<BN>::B_BYTES);
-          tma_load_2d(sa, &tmA, kb * BK, t.row0, full0 + 8 * s);
-          tma_load_2d(sb, &tmB, kb * BK, b_row, full0 + 8 * s);
         }
       }
     }
-    if (AMODE == A_GATHER) {
+    if (MD::kCpAsync) {
       // complete the last LAG stages (the MMA waits for them even after an abort is seen)
       cp_async_wait<0>();
       fence_proxy_async();
@@ -302,12 +398,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0, tcount = 0;
       bool ok = true;
       for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x, ++tcount) {
+        const Tile t = map_tile<SCHED>(p, L);
         const int acc = tcount & 1;
         const uint32_t aph = (tcount >> 1) & 1;
         if (!mbar_wait(tempty0 + 8 * acc, aph ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t dcol = tmem_base + acc * BN;
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
+        for (int kb = 0; kb < t.nkb; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!mbar_wait(full0 + 8 * s, ph, abort_flag, p.status)) {
@@ -318,9 +415,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = smem_u32(stage_base + s * Smem<BN>::STAGE);
           const uint32_t sb = sa + Smem<BN>::A_BYTES;
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            mma_bf16(dcol, desc_kmajor_sw128(sa + k * 32), desc_kmajor_sw128(sb + k * 32), IDESC,
-                     (kb > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t da = MD::kAMn ? desc_mnmajor(sa + k * 2048) : desc_kmajor(sa + k * 32);
+            const uint64_t db = MD::kBMn ? desc_mnmajor(sb + k * 2048) : desc_kmajor(sb + k * 32);
+            mma_bf16(dcol, da, db, IDESC, (kb > 0 || k > 0) ? 1u : 0u);
+          }
           mma_commit(empty0 + 8 * s);
         }
         if (!ok) break;
@@ -343,13 +442,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = ew * 32 + lane;             // tile row
     int tcount = 0;
     for (int L = blockIdx.x; L < ntiles; L += gridDim.x, ++tcount) {
-      const Tile t = map_tile(p, L);
+      const Tile t = map_tile<SCHED>(p, L);
       const int acc = tcount & 1;
       const uint32_t aph = (tcount >> 1) & 1;
       if (!mbar_wait(tfull0 + 8 * acc, aph, abort_flag, p.status)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(ew * 32) << 16);
-      const int row = t.row0 + r;
+      const int row = t.row0 + r;   // SEG_M / DENSE output row
       const bool valid = row < t.row_end;
       if (EPI == EPI_SWIGLU) {
         bf16* hrow = (bf16*)p.out + (size_t)row * p.ldo + t.n * (BN / 2);
@@ -361,21 +460,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tbase + BN / 2 + c0, v);
           tmem_ld_wait();
           if (valid) {
-            float hf[32];
+            float hf[32], uf[32], vf[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              const float uf = __uint_as_float(u[i]);
-              hf[i] = silu_f(uf) * __uint_as_float(v[i]);
+              uf[i] = __uint_as_float(u[i]);
+              vf[i] = __uint_as_float(v[i]);
+              hf[i] = silu_f(uf[i]) * vf[i];
             }
 #pragma unroll
             for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(hrow + c0 + q * 8) = pack8(hf + q * 8);
             if (uvrow) {
-              float uf[32], vf[32];
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                uf[i] = __uint_as_float(u[i]);
-                vf[i] = __uint_as_float(v[i]);
-              }
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
                 *reinterpret_cast<uint4*>(uvrow + c0 + q * 8) = pack8(uf + q * 8);
@@ -384,8 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-      } else if (EPI == EPI_GATE) {
-        const float g = valid ? p.row_gate[row] : 0.f;
+      } else if (EPI == EPI_GATE || EPI == EPI_STORE) {
+        const float g = (EPI == EPI_GATE && valid) ? p.row_gate[row] : 1.f;
         bf16* orow = (bf16*)p.out + (size_t)row * p.ldo + t.n * BN;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -400,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(orow + c0 + q * 8) = pack8(of + q * 8);
           }
         }
-      } else {
+      } else if (EPI == EPI_F32) {
         float* orow = (float*)p.out + (size_t)row * p.ldo + t.n * BN;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -412,6 +506,79 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i)
               if (t.n * BN + c0 + i < p.n_valid) orow[c0 + i] = __uint_as_float(a[i]);
           }
+        }
+      } else if (EPI == EPI_DH) {
+        // r = dy_t Wd[e] for 128 features n*128..: SwiGLU backward with the saved u, v;
+        // dg partials over each 64-feature half.
+        static_assert(EPI != EPI_DH || BN == 128, "EPI_DH works on one 128-feature block");
+        const float g = valid ? p.row_gate[row] : 0.f;
+        const bf16* urow = p.uv + (size_t)row * p.ld_uv + t.n * 256;
+        bf16* durow = (bf16*)p.out + (size_t)row * p.ld_uv + t.n * 256;
+        bf16* hgrow = (bf16*)p.out2 + (size_t)row * p.ldo + t.n * 128;
+        float dgp = 0.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t a[32];
+          tmem_ld32(tbase + c0, a);
+          tmem_ld_wait();
+          if (valid) {
+            float uf[32], vf[32], du[32], dv[32], hg[32];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              unpack8_to(urow + c0 + q * 8, uf + q * 8);
+              unpack8_to(urow + 128 + c0 + q * 8, vf + q * 8);
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float rr = __uint_as_float(a[i]);
+              const float su = sigmoid_f(uf[i]);
+              const float sl = uf[i] * su;
+              const float hv = sl * vf[i];
+              dgp = fmaf(rr, hv, dgp);
+              const float dh = g * rr;
+              du[i] = dh * vf[i] * su * (1.f + uf[i] * (1.f - su));
+              dv[i] = dh * sl;
+              hg[i] = g * hv;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              *reinterpret_cast<uint4*>(durow + c0 + q * 8) = pack8(du + q * 8);
+              *reinterpret_cast<uint4*>(durow + 128 + c0 + q * 8) = pack8(dv + q * 8);
+              *reinterpret_cast<uint4*>(hgrow + c0 + q * 8) = pack8(hg + q * 8);
+            }
+            if ((c0 & 63) == 32) {
+              if (row < p.A_rows) p.dg_part[(size_t)row * p.dg_slots + (t.n * 128 + c0 - 32) / 64] = dgp;
+              dgp = 0.f;
+            }
+          }
+        }
+      } else {
+        // weight gradients: tile rows are rows of dW13 (packed) or dWd
+        const bool empty = t.nkb == 0;
+        bf16* orow;
+        if (EPI == EPI_DW13) {
+          // an M tile of 128 packed rows is all gate rows (m even) or all up rows (m odd)
+          bf16* base = (t.m & 1) ? (bf16*)p.out2 : (bf16*)p.out;
+          const int feat = (t.m >> 1) * BM + r;
+          orow = base + ((size_t)t.e * (p.m_tiles / 2) * BM + feat) * p.ldo + t.n * BN;
+        } else {
+          orow = (bf16*)p.out + ((size_t)t.e * p.m_tiles * BM + t.m * BM + r) * p.ldo + t.n * BN;
+        }
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          float of[32];
+          if (!empty) {
+            uint32_t a[32];
+            tmem_ld32(tbase + c0, a);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) of[i] = __uint_as_float(a[i]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) of[i] = 0.f;
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(orow + c0 + q * 8) = pack8(of + q * 8);
         }
       }
       tc_fence_before();
@@ -455,9 +622,9 @@ bool make_tmap(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int AMODE, int EPI>
+template <int BN, int AMODE, int BMODE, int SCHED, int EPI>
 cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcParams& p, int grid, cudaStream_t s) {
-  auto kern = tc_gemm_kernel<BN, AMODE, EPI>;
+  auto kern = tc_gemm_kernel<BN, AMODE, BMODE, SCHED, EPI>;
   const int smem = Smem<BN>::TOTAL;
   static bool attr = false;
   if (!attr) {
@@ -472,6 +639,21 @@ cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcParam
 constexpr int kBNup = 256;     // gate/up: 128 gate + 128 up columns
 constexpr int kBNdown = 256;
 constexpr int kBNrouter = 256;
+constexpr int kBNdh = 128;     // one 128-feature block per tile
+constexpr int kBNdx = 256;
+constexpr int kBNdw13 = 256;
+constexpr int kBNdwd = 128;
+
+TcParams base_params(const Layer& L, const Bufs& B) {
+  TcParams p = {};
+  p.row_token = B.row_token;
+  p.off = B.off;
+  p.mt_off = B.mt_off;
+  p.nseg = L.E + L.S;
+  p.A_rows = B.A;
+  p.status = L.status;
+  return p;
+}
 
 }  // namespace
 
@@ -484,6 +666,8 @@ cudaError_t tc_init(Layer& L) {
   const uint64_t nseg = L.E + L.S;
   if (!make_tmap(&L.tm_W13, L.W13, L.d, nseg * 2 * L.f, BK, kBNup)) return cudaErrorInvalidValue;
   if (!make_tmap(&L.tm_Wd, L.Wd, L.f, nseg * L.d, BK, kBNdown)) return cudaErrorInvalidValue;
+  if (!make_tmap(&L.tm_W13_mn, L.W13, L.d, nseg * 2 * L.f, 64, BK)) return cudaErrorInvalidValue;
+  if (!make_tmap(&L.tm_Wd_mn, L.Wd, L.f, nseg * L.d, 64, BK)) return cudaErrorInvalidValue;
   return cudaSuccess;
 }
 
@@ -495,22 +679,19 @@ cudaError_t launch_tc_router_logits(const Layer& L, const void* x, int T, float*
   p.dense_rows = T;
   p.K = L.d;
   p.n_tiles = 1;
-  p.b_rows_per_seg = 0;
   p.out = logits;
   p.ldo = L.E;
   p.n_valid = L.E;
   p.status = L.status;
   const int tiles = (T + BM - 1) / BM;
-  return launch<kBNrouter, A_TMA, EPI_F32>(tx, tw, p, tiles < L.num_sms ? tiles : L.num_sms, s);
+  return launch<kBNrouter, A_TMA_K, B_TMA_K, SCHED_DENSE, EPI_F32>(tx, tw, p, tiles < L.num_sms ? tiles : L.num_sms,
+                                                                   s);
 }
 
 cudaError_t launch_tc_gateup(const Layer& L, const Bufs& B, const void* x, cudaStream_t s) {
-  TcParams p = {};
+  TcParams p = base_params(L, B);
   p.A = (const bf16*)x;
-  p.row_token = B.row_token;
-  p.off = B.off;
-  p.mt_off = B.mt_off;
-  p.nseg = L.E + L.S;
+  p.lda = L.d;
   p.K = L.d;
   p.n_tiles = 2 * L.f / kBNup;
   p.b_rows_per_seg = 2 * L.f;
@@ -518,35 +699,80 @@ cudaError_t launch_tc_gateup(const Layer& L, const Bufs& B, const void* x, cudaS
   p.ldo = L.f;
   p.uv = (bf16*)B.uv;
   p.ld_uv = 2 * L.f;
-  p.status = L.status;
-  return launch<kBNup, A_GATHER, EPI_SWIGLU>(L.tm_W13 /*unused*/, L.tm_W13, p, L.num_sms, s);
+  return launch<kBNup, A_GATHER_K, B_TMA_K, SCHED_SEG_M, EPI_SWIGLU>(L.tm_W13 /*unused*/, L.tm_W13, p, L.num_sms, s);
 }
 
 cudaError_t launch_tc_down(const Layer& L, const Bufs& B, cudaStream_t s) {
   CUtensorMap th;
   if (!make_tmap(&th, B.h, L.f, B.R, BK, BM)) return cudaErrorInvalidValue;
-  TcParams p = {};
-  p.off = B.off;
-  p.mt_off = B.mt_off;
-  p.nseg = L.E + L.S;
+  TcParams p = base_params(L, B);
   p.K = L.f;
   p.n_tiles = L.d / kBNdown;
   p.b_rows_per_seg = L.d;
   p.out = B.o;
   p.ldo = L.d;
   p.row_gate = B.row_gate;
-  p.status = L.status;
-  return launch<kBNdown, A_TMA, EPI_GATE>(th, L.tm_Wd, p, L.num_sms, s);
+  return launch<kBNdown, A_TMA_K, B_TMA_K, SCHED_SEG_M, EPI_GATE>(th, L.tm_Wd, p, L.num_sms, s);
 }
 
-// The backward GEMMs run on the CUDA-core kernels for now.
+// B1: r = dy_t Wd[e] (K = d; Wd read MN-major), SwiGLU backward, g*h, gate-gradient partials.
 cudaError_t launch_tc_bwd_dh(const Layer& L, const Bufs& B, const void* dy, cudaStream_t s) {
-  return launch_simt_bwd_dh(L, B, dy, s);
+  TcParams p = base_params(L, B);
+  p.A = (const bf16*)dy;
+  p.lda = L.d;
+  p.K = L.d;
+  p.n_tiles = L.f / kBNdh;
+  p.b_rows_per_seg = L.d;
+  p.out = B.dudv;
+  p.out2 = B.hg;
+  p.ldo = L.f;
+  p.row_gate = B.row_gate;
+  p.uv = (bf16*)B.uv;
+  p.ld_uv = 2 * L.f;
+  p.dg_part = B.dg_part;
+  p.dg_slots = L.f / 64;
+  return launch<kBNdh, A_GATHER_K, B_TMA_MN, SCHED_SEG_M, EPI_DH>(L.tm_Wd_mn /*unused*/, L.tm_Wd_mn, p, L.num_sms,
+                                                                  s);
 }
-cudaError_t launch_tc_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s) { return launch_simt_bwd_dx(L, B, s); }
+
+// B2: dx_rows = [du dv] W13[e] (K = 2f; W13 read MN-major).
+cudaError_t launch_tc_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s) {
+  CUtensorMap ta;
+  if (!make_tmap(&ta, B.dudv, 2 * L.f, B.R, BK, BM)) return cudaErrorInvalidValue;
+  TcParams p = base_params(L, B);
+  p.K = 2 * L.f;
+  p.n_tiles = L.d / kBNdx;
+  p.b_rows_per_seg = 2 * L.f;
+  p.out = B.dx_rows;
+  p.ldo = L.d;
+  return launch<kBNdx, A_TMA_K, B_TMA_MN, SCHED_SEG_M, EPI_STORE>(ta, L.tm_W13_mn, p, L.num_sms, s);
+}
+
+// B3: dW13[e] = [du dv]_seg^T x_seg and dWd[e] = dy_seg^T (g h)_seg, K over the expert's sorted rows.
 cudaError_t launch_tc_bwd_dw(const Layer& L, const Bufs& B, const void* x, const void* dy, void* dWg, void* dWu,
                              void* dWd, cudaStream_t s) {
-  return launch_simt_bwd_dw(L, B, x, dy, dWg, dWu, dWd, s);
+  CUtensorMap tdudv, thg;
+  if (!make_tmap(&tdudv, B.dudv, 2 * L.f, B.R, 64, BK) || !make_tmap(&thg, B.hg, L.f, B.R, 64, BK))
+    return cudaErrorInvalidValue;
+  TcParams p = base_params(L, B);
+  p.Bsrc = (const bf16*)x;
+  p.ldb = L.d;
+  p.m_tiles = 2 * L.f / BM;
+  p.n_tiles = L.d / kBNdw13;
+  p.out = dWg;
+  p.out2 = dWu;
+  p.ldo = L.d;
+  cudaError_t e =
+      launch<kBNdw13, A_TMA_MN, B_GATHER_MN, SCHED_SEG_K, EPI_DW13>(tdudv, tdudv /*unused*/, p, L.num_sms, s);
+  if (e != cudaSuccess) return e;
+  TcParams q = base_params(L, B);
+  q.A = (const bf16*)dy;
+  q.lda = L.d;
+  q.m_tiles = L.d / BM;
+  q.n_tiles = L.f / kBNdwd;
+  q.out = dWd;
+  q.ldo = L.f;
+  return launch<kBNdwd, A_GATHER_MN, B_TMA_MN, SCHED_SEG_K, EPI_DWD>(thg /*unused*/, thg, q, L.num_sms, s);
 }
 
 }  // namespace moe
