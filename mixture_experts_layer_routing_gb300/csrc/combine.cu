@@ -123,51 +123,114 @@ __global__ void __launch_bounds__(256) router_dl_kernel(const float* __restrict_
   }
 }
 
-// dWr[e, c] = sum_t dl[t, e] x[t, c]. Renormalised routers: only the tokens of
-// segment e contribute (dl is zero elsewhere), summed in sorted-row order.
-// Plain softmax: all tokens in order. One thread per (e, column).
+// dWr[e, c] = sum_t dl[t, e] x[t, c].
+// Renormalised routers: dl is zero off the selection, so only the rows of
+// segment e contribute. Block per (e, 32*V columns): warp w takes the
+// segment's rows w, w+8, ... (in sorted order), each lane 16 bytes of
+// columns; the 8 warp partials are then added in warp order.
 template <typename T>
-__global__ void __launch_bounds__(256) router_dw_kernel(const float* __restrict__ dl, const T* __restrict__ x,
-                                                        const int* __restrict__ off, const int* __restrict__ perm,
-                                                        int Tn, int d, int E, int k, int dense,
-                                                        float* __restrict__ dWr) {
+__global__ void __launch_bounds__(256) router_dw_seg_kernel(const float* __restrict__ dl, const T* __restrict__ x,
+                                                            const int* __restrict__ off, const int* __restrict__ perm,
+                                                            int d, int E, int k, float* __restrict__ dWr) {
+  constexpr int V = 16 / sizeof(T);
+  __shared__ float part[8][32 * V];
+  const int e = blockIdx.y, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int c = blockIdx.x * 32 * V + lane * V;
+  float acc[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) acc[i] = 0.f;
+  if (c < d) {
+    const int p1 = off[e + 1];
+#pragma unroll 4
+    for (int p = off[e] + w; p < p1; p += 8) {
+      const int t = perm[p] / k;
+      const float g = dl[(long)t * E + e];
+      const uint4 u = *reinterpret_cast<const uint4*>(x + (long)t * d + c);
+      if constexpr (sizeof(T) == 2) {
+        float f[8];
+        unpack8(u, f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, f[i], acc[i]);
+      } else {
+        acc[0] = fmaf(g, __uint_as_float(u.x), acc[0]);
+        acc[1] = fmaf(g, __uint_as_float(u.y), acc[1]);
+        acc[2] = fmaf(g, __uint_as_float(u.z), acc[2]);
+        acc[3] = fmaf(g, __uint_as_float(u.w), acc[3]);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < V; ++i) part[w][lane * V + i] = acc[i];
+  __syncthreads();
+  const int col = blockIdx.x * 32 * V + threadIdx.x;
+  if (threadIdx.x < 32 * V && col < d) {
+    float s = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) s += part[q][threadIdx.x];
+    dWr[(long)e * d + col] = s;
+  }
+}
+
+// Plain softmax: dl is dense; dWr[e, c] over all tokens in order, one thread per (e, column).
+template <typename T>
+__global__ void __launch_bounds__(256) router_dw_dense_kernel(const float* __restrict__ dl, const T* __restrict__ x,
+                                                              int Tn, int d, int E, float* __restrict__ dWr) {
   const int e = blockIdx.y;
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= d) return;
   float acc = 0.f;
-  if (dense) {
-    for (int t = 0; t < Tn; ++t) acc = fmaf(dl[(long)t * E + e], to_f(x[(long)t * d + c]), acc);
-  } else {
-    for (int p = off[e]; p < off[e + 1]; ++p) {
-      const int t = perm[p] / k;
-      acc = fmaf(dl[(long)t * E + e], to_f(x[(long)t * d + c]), acc);
-    }
-  }
+  for (int t = 0; t < Tn; ++t) acc = fmaf(dl[(long)t * E + e], to_f(x[(long)t * d + c]), acc);
   dWr[(long)e * d + c] = acc;
 }
 
 // dx[t, c] = dx_rows[A + t, c] (shared) + sum_j dx_rows[inv[t*k + j], c] + sum_e dl[t, e] Wr[e, c]
 // (selected experts in slot order when renormalised, all experts otherwise).
+// One thread per 16 bytes of a token row; fp32 sum in that fixed order.
 template <typename T>
 __global__ void __launch_bounds__(256) dx_gather_kernel(const T* __restrict__ dx_rows, const int* __restrict__ inv,
                                                         const int* __restrict__ idx, const float* __restrict__ dl,
                                                         const T* __restrict__ Wr, int Tn, int d, int E, int k, int A,
                                                         int S, int dense, T* __restrict__ dx) {
+  constexpr int V = 16 / sizeof(T);
+  const int vecs = d / V;
   const long q = (long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (q >= (long)Tn * d) return;
-  const int t = (int)(q / d), c = (int)(q % d);
-  float acc = 0.f;
-  if (S) acc += to_f(dx_rows[(long)(A + t) * d + c]);
-  for (int j = 0; j < k; ++j) acc += to_f(dx_rows[(long)inv[(long)t * k + j] * d + c]);
+  if (q >= (long)Tn * vecs) return;
+  const int t = (int)(q / vecs), c = (int)(q % vecs) * V;
+  float acc[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) acc[i] = 0.f;
+  auto add = [&](const T* src, float g) {
+    const uint4 u = *reinterpret_cast<const uint4*>(src);
+    if constexpr (sizeof(T) == 2) {
+      float f[8];
+      unpack8(u, f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, f[i], acc[i]);
+    } else {
+      acc[0] = fmaf(g, __uint_as_float(u.x), acc[0]);
+      acc[1] = fmaf(g, __uint_as_float(u.y), acc[1]);
+      acc[2] = fmaf(g, __uint_as_float(u.z), acc[2]);
+      acc[3] = fmaf(g, __uint_as_float(u.w), acc[3]);
+    }
+  };
+  if (S) add(dx_rows + (long)(A + t) * d + c, 1.f);
+  for (int j = 0; j < k; ++j) add(dx_rows + (long)inv[(long)t * k + j] * d + c, 1.f);
   if (dense) {
-    for (int e = 0; e < E; ++e) acc = fmaf(dl[(long)t * E + e], to_f(Wr[(long)e * d + c]), acc);
+    for (int e = 0; e < E; ++e) add(Wr + (long)e * d + c, dl[(long)t * E + e]);
   } else {
     for (int j = 0; j < k; ++j) {
       const int e = idx[(long)t * k + j];
-      acc = fmaf(dl[(long)t * E + e], to_f(Wr[(long)e * d + c]), acc);
+      add(Wr + (long)e * d + c, dl[(long)t * E + e]);
     }
   }
-  dx[q] = from_f<T>(acc);
+  uint4 out;
+  if constexpr (sizeof(T) == 2) {
+    out = pack8(acc);
+  } else {
+    out = make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]), __float_as_uint(acc[2]),
+                     __float_as_uint(acc[3]));
+  }
+  *reinterpret_cast<uint4*>(dx + (long)t * d + c) = out;
 }
 
 // Packing: W13 rows interleave gate and up in blocks of G rows; Wd, Wr, bias are copied.
@@ -200,17 +263,27 @@ cudaError_t launch_router_bwd(const Layer& L, const Bufs& B, const void* x, floa
   const int dense = (L.router == MOE_ROUTER_SOFTMAX && !L.renorm) ? 1 : 0;
   router_dl_kernel<<<(B.T * 32 + 255) / 256, 256, 0, s>>>(B.logits, B.idx, B.gate, B.inv, B.dg_part, L.f / 64, B.T,
                                                           L.E, L.k, L.router, L.renorm, L.scale, B.dgate, B.dl);
-  dim3 grid((L.d + 255) / 256, L.E);
-  if (L.prec == MOE_FP32)
-    router_dw_kernel<float><<<grid, 256, 0, s>>>(B.dl, (const float*)x, B.off, B.perm, B.T, L.d, L.E, L.k, dense, dWr);
-  else
-    router_dw_kernel<bf16><<<grid, 256, 0, s>>>(B.dl, (const bf16*)x, B.off, B.perm, B.T, L.d, L.E, L.k, dense, dWr);
+  if (dense) {
+    dim3 grid((L.d + 255) / 256, L.E);
+    if (L.prec == MOE_FP32)
+      router_dw_dense_kernel<float><<<grid, 256, 0, s>>>(B.dl, (const float*)x, B.T, L.d, L.E, dWr);
+    else
+      router_dw_dense_kernel<bf16><<<grid, 256, 0, s>>>(B.dl, (const bf16*)x, B.T, L.d, L.E, dWr);
+  } else {
+    const int cols = 32 * 16 / (int)elem_bytes(L.prec);
+    dim3 grid((L.d + cols - 1) / cols, L.E);
+    if (L.prec == MOE_FP32)
+      router_dw_seg_kernel<float><<<grid, 256, 0, s>>>(B.dl, (const float*)x, B.off, B.perm, L.d, L.E, L.k, dWr);
+    else
+      router_dw_seg_kernel<bf16><<<grid, 256, 0, s>>>(B.dl, (const bf16*)x, B.off, B.perm, L.d, L.E, L.k, dWr);
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_dx_gather(const Layer& L, const Bufs& B, void* dx, cudaStream_t s) {
   const int dense = (L.router == MOE_ROUTER_SOFTMAX && !L.renorm) ? 1 : 0;
-  const long n = (long)B.T * L.d;
+  const int V = 16 / (int)elem_bytes(L.prec);
+  const long n = (long)B.T * (L.d / V);
   const int blocks = (int)((n + 255) / 256);
   if (L.prec == MOE_FP32)
     dx_gather_kernel<float><<<blocks, 256, 0, s>>>((const float*)B.dx_rows, B.inv, B.idx, B.dl, (const float*)L.Wr,

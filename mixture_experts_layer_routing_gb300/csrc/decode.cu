@@ -56,23 +56,40 @@ DecodeWs carve(const Layer& L, int B, void* ws) {
 }
 
 constexpr int kRouteWarps = 8;
+constexpr int kBatch = 7;   // 16-byte chunks per lane loaded before they are used
 
 __global__ void __launch_bounds__(kRouteWarps * 32) decode_route_kernel(
     const bf16* __restrict__ x, const bf16* __restrict__ Wr, const float* __restrict__ bias, int B, int d, int E,
     int k, int S, int router, int renorm, float scale, DecodeWs w, int* counter) {
+  griddep_launch();
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const int item = blockIdx.x * kRouteWarps + wib;   // (t, e)
   if (item < B * E) {
     const int t = item / E, e = item % E;
     const bf16* xr = x + (size_t)t * d;
     const bf16* wr = Wr + (size_t)e * d;
+    const int nchunk = d / 8;
     float acc = 0.f;
-    for (int c = lane * 8; c < d; c += 256) {
-      float a[8], b[8];
-      unpack8(*reinterpret_cast<const uint4*>(xr + c), a);
-      unpack8(ld_stream(wr + c), b);
+    for (int cb = lane; cb < nchunk; cb += 32 * kBatch) {
+      uint4 wv[kBatch], xv[kBatch];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc = fmaf(a[i], b[i], acc);
+      for (int q = 0; q < kBatch; ++q) {
+        const int c = cb + q * 32;
+        if (c < nchunk) {
+          wv[q] = ld_stream(wr + c * 8);
+          xv[q] = *reinterpret_cast<const uint4*>(xr + c * 8);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        if (cb + q * 32 < nchunk) {
+          float a[8], b[8];
+          unpack8(xv[q], a);
+          unpack8(wv[q], b);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc = fmaf(a[i], b[i], acc);
+        }
+      }
     }
     acc = warp_sum(acc);
     if (lane == 0) w.logits[item] = acc;
@@ -134,54 +151,72 @@ __global__ void __launch_bounds__(kRouteWarps * 32) decode_route_kernel(
     }
 }
 
-constexpr int kTokGroup = 16;
+constexpr int kTokGroup = 4;
 
-// One warp per (U entry, row i) item, grid-stride over items.
+// One warp per (U entry, row i) item, grid-stride over items. Each lane loads
+// kBatch 16-byte chunks of both weight rows before using any of them.
 __global__ void __launch_bounds__(256) decode_gateup_kernel(const bf16* __restrict__ x, const bf16* __restrict__ W13,
                                                             int d, int f, int G, int k, DecodeWs w) {
+  griddep_launch();
+  griddep_wait();
   const int lane = threadIdx.x & 31;
   const int nU = *w.nU;
-  const long items = (long)nU * f;
-  const long nwarps = (long)gridDim.x * (blockDim.x >> 5);
-  for (long it = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items; it += nwarps) {
-    const int ui = (int)(it / f), i = (int)(it % f);
+  const int items = nU * f;
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  const int nchunk = d / 8;
+  for (int it = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items; it += nwarps) {
+    const int ui = it / f, i = it - ui * f;
     const int e = w.U[ui];
     const int a0 = w.u_off[ui], a1 = w.u_off[ui + 1];
     const bf16* wg = W13 + ((size_t)e * 2 * f + (i / G) * 2 * G + (i % G)) * d;
     const bf16* wu = wg + (size_t)G * d;
     for (int g0 = a0; g0 < a1; g0 += kTokGroup) {
       const int nt = min(kTokGroup, a1 - g0);
-      int tok[kTokGroup];
+      const bf16* xr[kTokGroup];
 #pragma unroll
-      for (int q = 0; q < kTokGroup; ++q) tok[q] = q < nt ? (w.a_tok[g0 + q] >> 8) : 0;
+      for (int q = 0; q < kTokGroup; ++q) xr[q] = x + (size_t)(q < nt ? (w.a_tok[g0 + q] >> 8) : 0) * d;
       float au[kTokGroup], av[kTokGroup];
 #pragma unroll
       for (int q = 0; q < kTokGroup; ++q) au[q] = av[q] = 0.f;
-#pragma unroll 2
-      for (int c = lane * 8; c < d; c += 256) {
-        float fg[8], fu[8];
-        unpack8(ld_stream(wg + c), fg);
-        unpack8(ld_stream(wu + c), fu);
+      for (int cb = lane; cb < nchunk; cb += 32 * kBatch) {
+        uint4 gv[kBatch], uvv[kBatch];
 #pragma unroll
-        for (int q = 0; q < kTokGroup; ++q) {
-          if (q < nt) {
-            float xv[8];
-            unpack8(*reinterpret_cast<const uint4*>(x + (size_t)tok[q] * d + c), xv);
+        for (int q = 0; q < kBatch; ++q) {
+          const int c = cb + q * 32;
+          if (c < nchunk) {
+            gv[q] = ld_stream(wg + c * 8);
+            uvv[q] = ld_stream(wu + c * 8);
+          }
+        }
 #pragma unroll
-            for (int r = 0; r < 8; ++r) {
-              au[q] = fmaf(xv[r], fg[r], au[q]);
-              av[q] = fmaf(xv[r], fu[r], av[q]);
+        for (int q = 0; q < kBatch; ++q) {
+          const int c = cb + q * 32;
+          if (c < nchunk) {
+            float fg[8], fu[8];
+            unpack8(gv[q], fg);
+            unpack8(uvv[q], fu);
+#pragma unroll
+            for (int tt = 0; tt < kTokGroup; ++tt) {
+              if (tt < nt) {
+                float xv[8];
+                unpack8(*reinterpret_cast<const uint4*>(xr[tt] + c * 8), xv);
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                  au[tt] = fmaf(xv[r], fg[r], au[tt]);
+                  av[tt] = fmaf(xv[r], fu[r], av[tt]);
+                }
+              }
             }
           }
         }
       }
 #pragma unroll
-      for (int q = 0; q < kTokGroup; ++q) {
-        if (q < nt) {
-          const float u = warp_sum(au[q]);
-          const float v = warp_sum(av[q]);
+      for (int tt = 0; tt < kTokGroup; ++tt) {
+        if (tt < nt) {
+          const float u = warp_sum(au[tt]);
+          const float v = warp_sum(av[tt]);
           if (lane == 0) {
-            const int code = w.a_tok[g0 + q];
+            const int code = w.a_tok[g0 + tt];
             const int t = code >> 8, slot = code & 255;
             w.h[((size_t)t * (k + 1) + slot) * f + i] = silu_f(u) * v;
           }
@@ -193,10 +228,27 @@ __global__ void __launch_bounds__(256) decode_gateup_kernel(const bf16* __restri
 
 constexpr int kCols = 2;       // output columns per warp in the down kernel
 constexpr int kDownWarps = 8;
+constexpr int kFChunks = 8;    // 16-byte chunks of a Wd row per lane (f <= 2048 per pass)
+
+// Loads the Wd rows c0.. (kCols of them) of expert e, features [f0, f0 + 2048), into registers.
+__device__ __forceinline__ void load_wd(const bf16* Wd, int e, int d, int f, int c0, int f0, int lane,
+                                        uint4 (&wv)[kCols][kFChunks]) {
+#pragma unroll
+  for (int cc = 0; cc < kCols; ++cc) {
+    const bf16* row = Wd + ((size_t)e * d + c0 + cc) * f + f0;
+#pragma unroll
+    for (int q = 0; q < kFChunks; ++q) {
+      const int c = (lane + 32 * q) * 8;
+      if (f0 + c < f) wv[cc][q] = ld_stream(row + c);
+    }
+  }
+}
 
 __global__ void __launch_bounds__(kDownWarps * 32) decode_down_kernel(const bf16* __restrict__ Wd, int B, int d, int f,
                                                                       int k, DecodeWs w, bf16* __restrict__ y) {
   extern __shared__ float acc_s[];   // [kDownWarps][B][kCols]
+  griddep_launch();
+  griddep_wait();
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   float* acc = acc_s + (size_t)wib * B * kCols;
   const int nU = *w.nU;
@@ -204,34 +256,45 @@ __global__ void __launch_bounds__(kDownWarps * 32) decode_down_kernel(const bf16
   if (c0 >= d) return;
   for (int q = lane; q < B * kCols; q += 32) acc[q] = 0.f;
   __syncwarp();
-  for (int ui = 0; ui < nU; ++ui) {
-    const int e = w.U[ui];
-    const int a0 = w.u_off[ui], a1 = w.u_off[ui + 1];
-    const bf16* w0 = Wd + ((size_t)e * d + c0) * f;
-    for (int a = a0; a < a1; ++a) {
-      const int code = w.a_tok[a];
-      const int t = code >> 8, slot = code & 255;
-      const float g = w.a_gate[a];
-      const float* hr = w.h + ((size_t)t * (k + 1) + slot) * f;
-      float s[kCols] = {};
-      for (int c = lane * 8; c < f; c += 256) {
-        const float4 h0 = *reinterpret_cast<const float4*>(hr + c);
-        const float4 h1 = *reinterpret_cast<const float4*>(hr + c + 4);
-        const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+  for (int f0 = 0; f0 < f; f0 += 32 * kFChunks * 8) {
+    uint4 wcur[kCols][kFChunks], wnext[kCols][kFChunks];
+    load_wd(Wd, w.U[0], d, f, c0, f0, lane, wnext);
+    for (int ui = 0; ui < nU; ++ui) {
+#pragma unroll
+      for (int cc = 0; cc < kCols; ++cc)
+#pragma unroll
+        for (int q = 0; q < kFChunks; ++q) wcur[cc][q] = wnext[cc][q];
+      if (ui + 1 < nU) load_wd(Wd, w.U[ui + 1], d, f, c0, f0, lane, wnext);   // next expert in flight
+      const int a0 = w.u_off[ui], a1 = w.u_off[ui + 1];
+      for (int a = a0; a < a1; ++a) {
+        const int code = w.a_tok[a];
+        const int t = code >> 8, slot = code & 255;
+        const float g = w.a_gate[a];
+        const float* hr = w.h + ((size_t)t * (k + 1) + slot) * f + f0;
+        float s[kCols] = {};
+#pragma unroll
+        for (int q = 0; q < kFChunks; ++q) {
+          const int c = (lane + 32 * q) * 8;
+          if (f0 + c < f) {
+            const float4 h0 = *reinterpret_cast<const float4*>(hr + c);
+            const float4 h1 = *reinterpret_cast<const float4*>(hr + c + 4);
+            const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+#pragma unroll
+            for (int cc = 0; cc < kCols; ++cc) {
+              float wf[8];
+              unpack8(wcur[cc][q], wf);
+#pragma unroll
+              for (int r = 0; r < 8; ++r) s[cc] = fmaf(hv[r], wf[r], s[cc]);
+            }
+          }
+        }
 #pragma unroll
         for (int cc = 0; cc < kCols; ++cc) {
-          float wv[8];
-          unpack8(*reinterpret_cast<const uint4*>(w0 + (size_t)cc * f + c), wv);
-#pragma unroll
-          for (int r = 0; r < 8; ++r) s[cc] = fmaf(hv[r], wv[r], s[cc]);
+          const float tot = warp_sum(s[cc]);
+          if (lane == 0) acc[t * kCols + cc] = fmaf(g, tot, acc[t * kCols + cc]);
         }
+        __syncwarp();
       }
-#pragma unroll
-      for (int cc = 0; cc < kCols; ++cc) {
-        const float tot = warp_sum(s[cc]);
-        if (lane == 0) acc[t * kCols + cc] = fmaf(g, tot, acc[t * kCols + cc]);
-      }
-      __syncwarp();
     }
   }
   __syncwarp();
@@ -239,6 +302,24 @@ __global__ void __launch_bounds__(kDownWarps * 32) decode_down_kernel(const bf16
     const int t = q / kCols, cc = q % kCols;
     if (c0 + cc < d) y[(size_t)t * d + c0 + cc] = __float2bfloat16_rn(acc[q]);
   }
+}
+
+// Launch with programmatic stream serialisation: the kernel may start while
+// its predecessor finishes; it waits (griddepcontrol.wait) before reading the
+// predecessor's results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), int grid, int block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
 }  // namespace
@@ -261,16 +342,16 @@ cudaError_t launch_decode_route(const Layer& L, const void* x, int B, void* ws, 
 
 cudaError_t launch_decode_gateup(const Layer& L, const void* x, int B, void* ws, cudaStream_t s) {
   DecodeWs w = carve(L, B, ws);
-  decode_gateup_kernel<<<L.num_sms * 8, 256, 0, s>>>((const bf16*)x, (const bf16*)L.W13, L.d, L.f, L.G, L.k, w);
-  return cudaGetLastError();
+  return launch_pdl(decode_gateup_kernel, L.num_sms * 4, 256, 0, s, (const bf16*)x, (const bf16*)L.W13, L.d, L.f, L.G,
+                    L.k, w);
 }
 
 cudaError_t launch_decode_down(const Layer& L, int B, void* y, void* ws, cudaStream_t s) {
   DecodeWs w = carve(L, B, ws);
   const int down_blocks = (L.d + kDownWarps * kCols - 1) / (kDownWarps * kCols);
   const size_t smem = sizeof(float) * kDownWarps * B * kCols;
-  decode_down_kernel<<<down_blocks, kDownWarps * 32, smem, s>>>((const bf16*)L.Wd, B, L.d, L.f, L.k, w, (bf16*)y);
-  return cudaGetLastError();
+  return launch_pdl(decode_down_kernel, down_blocks, kDownWarps * 32, smem, s, (const bf16*)L.Wd, B, L.d, L.f, L.k, w,
+                    (bf16*)y);
 }
 
 }  // namespace moe
