@@ -137,8 +137,8 @@ def work_per_group(spec, cnt, training=True):
     g["combine"] = (R * d, R * d * 2 + T * d * 2)
     g["bwd_dh"] = (2 * R * f * d, wd + T * d * 2 + R * 2 * f * 2 * 2 + R * f * 2)
     g["bwd_dx"] = (2 * R * d * 2 * f, w13 + R * 2 * f * 2 + R * d * 2)
-    g["bwd_dw"] = (2 * R * 2 * f * d + 2 * R * d * f,
-                   (E + S) * 3 * f * d * 2 + R * 2 * f * 2 + T * d * 2 * 2 + R * f * 2)
+    g["bwd_dw13"] = (2 * R * 2 * f * d, (E + S) * 2 * f * d * 2 + R * 2 * f * 2 + T * d * 2)
+    g["bwd_dwd"] = (2 * R * d * f, (E + S) * f * d * 2 + R * f * 2 + T * d * 2)
     g["dx_gather"] = (R * d, R * d * 2 + T * d * 2)
     g["decode_gateup"] = (2 * R * 2 * f * d, w13 + T * d * 2)
     g["decode_down"] = (2 * R * d * f, wd + R * f * 4 + T * d * 2)
@@ -191,7 +191,9 @@ class TrainStep:
         self.inp = inp
         self.layer = MoeLayer.from_spec(spec, device=dev)
         self.layer.set_weights(inp["Wr"], inp["b"], inp["Wg"], inp["Wu"], inp["Wd"])
+        torch.cuda.synchronize()
         del inp["Wg"], inp["Wu"], inp["Wd"]
+        torch.cuda.empty_cache()
         T, d, E, S, f = spec.T, spec.d, spec.E, spec.S, spec.f
         sz = self.layer.sizes(T)
         self.ctx = self.layer.new_ctx(T)

@@ -16,11 +16,11 @@ using namespace moe;
 // Kernel groups reported by moe_profile_read.
 enum Group {
   G_ROUTER_LOGITS, G_TOPK, G_SCAN_PERMUTE, G_GATEUP, G_DOWN, G_COMBINE, G_BWD_DH, G_BWD_DX, G_ROUTER_BWD,
-  G_DX_GATHER, G_BWD_DW, G_DECODE_ROUTE, G_DECODE_GATEUP, G_DECODE_DOWN, G_PACK, G_COUNT
+  G_DX_GATHER, G_BWD_DW13, G_BWD_DWD, G_DECODE_ROUTE, G_DECODE_GATEUP, G_DECODE_DOWN, G_PACK, G_COUNT
 };
 static const char* kGroupNames[G_COUNT] = {
     "router_logits", "topk", "scan_permute", "gateup", "down", "combine", "bwd_dh", "bwd_dx", "router_bwd",
-    "dx_gather", "bwd_dw", "decode_route", "decode_gateup", "decode_down", "pack_weights"};
+    "dx_gather", "bwd_dw13", "bwd_dwd", "decode_route", "decode_gateup", "decode_down", "pack_weights"};
 
 namespace {
 
@@ -335,9 +335,11 @@ moe_status moe_backward(moe_handle h, const void* x, const void* dy, int T, cons
   CK(run(h, s, G_ROUTER_BWD, 2, [&] { return launch_router_bwd(L, B, x, dWr, s); }));
   CK(run(h, s, G_DX_GATHER, 1, [&] { return launch_dx_gather(L, B, dx, s); }));
   if (h->tc) {
-    CK(run(h, s, G_BWD_DW, 2, [&] { return launch_tc_bwd_dw(L, B, x, dy, dWg, dWu, dWd, s); }));
+    CK(run(h, s, G_BWD_DW13, 1, [&] { return launch_tc_bwd_dw13(L, B, x, dWg, dWu, s); }));
+    CK(run(h, s, G_BWD_DWD, 1, [&] { return launch_tc_bwd_dwd(L, B, dy, dWd, s); }));
   } else {
-    CK(run(h, s, G_BWD_DW, 2, [&] { return launch_simt_bwd_dw(L, B, x, dy, dWg, dWu, dWd, s); }));
+    CK(run(h, s, G_BWD_DW13, 1, [&] { return launch_simt_bwd_dw13(L, B, x, dWg, dWu, s); }));
+    CK(run(h, s, G_BWD_DWD, 1, [&] { return launch_simt_bwd_dwd(L, B, dy, dWd, s); }));
   }
   return MOE_OK;
 }

@@ -77,8 +77,8 @@ cudaError_t launch_simt_gateup(const Layer& L, const Bufs& B, const void* x, cud
 cudaError_t launch_simt_down(const Layer& L, const Bufs& B, cudaStream_t s);
 cudaError_t launch_simt_bwd_dh(const Layer& L, const Bufs& B, const void* dy, cudaStream_t s);
 cudaError_t launch_simt_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s);
-cudaError_t launch_simt_bwd_dw(const Layer& L, const Bufs& B, const void* x, const void* dy,
-                               void* dWg, void* dWu, void* dWd, cudaStream_t s);
+cudaError_t launch_simt_bwd_dw13(const Layer& L, const Bufs& B, const void* x, void* dWg, void* dWu, cudaStream_t s);
+cudaError_t launch_simt_bwd_dwd(const Layer& L, const Bufs& B, const void* dy, void* dWd, cudaStream_t s);
 // combine.cu
 cudaError_t launch_combine(const Layer& L, const Bufs& B, void* y, cudaStream_t s);
 cudaError_t launch_router_bwd(const Layer& L, const Bufs& B, const void* x, float* dWr, cudaStream_t s);
@@ -98,8 +98,8 @@ cudaError_t launch_tc_gateup(const Layer& L, const Bufs& B, const void* x, cudaS
 cudaError_t launch_tc_down(const Layer& L, const Bufs& B, cudaStream_t s);
 cudaError_t launch_tc_bwd_dh(const Layer& L, const Bufs& B, const void* dy, cudaStream_t s);
 cudaError_t launch_tc_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s);
-cudaError_t launch_tc_bwd_dw(const Layer& L, const Bufs& B, const void* x, const void* dy,
-                             void* dWg, void* dWu, void* dWd, cudaStream_t s);
+cudaError_t launch_tc_bwd_dw13(const Layer& L, const Bufs& B, const void* x, void* dWg, void* dWu, cudaStream_t s);
+cudaError_t launch_tc_bwd_dwd(const Layer& L, const Bufs& B, const void* dy, void* dWd, cudaStream_t s);
 
 inline size_t elem_bytes(int prec) { return prec == MOE_FP32 ? 4 : 2; }
 

@@ -313,16 +313,17 @@ cudaError_t launch_simt_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_simt_bwd_dw(const Layer& L, const Bufs& B, const void* x, const void* dy, void* dWg, void* dWu,
-                               void* dWd, cudaStream_t s) {
-  const int nseg = L.E + L.S;
-  dim3 g13((L.d + TN - 1) / TN, 2 * L.f / TM, nseg);
-  dim3 gd(L.f / TN, (L.d + TM - 1) / TM, nseg);
-  MOE_DISPATCH(L, {
-    bwd_dw13_kernel<T><<<g13, 256, 0, s>>>((const T*)B.dudv, (const T*)x, B.off, B.row_token, L.d, L.f, L.G,
-                                           (T*)dWg, (T*)dWu);
-    bwd_dwd_kernel<T><<<gd, 256, 0, s>>>((const T*)dy, (const T*)B.hg, B.off, B.row_token, L.d, L.f, (T*)dWd);
-  });
+cudaError_t launch_simt_bwd_dw13(const Layer& L, const Bufs& B, const void* x, void* dWg, void* dWu, cudaStream_t s) {
+  dim3 g13((L.d + TN - 1) / TN, 2 * L.f / TM, L.E + L.S);
+  MOE_DISPATCH(L, bwd_dw13_kernel<T><<<g13, 256, 0, s>>>((const T*)B.dudv, (const T*)x, B.off, B.row_token, L.d, L.f,
+                                                         L.G, (T*)dWg, (T*)dWu));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_simt_bwd_dwd(const Layer& L, const Bufs& B, const void* dy, void* dWd, cudaStream_t s) {
+  dim3 gd(L.f / TN, (L.d + TM - 1) / TM, L.E + L.S);
+  MOE_DISPATCH(L, bwd_dwd_kernel<T><<<gd, 256, 0, s>>>((const T*)dy, (const T*)B.hg, B.off, B.row_token, L.d, L.f,
+                                                       (T*)dWd));
   return cudaGetLastError();
 }
 

@@ -121,6 +121,21 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, int c0, int c1, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(tm)),
+               "r"(c0), "r"(c1), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
@@ -228,12 +243,16 @@ __device__ __forceinline__ Tile map_tile(const TcParams& p, int L) {
   return t;
 }
 
-template <int BN>
+// Epilogue staging for TMA stores: per epilogue warp two 32-row x 64-column bf16 sub-tiles (4 KB each).
+constexpr int kStageOutBytes = kEpiWarps * 2 * 32 * 128;
+
+template <int BN, int SCHED = SCHED_SEG_M>
 struct Smem {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int TOTAL = STAGES * STAGE + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int OUT = SCHED == SCHED_SEG_K ? kStageOutBytes : 0;
+  static constexpr int TOTAL = STAGES * STAGE + OUT + 1024 /*align*/ + 256 /*barriers*/;
 };
 
 template <int AMODE, int BMODE>
@@ -247,7 +266,7 @@ struct Modes {
 template <int BN, int AMODE, int BMODE, int SCHED>
 __device__ __forceinline__ void load_stage(const TcParams& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
                                            const Tile& t, int kb, uint32_t sa, uint32_t sb, uint32_t full_bar,
-                                           const bf16* const (&gsrc)[8], const uint32_t (&gbytes)[8]) {
+                                           const bf16* const (&gsrc)[8], const uint32_t (&gbytes)[8], int ktok) {
   constexpr uint32_t tma_bytes = (AMODE == A_TMA_K || AMODE == A_TMA_MN ? Smem<BN>::A_BYTES : 0) +
                                  (BMODE == B_TMA_K || BMODE == B_TMA_MN ? Smem<BN>::B_BYTES : 0);
   const int ptid = threadIdx.x;
@@ -276,27 +295,36 @@ __device__ __forceinline__ void load_stage(const TcParams& p, const CUtensorMap*
     }
   }
   if (AMODE == A_GATHER_MN || BMODE == B_GATHER_MN) {
-    // one K row (sorted row of the segment) per thread pair
-    const int kk = ptid >> 1, half = ptid & 1;
-    const int row = t.row0 + kb * BK + kk;
-    const bool v = row < t.row_end;
-    const int tok = v ? p.row_token[row] : 0;
-    const uint32_t nb = v ? 16u : 0u;
-    const uint32_t swz = (uint32_t)(kk & 7);
+    // Warp w copies the K rows 16w..16w+15 of this block, one whole row per instruction (4 full
+    // 128-byte lines), so the gather is coalesced. ktok holds, in lanes 0..15, the token of row
+    // 16w + lane (loaded two blocks ahead); it is broadcast per row.
+    const int warp = ptid >> 5, lane = ptid & 31;
     if (AMODE == A_GATHER_MN) {
-      const bf16* src = p.A + (size_t)tok * p.lda + t.m * BM + half * 64;
-      const uint32_t dst = sa + half * kChunkBytes + kk * 128;
+      // 128 M columns = 2 lines per row: two rows per instruction
 #pragma unroll
-      for (int q = 0; q < 8; ++q) cp_async16(dst + ((q ^ swz) << 4), src + q * 8, nb);
+      for (int i = 0; i < 8; ++i) {
+        const int rr = 2 * i + (lane >> 4);
+        const int kk = 16 * warp + rr;
+        const int tok = __shfl_sync(0xffffffffu, ktok, rr);
+        const bool v = t.row0 + kb * BK + kk < t.row_end;
+        const int j = (lane >> 3) & 1, q = lane & 7;
+        const bf16* src = p.A + (size_t)tok * p.lda + t.m * BM + j * 64 + q * 8;
+        cp_async16(sa + j * kChunkBytes + kk * 128 + ((q ^ (kk & 7)) << 4), src, v ? 16u : 0u);
+      }
     }
     if (BMODE == B_GATHER_MN) {
+      // BN columns = BN/64 lines per row
+      constexpr int LPR = BN / 64;                 // lines per row
+      constexpr int RPI = 4 / LPR;                 // rows per instruction
 #pragma unroll
-      for (int jj = 0; jj < BN / 128; ++jj) {
-        const int j = half * (BN / 128) + jj;
-        const bf16* src = p.Bsrc + (size_t)tok * p.ldb + t.n * BN + j * 64;
-        const uint32_t dst = sb + j * kChunkBytes + kk * 128;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) cp_async16(dst + ((q ^ swz) << 4), src + q * 8, nb);
+      for (int i = 0; i < 16 / RPI; ++i) {
+        const int rr = RPI * i + (lane >> 3) / LPR;
+        const int kk = 16 * warp + rr;
+        const int tok = __shfl_sync(0xffffffffu, ktok, rr);
+        const bool v = t.row0 + kb * BK + kk < t.row_end;
+        const int j = (lane >> 3) % LPR, q = lane & 7;
+        const bf16* src = p.Bsrc + (size_t)tok * p.ldb + t.n * BN + j * 64 + q * 8;
+        cp_async16(sb + j * kChunkBytes + kk * 128 + ((q ^ (kk & 7)) << 4), src, v ? 16u : 0u);
       }
     }
   }
@@ -305,7 +333,8 @@ __device__ __forceinline__ void load_stage(const TcParams& p, const CUtensorMap*
 // ------------------------------------------------------------------ kernel
 template <int BN, int AMODE, int BMODE, int SCHED, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcParams p) {
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2, TcParams p) {
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   using MD = Modes<AMODE, BMODE>;
   constexpr uint32_t TMEM_COLS = 2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512);
@@ -313,7 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* stage_base = smem;
-  uint64_t* bars = (uint64_t*)(smem + STAGES * Smem<BN>::STAGE);
+  uint8_t* out_stage = smem + STAGES * Smem<BN, SCHED>::STAGE;     // SEG_K epilogue staging (1024-aligned)
+  uint64_t* bars = (uint64_t*)(out_stage + Smem<BN, SCHED>::OUT);
   // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
   const uint32_t tfull0 = smem_u32(bars + 2 * STAGES), tempty0 = smem_u32(bars + 2 * STAGES + 2);
@@ -366,7 +396,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           gbytes[j] = v ? 16u : 0u;
         }
       }
+      // GATHER_MN: the token index of each gathered K row is loaded two blocks ahead so the L2
+      // round trip overlaps the pipeline.
+      constexpr bool kTokRing = AMODE == A_GATHER_MN || BMODE == B_GATHER_MN;
+      int tk0 = 0, tk1 = 0, tk2 = 0;
+      auto tok_at = [&](int kb) {
+        // lane l < 16 of warp w: token of K row 16w + l of block kb
+        const int row = t.row0 + kb * BK + 16 * warp + (lane & 15);
+        return (kb < t.nkb && row < t.row_end) ? p.row_token[row] : 0;
+      };
+      if (kTokRing) {
+        tk1 = tok_at(0);
+        tk2 = tok_at(1);
+      }
       for (int kb = 0; kb < t.nkb; ++kb, ++it) {
+        if (kTokRing) {
+          tk0 = tk1;
+          tk1 = tk2;
+          tk2 = tok_at(kb + 2);
+        }
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
         if (!mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, p.status)) {
@@ -375,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t sa = smem_u32(stage_base + s * Smem<BN>::STAGE);
         const uint32_t sb = sa + Smem<BN>::A_BYTES;
-        load_stage<BN, AMODE, BMODE, SCHED>(p, &tmA, &tmB, t, kb, sa, sb, full0 + 8 * s, gsrc, gbytes);
+        load_stage<BN, AMODE, BMODE, SCHED>(p, &tmA, &tmB, t, kb, sa, sb, full0 + 8 * s, gsrc, gbytes, tk0);
         if (MD::kCpAsync) {
           cp_async_commit();
           if (it >= LAG) {
@@ -553,38 +601,61 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        // weight gradients: tile rows are rows of dW13 (packed) or dWd
+        // Weight gradients: each warp writes its 32 rows of the tile as 32x64 sub-tiles through a
+        // double-buffered 128-byte-swizzled staging buffer, stored by TMA.
         const bool empty = t.nkb == 0;
-        bf16* orow;
+        const CUtensorMap* tmo = &tmC;
+        int orow0;
         if (EPI == EPI_DW13) {
-          // an M tile of 128 packed rows is all gate rows (m even) or all up rows (m odd)
-          bf16* base = (t.m & 1) ? (bf16*)p.out2 : (bf16*)p.out;
-          const int feat = (t.m >> 1) * BM + r;
-          orow = base + ((size_t)t.e * (p.m_tiles / 2) * BM + feat) * p.ldo + t.n * BN;
+          // an M tile of 128 packed rows is all gate rows (m even, dWg) or all up rows (m odd, dWu)
+          if (t.m & 1) tmo = &tmC2;
+          orow0 = t.e * (p.m_tiles / 2) * BM + (t.m >> 1) * BM + ew * 32;
         } else {
-          orow = (bf16*)p.out + ((size_t)t.e * p.m_tiles * BM + t.m * BM + r) * p.ldo + t.n * BN;
+          orow0 = (t.e * p.m_tiles + t.m) * BM + ew * 32;
         }
+        const uint32_t wbuf = smem_u32(out_stage) + ew * 2 * 4096;
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-          float of[32];
+        for (int c0 = 0; c0 < BN; c0 += 64) {
+          const int sub = c0 >> 6;
+          const uint32_t buf = wbuf + (sub & 1) * 4096;
+          float of[64];
           if (!empty) {
-            uint32_t a[32];
+            uint32_t a[32], b[32];
             tmem_ld32(tbase + c0, a);
+            tmem_ld32(tbase + c0 + 32, b);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) of[i] = __uint_as_float(a[i]);
+            for (int i = 0; i < 32; ++i) {
+              of[i] = __uint_as_float(a[i]);
+              of[32 + i] = __uint_as_float(b[i]);
+            }
           } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) of[i] = 0.f;
+            for (int i = 0; i < 64; ++i) of[i] = 0.f;
           }
+          // the store that last read this buffer (two sub-tiles ago) must have finished reading it
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
 #pragma unroll
-          for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(orow + c0 + q * 8) = pack8(of + q * 8);
+          for (int q = 0; q < 8; ++q) {
+            const uint4 v = pack8(of + q * 8);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf + lane * 128 + ((q ^ (lane & 7)) << 4)),
+                         "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                         : "memory");
+          }
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(tmo, t.n * BN + c0, orow0, buf);
+            bulk_commit();
+          }
         }
       }
       tc_fence_before();
       mbar_arrive(tempty0 + 8 * acc);
     }
   }
+  if (SCHED == SCHED_SEG_K && warp >= kProducerWarps && warp < kMmaWarp && lane == 0) bulk_wait<0>();
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
@@ -623,16 +694,17 @@ bool make_tmap(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, 
 }
 
 template <int BN, int AMODE, int BMODE, int SCHED, int EPI>
-cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcParams& p, int grid, cudaStream_t s) {
+cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcParams& p, int grid, cudaStream_t s,
+                   const CUtensorMap* tmC = nullptr, const CUtensorMap* tmC2 = nullptr) {
   auto kern = tc_gemm_kernel<BN, AMODE, BMODE, SCHED, EPI>;
-  const int smem = Smem<BN>::TOTAL;
+  const int smem = Smem<BN, SCHED>::TOTAL;
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  kern<<<grid, kThreads, smem, s>>>(tmA, tmB, p);
+  kern<<<grid, kThreads, smem, s>>>(tmA, tmB, tmC ? *tmC : tmA, tmC2 ? *tmC2 : tmA, p);
   return cudaGetLastError();
 }
 
@@ -748,12 +820,10 @@ cudaError_t launch_tc_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s) {
   return launch<kBNdx, A_TMA_K, B_TMA_MN, SCHED_SEG_M, EPI_STORE>(ta, L.tm_W13_mn, p, L.num_sms, s);
 }
 
-// B3: dW13[e] = [du dv]_seg^T x_seg and dWd[e] = dy_seg^T (g h)_seg, K over the expert's sorted rows.
-cudaError_t launch_tc_bwd_dw(const Layer& L, const Bufs& B, const void* x, const void* dy, void* dWg, void* dWu,
-                             void* dWd, cudaStream_t s) {
-  CUtensorMap tdudv, thg;
-  if (!make_tmap(&tdudv, B.dudv, 2 * L.f, B.R, 64, BK) || !make_tmap(&thg, B.hg, L.f, B.R, 64, BK))
-    return cudaErrorInvalidValue;
+// B3: dW13[e] = [du dv]_seg^T x_seg, K over the expert's sorted rows.
+cudaError_t launch_tc_bwd_dw13(const Layer& L, const Bufs& B, const void* x, void* dWg, void* dWu, cudaStream_t s) {
+  CUtensorMap tdudv;
+  if (!make_tmap(&tdudv, B.dudv, 2 * L.f, B.R, 64, BK)) return cudaErrorInvalidValue;
   TcParams p = base_params(L, B);
   p.Bsrc = (const bf16*)x;
   p.ldb = L.d;
@@ -762,9 +832,18 @@ cudaError_t launch_tc_bwd_dw(const Layer& L, const Bufs& B, const void* x, const
   p.out = dWg;
   p.out2 = dWu;
   p.ldo = L.d;
-  cudaError_t e =
-      launch<kBNdw13, A_TMA_MN, B_GATHER_MN, SCHED_SEG_K, EPI_DW13>(tdudv, tdudv /*unused*/, p, L.num_sms, s);
-  if (e != cudaSuccess) return e;
+  const uint64_t nseg = L.E + L.S;
+  CUtensorMap tg, tu;
+  if (!make_tmap(&tg, dWg, L.d, nseg * L.f, 64, 32) || !make_tmap(&tu, dWu, L.d, nseg * L.f, 64, 32))
+    return cudaErrorInvalidValue;
+  return launch<kBNdw13, A_TMA_MN, B_GATHER_MN, SCHED_SEG_K, EPI_DW13>(tdudv, tdudv /*unused*/, p, L.num_sms, s, &tg,
+                                                                       &tu);
+}
+
+// B3: dWd[e] = dy_seg^T (g h)_seg, K over the expert's sorted rows.
+cudaError_t launch_tc_bwd_dwd(const Layer& L, const Bufs& B, const void* dy, void* dWd, cudaStream_t s) {
+  CUtensorMap thg;
+  if (!make_tmap(&thg, B.hg, L.f, B.R, 64, BK)) return cudaErrorInvalidValue;
   TcParams q = base_params(L, B);
   q.A = (const bf16*)dy;
   q.lda = L.d;
@@ -772,7 +851,9 @@ cudaError_t launch_tc_bwd_dw(const Layer& L, const Bufs& B, const void* x, const
   q.n_tiles = L.f / kBNdwd;
   q.out = dWd;
   q.ldo = L.f;
-  return launch<kBNdwd, A_GATHER_MN, B_TMA_MN, SCHED_SEG_K, EPI_DWD>(thg /*unused*/, thg, q, L.num_sms, s);
+  CUtensorMap td;
+  if (!make_tmap(&td, dWd, L.f, (uint64_t)(L.E + L.S) * L.d, 64, 32)) return cudaErrorInvalidValue;
+  return launch<kBNdwd, A_GATHER_MN, B_TMA_MN, SCHED_SEG_K, EPI_DWD>(thg /*unused*/, thg, q, L.num_sms, s, &td);
 }
 
 }  // namespace moe
