@@ -385,8 +385,19 @@ def router_grad(logits, idx, g, dg, router: str, renorm: bool, scale: float):
     return dl
 
 
+def mx_fake_quant_tokens(a):
+    """MXFP8 values of a [n, ...] quantised along its token axis (axis 0) in blocks of 32 rows,
+    the last block zero-padded (padding rows are dropped again)."""
+    a = np.asarray(a, f64)
+    n = a.shape[0]
+    pad = (-n) % 32
+    if pad:
+        a = np.concatenate([a, np.zeros((pad,) + a.shape[1:], f64)])
+    return mx_fake_quant(a, axis=0)[:n]
+
+
 def backward(x, Wr, b, Wg, Wu, Wd, dy, k: int, router: str, renorm: bool, scale: float,
-             n_shared: int = 0, logits32=None):
+             n_shared: int = 0, logits32=None, mx: bool = False):
     """Gradients of sum(y * dy) with respect to x, Wr, Wg, Wu, Wd (b gets none).
 
     Per assignment (expert e, token t, gate g):
@@ -395,9 +406,22 @@ def backward(x, Wr, b, Wg, Wu, Wd, dy, k: int, router: str, renorm: bool, scale:
       dWd[e] += g dy_t^T h        dWg[e] += du^T x_t  dWu[e] += dv^T x_t
       dx_t += du Wg[e] + dv Wu[e]
     then the router: dl from dg, dWr = dl^T x, dx += dl Wr.
+
+    mx=True: every expert GEMM operand is an MXFP8 value quantised along that
+    GEMM's K (reading: E4M3 + E8M0 per 32 along K for activations and weights):
+      forward   u, v from x (along d) and Wg, Wu (along d); h unquantised for dg
+      r         dy (along d) times Wd (along d, i.e. its axis 0)
+      dx        du, dv (along f) times Wg, Wu (along f, axis 0)
+      dW        both operands along the expert's token axis (blocks of 32 tokens
+                in sorted order, zero-padded): dWg = du^T x, dWu = dv^T x,
+                dWd = dy^T (g h)
+    The router GEMMs stay unquantised.
     """
     x = np.asarray(x, f64)
     dy = np.asarray(dy, f64)
+    if mx:
+        xq = mx_fake_quant(x, axis=1)
+        dyq = mx_fake_quant(dy, axis=1)
     T, d = x.shape
     E = np.asarray(Wr).shape[0]
     r = route(x, Wr, b, k, router, renorm, scale, logits32)
@@ -421,17 +445,31 @@ def backward(x, Wr, b, Wg, Wu, Wd, dy, k: int, router: str, renorm: bool, scale:
             tok = rows // k
             ge = gflat[rows]
         xr = x[tok]
-        u, v, h, _ = expert_ffn(xr, Wg[e], Wu[e], Wd[e])
-        rr = dy[tok] @ np.asarray(Wd[e], f64)
+        if not mx:
+            u, v, h, _ = expert_ffn(xr, Wg[e], Wu[e], Wd[e])
+            rr = dy[tok] @ np.asarray(Wd[e], f64)
+        else:
+            u = xq[tok] @ mx_fake_quant(Wg[e], axis=1).T
+            v = xq[tok] @ mx_fake_quant(Wu[e], axis=1).T
+            h = silu(u) * v
+            rr = dyq[tok] @ mx_fake_quant(Wd[e], axis=0)
         if rows is not None:
             dg[rows] = np.sum(rr * h, axis=1)
         dh = ge[:, None] * rr
         du = dh * v * silu_grad(u)
         dv = dh * silu(u)
-        dWd[e] = (ge[:, None] * dy[tok]).T @ h
-        dWg[e] = du.T @ xr
-        dWu[e] = dv.T @ xr
-        dx[tok] += du @ np.asarray(Wg[e], f64) + dv @ np.asarray(Wu[e], f64)
+        if not mx:
+            dWd[e] = (ge[:, None] * dy[tok]).T @ h
+            dWg[e] = du.T @ xr
+            dWu[e] = dv.T @ xr
+            dx[tok] += du @ np.asarray(Wg[e], f64) + dv @ np.asarray(Wu[e], f64)
+        else:
+            xt = mx_fake_quant_tokens(xr)
+            dWd[e] = mx_fake_quant_tokens(dy[tok]).T @ mx_fake_quant_tokens(ge[:, None] * h)
+            dWg[e] = mx_fake_quant_tokens(du).T @ xt
+            dWu[e] = mx_fake_quant_tokens(dv).T @ xt
+            dx[tok] += (mx_fake_quant(du, axis=1) @ mx_fake_quant(Wg[e], axis=0) +
+                        mx_fake_quant(dv, axis=1) @ mx_fake_quant(Wu[e], axis=0))
     dl = router_grad(r["logits"], idx, g, dg.reshape(T, k), router, renorm, scale)
     dWr = dl.T @ x
     dx += dl @ np.asarray(Wr, f64)

@@ -421,3 +421,70 @@ def test_planted_mistakes_are_caught(monkeypatch):
                      logits32=np.array(cr["logits"], np.float32))
     assert r["idx"].tolist() != cr["idx"]
     monkeypatch.setattr(oracle, "select_experts", good_sel)
+
+
+# ------------------------------------------------------------ MX layer math
+
+def _mx_layer(seed=20, T=9, d=64, f=96, E=3):
+    rng = np.random.default_rng(seed)
+    return dict(x=rng.standard_normal((T, d)), Wr=rng.standard_normal((E, d)), b=np.zeros(E, np.float32),
+                Wg=rng.standard_normal((E + 1, f, d)) / 8, Wu=rng.standard_normal((E + 1, f, d)) / 8,
+                Wd=rng.standard_normal((E + 1, d, f)) / 8, dy=rng.standard_normal((T, d)))
+
+
+MXKW = dict(k=2, router="sigmoid", renorm=True, scale=2.5, n_shared=1)
+
+
+def test_mx_paths_reduce_to_exact_with_identity_quantisers(monkeypatch):
+    L = _mx_layer()
+    args = (L["x"], L["Wr"], L["b"], L["Wg"], L["Wu"], L["Wd"])
+    y = oracle.forward(*args, **MXKW)["y"]
+    g = oracle.backward(*args, L["dy"], **MXKW)
+    monkeypatch.setattr(oracle, "mx_fake_quant", lambda a, axis=-1: np.asarray(a, np.float64))
+    ym = oracle.forward(*args, mx=True, **MXKW)["y"]
+    gm = oracle.backward(*args, L["dy"], mx=True, **MXKW)
+    np.testing.assert_allclose(ym, y, rtol=1e-12, atol=1e-12)
+    for n in ("dx", "dWg", "dWu", "dWd", "dWr"):
+        np.testing.assert_allclose(gm[n], g[n], rtol=1e-11, atol=1e-12, err_msg=n)
+
+
+def test_mx_quantisation_axes(monkeypatch):
+    """Each operand is quantised along its GEMM's K (d != f, so a transposed operand shows)."""
+    L = _mx_layer(T=9, d=64, f=96)
+    calls = []
+    real = oracle.mx_fake_quant
+
+    def spy(a, axis=-1):
+        a = np.asarray(a, np.float64)
+        calls.append((a.shape, axis % a.ndim))
+        return real(a, axis)
+    monkeypatch.setattr(oracle, "mx_fake_quant", spy)
+    args = (L["x"], L["Wr"], L["b"], L["Wg"], L["Wu"], L["Wd"])
+    oracle.forward(*args, mx=True, **MXKW)
+    fwd = set(calls)
+    assert ((9, 64), 1) in fwd                      # x along d
+    assert ((96, 64), 1) in fwd                     # Wg, Wu [f, d] along d
+    assert ((64, 96), 1) in fwd                     # Wd [d, f] along f
+    assert all(s[1] == 96 and ax == 1 for s, ax in fwd if s[0] not in (9, 96, 64))   # h rows along f
+    calls.clear()
+    oracle.backward(*args, L["dy"], mx=True, **MXKW)
+    bwd = set(calls)
+    assert ((64, 96), 0) in bwd                     # Wd along d (its axis 0) for dy . Wd
+    assert ((96, 64), 0) in bwd                     # Wg, Wu along f (axis 0) for du . Wg
+    assert ((96, 64), 1) in bwd                     # and along d in the recomputed forward
+    token_calls = [(s, ax) for s, ax in bwd if ax == 0 and s[0] % 32 == 0 and s not in ((64, 96), (96, 64))]
+    assert token_calls and all(s[1] in (64, 96) for s, _ in token_calls)   # token-axis blocks, zero padded
+
+
+def test_token_axis_quantiser_brute_force():
+    rng = np.random.default_rng(3)
+    a = rng.standard_normal((45, 7)) * np.exp(rng.standard_normal((45, 7)))
+    q = oracle.mx_fake_quant_tokens(a)
+    assert q.shape == a.shape
+    for c in range(7):
+        for b0 in (0, 32):
+            blk = a[b0:b0 + 32, c]
+            full = np.zeros(32)
+            full[:len(blk)] = blk
+            want = oracle.mx_fake_quant(full[None, :], axis=1)[0][:len(blk)]
+            assert np.array_equal(q[b0:b0 + 32, c], want)
