@@ -16,15 +16,21 @@ using namespace moe;
 // Kernel groups reported by moe_profile_read.
 enum Group {
   G_ROUTER_LOGITS, G_TOPK, G_SCAN_PERMUTE, G_GATEUP, G_DOWN, G_COMBINE, G_BWD_DH, G_BWD_DX, G_ROUTER_BWD,
-  G_DX_GATHER, G_BWD_DW13, G_BWD_DWD, G_DECODE_ROUTE, G_DECODE_GATEUP, G_DECODE_DOWN, G_PACK, G_COUNT
+  G_DX_GATHER, G_BWD_DW13, G_BWD_DWD, G_DECODE_ROUTE, G_DECODE_GATEUP, G_DECODE_DOWN, G_PACK, G_MX_QUANT, G_COUNT
 };
 static const char* kGroupNames[G_COUNT] = {
     "router_logits", "topk", "scan_permute", "gateup", "down", "combine", "bwd_dh", "bwd_dx", "router_bwd",
-    "dx_gather", "bwd_dw13", "bwd_dwd", "decode_route", "decode_gateup", "decode_down", "pack_weights"};
+    "dx_gather", "bwd_dw13", "bwd_dwd", "decode_route", "decode_gateup", "decode_down", "pack_weights", "mx_quant"};
 
 namespace {
 
 inline size_t al(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Rows of the token-axis MXFP8 operands: every segment padded to 128 rows (upper bound over routings).
+size_t rp_max(const Layer& L, int T) {
+  const size_t R = (size_t)T * L.k + (size_t)L.S * T;
+  return (R + 127) / 128 * 128 + 128 * (size_t)(L.E + L.S);
+}
 
 struct Sizes {
   size_t route, uv, fwd_scratch, ctx, fwd_ws, bwd_ws, packed;
@@ -47,6 +53,14 @@ Sizes sizes_for(const Layer& L, int T) {
   z.bwd_ws = al(eb * R * 2 * L.f) + al(eb * R * L.f) + al(4 * A * (L.f / 64)) + al(eb * R * L.d) +
              al(4 * T * (size_t)L.E) + al(4 * A);
   z.packed = al(eb * nseg * 2 * L.f * L.d) + al(eb * nseg * L.d * L.f) + al(eb * L.E * L.d) + al(4 * L.E);
+  if (L.prec == MOE_MXFP8) {
+    const size_t d = L.d, f = L.f, Rp = rp_max(L, T);
+    z.fwd_scratch = 2 * al(4 * nch * L.E) + al(T * d) + al(T * d / 32) + al(R * f) + al(R * f / 32) + al(2 * R * d);
+    z.fwd_ws = z.route + z.fwd_scratch;
+    z.bwd_ws += al(T * d) + al(T * d / 32) + al(R * 2 * f) + al(R * 2 * f / 32) + al(Rp * 2 * f) +
+                al(Rp * 2 * f / 32) + 2 * (al(Rp * d) + al(Rp * d / 32)) + al(Rp * f) + al(Rp * f / 32);
+    z.packed = mx_packed_bytes(L) + al(2 * L.E * d) + al(4 * L.E);
+  }
   return z;
 }
 
@@ -81,10 +95,19 @@ Bufs carve(const Layer& L, int T, void* ws, const void* ctx, void* bws) {
   } else if (w) {
     w = carve_route(B, L, w);
   }
+  const bool mx = L.prec == MOE_MXFP8;
+  const size_t d = L.d, f = L.f, R = B.R, Tt = T;
   if (w) {
     B.chunk_hist = (int*)w; w += al(4 * (size_t)B.nch * L.E);
     B.chunk_base = (int*)w; w += al(4 * (size_t)B.nch * L.E);
-    B.h = w; w += al(eb * B.R * L.f);
+    if (mx) {
+      B.xq = (uint8_t*)w; w += al(Tt * d);
+      B.xs = (uint8_t*)w; w += al(Tt * d / 32);
+      B.hq = (uint8_t*)w; w += al(R * f);
+      B.hs = (uint8_t*)w; w += al(R * f / 32);
+    } else {
+      B.h = w; w += al(eb * B.R * L.f);
+    }
     B.o = w; w += al(eb * B.R * L.d);
   }
   if (bws) {
@@ -95,6 +118,22 @@ Bufs carve(const Layer& L, int T, void* ws, const void* ctx, void* bws) {
     B.dx_rows = b; b += al(eb * B.R * L.d);
     B.dl = (float*)b; b += al(4 * (size_t)B.T * L.E);
     B.dgate = (float*)b; b += al(4 * (size_t)B.A);
+    if (mx) {
+      const size_t Rp = rp_max(L, T);
+      B.Rp_max = (int)Rp;
+      B.dyq = (uint8_t*)b; b += al(Tt * d);
+      B.dys = (uint8_t*)b; b += al(Tt * d / 32);
+      B.dudvq = (uint8_t*)b; b += al(R * 2 * f);
+      B.dudvs = (uint8_t*)b; b += al(R * 2 * f / 32);
+      B.dudv_t = (uint8_t*)b; b += al(Rp * 2 * f);
+      B.dudv_ts = (uint8_t*)b; b += al(Rp * 2 * f / 32);
+      B.x_t = (uint8_t*)b; b += al(Rp * d);
+      B.x_ts = (uint8_t*)b; b += al(Rp * d / 32);
+      B.dy_t = (uint8_t*)b; b += al(Rp * d);
+      B.dy_ts = (uint8_t*)b; b += al(Rp * d / 32);
+      B.hg_t = (uint8_t*)b; b += al(Rp * f);
+      B.hg_ts = (uint8_t*)b; b += al(Rp * f / 32);
+    }
   }
   return B;
 }
@@ -148,7 +187,7 @@ moe_status run_route(moe_handle_s* h, const Bufs& B, const void* x, const float*
   const float* lg = B.logits;
   if (logits_override) {
     lg = logits_override;
-  } else if (h->tc) {
+  } else if (h->tc_router) {
     CK(run(h, s, G_ROUTER_LOGITS, 1, [&] { return launch_tc_router_logits(L, x, B.T, B.logits, s); }));
   } else {
     CK(run(h, s, G_ROUTER_LOGITS, 1, [&] { return launch_router_logits(L, x, B.T, B.logits, s); }));
@@ -187,7 +226,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
       (c.prec != MOE_FP32 && c.prec != MOE_BF16 && c.prec != MOE_MXFP8) || !std::isfinite(c.route_scale) ||
       c.route_scale <= 0.f || c.chunk_tokens < 0)
     return MOE_ERR_INVALID_ARG;
-  if (c.E > kMaxE || c.f % 64 != 0 || c.d % 8 != 0 || c.prec == MOE_MXFP8 ||
+  if (c.E > kMaxE || c.f % 64 != 0 || c.d % 8 != 0 || (c.prec == MOE_MXFP8 && (c.d % 128 || c.f % 128)) ||
       (long)c.T_max * c.k >= (1L << 30))
     return MOE_ERR_UNSUPPORTED;
   moe_handle_s* h = new (std::nothrow) moe_handle_s();
@@ -211,7 +250,16 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
   }
   L.status = words;
   L.decode_counter = words + 32;
+  if (c.prec == MOE_MXFP8) L.G = kGateMx;
   h->tc = (c.prec == MOE_BF16) && tc_supported(L);
+  h->mx = (c.prec == MOE_MXFP8) && mx_supported(L);
+  h->tc_router = h->tc || h->mx;
+  if (c.prec == MOE_MXFP8 && !h->mx) {
+    cudaFree(words);
+    delete h;
+    *out = nullptr;
+    return MOE_ERR_UNSUPPORTED;
+  }
   *out = h;
   return MOE_OK;
 }
@@ -244,6 +292,19 @@ moe_status moe_set_weights(moe_handle h, const void* Wr, const float* bias, cons
   if (!aligned256(packed)) return MOE_ERR_WORKSPACE;
   if (!aligned16(Wr) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd)) return MOE_ERR_INVALID_ARG;
   Layer& L = h->L;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (h->mx) {
+    // MXFP8: quantised weight copies, then the bf16 router weight and the bias
+    L.W13 = L.Wd = nullptr;
+    L.Wr = (char*)packed + mx_packed_bytes(L);
+    L.bias = (float*)((char*)L.Wr + al(2 * (size_t)L.E * L.d));
+    CK(run(h, s, G_PACK, 4, [&] { return mx_pack_weights(L, Wg, Wu, Wd, packed, s); }));
+    CK(cudaMemcpyAsync(L.Wr, Wr, 2 * (size_t)L.E * L.d, cudaMemcpyDeviceToDevice, s));
+    if (bias) CK(cudaMemcpyAsync(L.bias, bias, 4 * (size_t)L.E, cudaMemcpyDeviceToDevice, s));
+    else CK(cudaMemsetAsync(L.bias, 0, 4 * (size_t)L.E, s));
+    L.has_weights = true;
+    return MOE_OK;
+  }
   const size_t eb = elem_bytes(L.prec);
   const size_t nseg = L.E + L.S;
   char* p = (char*)packed;
@@ -251,7 +312,6 @@ moe_status moe_set_weights(moe_handle h, const void* Wr, const float* bias, cons
   L.Wd = p; p += al(eb * nseg * L.d * L.f);
   L.Wr = p; p += al(eb * L.E * L.d);
   L.bias = (float*)p;
-  cudaStream_t s = (cudaStream_t)stream;
   CK(run(h, s, G_PACK, 1, [&] { return launch_pack_weights(L, Wr, bias, Wg, Wu, Wd, s); }));
   if (h->tc) CK(tc_init(L));
   L.has_weights = true;
@@ -295,7 +355,11 @@ moe_status moe_forward(moe_handle h, const void* x, int T, void* y, void* ctx, v
   Bufs B = carve(L, T, workspace, ctx, nullptr);
   moe_status st = run_route(h, B, x, nullptr, s);
   if (st != MOE_OK) return st;
-  if (h->tc) {
+  if (h->mx) {
+    CK(run(h, s, G_MX_QUANT, 1, [&] { return launch_mx_quant_rows(x, T, L.d, B.xq, B.xs, s); }));
+    CK(run(h, s, G_GATEUP, 1, [&] { return launch_mx_gateup(L, B, s); }));
+    CK(run(h, s, G_DOWN, 1, [&] { return launch_mx_down(L, B, s); }));
+  } else if (h->tc) {
     CK(run(h, s, G_GATEUP, 1, [&] { return launch_tc_gateup(L, B, x, s); }));
     CK(run(h, s, G_DOWN, 1, [&] { return launch_tc_down(L, B, s); }));
   } else {
@@ -325,7 +389,11 @@ moe_status moe_backward(moe_handle h, const void* x, const void* dy, int T, cons
     return MOE_OK;
   }
   Bufs B = carve(L, T, nullptr, ctx, workspace);
-  if (h->tc) {
+  if (h->mx) {
+    CK(run(h, s, G_MX_QUANT, 1, [&] { return launch_mx_quant_rows(dy, T, L.d, B.dyq, B.dys, s); }));
+    CK(run(h, s, G_BWD_DH, 1, [&] { return launch_mx_bwd_dh(L, B, s); }));
+    CK(run(h, s, G_BWD_DX, 1, [&] { return launch_mx_bwd_dx(L, B, s); }));
+  } else if (h->tc) {
     CK(run(h, s, G_BWD_DH, 1, [&] { return launch_tc_bwd_dh(L, B, dy, s); }));
     CK(run(h, s, G_BWD_DX, 1, [&] { return launch_tc_bwd_dx(L, B, s); }));
   } else {
@@ -334,7 +402,17 @@ moe_status moe_backward(moe_handle h, const void* x, const void* dy, int T, cons
   }
   CK(run(h, s, G_ROUTER_BWD, 2, [&] { return launch_router_bwd(L, B, x, dWr, s); }));
   CK(run(h, s, G_DX_GATHER, 1, [&] { return launch_dx_gather(L, B, dx, s); }));
-  if (h->tc) {
+  if (h->mx) {
+    CK(run(h, s, G_MX_QUANT, 4, [&] {
+      cudaError_t e = launch_mx_quant_tokens(L, B, B.dudv, false, 2 * L.f, B.dudv_t, B.dudv_ts, s);
+      if (e == cudaSuccess) e = launch_mx_quant_tokens(L, B, x, true, L.d, B.x_t, B.x_ts, s);
+      if (e == cudaSuccess) e = launch_mx_quant_tokens(L, B, dy, true, L.d, B.dy_t, B.dy_ts, s);
+      if (e == cudaSuccess) e = launch_mx_quant_tokens(L, B, B.hg, false, L.f, B.hg_t, B.hg_ts, s);
+      return e;
+    }));
+    CK(run(h, s, G_BWD_DW13, 1, [&] { return launch_mx_bwd_dw13(L, B, dWg, dWu, s); }));
+    CK(run(h, s, G_BWD_DWD, 1, [&] { return launch_mx_bwd_dwd(L, B, dWd, s); }));
+  } else if (h->tc) {
     CK(run(h, s, G_BWD_DW13, 1, [&] { return launch_tc_bwd_dw13(L, B, x, dWg, dWu, s); }));
     CK(run(h, s, G_BWD_DWD, 1, [&] { return launch_tc_bwd_dwd(L, B, dy, dWd, s); }));
   } else {

@@ -13,7 +13,9 @@ struct moe_handle_s {
   moe_config cfg;
   moe::Layer L;
   int device;
-  bool tc;   // bf16 tensor-core path available for this shape
+  bool tc;         // bf16 tensor-core path available for this shape
+  bool mx;         // MXFP8 tensor-core path (cfg.prec == MOE_MXFP8)
+  bool tc_router;  // router logits on the tensor cores
   bool prof = false;
   long long launches = 0;
   std::vector<ProfRec> recs;

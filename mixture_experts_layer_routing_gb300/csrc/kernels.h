@@ -13,7 +13,8 @@ constexpr int kMaxE = 256;        // routed experts supported by the routing ker
 constexpr int kMaxK = 8;          // experts per token
 constexpr int kChunk = 1024;      // assignments per block of the histogram / permutation kernels
 constexpr int kBM = 128;          // rows per M-tile of the grouped GEMMs (segment padding unit)
-constexpr int kGate = 128;        // gate/up interleave block of the packed W13 (rows)
+constexpr int kGate = 128;        // gate/up interleave block of the packed bf16 W13 (rows)
+constexpr int kGateMx = 64;       // gate/up interleave block of the MXFP8 W13 (rows)
 constexpr int kMaxDecodeB = 64;
 
 // Shape of one layer and the pointers that stay fixed after moe_set_weights.
@@ -35,6 +36,12 @@ struct Layer {
   CUtensorMap tm_Wd;        // K-major rows of Wd (box 64 x 256)
   CUtensorMap tm_W13_mn;    // W13 as [K=2f rows][N=d] for dx (box 64 x 64)
   CUtensorMap tm_Wd_mn;     // Wd as [K=d rows][N=f] for the dY.Wd product (box 64 x 64)
+  // MXFP8 packed weights: E4M3 codes and E8M0 scales (one per 32 along the named axis)
+  uint8_t *W13q, *W13s;     // [E+S][2f][d] along d (gate/up interleaved in blocks of kGateMx rows); [..][d/32]
+  uint8_t *W13c, *W13cs;    // same rows quantised along the packed 2f rows; scales [(E+S)*2f/32][d]
+  uint8_t *Wdq, *Wds;       // [E+S][d][f] along f; [..][f/32]
+  uint8_t *Wdc, *Wdcs;      // same rows quantised along d; scales [(E+S)*d/32][f]
+  CUtensorMap tm_W13q, tm_Wdq, tm_W13c, tm_Wdc;
 };
 
 // Device buffers of one forward / backward, carved from the caller's workspace and context.
@@ -65,6 +72,13 @@ struct Bufs {
   void* dx_rows;         // [R, d]
   float* dl;             // [T, E]
   float* dgate;          // [T, k]
+  // MXFP8 operands (codes, scales)
+  uint8_t *xq, *xs;      // [T, d], [T, d/32]
+  uint8_t *hq, *hs;      // [R, f], [R, f/32]
+  uint8_t *dyq, *dys;    // [T, d], [T, d/32]
+  uint8_t *dudvq, *dudvs;  // [R, 2f], [R, 2f/32]
+  int Rp_max;            // rows of the token-axis operands: each segment padded to 128 (upper bound)
+  uint8_t *dudv_t, *dudv_ts, *x_t, *x_ts, *dy_t, *dy_ts, *hg_t, *hg_ts;  // [Rp, W], [Rp/32, W]
 };
 
 // ----------------------------------------------------------- launchers
@@ -101,6 +115,22 @@ cudaError_t launch_tc_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s);
 cudaError_t launch_tc_bwd_dw13(const Layer& L, const Bufs& B, const void* x, void* dWg, void* dWu, cudaStream_t s);
 cudaError_t launch_tc_bwd_dwd(const Layer& L, const Bufs& B, const void* dy, void* dWd, cudaStream_t s);
 
+// mx.cu (MXFP8 tcgen05 path)
+bool mx_supported(const Layer& L);
+size_t mx_packed_bytes(const Layer& L);
+cudaError_t mx_pack_weights(Layer& L, const void* Wg, const void* Wu, const void* Wd, void* base, cudaStream_t s);
+cudaError_t launch_mx_quant_rows(const void* src, int rows, int K, uint8_t* q, uint8_t* s, cudaStream_t st);
+cudaError_t launch_mx_quant_tokens(const Layer& L, const Bufs& B, const void* src, bool gather, int W, uint8_t* q,
+                                   uint8_t* s, cudaStream_t st);
+cudaError_t launch_mx_gateup(const Layer& L, const Bufs& B, cudaStream_t s);
+cudaError_t launch_mx_down(const Layer& L, const Bufs& B, cudaStream_t s);
+cudaError_t launch_mx_bwd_dh(const Layer& L, const Bufs& B, cudaStream_t s);
+cudaError_t launch_mx_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s);
+cudaError_t launch_mx_bwd_dw13(const Layer& L, const Bufs& B, void* dWg, void* dWu, cudaStream_t s);
+cudaError_t launch_mx_bwd_dwd(const Layer& L, const Bufs& B, void* dWd, cudaStream_t s);
+bool tc_router_supported(const Layer& L);
+
+// Storage bytes of activations, outputs and bf16 weights (MXFP8 layers take bf16 activations).
 inline size_t elem_bytes(int prec) { return prec == MOE_FP32 ? 4 : 2; }
 
 }  // namespace moe

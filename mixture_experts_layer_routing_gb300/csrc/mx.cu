@@ -1,0 +1,789 @@
+// MXFP8 path: E4M3 elements with one E8M0 scale per 32 elements along each
+// GEMM's K (OCP Microscaling v1.0), on tcgen05.mma kind::mxf8f6f4 with block
+// scales in TMEM.
+//
+// The MoK page ("Cursor открыл код ядра Mixture of Experts ...", dzen.guru,
+// section "Три решения, которые дали результат") names BF16 and MXFP8 support
+// for the fused MoE layer. Quantisation here:
+//   scale exponent X = floor(log2(amax of the block)) - 8 (E4M3's largest
+//   exponent), clamped to [-127, 127], stored as X + 127; elements are
+//   round-to-nearest-even E4M3 of v * 2^-X, saturated at +-448.
+// Operands per GEMM (all quantised along that GEMM's K):
+//   gate/up   x rows (along d)          x  W13 rows (along d)
+//   down      h rows (along f)          x  Wd rows (along f)
+//   dy.Wd     dy rows (along d)         x  Wd read MN-major, quantised along d
+//   dx        [du dv] rows (along 2f)   x  W13 read MN-major, quantised along 2f
+//   dW13      [du dv] and x, both along the expert's sorted tokens (32-token
+//   dWd       dy and g*h                 blocks, each segment zero-padded to 128)
+// Gate/up rows of the MXFP8 W13 are interleaved in blocks of 64 so that one
+// 128-column tile holds 64 gate and the matching 64 up features.
+//
+// Scale factors reach TMEM through tcgen05.st from the producer warps. For a
+// 128-row operand tile the MMA reads row r's four k-block scales (one per 32
+// elements of a 128-element stage, selected by the instruction's scale id)
+// from column r/32 of lane 32q + (r mod 32) of the lane quadrant q serving the
+// output row, so every quadrant holds all four columns.
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int MBM = 128, MBN = 128, MBK = 128, MSTAGES = 6, MLAG = 2;
+constexpr int kProd = 4, kEpi = 4;
+constexpr int kMxThreads = (kProd + kEpi + 1) * 32;
+constexpr int kMxMmaWarp = kProd + kEpi;
+constexpr int kStageBytes = MBM * MBK + MBN * MBK;                 // 32 KB
+constexpr int kScaleCol0 = 2 * MBN;                                 // TMEM columns after the two accumulators
+constexpr int kMxSmem = MSTAGES * kStageBytes + 1024 + 256;
+
+enum { MA_GATHER_K = 0, MA_TMA_K = 1, MA_TMA_MN = 2 };
+enum { MB_TMA_K = 0, MB_TMA_MN = 1 };
+enum { MS_SEG_M = 0, MS_SEG_K = 1 };
+enum { ME_SWIGLU_Q = 0, ME_GATE = 1, ME_DH_Q = 2, ME_STORE = 3, ME_DW13 = 4, ME_DWD = 5 };
+
+struct MxParams {
+  const uint8_t* Ag;      // gathered A codes [*, K] (MA_GATHER_K)
+  const uint8_t* As;      // A scales: [rows][K/32] (K-major) or [Krows/32][W] (MN-major)
+  int a_w;                // MN-major A: row width W of the code / scale arrays
+  int a_rows;             // rows of a K-major TMA A operand (guards scale reads)
+  const uint8_t* Bs;      // B scales
+  int b_w;                // MN-major B: row width W
+  int b_rows_per_seg;     // B rows (K-major) or K rows (MN-major) per segment
+  const int* row_token;
+  const int* off;
+  const int* mt_off;
+  int nseg;
+  int K;                  // SEG_M reduction length (multiple of 128)
+  int m_tiles, n_tiles;
+  void* out;
+  int ldo;
+  void* out2;
+  uint8_t* oq;            // quantised output codes (ME_SWIGLU_Q: h, ME_DH_Q: dudv)
+  uint8_t* os;            // and their scales
+  const float* row_gate;
+  bf16* uv;
+  int ld_uv;
+  float* dg_part;
+  int dg_slots;
+  int A_rows;
+  int f;
+  int* status;
+};
+
+// ------------------------------------------------------------- quantise
+__device__ __forceinline__ int mx_exponent(float amax) {
+  const int e = (int)((__float_as_uint(amax) >> 23) & 0xff);
+  if (e == 0) return -127;                       // zero or below the normal range
+  const int X = e - 127 - 8;
+  return X < -127 ? -127 : (X > 127 ? 127 : X);
+}
+// 32 values -> 32 E4M3 codes (two uint4) and the E8M0 byte.
+__device__ __forceinline__ uint8_t quant32(const float* v, uint4& lo, uint4& hi) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const int X = mx_exponent(amax);
+  const float inv = __uint_as_float((uint32_t)(127 - X) << 23);   // 2^-X, X <= 126 for finite bf16 input
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t a = __nv_cvt_float2_to_fp8x2(make_float2(v[4 * i] * inv, v[4 * i + 1] * inv), __NV_SATFINITE,
+                                                 __NV_E4M3);
+    const uint32_t b = __nv_cvt_float2_to_fp8x2(make_float2(v[4 * i + 2] * inv, v[4 * i + 3] * inv), __NV_SATFINITE,
+                                                 __NV_E4M3);
+    w[i] = a | (b << 16);
+  }
+  lo = make_uint4(w[0], w[1], w[2], w[3]);
+  hi = make_uint4(w[4], w[5], w[6], w[7]);
+  return (uint8_t)(X + 127);
+}
+
+enum { SRC_PLAIN = 0, SRC_GATHER = 1, SRC_W13 = 2 };
+
+// Source row of packed W13 row `row` (gate/up interleaved in blocks of G rows).
+__device__ __forceinline__ const bf16* w13_src(const bf16* Wg, const bf16* Wu, long row, int f, int G, int K) {
+  const long e = row / (2 * f);
+  const int pr = (int)(row % (2 * f));
+  const int blk = pr / (2 * G), w = pr % (2 * G);
+  const int feat = blk * G + (w % G);
+  return (w < G ? Wg : Wu) + (e * f + feat) * (long)K;
+}
+
+// Along K: one warp per row, one lane per 32-element block.
+template <int SRC>
+__global__ void __launch_bounds__(256) mx_quant_rows_kernel(const bf16* __restrict__ src, const bf16* __restrict__ src2,
+                                                            const int* __restrict__ map, long rows, int K, int f, int G,
+                                                            uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
+  const long row = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const bf16* sr = SRC == SRC_PLAIN ? src + row * K
+                 : SRC == SRC_GATHER ? src + (long)map[row] * K
+                                     : w13_src(src, src2, row, f, G, K);
+  for (int b = lane; b < K / 32; b += 32) {
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) unpack8(*reinterpret_cast<const uint4*>(sr + b * 32 + 8 * i), v + 8 * i);
+    uint4 lo, hi;
+    const uint8_t sc = quant32(v, lo, hi);
+    *reinterpret_cast<uint4*>(q + row * K + b * 32) = lo;
+    *reinterpret_cast<uint4*>(q + row * K + b * 32 + 16) = hi;
+    s[row * (K / 32) + b] = sc;
+  }
+}
+
+enum { CSRC_PLAIN = 0, CSRC_W13 = 1, CSRC_SEG_GATHER = 2, CSRC_SEG_DIRECT = 3 };
+
+// Along rows, in blocks of 32 rows: one thread per column, one block of 256
+// columns x 32 rows per CTA. Segment modes write each expert's sorted rows at
+// mt_off[e] * 128 (segments padded to 128 rows with zero codes).
+template <int SRC>
+__global__ void __launch_bounds__(256) mx_quant_cols_kernel(const bf16* __restrict__ src, const bf16* __restrict__ src2,
+                                                            const int* __restrict__ row_token,
+                                                            const int* __restrict__ off,
+                                                            const int* __restrict__ mt_off, int nseg, int W, int f,
+                                                            int G, uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
+  const int c = blockIdx.x * 256 + threadIdx.x;
+  const long rb = blockIdx.y;              // 32-row block of the output
+  if (c >= W) return;
+  long seg_first = 0, seg_len = 0, seg_src0 = 0;
+  if (SRC == CSRC_SEG_GATHER || SRC == CSRC_SEG_DIRECT) {
+    const int pr = (int)(rb * 32);
+    if (pr >= mt_off[nseg] * 128) return;
+    int lo = 0, hi = nseg;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (mt_off[mid] * 128 <= pr) lo = mid; else hi = mid;
+    }
+    seg_first = (long)mt_off[lo] * 128;
+    seg_len = off[lo + 1] - off[lo];
+    seg_src0 = off[lo];
+  }
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const long orow = rb * 32 + i;
+    const bf16* row = nullptr;
+    if (SRC == CSRC_PLAIN) row = src + orow * W;
+    if (SRC == CSRC_W13) row = w13_src(src, src2, orow, f, G, W);
+    if (SRC == CSRC_SEG_GATHER || SRC == CSRC_SEG_DIRECT) {
+      const long local = orow - seg_first;
+      if (local < seg_len) {
+        const long p = seg_src0 + local;
+        row = src + (SRC == CSRC_SEG_GATHER ? (long)row_token[p] : p) * W;
+      }
+    }
+    v[i] = row ? __bfloat162float(row[c]) : 0.f;
+  }
+  uint4 lo, hi;
+  const uint8_t sc = quant32(v, lo, hi);
+  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+  for (int i = 0; i < 32; ++i) q[(rb * 32 + i) * W + c] = (uint8_t)(w[i >> 2] >> (8 * (i & 3)));
+  s[rb * W + c] = sc;
+}
+
+// ---------------------------------------------------------------- GEMM
+__host__ __device__ constexpr uint32_t idesc_mx(int a_mn, int b_mn, int sf_id) {
+  return ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) | ((uint32_t)(MBN >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(MBM >> 4) << 24) | ((uint32_t)sf_id << 4) | ((uint32_t)sf_id << 29);
+}
+__device__ __forceinline__ void mma_mx(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                       uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.block32 [%0], "
+      "%1, %2, %3, [%4], [%5], p;\n}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+struct MTile {
+  int e, m, n, row0, row_end, nkb;
+};
+
+template <int SCHED>
+__device__ __forceinline__ int mx_total(const MxParams& p) {
+  return SCHED == MS_SEG_K ? p.nseg * p.m_tiles * p.n_tiles : p.mt_off[p.nseg] * p.n_tiles;
+}
+
+template <int SCHED>
+__device__ __forceinline__ MTile mx_map(const MxParams& p, int L) {
+  MTile t;
+  if (SCHED == MS_SEG_K) {
+    const int per = p.m_tiles * p.n_tiles;
+    t.e = L / per;
+    const int rem = L % per;
+    t.n = rem / p.m_tiles;
+    t.m = rem % p.m_tiles;
+    t.row0 = p.mt_off[t.e] * MBK;                  // padded token rows of the segment
+    t.row_end = t.row0 + (p.off[t.e + 1] - p.off[t.e]);
+    t.nkb = p.mt_off[t.e + 1] - p.mt_off[t.e];
+    return t;
+  }
+  int lo = 0, hi = p.nseg;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (p.mt_off[mid] * p.n_tiles <= L) lo = mid; else hi = mid;
+  }
+  const int Me = p.mt_off[lo + 1] - p.mt_off[lo];
+  const int local = L - p.mt_off[lo] * p.n_tiles;
+  t.e = lo;
+  t.n = local / Me;
+  t.m = local % Me;
+  t.row0 = p.off[lo] + t.m * MBM;
+  t.row_end = p.off[lo + 1];
+  t.nkb = p.K / MBK;
+  return t;
+}
+
+// Four E8M0 bytes (k blocks kb*4 .. kb*4+3) of MMA row `r` of an operand.
+//  K-major: scales [rows][K/32], row-contiguous, one 32-bit word.
+//  MN-major: scales [Krows/32][W], one byte per k block.
+__device__ __forceinline__ uint32_t scale_word_k(const uint8_t* s, long row, int K, int kb) {
+  return *reinterpret_cast<const uint32_t*>(s + row * (K / 32) + kb * 4);
+}
+__device__ __forceinline__ uint32_t scale_word_mn(const uint8_t* s, long krow0, int W, int col) {
+  const uint8_t* p = s + (krow0 / 32) * (long)W + col;
+  return (uint32_t)p[0] | ((uint32_t)p[W] << 8) | ((uint32_t)p[2 * (long)W] << 16) | ((uint32_t)p[3 * (long)W] << 24);
+}
+
+template <int AMODE, int BMODE, int SCHED, int EPI>
+__global__ void __launch_bounds__(kMxThreads, 1)
+    mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, MxParams p) {
+  constexpr int A_MN = AMODE == MA_TMA_MN ? 1 : 0;
+  constexpr int B_MN = BMODE == MB_TMA_MN ? 1 : 0;
+  constexpr bool kGather = AMODE == MA_GATHER_K;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = (uint64_t*)(smem + MSTAGES * kStageBytes);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + MSTAGES);
+  const uint32_t tfull0 = smem_u32(bars + 2 * MSTAGES), tempty0 = smem_u32(bars + 2 * MSTAGES + 2);
+  const uint32_t drain = smem_u32(bars + 2 * MSTAGES + 4);
+  volatile int* abort_flag = (volatile int*)(bars + 2 * MSTAGES + 5);
+  uint32_t* tmem_slot = (uint32_t*)(bars + 2 * MSTAGES + 6);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < MSTAGES; ++s) {
+      mbar_init(full0 + 8 * s, kProd * 32);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, kEpi * 32);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kMxMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_slot))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int ntiles = mx_total<SCHED>(p);
+
+  if (warp < kProd) {
+    // ------------------------------------------------------------ producers
+    const int ptid = threadIdx.x;
+    const uint32_t lanebits = (uint32_t)(warp * 32) << 16;
+    int it = 0;
+    bool ok = true;
+    for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
+      const MTile t = mx_map<SCHED>(p, L);
+      const uint8_t* gsrc[8];
+      uint32_t gbytes[8];
+      long arow[4];        // K-major A: source row (token for gathers) of MMA rows lane + 32c
+      if (kGather) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int r = warp * 32 + j * 4 + (lane >> 3);
+          const int row = t.row0 + r;
+          const bool v = row < t.row_end;
+          const int tok = v ? p.row_token[row] : 0;
+          gsrc[j] = p.Ag + (size_t)tok * p.K + (lane & 7) * 16;
+          gbytes[j] = v ? 16u : 0u;
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int row = t.row0 + lane + 32 * c;
+          arow[c] = row < t.row_end ? p.row_token[row] : -1;
+        }
+      } else if (AMODE == MA_TMA_K) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const long row = t.row0 + lane + 32 * c;
+          arow[c] = row < p.a_rows ? row : -1;
+        }
+      }
+      for (int kb = 0; kb < t.nkb; ++kb, ++it) {
+        const int s = it % MSTAGES;
+        const uint32_t ph = (it / MSTAGES) & 1;
+        if (!mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sa = smem_u32(smem + s * kStageBytes);
+        const uint32_t sb = sa + MBM * MBK;
+        const uint32_t fb = full0 + 8 * s;
+        const long krowB = (SCHED == MS_SEG_K ? (long)t.row0 : (long)t.e * p.b_rows_per_seg) + (long)kb * MBK;
+        if (ptid == 0) {
+          mbar_expect_tx(fb, (kGather ? 0 : MBM * MBK) + MBN * MBK);
+          if (AMODE == MA_TMA_K) tma_load_2d(sa, &tmA, kb * MBK, t.row0, fb);
+          if (AMODE == MA_TMA_MN) tma_load_2d(sa, &tmA, t.m * MBM, t.row0 + kb * MBK, fb);
+          if (BMODE == MB_TMA_K) tma_load_2d(sb, &tmB, kb * MBK, t.e * p.b_rows_per_seg + t.n * MBN, fb);
+          if (BMODE == MB_TMA_MN) tma_load_2d(sb, &tmB, t.n * MBN, (int)krowB, fb);
+        }
+        if (kGather) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int r = warp * 32 + j * 4 + (lane >> 3);
+            const int c = lane & 7;
+            cp_async16(sa + r * 128 + ((c ^ (r & 7)) << 4), gsrc[j] + kb * MBK, gbytes[j]);
+          }
+        }
+        // block scales of this stage into TMEM (replicated layout, see the file header)
+        uint32_t wa[4], wb[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (AMODE == MA_TMA_MN) {
+            wa[c] = scale_word_mn(p.As, (long)t.row0 + (long)kb * MBK, p.a_w, t.m * MBM + lane + 32 * c);
+          } else {
+            wa[c] = arow[c] >= 0 ? scale_word_k(p.As, arow[c], p.K, kb) : 0u;
+          }
+          if (BMODE == MB_TMA_MN) {
+            wb[c] = scale_word_mn(p.Bs, krowB, p.b_w, t.n * MBN + lane + 32 * c);
+          } else {
+            wb[c] = scale_word_k(p.Bs, (long)t.e * p.b_rows_per_seg + t.n * MBN + lane + 32 * c, p.K, kb);
+          }
+        }
+        const uint32_t scol = tmem_base + kScaleCol0 + s * 8;
+        tmem_st4(scol + lanebits, wa[0], wa[1], wa[2], wa[3]);
+        tmem_st4(scol + 4 + lanebits, wb[0], wb[1], wb[2], wb[3]);
+        tmem_st_wait();
+        tc_fence_before();
+        if (kGather) {
+          cp_async_commit();
+          if (it >= MLAG) {
+            cp_async_wait<MLAG>();
+            fence_proxy_async();
+            mbar_arrive(full0 + 8 * ((it - MLAG) % MSTAGES));
+          }
+        } else {
+          mbar_arrive(fb);
+        }
+      }
+    }
+    if (kGather) {
+      cp_async_wait<0>();
+      fence_proxy_async();
+      for (int q = (it > MLAG ? it - MLAG : 0); q < it; ++q) mbar_arrive(full0 + 8 * (q % MSTAGES));
+    }
+  } else if (warp == kMxMmaWarp) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      int it = 0, tcount = 0;
+      bool ok = true;
+      for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x, ++tcount) {
+        const MTile t = mx_map<SCHED>(p, L);
+        const int acc = tcount & 1;
+        const uint32_t aph = (tcount >> 1) & 1;
+        if (!mbar_wait(tempty0 + 8 * acc, aph ^ 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t dcol = tmem_base + acc * MBN;
+        for (int kb = 0; kb < t.nkb; ++kb, ++it) {
+          const int s = it % MSTAGES;
+          const uint32_t ph = (it / MSTAGES) & 1;
+          if (!mbar_wait(full0 + 8 * s, ph, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + s * kStageBytes);
+          const uint32_t sb = sa + MBM * MBK;
+          const uint32_t scol = tmem_base + kScaleCol0 + s * 8;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t da = A_MN ? desc_mnmajor(sa + k * 4096) : desc_kmajor(sa + k * 32);
+            const uint64_t db = B_MN ? desc_mnmajor(sb + k * 4096) : desc_kmajor(sb + k * 32);
+            mma_mx(dcol, da, db, idesc_mx(A_MN, B_MN, k), scol, scol + 4, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit(empty0 + 8 * s);
+        }
+        if (!ok) break;
+        mma_commit(tfull0 + 8 * acc);
+      }
+      mma_commit(drain);
+      const uint64_t t0 = global_ns();
+      while (!mbar_try_wait(drain, 0)) {
+        if (global_ns() - t0 > kWaitLimitNs) {
+          set_error(p.status, MOE_ERR_TIMEOUT);
+          break;
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - kProd;
+    const int r = ew * 32 + lane;
+    int tcount = 0;
+    for (int L = blockIdx.x; L < ntiles; L += gridDim.x, ++tcount) {
+      const MTile t = mx_map<SCHED>(p, L);
+      const int acc = tcount & 1;
+      const uint32_t aph = (tcount >> 1) & 1;
+      if (!mbar_wait(tfull0 + 8 * acc, aph, abort_flag, p.status)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + acc * MBN + ((uint32_t)(ew * 32) << 16);
+      const int row = t.row0 + r;
+      const bool valid = row < t.row_end;
+      if (EPI == ME_SWIGLU_Q) {
+        // 64 gate (cols 0..63) + 64 up (64..127) accumulators of features n*64..n*64+63
+#pragma unroll 1
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          uint32_t u[32], v[32];
+          tmem_ld32(tbase + c0, u);
+          tmem_ld32(tbase + 64 + c0, v);
+          tmem_ld_wait();
+          if (valid) {
+            float hf[32], uf[32], vf[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              uf[i] = __uint_as_float(u[i]);
+              vf[i] = __uint_as_float(v[i]);
+              hf[i] = silu_f(uf[i]) * vf[i];
+            }
+            const int col = t.n * 64 + c0;
+            uint4 lo, hi;
+            const uint8_t sc = quant32(hf, lo, hi);
+            *reinterpret_cast<uint4*>(p.oq + (size_t)row * p.f + col) = lo;
+            *reinterpret_cast<uint4*>(p.oq + (size_t)row * p.f + col + 16) = hi;
+            p.os[(size_t)row * (p.f / 32) + col / 32] = sc;
+            if (p.uv) {
+              bf16* uvrow = p.uv + (size_t)row * p.ld_uv + t.n * 128;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                *reinterpret_cast<uint4*>(uvrow + c0 + q * 8) = pack8(uf + q * 8);
+                *reinterpret_cast<uint4*>(uvrow + 64 + c0 + q * 8) = pack8(vf + q * 8);
+              }
+            }
+          }
+        }
+      } else if (EPI == ME_GATE || EPI == ME_STORE) {
+        const float g = (EPI == ME_GATE && valid) ? p.row_gate[row] : 1.f;
+        bf16* orow = (bf16*)p.out + (size_t)row * p.ldo + t.n * MBN;
+#pragma unroll 1
+        for (int c0 = 0; c0 < MBN; c0 += 32) {
+          uint32_t a[32];
+          tmem_ld32(tbase + c0, a);
+          tmem_ld_wait();
+          if (valid) {
+            float of[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) of[i] = g * __uint_as_float(a[i]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(orow + c0 + q * 8) = pack8(of + q * 8);
+          }
+        }
+      } else if (EPI == ME_DH_Q) {
+        // r for features n*128 .. n*128+127 = gate/up blocks 2n, 2n+1 (64 features each)
+        const float g = valid ? p.row_gate[row] : 0.f;
+        float dgp = 0.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t a[32];
+          tmem_ld32(tbase + c0, a);
+          tmem_ld_wait();
+          if (valid) {
+            const int blk = 2 * t.n + (c0 >> 6), within = c0 & 63;
+            const size_t ucol = (size_t)blk * 128 + within;          // packed column of u; v at + 64
+            const bf16* urow = p.uv + (size_t)row * p.ld_uv;
+            float uf[32], vf[32], du[32], dv[32], hg[32];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              unpack8(*reinterpret_cast<const uint4*>(urow + ucol + q * 8), uf + q * 8);
+              unpack8(*reinterpret_cast<const uint4*>(urow + ucol + 64 + q * 8), vf + q * 8);
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float rr = __uint_as_float(a[i]);
+              const float su = sigmoid_f(uf[i]);
+              const float sl = uf[i] * su;
+              const float hv = sl * vf[i];
+              dgp = fmaf(rr, hv, dgp);
+              const float dh = g * rr;
+              du[i] = dh * vf[i] * su * (1.f + uf[i] * (1.f - su));
+              dv[i] = dh * sl;
+              hg[i] = g * hv;
+            }
+            bf16* drow = (bf16*)p.out + (size_t)row * p.ld_uv;
+            bf16* hgrow = (bf16*)p.out2 + (size_t)row * p.f + t.n * 128 + c0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              *reinterpret_cast<uint4*>(drow + ucol + q * 8) = pack8(du + q * 8);
+              *reinterpret_cast<uint4*>(drow + ucol + 64 + q * 8) = pack8(dv + q * 8);
+              *reinterpret_cast<uint4*>(hgrow + q * 8) = pack8(hg + q * 8);
+            }
+            uint4 lo, hi;
+            uint8_t sc = quant32(du, lo, hi);
+            uint8_t* qrow = p.oq + (size_t)row * p.ld_uv;
+            *reinterpret_cast<uint4*>(qrow + ucol) = lo;
+            *reinterpret_cast<uint4*>(qrow + ucol + 16) = hi;
+            p.os[(size_t)row * (p.ld_uv / 32) + ucol / 32] = sc;
+            sc = quant32(dv, lo, hi);
+            *reinterpret_cast<uint4*>(qrow + ucol + 64) = lo;
+            *reinterpret_cast<uint4*>(qrow + ucol + 80) = hi;
+            p.os[(size_t)row * (p.ld_uv / 32) + (ucol + 64) / 32] = sc;
+            if ((c0 & 63) == 32) {
+              if (row < p.A_rows) p.dg_part[(size_t)row * p.dg_slots + (t.n * 128 + c0 - 32) / 64] = dgp;
+              dgp = 0.f;
+            }
+          }
+        }
+      } else {
+        // weight gradients (SEG_K): tile rows are packed dW13 rows (gate/up blocks of 64) or dWd rows
+        const bool empty = t.nkb == 0;
+        bf16* orow;
+        if (EPI == ME_DW13) {
+          const int pr = t.m * MBM + r;
+          const int blk = pr >> 7, w = pr & 127;
+          const int feat = blk * 64 + (w & 63);
+          orow = (w < 64 ? (bf16*)p.out : (bf16*)p.out2) + ((size_t)t.e * p.f + feat) * p.ldo + t.n * MBN;
+        } else {
+          orow = (bf16*)p.out + ((size_t)t.e * p.m_tiles * MBM + t.m * MBM + r) * p.ldo + t.n * MBN;
+        }
+#pragma unroll 1
+        for (int c0 = 0; c0 < MBN; c0 += 32) {
+          float of[32];
+          if (!empty) {
+            uint32_t a[32];
+            tmem_ld32(tbase + c0, a);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) of[i] = __uint_as_float(a[i]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) of[i] = 0.f;
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(orow + c0 + q * 8) = pack8(of + q * 8);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty0 + 8 * acc);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMxMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base) : "memory");
+  }
+}
+
+template <int AMODE, int BMODE, int SCHED, int EPI>
+cudaError_t mx_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const MxParams& p, int grid, cudaStream_t s) {
+  auto kern = mx_gemm_kernel<AMODE, BMODE, SCHED, EPI>;
+  static bool attr = false;
+  if (!attr) {
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  kern<<<grid, kMxThreads, kMxSmem, s>>>(tmA, tmB, p);
+  return cudaGetLastError();
+}
+
+MxParams mx_base(const Layer& L, const Bufs& B) {
+  MxParams p = {};
+  p.row_token = B.row_token;
+  p.off = B.off;
+  p.mt_off = B.mt_off;
+  p.nseg = L.E + L.S;
+  p.A_rows = B.A;
+  p.f = L.f;
+  p.status = L.status;
+  return p;
+}
+
+inline unsigned blocks_for(long n, int per) { return (unsigned)((n + per - 1) / per); }
+
+}  // namespace
+
+bool mx_supported(const Layer& L) {
+  return L.d % 128 == 0 && L.f % 128 == 0 && L.E <= kMaxE && encode_fn() != nullptr;
+}
+
+size_t mx_packed_bytes(const Layer& L) {
+  const size_t nseg = L.E + L.S, d = L.d, f = L.f;
+  auto al = [](size_t v) { return (v + 255) & ~size_t(255); };
+  const size_t w13 = nseg * 2 * f * d, wd = nseg * d * f;
+  return 2 * (al(w13) + al(w13 / 32)) + 2 * (al(wd) + al(wd / 32));
+}
+
+cudaError_t mx_pack_weights(Layer& L, const void* Wg, const void* Wu, const void* Wd, void* base, cudaStream_t s) {
+  auto al = [](size_t v) { return (v + 255) & ~size_t(255); };
+  const size_t nseg = L.E + L.S, d = L.d, f = L.f;
+  const size_t w13 = nseg * 2 * f * d, wd = nseg * d * f;
+  uint8_t* p = (uint8_t*)base;
+  L.W13q = p; p += al(w13);
+  L.W13s = p; p += al(w13 / 32);
+  L.W13c = p; p += al(w13);
+  L.W13cs = p; p += al(w13 / 32);
+  L.Wdq = p; p += al(wd);
+  L.Wds = p; p += al(wd / 32);
+  L.Wdc = p; p += al(wd);
+  L.Wdcs = p; p += al(wd / 32);
+  const bf16 *g = (const bf16*)Wg, *u = (const bf16*)Wu, *dw = (const bf16*)Wd;
+  const long r13 = (long)nseg * 2 * f, rd = (long)nseg * d;
+  mx_quant_rows_kernel<SRC_W13><<<blocks_for(r13, 8), 256, 0, s>>>(g, u, nullptr, r13, L.d, L.f, kGateMx, L.W13q,
+                                                                     L.W13s);
+  mx_quant_rows_kernel<SRC_PLAIN><<<blocks_for(rd, 8), 256, 0, s>>>(dw, nullptr, nullptr, rd, L.f, L.f, 0, L.Wdq,
+                                                                     L.Wds);
+  mx_quant_cols_kernel<CSRC_W13><<<dim3(blocks_for(d, 256), (unsigned)(r13 / 32)), 256, 0, s>>>(
+      g, u, nullptr, nullptr, nullptr, 0, L.d, L.f, kGateMx, L.W13c, L.W13cs);
+  mx_quant_cols_kernel<CSRC_PLAIN><<<dim3(blocks_for(f, 256), (unsigned)(rd / 32)), 256, 0, s>>>(
+      dw, nullptr, nullptr, nullptr, nullptr, 0, L.f, L.f, 0, L.Wdc, L.Wdcs);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (!make_tmap(&L.tm_W13q, L.W13q, d, r13, MBK, MBN, 1) || !make_tmap(&L.tm_Wdq, L.Wdq, f, rd, MBK, MBN, 1) ||
+      !make_tmap(&L.tm_W13c, L.W13c, d, r13, MBN, MBK, 1) || !make_tmap(&L.tm_Wdc, L.Wdc, f, rd, MBN, MBK, 1))
+    return cudaErrorInvalidValue;
+  return cudaSuccess;
+}
+
+cudaError_t launch_mx_quant_rows(const void* src, int rows, int K, uint8_t* q, uint8_t* s, cudaStream_t st) {
+  mx_quant_rows_kernel<SRC_PLAIN><<<blocks_for(rows, 8), 256, 0, st>>>((const bf16*)src, nullptr, nullptr, rows, K, 0,
+                                                                        0, q, s);
+  return cudaGetLastError();
+}
+
+// Token-axis operands of the weight gradients: [Rp, W] codes, [Rp/32, W] scales, Rp = mt_off[nseg] * 128.
+cudaError_t launch_mx_quant_tokens(const Layer& L, const Bufs& B, const void* src, bool gather, int W, uint8_t* q,
+                                   uint8_t* s, cudaStream_t st) {
+  const dim3 grid(blocks_for(W, 256), (unsigned)(B.Rp_max / 32));
+  if (gather)
+    mx_quant_cols_kernel<CSRC_SEG_GATHER><<<grid, 256, 0, st>>>((const bf16*)src, nullptr, B.row_token, B.off,
+                                                                B.mt_off, L.E + L.S, W, 0, 0, q, s);
+  else
+    mx_quant_cols_kernel<CSRC_SEG_DIRECT><<<grid, 256, 0, st>>>((const bf16*)src, nullptr, B.row_token, B.off,
+                                                                B.mt_off, L.E + L.S, W, 0, 0, q, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_gateup(const Layer& L, const Bufs& B, cudaStream_t s) {
+  MxParams p = mx_base(L, B);
+  p.Ag = B.xq;
+  p.As = B.xs;
+  p.Bs = L.W13s;
+  p.K = L.d;
+  p.n_tiles = 2 * L.f / MBN;
+  p.b_rows_per_seg = 2 * L.f;
+  p.oq = B.hq;
+  p.os = B.hs;
+  p.uv = (bf16*)B.uv;
+  p.ld_uv = 2 * L.f;
+  return mx_launch<MA_GATHER_K, MB_TMA_K, MS_SEG_M, ME_SWIGLU_Q>(L.tm_W13q /*unused*/, L.tm_W13q, p, L.num_sms, s);
+}
+
+cudaError_t launch_mx_down(const Layer& L, const Bufs& B, cudaStream_t s) {
+  CUtensorMap th;
+  if (!make_tmap(&th, B.hq, L.f, B.R, MBK, MBM, 1)) return cudaErrorInvalidValue;
+  MxParams p = mx_base(L, B);
+  p.As = B.hs;
+  p.a_rows = B.R;
+  p.Bs = L.Wds;
+  p.K = L.f;
+  p.n_tiles = L.d / MBN;
+  p.b_rows_per_seg = L.d;
+  p.out = B.o;
+  p.ldo = L.d;
+  p.row_gate = B.row_gate;
+  return mx_launch<MA_TMA_K, MB_TMA_K, MS_SEG_M, ME_GATE>(th, L.tm_Wdq, p, L.num_sms, s);
+}
+
+cudaError_t launch_mx_bwd_dh(const Layer& L, const Bufs& B, cudaStream_t s) {
+  MxParams p = mx_base(L, B);
+  p.Ag = B.dyq;
+  p.As = B.dys;
+  p.Bs = L.Wdcs;
+  p.b_w = L.f;
+  p.K = L.d;
+  p.n_tiles = L.f / MBN;
+  p.b_rows_per_seg = L.d;
+  p.out = B.dudv;
+  p.out2 = B.hg;
+  p.oq = B.dudvq;
+  p.os = B.dudvs;
+  p.row_gate = B.row_gate;
+  p.uv = (bf16*)B.uv;
+  p.ld_uv = 2 * L.f;
+  p.dg_part = B.dg_part;
+  p.dg_slots = L.f / 64;
+  return mx_launch<MA_GATHER_K, MB_TMA_MN, MS_SEG_M, ME_DH_Q>(L.tm_Wdc /*unused*/, L.tm_Wdc, p, L.num_sms, s);
+}
+
+cudaError_t launch_mx_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s) {
+  CUtensorMap ta;
+  if (!make_tmap(&ta, B.dudvq, 2 * L.f, B.R, MBK, MBM, 1)) return cudaErrorInvalidValue;
+  MxParams p = mx_base(L, B);
+  p.As = B.dudvs;
+  p.a_rows = B.R;
+  p.Bs = L.W13cs;
+  p.b_w = L.d;
+  p.K = 2 * L.f;
+  p.n_tiles = L.d / MBN;
+  p.b_rows_per_seg = 2 * L.f;
+  p.out = B.dx_rows;
+  p.ldo = L.d;
+  return mx_launch<MA_TMA_K, MB_TMA_MN, MS_SEG_M, ME_STORE>(ta, L.tm_W13c, p, L.num_sms, s);
+}
+
+cudaError_t launch_mx_bwd_dw13(const Layer& L, const Bufs& B, void* dWg, void* dWu, cudaStream_t s) {
+  CUtensorMap ta, tb;
+  if (!make_tmap(&ta, B.dudv_t, 2 * L.f, B.Rp_max, MBM, MBK, 1) || !make_tmap(&tb, B.x_t, L.d, B.Rp_max, MBN, MBK, 1))
+    return cudaErrorInvalidValue;
+  MxParams p = mx_base(L, B);
+  p.As = B.dudv_ts;
+  p.a_w = 2 * L.f;
+  p.Bs = B.x_ts;
+  p.b_w = L.d;
+  p.m_tiles = 2 * L.f / MBM;
+  p.n_tiles = L.d / MBN;
+  p.out = dWg;
+  p.out2 = dWu;
+  p.ldo = L.d;
+  return mx_launch<MA_TMA_MN, MB_TMA_MN, MS_SEG_K, ME_DW13>(ta, tb, p, L.num_sms, s);
+}
+
+cudaError_t launch_mx_bwd_dwd(const Layer& L, const Bufs& B, void* dWd, cudaStream_t s) {
+  CUtensorMap ta, tb;
+  if (!make_tmap(&ta, B.dy_t, L.d, B.Rp_max, MBM, MBK, 1) || !make_tmap(&tb, B.hg_t, L.f, B.Rp_max, MBN, MBK, 1))
+    return cudaErrorInvalidValue;
+  MxParams p = mx_base(L, B);
+  p.As = B.dy_ts;
+  p.a_w = L.d;
+  p.Bs = B.hg_ts;
+  p.b_w = L.f;
+  p.m_tiles = L.d / MBM;
+  p.n_tiles = L.f / MBN;
+  p.out = dWd;
+  p.ldo = L.f;
+  return mx_launch<MA_TMA_MN, MB_TMA_MN, MS_SEG_K, ME_DWD>(ta, tb, p, L.num_sms, s);
+}
+
+}  // namespace moe
