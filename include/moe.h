@@ -80,7 +80,7 @@ typedef struct {
   float route_scale;  /* multiplies the routed gates (1 for a plain softmax router) */
   int prec;           /* moe_precision of activations, weights and outputs */
   int chunk_tokens;   /* tokens per chunk of moe_train_chunked (0: whole batch) */
-  size_t ring_bytes;  /* bytes of saved activations moe_train_chunked may keep */
+  size_t ring_bytes;  /* informational: the ring size the caller intends to pass to moe_train_chunked */
 } moe_config;
 
 /* Create a handle for one layer shape on the current CUDA device. Validates
@@ -134,6 +134,28 @@ moe_status moe_forward(moe_handle h, const void* x, int T, void* y, void* ctx, v
 moe_status moe_backward(moe_handle h, const void* x, const void* dy, int T, const void* ctx,
                         void* dx, float* dWr, void* dWg, void* dWu, void* dWd, void* workspace,
                         void* stream);
+
+/* Chunked training step over a fixed ring of saved activations. The MoK page
+ * ("Три решения, которые дали результат") processes tokens in compute batches
+ * of at least 2368 tokens and keeps saved activations in a fixed ring buffer
+ * of a few hundred MB, walked in reverse in the backward pass so that fewer
+ * activations are replayed. Here: chunks of cfg.chunk_tokens tokens (the whole
+ * batch when 0); the forward of chunk c saves its routing and expert
+ * pre-activations into ring slot c mod R, R = ring_bytes / slot_bytes; the
+ * backward walks c = n-1 .. 0 and recomputes chunk c's forward only when a
+ * later chunk overwrote its slot (c < n - R), i.e. n - R recomputes.
+ * x, dy [T, d] in, y, dx [T, d] out (device, storage type of cfg.prec, bf16 for
+ * MXFP8); dWr, dWg, dWu, dWd as in moe_backward, summed over chunks in backward
+ * order (fp32 within a chunk, one bf16 rounding per chunk; dWr in fp32).
+ * ring (device, >= slot_bytes, 256-byte aligned) and workspace (device,
+ * workspace_bytes) come from moe_train_chunked_sizes. *recomputed (nullable,
+ * host) receives the number of recomputed chunk forwards. Asynchronous on
+ * `stream` like every compute call. */
+moe_status moe_train_chunked_sizes(moe_handle h, int T, size_t* slot_bytes, size_t* workspace_bytes,
+                                   int* n_chunks);
+moe_status moe_train_chunked(moe_handle h, const void* x, const void* dy, int T, void* y, void* dx, float* dWr,
+                             void* dWg, void* dWu, void* dWd, void* ring, size_t ring_bytes, void* workspace,
+                             int* recomputed, void* stream);
 
 /* Small-batch decode: y [B, d] bf16 = layer(x [B, d] bf16), 1 <= B <= 64,
  * cfg.prec == MOE_BF16. Warp-per-output kernels with fp32 intermediates. */

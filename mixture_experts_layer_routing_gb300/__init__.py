@@ -23,7 +23,8 @@ MOE_FP32, MOE_BF16, MOE_MXFP8 = 0, 1, 2
 
 EXPORTED = ("moe_create", "moe_destroy", "moe_workspace_size", "moe_set_weights", "moe_route", "moe_forward",
             "moe_backward", "moe_decode", "moe_get_status", "moe_profile_enable", "moe_profile_read",
-            "moe_launch_count", "moe_route_noalloc", "moe_status_string")
+            "moe_launch_count", "moe_route_noalloc", "moe_train_chunked_sizes", "moe_train_chunked",
+            "moe_status_string")
 
 
 class MoeError(RuntimeError):
@@ -65,6 +66,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_profile_read.argtypes = [vp, i32, ctypes.c_char_p, P(ctypes.c_longlong), P(ctypes.c_double), P(i32)]
     lib.moe_launch_count.argtypes = [vp, P(ctypes.c_longlong)]
     lib.moe_route_noalloc.argtypes = [vp, vp, i32] + [vp] * 8
+    lib.moe_train_chunked_sizes.argtypes = [vp, i32, P(sz), P(sz), P(i32)]
+    lib.moe_train_chunked.argtypes = [vp, vp, vp, i32] + [vp] * 7 + [sz, vp, P(i32), vp]
     lib.moe_status_string.argtypes = [i32]
     lib.moe_status_string.restype = ctypes.c_char_p
     for name in EXPORTED[:-1]:
@@ -144,6 +147,22 @@ def moe_forward(h, x, T, y, ctx, workspace, stream=None):
 def moe_backward(h, x, dy, T, ctx, dx, dWr, dWg, dWu, dWd, workspace, stream=None):
     _check(load_library().moe_backward(h, _ptr(x), _ptr(dy), T, _ptr(ctx), _ptr(dx), _ptr(dWr), _ptr(dWg),
                                        _ptr(dWu), _ptr(dWd), _ptr(workspace), _stream(stream)), "moe_backward")
+
+
+def moe_train_chunked_sizes(h, T) -> dict:
+    slot, ws, n = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_int()
+    _check(load_library().moe_train_chunked_sizes(h, T, ctypes.byref(slot), ctypes.byref(ws), ctypes.byref(n)),
+           "moe_train_chunked_sizes")
+    return dict(slot=slot.value, workspace=ws.value, n_chunks=n.value)
+
+
+def moe_train_chunked(h, x, dy, T, y, dx, dWr, dWg, dWu, dWd, ring, ring_bytes, workspace, stream=None) -> int:
+    """Returns the number of recomputed chunk forwards."""
+    rec = ctypes.c_int(-1)
+    _check(load_library().moe_train_chunked(h, _ptr(x), _ptr(dy), T, _ptr(y), _ptr(dx), _ptr(dWr), _ptr(dWg),
+                                            _ptr(dWu), _ptr(dWd), _ptr(ring), int(ring_bytes), _ptr(workspace),
+                                            ctypes.byref(rec), _stream(stream)), "moe_train_chunked")
+    return rec.value
 
 
 def moe_decode(h, x, B, y, workspace, stream=None):
@@ -261,6 +280,28 @@ class MoeLayer:
         ws = self.buffer("bwd", self.sizes(T)["bwd_ws"])
         moe_backward(self.h, x, dy, T, ctx, dx, dWr, dWg, dWu, dWd, ws, stream)
         return dict(dx=dx, dWr=dWr, dWg=dWg, dWu=dWu, dWd=dWd)
+
+    def grads_like(self, x):
+        T, d = x.shape
+        S, E, f = self.shape["S"], self.shape["E"], self.shape["f"]
+        wdt = torch.float32 if self.prec == "fp32" else torch.bfloat16
+        return dict(dx=torch.empty_like(x), dWr=torch.empty((E, d), dtype=torch.float32, device=self.device),
+                    dWg=torch.empty((E + S, f, d), dtype=wdt, device=self.device),
+                    dWu=torch.empty((E + S, f, d), dtype=wdt, device=self.device),
+                    dWd=torch.empty((E + S, d, f), dtype=wdt, device=self.device))
+
+    def train_chunked(self, x, dy, slots, stream=None):
+        """Chunked forward + backward with a ring of `slots` activation slots."""
+        T = x.shape[0]
+        z = moe_train_chunked_sizes(self.h, T)
+        ring = self.buffer("ring", z["slot"] * slots)
+        ws = self.buffer("chunk_ws", z["workspace"])
+        out = self.grads_like(x)
+        out["y"] = torch.empty_like(x)
+        out["recomputed"] = moe_train_chunked(self.h, x, dy, T, out["y"], out["dx"], out["dWr"], out["dWg"],
+                                              out["dWu"], out["dWd"], ring, z["slot"] * slots, ws, stream)
+        out["n_chunks"] = z["n_chunks"]
+        return out
 
     def route(self, x=None, T=None, logits_override=None, stream=None):
         T = T if T is not None else x.shape[0]

@@ -199,6 +199,82 @@ moe_status run_route(moe_handle_s* h, const Bufs& B, const void* x, const float*
   return MOE_OK;
 }
 
+// Forward of T >= 1 tokens (arguments already validated).
+moe_status forward_body(moe_handle_s* h, const void* x, int T, void* y, void* ctx, void* workspace, cudaStream_t s) {
+  const Layer& L = h->L;
+  Bufs B = carve(L, T, workspace, ctx, nullptr);
+  moe_status st = run_route(h, B, x, nullptr, s);
+  if (st != MOE_OK) return st;
+  if (h->mx) {
+    CK(run(h, s, G_MX_QUANT, 1, [&] { return launch_mx_quant_rows(x, T, L.d, B.xq, B.xs, s); }));
+    CK(run(h, s, G_GATEUP, 1, [&] { return launch_mx_gateup(L, B, s); }));
+    CK(run(h, s, G_DOWN, 1, [&] { return launch_mx_down(L, B, s); }));
+  } else if (h->tc) {
+    CK(run(h, s, G_GATEUP, 1, [&] { return launch_tc_gateup(L, B, x, s); }));
+    CK(run(h, s, G_DOWN, 1, [&] { return launch_tc_down(L, B, s); }));
+  } else {
+    CK(run(h, s, G_GATEUP, 1, [&] { return launch_simt_gateup(L, B, x, s); }));
+    CK(run(h, s, G_DOWN, 1, [&] { return launch_simt_down(L, B, s); }));
+  }
+  CK(run(h, s, G_COMBINE, 1, [&] { return launch_combine(L, B, y, s); }));
+  return MOE_OK;
+}
+
+// Backward of T >= 1 tokens with the forward's ctx (arguments already validated). acc: add the
+// weight gradients to the values already in dWr, dWg, dWu, dWd instead of overwriting them.
+moe_status backward_body(moe_handle_s* h, const void* x, const void* dy, int T, const void* ctx, void* dx, float* dWr,
+                         void* dWg, void* dWu, void* dWd, void* workspace, cudaStream_t s, bool acc) {
+  const Layer& L = h->L;
+  Bufs B = carve(L, T, nullptr, ctx, workspace);
+  if (h->mx) {
+    CK(run(h, s, G_MX_QUANT, 1, [&] { return launch_mx_quant_rows(dy, T, L.d, B.dyq, B.dys, s); }));
+    CK(run(h, s, G_BWD_DH, 1, [&] { return launch_mx_bwd_dh(L, B, s); }));
+    CK(run(h, s, G_BWD_DX, 1, [&] { return launch_mx_bwd_dx(L, B, s); }));
+  } else if (h->tc) {
+    CK(run(h, s, G_BWD_DH, 1, [&] { return launch_tc_bwd_dh(L, B, dy, s); }));
+    CK(run(h, s, G_BWD_DX, 1, [&] { return launch_tc_bwd_dx(L, B, s); }));
+  } else {
+    CK(run(h, s, G_BWD_DH, 1, [&] { return launch_simt_bwd_dh(L, B, dy, s); }));
+    CK(run(h, s, G_BWD_DX, 1, [&] { return launch_simt_bwd_dx(L, B, s); }));
+  }
+  CK(run(h, s, G_ROUTER_BWD, 2, [&] { return launch_router_bwd(L, B, x, dWr, acc, s); }));
+  CK(run(h, s, G_DX_GATHER, 1, [&] { return launch_dx_gather(L, B, dx, s); }));
+  if (h->mx) {
+    CK(run(h, s, G_MX_QUANT, 4, [&] {
+      cudaError_t e = launch_mx_quant_tokens(L, B, B.dudv, false, 2 * L.f, B.dudv_t, B.dudv_ts, s);
+      if (e == cudaSuccess) e = launch_mx_quant_tokens(L, B, x, true, L.d, B.x_t, B.x_ts, s);
+      if (e == cudaSuccess) e = launch_mx_quant_tokens(L, B, dy, true, L.d, B.dy_t, B.dy_ts, s);
+      if (e == cudaSuccess) e = launch_mx_quant_tokens(L, B, B.hg, false, L.f, B.hg_t, B.hg_ts, s);
+      return e;
+    }));
+    CK(run(h, s, G_BWD_DW13, 1, [&] { return launch_mx_bwd_dw13(L, B, dWg, dWu, acc, s); }));
+    CK(run(h, s, G_BWD_DWD, 1, [&] { return launch_mx_bwd_dwd(L, B, dWd, acc, s); }));
+  } else if (h->tc) {
+    CK(run(h, s, G_BWD_DW13, 1, [&] { return launch_tc_bwd_dw13(L, B, x, dWg, dWu, acc, s); }));
+    CK(run(h, s, G_BWD_DWD, 1, [&] { return launch_tc_bwd_dwd(L, B, dy, dWd, acc, s); }));
+  } else {
+    CK(run(h, s, G_BWD_DW13, 1, [&] { return launch_simt_bwd_dw13(L, B, x, dWg, dWu, acc, s); }));
+    CK(run(h, s, G_BWD_DWD, 1, [&] { return launch_simt_bwd_dwd(L, B, dy, dWd, acc, s); }));
+  }
+  return MOE_OK;
+}
+
+// Chunking of a training step over a ring of saved activations.
+struct ChunkPlan {
+  int chunk, n;
+  size_t slot, fwd_ws, bwd_ws;
+};
+ChunkPlan chunk_plan(const moe_handle_s* h, int T) {
+  ChunkPlan c;
+  c.chunk = (h->cfg.chunk_tokens > 0 && h->cfg.chunk_tokens < T) ? h->cfg.chunk_tokens : T;
+  c.n = c.chunk > 0 ? (T + c.chunk - 1) / c.chunk : 0;
+  const Sizes z = sizes_for(h->L, c.chunk);
+  c.slot = al(z.ctx);
+  c.fwd_ws = al(z.fwd_ws);
+  c.bwd_ws = al(z.bwd_ws);
+  return c;
+}
+
 }  // namespace
 
 extern "C" {
@@ -350,24 +426,7 @@ moe_status moe_forward(moe_handle h, const void* x, int T, void* y, void* ctx, v
   if (!aligned256(workspace) || (ctx && !aligned256(ctx))) return MOE_ERR_WORKSPACE;
   if (!aligned16(x) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
-  const Layer& L = h->L;
-  cudaStream_t s = (cudaStream_t)stream;
-  Bufs B = carve(L, T, workspace, ctx, nullptr);
-  moe_status st = run_route(h, B, x, nullptr, s);
-  if (st != MOE_OK) return st;
-  if (h->mx) {
-    CK(run(h, s, G_MX_QUANT, 1, [&] { return launch_mx_quant_rows(x, T, L.d, B.xq, B.xs, s); }));
-    CK(run(h, s, G_GATEUP, 1, [&] { return launch_mx_gateup(L, B, s); }));
-    CK(run(h, s, G_DOWN, 1, [&] { return launch_mx_down(L, B, s); }));
-  } else if (h->tc) {
-    CK(run(h, s, G_GATEUP, 1, [&] { return launch_tc_gateup(L, B, x, s); }));
-    CK(run(h, s, G_DOWN, 1, [&] { return launch_tc_down(L, B, s); }));
-  } else {
-    CK(run(h, s, G_GATEUP, 1, [&] { return launch_simt_gateup(L, B, x, s); }));
-    CK(run(h, s, G_DOWN, 1, [&] { return launch_simt_down(L, B, s); }));
-  }
-  CK(run(h, s, G_COMBINE, 1, [&] { return launch_combine(L, B, y, s); }));
-  return MOE_OK;
+  return forward_body(h, x, T, y, ctx, workspace, (cudaStream_t)stream);
 }
 
 moe_status moe_backward(moe_handle h, const void* x, const void* dy, int T, const void* ctx, void* dx, float* dWr,
@@ -388,37 +447,65 @@ moe_status moe_backward(moe_handle h, const void* x, const void* dy, int T, cons
     CK(cudaMemsetAsync(dWd, 0, eb * nseg * L.d * L.f, s));
     return MOE_OK;
   }
-  Bufs B = carve(L, T, nullptr, ctx, workspace);
-  if (h->mx) {
-    CK(run(h, s, G_MX_QUANT, 1, [&] { return launch_mx_quant_rows(dy, T, L.d, B.dyq, B.dys, s); }));
-    CK(run(h, s, G_BWD_DH, 1, [&] { return launch_mx_bwd_dh(L, B, s); }));
-    CK(run(h, s, G_BWD_DX, 1, [&] { return launch_mx_bwd_dx(L, B, s); }));
-  } else if (h->tc) {
-    CK(run(h, s, G_BWD_DH, 1, [&] { return launch_tc_bwd_dh(L, B, dy, s); }));
-    CK(run(h, s, G_BWD_DX, 1, [&] { return launch_tc_bwd_dx(L, B, s); }));
-  } else {
-    CK(run(h, s, G_BWD_DH, 1, [&] { return launch_simt_bwd_dh(L, B, dy, s); }));
-    CK(run(h, s, G_BWD_DX, 1, [&] { return launch_simt_bwd_dx(L, B, s); }));
+  return backward_body(h, x, dy, T, ctx, dx, dWr, dWg, dWu, dWd, workspace, s, false);
+}
+
+moe_status moe_train_chunked_sizes(moe_handle h, int T, size_t* slot_bytes, size_t* workspace_bytes,
+                                   int* n_chunks) {
+  if (!h || T < 1 || T > h->cfg.T_max) return MOE_ERR_INVALID_ARG;
+  const ChunkPlan c = chunk_plan(h, T);
+  if (slot_bytes) *slot_bytes = c.slot;
+  if (workspace_bytes) *workspace_bytes = c.fwd_ws + c.bwd_ws;
+  if (n_chunks) *n_chunks = c.n;
+  return MOE_OK;
+}
+
+moe_status moe_train_chunked(moe_handle h, const void* x, const void* dy, int T, void* y, void* dx, float* dWr,
+                             void* dWg, void* dWu, void* dWd, void* ring, size_t ring_bytes, void* workspace,
+                             int* recomputed, void* stream) {
+  if (!h || !x || !dy || !y || !dx || !dWr || !dWg || !dWu || !dWd || !ring || !workspace) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || T > h->cfg.T_max) return MOE_ERR_INVALID_ARG;
+  if (!h->L.has_weights) return MOE_ERR_NO_WEIGHTS;
+  if (!aligned256(workspace) || !aligned256(ring)) return MOE_ERR_WORKSPACE;
+  if (!aligned16(x) || !aligned16(dy) || !aligned16(y) || !aligned16(dx)) return MOE_ERR_INVALID_ARG;
+  const ChunkPlan c = chunk_plan(h, T);
+  const size_t R = ring_bytes / c.slot;
+  if (R < 1) return MOE_ERR_WORKSPACE;
+  const Layer& L = h->L;
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t row_bytes = elem_bytes(L.prec) * (size_t)L.d;
+  char* ws_f = (char*)workspace;
+  char* ws_b = ws_f + c.fwd_ws;
+  auto slot_of = [&](int ch) { return (char*)ring + (size_t)(ch % R) * c.slot; };
+  auto span = [&](int ch, int& t0, int& Tc) {
+    t0 = ch * c.chunk;
+    Tc = (T - t0) < c.chunk ? (T - t0) : c.chunk;
+  };
+  // forward: chunk ch saves its routing and pre-activations into slot ch mod R
+  for (int ch = 0; ch < c.n; ++ch) {
+    int t0, Tc;
+    span(ch, t0, Tc);
+    const moe_status st = forward_body(h, (const char*)x + t0 * row_bytes, Tc, (char*)y + t0 * row_bytes,
+                                       slot_of(ch), ws_f, s);
+    if (st != MOE_OK) return st;
   }
-  CK(run(h, s, G_ROUTER_BWD, 2, [&] { return launch_router_bwd(L, B, x, dWr, s); }));
-  CK(run(h, s, G_DX_GATHER, 1, [&] { return launch_dx_gather(L, B, dx, s); }));
-  if (h->mx) {
-    CK(run(h, s, G_MX_QUANT, 4, [&] {
-      cudaError_t e = launch_mx_quant_tokens(L, B, B.dudv, false, 2 * L.f, B.dudv_t, B.dudv_ts, s);
-      if (e == cudaSuccess) e = launch_mx_quant_tokens(L, B, x, true, L.d, B.x_t, B.x_ts, s);
-      if (e == cudaSuccess) e = launch_mx_quant_tokens(L, B, dy, true, L.d, B.dy_t, B.dy_ts, s);
-      if (e == cudaSuccess) e = launch_mx_quant_tokens(L, B, B.hg, false, L.f, B.hg_t, B.hg_ts, s);
-      return e;
-    }));
-    CK(run(h, s, G_BWD_DW13, 1, [&] { return launch_mx_bwd_dw13(L, B, dWg, dWu, s); }));
-    CK(run(h, s, G_BWD_DWD, 1, [&] { return launch_mx_bwd_dwd(L, B, dWd, s); }));
-  } else if (h->tc) {
-    CK(run(h, s, G_BWD_DW13, 1, [&] { return launch_tc_bwd_dw13(L, B, x, dWg, dWu, s); }));
-    CK(run(h, s, G_BWD_DWD, 1, [&] { return launch_tc_bwd_dwd(L, B, dy, dWd, s); }));
-  } else {
-    CK(run(h, s, G_BWD_DW13, 1, [&] { return launch_simt_bwd_dw13(L, B, x, dWg, dWu, s); }));
-    CK(run(h, s, G_BWD_DWD, 1, [&] { return launch_simt_bwd_dwd(L, B, dy, dWd, s); }));
+  // backward, last chunk first: a chunk whose slot a later chunk overwrote is recomputed
+  int rec = 0;
+  for (int ch = c.n - 1; ch >= 0; --ch) {
+    int t0, Tc;
+    span(ch, t0, Tc);
+    if ((size_t)ch + R < (size_t)c.n) {
+      const moe_status st = forward_body(h, (const char*)x + t0 * row_bytes, Tc, (char*)y + t0 * row_bytes,
+                                         slot_of(ch), ws_f, s);
+      if (st != MOE_OK) return st;
+      ++rec;
+    }
+    const moe_status st =
+        backward_body(h, (const char*)x + t0 * row_bytes, (const char*)dy + t0 * row_bytes, Tc, slot_of(ch),
+                      (char*)dx + t0 * row_bytes, dWr, dWg, dWu, dWd, ws_b, s, ch != c.n - 1);
+    if (st != MOE_OK) return st;
   }
+  if (recomputed) *recomputed = rec;
   return MOE_OK;
 }
 

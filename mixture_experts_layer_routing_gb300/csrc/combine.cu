@@ -131,7 +131,8 @@ __global__ void __launch_bounds__(256) router_dl_kernel(const float* __restrict_
 template <typename T>
 __global__ void __launch_bounds__(256) router_dw_seg_kernel(const float* __restrict__ dl, const T* __restrict__ x,
                                                             const int* __restrict__ off, const int* __restrict__ perm,
-                                                            int d, int E, int k, float* __restrict__ dWr) {
+                                                            int d, int E, int k, int accumulate,
+                                                            float* __restrict__ dWr) {
   constexpr int V = 16 / sizeof(T);
   __shared__ float part[8][32 * V];
   const int e = blockIdx.y, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -167,20 +168,21 @@ __global__ void __launch_bounds__(256) router_dw_seg_kernel(const float* __restr
     float s = 0.f;
 #pragma unroll
     for (int q = 0; q < 8; ++q) s += part[q][threadIdx.x];
-    dWr[(long)e * d + col] = s;
+    dWr[(long)e * d + col] = accumulate ? dWr[(long)e * d + col] + s : s;
   }
 }
 
 // Plain softmax: dl is dense; dWr[e, c] over all tokens in order, one thread per (e, column).
 template <typename T>
 __global__ void __launch_bounds__(256) router_dw_dense_kernel(const float* __restrict__ dl, const T* __restrict__ x,
-                                                              int Tn, int d, int E, float* __restrict__ dWr) {
+                                                              int Tn, int d, int E, int accumulate,
+                                                              float* __restrict__ dWr) {
   const int e = blockIdx.y;
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= d) return;
   float acc = 0.f;
   for (int t = 0; t < Tn; ++t) acc = fmaf(dl[(long)t * E + e], to_f(x[(long)t * d + c]), acc);
-  dWr[(long)e * d + c] = acc;
+  dWr[(long)e * d + c] = accumulate ? dWr[(long)e * d + c] + acc : acc;
 }
 
 // dx[t, c] = dx_rows[A + t, c] (shared) + sum_j dx_rows[inv[t*k + j], c] + sum_e dl[t, e] Wr[e, c]
@@ -259,23 +261,25 @@ cudaError_t launch_combine(const Layer& L, const Bufs& B, void* y, cudaStream_t 
   return cudaGetLastError();
 }
 
-cudaError_t launch_router_bwd(const Layer& L, const Bufs& B, const void* x, float* dWr, cudaStream_t s) {
+cudaError_t launch_router_bwd(const Layer& L, const Bufs& B, const void* x, float* dWr, bool acc, cudaStream_t s) {
   const int dense = (L.router == MOE_ROUTER_SOFTMAX && !L.renorm) ? 1 : 0;
   router_dl_kernel<<<(B.T * 32 + 255) / 256, 256, 0, s>>>(B.logits, B.idx, B.gate, B.inv, B.dg_part, L.f / 64, B.T,
                                                           L.E, L.k, L.router, L.renorm, L.scale, B.dgate, B.dl);
   if (dense) {
     dim3 grid((L.d + 255) / 256, L.E);
     if (L.prec == MOE_FP32)
-      router_dw_dense_kernel<float><<<grid, 256, 0, s>>>(B.dl, (const float*)x, B.T, L.d, L.E, dWr);
+      router_dw_dense_kernel<float><<<grid, 256, 0, s>>>(B.dl, (const float*)x, B.T, L.d, L.E, acc, dWr);
     else
-      router_dw_dense_kernel<bf16><<<grid, 256, 0, s>>>(B.dl, (const bf16*)x, B.T, L.d, L.E, dWr);
+      router_dw_dense_kernel<bf16><<<grid, 256, 0, s>>>(B.dl, (const bf16*)x, B.T, L.d, L.E, acc, dWr);
   } else {
     const int cols = 32 * 16 / (int)elem_bytes(L.prec);
     dim3 grid((L.d + cols - 1) / cols, L.E);
     if (L.prec == MOE_FP32)
-      router_dw_seg_kernel<float><<<grid, 256, 0, s>>>(B.dl, (const float*)x, B.off, B.perm, L.d, L.E, L.k, dWr);
+      router_dw_seg_kernel<float><<<grid, 256, 0, s>>>(B.dl, (const float*)x, B.off, B.perm, L.d, L.E, L.k, acc,
+                                                              dWr);
     else
-      router_dw_seg_kernel<bf16><<<grid, 256, 0, s>>>(B.dl, (const bf16*)x, B.off, B.perm, L.d, L.E, L.k, dWr);
+      router_dw_seg_kernel<bf16><<<grid, 256, 0, s>>>(B.dl, (const bf16*)x, B.off, B.perm, L.d, L.E, L.k, acc,
+                                                             dWr);
   }
   return cudaGetLastError();
 }

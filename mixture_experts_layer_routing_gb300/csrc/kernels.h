@@ -91,11 +91,12 @@ cudaError_t launch_simt_gateup(const Layer& L, const Bufs& B, const void* x, cud
 cudaError_t launch_simt_down(const Layer& L, const Bufs& B, cudaStream_t s);
 cudaError_t launch_simt_bwd_dh(const Layer& L, const Bufs& B, const void* dy, cudaStream_t s);
 cudaError_t launch_simt_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s);
-cudaError_t launch_simt_bwd_dw13(const Layer& L, const Bufs& B, const void* x, void* dWg, void* dWu, cudaStream_t s);
-cudaError_t launch_simt_bwd_dwd(const Layer& L, const Bufs& B, const void* dy, void* dWd, cudaStream_t s);
+cudaError_t launch_simt_bwd_dw13(const Layer& L, const Bufs& B, const void* x, void* dWg, void* dWu, bool acc,
+                                cudaStream_t s);
+cudaError_t launch_simt_bwd_dwd(const Layer& L, const Bufs& B, const void* dy, void* dWd, bool acc, cudaStream_t s);
 // combine.cu
 cudaError_t launch_combine(const Layer& L, const Bufs& B, void* y, cudaStream_t s);
-cudaError_t launch_router_bwd(const Layer& L, const Bufs& B, const void* x, float* dWr, cudaStream_t s);
+cudaError_t launch_router_bwd(const Layer& L, const Bufs& B, const void* x, float* dWr, bool acc, cudaStream_t s);
 cudaError_t launch_dx_gather(const Layer& L, const Bufs& B, void* dx, cudaStream_t s);
 cudaError_t launch_pack_weights(const Layer& L, const void* Wr, const float* bias, const void* Wg,
                                 const void* Wu, const void* Wd, cudaStream_t s);
@@ -112,8 +113,9 @@ cudaError_t launch_tc_gateup(const Layer& L, const Bufs& B, const void* x, cudaS
 cudaError_t launch_tc_down(const Layer& L, const Bufs& B, cudaStream_t s);
 cudaError_t launch_tc_bwd_dh(const Layer& L, const Bufs& B, const void* dy, cudaStream_t s);
 cudaError_t launch_tc_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s);
-cudaError_t launch_tc_bwd_dw13(const Layer& L, const Bufs& B, const void* x, void* dWg, void* dWu, cudaStream_t s);
-cudaError_t launch_tc_bwd_dwd(const Layer& L, const Bufs& B, const void* dy, void* dWd, cudaStream_t s);
+cudaError_t launch_tc_bwd_dw13(const Layer& L, const Bufs& B, const void* x, void* dWg, void* dWu, bool acc,
+                              cudaStream_t s);
+cudaError_t launch_tc_bwd_dwd(const Layer& L, const Bufs& B, const void* dy, void* dWd, bool acc, cudaStream_t s);
 
 // mx.cu (MXFP8 tcgen05 path)
 bool mx_supported(const Layer& L);
@@ -126,8 +128,8 @@ cudaError_t launch_mx_gateup(const Layer& L, const Bufs& B, cudaStream_t s);
 cudaError_t launch_mx_down(const Layer& L, const Bufs& B, cudaStream_t s);
 cudaError_t launch_mx_bwd_dh(const Layer& L, const Bufs& B, cudaStream_t s);
 cudaError_t launch_mx_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s);
-cudaError_t launch_mx_bwd_dw13(const Layer& L, const Bufs& B, void* dWg, void* dWu, cudaStream_t s);
-cudaError_t launch_mx_bwd_dwd(const Layer& L, const Bufs& B, void* dWd, cudaStream_t s);
+cudaError_t launch_mx_bwd_dw13(const Layer& L, const Bufs& B, void* dWg, void* dWu, bool acc, cudaStream_t s);
+cudaError_t launch_mx_bwd_dwd(const Layer& L, const Bufs& B, void* dWd, bool acc, cudaStream_t s);
 bool tc_router_supported(const Layer& L);
 
 // Storage bytes of activations, outputs and bf16 weights (MXFP8 layers take bf16 activations).

@@ -72,6 +72,7 @@ struct MxParams {
   int dg_slots;
   int A_rows;
   int f;
+  int accumulate;         // ME_DW13 / ME_DWD: add to the values already in the output
   int* status;
 };
 
@@ -579,6 +580,15 @@ __global__ void __launch_bounds__(kMxThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) of[i] = 0.f;
           }
+          if (p.accumulate) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              float o8[8];
+              unpack8(*reinterpret_cast<const uint4*>(orow + c0 + q * 8), o8);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) of[q * 8 + i] += o8[i];
+            }
+          }
 #pragma unroll
           for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(orow + c0 + q * 8) = pack8(of + q * 8);
         }
@@ -753,7 +763,7 @@ cudaError_t launch_mx_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s) {
   return mx_launch<MA_TMA_K, MB_TMA_MN, MS_SEG_M, ME_STORE>(ta, L.tm_W13c, p, L.num_sms, s);
 }
 
-cudaError_t launch_mx_bwd_dw13(const Layer& L, const Bufs& B, void* dWg, void* dWu, cudaStream_t s) {
+cudaError_t launch_mx_bwd_dw13(const Layer& L, const Bufs& B, void* dWg, void* dWu, bool acc, cudaStream_t s) {
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, B.dudv_t, 2 * L.f, B.Rp_max, MBM, MBK, 1) || !make_tmap(&tb, B.x_t, L.d, B.Rp_max, MBN, MBK, 1))
     return cudaErrorInvalidValue;
@@ -767,10 +777,11 @@ cudaError_t launch_mx_bwd_dw13(const Layer& L, const Bufs& B, void* dWg, void* d
   p.out = dWg;
   p.out2 = dWu;
   p.ldo = L.d;
+  p.accumulate = acc ? 1 : 0;
   return mx_launch<MA_TMA_MN, MB_TMA_MN, MS_SEG_K, ME_DW13>(ta, tb, p, L.num_sms, s);
 }
 
-cudaError_t launch_mx_bwd_dwd(const Layer& L, const Bufs& B, void* dWd, cudaStream_t s) {
+cudaError_t launch_mx_bwd_dwd(const Layer& L, const Bufs& B, void* dWd, bool acc, cudaStream_t s) {
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, B.dy_t, L.d, B.Rp_max, MBM, MBK, 1) || !make_tmap(&tb, B.hg_t, L.f, B.Rp_max, MBN, MBK, 1))
     return cudaErrorInvalidValue;
@@ -783,6 +794,7 @@ cudaError_t launch_mx_bwd_dwd(const Layer& L, const Bufs& B, void* dWd, cudaStre
   p.n_tiles = L.f / MBN;
   p.out = dWd;
   p.ldo = L.f;
+  p.accumulate = acc ? 1 : 0;
   return mx_launch<MA_TMA_MN, MB_TMA_MN, MS_SEG_K, ME_DWD>(ta, tb, p, L.num_sms, s);
 }
 

@@ -221,7 +221,8 @@ __global__ void __launch_bounds__(256) bwd_dx_kernel(const T* __restrict__ dudv,
 template <typename T>
 __global__ void __launch_bounds__(256) bwd_dw13_kernel(const T* __restrict__ dudv, const T* __restrict__ x,
                                                        const int* __restrict__ off, const int* __restrict__ row_token,
-                                                       int d, int f, int G, T* __restrict__ dWg, T* __restrict__ dWu) {
+                                                       int d, int f, int G, int accumulate, T* __restrict__ dWg,
+                                                       T* __restrict__ dWu) {
   __shared__ float sA[TK][TM], sB[TK][TN];
   const int e = blockIdx.z, r0 = blockIdx.y * TM, c0 = blockIdx.x * TN;
   const int p0 = off[e], K = off[e + 1] - off[e];
@@ -241,7 +242,7 @@ __global__ void __launch_bounds__(256) bwd_dw13_kernel(const T* __restrict__ dud
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int c = c0 + tx * 4 + j;
-      if (c < d) dst[c] = from_f<T>(acc[i][j]);
+      if (c < d) dst[c] = from_f<T>(accumulate ? acc[i][j] + to_f(dst[c]) : acc[i][j]);
     }
   }
 }
@@ -249,7 +250,7 @@ __global__ void __launch_bounds__(256) bwd_dw13_kernel(const T* __restrict__ dud
 template <typename T>
 __global__ void __launch_bounds__(256) bwd_dwd_kernel(const T* __restrict__ dy, const T* __restrict__ hg,
                                                       const int* __restrict__ off, const int* __restrict__ row_token,
-                                                      int d, int f, T* __restrict__ dWd) {
+                                                      int d, int f, int accumulate, T* __restrict__ dWd) {
   __shared__ float sA[TK][TM], sB[TK][TN];
   const int e = blockIdx.z, c0 = blockIdx.y * TM, i0 = blockIdx.x * TN;
   const int p0 = off[e], K = off[e + 1] - off[e];
@@ -265,7 +266,10 @@ __global__ void __launch_bounds__(256) bwd_dwd_kernel(const T* __restrict__ dy, 
     const int c = c0 + ty * 4 + i;
     if (c >= d) continue;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) dWd[((size_t)e * d + c) * f + i0 + tx * 4 + j] = from_f<T>(acc[i][j]);
+    for (int j = 0; j < 4; ++j) {
+      T& o = dWd[((size_t)e * d + c) * f + i0 + tx * 4 + j];
+      o = from_f<T>(accumulate ? acc[i][j] + to_f(o) : acc[i][j]);
+    }
   }
 }
 
@@ -313,17 +317,18 @@ cudaError_t launch_simt_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_simt_bwd_dw13(const Layer& L, const Bufs& B, const void* x, void* dWg, void* dWu, cudaStream_t s) {
+cudaError_t launch_simt_bwd_dw13(const Layer& L, const Bufs& B, const void* x, void* dWg, void* dWu, bool acc,
+                                cudaStream_t s) {
   dim3 g13((L.d + TN - 1) / TN, 2 * L.f / TM, L.E + L.S);
   MOE_DISPATCH(L, bwd_dw13_kernel<T><<<g13, 256, 0, s>>>((const T*)B.dudv, (const T*)x, B.off, B.row_token, L.d, L.f,
-                                                         L.G, (T*)dWg, (T*)dWu));
+                                                         L.G, acc ? 1 : 0, (T*)dWg, (T*)dWu));
   return cudaGetLastError();
 }
 
-cudaError_t launch_simt_bwd_dwd(const Layer& L, const Bufs& B, const void* dy, void* dWd, cudaStream_t s) {
+cudaError_t launch_simt_bwd_dwd(const Layer& L, const Bufs& B, const void* dy, void* dWd, bool acc, cudaStream_t s) {
   dim3 gd(L.f / TN, (L.d + TM - 1) / TM, L.E + L.S);
   MOE_DISPATCH(L, bwd_dwd_kernel<T><<<gd, 256, 0, s>>>((const T*)dy, (const T*)B.hg, B.off, B.row_token, L.d, L.f,
-                                                       (T*)dWd));
+                                                       acc ? 1 : 0, (T*)dWd));
   return cudaGetLastError();
 }
 

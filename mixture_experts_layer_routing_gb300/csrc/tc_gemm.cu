@@ -70,6 +70,7 @@ struct TcParams {
   float* dg_part;         // EPI_DH: gate-gradient partials [A_rows, dg_slots]
   int dg_slots;
   int A_rows;             // routed rows (rows >= A_rows are the shared expert)
+  int accumulate;         // EPI_DW13 / EPI_DWD: add to the values already in the output
   int* status;
 };
 
@@ -518,6 +519,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 64; ++i) of[i] = 0.f;
           }
+          if (p.accumulate) {
+            const bf16* base = (EPI == EPI_DW13 && (t.m & 1)) ? (const bf16*)p.out2 : (const bf16*)p.out;
+            const bf16* old = base + (size_t)(orow0 + lane) * p.ldo + t.n * BN + c0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              float o8[8];
+              unpack8(*reinterpret_cast<const uint4*>(old + q * 8), o8);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) of[q * 8 + i] += o8[i];
+            }
+          }
           // the store that last read this buffer (two sub-tiles ago) must have finished reading it
           if (lane == 0) bulk_wait_read<1>();
           __syncwarp();
@@ -683,7 +695,8 @@ cudaError_t launch_tc_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s) {
 }
 
 // B3: dW13[e] = [du dv]_seg^T x_seg, K over the expert's sorted rows.
-cudaError_t launch_tc_bwd_dw13(const Layer& L, const Bufs& B, const void* x, void* dWg, void* dWu, cudaStream_t s) {
+cudaError_t launch_tc_bwd_dw13(const Layer& L, const Bufs& B, const void* x, void* dWg, void* dWu, bool acc,
+                              cudaStream_t s) {
   CUtensorMap tdudv;
   if (!make_tmap(&tdudv, B.dudv, 2 * L.f, B.R, 64, BK)) return cudaErrorInvalidValue;
   TcParams p = base_params(L, B);
@@ -694,6 +707,7 @@ cudaError_t launch_tc_bwd_dw13(const Layer& L, const Bufs& B, const void* x, voi
   p.out = dWg;
   p.out2 = dWu;
   p.ldo = L.d;
+  p.accumulate = acc ? 1 : 0;
   const uint64_t nseg = L.E + L.S;
   CUtensorMap tg, tu;
   if (!make_tmap(&tg, dWg, L.d, nseg * L.f, 64, 32) || !make_tmap(&tu, dWu, L.d, nseg * L.f, 64, 32))
@@ -703,7 +717,7 @@ cudaError_t launch_tc_bwd_dw13(const Layer& L, const Bufs& B, const void* x, voi
 }
 
 // B3: dWd[e] = dy_seg^T (g h)_seg, K over the expert's sorted rows.
-cudaError_t launch_tc_bwd_dwd(const Layer& L, const Bufs& B, const void* dy, void* dWd, cudaStream_t s) {
+cudaError_t launch_tc_bwd_dwd(const Layer& L, const Bufs& B, const void* dy, void* dWd, bool acc, cudaStream_t s) {
   CUtensorMap thg;
   if (!make_tmap(&thg, B.hg, L.f, B.R, 64, BK)) return cudaErrorInvalidValue;
   TcParams q = base_params(L, B);
@@ -713,6 +727,7 @@ cudaError_t launch_tc_bwd_dwd(const Layer& L, const Bufs& B, const void* dy, voi
   q.n_tiles = L.f / kBNdwd;
   q.out = dWd;
   q.ldo = L.f;
+  q.accumulate = acc ? 1 : 0;
   CUtensorMap td;
   if (!make_tmap(&td, dWd, L.f, (uint64_t)(L.E + L.S) * L.d, 64, 32)) return cudaErrorInvalidValue;
   return launch<kBNdwd, A_GATHER_MN, B_TMA_MN, SCHED_SEG_K, EPI_DWD>(thg /*unused*/, thg, q, L.num_sms, s, &td);
