@@ -404,7 +404,49 @@ def run_extra(args, dev, pk):
         layer.close()
         del layer, inp
         torch.cuda.empty_cache()
+    extra.update(run_extra_mxfp8(dev, pk))
     return extra
+
+
+def run_extra_mxfp8(dev, pk):
+    """DeepSeek-V3-shaped MXFP8 forward + backward, T=8192 in 2368-token chunks over a 512 MB ring."""
+    from mixture_experts_layer_routing_gb300 import MoeLayer, moe_train_chunked, moe_train_chunked_sizes
+    spec = moe_synth.DSV3_MXFP8
+    inp = moe_synth.make_inputs(spec, dev, grad=True)
+    layer = MoeLayer.from_spec(spec, device=dev)
+    layer.set_weights(inp["Wr"], inp["b"], inp["Wg"], inp["Wu"], inp["Wd"])
+    torch.cuda.synchronize()
+    del inp["Wg"], inp["Wu"], inp["Wd"]
+    torch.cuda.empty_cache()
+    cnt = layer.route(inp["x"])["cnt"].cpu().numpy()
+    z = moe_train_chunked_sizes(layer.h, spec.T)
+    ring_bytes = (512 << 20) // z["slot"] * z["slot"]
+    ring = layer.buffer("ring", ring_bytes)
+    ws = layer.buffer("chunk_ws", z["workspace"])
+    g = layer.grads_like(inp["x"])
+    y = torch.empty_like(inp["x"])
+    rec = []
+    fn = lambda: rec.append(moe_train_chunked(layer.h, inp["x"], inp["dy"], spec.T, y, g["dx"], g["dWr"],  # noqa: E731
+                                              g["dWg"], g["dWu"], g["dWd"], ring, ring_bytes, ws))
+    ms = time_steps(fn, 3, 3, 1)
+    prof = profile_groups(layer.h, fn, 2)
+    work_f = work_per_group(spec, cnt, training=True)
+    fl = sum(work_f[k][0] for k in ("router_logits", "gateup", "down", "bwd_dh", "bwd_dx", "bwd_dw13", "bwd_dwd"))
+    nseg, d, f = spec.E + spec.S, spec.d, spec.f
+    # ideal bytes: each weight once per quantisation axis (E4M3 + E8M0), weight gradients written once (bf16),
+    # activations in and out once
+    by = 2 * (3 * nseg * f * d) * (1 + 1 / 32) + 3 * nseg * f * d * 2 + 4 * spec.T * d * 2
+    mx_peak = 2 * pk["bf16_tflops"]          # MXFP8 dense = 2x bf16 (nominal ratio) of the measured bf16 peak
+    t_roof = max(fl / (mx_peak * 1e12), by / (pk["hbm_gbs"] * 1e9))
+    out = {spec.name + " fwd+bwd": {
+        "tokens_per_s": spec.T / (ms * 1e-3), "ms": ms, "roofline_ms": t_roof * 1e3,
+        "frac_of_roofline": t_roof * 1e3 / ms, "chunks": z["n_chunks"], "ring_slots": ring_bytes // z["slot"],
+        "recomputed_chunks": rec[-1] if rec else None, "peak_mxfp8_tflops": mx_peak,
+        "groups_ms": {k: v[1] / 2 for k, v in prof.items()}}}
+    layer.close()
+    del layer, inp, g, y
+    torch.cuda.empty_cache()
+    return out
 
 
 # -------------------------------------------------------- reference arm

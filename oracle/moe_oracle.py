@@ -397,7 +397,7 @@ def mx_fake_quant_tokens(a):
 
 
 def backward(x, Wr, b, Wg, Wu, Wd, dy, k: int, router: str, renorm: bool, scale: float,
-             n_shared: int = 0, logits32=None, mx: bool = False):
+             n_shared: int = 0, logits32=None, mx: bool = False, experts=None):
     """Gradients of sum(y * dy) with respect to x, Wr, Wg, Wu, Wd (b gets none).
 
     Per assignment (expert e, token t, gate g):
@@ -416,6 +416,11 @@ def backward(x, Wr, b, Wg, Wu, Wd, dy, k: int, router: str, renorm: bool, scale:
                 in sorted order, zero-padded): dWg = du^T x, dWu = dv^T x,
                 dWd = dy^T (g h)
     The router GEMMs stay unquantised.
+
+    experts (optional): evaluate only these experts (the shared expert is E);
+    dWg, dWu, dWd are then dicts {expert: gradient} holding exactly those
+    experts' gradients, while dx, dWr and dg miss the other experts' terms.
+    Used to check single experts of a full-size layer.
     """
     x = np.asarray(x, f64)
     dy = np.asarray(dy, f64)
@@ -428,14 +433,19 @@ def backward(x, Wr, b, Wg, Wu, Wd, dy, k: int, router: str, renorm: bool, scale:
     idx, g, perm, off = r["idx"], r["gate"], r["perm"], r["off"]
     gflat = g.ravel()
     dx = np.zeros((T, d), f64)
-    dWg = np.zeros(np.asarray(Wg).shape, f64)
-    dWu = np.zeros(np.asarray(Wu).shape, f64)
-    dWd = np.zeros(np.asarray(Wd).shape, f64)
+    if experts is None:
+        dWg = np.zeros(np.asarray(Wg).shape, f64)
+        dWu = np.zeros(np.asarray(Wu).shape, f64)
+        dWd = np.zeros(np.asarray(Wd).shape, f64)
+    else:
+        dWg, dWu, dWd = {}, {}, {}             # {expert: gradient} for the listed experts
     dg = np.zeros(T * k, f64)
-    experts = [(e, perm[off[e]:off[e + 1]]) for e in range(E)]
+    todo = [(e, perm[off[e]:off[e + 1]]) for e in range(E)]
     if n_shared:
-        experts.append((E, None))
-    for e, rows in experts:
+        todo.append((E, None))
+    if experts is not None:
+        todo = [(e, rows) for e, rows in todo if e in set(experts)]
+    for e, rows in todo:
         if rows is None:                      # shared expert: every token, gate 1
             tok = np.arange(T)
             ge = np.ones(T, f64)

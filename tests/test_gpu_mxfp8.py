@@ -104,3 +104,58 @@ def test_mx_forward_backward_parity_and_reruns():
     for name in grads:
         assert torch.equal(grads[name], g2[name]), name
     layer.close()
+
+
+class DeviceExperts:
+    """Indexable view of a device weight stack [E+S, ...] that yields one expert's float64 array at a time."""
+
+    def __init__(self, t):
+        self.t = t
+
+    def __getitem__(self, e):
+        return self.t[e].double().cpu().numpy()
+
+    def __len__(self):
+        return self.t.shape[0]
+
+
+def test_dsv3_mxfp8_chunked_fullsize_sampled_experts():
+    """DeepSeek-V3 shapes, T=8192 in 2368-token chunks, 512 MB ring: properties at full size and the
+    weight gradients of sampled experts against the oracle (per chunk, summed in backward order)."""
+    spec = moe_synth.DSV3_MXFP8
+    inp = moe_synth.make_inputs(spec, DEV, grad=True)
+    layer = MoeLayer.from_spec(spec, device=DEV)
+    layer.set_weights(inp["Wr"], inp["b"], inp["Wg"], inp["Wu"], inp["Wd"])
+    from mixture_experts_layer_routing_gb300 import moe_train_chunked_sizes
+    z = moe_train_chunked_sizes(layer.h, spec.T)
+    assert z["n_chunks"] == 4
+    slots = (512 << 20) // z["slot"]
+    assert slots >= 1
+    out = layer.train_chunked(inp["x"], inp["dy"], slots=slots)
+    keep = {k: v.clone() for k, v in out.items() if torch.is_tensor(v)}
+    out4 = layer.train_chunked(inp["x"], inp["dy"], slots=4)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert out["recomputed"] == max(0, 4 - slots) and out4["recomputed"] == 0
+    for name, v in keep.items():
+        assert torch.equal(v, out4[name]), name           # ring size never changes a result
+    r = layer.route(inp["x"])
+    cnt = r["cnt"].cpu().numpy()
+    assert cnt.sum() == spec.T * spec.k                    # dropless
+    logits = r["logits"].cpu().numpy()
+    rng = np.random.default_rng(1)
+    sample = sorted({int(np.argmax(cnt)), spec.E, int(rng.integers(spec.E))})   # hottest, shared, random
+    n = {k: np64(inp[k]) for k in ("x", "dy", "Wr", "b")}
+    W = {k: DeviceExperts(inp[k]) for k in ("Wg", "Wu", "Wd")}
+    acc = {k: {e: 0.0 for e in sample} for k in ("dWg", "dWu", "dWd")}
+    for a, b in reversed(oracle.chunk_bounds(spec.T, spec.chunk)):
+        g = oracle.backward(n["x"][a:b], n["Wr"], n["b"], W["Wg"], W["Wu"], W["Wd"], n["dy"][a:b],
+                            logits32=logits[a:b], mx=True, experts=sample, **kw(spec))
+        for k in acc:
+            for e in sample:
+                acc[k][e] = acc[k][e] + g[k].get(e, 0.0)     # an expert with no token in a chunk adds 0
+    for e in sample:
+        for k in ("dWg", "dWu", "dWd"):
+            err = oracle.rel_frobenius(np64(keep[k][e]), acc[k][e])
+            assert err <= TOL_MX, (e, k, err)
+    layer.close()

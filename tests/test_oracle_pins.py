@@ -488,3 +488,15 @@ def test_token_axis_quantiser_brute_force():
             full[:len(blk)] = blk
             want = oracle.mx_fake_quant(full[None, :], axis=1)[0][:len(blk)]
             assert np.array_equal(q[b0:b0 + 32, c], want)
+
+
+def test_backward_expert_filter_matches_full_backward():
+    L = _mx_layer(T=11)
+    args = (L["x"], L["Wr"], L["b"], L["Wg"], L["Wu"], L["Wd"], L["dy"])
+    for mx in (False, True):
+        full = oracle.backward(*args, mx=mx, **MXKW)
+        part = oracle.backward(*args, mx=mx, experts=[1, 3], **MXKW)      # expert 3 is the shared one
+        assert set(part["dWg"]) == {1, 3}
+        for e in (1, 3):
+            for n in ("dWg", "dWu", "dWd"):
+                np.testing.assert_array_equal(part[n][e], full[n][e])
