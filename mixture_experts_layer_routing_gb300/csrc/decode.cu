@@ -106,34 +106,62 @@ __global__ void __launch_bounds__(kRouteWarps * 32) decode_route_kernel(
     warp_topk_gates(w.logits + (size_t)t * E, bias, E, k, router, renorm, scale, w.idx + (size_t)t * k,
                     w.gate + (size_t)t * k);
   __syncthreads();
-  // experts in use and their token lists (stable: ascending assignment)
+  // experts in use and their token lists (stable: ascending assignment); thread e owns expert e
   __shared__ int cnt[kMaxE + 1];
   __shared__ int start[kMaxE + 2];
+  __shared__ int wsum[kRouteWarps][2];
   for (int e = threadIdx.x; e <= E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
   const int A = B * k;
   for (int a = threadIdx.x; a < A; a += blockDim.x) atomicAdd(&cnt[__ldcg(w.idx + a)], 1);
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int nU = 0, run = 0;
-    for (int e = 0; e < E; ++e)
-      if (cnt[e]) {
-        start[e] = run;
-        w.U[nU] = e;
-        w.u_off[nU] = run;
-        run += cnt[e];
+  {
+    // block-wide exclusive scans of (expert used, its count) over e = threadIdx.x < E
+    const int e = threadIdx.x;
+    const int c = e < E ? cnt[e] : 0;
+    int used = c > 0 ? 1 : 0, run = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int nu = __shfl_up_sync(0xffffffffu, used, o), nr = __shfl_up_sync(0xffffffffu, run, o);
+      if (lane >= o) {
+        used += nu;
+        run += nr;
+      }
+    }
+    if (lane == 31) {
+      wsum[wib][0] = used;
+      wsum[wib][1] = run;
+    }
+    __syncthreads();
+    int bu = 0, br = 0;
+    for (int q = 0; q < wib; ++q) {
+      bu += wsum[q][0];
+      br += wsum[q][1];
+    }
+    int totu = 0, totr = 0;
+    for (int q = 0; q < kRouteWarps; ++q) {
+      totu += wsum[q][0];
+      totr += wsum[q][1];
+    }
+    const int pos_u = bu + used - (c > 0 ? 1 : 0), pos_r = br + run - c;
+    if (c > 0) {
+      start[e] = pos_r;
+      w.U[pos_u] = e;
+      w.u_off[pos_u] = pos_r;
+    }
+    if (threadIdx.x == 0) {
+      int nU = totu, r0 = totr;
+      if (S) {
+        start[E] = r0;
+        w.U[nU] = E;
+        w.u_off[nU] = r0;
+        r0 += B;
         ++nU;
       }
-    if (S) {
-      start[E] = run;
-      w.U[nU] = E;
-      w.u_off[nU] = run;
-      run += B;
-      ++nU;
+      w.u_off[nU] = r0;
+      *w.nU = nU;
+      *counter = 0;                         // ready for the next call
     }
-    w.u_off[nU] = run;
-    *w.nU = nU;
-    *counter = 0;                         // ready for the next call
   }
   __syncthreads();
   for (int a = threadIdx.x; a < A; a += blockDim.x) {
@@ -156,8 +184,23 @@ constexpr int kTokGroup = 4;
 // One warp per (U entry, row i) item, grid-stride over items. Each lane loads
 // kBatch 16-byte chunks of both weight rows before using any of them.
 __global__ void __launch_bounds__(256) decode_gateup_kernel(const bf16* __restrict__ x, const bf16* __restrict__ W13,
-                                                            int d, int f, int G, int k, DecodeWs w) {
+                                                            int d, int f, int G, int k, int E, int S, DecodeWs w) {
   griddep_launch();
+  // The shared expert is used by every token whatever the routing: while the
+  // router still runs, pull its gate/up rows into L2 (each block one slice).
+  if (S && threadIdx.x == 0) {
+    const size_t bytes = (size_t)2 * f * d * sizeof(bf16);
+    const size_t slice = ((bytes + gridDim.x - 1) / gridDim.x + 15) & ~(size_t)15;
+    const size_t b0 = (size_t)blockIdx.x * slice;
+    if (b0 < bytes) {
+      const char* base = (const char*)(W13 + (size_t)E * 2 * f * d) + b0;
+      const size_t n = (bytes - b0) < slice ? (bytes - b0) : slice;
+      for (size_t o = 0; o < n; o += 65536) {
+        const uint32_t sz = (uint32_t)((n - o) < 65536 ? (n - o) : 65536);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + o), "r"(sz) : "memory");
+      }
+    }
+  }
   griddep_wait();
   const int lane = threadIdx.x & 31;
   const int nU = *w.nU;
@@ -165,7 +208,8 @@ __global__ void __launch_bounds__(256) decode_gateup_kernel(const bf16* __restri
   const int nwarps = gridDim.x * (blockDim.x >> 5);
   const int nchunk = d / 8;
   for (int it = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items; it += nwarps) {
-    const int ui = it / f, i = it - ui * f;
+    // the last U entry (the shared expert when there is one) first: its rows are already in L2
+    const int ui = (it / f + nU - 1) % nU, i = it % f;
     const int e = w.U[ui];
     const int a0 = w.u_off[ui], a1 = w.u_off[ui + 1];
     const bf16* wg = W13 + ((size_t)e * 2 * f + (i / G) * 2 * G + (i % G)) * d;
@@ -343,7 +387,7 @@ cudaError_t launch_decode_route(const Layer& L, const void* x, int B, void* ws, 
 cudaError_t launch_decode_gateup(const Layer& L, const void* x, int B, void* ws, cudaStream_t s) {
   DecodeWs w = carve(L, B, ws);
   return launch_pdl(decode_gateup_kernel, L.num_sms * 4, 256, 0, s, (const bf16*)x, (const bf16*)L.W13, L.d, L.f, L.G,
-                    L.k, w);
+                    L.k, L.E, L.S, w);
 }
 
 cudaError_t launch_decode_down(const Layer& L, int B, void* y, void* ws, cudaStream_t s) {

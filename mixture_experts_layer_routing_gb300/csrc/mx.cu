@@ -239,9 +239,13 @@ __device__ __forceinline__ MTile mx_map(const MxParams& p, int L) {
   }
   const int Me = p.mt_off[lo + 1] - p.mt_off[lo];
   const int local = L - p.mt_off[lo] * p.n_tiles;
+  // m-tiles in groups of kRasterM, every n-tile of a group before the next group (L2 reuse)
+  const int g = local / (kRasterM * p.n_tiles);
+  const int gm = min(kRasterM, Me - g * kRasterM);
+  const int within = local - g * kRasterM * p.n_tiles;
   t.e = lo;
-  t.n = local / Me;
-  t.m = local % Me;
+  t.n = within / gm;
+  t.m = g * kRasterM + within % gm;
   t.row0 = p.off[lo] + t.m * MBM;
   t.row_end = p.off[lo + 1];
   t.nkb = p.K / MBK;

@@ -120,9 +120,14 @@ __device__ __forceinline__ Tile map_tile(const TcParams& p, int L) {
   }
   const int Me = p.mt_off[lo + 1] - p.mt_off[lo];
   const int local = L - p.mt_off[lo] * p.n_tiles;
+  // m-tiles in groups of kRasterM, every n-tile of a group before the next group: CTAs running
+  // together share the group's token rows and the expert's weight tiles in L2
+  const int g = local / (kRasterM * p.n_tiles);
+  const int gm = min(kRasterM, Me - g * kRasterM);
+  const int within = local - g * kRasterM * p.n_tiles;
   t.e = lo;
-  t.n = local / Me;
-  t.m = local % Me;
+  t.n = within / gm;
+  t.m = g * kRasterM + within % gm;
   t.row0 = p.off[lo] + t.m * BM;
   t.row_end = p.off[lo + 1];
   t.nkb = p.K / BK;

@@ -8,6 +8,7 @@ namespace moe {
 namespace {
 
 constexpr int kChunkBytes = 64 * 128;   // 64 rows of 128 bytes (one bf16 MN-major column chunk)
+constexpr int kRasterM = 16;            // m-tiles per rasterisation group of the segment schedules
 
 // ------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
