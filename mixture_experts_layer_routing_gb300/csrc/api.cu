@@ -199,6 +199,12 @@ moe_status run_route(moe_handle_s* h, const Bufs& B, const void* x, const float*
   return MOE_OK;
 }
 
+// Combined token-axis operands of a chunked MXFP8 step (see moe_train_chunked).
+struct MxDefer {
+  Bufs comb;        // dudv_t, x_t, dy_t, hg_t (+ scales) over all chunks; mt_off = per-expert block prefix
+  const int* base;  // [nseg] row where each expert's rows of the current chunk start
+};
+
 // Forward of T >= 1 tokens (arguments already validated).
 moe_status forward_body(moe_handle_s* h, const void* x, int T, void* y, void* ctx, void* workspace, cudaStream_t s) {
   const Layer& L = h->L;
@@ -223,7 +229,8 @@ moe_status forward_body(moe_handle_s* h, const void* x, int T, void* y, void* ct
 // Backward of T >= 1 tokens with the forward's ctx (arguments already validated). acc: add the
 // weight gradients to the values already in dWr, dWg, dWu, dWd instead of overwriting them.
 moe_status backward_body(moe_handle_s* h, const void* x, const void* dy, int T, const void* ctx, void* dx, float* dWr,
-                         void* dWg, void* dWu, void* dWd, void* workspace, cudaStream_t s, bool acc) {
+                         void* dWg, void* dWu, void* dWd, void* workspace, cudaStream_t s, bool acc,
+                         const MxDefer* defer = nullptr) {
   const Layer& L = h->L;
   Bufs B = carve(L, T, nullptr, ctx, workspace);
   if (h->mx) {
@@ -240,15 +247,21 @@ moe_status backward_body(moe_handle_s* h, const void* x, const void* dy, int T, 
   CK(run(h, s, G_ROUTER_BWD, 2, [&] { return launch_router_bwd(L, B, x, dWr, acc, s); }));
   CK(run(h, s, G_DX_GATHER, 1, [&] { return launch_dx_gather(L, B, dx, s); }));
   if (h->mx) {
+    // token-axis operands of the weight gradients: into this call's buffers, or (chunked step)
+    // into the step's combined buffers, whose single weight-gradient pass runs after the last chunk
+    const Bufs& O = defer ? defer->comb : B;
+    const int* base = defer ? defer->base : nullptr;
     CK(run(h, s, G_MX_QUANT, 4, [&] {
-      cudaError_t e = launch_mx_quant_tokens(L, B, B.dudv, false, 2 * L.f, B.dudv_t, B.dudv_ts, s);
-      if (e == cudaSuccess) e = launch_mx_quant_tokens(L, B, x, true, L.d, B.x_t, B.x_ts, s);
-      if (e == cudaSuccess) e = launch_mx_quant_tokens(L, B, dy, true, L.d, B.dy_t, B.dy_ts, s);
-      if (e == cudaSuccess) e = launch_mx_quant_tokens(L, B, B.hg, false, L.f, B.hg_t, B.hg_ts, s);
+      cudaError_t e = launch_mx_quant_tokens(L, B, B.dudv, false, 2 * L.f, O.dudv_t, O.dudv_ts, s, base);
+      if (e == cudaSuccess) e = launch_mx_quant_tokens(L, B, x, true, L.d, O.x_t, O.x_ts, s, base);
+      if (e == cudaSuccess) e = launch_mx_quant_tokens(L, B, dy, true, L.d, O.dy_t, O.dy_ts, s, base);
+      if (e == cudaSuccess) e = launch_mx_quant_tokens(L, B, B.hg, false, L.f, O.hg_t, O.hg_ts, s, base);
       return e;
     }));
-    CK(run(h, s, G_BWD_DW13, 1, [&] { return launch_mx_bwd_dw13(L, B, dWg, dWu, acc, s); }));
-    CK(run(h, s, G_BWD_DWD, 1, [&] { return launch_mx_bwd_dwd(L, B, dWd, acc, s); }));
+    if (!defer) {
+      CK(run(h, s, G_BWD_DW13, 1, [&] { return launch_mx_bwd_dw13(L, B, dWg, dWu, acc, s); }));
+      CK(run(h, s, G_BWD_DWD, 1, [&] { return launch_mx_bwd_dwd(L, B, dWd, acc, s); }));
+    }
   } else if (h->tc) {
     CK(run(h, s, G_BWD_DW13, 1, [&] { return launch_tc_bwd_dw13(L, B, x, dWg, dWu, acc, s); }));
     CK(run(h, s, G_BWD_DWD, 1, [&] { return launch_tc_bwd_dwd(L, B, dy, dWd, acc, s); }));
@@ -262,16 +275,26 @@ moe_status backward_body(moe_handle_s* h, const void* x, const void* dy, int T, 
 // Chunking of a training step over a ring of saved activations.
 struct ChunkPlan {
   int chunk, n;
-  size_t slot, fwd_ws, bwd_ws;
+  size_t slot, fwd_ws, bwd_ws, comb;   // comb: MXFP8 combined weight-gradient operands (0 otherwise)
+  size_t rc;                           // rows of the combined operands
 };
 ChunkPlan chunk_plan(const moe_handle_s* h, int T) {
   ChunkPlan c;
+  const Layer& L = h->L;
   c.chunk = (h->cfg.chunk_tokens > 0 && h->cfg.chunk_tokens < T) ? h->cfg.chunk_tokens : T;
   c.n = c.chunk > 0 ? (T + c.chunk - 1) / c.chunk : 0;
-  const Sizes z = sizes_for(h->L, c.chunk);
+  const Sizes z = sizes_for(L, c.chunk);
   c.slot = al(z.ctx);
   c.fwd_ws = al(z.fwd_ws);
   c.bwd_ws = al(z.bwd_ws);
+  c.comb = 0;
+  c.rc = 0;
+  if (h->mx) {
+    const size_t nseg = L.E + L.S, d = L.d, f = L.f;
+    c.rc = ((size_t)T * L.k + (size_t)L.S * T + 127) / 128 * 128 + 128 * nseg * (size_t)c.n;
+    c.comb = al(c.rc * 2 * f) + al(c.rc * 2 * f / 32) + 2 * (al(c.rc * d) + al(c.rc * d / 32)) + al(c.rc * f) +
+             al(c.rc * f / 32) + al(4 * (size_t)c.n * (nseg + 1)) + al(4 * (size_t)c.n * nseg) + al(4 * (nseg + 1));
+  }
   return c;
 }
 
@@ -455,7 +478,7 @@ moe_status moe_train_chunked_sizes(moe_handle h, int T, size_t* slot_bytes, size
   if (!h || T < 1 || T > h->cfg.T_max) return MOE_ERR_INVALID_ARG;
   const ChunkPlan c = chunk_plan(h, T);
   if (slot_bytes) *slot_bytes = c.slot;
-  if (workspace_bytes) *workspace_bytes = c.fwd_ws + c.bwd_ws;
+  if (workspace_bytes) *workspace_bytes = c.fwd_ws + c.bwd_ws + c.comb;
   if (n_chunks) *n_chunks = c.n;
   return MOE_OK;
 }
@@ -477,6 +500,27 @@ moe_status moe_train_chunked(moe_handle h, const void* x, const void* dy, int T,
   char* ws_f = (char*)workspace;
   char* ws_b = ws_f + c.fwd_ws;
   auto slot_of = [&](int ch) { return (char*)ring + (size_t)(ch % R) * c.slot; };
+  // MXFP8: weight-gradient operands of every chunk go to combined buffers (one gradient pass at the end)
+  MxDefer defer;
+  int* chunk_mt = nullptr;
+  if (h->mx) {
+    const size_t nseg = L.E + L.S, d = L.d, f = L.f, rc = c.rc;
+    char* q = ws_b + c.bwd_ws;
+    std::memset(&defer.comb, 0, sizeof(Bufs));
+    defer.comb.dudv_t = (uint8_t*)q; q += al(rc * 2 * f);
+    defer.comb.dudv_ts = (uint8_t*)q; q += al(rc * 2 * f / 32);
+    defer.comb.x_t = (uint8_t*)q; q += al(rc * d);
+    defer.comb.x_ts = (uint8_t*)q; q += al(rc * d / 32);
+    defer.comb.dy_t = (uint8_t*)q; q += al(rc * d);
+    defer.comb.dy_ts = (uint8_t*)q; q += al(rc * d / 32);
+    defer.comb.hg_t = (uint8_t*)q; q += al(rc * f);
+    defer.comb.hg_ts = (uint8_t*)q; q += al(rc * f / 32);
+    chunk_mt = (int*)q; q += al(4 * (size_t)c.n * (nseg + 1));
+    int* comb_base = (int*)q; q += al(4 * (size_t)c.n * nseg);
+    defer.comb.mt_off = (int*)q;
+    defer.comb.Rp_max = (int)rc;
+    defer.base = comb_base;
+  }
   auto span = [&](int ch, int& t0, int& Tc) {
     t0 = ch * c.chunk;
     Tc = (T - t0) < c.chunk ? (T - t0) : c.chunk;
@@ -488,7 +532,13 @@ moe_status moe_train_chunked(moe_handle h, const void* x, const void* dy, int T,
     const moe_status st = forward_body(h, (const char*)x + t0 * row_bytes, Tc, (char*)y + t0 * row_bytes,
                                        slot_of(ch), ws_f, s);
     if (st != MOE_OK) return st;
+    if (h->mx) {
+      const Bufs Bc = carve(L, Tc, nullptr, slot_of(ch), nullptr);
+      CK(cudaMemcpyAsync(chunk_mt + (size_t)ch * (L.E + L.S + 1), Bc.mt_off, 4 * (size_t)(L.E + L.S + 1),
+                         cudaMemcpyDeviceToDevice, s));
+    }
   }
+  if (h->mx) CK(launch_mx_chunk_layout(L, chunk_mt, c.n, (int*)defer.base, defer.comb.mt_off, s));
   // backward, last chunk first: a chunk whose slot a later chunk overwrote is recomputed
   int rec = 0;
   for (int ch = c.n - 1; ch >= 0; --ch) {
@@ -500,10 +550,29 @@ moe_status moe_train_chunked(moe_handle h, const void* x, const void* dy, int T,
       if (st != MOE_OK) return st;
       ++rec;
     }
+    MxDefer dch = defer;
+    dch.base = defer.base + (size_t)ch * (L.E + L.S);
     const moe_status st =
         backward_body(h, (const char*)x + t0 * row_bytes, (const char*)dy + t0 * row_bytes, Tc, slot_of(ch),
-                      (char*)dx + t0 * row_bytes, dWr, dWg, dWu, dWd, ws_b, s, ch != c.n - 1);
+                      (char*)dx + t0 * row_bytes, dWr, dWg, dWu, dWd, ws_b, s, ch != c.n - 1,
+                      h->mx ? &dch : nullptr);
     if (st != MOE_OK) return st;
+  }
+  if (h->mx) {
+    // one weight-gradient pass over all chunks' rows (chunk order within each expert)
+    Bufs Bw = carve(L, c.chunk, nullptr, slot_of(0), ws_b);
+    Bw.mt_off = defer.comb.mt_off;
+    Bw.Rp_max = defer.comb.Rp_max;
+    Bw.dudv_t = defer.comb.dudv_t;
+    Bw.dudv_ts = defer.comb.dudv_ts;
+    Bw.x_t = defer.comb.x_t;
+    Bw.x_ts = defer.comb.x_ts;
+    Bw.dy_t = defer.comb.dy_t;
+    Bw.dy_ts = defer.comb.dy_ts;
+    Bw.hg_t = defer.comb.hg_t;
+    Bw.hg_ts = defer.comb.hg_ts;
+    CK(run(h, s, G_BWD_DW13, 1, [&] { return launch_mx_bwd_dw13(L, Bw, dWg, dWu, false, s); }));
+    CK(run(h, s, G_BWD_DWD, 1, [&] { return launch_mx_bwd_dwd(L, Bw, dWd, false, s); }));
   }
   if (recomputed) *recomputed = rec;
   return MOE_OK;

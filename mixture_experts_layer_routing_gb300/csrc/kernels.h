@@ -123,7 +123,9 @@ size_t mx_packed_bytes(const Layer& L);
 cudaError_t mx_pack_weights(Layer& L, const void* Wg, const void* Wu, const void* Wd, void* base, cudaStream_t s);
 cudaError_t launch_mx_quant_rows(const void* src, int rows, int K, uint8_t* q, uint8_t* s, cudaStream_t st);
 cudaError_t launch_mx_quant_tokens(const Layer& L, const Bufs& B, const void* src, bool gather, int W, uint8_t* q,
-                                   uint8_t* s, cudaStream_t st);
+                                   uint8_t* s, cudaStream_t st, const int* out_base = nullptr);
+cudaError_t launch_mx_chunk_layout(const Layer& L, const int* chunk_mt, int n, int* comb_base, int* comb_mt,
+                                   cudaStream_t st);
 cudaError_t launch_mx_gateup(const Layer& L, const Bufs& B, cudaStream_t s);
 cudaError_t launch_mx_down(const Layer& L, const Bufs& B, cudaStream_t s);
 cudaError_t launch_mx_bwd_dh(const Layer& L, const Bufs& B, cudaStream_t s);

@@ -148,11 +148,12 @@ __global__ void __launch_bounds__(256) mx_quant_cols_kernel(const bf16* __restri
                                                             const int* __restrict__ row_token,
                                                             const int* __restrict__ off,
                                                             const int* __restrict__ mt_off, int nseg, int W, int f,
-                                                            int G, uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
+                                                            int G, uint8_t* __restrict__ q, uint8_t* __restrict__ s,
+                                                            const int* __restrict__ out_base) {
   const int c = blockIdx.x * 256 + threadIdx.x;
-  const long rb = blockIdx.y;              // 32-row block of the output
+  long rb = blockIdx.y;                    // 32-row block (of the chunk's padded segment layout)
   if (c >= W) return;
-  long seg_first = 0, seg_len = 0, seg_src0 = 0;
+  long seg_first = 0, seg_len = 0, seg_src0 = 0, out_shift = 0;
   if (SRC == CSRC_SEG_GATHER || SRC == CSRC_SEG_DIRECT) {
     const int pr = (int)(rb * 32);
     if (pr >= mt_off[nseg] * 128) return;
@@ -164,6 +165,8 @@ __global__ void __launch_bounds__(256) mx_quant_cols_kernel(const bf16* __restri
     seg_first = (long)mt_off[lo] * 128;
     seg_len = off[lo + 1] - off[lo];
     seg_src0 = off[lo];
+    // out_base (optional): segment lo's rows go to out_base[lo] onwards instead of seg_first
+    if (out_base) out_shift = (long)out_base[lo] - seg_first;
   }
   float v[32];
 #pragma unroll
@@ -184,6 +187,7 @@ __global__ void __launch_bounds__(256) mx_quant_cols_kernel(const bf16* __restri
   uint4 lo, hi;
   const uint8_t sc = quant32(v, lo, hi);
   const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  rb += out_shift / 32;                    // segment bases are multiples of 128 rows
 #pragma unroll
   for (int i = 0; i < 32; ++i) q[(rb * 32 + i) * W + c] = (uint8_t)(w[i >> 2] >> (8 * (i & 3)));
   s[rb * W + c] = sc;
@@ -669,9 +673,9 @@ cudaError_t mx_pack_weights(Layer& L, const void* Wg, const void* Wu, const void
   mx_quant_rows_kernel<SRC_PLAIN><<<blocks_for(rd, 8), 256, 0, s>>>(dw, nullptr, nullptr, rd, L.f, L.f, 0, L.Wdq,
                                                                      L.Wds);
   mx_quant_cols_kernel<CSRC_W13><<<dim3(blocks_for(d, 256), (unsigned)(r13 / 32)), 256, 0, s>>>(
-      g, u, nullptr, nullptr, nullptr, 0, L.d, L.f, kGateMx, L.W13c, L.W13cs);
+      g, u, nullptr, nullptr, nullptr, 0, L.d, L.f, kGateMx, L.W13c, L.W13cs, nullptr);
   mx_quant_cols_kernel<CSRC_PLAIN><<<dim3(blocks_for(f, 256), (unsigned)(rd / 32)), 256, 0, s>>>(
-      dw, nullptr, nullptr, nullptr, nullptr, 0, L.f, L.f, 0, L.Wdc, L.Wdcs);
+      dw, nullptr, nullptr, nullptr, nullptr, 0, L.f, L.f, 0, L.Wdc, L.Wdcs, nullptr);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (!make_tmap(&L.tm_W13q, L.W13q, d, r13, MBK, MBN, 1) || !make_tmap(&L.tm_Wdq, L.Wdq, f, rd, MBK, MBN, 1) ||
@@ -687,15 +691,55 @@ cudaError_t launch_mx_quant_rows(const void* src, int rows, int K, uint8_t* q, u
 }
 
 // Token-axis operands of the weight gradients: [Rp, W] codes, [Rp/32, W] scales, Rp = mt_off[nseg] * 128.
+// out_base (nullable, device [nseg]): row where each segment's rows start in q (default mt_off[e] * 128).
 cudaError_t launch_mx_quant_tokens(const Layer& L, const Bufs& B, const void* src, bool gather, int W, uint8_t* q,
-                                   uint8_t* s, cudaStream_t st) {
+                                   uint8_t* s, cudaStream_t st, const int* out_base) {
   const dim3 grid(blocks_for(W, 256), (unsigned)(B.Rp_max / 32));
   if (gather)
     mx_quant_cols_kernel<CSRC_SEG_GATHER><<<grid, 256, 0, st>>>((const bf16*)src, nullptr, B.row_token, B.off,
-                                                                B.mt_off, L.E + L.S, W, 0, 0, q, s);
+                                                                B.mt_off, L.E + L.S, W, 0, 0, q, s, out_base);
   else
     mx_quant_cols_kernel<CSRC_SEG_DIRECT><<<grid, 256, 0, st>>>((const bf16*)src, nullptr, B.row_token, B.off,
-                                                                B.mt_off, L.E + L.S, W, 0, 0, q, s);
+                                                                B.mt_off, L.E + L.S, W, 0, 0, q, s, out_base);
+  return cudaGetLastError();
+}
+
+// Layout of the combined token-axis operands of a chunked step: chunk_mt [n][nseg+1] holds each chunk's
+// 128-row tile prefix. Expert e's rows of chunk c start at comb_base[c][e] (all chunks of expert e
+// contiguous, in chunk order); comb_mt [nseg+1] is the prefix of 128-row blocks per expert.
+// One block; thread e per expert (nseg <= 1024).
+__global__ void __launch_bounds__(1024) mx_chunk_layout_kernel(const int* __restrict__ chunk_mt, int n, int nseg,
+                                                                int* __restrict__ comb_base, int* __restrict__ comb_mt) {
+  __shared__ int wsum[32];
+  const int e = threadIdx.x, lane = e & 31, w = e >> 5;
+  int tot = 0;
+  if (e < nseg)
+    for (int c = 0; c < n; ++c) tot += chunk_mt[c * (nseg + 1) + e + 1] - chunk_mt[c * (nseg + 1) + e];
+  int incl = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) wsum[w] = incl;
+  __syncthreads();
+  int base = 0;
+  for (int q = 0; q < w; ++q) base += wsum[q];
+  const int excl = base + incl - tot;
+  if (e < nseg) {
+    comb_mt[e] = excl;
+    int run = excl;
+    for (int c = 0; c < n; ++c) {
+      comb_base[c * nseg + e] = run * 128;
+      run += chunk_mt[c * (nseg + 1) + e + 1] - chunk_mt[c * (nseg + 1) + e];
+    }
+    if (e == nseg - 1) comb_mt[nseg] = excl + tot;
+  }
+}
+
+cudaError_t launch_mx_chunk_layout(const Layer& L, const int* chunk_mt, int n, int* comb_base, int* comb_mt,
+                                   cudaStream_t st) {
+  mx_chunk_layout_kernel<<<1, 1024, 0, st>>>(chunk_mt, n, L.E + L.S, comb_base, comb_mt);
   return cudaGetLastError();
 }
 
