@@ -169,9 +169,11 @@ def stored_traffic(group):
         ent = tab.get(group)
         if not ent:
             return None
-        src = os.path.join(ROOT, ent["source"])
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        if digest != ent["source_sha256_16"]:
+        h = hashlib.sha256()
+        for src in ent["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as fh:
+                h.update(fh.read())
+        if h.hexdigest()[:16] != ent["source_sha256_16"]:
             return None
         return ent["dram_bytes_per_launch"]
     except (OSError, KeyError, ValueError):
@@ -231,10 +233,15 @@ def time_steps(fn, steps, warmup, world):
         torch.distributed.barrier()
     ms = a.elapsed_time(b) / steps
     if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = reduce_max(ms, "cuda")
     return ms
+
+
+def reduce_max(value: float, device) -> float:
+    """The largest value over all ranks (the slowest rank sets the step time)."""
+    t = torch.tensor([float(value)], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
 
 
 def profile_groups(layer_h, fn, steps):

@@ -186,6 +186,14 @@ moe_status moe_get_status(moe_handle h, void* stream, int* device_status);
 moe_status moe_route_noalloc(moe_handle h, const void* x, int T, float* logits, int32_t* idx, float* gate,
                              int32_t* cnt, int32_t* off, int32_t* perm, int32_t* inv, void* stream);
 
+/* Self-test of the device-side failure path (the pages describe no such call):
+ * launches one block that waits, with the bounded wait every tcgen05 pipeline
+ * of the library uses, on an mbarrier that nothing arrives at. After limit_ms
+ * (1..10000) the wait gives up, MOE_ERR_TIMEOUT is recorded in the status word
+ * (read it with moe_get_status) and the kernel returns; the CUDA context stays
+ * usable. Asynchronous on `stream`. */
+moe_status moe_selftest_timeout(moe_handle h, int limit_ms, void* stream);
+
 /* Tracing. When enabled, every kernel launch of later calls on this handle is
  * bracketed by two CUDA events recorded on the call's stream (no extra device
  * memory). moe_profile_read waits for the recorded events and returns, for

@@ -24,7 +24,7 @@ MOE_FP32, MOE_BF16, MOE_MXFP8 = 0, 1, 2
 EXPORTED = ("moe_create", "moe_destroy", "moe_workspace_size", "moe_set_weights", "moe_route", "moe_forward",
             "moe_backward", "moe_decode", "moe_get_status", "moe_profile_enable", "moe_profile_read",
             "moe_launch_count", "moe_route_noalloc", "moe_train_chunked_sizes", "moe_train_chunked",
-            "moe_status_string")
+            "moe_selftest_timeout", "moe_status_string")
 
 
 class MoeError(RuntimeError):
@@ -66,6 +66,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_profile_read.argtypes = [vp, i32, ctypes.c_char_p, P(ctypes.c_longlong), P(ctypes.c_double), P(i32)]
     lib.moe_launch_count.argtypes = [vp, P(ctypes.c_longlong)]
     lib.moe_route_noalloc.argtypes = [vp, vp, i32] + [vp] * 8
+    lib.moe_selftest_timeout.argtypes = [vp, i32, vp]
     lib.moe_train_chunked_sizes.argtypes = [vp, i32, P(sz), P(sz), P(i32)]
     lib.moe_train_chunked.argtypes = [vp, vp, vp, i32] + [vp] * 7 + [sz, vp, P(i32), vp]
     lib.moe_status_string.argtypes = [i32]
@@ -147,6 +148,10 @@ def moe_forward(h, x, T, y, ctx, workspace, stream=None):
 def moe_backward(h, x, dy, T, ctx, dx, dWr, dWg, dWu, dWd, workspace, stream=None):
     _check(load_library().moe_backward(h, _ptr(x), _ptr(dy), T, _ptr(ctx), _ptr(dx), _ptr(dWr), _ptr(dWg),
                                        _ptr(dWu), _ptr(dWd), _ptr(workspace), _stream(stream)), "moe_backward")
+
+
+def moe_selftest_timeout(h, limit_ms: int, stream=None):
+    _check(load_library().moe_selftest_timeout(h, limit_ms, _stream(stream)), "moe_selftest_timeout")
 
 
 def moe_train_chunked_sizes(h, T) -> dict:
