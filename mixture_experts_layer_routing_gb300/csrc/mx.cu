@@ -33,7 +33,7 @@ namespace moe {
 
 namespace {
 
-constexpr int MBM = 128, MBN = 128, MBK = 128, MSTAGES = 6, MLAG = 2;
+constexpr int MBM = 128, MBN = 128, MBK = 128, MSTAGES = 6;
 constexpr int kProd = 4, kEpi = 4;
 constexpr int kMxThreads = (kProd + kEpi + 1) * 32;
 constexpr int kMxMmaWarp = kProd + kEpi;
@@ -385,23 +385,12 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         tmem_st4(scol + 4 + lanebits, wb[0], wb[1], wb[2], wb[3]);
         tmem_st_wait();
         tc_fence_before();
-        if (kGather) {
-          cp_async_commit();
-          if (it >= MLAG) {
-            cp_async_wait<MLAG>();
-            fence_proxy_async();
-            mbar_arrive(full0 + 8 * ((it - MLAG) % MSTAGES));
-          }
-        } else {
-          mbar_arrive(fb);
-        }
+        // gathered rows: the arrival is counted once this thread's copies have landed
+        if (kGather) cp_async_mbar_arrive_noinc(fb);
+        else mbar_arrive(fb);
       }
     }
-    if (kGather) {
-      cp_async_wait<0>();
-      fence_proxy_async();
-      for (int q = (it > MLAG ? it - MLAG : 0); q < it; ++q) mbar_arrive(full0 + 8 * (q % MSTAGES));
-    }
+    if (kGather) cp_async_wait<0>();
   } else if (warp == kMxMmaWarp) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
@@ -422,6 +411,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             break;
           }
           tc_fence_after();
+          if (kGather) fence_proxy_async();   // cp.async (generic proxy) writes seen by the MMA
           const uint32_t sa = smem_u32(smem + s * kStageBytes);
           const uint32_t sb = sa + MBM * MBK;
           const uint32_t scol = tmem_base + kScaleCol0 + s * 8;

@@ -36,7 +36,7 @@ namespace moe {
 
 namespace {
 
-constexpr int BM = 128, BK = 64, STAGES = 4, LAG = 2;
+constexpr int BM = 128, BK = 64, STAGES = 4;
 constexpr int kProducerWarps = 4, kEpiWarps = 4;
 constexpr int kThreads = (kProducerWarps + kEpiWarps + 1) * 32;   // 288
 constexpr int kMmaWarp = kProducerWarps + kEpiWarps;               // warp 8
@@ -315,22 +315,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sa = smem_u32(stage_base + s * Smem<BN>::STAGE);
         const uint32_t sb = sa + Smem<BN>::A_BYTES;
         load_stage<BN, AMODE, BMODE, SCHED>(p, &tmA, &tmB, t, kb, sa, sb, full0 + 8 * s, gsrc, gbytes, tk0);
-        if (MD::kCpAsync) {
-          cp_async_commit();
-          if (it >= LAG) {
-            cp_async_wait<LAG>();
-            fence_proxy_async();
-            mbar_arrive(full0 + 8 * ((it - LAG) % STAGES));
-          }
-        }
+        // the stage's full barrier counts this thread's arrival once all of its copies so far have
+        // landed; the producer goes straight on to the next stage
+        if (MD::kCpAsync) cp_async_mbar_arrive_noinc(full0 + 8 * s);
       }
     }
-    if (MD::kCpAsync) {
-      // complete the last LAG stages (the MMA waits for them even after an abort is seen)
-      cp_async_wait<0>();
-      fence_proxy_async();
-      for (int q = (it > LAG ? it - LAG : 0); q < it; ++q) mbar_arrive(full0 + 8 * (q % STAGES));
-    }
+    if (MD::kCpAsync) cp_async_wait<0>();
   } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
@@ -351,6 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
+          if (MD::kCpAsync) fence_proxy_async();   // cp.async (generic proxy) writes seen by the MMA
           const uint32_t sa = smem_u32(stage_base + s * Smem<BN>::STAGE);
           const uint32_t sb = sa + Smem<BN>::A_BYTES;
 #pragma unroll
