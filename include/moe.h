@@ -161,6 +161,16 @@ moe_status moe_train_chunked(moe_handle h, const void* x, const void* dy, int T,
  * cfg.prec == MOE_BF16. Warp-per-output kernels with fp32 intermediates. */
 moe_status moe_decode(moe_handle h, const void* x, int B, void* y, void* workspace, void* stream);
 
+/* Tensor-core scheduling of the bf16 expert GEMMs (gate/up, down, dY.Wd, dx).
+ * mode 1 runs them on pairs of SMs: 2-CTA clusters, one
+ * tcgen05.mma.cta_group::2 per K step over a 256-row tile, each CTA holding
+ * its own 128 rows and half of the weight tile. mode 0 (the default) runs one
+ * CTA per 128-row tile. The modes agree up to fp32 summation order and each is
+ * deterministic; on GB300 the pairs measured no faster for this layer's
+ * shapes, so they are opt-in. Host-only; another mode returns
+ * MOE_ERR_INVALID_ARG. */
+moe_status moe_set_pairs(moe_handle h, int mode);
+
 /* Wait for the handle's queued work on `stream`, then read and clear the
  * device status word into *device_status (MOE_OK if no device error). */
 moe_status moe_get_status(moe_handle h, void* stream, int* device_status);

@@ -41,7 +41,8 @@ Sizes sizes_for(const Layer& L, int T) {
   const size_t eb = elem_bytes(L.prec);
   const size_t nch = (A + kChunk - 1) / kChunk;
   Sizes z;
-  z.route = al(4 * T * (size_t)L.E) + 2 * al(4 * A) + 3 * al(4 * (nseg + 1)) + 2 * al(4 * A) + 2 * al(4 * R);
+  z.route = al(4 * T * (size_t)L.E) + 2 * al(4 * A) + 2 * al(4 * (nseg + 1)) + al(8 * (nseg + 1)) + 2 * al(4 * A) +
+            2 * al(4 * R);
   z.uv = al(eb * R * 2 * L.f);
   z.fwd_scratch = 2 * al(4 * nch * L.E) + al(eb * R * L.f) + al(eb * R * L.d);
   z.ctx = z.route + z.uv;
@@ -72,7 +73,7 @@ char* carve_route(Bufs& B, const Layer& L, char* p) {
   B.gate = (float*)p; p += al(4 * (size_t)B.A);
   B.cnt = (int*)p; p += al(4 * (nseg + 1));
   B.off = (int*)p; p += al(4 * (nseg + 1));
-  B.mt_off = (int*)p; p += al(4 * (nseg + 1));
+  B.mt_off = (int*)p; p += al(8 * (nseg + 1));   // mt_off, then the pair prefix
   B.perm = (int*)p; p += al(4 * (size_t)B.A);
   B.inv = (int*)p; p += al(4 * (size_t)B.A);
   B.row_token = (int*)p; p += al(4 * (size_t)B.R);
@@ -335,6 +336,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
   L.d = c.d; L.E = c.E; L.S = c.n_shared; L.f = c.f; L.k = c.k;
   L.router = c.router; L.renorm = c.renorm ? 1 : 0; L.prec = c.prec; L.scale = c.route_scale;
   L.G = (c.f % kGate == 0) ? kGate : 64;
+  L.pairs = 0;
   L.has_weights = false;
   if (cudaGetDevice(&h->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&L.num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
@@ -634,6 +636,12 @@ moe_status moe_profile_read(moe_handle h, int max_groups, char* names, long long
 moe_status moe_launch_count(moe_handle h, long long* launches) {
   if (!h || !launches) return MOE_ERR_INVALID_ARG;
   *launches = h->launches;
+  return MOE_OK;
+}
+
+moe_status moe_set_pairs(moe_handle h, int mode) {
+  if (!h || mode < 0 || mode > 1) return MOE_ERR_INVALID_ARG;
+  h->L.pairs = mode;
   return MOE_OK;
 }
 

@@ -36,6 +36,9 @@ struct Layer {
   CUtensorMap tm_Wd;        // K-major rows of Wd (box 64 x 256)
   CUtensorMap tm_W13_mn;    // W13 as [K=2f rows][N=d] for dx (box 64 x 64)
   CUtensorMap tm_Wd_mn;     // Wd as [K=d rows][N=f] for the dY.Wd product (box 64 x 64)
+  CUtensorMap tm_W13_h;     // K-major rows of W13, box 64 x 128 (half an n-tile: one CTA of a pair)
+  CUtensorMap tm_Wd_h;      // K-major rows of Wd, box 64 x 128
+  int pairs;                // 1: expert GEMMs on 2-SM CTA pairs; 0 (default): one CTA per tile
   // MXFP8 packed weights: E4M3 codes and E8M0 scales (one per 32 along the named axis)
   uint8_t *W13q, *W13s;     // [E+S][2f][d] along d (gate/up interleaved in blocks of kGateMx rows); [..][d/32]
   uint8_t *W13c, *W13cs;    // same rows quantised along the packed 2f rows; scales [(E+S)*2f/32][d]

@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(512) scan_kernel(const int* __restrict__ chunk
                                                    int* __restrict__ chunk_base, int* __restrict__ cnt,
                                                    int* __restrict__ off, int* __restrict__ mt_off) {
   __shared__ int c_s[kMaxE + 1];
-  __shared__ int warp_tot[16][2];
+  __shared__ int warp_tot[16][3];
   const int tid = threadIdx.x;
   const int nseg = E + S;
   int c = 0;
@@ -104,39 +104,46 @@ __global__ void __launch_bounds__(512) scan_kernel(const int* __restrict__ chunk
   } else if (tid == E && S) {
     c = T;
   }
-  // exclusive scans of c and of ceil(c / kBM) over the 512 threads
+  // exclusive scans of c, of ceil(c / kBM) and of ceil(tiles / 2) over the 512 threads
   const int lane = tid & 31, w = tid >> 5;
-  int tiles = (c + kBM - 1) / kBM;
-  int ic = c, it = tiles;
+  const int tiles = (c + kBM - 1) / kBM, pairs = (tiles + 1) / 2;
+  int ic = c, it = tiles, ip = pairs;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int nc = __shfl_up_sync(0xffffffffu, ic, o);
     const int nt = __shfl_up_sync(0xffffffffu, it, o);
+    const int np = __shfl_up_sync(0xffffffffu, ip, o);
     if (lane >= o) {
       ic += nc;
       it += nt;
+      ip += np;
     }
   }
   if (lane == 31) {
     warp_tot[w][0] = ic;
     warp_tot[w][1] = it;
+    warp_tot[w][2] = ip;
   }
   __syncthreads();
-  int bc = 0, bt = 0;
+  int bc = 0, bt = 0, bp = 0;
   for (int q = 0; q < w; ++q) {
     bc += warp_tot[q][0];
     bt += warp_tot[q][1];
+    bp += warp_tot[q][2];
   }
-  const int ex_c = bc + ic - c, ex_t = bt + it - tiles;
+  const int ex_c = bc + ic - c, ex_t = bt + it - tiles, ex_p = bp + ip - pairs;
+  int* mp_off = mt_off + nseg + 1;   // prefix of pairs of 128-row tiles, stored after mt_off
   if (tid < nseg) {
     cnt[tid] = c;
     off[tid] = ex_c;
     mt_off[tid] = ex_t;
+    mp_off[tid] = ex_p;
     c_s[tid] = ex_c;
   }
   if (tid == nseg - 1) {
     off[nseg] = ex_c + c;
     mt_off[nseg] = ex_t + tiles;
+    mp_off[nseg] = ex_p + pairs;
   }
   __syncthreads();
   if (tid < E) {

@@ -36,7 +36,8 @@ namespace moe {
 
 namespace {
 
-constexpr int BM = 128, BK = 64, STAGES = 4;
+constexpr int BM = 128, BK = 64;
+constexpr int kSmemMax = 227 * 1024;   // dynamic shared memory per CTA
 constexpr int kProducerWarps = 4, kEpiWarps = 4;
 constexpr int kThreads = (kProducerWarps + kEpiWarps + 1) * 32;   // 288
 constexpr int kMmaWarp = kProducerWarps + kEpiWarps;               // warp 8
@@ -54,6 +55,7 @@ struct TcParams {
   const int* row_token;   // sorted row -> token
   const int* off;         // [nseg+1] segment row offsets
   const int* mt_off;      // [nseg+1] prefix of 128-row tiles (SEG_M)
+  const int* mp_off;      // [nseg+1] prefix of pairs of 128-row tiles (SEG_M over CTA pairs)
   int nseg;
   int dense_rows;         // DENSE: rows of the single segment
   int K;                  // reduction length for SEG_M / DENSE (multiple of 64)
@@ -83,15 +85,41 @@ struct Tile {
   int nkb;             // K blocks of 64
 };
 
-template <int SCHED>
+template <int SCHED, int CG>
 __device__ __forceinline__ int total_tiles(const TcParams& p) {
   if (SCHED == SCHED_DENSE) return ((p.dense_rows + BM - 1) / BM) * p.n_tiles;
   if (SCHED == SCHED_SEG_K) return p.nseg * p.m_tiles * p.n_tiles;
-  return p.mt_off[p.nseg] * p.n_tiles;
+  return (CG == 2 ? p.mp_off[p.nseg] : p.mt_off[p.nseg]) * p.n_tiles;
 }
 
-template <int SCHED>
-__device__ __forceinline__ Tile map_tile(const TcParams& p, int L) {
+// CTA pairs: tile L is (segment, pair of m-tiles 2j and 2j+1, n); the CTA of cluster rank r takes
+// m-tile 2j + r and half of the n-tile's B columns. Pairs in groups of kRasterM / 2, every n-tile
+// of a group before the next group.
+__device__ __forceinline__ Tile map_tile_pair(const TcParams& p, int L, int rank) {
+  Tile t;
+  int lo = 0, hi = p.nseg;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (p.mp_off[mid] * p.n_tiles <= L) lo = mid; else hi = mid;
+  }
+  constexpr int kRasterP = kRasterM / 2;
+  const int Pe = p.mp_off[lo + 1] - p.mp_off[lo];
+  const int local = L - p.mp_off[lo] * p.n_tiles;
+  const int g = local / (kRasterP * p.n_tiles);
+  const int gp = min(kRasterP, Pe - g * kRasterP);
+  const int within = local - g * kRasterP * p.n_tiles;
+  t.e = lo;
+  t.n = within / gp;
+  t.m = 2 * (g * kRasterP + within % gp) + rank;
+  t.row0 = p.off[lo] + t.m * BM;
+  t.row_end = p.off[lo + 1];
+  t.nkb = p.K / BK;
+  return t;
+}
+
+template <int SCHED, int CG>
+__device__ __forceinline__ Tile map_tile(const TcParams& p, int L, int rank) {
+  if (CG == 2) return map_tile_pair(p, L, rank);
   Tile t;
   if (SCHED == SCHED_DENSE) {
     t.e = 0;
@@ -137,13 +165,20 @@ __device__ __forceinline__ Tile map_tile(const TcParams& p, int L) {
 // Epilogue staging for TMA stores: per epilogue warp two 32-row x 64-column bf16 sub-tiles (4 KB each).
 constexpr int kStageOutBytes = kEpiWarps * 2 * 32 * 128;
 
-template <int BN, int SCHED = SCHED_SEG_M>
+// Shared memory of one CTA: a ring of NS stages (A tile + this CTA's B columns: all BN, or BN/2
+// when a CTA pair shares the B tile), then staging and barriers. Single CTAs keep 4 stages (deeper
+// rings measured no faster and leave no L1 for the epilogue's loads); pairs take as many as fit,
+// up to 8.
+template <int BN, int SCHED, int CG>
 struct Smem {
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_BYTES = (BN / CG) * BK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int OUT = SCHED == SCHED_SEG_K ? kStageOutBytes : 0;
-  static constexpr int TOTAL = STAGES * STAGE + OUT + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int FIXED = OUT + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int NS_CAP = CG == 2 ? 8 : 4;
+  static constexpr int NS = (kSmemMax - FIXED) / STAGE < NS_CAP ? (kSmemMax - FIXED) / STAGE : NS_CAP;
+  static constexpr int TOTAL = NS * STAGE + FIXED;
 };
 
 template <int AMODE, int BMODE>
@@ -154,26 +189,38 @@ struct Modes {
 };
 
 // Issues one stage: A and B of K block kb of tile t.
-template <int BN, int AMODE, int BMODE, int SCHED>
+// With CTA pairs (CG = 2) this CTA loads B columns rank*BN/2 .. of the n-tile, and every TMA load
+// of either CTA completes on rank 0's full barrier (lead_full), which rank 0 arms with the bytes of
+// both CTAs.
+template <int BN, int AMODE, int BMODE, int SCHED, int CG>
 __device__ __forceinline__ void load_stage(const TcParams& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
                                            const Tile& t, int kb, uint32_t sa, uint32_t sb, uint32_t full_bar,
-                                           const bf16* const (&gsrc)[8], const uint32_t (&gbytes)[8], int ktok) {
-  constexpr uint32_t tma_bytes = (AMODE == A_TMA_K || AMODE == A_TMA_MN ? Smem<BN>::A_BYTES : 0) +
-                                 (BMODE == B_TMA_K || BMODE == B_TMA_MN ? Smem<BN>::B_BYTES : 0);
+                                           const bf16* const (&gsrc)[8], const uint32_t (&gbytes)[8], int ktok,
+                                           int rank, uint32_t lead_full) {
+  using SM = Smem<BN, SCHED, CG>;
+  constexpr int BNC = BN / CG;   // B columns held by this CTA
+  constexpr uint32_t tma_bytes = (AMODE == A_TMA_K || AMODE == A_TMA_MN ? SM::A_BYTES : 0) +
+                                 (BMODE == B_TMA_K || BMODE == B_TMA_MN ? SM::B_BYTES : 0);
   const int ptid = threadIdx.x;
   if (ptid == 0 && tma_bytes) {
-    if (Modes<AMODE, BMODE>::kCpAsync) mbar_expect_tx(full_bar, tma_bytes);
-    else mbar_arrive_expect_tx(full_bar, tma_bytes);
-    if (AMODE == A_TMA_K) tma_load_2d(sa, tmA, kb * BK, t.row0, full_bar);
+    if (rank == 0) {
+      if (Modes<AMODE, BMODE>::kCpAsync) mbar_expect_tx(full_bar, CG * tma_bytes);
+      else mbar_arrive_expect_tx(full_bar, CG * tma_bytes);
+    }
+    auto load = [&](uint32_t dst, const CUtensorMap* tm, int c0, int c1) {
+      if (CG == 2) tma_load_2d_pair(dst, tm, c0, c1, lead_full);
+      else tma_load_2d(dst, tm, c0, c1, full_bar);
+    };
+    if (AMODE == A_TMA_K) load(sa, tmA, kb * BK, t.row0);
     if (AMODE == A_TMA_MN) {
 #pragma unroll
-      for (int j = 0; j < BM / 64; ++j) tma_load_2d(sa + j * kChunkBytes, tmA, t.m * BM + j * 64, t.row0 + kb * BK, full_bar);
+      for (int j = 0; j < BM / 64; ++j) load(sa + j * kChunkBytes, tmA, t.m * BM + j * 64, t.row0 + kb * BK);
     }
-    if (BMODE == B_TMA_K) tma_load_2d(sb, tmB, kb * BK, t.e * p.b_rows_per_seg + t.n * BN, full_bar);
+    if (BMODE == B_TMA_K) load(sb, tmB, kb * BK, t.e * p.b_rows_per_seg + t.n * BN + rank * BNC);
     if (BMODE == B_TMA_MN) {
       const int krow = (SCHED == SCHED_SEG_K ? t.row0 : t.e * p.b_rows_per_seg) + kb * BK;
 #pragma unroll
-      for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * kChunkBytes, tmB, t.n * BN + j * 64, krow, full_bar);
+      for (int j = 0; j < BNC / 64; ++j) load(sb + j * kChunkBytes, tmB, t.n * BN + rank * BNC + j * 64, krow);
     }
   }
   if (AMODE == A_GATHER_K) {
@@ -222,58 +269,82 @@ __device__ __forceinline__ void load_stage(const TcParams& p, const CUtensorMap*
 }
 
 // ------------------------------------------------------------------ kernel
-template <int BN, int AMODE, int BMODE, int SCHED, int EPI>
+// CG = 2: launched as clusters of two CTAs on two SMs. The pair computes a 256 x BN tile with
+// one tcgen05.mma.cta_group::2 per K step, issued by rank 0: each CTA stages its own 128 A rows
+// and half of the B columns, so each SM moves 2/3 of the shared-memory bytes of a 128 x BN tile
+// per MAC and the ring is deeper. Rank 1's MMA-warp lane relays "stage s of this CTA is full" to
+// rank 0's full barrier; rank 0's commits are multicast to both CTAs' empty / accumulator-full
+// barriers; both epilogues report "accumulator drained" to rank 0.
+template <int BN, int AMODE, int BMODE, int SCHED, int EPI, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2, TcParams p) {
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
+  static_assert(CG == 1 || (CG == 2 && SCHED == SCHED_SEG_M && (AMODE == A_GATHER_K || AMODE == A_TMA_K) &&
+                            (BMODE == B_TMA_K || BMODE == B_TMA_MN) && BN >= 128),
+                "CTA pairs: segment-M schedule, K-major A, B by TMA");
   using MD = Modes<AMODE, BMODE>;
+  using SM = Smem<BN, SCHED, CG>;
+  constexpr int NS = SM::NS;
   constexpr uint32_t TMEM_COLS = 2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512);
-  constexpr uint32_t IDESC = idesc_bf16(BM, BN, MD::kAMn, MD::kBMn);
+  constexpr uint32_t IDESC = idesc_bf16(BM * CG, BN, MD::kAMn, MD::kBMn);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* stage_base = smem;
-  uint8_t* out_stage = smem + STAGES * Smem<BN, SCHED>::STAGE;     // SEG_K epilogue staging (1024-aligned)
-  uint64_t* bars = (uint64_t*)(out_stage + Smem<BN, SCHED>::OUT);
-  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
-  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
-  const uint32_t tfull0 = smem_u32(bars + 2 * STAGES), tempty0 = smem_u32(bars + 2 * STAGES + 2);
-  const uint32_t drain = smem_u32(bars + 2 * STAGES + 4);
-  volatile int* abort_flag = (volatile int*)(bars + 2 * STAGES + 5);
-  uint32_t* tmem_slot = (uint32_t*)(bars + 2 * STAGES + 6);
+  uint8_t* out_stage = smem + NS * SM::STAGE;     // SEG_K epilogue staging (1024-aligned)
+  uint64_t* bars = (uint64_t*)(out_stage + SM::OUT);
+  // bars: full[NS], empty[NS], tfull[2], tempty[2], drain
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + NS);
+  const uint32_t tfull0 = smem_u32(bars + 2 * NS), tempty0 = smem_u32(bars + 2 * NS + 2);
+  const uint32_t drain = smem_u32(bars + 2 * NS + 4);
+  volatile int* abort_flag = (volatile int*)(bars + 2 * NS + 5);
+  uint32_t* tmem_slot = (uint32_t*)(bars + 2 * NS + 6);
+  const int rank = CG == 2 ? (int)cluster_ctarank() : 0;
+  const bool leader = rank == 0;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full0 + 8 * s, MD::kCpAsync ? kProducerWarps * 32 : 1);
+    for (int s = 0; s < NS; ++s) {
+      // rank 0 of a pair with gathered rows also counts the relay of rank 1's gathers
+      mbar_init(full0 + 8 * s, (MD::kCpAsync ? kProducerWarps * 32 : 1) + (CG == 2 && leader && MD::kCpAsync ? 1 : 0));
       mbar_init(empty0 + 8 * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, kEpiWarps * 32);
+      mbar_init(tempty0 + 8 * a, CG == 2 ? 2 * kEpiWarps : kEpiWarps * 32);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == kMmaWarp) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if (CG == 2) {
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                   "r"(TMEM_COLS)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                   "r"(TMEM_COLS)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (CG == 2) cluster_sync();   // the peer's barriers are initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int ntiles = total_tiles<SCHED>(p);
+  const int ntiles = total_tiles<SCHED, CG>(p);
+  const int tile0 = blockIdx.x / CG, tstep = gridDim.x / CG;
+  const uint32_t lead_full0 = CG == 2 ? mapa_shared(full0, 0) : full0;   // rank 0's full barriers
 
   if (warp < kProducerWarps) {
     // ------------------------------------------------------------ producers
     int it = 0;
     bool ok = true;
-    for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
-      const Tile t = map_tile<SCHED>(p, L);
+    for (int L = tile0; L < ntiles && ok; L += tstep) {
+      const Tile t = map_tile<SCHED, CG>(p, L, rank);
       const bf16* gsrc[8];
       uint32_t gbytes[8];
       if (AMODE == A_GATHER_K) {
@@ -306,15 +377,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           tk1 = tk2;
           tk2 = tok_at(kb + 2);
         }
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
+        const int s = it % NS;
+        const uint32_t ph = (it / NS) & 1;
         if (!mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
-        const uint32_t sa = smem_u32(stage_base + s * Smem<BN>::STAGE);
-        const uint32_t sb = sa + Smem<BN>::A_BYTES;
-        load_stage<BN, AMODE, BMODE, SCHED>(p, &tmA, &tmB, t, kb, sa, sb, full0 + 8 * s, gsrc, gbytes, tk0);
+        const uint32_t sa = smem_u32(stage_base + s * SM::STAGE);
+        const uint32_t sb = sa + SM::A_BYTES;
+        load_stage<BN, AMODE, BMODE, SCHED, CG>(p, &tmA, &tmB, t, kb, sa, sb, full0 + 8 * s, gsrc, gbytes, tk0,
+                                                rank, lead_full0 + 8 * s);
         // the stage's full barrier counts this thread's arrival once all of its copies so far have
         // landed; the producer goes straight on to the next stage
         if (MD::kCpAsync) cp_async_mbar_arrive_noinc(full0 + 8 * s);
@@ -323,40 +395,63 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (MD::kCpAsync) cp_async_wait<0>();
   } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
-    if (lane == 0) {
+    if (lane == 0 && CG == 2 && !leader && MD::kCpAsync) {
+      // rank 1: relay each stage's gathered rows, once landed, to rank 0's full barrier
+      int it = 0;
+      bool ok = true;
+      for (int L = tile0; L < ntiles && ok; L += tstep) {
+        const Tile t = map_tile<SCHED, CG>(p, L, rank);
+        for (int kb = 0; kb < t.nkb; ++kb, ++it) {
+          const int s = it % NS;
+          if (!mbar_wait(full0 + 8 * s, (it / NS) & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          if (MD::kCpAsync) fence_proxy_async();   // cp.async (generic proxy) writes seen by the pair's MMA
+          mbar_arrive_cluster(lead_full0 + 8 * s);
+        }
+      }
+    } else if (lane == 0 && leader) {
       int it = 0, tcount = 0;
       bool ok = true;
-      for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x, ++tcount) {
-        const Tile t = map_tile<SCHED>(p, L);
+      for (int L = tile0; L < ntiles && ok; L += tstep, ++tcount) {
+        const Tile t = map_tile<SCHED, CG>(p, L, rank);
         const int acc = tcount & 1;
         const uint32_t aph = (tcount >> 1) & 1;
-        if (!mbar_wait(tempty0 + 8 * acc, aph ^ 1, abort_flag, p.status)) break;
+        if (!(CG == 2 ? mbar_wait_cluster(tempty0 + 8 * acc, aph ^ 1, abort_flag, p.status)
+                      : mbar_wait(tempty0 + 8 * acc, aph ^ 1, abort_flag, p.status)))
+          break;
         tc_fence_after();
         const uint32_t dcol = tmem_base + acc * BN;
         for (int kb = 0; kb < t.nkb; ++kb, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
-          if (!mbar_wait(full0 + 8 * s, ph, abort_flag, p.status)) {
+          const int s = it % NS;
+          const uint32_t ph = (it / NS) & 1;
+          if (!(CG == 2 && MD::kCpAsync ? mbar_wait_cluster(full0 + 8 * s, ph, abort_flag, p.status)
+                                        : mbar_wait(full0 + 8 * s, ph, abort_flag, p.status))) {
             ok = false;
             break;
           }
           tc_fence_after();
           if (MD::kCpAsync) fence_proxy_async();   // cp.async (generic proxy) writes seen by the MMA
-          const uint32_t sa = smem_u32(stage_base + s * Smem<BN>::STAGE);
-          const uint32_t sb = sa + Smem<BN>::A_BYTES;
+          const uint32_t sa = smem_u32(stage_base + s * SM::STAGE);
+          const uint32_t sb = sa + SM::A_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t da = MD::kAMn ? desc_mnmajor(sa + k * 2048) : desc_kmajor(sa + k * 32);
             const uint64_t db = MD::kBMn ? desc_mnmajor(sb + k * 2048) : desc_kmajor(sb + k * 32);
-            mma_bf16(dcol, da, db, IDESC, (kb > 0 || k > 0) ? 1u : 0u);
+            if (CG == 2) mma_bf16_pair(dcol, da, db, IDESC, (kb > 0 || k > 0) ? 1u : 0u);
+            else mma_bf16(dcol, da, db, IDESC, (kb > 0 || k > 0) ? 1u : 0u);
           }
-          mma_commit(empty0 + 8 * s);
+          if (CG == 2) mma_commit_pair_mc(empty0 + 8 * s, 0x3);
+          else mma_commit(empty0 + 8 * s);
         }
         if (!ok) break;
-        mma_commit(tfull0 + 8 * acc);
+        if (CG == 2) mma_commit_pair_mc(tfull0 + 8 * acc, 0x3);
+        else mma_commit(tfull0 + 8 * acc);
       }
       // drain: wait until every issued MMA has completed before TMEM is freed
-      mma_commit(drain);
+      if (CG == 2) mma_commit_pair(drain);
+      else mma_commit(drain);
       const uint64_t t0 = global_ns();
       while (!mbar_try_wait(drain, 0)) {
         if (global_ns() - t0 > kWaitLimitNs) {
@@ -371,11 +466,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ew = warp - kProducerWarps;     // 0..3 == warp % 4: TMEM lanes 32*ew..
     const int r = ew * 32 + lane;             // tile row
     int tcount = 0;
-    for (int L = blockIdx.x; L < ntiles; L += gridDim.x, ++tcount) {
-      const Tile t = map_tile<SCHED>(p, L);
+    for (int L = tile0; L < ntiles; L += tstep, ++tcount) {
+      const Tile t = map_tile<SCHED, CG>(p, L, rank);
       const int acc = tcount & 1;
       const uint32_t aph = (tcount >> 1) & 1;
-      if (!mbar_wait(tfull0 + 8 * acc, aph, abort_flag, p.status)) break;
+      if (!(CG == 2 ? mbar_wait_cluster(tfull0 + 8 * acc, aph, abort_flag, p.status)
+                    : mbar_wait(tfull0 + 8 * acc, aph, abort_flag, p.status)))
+        break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(ew * 32) << 16);
       const int row = t.row0 + r;   // SEG_M / DENSE output row
@@ -545,33 +642,72 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(tempty0 + 8 * acc);
+      if (CG == 2) {
+        // one arrival per epilogue warp of either CTA, on rank 0's barrier
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(tempty0 + 8 * acc);
+          else mbar_arrive_cluster(mapa_shared(tempty0 + 8 * acc, 0));
+        }
+      } else {
+        mbar_arrive(tempty0 + 8 * acc);
+      }
     }
   }
   if (SCHED == SCHED_SEG_K && warp >= kProducerWarps && warp < kMmaWarp && lane == 0) bulk_wait<0>();
   tc_fence_before();
   __syncthreads();
+  if (CG == 2) cluster_sync();   // neither CTA leaves while the pair's MMAs or arrivals may touch it
   if (warp == kMmaWarp) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
-                 : "memory");
+    if (CG == 2)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                   : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                   : "memory");
   }
 }
 
 // -------------------------------------------------------------- host side
-template <int BN, int AMODE, int BMODE, int SCHED, int EPI>
+template <int BN, int AMODE, int BMODE, int SCHED, int EPI, int CG = 1>
 cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcParams& p, int grid, cudaStream_t s,
                    const CUtensorMap* tmC = nullptr, const CUtensorMap* tmC2 = nullptr) {
-  auto kern = tc_gemm_kernel<BN, AMODE, BMODE, SCHED, EPI>;
-  const int smem = Smem<BN, SCHED>::TOTAL;
+  auto kern = tc_gemm_kernel<BN, AMODE, BMODE, SCHED, EPI, CG>;
+  const int smem = Smem<BN, SCHED, CG>::TOTAL;
   static bool attr = false;
+  static int pair_grid = 0;   // CTAs of as many 2-CTA clusters as fit on the GPU at once
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  kern<<<grid, kThreads, smem, s>>>(tmA, tmB, tmC ? *tmC : tmA, tmC2 ? *tmC2 : tmA, p);
-  return cudaGetLastError();
+  if (CG == 1) {
+    kern<<<grid, kThreads, smem, s>>>(tmA, tmB, tmC ? *tmC : tmA, tmC2 ? *tmC2 : tmA, p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (!pair_grid) {
+    cfg.gridDim = dim3(2 * (grid / 2));
+    int clusters = 0;
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    pair_grid = 2 * clusters;
+  }
+  // persistent: never more clusters than run at once (a second wave would serialise the tail)
+  cfg.gridDim = dim3(pair_grid < grid ? pair_grid : 2 * (grid / 2));
+  return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC ? *tmC : tmA, tmC2 ? *tmC2 : tmA, p);
 }
 
 constexpr int kBNup = 256;     // gate/up: 128 gate + 128 up columns
@@ -582,11 +718,17 @@ constexpr int kBNdx = 256;
 constexpr int kBNdw13 = 256;
 constexpr int kBNdwd = 128;
 
+// CTA pairs are opt-in: on GB300 they measured no faster than single CTAs for these GEMMs (a
+// segment with an odd tile count also computes an empty second tile), and the relay of gathered
+// rows to rank 0 costs a cluster-scope release per stage.
+bool use_pairs(const Layer& L, const Bufs&) { return L.pairs == 1; }
+
 TcParams base_params(const Layer& L, const Bufs& B) {
   TcParams p = {};
   p.row_token = B.row_token;
   p.off = B.off;
   p.mt_off = B.mt_off;
+  p.mp_off = B.mt_off + (L.E + L.S + 1);   // the routing scan stores the pair prefix after mt_off
   p.nseg = L.E + L.S;
   p.A_rows = B.A;
   p.status = L.status;
@@ -610,6 +752,8 @@ cudaError_t tc_init(Layer& L) {
   if (!make_tmap(&L.tm_Wd, L.Wd, L.f, nseg * L.d, BK, kBNdown)) return cudaErrorInvalidValue;
   if (!make_tmap(&L.tm_W13_mn, L.W13, L.d, nseg * 2 * L.f, 64, BK)) return cudaErrorInvalidValue;
   if (!make_tmap(&L.tm_Wd_mn, L.Wd, L.f, nseg * L.d, 64, BK)) return cudaErrorInvalidValue;
+  if (!make_tmap(&L.tm_W13_h, L.W13, L.d, nseg * 2 * L.f, BK, kBNup / 2)) return cudaErrorInvalidValue;
+  if (!make_tmap(&L.tm_Wd_h, L.Wd, L.f, nseg * L.d, BK, kBNdown / 2)) return cudaErrorInvalidValue;
   return cudaSuccess;
 }
 
@@ -641,6 +785,9 @@ cudaError_t launch_tc_gateup(const Layer& L, const Bufs& B, const void* x, cudaS
   p.ldo = L.f;
   p.uv = (bf16*)B.uv;
   p.ld_uv = 2 * L.f;
+  if (use_pairs(L, B))
+    return launch<kBNup, A_GATHER_K, B_TMA_K, SCHED_SEG_M, EPI_SWIGLU, 2>(L.tm_W13_h /*unused*/, L.tm_W13_h, p,
+                                                                          L.num_sms, s);
   return launch<kBNup, A_GATHER_K, B_TMA_K, SCHED_SEG_M, EPI_SWIGLU>(L.tm_W13 /*unused*/, L.tm_W13, p, L.num_sms, s);
 }
 
@@ -654,6 +801,7 @@ cudaError_t launch_tc_down(const Layer& L, const Bufs& B, cudaStream_t s) {
   p.out = B.o;
   p.ldo = L.d;
   p.row_gate = B.row_gate;
+  if (use_pairs(L, B)) return launch<kBNdown, A_TMA_K, B_TMA_K, SCHED_SEG_M, EPI_GATE, 2>(th, L.tm_Wd_h, p, L.num_sms, s);
   return launch<kBNdown, A_TMA_K, B_TMA_K, SCHED_SEG_M, EPI_GATE>(th, L.tm_Wd, p, L.num_sms, s);
 }
 
@@ -673,6 +821,9 @@ cudaError_t launch_tc_bwd_dh(const Layer& L, const Bufs& B, const void* dy, cuda
   p.ld_uv = 2 * L.f;
   p.dg_part = B.dg_part;
   p.dg_slots = L.f / 64;
+  if (use_pairs(L, B))
+    return launch<kBNdh, A_GATHER_K, B_TMA_MN, SCHED_SEG_M, EPI_DH, 2>(L.tm_Wd_mn /*unused*/, L.tm_Wd_mn, p,
+                                                                       L.num_sms, s);
   return launch<kBNdh, A_GATHER_K, B_TMA_MN, SCHED_SEG_M, EPI_DH>(L.tm_Wd_mn /*unused*/, L.tm_Wd_mn, p, L.num_sms,
                                                                   s);
 }
@@ -687,6 +838,7 @@ cudaError_t launch_tc_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s) {
   p.b_rows_per_seg = 2 * L.f;
   p.out = B.dx_rows;
   p.ldo = L.d;
+  if (use_pairs(L, B)) return launch<kBNdx, A_TMA_K, B_TMA_MN, SCHED_SEG_M, EPI_STORE, 2>(ta, L.tm_W13_mn, p, L.num_sms, s);
   return launch<kBNdx, A_TMA_K, B_TMA_MN, SCHED_SEG_M, EPI_STORE>(ta, L.tm_W13_mn, p, L.num_sms, s);
 }
 
