@@ -40,6 +40,8 @@ struct Layer {
   CUtensorMap tm_Wd_h;      // K-major rows of Wd, box 64 x 128
   int pairs;                // 1: expert GEMMs on 2-SM CTA pairs; 0 (default): one CTA per tile
   // MXFP8 packed weights: E4M3 codes and E8M0 scales (one per 32 along the named axis)
+  // MXFP8 scales: K-major arrays row-major (rows, K/32); MN-major arrays (Krows/32, W) stored
+  // as [Krows/128][W][4] (the four scales of a column's 128-row K block in one word).
   uint8_t *W13q, *W13s;     // [E+S][2f][d] along d (gate/up interleaved in blocks of kGateMx rows); [..][d/32]
   uint8_t *W13c, *W13cs;    // same rows quantised along the packed 2f rows; scales [(E+S)*2f/32][d]
   uint8_t *Wdq, *Wds;       // [E+S][d][f] along f; [..][f/32]

@@ -39,18 +39,25 @@ constexpr int kMxThreads = (kProd + kEpi + 1) * 32;
 constexpr int kMxMmaWarp = kProd + kEpi;
 constexpr int kStageBytes = MBM * MBK + MBN * MBK;                 // 32 KB
 constexpr int kScaleCol0 = 2 * MBN;                                 // TMEM columns after the two accumulators
-constexpr int kMxSmem = MSTAGES * kStageBytes + 1024 + 256;
 
 enum { MA_GATHER_K = 0, MA_TMA_K = 1, MA_TMA_MN = 2 };
 enum { MB_TMA_K = 0, MB_TMA_MN = 1 };
 enum { MS_SEG_M = 0, MS_SEG_K = 1 };
 enum { ME_SWIGLU_Q = 0, ME_GATE = 1, ME_DH_Q = 2, ME_STORE = 3, ME_DW13 = 4, ME_DWD = 5 };
 
+// Weight-gradient epilogue staging: per epilogue warp two 32-row x 64-column bf16 sub-tiles.
+constexpr int kMxOut = kEpi * 2 * 32 * 128;
+template <int SCHED>
+constexpr int mx_smem() {
+  return MSTAGES * kStageBytes + (SCHED == MS_SEG_K ? kMxOut : 0) + 1024 + 256;
+}
+
 struct MxParams {
   const uint8_t* Ag;      // gathered A codes [*, K] (MA_GATHER_K)
   const uint8_t* As;      // A scales: [rows][K/32] (K-major) or [Krows/32][W] (MN-major)
   int a_w;                // MN-major A: row width W of the code / scale arrays
   int a_rows;             // rows of a K-major TMA A operand (guards scale reads)
+  long a_kb_rows;         // > 0: A's K-major scales are k-block-major with this many rows
   const uint8_t* Bs;      // B scales
   int b_w;                // MN-major B: row width W
   int b_rows_per_seg;     // B rows (K-major) or K rows (MN-major) per segment
@@ -104,6 +111,22 @@ __device__ __forceinline__ uint8_t quant32(const float* v, uint4& lo, uint4& hi)
   return (uint8_t)(X + 127);
 }
 
+// Scale layouts.
+//  K-major operands: row-major [rows][K/32], byte (row, j = k/32) at row * K/32 + j; the four
+//  bytes of one 128-element K block of a row are one aligned 32-bit word.
+//  The du/dv scales (K-major, read by dx) are instead k-block-major [2f/128][R][4], byte (row, j)
+//  at ((j/4) * R + row) * 4 + j%4: one stage's words of 32 consecutive rows are one request
+//  (measured faster for dx; for the weights' K-major scales the row-major layout, whose
+//  sectors are reused by eight consecutive K blocks, measured faster).
+//  MN-major operands: [Krows/128][W][4], byte (krow/32 = j, col) at ((j/4) * W + col) * 4 + j%4:
+//  the four bytes of one K block of a column are one 32-bit word and the words of consecutive
+//  columns are adjacent, so a warp reads one stage's words of 32 columns in one coalesced request
+//  (the row-major [Krows/32][W] layout took four byte loads per column).
+__host__ __device__ __forceinline__ long sc_index_k(long row, long j, long K) { return row * (K / 32) + j; }
+__host__ __device__ __forceinline__ long sc_index_kb(long row, long j, long rows) {
+  return ((j >> 2) * rows + row) * 4 + (j & 3);
+}
+__host__ __device__ __forceinline__ long sc_index_mn(long j, long col, long W) { return ((j >> 2) * W + col) * 4 + (j & 3); }
 enum { SRC_PLAIN = 0, SRC_GATHER = 1, SRC_W13 = 2 };
 
 // Source row of packed W13 row `row` (gate/up interleaved in blocks of G rows).
@@ -134,7 +157,7 @@ __global__ void __launch_bounds__(256) mx_quant_rows_kernel(const bf16* __restri
     const uint8_t sc = quant32(v, lo, hi);
     *reinterpret_cast<uint4*>(q + row * K + b * 32) = lo;
     *reinterpret_cast<uint4*>(q + row * K + b * 32 + 16) = hi;
-    s[row * (K / 32) + b] = sc;
+    s[sc_index_k(row, b, K)] = sc;
   }
 }
 
@@ -190,7 +213,7 @@ __global__ void __launch_bounds__(256) mx_quant_cols_kernel(const bf16* __restri
   rb += out_shift / 32;                    // segment bases are multiples of 128 rows
 #pragma unroll
   for (int i = 0; i < 32; ++i) q[(rb * 32 + i) * W + c] = (uint8_t)(w[i >> 2] >> (8 * (i & 3)));
-  s[rb * W + c] = sc;
+  s[sc_index_mn(rb, c, W)] = sc;
 }
 
 // ---------------------------------------------------------------- GEMM
@@ -256,26 +279,24 @@ __device__ __forceinline__ MTile mx_map(const MxParams& p, int L) {
   return t;
 }
 
-// Four E8M0 bytes (k blocks kb*4 .. kb*4+3) of MMA row `r` of an operand.
-//  K-major: scales [rows][K/32], row-contiguous, one 32-bit word.
-//  MN-major: scales [Krows/32][W], one byte per k block.
 __device__ __forceinline__ uint32_t scale_word_k(const uint8_t* s, long row, int K, int kb) {
   return *reinterpret_cast<const uint32_t*>(s + row * (K / 32) + kb * 4);
 }
 __device__ __forceinline__ uint32_t scale_word_mn(const uint8_t* s, long krow0, int W, int col) {
-  const uint8_t* p = s + (krow0 / 32) * (long)W + col;
-  return (uint32_t)p[0] | ((uint32_t)p[W] << 8) | ((uint32_t)p[2 * (long)W] << 16) | ((uint32_t)p[3 * (long)W] << 24);
+  return *reinterpret_cast<const uint32_t*>(s + ((krow0 >> 7) * (long)W + col) * 4);   // krow0: multiple of 128
 }
 
 template <int AMODE, int BMODE, int SCHED, int EPI>
 __global__ void __launch_bounds__(kMxThreads, 1)
-    mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, MxParams p) {
+    mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2, MxParams p) {
   constexpr int A_MN = AMODE == MA_TMA_MN ? 1 : 0;
   constexpr int B_MN = BMODE == MB_TMA_MN ? 1 : 0;
   constexpr bool kGather = AMODE == MA_GATHER_K;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint64_t* bars = (uint64_t*)(smem + MSTAGES * kStageBytes);
+  uint8_t* out_stage = smem + MSTAGES * kStageBytes;   // SEG_K epilogue staging (1024-aligned)
+  uint64_t* bars = (uint64_t*)(out_stage + (SCHED == MS_SEG_K ? kMxOut : 0));
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + MSTAGES);
   const uint32_t tfull0 = smem_u32(bars + 2 * MSTAGES), tempty0 = smem_u32(bars + 2 * MSTAGES + 2);
   const uint32_t drain = smem_u32(bars + 2 * MSTAGES + 4);
@@ -339,7 +360,50 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           arow[c] = row < p.a_rows ? row : -1;
         }
       }
+      // Block-scale words of K block kb for MMA rows / columns lane + 32c. For the weight
+      // gradients (a few K blocks per tile) they are read two blocks ahead of their stage (a
+      // register ring), so the L2 round trip overlaps the pipeline instead of delaying each
+      // stage's full barrier; the long-K products read them at the stage (measured faster there).
+      constexpr bool kScaleRing = SCHED == MS_SEG_K;
+      auto scale_words = [&](int kb, uint32_t (&wa)[4], uint32_t (&wb)[4]) {
+        const long krowB = (SCHED == MS_SEG_K ? (long)t.row0 : (long)t.e * p.b_rows_per_seg) + (long)kb * MBK;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (kb >= t.nkb) {
+            wa[c] = wb[c] = 0u;
+            continue;
+          }
+          if (AMODE == MA_TMA_MN) {
+            wa[c] = scale_word_mn(p.As, (long)t.row0 + (long)kb * MBK, p.a_w, t.m * MBM + lane + 32 * c);
+          } else {
+            wa[c] = arow[c] < 0 ? 0u
+                    : p.a_kb_rows ? *reinterpret_cast<const uint32_t*>(p.As + ((long)kb * p.a_kb_rows + arow[c]) * 4)
+                                  : scale_word_k(p.As, arow[c], p.K, kb);
+          }
+          if (BMODE == MB_TMA_MN) {
+            wb[c] = scale_word_mn(p.Bs, krowB, p.b_w, t.n * MBN + lane + 32 * c);
+          } else {
+            wb[c] = scale_word_k(p.Bs, (long)t.e * p.b_rows_per_seg + t.n * MBN + lane + 32 * c, p.K, kb);
+          }
+        }
+      };
+      uint32_t wa1[4], wb1[4], wa2[4], wb2[4];
+      if (kScaleRing) {
+        scale_words(0, wa1, wb1);
+        scale_words(1, wa2, wb2);
+      }
       for (int kb = 0; kb < t.nkb; ++kb, ++it) {
+        uint32_t wa[4], wb[4];
+        if (kScaleRing) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            wa[c] = wa1[c];
+            wb[c] = wb1[c];
+            wa1[c] = wa2[c];
+            wb1[c] = wb2[c];
+          }
+          scale_words(kb + 2, wa2, wb2);
+        }
         const int s = it % MSTAGES;
         const uint32_t ph = (it / MSTAGES) & 1;
         if (!mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, p.status)) {
@@ -366,20 +430,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           }
         }
         // block scales of this stage into TMEM (replicated layout, see the file header)
-        uint32_t wa[4], wb[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (AMODE == MA_TMA_MN) {
-            wa[c] = scale_word_mn(p.As, (long)t.row0 + (long)kb * MBK, p.a_w, t.m * MBM + lane + 32 * c);
-          } else {
-            wa[c] = arow[c] >= 0 ? scale_word_k(p.As, arow[c], p.K, kb) : 0u;
-          }
-          if (BMODE == MB_TMA_MN) {
-            wb[c] = scale_word_mn(p.Bs, krowB, p.b_w, t.n * MBN + lane + 32 * c);
-          } else {
-            wb[c] = scale_word_k(p.Bs, (long)t.e * p.b_rows_per_seg + t.n * MBN + lane + 32 * c, p.K, kb);
-          }
-        }
+        if (!kScaleRing) scale_words(kb, wa, wb);
         const uint32_t scol = tmem_base + kScaleCol0 + s * 8;
         tmem_st4(scol + lanebits, wa[0], wa[1], wa[2], wa[3]);
         tmem_st4(scol + 4 + lanebits, wb[0], wb[1], wb[2], wb[3]);
@@ -471,7 +522,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             const uint8_t sc = quant32(hf, lo, hi);
             *reinterpret_cast<uint4*>(p.oq + (size_t)row * p.f + col) = lo;
             *reinterpret_cast<uint4*>(p.oq + (size_t)row * p.f + col + 16) = hi;
-            p.os[(size_t)row * (p.f / 32) + col / 32] = sc;
+            p.os[sc_index_k(row, col / 32, p.f)] = sc;
             if (p.uv) {
               bf16* uvrow = p.uv + (size_t)row * p.ld_uv + t.n * 128;
 #pragma unroll
@@ -542,11 +593,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             uint8_t* qrow = p.oq + (size_t)row * p.ld_uv;
             *reinterpret_cast<uint4*>(qrow + ucol) = lo;
             *reinterpret_cast<uint4*>(qrow + ucol + 16) = hi;
-            p.os[(size_t)row * (p.ld_uv / 32) + ucol / 32] = sc;
+            p.os[sc_index_kb(row, ucol / 32, p.a_rows)] = sc;
             sc = quant32(dv, lo, hi);
             *reinterpret_cast<uint4*>(qrow + ucol + 64) = lo;
             *reinterpret_cast<uint4*>(qrow + ucol + 80) = hi;
-            p.os[(size_t)row * (p.ld_uv / 32) + (ucol + 64) / 32] = sc;
+            p.os[sc_index_kb(row, (ucol + 64) / 32, p.a_rows)] = sc;
             if ((c0 & 63) == 32) {
               if (row < p.A_rows) p.dg_part[(size_t)row * p.dg_slots + (t.n * 128 + c0 - 32) / 64] = dgp;
               dgp = 0.f;
@@ -554,47 +605,73 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           }
         }
       } else {
-        // weight gradients (SEG_K): tile rows are packed dW13 rows (gate/up blocks of 64) or dWd rows
+        // Weight gradients (SEG_K). Tile rows are packed dW13 rows (blocks of 64 gate then 64 up
+        // features: warps 0-1 write dWg rows, warps 2-3 dWu rows) or dWd rows. Each warp writes its
+        // 32 rows as 32 x 64 sub-tiles through a double-buffered 128-byte-swizzled staging buffer,
+        // stored by TMA (whole lines, no partial-sector writes).
         const bool empty = t.nkb == 0;
-        bf16* orow;
+        const CUtensorMap* tmo = &tmC;
+        int orow0;
         if (EPI == ME_DW13) {
-          const int pr = t.m * MBM + r;
-          const int blk = pr >> 7, w = pr & 127;
-          const int feat = blk * 64 + (w & 63);
-          orow = (w < 64 ? (bf16*)p.out : (bf16*)p.out2) + ((size_t)t.e * p.f + feat) * p.ldo + t.n * MBN;
+          if (ew >= 2) tmo = &tmC2;
+          orow0 = t.e * p.f + t.m * 64 + (ew & 1) * 32;
         } else {
-          orow = (bf16*)p.out + ((size_t)t.e * p.m_tiles * MBM + t.m * MBM + r) * p.ldo + t.n * MBN;
+          orow0 = (t.e * p.m_tiles + t.m) * MBM + ew * 32;
         }
+        const uint32_t wbuf = smem_u32(out_stage) + ew * 2 * 4096;
 #pragma unroll 1
-        for (int c0 = 0; c0 < MBN; c0 += 32) {
-          float of[32];
+        for (int c0 = 0; c0 < MBN; c0 += 64) {
+          const uint32_t buf = wbuf + ((c0 >> 6) & 1) * 4096;
+          float of[64];
           if (!empty) {
-            uint32_t a[32];
+            uint32_t a[32], b[32];
             tmem_ld32(tbase + c0, a);
+            tmem_ld32(tbase + c0 + 32, b);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) of[i] = __uint_as_float(a[i]);
+            for (int i = 0; i < 32; ++i) {
+              of[i] = __uint_as_float(a[i]);
+              of[32 + i] = __uint_as_float(b[i]);
+            }
           } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) of[i] = 0.f;
+            for (int i = 0; i < 64; ++i) of[i] = 0.f;
           }
           if (p.accumulate) {
+            const bf16* base = (EPI == ME_DW13 && ew >= 2) ? (const bf16*)p.out2 : (const bf16*)p.out;
+            const bf16* old = base + (size_t)(orow0 + lane) * p.ldo + t.n * MBN + c0;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 8; ++q) {
               float o8[8];
-              unpack8(*reinterpret_cast<const uint4*>(orow + c0 + q * 8), o8);
+              unpack8(*reinterpret_cast<const uint4*>(old + q * 8), o8);
 #pragma unroll
               for (int i = 0; i < 8; ++i) of[q * 8 + i] += o8[i];
             }
           }
+          // the store that last read this buffer (two sub-tiles ago) must have finished reading it
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
 #pragma unroll
-          for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(orow + c0 + q * 8) = pack8(of + q * 8);
+          for (int q = 0; q < 8; ++q) {
+            const uint4 v = pack8(of + q * 8);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf + lane * 128 + ((q ^ (lane & 7)) << 4)),
+                         "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                         : "memory");
+          }
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(tmo, t.n * MBN + c0, orow0, buf);
+            bulk_commit();
+          }
         }
       }
       tc_fence_before();
       mbar_arrive(tempty0 + 8 * acc);
     }
   }
+  // the weight-gradient stores must have read their staging before the CTA exits
+  if (SCHED == MS_SEG_K && warp >= kProd && warp < kMxMmaWarp && lane == 0) bulk_wait<0>();
   tc_fence_before();
   __syncthreads();
   if (warp == kMxMmaWarp) {
@@ -604,15 +681,17 @@ __global__ void __launch_bounds__(kMxThreads, 1)
 }
 
 template <int AMODE, int BMODE, int SCHED, int EPI>
-cudaError_t mx_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const MxParams& p, int grid, cudaStream_t s) {
+cudaError_t mx_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const MxParams& p, int grid, cudaStream_t s,
+                      const CUtensorMap* tmC = nullptr, const CUtensorMap* tmC2 = nullptr) {
   auto kern = mx_gemm_kernel<AMODE, BMODE, SCHED, EPI>;
+  constexpr int smem = mx_smem<SCHED>();
   static bool attr = false;
   if (!attr) {
-    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmem);
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  kern<<<grid, kMxThreads, kMxSmem, s>>>(tmA, tmB, p);
+  kern<<<grid, kMxThreads, smem, s>>>(tmA, tmB, tmC ? *tmC : tmA, tmC2 ? *tmC2 : tmA, p);
   return cudaGetLastError();
 }
 
@@ -777,6 +856,7 @@ cudaError_t launch_mx_bwd_dh(const Layer& L, const Bufs& B, cudaStream_t s) {
   p.out2 = B.hg;
   p.oq = B.dudvq;
   p.os = B.dudvs;
+  p.a_rows = B.R;   // rows of the du/dv scale array written k-block-major (A is gathered: no guard)
   p.row_gate = B.row_gate;
   p.uv = (bf16*)B.uv;
   p.ld_uv = 2 * L.f;
@@ -791,6 +871,7 @@ cudaError_t launch_mx_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s) {
   MxParams p = mx_base(L, B);
   p.As = B.dudvs;
   p.a_rows = B.R;
+  p.a_kb_rows = B.R;
   p.Bs = L.W13cs;
   p.b_w = L.d;
   p.K = 2 * L.f;
@@ -816,7 +897,11 @@ cudaError_t launch_mx_bwd_dw13(const Layer& L, const Bufs& B, void* dWg, void* d
   p.out2 = dWu;
   p.ldo = L.d;
   p.accumulate = acc ? 1 : 0;
-  return mx_launch<MA_TMA_MN, MB_TMA_MN, MS_SEG_K, ME_DW13>(ta, tb, p, L.num_sms, s);
+  const uint64_t nseg = L.E + L.S;
+  CUtensorMap tg, tu;
+  if (!make_tmap(&tg, dWg, L.d, nseg * L.f, 64, 32) || !make_tmap(&tu, dWu, L.d, nseg * L.f, 64, 32))
+    return cudaErrorInvalidValue;
+  return mx_launch<MA_TMA_MN, MB_TMA_MN, MS_SEG_K, ME_DW13>(ta, tb, p, L.num_sms, s, &tg, &tu);
 }
 
 cudaError_t launch_mx_bwd_dwd(const Layer& L, const Bufs& B, void* dWd, bool acc, cudaStream_t s) {
@@ -833,7 +918,9 @@ cudaError_t launch_mx_bwd_dwd(const Layer& L, const Bufs& B, void* dWd, bool acc
   p.out = dWd;
   p.ldo = L.f;
   p.accumulate = acc ? 1 : 0;
-  return mx_launch<MA_TMA_MN, MB_TMA_MN, MS_SEG_K, ME_DWD>(ta, tb, p, L.num_sms, s);
+  CUtensorMap td;
+  if (!make_tmap(&td, dWd, L.f, (uint64_t)(L.E + L.S) * L.d, 64, 32)) return cudaErrorInvalidValue;
+  return mx_launch<MA_TMA_MN, MB_TMA_MN, MS_SEG_K, ME_DWD>(ta, tb, p, L.num_sms, s, &td);
 }
 
 }  // namespace moe

@@ -52,6 +52,11 @@ def packed_w13(Wg, Wu, G):
     return out
 
 
+def scales_mn(raw, Krows, W):
+    """Scale bytes of an MN-major operand, stored [Krows/128][W][4], as [Krows/32][W]."""
+    return raw.reshape(Krows // 128, W, 4).transpose(0, 2, 1).reshape(Krows // 32, W)
+
+
 def test_mx_weight_quantisation_byte_exact():
     spec = SMALL_MX
     layer, g, n = setup(spec)
@@ -74,10 +79,10 @@ def test_mx_weight_quantisation_byte_exact():
     assert np.array_equal(parts["Wds"].reshape(s.shape), s)
     c, s = oracle.mx_quantize(W13, axis=1)                 # along the packed 2f rows
     assert np.array_equal(parts["W13c"].reshape(c.shape), c)
-    assert np.array_equal(parts["W13cs"].reshape(s.shape), s)
+    assert np.array_equal(scales_mn(parts["W13cs"], nseg * 2 * f, d).reshape(s.shape), s)
     c, s = oracle.mx_quantize(n["Wd"], axis=1)             # along d
     assert np.array_equal(parts["Wdc"].reshape(c.shape), c)
-    assert np.array_equal(parts["Wdcs"].reshape(s.shape), s)
+    assert np.array_equal(scales_mn(parts["Wdcs"], nseg * d, f).reshape(s.shape), s)
     layer.close()
 
 
