@@ -41,7 +41,7 @@ Sizes sizes_for(const Layer& L, int T) {
   const size_t eb = elem_bytes(L.prec);
   const size_t nch = (A + kChunk - 1) / kChunk;
   Sizes z;
-  z.route = al(4 * T * (size_t)L.E) + 2 * al(4 * A) + 2 * al(4 * (nseg + 1)) + al(8 * (nseg + 1)) + 2 * al(4 * A) +
+  z.route = al(4 * T * (size_t)L.E) + 2 * al(4 * A) + 2 * al(4 * (nseg + 1)) + al(16 * (nseg + 1)) + 2 * al(4 * A) +
             2 * al(4 * R);
   z.uv = al(eb * R * 2 * L.f);
   z.fwd_scratch = 2 * al(4 * nch * L.E) + al(eb * R * L.f) + al(eb * R * L.d);
@@ -73,7 +73,7 @@ char* carve_route(Bufs& B, const Layer& L, char* p) {
   B.gate = (float*)p; p += al(4 * (size_t)B.A);
   B.cnt = (int*)p; p += al(4 * (nseg + 1));
   B.off = (int*)p; p += al(4 * (nseg + 1));
-  B.mt_off = (int*)p; p += al(8 * (nseg + 1));   // mt_off, then the pair prefix
+  B.mt_off = (int*)p; p += al(16 * (nseg + 1));   // mt_off, then the pair / dense / sparse prefixes
   B.perm = (int*)p; p += al(4 * (size_t)B.A);
   B.inv = (int*)p; p += al(4 * (size_t)B.A);
   B.row_token = (int*)p; p += al(4 * (size_t)B.R);

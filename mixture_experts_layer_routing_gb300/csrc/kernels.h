@@ -13,6 +13,7 @@ constexpr int kMaxE = 256;        // routed experts supported by the routing ker
 constexpr int kMaxK = 8;          // experts per token
 constexpr int kChunk = 1024;      // assignments per block of the histogram / permutation kernels
 constexpr int kBM = 128;          // rows per M-tile of the grouped GEMMs (segment padding unit)
+constexpr int kDenseTiles = 8;    // segments with this many M-tiles or more are scheduled as "dense"
 constexpr int kGate = 128;        // gate/up interleave block of the packed bf16 W13 (rows)
 constexpr int kGateMx = 64;       // gate/up interleave block of the MXFP8 W13 (rows)
 constexpr int kMaxDecodeB = 64;
@@ -59,7 +60,8 @@ struct Bufs {
   float* gate;           // [T, k]
   int* cnt;              // [E+S]
   int* off;              // [E+S+1]
-  int* mt_off;           // [E+S+1] prefix of ceil(cnt / kBM)
+  int* mt_off;           // [E+S+1] prefix of ceil(cnt / kBM), then [E+S+1] each: prefixes of
+                         // pairs of tiles, of the tiles of dense segments and of the others
   int* perm;             // [A]
   int* inv;              // [A]
   int* row_token;        // [R]

@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(512) scan_kernel(const int* __restrict__ chunk
                                                    int* __restrict__ chunk_base, int* __restrict__ cnt,
                                                    int* __restrict__ off, int* __restrict__ mt_off) {
   __shared__ int c_s[kMaxE + 1];
-  __shared__ int warp_tot[16][3];
+  __shared__ int warp_tot[16][5];
   const int tid = threadIdx.x;
   const int nseg = E + S;
   int c = 0;
@@ -104,46 +104,52 @@ __global__ void __launch_bounds__(512) scan_kernel(const int* __restrict__ chunk
   } else if (tid == E && S) {
     c = T;
   }
-  // exclusive scans of c, of ceil(c / kBM) and of ceil(tiles / 2) over the 512 threads
+  // exclusive scans over the 512 threads of: c, ceil(c / kBM) (tiles), ceil(tiles / 2) (pairs),
+  // and the tiles of "dense" segments (>= kDenseTiles tiles) and of the others
   const int lane = tid & 31, w = tid >> 5;
   const int tiles = (c + kBM - 1) / kBM, pairs = (tiles + 1) / 2;
-  int ic = c, it = tiles, ip = pairs;
+  const int dense = tiles >= kDenseTiles ? tiles : 0, sparse = tiles - dense;
+  int v[5] = {c, tiles, pairs, dense, sparse};
+  const int own[5] = {c, tiles, pairs, dense, sparse};
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int nc = __shfl_up_sync(0xffffffffu, ic, o);
-    const int nt = __shfl_up_sync(0xffffffffu, it, o);
-    const int np = __shfl_up_sync(0xffffffffu, ip, o);
-    if (lane >= o) {
-      ic += nc;
-      it += nt;
-      ip += np;
+#pragma unroll
+    for (int q = 0; q < 5; ++q) {
+      const int n = __shfl_up_sync(0xffffffffu, v[q], o);
+      if (lane >= o) v[q] += n;
     }
   }
   if (lane == 31) {
-    warp_tot[w][0] = ic;
-    warp_tot[w][1] = it;
-    warp_tot[w][2] = ip;
+#pragma unroll
+    for (int q = 0; q < 5; ++q) warp_tot[w][q] = v[q];
   }
   __syncthreads();
-  int bc = 0, bt = 0, bp = 0;
-  for (int q = 0; q < w; ++q) {
-    bc += warp_tot[q][0];
-    bt += warp_tot[q][1];
-    bp += warp_tot[q][2];
+  int ex[5];
+#pragma unroll
+  for (int q = 0; q < 5; ++q) {
+    int b = 0;
+    for (int u = 0; u < w; ++u) b += warp_tot[u][q];
+    ex[q] = b + v[q] - own[q];
   }
-  const int ex_c = bc + ic - c, ex_t = bt + it - tiles, ex_p = bp + ip - pairs;
-  int* mp_off = mt_off + nseg + 1;   // prefix of pairs of 128-row tiles, stored after mt_off
+  // after mt_off: the pair prefix, then the dense-tile and sparse-tile prefixes
+  int* mp_off = mt_off + (nseg + 1);
+  int* dn_off = mt_off + 2 * (nseg + 1);
+  int* sp_off = mt_off + 3 * (nseg + 1);
   if (tid < nseg) {
     cnt[tid] = c;
-    off[tid] = ex_c;
-    mt_off[tid] = ex_t;
-    mp_off[tid] = ex_p;
-    c_s[tid] = ex_c;
+    off[tid] = ex[0];
+    mt_off[tid] = ex[1];
+    mp_off[tid] = ex[2];
+    dn_off[tid] = ex[3];
+    sp_off[tid] = ex[4];
+    c_s[tid] = ex[0];
   }
   if (tid == nseg - 1) {
-    off[nseg] = ex_c + c;
-    mt_off[nseg] = ex_t + tiles;
-    mp_off[nseg] = ex_p + pairs;
+    off[nseg] = ex[0] + c;
+    mt_off[nseg] = ex[1] + tiles;
+    mp_off[nseg] = ex[2] + pairs;
+    dn_off[nseg] = ex[3] + dense;
+    sp_off[nseg] = ex[4] + sparse;
   }
   __syncthreads();
   if (tid < E) {

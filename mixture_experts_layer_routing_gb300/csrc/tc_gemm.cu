@@ -141,13 +141,27 @@ __device__ __forceinline__ Tile map_tile(const TcParams& p, int L, int rank) {
     t.nkb = (t.row_end - t.row0 + BK - 1) / BK;
     return t;
   }
+  // Segments with kDenseTiles or more m-tiles ("dense": each weight tile serves many row tiles,
+  // tensor-bound) and the others (each weight tile streamed for a few rows, HBM-bound) form two
+  // tile streams, interleaved in proportion: tile L is dense iff floor((L+1) Nd / N) steps, so
+  // CTAs running at the same time mix both kinds and keep the tensor pipe and HBM busy together.
+  // A dense stream under a quarter of the tiles (uniform routing: only the shared expert) stays in
+  // segment order at the end: spread thin, its weight and row tiles would leave L2 between uses.
+  const int* dn = p.mt_off + 2 * (p.nseg + 1);
+  const int* sp = p.mt_off + 3 * (p.nseg + 1);
+  const long N = (long)p.mt_off[p.nseg] * p.n_tiles, Nd = (long)dn[p.nseg] * p.n_tiles;
+  const bool mix = 4 * Nd >= N;
+  const long cd = mix ? (long)L * Nd / N : 0;
+  const bool is_dense = mix && (long)(L + 1) * Nd / N > cd;
+  const int* pre = !mix ? p.mt_off : (is_dense ? dn : sp);
+  const int Lc = (int)(is_dense ? cd : L - cd);   // index within the stream
   int lo = 0, hi = p.nseg;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (p.mt_off[mid] * p.n_tiles <= L) lo = mid; else hi = mid;
+    if (pre[mid] * p.n_tiles <= Lc) lo = mid; else hi = mid;
   }
-  const int Me = p.mt_off[lo + 1] - p.mt_off[lo];
-  const int local = L - p.mt_off[lo] * p.n_tiles;
+  const int Me = pre[lo + 1] - pre[lo];
+  const int local = Lc - pre[lo] * p.n_tiles;
   // m-tiles in groups of kRasterM, every n-tile of a group before the next group: CTAs running
   // together share the group's token rows and the expert's weight tiles in L2
   const int g = local / (kRasterM * p.n_tiles);
