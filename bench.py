@@ -453,27 +453,70 @@ def run_extra(args, dev, pk):
             "groups_ms": {g: v[1] / steps for g, v in prof.items()}}
         # decode on the same weights
         if spec is moe_synth.DSV3_UNIFORM:
-            for B in (1, 4, 16):
-                xb = moe_synth.make_tokens(spec.with_(T=B), 1, dev)[0]
-                yb = torch.empty_like(xb)
-                wsb = layer.buffer("fwd", layer.sizes(B)["fwd_ws"])
-                fnb = lambda: moe_decode(layer.h, xb, B, yb, wsb)  # noqa: E731
-                msb = time_steps(fnb, 50, 5, 1)
-                profb = profile_groups(layer.h, fnb, 20)
-                rb = layer.route(xb)
-                cb = rb["cnt"].cpu().numpy()
-                nact = int(np.count_nonzero(cb)) + spec.S
-                nbytes = nact * 3 * spec.f * spec.d * 2 + spec.E * spec.d * 2
-                t_roof = nbytes / (pk["hbm_gbs"] * 1e9)
-                extra[f"dsv3_bf16_decode_B{B}"] = {
-                    "tokens_per_s": B / (msb * 1e-3), "ms": msb, "weight_gbs": nbytes / (msb * 1e-3) / 1e9,
-                    "roofline_ms": t_roof * 1e3, "frac_of_roofline": t_roof * 1e3 / msb, "experts_read": nact,
-                    "groups_ms": {g: v[1] / 20 for g, v in profb.items()}}
+            extra.update(decode_lines(layer, spec, dev, pk, "dsv3_bf16", 3 * spec.f * spec.d * 2))
+            extra["dsv3_bf16_decode_vs_grouped_gemm"] = decode_crossover(layer, spec, dev)
         layer.close()
         del layer, inp
         torch.cuda.empty_cache()
     extra.update(run_extra_mxfp8(dev, pk))
     return extra
+
+
+def decode_lines(layer, spec, dev, pk, tag, expert_bytes, n_batches=16):
+    """Decode B=1/4/16 over n_batches independent token batches taken in turn (consecutive steps route
+    to different experts, so the weights come from HBM); bytes = the router weight plus, per batch,
+    expert_bytes for each distinct expert it uses (routed ones plus the shared expert)."""
+    from mixture_experts_layer_routing_gb300 import moe_decode
+    out = {}
+    for B in (1, 4, 16):
+        xs = [t.contiguous() for t in moe_synth.make_tokens(spec.with_(T=B), n_batches, dev)]
+        yb = torch.empty_like(xs[0])
+        wsb = layer.buffer("fwd", layer.sizes(B)["fwd_ws"])
+        it = [0]
+
+        def fnb():
+            moe_decode(layer.h, xs[it[0] % n_batches], B, yb, wsb)
+            it[0] += 1
+
+        msb = time_steps(fnb, 64, 8, 1)
+        profb = profile_groups(layer.h, fnb, 32)
+        nact = [int(np.count_nonzero(layer.route(x)["cnt"].cpu().numpy())) + spec.S for x in xs]
+        nbytes = float(np.mean(nact)) * expert_bytes + spec.E * spec.d * 2
+        t_roof = nbytes / (pk["hbm_gbs"] * 1e9)
+        out[f"{tag}_decode_B{B}"] = {
+            "tokens_per_s": B / (msb * 1e-3), "ms": msb, "weight_gbs": nbytes / (msb * 1e-3) / 1e9,
+            "roofline_ms": t_roof * 1e3, "frac_of_roofline": t_roof * 1e3 / msb,
+            "experts_read_mean": float(np.mean(nact)), "batches": n_batches,
+            "groups_ms": {g: v[1] / 32 for g, v in profb.items()}}
+    return out
+
+
+def decode_crossover(layer, spec, dev, n_batches=8):
+    """Milliseconds per step of the warp-per-output decode kernels and of the grouped-GEMM forward on
+    the same B tokens (independent batches in turn), and the smallest B where the GEMM path wins."""
+    from mixture_experts_layer_routing_gb300 import moe_decode, moe_forward
+    rows = {}
+    cross = None
+    for B in (1, 2, 4, 8, 16, 32, 64):
+        xs = [t.contiguous() for t in moe_synth.make_tokens(spec.with_(T=B), n_batches, dev, seed_offset=11)]
+        yb = torch.empty_like(xs[0])
+        ws = layer.buffer("fwd", layer.sizes(B)["fwd_ws"])
+        it = [0]
+
+        def dec():
+            moe_decode(layer.h, xs[it[0] % n_batches], B, yb, ws)
+            it[0] += 1
+
+        def gemm():
+            moe_forward(layer.h, xs[it[0] % n_batches], B, yb, None, ws)
+            it[0] += 1
+
+        md = time_steps(dec, 24, 4, 1)
+        mg = time_steps(gemm, 24, 4, 1)
+        rows[str(B)] = {"decode_ms": md, "grouped_gemm_ms": mg}
+        if cross is None and mg < md:
+            cross = B
+    return {"ms": rows, "gemm_faster_from_B": cross}
 
 
 def run_extra_mxfp8(dev, pk):
@@ -511,6 +554,8 @@ def run_extra_mxfp8(dev, pk):
         "frac_of_roofline": t_roof * 1e3 / ms, "chunks": z["n_chunks"], "ring_slots": ring_bytes // z["slot"],
         "recomputed_chunks": rec[-1] if rec else None, "peak_mxfp8_tflops": mx_peak,
         "groups_ms": {k: v[1] / 2 for k, v in prof.items()}}}
+    # decode on the E4M3 weights: per expert W13 and Wd codes plus one scale byte per 32
+    out.update(decode_lines(layer, spec, dev, pk, "dsv3_mxfp8", 3 * f * d * (1 + 1 / 32)))
     layer.close()
     del layer, inp, g, y
     torch.cuda.empty_cache()

@@ -158,7 +158,10 @@ moe_status moe_train_chunked(moe_handle h, const void* x, const void* dy, int T,
                              int* recomputed, void* stream);
 
 /* Small-batch decode: y [B, d] bf16 = layer(x [B, d] bf16), 1 <= B <= 64,
- * cfg.prec == MOE_BF16. Warp-per-output kernels with fp32 intermediates. */
+ * cfg.prec MOE_BF16 or MOE_MXFP8 (MOE_FP32: MOE_ERR_UNSUPPORTED). Warp-per-output
+ * kernels with fp32 intermediates ("Cursor a réécrit le décodage de MoE",
+ * toolnavs.com). An MXFP8 layer decodes on its E4M3 weights and computes its
+ * MXFP8 forward on the B tokens: x quantised along d, h along f. */
 moe_status moe_decode(moe_handle h, const void* x, int B, void* y, void* workspace, void* stream);
 
 /* Tensor-core scheduling of the bf16 expert GEMMs (gate/up, down, dY.Wd, dx).

@@ -47,10 +47,6 @@ Sizes sizes_for(const Layer& L, int T) {
   z.fwd_scratch = 2 * al(4 * nch * L.E) + al(eb * R * L.f) + al(eb * R * L.d);
   z.ctx = z.route + z.uv;
   z.fwd_ws = z.route + z.fwd_scratch;
-  if (L.prec == MOE_BF16) {
-    const size_t dec = decode_workspace_bytes(L, T < kMaxDecodeB ? T : kMaxDecodeB);
-    if (dec > z.fwd_ws) z.fwd_ws = dec;
-  }
   z.bwd_ws = al(eb * R * 2 * L.f) + al(eb * R * L.f) + al(4 * A * (L.f / 64)) + al(eb * R * L.d) +
              al(4 * T * (size_t)L.E) + al(4 * A);
   z.packed = al(eb * nseg * 2 * L.f * L.d) + al(eb * nseg * L.d * L.f) + al(eb * L.E * L.d) + al(4 * L.E);
@@ -61,6 +57,10 @@ Sizes sizes_for(const Layer& L, int T) {
     z.bwd_ws += al(T * d) + al(T * d / 32) + al(R * 2 * f) + al(R * 2 * f / 32) + al(Rp * 2 * f) +
                 al(Rp * 2 * f / 32) + 2 * (al(Rp * d) + al(Rp * d / 32)) + al(Rp * f) + al(Rp * f / 32);
     z.packed = mx_packed_bytes(L) + al(2 * L.E * d) + al(4 * L.E);
+  }
+  if (L.prec != MOE_FP32) {   // decode uses the forward workspace
+    const size_t dec = decode_workspace_bytes(L, T < kMaxDecodeB ? T : kMaxDecodeB);
+    if (dec > z.fwd_ws) z.fwd_ws = dec;
   }
   return z;
 }
@@ -583,13 +583,20 @@ moe_status moe_train_chunked(moe_handle h, const void* x, const void* dy, int T,
 moe_status moe_decode(moe_handle h, const void* x, int B, void* y, void* workspace, void* stream) {
   if (!h || !x || !y || !workspace) return MOE_ERR_INVALID_ARG;
   if (B < 1 || B > kMaxDecodeB || B > h->cfg.T_max) return MOE_ERR_INVALID_ARG;
-  if (h->L.prec != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (h->L.prec == MOE_FP32) return MOE_ERR_UNSUPPORTED;
   if (!h->L.has_weights) return MOE_ERR_NO_WEIGHTS;
   if (!aligned256(workspace)) return MOE_ERR_WORKSPACE;
   if (!aligned16(x) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   const Layer& L = h->L;
   CK(run(h, s, G_DECODE_ROUTE, 1, [&] { return launch_decode_route(L, x, B, workspace, s); }));
+  if (L.prec == MOE_MXFP8) {
+    CK(run(h, s, G_MX_QUANT, 1, [&] { return launch_decode_quant_x_mx(L, x, B, workspace, s); }));
+    CK(run(h, s, G_DECODE_GATEUP, 1, [&] { return launch_decode_gateup_mx(L, B, workspace, s); }));
+    CK(run(h, s, G_MX_QUANT, 1, [&] { return launch_decode_quant_h_mx(L, B, workspace, s); }));
+    CK(run(h, s, G_DECODE_DOWN, 1, [&] { return launch_decode_down_mx(L, B, y, workspace, s); }));
+    return MOE_OK;
+  }
   CK(run(h, s, G_DECODE_GATEUP, 1, [&] { return launch_decode_gateup(L, x, B, workspace, s); }));
   CK(run(h, s, G_DECODE_DOWN, 1, [&] { return launch_decode_down(L, B, y, workspace, s); }));
   return MOE_OK;

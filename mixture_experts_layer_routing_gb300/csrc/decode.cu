@@ -17,8 +17,16 @@
 //             streams Wd[e][c,:] once and adds gate * (h . w) to each token's
 //             fp32 accumulator; y[:, c] is written once. No atomics.
 // Intermediates stay fp32 (h is never rounded to bf16).
+//
+// MXFP8 layers decode the same way on their E4M3 weights (one E8M0 scale per
+// 32 values along each product's K): x is quantised along d and h along f
+// before the down projection, as the MXFP8 layer forward does, so decode is
+// that forward on B tokens. The weight bytes per expert halve.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "mx_quant.cuh"
 #include "topk.cuh"
 
 namespace moe {
@@ -35,6 +43,10 @@ struct DecodeWs {
   int* a_tok;      // [B*k + B] (t << 8) | slot
   float* a_gate;   // [B*k + B]
   float* h;        // [B, k+1, f]
+  // MXFP8 layers only. E4M3 x E8M0 values are exact in bf16 (4 significant bits, exponents within
+  // bf16's range), so the quantised activations are held as bf16.
+  bf16* xd;        // [B, d]      x quantised along d
+  bf16* hd;        // [B, k+1, f] h quantised along f
 };
 
 inline size_t al(size_t v) { return (v + 255) & ~size_t(255); }
@@ -52,6 +64,11 @@ DecodeWs carve(const Layer& L, int B, void* ws) {
   w.a_tok = (int*)p; p += al(sizeof(int) * na);
   w.a_gate = (float*)p; p += al(sizeof(float) * na);
   w.h = (float*)p; p += al(sizeof(float) * B * (L.k + 1) * L.f);
+  w.xd = w.hd = nullptr;
+  if (L.prec == MOE_MXFP8) {
+    w.xd = (bf16*)p; p += al(sizeof(bf16) * B * L.d);
+    w.hd = (bf16*)p; p += al(sizeof(bf16) * B * (L.k + 1) * L.f);
+  }
   return w;
 }
 
@@ -348,6 +365,313 @@ __global__ void __launch_bounds__(kDownWarps * 32) decode_down_kernel(const bf16
   }
 }
 
+// ------------------------------------------------------------------ MXFP8
+// 16 E4M3 codes -> floats (exact).
+__device__ __forceinline__ void fp8x16(const uint4& v, float (&o)[16]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[q] & 0xffffu), __NV_E4M3);
+    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[q] >> 16), __NV_E4M3);
+    const float2 a = __half22float2(__half2(lo)), b = __half22float2(__half2(hi));
+    o[4 * q] = a.x;
+    o[4 * q + 1] = a.y;
+    o[4 * q + 2] = b.x;
+    o[4 * q + 3] = b.y;
+  }
+}
+// 2^(s - 127) for an E8M0 byte s (s = 0 is the subnormal 2^-127).
+__device__ __forceinline__ float e8m0(uint32_t s) {
+  return s ? __uint_as_float(s << 23) : __uint_as_float(0x00400000u);
+}
+
+// In place: 32 fp32 values -> their MX quantisation (E4M3 codes times the block's E8M0 scale),
+// held as the exact fp32 values.
+__device__ __forceinline__ void fake_quant32(float (&v)[32]) {
+  uint4 lo, hi;
+  const float s = e8m0(quant32(v, lo, hi));
+  float c[16];
+  fp8x16(lo, c);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = c[i] * s;
+  fp8x16(hi, c);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[16 + i] = c[i] * s;
+}
+
+// x [B, d] bf16 -> xd: one thread per 32-value block.
+__global__ void __launch_bounds__(256) decode_quant_x_kernel(const bf16* __restrict__ x, int nblocks, DecodeWs w) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= nblocks) return;
+  float v[32];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) unpack8(*reinterpret_cast<const uint4*>(x + (size_t)b * 32 + 8 * q), v + 8 * q);
+  fake_quant32(v);
+  uint4* dst = reinterpret_cast<uint4*>(w.xd + (size_t)b * 32);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) dst[q] = pack8(v + 8 * q);   // exact
+}
+
+constexpr int kBatchMx = 4;   // 16-byte chunks per lane per row in flight (two blocks per SM fit)
+
+// Gate/up on E4M3 weights: one warp per (U entry, row i); each lane takes 16-byte chunks (16
+// values, half of a 32-value scale block) of the gate and up rows, decodes them once and applies
+// the block scale to each token's partial dot product.
+__global__ void __launch_bounds__(256, 2) decode_gateup_mx_kernel(const uint8_t* __restrict__ W13q,
+                                                               const uint8_t* __restrict__ W13s, int d, int f, int G,
+                                                               int k, int E, int S, DecodeWs w) {
+  griddep_launch();
+  if (S && threadIdx.x == 0) {   // the shared expert's rows into L2 while the router runs
+    const size_t bytes = (size_t)2 * f * d;
+    const size_t slice = ((bytes + gridDim.x - 1) / gridDim.x + 15) & ~(size_t)15;
+    const size_t b0 = (size_t)blockIdx.x * slice;
+    if (b0 < bytes) {
+      const char* base = (const char*)(W13q + (size_t)E * 2 * f * d) + b0;
+      const size_t n = (bytes - b0) < slice ? (bytes - b0) : slice;
+      for (size_t o = 0; o < n; o += 65536) {
+        const uint32_t sz = (uint32_t)((n - o) < 65536 ? (n - o) : 65536);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + o), "r"(sz) : "memory");
+      }
+    }
+  }
+  griddep_wait();
+  const int lane = threadIdx.x & 31;
+  const int nU = *w.nU;
+  const int items = nU * f;
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  const int nchunk = d / 16, nb = d / 32;
+  for (int it = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items; it += nwarps) {
+    const int ui = (it / f + nU - 1) % nU, i = it % f;
+    const int e = w.U[ui];
+    const int a0 = w.u_off[ui], a1 = w.u_off[ui + 1];
+    const size_t rg = (size_t)e * 2 * f + (i / G) * 2 * G + (i % G), ru = rg + G;
+    const uint8_t* wg = W13q + rg * d;
+    const uint8_t* wu = W13q + ru * d;
+    const uint8_t* sg = W13s + rg * nb;
+    const uint8_t* su = W13s + ru * nb;
+    for (int g0 = a0; g0 < a1; g0 += kTokGroup) {
+      const int nt = min(kTokGroup, a1 - g0);
+      const bf16* xr[kTokGroup];
+#pragma unroll
+      for (int q = 0; q < kTokGroup; ++q) xr[q] = w.xd + (size_t)(q < nt ? (w.a_tok[g0 + q] >> 8) : 0) * d;
+      float au[kTokGroup], av[kTokGroup];
+#pragma unroll
+      for (int q = 0; q < kTokGroup; ++q) au[q] = av[q] = 0.f;
+      for (int cb = lane; cb < nchunk; cb += 32 * kBatchMx) {
+        uint4 gv[kBatchMx], uvv[kBatchMx];
+        uint32_t sgv[kBatchMx], suv[kBatchMx];
+#pragma unroll
+        for (int q = 0; q < kBatchMx; ++q) {
+          const int c = cb + q * 32;
+          if (c < nchunk) {
+            gv[q] = ld_stream(reinterpret_cast<const bf16*>(wg + (size_t)c * 16));
+            uvv[q] = ld_stream(reinterpret_cast<const bf16*>(wu + (size_t)c * 16));
+            sgv[q] = sg[c >> 1];
+            suv[q] = su[c >> 1];
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < kBatchMx; ++q) {
+          const int c = cb + q * 32;
+          if (c < nchunk) {
+            float fg[16], fu[16];
+            fp8x16(gv[q], fg);
+            fp8x16(uvv[q], fu);
+            const float s_g = e8m0(sgv[q]), s_u = e8m0(suv[q]);
+#pragma unroll
+            for (int tt = 0; tt < kTokGroup; ++tt) {
+              if (tt < nt) {
+                const uint4* xv8 = reinterpret_cast<const uint4*>(xr[tt] + (size_t)c * 16);
+                float pg = 0.f, pu = 0.f;
+#pragma unroll
+                for (int h8 = 0; h8 < 2; ++h8) {
+                  float xv[8];
+                  unpack8(xv8[h8], xv);
+#pragma unroll
+                  for (int r = 0; r < 8; ++r) {
+                    pg = fmaf(xv[r], fg[8 * h8 + r], pg);
+                    pu = fmaf(xv[r], fu[8 * h8 + r], pu);
+                  }
+                }
+                au[tt] = fmaf(pg, s_g, au[tt]);
+                av[tt] = fmaf(pu, s_u, av[tt]);
+              }
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int tt = 0; tt < kTokGroup; ++tt) {
+        if (tt < nt) {
+          const float u = warp_sum(au[tt]);
+          const float v = warp_sum(av[tt]);
+          if (lane == 0) {
+            const int code = w.a_tok[g0 + tt];
+            const int t = code >> 8, slot = code & 255;
+            w.h[((size_t)t * (k + 1) + slot) * f + i] = silu_f(u) * v;
+          }
+        }
+      }
+    }
+  }
+}
+
+// h [B, k+1, f] fp32 -> its MX quantisation along f (hd, bf16); one thread per 32-value block.
+__global__ void __launch_bounds__(256) decode_quant_h_kernel(int nblocks, DecodeWs w) {
+  griddep_launch();
+  griddep_wait();
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= nblocks) return;
+  float v[32];
+  const float4* src = reinterpret_cast<const float4*>(w.h + (size_t)b * 32);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float4 t = src[q];
+    v[4 * q] = t.x;
+    v[4 * q + 1] = t.y;
+    v[4 * q + 2] = t.z;
+    v[4 * q + 3] = t.w;
+  }
+  fake_quant32(v);
+  uint4* dst = reinterpret_cast<uint4*>(w.hd + (size_t)b * 32);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) dst[q] = pack8(v + 8 * q);   // exact
+}
+
+constexpr int kFChunksMx = 4;   // 16-byte chunks (16 values) of a Wd row per lane (f <= 2048 per pass)
+
+__device__ __forceinline__ void load_wd_mx(const uint8_t* Wdq, int e, int d, int f, int c0, int f0, int lane,
+                                           uint4 (&wv)[kCols][kFChunksMx]) {
+#pragma unroll
+  for (int cc = 0; cc < kCols; ++cc) {
+    const uint8_t* row = Wdq + ((size_t)e * d + c0 + cc) * f + f0;
+#pragma unroll
+    for (int q = 0; q < kFChunksMx; ++q) {
+      const int c = (lane + 32 * q) * 16;
+      if (f0 + c < f) wv[cc][q] = ld_stream(reinterpret_cast<const bf16*>(row + c));
+    }
+  }
+}
+
+// Down on E4M3 weights: warp per pair of output columns, as the bf16 kernel; h comes quantised
+// (as exact fp32 values); each Wd chunk is decoded and scaled once per expert.
+__global__ void __launch_bounds__(kDownWarps * 32) decode_down_mx_kernel(const uint8_t* __restrict__ Wdq,
+                                                                         const uint8_t* __restrict__ Wds, int B, int d,
+                                                                         int f, int k, DecodeWs w,
+                                                                         bf16* __restrict__ y) {
+  extern __shared__ float acc_s[];   // [kDownWarps][B][kCols]
+  griddep_launch();
+  griddep_wait();
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  float* acc = acc_s + (size_t)wib * B * kCols;
+  const int nU = *w.nU;
+  const int c0 = (blockIdx.x * kDownWarps + wib) * kCols;
+  if (c0 >= d) return;
+  const int nb = f / 32;
+  for (int q = lane; q < B * kCols; q += 32) acc[q] = 0.f;
+  __syncwarp();
+  for (int f0 = 0; f0 < f; f0 += 32 * kFChunksMx * 16) {
+    uint4 wcur[kCols][kFChunksMx], wnext[kCols][kFChunksMx];
+    load_wd_mx(Wdq, w.U[0], d, f, c0, f0, lane, wnext);
+    for (int ui = 0; ui < nU; ++ui) {
+      const int e = w.U[ui];
+#pragma unroll
+      for (int cc = 0; cc < kCols; ++cc)
+#pragma unroll
+        for (int q = 0; q < kFChunksMx; ++q) wcur[cc][q] = wnext[cc][q];
+      if (ui + 1 < nU) load_wd_mx(Wdq, w.U[ui + 1], d, f, c0, f0, lane, wnext);   // next expert in flight
+      const int a0 = w.u_off[ui], a1 = w.u_off[ui + 1];
+      if (a1 - a0 == 1) {
+        // one token (the common case at small B): no decoded copy of the chunk is kept
+        const int code = w.a_tok[a0];
+        const int t = code >> 8, slot = code & 255;
+        const float g = w.a_gate[a0];
+        const bf16* hr = w.hd + ((size_t)t * (k + 1) + slot) * f;
+        float s[kCols] = {};
+#pragma unroll
+        for (int q = 0; q < kFChunksMx; ++q) {
+          const int c = f0 + (lane + 32 * q) * 16;
+          if (c < f) {
+            float hv[16];
+            unpack8(*reinterpret_cast<const uint4*>(hr + c), hv);
+            unpack8(*reinterpret_cast<const uint4*>(hr + c + 8), hv + 8);
+#pragma unroll
+            for (int cc = 0; cc < kCols; ++cc) {
+              float wf[16];
+              fp8x16(wcur[cc][q], wf);
+              float pr = 0.f;
+#pragma unroll
+              for (int r = 0; r < 16; ++r) pr = fmaf(hv[r], wf[r], pr);
+              s[cc] = fmaf(pr, e8m0(Wds[((size_t)e * d + c0 + cc) * nb + (c >> 5)]), s[cc]);
+            }
+          }
+        }
+#pragma unroll
+        for (int cc = 0; cc < kCols; ++cc) {
+          const float tot = warp_sum(s[cc]);
+          if (lane == 0) acc[t * kCols + cc] = fmaf(g, tot, acc[t * kCols + cc]);
+        }
+        __syncwarp();
+        continue;
+      }
+      // several tokens: in groups of kTokGroup, each chunk decoded and scaled once per group
+      for (int g0 = a0; g0 < a1; g0 += kTokGroup) {
+        const int nt = min(kTokGroup, a1 - g0);
+        const bf16* hr[kTokGroup];
+#pragma unroll
+        for (int tt = 0; tt < kTokGroup; ++tt) {
+          const int code = w.a_tok[g0 + (tt < nt ? tt : 0)];
+          hr[tt] = w.hd + ((size_t)(code >> 8) * (k + 1) + (code & 255)) * f;
+        }
+        float s[kTokGroup][kCols] = {};
+#pragma unroll
+        for (int q = 0; q < kFChunksMx; ++q) {
+          const int c = f0 + (lane + 32 * q) * 16;
+          if (c < f) {
+#pragma unroll
+            for (int cc = 0; cc < kCols; ++cc) {
+              float wf[16];
+              fp8x16(wcur[cc][q], wf);
+              const float sw = e8m0(Wds[((size_t)e * d + c0 + cc) * nb + (c >> 5)]);
+#pragma unroll
+              for (int tt = 0; tt < kTokGroup; ++tt) {
+                if (tt < nt) {
+                  float hv[16];
+                  unpack8(*reinterpret_cast<const uint4*>(hr[tt] + c), hv);
+                  unpack8(*reinterpret_cast<const uint4*>(hr[tt] + c + 8), hv + 8);
+                  float pr = 0.f;
+#pragma unroll
+                  for (int r = 0; r < 16; ++r) pr = fmaf(hv[r], wf[r], pr);
+                  s[tt][cc] = fmaf(pr, sw, s[tt][cc]);
+                }
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int tt = 0; tt < kTokGroup; ++tt) {
+          if (tt < nt) {
+            const int code = w.a_tok[g0 + tt];
+            const int t = code >> 8;
+            const float g = w.a_gate[g0 + tt];
+#pragma unroll
+            for (int cc = 0; cc < kCols; ++cc) {
+              const float tot = warp_sum(s[tt][cc]);
+              if (lane == 0) acc[t * kCols + cc] = fmaf(g, tot, acc[t * kCols + cc]);
+            }
+          }
+        }
+        __syncwarp();
+      }
+    }
+  }
+  __syncwarp();
+  for (int q = lane; q < B * kCols; q += 32) {
+    const int t = q / kCols, cc = q % kCols;
+    if (c0 + cc < d) y[(size_t)t * d + c0 + cc] = __float2bfloat16_rn(acc[q]);
+  }
+}
+
 // Launch with programmatic stream serialisation: the kernel may start while
 // its predecessor finishes; it waits (griddepcontrol.wait) before reading the
 // predecessor's results.
@@ -370,9 +694,11 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), int grid, int block, size_t smem,
 
 size_t decode_workspace_bytes(const Layer& L, int B) {
   const int na = B * L.k + B;
-  return al(sizeof(float) * B * L.E) + al(sizeof(int) * B * L.k) + al(sizeof(float) * B * L.k) + al(sizeof(int)) +
-         al(sizeof(int) * (L.E + 1)) + al(sizeof(int) * (L.E + 2)) + al(sizeof(int) * na) +
-         al(sizeof(float) * na) + al(sizeof(float) * B * (L.k + 1) * L.f);
+  size_t z = al(sizeof(float) * B * L.E) + al(sizeof(int) * B * L.k) + al(sizeof(float) * B * L.k) + al(sizeof(int)) +
+             al(sizeof(int) * (L.E + 1)) + al(sizeof(int) * (L.E + 2)) + al(sizeof(int) * na) +
+             al(sizeof(float) * na) + al(sizeof(float) * B * (L.k + 1) * L.f);
+  if (L.prec == MOE_MXFP8) z += al(sizeof(bf16) * B * L.d) + al(sizeof(bf16) * B * (L.k + 1) * L.f);
+  return z;
 }
 
 cudaError_t launch_decode_route(const Layer& L, const void* x, int B, void* ws, cudaStream_t s) {
@@ -388,6 +714,33 @@ cudaError_t launch_decode_gateup(const Layer& L, const void* x, int B, void* ws,
   DecodeWs w = carve(L, B, ws);
   return launch_pdl(decode_gateup_kernel, L.num_sms * 4, 256, 0, s, (const bf16*)x, (const bf16*)L.W13, L.d, L.f, L.G,
                     L.k, L.E, L.S, w);
+}
+
+cudaError_t launch_decode_quant_x_mx(const Layer& L, const void* x, int B, void* ws, cudaStream_t s) {
+  DecodeWs w = carve(L, B, ws);
+  const int nblocks = B * L.d / 32;
+  decode_quant_x_kernel<<<(nblocks + 255) / 256, 256, 0, s>>>((const bf16*)x, nblocks, w);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_gateup_mx(const Layer& L, int B, void* ws, cudaStream_t s) {
+  DecodeWs w = carve(L, B, ws);
+  return launch_pdl(decode_gateup_mx_kernel, L.num_sms * 4, 256, 0, s, (const uint8_t*)L.W13q, (const uint8_t*)L.W13s,
+                    L.d, L.f, L.G, L.k, L.E, L.S, w);
+}
+
+cudaError_t launch_decode_quant_h_mx(const Layer& L, int B, void* ws, cudaStream_t s) {
+  DecodeWs w = carve(L, B, ws);
+  const int nblocks = B * (L.k + 1) * L.f / 32;
+  return launch_pdl(decode_quant_h_kernel, (nblocks + 255) / 256, 256, 0, s, nblocks, w);
+}
+
+cudaError_t launch_decode_down_mx(const Layer& L, int B, void* y, void* ws, cudaStream_t s) {
+  DecodeWs w = carve(L, B, ws);
+  const int down_blocks = (L.d + kDownWarps * kCols - 1) / (kDownWarps * kCols);
+  const size_t smem = sizeof(float) * kDownWarps * B * kCols;
+  return launch_pdl(decode_down_mx_kernel, down_blocks, kDownWarps * 32, smem, s, (const uint8_t*)L.Wdq,
+                    (const uint8_t*)L.Wds, B, L.d, L.f, L.k, w, (bf16*)y);
 }
 
 cudaError_t launch_decode_down(const Layer& L, int B, void* y, void* ws, cudaStream_t s) {

@@ -112,6 +112,11 @@ size_t decode_workspace_bytes(const Layer& L, int B);
 cudaError_t launch_decode_route(const Layer& L, const void* x, int B, void* ws, cudaStream_t s);
 cudaError_t launch_decode_gateup(const Layer& L, const void* x, int B, void* ws, cudaStream_t s);
 cudaError_t launch_decode_down(const Layer& L, int B, void* y, void* ws, cudaStream_t s);
+// MXFP8 layers: x quantised along d, gate/up on E4M3 W13, h quantised along f, down on E4M3 Wd.
+cudaError_t launch_decode_quant_x_mx(const Layer& L, const void* x, int B, void* ws, cudaStream_t s);
+cudaError_t launch_decode_gateup_mx(const Layer& L, int B, void* ws, cudaStream_t s);
+cudaError_t launch_decode_quant_h_mx(const Layer& L, int B, void* ws, cudaStream_t s);
+cudaError_t launch_decode_down_mx(const Layer& L, int B, void* y, void* ws, cudaStream_t s);
 // tc_gemm.cu (bf16 tcgen05 path)
 bool tc_supported(const Layer& L);
 cudaError_t tc_init(Layer& L);   // encodes the weight tensor maps, sets kernel attributes

@@ -546,9 +546,9 @@ def chunked_forward_backward(x, Wr, b, Wg, Wu, Wd, dy, chunk: int, **kw):
 # Decode  [warp: small-batch decode; the same function as the forward at T = B]
 # --------------------------------------------------------------------------
 
-def decode(x, Wr, b, Wg, Wu, Wd, k, router, renorm, scale, n_shared=0, logits32=None):
-    """Small-batch decode computes exactly the layer forward on B tokens."""
-    return forward(x, Wr, b, Wg, Wu, Wd, k, router, renorm, scale, n_shared, logits32)
+def decode(x, Wr, b, Wg, Wu, Wd, k, router, renorm, scale, n_shared=0, logits32=None, mx: bool = False):
+    """Small-batch decode computes exactly the layer forward on B tokens (MXFP8 layers: the MXFP8 forward)."""
+    return forward(x, Wr, b, Wg, Wu, Wd, k, router, renorm, scale, n_shared, logits32, mx=mx)
 
 
 def rel_frobenius(a, ref):
