@@ -562,6 +562,41 @@ def run_extra_mxfp8(dev, pk):
     return out
 
 
+def run_chunk_sweep(args):
+    """The DeepSeek-V3 MXFP8 forward + backward of T=8192 tokens for several chunk sizes, each with a
+    512 MB ring of saved activations: ms per step, chunks, ring slots and recomputed chunk forwards.
+    Prints one JSON line."""
+    from mixture_experts_layer_routing_gb300 import MoeLayer, moe_train_chunked, moe_train_chunked_sizes
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    base = moe_synth.DSV3_MXFP8
+    inp = moe_synth.make_inputs(base, dev, grad=True)
+    rows = {}
+    for chunk in (1024, 2048, 2368, 4096, 8192):
+        spec = base.with_(chunk=chunk)
+        layer = MoeLayer.from_spec(spec, device=dev)
+        layer.set_weights(inp["Wr"], inp["b"], inp["Wg"], inp["Wu"], inp["Wd"])
+        z = moe_train_chunked_sizes(layer.h, spec.T)
+        slots = max(1, (512 << 20) // z["slot"])
+        ring = layer.buffer("ring", slots * z["slot"])
+        ws = layer.buffer("chunk_ws", z["workspace"])
+        g = layer.grads_like(inp["x"])
+        y = torch.empty_like(inp["x"])
+        rec = []
+        fn = lambda: rec.append(moe_train_chunked(layer.h, inp["x"], inp["dy"], spec.T, y, g["dx"], g["dWr"],  # noqa: E731
+                                                  g["dWg"], g["dWu"], g["dWd"], ring, slots * z["slot"], ws))
+        ms = time_steps(fn, args.steps, args.warmup, 1)
+        rows[str(chunk)] = {"ms": ms, "tokens_per_s": spec.T / (ms * 1e-3), "chunks": z["n_chunks"],
+                            "ring_slots": slots, "slot_mb": z["slot"] / 2**20, "recomputed_chunks": rec[-1]}
+        layer.close()
+        del layer, g, y, ring, ws
+        torch.cuda.empty_cache()
+    print(json.dumps({"sweep": "dsv3 mxfp8 fwd+bwd, T=8192, 512 MB ring", "steps": args.steps,
+                      "warmup": args.warmup, "by_chunk_tokens": rows}), flush=True)
+
+
 # -------------------------------------------------------- reference arm
 
 def run_reference(args):
@@ -597,10 +632,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=128, help="oracle sample for cpu_baseline")
     ap.add_argument("--ref-tokens", type=int, default=16, help="oracle sample per reference-arm step")
+    ap.add_argument("--chunk-sweep", action="store_true",
+                    help="instead of the bench line: the DeepSeek-V3 MXFP8 fwd+bwd over chunk sizes 1024..8192")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.impl == "reference":
+    if args.chunk_sweep:
+        run_chunk_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
