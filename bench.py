@@ -459,6 +459,7 @@ def run_extra(args, dev, pk):
         del layer, inp
         torch.cuda.empty_cache()
     extra.update(run_extra_mxfp8(dev, pk))
+    extra["bf16_T128_d2048_E64_f1408_top6 fwd+bwd, eager vs CUDA graph"] = graph_vs_eager(dev)
     return extra
 
 
@@ -489,6 +490,28 @@ def decode_lines(layer, spec, dev, pk, tag, expert_bytes, n_batches=16):
             "experts_read_mean": float(np.mean(nact)), "batches": n_batches,
             "groups_ms": {g: v[1] / 32 for g, v in profb.items()}}
     return out
+
+
+def graph_vs_eager(dev, T=128, steps=50):
+    """Launch overhead at a small batch: the 2048-token bench layer's forward + backward on T tokens,
+    eager through the C ABI and replayed from one captured CUDA graph (same calls, same buffers)."""
+    spec = moe_synth.BF16_T2048.with_(T=T)
+    step = TrainStep(spec, dev)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    from mixture_experts_layer_routing_gb300 import moe_launch_count
+    n0 = moe_launch_count(step.layer.h)
+    eager = time_steps(step, steps, 5, 1)
+    launches = (moe_launch_count(step.layer.h) - n0) // (steps + 5)
+    replay = time_steps(graph.replay, steps, 5, 1)
+    step.layer.close()
+    return {"T": T, "eager_ms": eager, "graph_ms": replay, "kernel_launches_per_step": launches}
 
 
 def decode_crossover(layer, spec, dev, n_batches=8):
