@@ -158,6 +158,29 @@ def roofline_entry(group, ms_per_launch, flops, nbytes, pk, traffic=None):
             "frac": achieved / pk["hbm_gbs"], "traffic": traffic, "peak_source": pk["source"]}
 
 
+def written_bytes(spec):
+    """Bytes the weight-gradient kernels write (bf16 gradients of every expert)."""
+    nseg = spec.E + spec.S
+    return {"bwd_dw13": nseg * 2 * spec.f * spec.d * 2, "bwd_dwd": nseg * spec.f * spec.d * 2}
+
+
+def write_bandwidth(dev, nbytes=1 << 30, reps=10):
+    """HBM write rate (GB/s): time of filling a buffer larger than L2, CUDA events."""
+    buf = torch.empty(nbytes // 2, dtype=torch.bfloat16, device=dev)
+    for _ in range(3):
+        buf.fill_(1.0)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        buf.fill_(1.0)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    del buf
+    return nbytes / (ms * 1e-3) / 1e9
+
+
 def stored_traffic(group):
     """dram bytes per launch from the committed ncu summary, if its kernel source is unchanged."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -399,6 +422,14 @@ def run_ours(args):
     dom = max((g for g in prof if g in work), key=lambda g: prof[g][1])
     dom_ms = prof[dom][1] / args.steps
     roof = roofline_entry(dom, dom_ms, *work[dom], pk, stored_traffic(dom))
+    wbytes = written_bytes(spec).get(dom)
+    if wbytes:
+        # a weight-gradient kernel mostly writes: its bound is the HBM write rate, measured here
+        wpk = write_bandwidth(dev)
+        roof["write_bound"] = {"written_bytes": wbytes, "achieved_write_gbs": wbytes / (dom_ms * 1e-3) / 1e9,
+                               "measured_write_peak_gbs": wpk,
+                               "frac": wbytes / (dom_ms * 1e-3) / 1e9 / wpk,
+                               "peak_source": "fill of a 1 GiB buffer, CUDA events, this run"}
 
     out = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
