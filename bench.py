@@ -624,6 +624,46 @@ def run_extra_mxfp8(dev, pk):
     return out
 
 
+# Small workloads for profiler captures (a few GB on the device): DeepSeek-V3 shapes with 32 routed
+# experts (+1 shared) instead of 256.
+PROFILE_CASES = {
+    "dsv3_e32_bf16_decode_b4": (moe_synth.DSV3_UNIFORM.with_(name="dsv3_e32_bf16", E=32, T=64, seed=12), "decode", 4),
+    "dsv3_e32_mxfp8_decode_b4": (moe_synth.DSV3_MXFP8.with_(name="dsv3_e32_mxfp8", E=32, T=64, chunk=0, seed=12),
+                                 "decode", 4),
+    "dsv3_e32_bf16_fwd_t4096": (moe_synth.DSV3_UNIFORM.with_(name="dsv3_e32_bf16", E=32, T=4096, seed=9), "fwd", 4096),
+    "dsv3_e32_mxfp8_chunked_t4096": (moe_synth.DSV3_MXFP8.with_(name="dsv3_e32_mxfp8", E=32, T=4096, chunk=2048,
+                                                                seed=11), "chunked", 4096),
+}
+
+
+def run_profile_case(args):
+    from mixture_experts_layer_routing_gb300 import MoeLayer, moe_decode
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    spec, kind, n = PROFILE_CASES[args.profile_case]
+    inp = moe_synth.make_inputs(spec, dev, grad=kind == "chunked")
+    layer = MoeLayer.from_spec(spec, device=dev)
+    layer.set_weights(inp["Wr"], inp["b"], inp["Wg"], inp["Wu"], inp["Wd"])
+    if kind == "decode":
+        xs = [t.contiguous() for t in moe_synth.make_tokens(spec.with_(T=n), 8, dev)]
+        y = torch.empty_like(xs[0])
+        ws = layer.buffer("fwd", layer.sizes(n)["fwd_ws"])
+        it = [0]
+
+        def fn():
+            moe_decode(layer.h, xs[it[0] % 8], n, y, ws)
+            it[0] += 1
+    elif kind == "fwd":
+        fn = lambda: layer.forward(inp["x"])  # noqa: E731
+    else:
+        fn = lambda: layer.train_chunked(inp["x"], inp["dy"], slots=1)  # noqa: E731
+    ms = time_steps(fn, args.steps, args.warmup, 1)
+    print(json.dumps({"profile_case": args.profile_case, "ms": ms, "status": layer.status()}), flush=True)
+    layer.close()
+
+
 def run_chunk_sweep(args):
     """The DeepSeek-V3 MXFP8 forward + backward of T=8192 tokens for several chunk sizes, each with a
     512 MB ring of saved activations: ms per step, chunks, ring slots and recomputed chunk forwards.
@@ -696,10 +736,14 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=16, help="oracle sample per reference-arm step")
     ap.add_argument("--chunk-sweep", action="store_true",
                     help="instead of the bench line: the DeepSeek-V3 MXFP8 fwd+bwd over chunk sizes 1024..8192")
+    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES),
+                    help="instead of the bench line: run one small workload --steps times (for a profiler)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.chunk_sweep:
+    if args.profile_case:
+        run_profile_case(args)
+    elif args.chunk_sweep:
         run_chunk_sweep(args)
     elif args.impl == "reference":
         run_reference(args)
