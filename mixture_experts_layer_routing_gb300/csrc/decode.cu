@@ -540,15 +540,20 @@ __global__ void __launch_bounds__(256) decode_quant_h_kernel(int nblocks, Decode
 
 constexpr int kFChunksMx = 4;   // 16-byte chunks (16 values) of a Wd row per lane (f <= 2048 per pass)
 
-__device__ __forceinline__ void load_wd_mx(const uint8_t* Wdq, int e, int d, int f, int c0, int f0, int lane,
-                                           uint4 (&wv)[kCols][kFChunksMx]) {
+// The Wd rows c0.. of expert e, features [f0, f0 + 2048), and their block scales (as 2^(s-127)).
+__device__ __forceinline__ void load_wd_mx(const uint8_t* Wdq, const uint8_t* Wds, int e, int d, int f, int c0, int f0,
+                                           int lane, uint4 (&wv)[kCols][kFChunksMx], uint32_t (&sv)[kCols][kFChunksMx]) {
 #pragma unroll
   for (int cc = 0; cc < kCols; ++cc) {
-    const uint8_t* row = Wdq + ((size_t)e * d + c0 + cc) * f + f0;
+    const size_t r = (size_t)e * d + c0 + cc;
+    const uint8_t* row = Wdq + r * f + f0;
 #pragma unroll
     for (int q = 0; q < kFChunksMx; ++q) {
       const int c = (lane + 32 * q) * 16;
-      if (f0 + c < f) wv[cc][q] = ld_stream(reinterpret_cast<const bf16*>(row + c));
+      if (f0 + c < f) {
+        wv[cc][q] = ld_stream(reinterpret_cast<const bf16*>(row + c));
+        sv[cc][q] = Wds[r * (f / 32) + ((f0 + c) >> 5)];
+      }
     }
   }
 }
@@ -572,14 +577,18 @@ __global__ void __launch_bounds__(kDownWarps * 32) decode_down_mx_kernel(const u
   __syncwarp();
   for (int f0 = 0; f0 < f; f0 += 32 * kFChunksMx * 16) {
     uint4 wcur[kCols][kFChunksMx], wnext[kCols][kFChunksMx];
-    load_wd_mx(Wdq, w.U[0], d, f, c0, f0, lane, wnext);
+    uint32_t scur[kCols][kFChunksMx], snext[kCols][kFChunksMx];
+    load_wd_mx(Wdq, Wds, w.U[0], d, f, c0, f0, lane, wnext, snext);
     for (int ui = 0; ui < nU; ++ui) {
       const int e = w.U[ui];
 #pragma unroll
       for (int cc = 0; cc < kCols; ++cc)
 #pragma unroll
-        for (int q = 0; q < kFChunksMx; ++q) wcur[cc][q] = wnext[cc][q];
-      if (ui + 1 < nU) load_wd_mx(Wdq, w.U[ui + 1], d, f, c0, f0, lane, wnext);   // next expert in flight
+        for (int q = 0; q < kFChunksMx; ++q) {
+          wcur[cc][q] = wnext[cc][q];
+          scur[cc][q] = snext[cc][q];
+        }
+      if (ui + 1 < nU) load_wd_mx(Wdq, Wds, w.U[ui + 1], d, f, c0, f0, lane, wnext, snext);   // next expert in flight
       const int a0 = w.u_off[ui], a1 = w.u_off[ui + 1];
       if (a1 - a0 == 1) {
         // one token (the common case at small B): no decoded copy of the chunk is kept
@@ -602,7 +611,7 @@ __global__ void __launch_bounds__(kDownWarps * 32) decode_down_mx_kernel(const u
               float pr = 0.f;
 #pragma unroll
               for (int r = 0; r < 16; ++r) pr = fmaf(hv[r], wf[r], pr);
-              s[cc] = fmaf(pr, e8m0(Wds[((size_t)e * d + c0 + cc) * nb + (c >> 5)]), s[cc]);
+              s[cc] = fmaf(pr, e8m0(scur[cc][q]), s[cc]);
             }
           }
         }
@@ -632,7 +641,7 @@ __global__ void __launch_bounds__(kDownWarps * 32) decode_down_mx_kernel(const u
             for (int cc = 0; cc < kCols; ++cc) {
               float wf[16];
               fp8x16(wcur[cc][q], wf);
-              const float sw = e8m0(Wds[((size_t)e * d + c0 + cc) * nb + (c >> 5)]);
+              const float sw = e8m0(scur[cc][q]);
 #pragma unroll
               for (int tt = 0; tt < kTokGroup; ++tt) {
                 if (tt < nt) {
