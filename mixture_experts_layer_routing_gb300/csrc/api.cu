@@ -48,7 +48,7 @@ Sizes sizes_for(const Layer& L, int T) {
   z.ctx = z.route + z.uv;
   z.fwd_ws = z.route + z.fwd_scratch;
   z.bwd_ws = al(eb * R * 2 * L.f) + al(eb * R * L.f) + al(4 * A * (L.f / 64)) + al(eb * R * L.d) +
-             al(4 * T * (size_t)L.E) + al(4 * A);
+             al(4 * T * (size_t)L.E) + al(4 * A) + al(4 * (size_t)kRouterSplit * L.E * L.d);
   z.packed = al(eb * nseg * 2 * L.f * L.d) + al(eb * nseg * L.d * L.f) + al(eb * L.E * L.d) + al(4 * L.E);
   if (L.prec == MOE_MXFP8) {
     const size_t d = L.d, f = L.f, Rp = rp_max(L, T);
@@ -119,6 +119,7 @@ Bufs carve(const Layer& L, int T, void* ws, const void* ctx, void* bws) {
     B.dx_rows = b; b += al(eb * B.R * L.d);
     B.dl = (float*)b; b += al(4 * (size_t)B.T * L.E);
     B.dgate = (float*)b; b += al(4 * (size_t)B.A);
+    B.dwr_part = (float*)b; b += al(4 * (size_t)kRouterSplit * L.E * L.d);
     if (mx) {
       const size_t Rp = rp_max(L, T);
       B.Rp_max = (int)Rp;
@@ -245,7 +246,8 @@ moe_status backward_body(moe_handle_s* h, const void* x, const void* dy, int T, 
     CK(run(h, s, G_BWD_DH, 1, [&] { return launch_simt_bwd_dh(L, B, dy, s); }));
     CK(run(h, s, G_BWD_DX, 1, [&] { return launch_simt_bwd_dx(L, B, s); }));
   }
-  CK(run(h, s, G_ROUTER_BWD, 2, [&] { return launch_router_bwd(L, B, x, dWr, acc, s); }));
+  const int router_kernels = (L.router == MOE_ROUTER_SOFTMAX && !L.renorm) ? 2 : 3;
+  CK(run(h, s, G_ROUTER_BWD, router_kernels, [&] { return launch_router_bwd(L, B, x, dWr, acc, s); }));
   CK(run(h, s, G_DX_GATHER, 1, [&] { return launch_dx_gather(L, B, dx, s); }));
   if (h->mx) {
     // token-axis operands of the weight gradients: into this call's buffers, or (chunked step)

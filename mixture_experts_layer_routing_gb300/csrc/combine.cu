@@ -123,19 +123,19 @@ __global__ void __launch_bounds__(256) router_dl_kernel(const float* __restrict_
   }
 }
 
-// dWr[e, c] = sum_t dl[t, e] x[t, c].
-// Renormalised routers: dl is zero off the selection, so only the rows of
-// segment e contribute. Block per (e, 32*V columns): warp w takes the
-// segment's rows w, w+8, ... (in sorted order), each lane 16 bytes of
-// columns; the 8 warp partials are then added in warp order.
+// Renormalised routers: dl is nonzero only at the selected experts, so dWr[e] = sum over the
+// segment's rows p of dl[t_p, e] x[t_p]. Block (column block, e, split s) takes the rows
+// p = off[e] + s + kRouterSplit * (w + 8 i) of its warp w, each lane 16 bytes of columns; the 8 warp
+// partials are added in warp order into part[s][e]. Splitting each segment kRouterSplit ways spreads
+// a hot expert (thousands of rows) over that many more SMs; router_dw_reduce_kernel then adds the
+// splits in order.
 template <typename T>
 __global__ void __launch_bounds__(256) router_dw_seg_kernel(const float* __restrict__ dl, const T* __restrict__ x,
                                                             const int* __restrict__ off, const int* __restrict__ perm,
-                                                            int d, int E, int k, int accumulate,
-                                                            float* __restrict__ dWr) {
+                                                            int d, int E, int k, float* __restrict__ part) {
   constexpr int V = 16 / sizeof(T);
-  __shared__ float part[8][32 * V];
-  const int e = blockIdx.y, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  __shared__ float red[8][32 * V];
+  const int e = blockIdx.y, sp = blockIdx.z, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int c = blockIdx.x * 32 * V + lane * V;
   float acc[V];
 #pragma unroll
@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(256) router_dw_seg_kernel(const float* __restr
   if (c < d) {
     const int p1 = off[e + 1];
 #pragma unroll 4
-    for (int p = off[e] + w; p < p1; p += 8) {
+    for (int p = off[e] + sp + kRouterSplit * w; p < p1; p += kRouterSplit * 8) {
       const int t = perm[p] / k;
       const float g = dl[(long)t * E + e];
       const uint4 u = *reinterpret_cast<const uint4*>(x + (long)t * d + c);
@@ -161,15 +161,26 @@ __global__ void __launch_bounds__(256) router_dw_seg_kernel(const float* __restr
     }
   }
 #pragma unroll
-  for (int i = 0; i < V; ++i) part[w][lane * V + i] = acc[i];
+  for (int i = 0; i < V; ++i) red[w][lane * V + i] = acc[i];
   __syncthreads();
   const int col = blockIdx.x * 32 * V + threadIdx.x;
   if (threadIdx.x < 32 * V && col < d) {
-    float s = 0.f;
+    float sum = 0.f;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) s += part[q][threadIdx.x];
-    dWr[(long)e * d + col] = accumulate ? dWr[(long)e * d + col] + s : s;
+    for (int q = 0; q < 8; ++q) sum += red[q][threadIdx.x];
+    part[((long)sp * E + e) * d + col] = sum;
   }
+}
+
+// dWr = (dWr if accumulating) + sum over the splits s = 0 .. kRouterSplit-1, in that order.
+__global__ void __launch_bounds__(256) router_dw_reduce_kernel(const float* __restrict__ part, long n, int accumulate,
+                                                               float* __restrict__ dWr) {
+  const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float sum = 0.f;
+#pragma unroll
+  for (int sp = 0; sp < kRouterSplit; ++sp) sum += part[sp * n + i];
+  dWr[i] = accumulate ? dWr[i] + sum : sum;
 }
 
 // Plain softmax: dl is dense; dWr[e, c] over all tokens in order, one thread per (e, column).
@@ -273,13 +284,15 @@ cudaError_t launch_router_bwd(const Layer& L, const Bufs& B, const void* x, floa
       router_dw_dense_kernel<bf16><<<grid, 256, 0, s>>>(B.dl, (const bf16*)x, B.T, L.d, L.E, acc, dWr);
   } else {
     const int cols = 32 * 16 / (int)elem_bytes(L.prec);
-    dim3 grid((L.d + cols - 1) / cols, L.E);
+    dim3 grid((L.d + cols - 1) / cols, L.E, kRouterSplit);
     if (L.prec == MOE_FP32)
-      router_dw_seg_kernel<float><<<grid, 256, 0, s>>>(B.dl, (const float*)x, B.off, B.perm, L.d, L.E, L.k, acc,
-                                                              dWr);
+      router_dw_seg_kernel<float><<<grid, 256, 0, s>>>(B.dl, (const float*)x, B.off, B.perm, L.d, L.E, L.k,
+                                                              B.dwr_part);
     else
-      router_dw_seg_kernel<bf16><<<grid, 256, 0, s>>>(B.dl, (const bf16*)x, B.off, B.perm, L.d, L.E, L.k, acc,
-                                                             dWr);
+      router_dw_seg_kernel<bf16><<<grid, 256, 0, s>>>(B.dl, (const bf16*)x, B.off, B.perm, L.d, L.E, L.k,
+                                                             B.dwr_part);
+    const long n = (long)L.E * L.d;
+    router_dw_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(B.dwr_part, n, acc, dWr);
   }
   return cudaGetLastError();
 }

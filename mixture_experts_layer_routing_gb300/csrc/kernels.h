@@ -13,6 +13,7 @@ constexpr int kMaxE = 256;        // routed experts supported by the routing ker
 constexpr int kMaxK = 8;          // experts per token
 constexpr int kChunk = 1024;      // assignments per block of the histogram / permutation kernels
 constexpr int kBM = 128;          // rows per M-tile of the grouped GEMMs (segment padding unit)
+constexpr int kRouterSplit = 8;   // row splits of each expert segment in the router weight gradient
 constexpr int kDenseTiles = 8;    // segments with this many M-tiles or more are scheduled as "dense"
 constexpr int kGate = 128;        // gate/up interleave block of the packed bf16 W13 (rows)
 constexpr int kGateMx = 64;       // gate/up interleave block of the MXFP8 W13 (rows)
@@ -78,6 +79,7 @@ struct Bufs {
   float* dg_part;        // [A, f / 64] gate-gradient partials, one per 64 features
   void* dx_rows;         // [R, d]
   float* dl;             // [T, E]
+  float* dwr_part;       // [kRouterSplit, E, d] router weight-gradient partials
   float* dgate;          // [T, k]
   // MXFP8 operands (codes, scales)
   uint8_t *xq, *xs;      // [T, d], [T, d/32]
