@@ -185,11 +185,13 @@ moe_status moe_get_status(moe_handle h, void* stream, int* device_status);
  * such as a plugin inside a host program that owns all device memory, or a
  * serving loop that bans cudaMalloc/cudaFree after start-up because they can
  * block and synchronise the device.
- * Its scratch is one fixed 4 MiB array inside the library (held on every GPU
- * that loads the library until the process exits). A call needs
- *   2*pad(4*ceil(T*k/1024)*E) + 3*pad(4*(E+S+1)) + 2*pad(4*T*(k+S)) bytes,
+ * Its scratch is one fixed 4 MiB array inside the library, plus an 8 MiB one
+ * for the split-K partials of the router GEMM (both held on every GPU that
+ * loads the library until the process exits). A call needs
+ *   2*pad(4*ceil(T*k/1024)*E) + 2*pad(4*(E+S+1)) + pad(16*(E+S+1))
+ *   + 2*pad(4*T*(k+S)) bytes of the 4 MiB,
  * pad() rounding up to 256; larger T returns MOE_ERR_WORKSPACE before any
- * launch (E = 256, k = 8, S = 1 allows T up to 47,616 tokens).
+ * launch (E = 256, k = 8, S = 1 allows T up to 47,573 tokens).
  * The first call on a device looks up the array's address there; make that
  * first call before any stream capture. Every call on a device shares the one
  * array and it keeps the last call's contents (each call writes every entry

@@ -190,7 +190,11 @@ moe_status run_route(moe_handle_s* h, const Bufs& B, const void* x, const float*
   if (logits_override) {
     lg = logits_override;
   } else if (h->tc_router) {
-    CK(run(h, s, G_ROUTER_LOGITS, 1, [&] { return launch_tc_router_logits(L, x, B.T, B.logits, s); }));
+    // the forward scratch o (not yet written) holds the split-K partials of the router GEMM
+    const size_t part_bytes = B.o ? (size_t)B.R * L.d * elem_bytes(L.prec) : 0;
+    const int nk = tc_router_splits(L, B.T) > 1 ? 2 : 1;
+    CK(run(h, s, G_ROUTER_LOGITS, nk,
+           [&] { return launch_tc_router_logits(L, x, B.T, B.logits, s, (float*)B.o, part_bytes); }));
   } else {
     CK(run(h, s, G_ROUTER_LOGITS, 1, [&] { return launch_router_logits(L, x, B.T, B.logits, s); }));
   }

@@ -124,26 +124,35 @@ __global__ void __launch_bounds__(256) router_dl_kernel(const float* __restrict_
 }
 
 // Renormalised routers: dl is nonzero only at the selected experts, so dWr[e] = sum over the
-// segment's rows p of dl[t_p, e] x[t_p]. Block (column block, e, split s) takes the rows
-// p = off[e] + s + kRouterSplit * (w + 8 i) of its warp w, each lane 16 bytes of columns; the 8 warp
-// partials are added in warp order into part[s][e]. Splitting each segment kRouterSplit ways spreads
-// a hot expert (thousands of rows) over that many more SMs; router_dw_reduce_kernel then adds the
-// splits in order.
+// segment's rows p of dl[t_p, e] x[t_p]. A segment of cnt rows is split ns = min(kRouterSplit,
+// ceil(cnt / kRouterSplitRows)) ways, so a hot expert (thousands of rows) spreads over more SMs
+// while ordinary ones stay whole. Block (column block, e, split s < ns) takes the rows
+// p = off[e] + s + ns * (w + 8 i) of its warp w, each lane 16 bytes of columns; the 8 warp partials
+// are added in warp order. With one split the block writes dWr[e] itself; otherwise it writes
+// part[s][e] and router_dw_reduce_kernel adds the splits in order.
+__device__ __forceinline__ int router_splits(int cnt) {
+  const int ns = (cnt + kRouterSplitRows - 1) / kRouterSplitRows;
+  return ns < 1 ? 1 : (ns > kRouterSplit ? kRouterSplit : ns);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) router_dw_seg_kernel(const float* __restrict__ dl, const T* __restrict__ x,
                                                             const int* __restrict__ off, const int* __restrict__ perm,
-                                                            int d, int E, int k, float* __restrict__ part) {
+                                                            int d, int E, int k, int accumulate,
+                                                            float* __restrict__ dWr, float* __restrict__ part) {
   constexpr int V = 16 / sizeof(T);
   __shared__ float red[8][32 * V];
   const int e = blockIdx.y, sp = blockIdx.z, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int p0 = off[e], p1 = off[e + 1];
+  const int ns = router_splits(p1 - p0);
+  if (sp >= ns) return;
   const int c = blockIdx.x * 32 * V + lane * V;
   float acc[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) acc[i] = 0.f;
   if (c < d) {
-    const int p1 = off[e + 1];
 #pragma unroll 4
-    for (int p = off[e] + sp + kRouterSplit * w; p < p1; p += kRouterSplit * 8) {
+    for (int p = p0 + sp + ns * w; p < p1; p += ns * 8) {
       const int t = perm[p] / k;
       const float g = dl[(long)t * E + e];
       const uint4 u = *reinterpret_cast<const uint4*>(x + (long)t * d + c);
@@ -168,18 +177,24 @@ __global__ void __launch_bounds__(256) router_dw_seg_kernel(const float* __restr
     float sum = 0.f;
 #pragma unroll
     for (int q = 0; q < 8; ++q) sum += red[q][threadIdx.x];
-    part[((long)sp * E + e) * d + col] = sum;
+    const long o = (long)e * d + col;
+    if (ns == 1) dWr[o] = accumulate ? dWr[o] + sum : sum;
+    else part[(long)sp * E * d + o] = sum;
   }
 }
 
-// dWr = (dWr if accumulating) + sum over the splits s = 0 .. kRouterSplit-1, in that order.
-__global__ void __launch_bounds__(256) router_dw_reduce_kernel(const float* __restrict__ part, long n, int accumulate,
-                                                               float* __restrict__ dWr) {
+// Split segments: dWr[e] = (dWr[e] if accumulating) + sum over their splits s = 0 .. ns-1, in order.
+__global__ void __launch_bounds__(256) router_dw_reduce_kernel(const float* __restrict__ part,
+                                                               const int* __restrict__ off, int E, int d,
+                                                               int accumulate, float* __restrict__ dWr) {
   const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long n = (long)E * d;
   if (i >= n) return;
+  const int e = (int)(i / d);
+  const int ns = router_splits(off[e + 1] - off[e]);
+  if (ns == 1) return;
   float sum = 0.f;
-#pragma unroll
-  for (int sp = 0; sp < kRouterSplit; ++sp) sum += part[sp * n + i];
+  for (int sp = 0; sp < ns; ++sp) sum += part[sp * n + i];
   dWr[i] = accumulate ? dWr[i] + sum : sum;
 }
 
@@ -286,13 +301,13 @@ cudaError_t launch_router_bwd(const Layer& L, const Bufs& B, const void* x, floa
     const int cols = 32 * 16 / (int)elem_bytes(L.prec);
     dim3 grid((L.d + cols - 1) / cols, L.E, kRouterSplit);
     if (L.prec == MOE_FP32)
-      router_dw_seg_kernel<float><<<grid, 256, 0, s>>>(B.dl, (const float*)x, B.off, B.perm, L.d, L.E, L.k,
-                                                              B.dwr_part);
+      router_dw_seg_kernel<float><<<grid, 256, 0, s>>>(B.dl, (const float*)x, B.off, B.perm, L.d, L.E, L.k, acc,
+                                                              dWr, B.dwr_part);
     else
-      router_dw_seg_kernel<bf16><<<grid, 256, 0, s>>>(B.dl, (const bf16*)x, B.off, B.perm, L.d, L.E, L.k,
-                                                             B.dwr_part);
+      router_dw_seg_kernel<bf16><<<grid, 256, 0, s>>>(B.dl, (const bf16*)x, B.off, B.perm, L.d, L.E, L.k, acc,
+                                                             dWr, B.dwr_part);
     const long n = (long)L.E * L.d;
-    router_dw_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(B.dwr_part, n, acc, dWr);
+    router_dw_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(B.dwr_part, B.off, L.E, L.d, acc, dWr);
   }
   return cudaGetLastError();
 }

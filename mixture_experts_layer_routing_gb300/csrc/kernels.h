@@ -13,7 +13,8 @@ constexpr int kMaxE = 256;        // routed experts supported by the routing ker
 constexpr int kMaxK = 8;          // experts per token
 constexpr int kChunk = 1024;      // assignments per block of the histogram / permutation kernels
 constexpr int kBM = 128;          // rows per M-tile of the grouped GEMMs (segment padding unit)
-constexpr int kRouterSplit = 8;   // row splits of each expert segment in the router weight gradient
+constexpr int kRouterSplit = 8;   // most row splits of an expert segment in the router weight gradient
+constexpr int kRouterSplitRows = 256;   // rows per split
 constexpr int kDenseTiles = 8;    // segments with this many M-tiles or more are scheduled as "dense"
 constexpr int kGate = 128;        // gate/up interleave block of the packed bf16 W13 (rows)
 constexpr int kGateMx = 64;       // gate/up interleave block of the MXFP8 W13 (rows)
@@ -122,7 +123,11 @@ cudaError_t launch_decode_down_mx(const Layer& L, int B, void* y, void* ws, cuda
 // tc_gemm.cu (bf16 tcgen05 path)
 bool tc_supported(const Layer& L);
 cudaError_t tc_init(Layer& L);   // encodes the weight tensor maps, sets kernel attributes
-cudaError_t launch_tc_router_logits(const Layer& L, const void* x, int T, float* logits, cudaStream_t s);
+// part (nullable, part_bytes): scratch for split-K partials when T gives few row tiles
+constexpr size_t kRouterPartBytes = 8u << 20;   // router split-K partials, at most
+int tc_router_splits(const Layer& L, int T);
+cudaError_t launch_tc_router_logits(const Layer& L, const void* x, int T, float* logits, cudaStream_t s,
+                                    float* part, size_t part_bytes);
 cudaError_t launch_tc_gateup(const Layer& L, const Bufs& B, const void* x, cudaStream_t s);
 cudaError_t launch_tc_down(const Layer& L, const Bufs& B, cudaStream_t s);
 cudaError_t launch_tc_bwd_dh(const Layer& L, const Bufs& B, const void* dy, cudaStream_t s);

@@ -28,9 +28,13 @@ constexpr size_t kScratchBytes = size_t(4) << 20;   // 4 MiB
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_route_scratch[kScratchBytes];
+// split-K partials of the router GEMM (the same splits as every other routing call, so the logits
+// are summed in the same order)
+static __device__ __align__(256) float g_router_part[kRouterPartBytes / sizeof(float)];
 
 std::mutex g_mu;
 void* g_scratch[kMaxDevices] = {};
+void* g_part[kMaxDevices] = {};
 
 inline size_t al(size_t v) { return (v + 255) & ~size_t(255); }
 
@@ -41,18 +45,23 @@ size_t scratch_bytes(const Layer& L, int T) {
   return 2 * al(4 * nch * L.E) + 2 * al(4 * (nseg + 1)) + al(16 * (nseg + 1)) + al(4 * R) + al(4 * R);
 }
 
-// Device address of the array on device `dev` (the current device). Looked up
-// on the first call for that device and remembered.
+// Device addresses of the arrays on device `dev` (the current device): out[0] the routing scratch,
+// out[1] the router partials. Looked up on the first call for that device and remembered.
 cudaError_t scratch_address(int dev, void** out) {
   std::lock_guard<std::mutex> lock(g_mu);
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (!g_scratch[dev]) {
     void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_route_scratch);
+    cudaError_t e = cudaGetSymbolAddress(&p, g_route_scratch);
+    if (e != cudaSuccess) return e;
+    void* q = nullptr;
+    e = cudaGetSymbolAddress(&q, g_router_part);
     if (e != cudaSuccess) return e;
     g_scratch[dev] = p;
+    g_part[dev] = q;
   }
-  *out = g_scratch[dev];
+  out[0] = g_scratch[dev];
+  out[1] = g_part[dev];
   return cudaSuccess;
 }
 
@@ -70,8 +79,9 @@ extern "C" moe_status moe_route_noalloc(moe_handle h, const void* x, int T, floa
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (dev != h->device) return MOE_ERR_INVALID_ARG;
-  void* base = nullptr;
-  if (scratch_address(dev, &base) != cudaSuccess) return MOE_ERR_CUDA;
+  void* addr[2] = {};
+  if (scratch_address(dev, addr) != cudaSuccess) return MOE_ERR_CUDA;
+  void* base = addr[0];
 
   Bufs B = {};
   B.T = T;
@@ -96,7 +106,7 @@ extern "C" moe_status moe_route_noalloc(moe_handle h, const void* x, int T, floa
   cudaStream_t s = (cudaStream_t)stream;
   // Every scratch entry the kernels read is written earlier in the same call,
   // so nothing needs clearing between calls.
-  cudaError_t e = h->tc ? launch_tc_router_logits(L, x, T, logits, s) : launch_router_logits(L, x, T, logits, s);
+  cudaError_t e = h->tc ? launch_tc_router_logits(L, x, T, logits, s, (float*)addr[1], kRouterPartBytes) : launch_router_logits(L, x, T, logits, s);
   if (e == cudaSuccess) e = launch_topk(L, logits, T, idx, gate, s);
   if (e == cudaSuccess) e = launch_scan_permute(L, B, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(cnt, B.cnt, 4 * (size_t)L.E, cudaMemcpyDeviceToDevice, s);

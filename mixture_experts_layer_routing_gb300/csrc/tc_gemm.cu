@@ -73,6 +73,8 @@ struct TcParams {
   int dg_slots;
   int A_rows;             // routed rows (rows >= A_rows are the shared expert)
   int accumulate;         // EPI_DW13 / EPI_DWD: add to the values already in the output
+  int ksplit;             // DENSE: K splits (1: none); split s writes part + s * dense_rows * ldo
+  float* part;            // DENSE split-K partial outputs (EPI_F32)
   int* status;
 };
 
@@ -82,12 +84,14 @@ __device__ __forceinline__ void unpack8_to(const bf16* p, float* f) { unpack8(*r
 struct Tile {
   int e, m, n;
   int row0, row_end;   // SEG_M / DENSE: output rows; SEG_K: the segment's sorted rows (the K range)
-  int nkb;             // K blocks of 64
+  int nkb;             // end of the K-block range (blocks of 64)
+  int kb0 = 0;         // first K block (DENSE split-K; 0 otherwise)
+  int ks = 0;          // K split index (DENSE split-K)
 };
 
 template <int SCHED, int CG>
 __device__ __forceinline__ int total_tiles(const TcParams& p) {
-  if (SCHED == SCHED_DENSE) return ((p.dense_rows + BM - 1) / BM) * p.n_tiles;
+  if (SCHED == SCHED_DENSE) return ((p.dense_rows + BM - 1) / BM) * p.n_tiles * p.ksplit;
   if (SCHED == SCHED_SEG_K) return p.nseg * p.m_tiles * p.n_tiles;
   return (CG == 2 ? p.mp_off[p.nseg] : p.mt_off[p.nseg]) * p.n_tiles;
 }
@@ -122,12 +126,16 @@ __device__ __forceinline__ Tile map_tile(const TcParams& p, int L, int rank) {
   if (CG == 2) return map_tile_pair(p, L, rank);
   Tile t;
   if (SCHED == SCHED_DENSE) {
+    const int nk = p.K / BK;
+    t.ks = L % p.ksplit;
+    const int rest = L / p.ksplit;
     t.e = 0;
-    t.n = L % p.n_tiles;
-    t.m = L / p.n_tiles;
+    t.n = rest % p.n_tiles;
+    t.m = rest / p.n_tiles;
     t.row0 = t.m * BM;
     t.row_end = p.dense_rows;
-    t.nkb = p.K / BK;
+    t.kb0 = t.ks * nk / p.ksplit;
+    t.nkb = (t.ks + 1) * nk / p.ksplit;
     return t;
   }
   if (SCHED == SCHED_SEG_K) {
@@ -385,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tk1 = tok_at(0);
         tk2 = tok_at(1);
       }
-      for (int kb = 0; kb < t.nkb; ++kb, ++it) {
+      for (int kb = t.kb0; kb < t.nkb; ++kb, ++it) {
         if (kTokRing) {
           tk0 = tk1;
           tk1 = tk2;
@@ -415,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int L = tile0; L < ntiles && ok; L += tstep) {
         const Tile t = map_tile<SCHED, CG>(p, L, rank);
-        for (int kb = 0; kb < t.nkb; ++kb, ++it) {
+        for (int kb = t.kb0; kb < t.nkb; ++kb, ++it) {
           const int s = it % NS;
           if (!mbar_wait(full0 + 8 * s, (it / NS) & 1, abort_flag, p.status)) {
             ok = false;
@@ -437,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         tc_fence_after();
         const uint32_t dcol = tmem_base + acc * BN;
-        for (int kb = 0; kb < t.nkb; ++kb, ++it) {
+        for (int kb = t.kb0; kb < t.nkb; ++kb, ++it) {
           const int s = it % NS;
           const uint32_t ph = (it / NS) & 1;
           if (!(CG == 2 && MD::kCpAsync ? mbar_wait_cluster(full0 + 8 * s, ph, abort_flag, p.status)
@@ -453,8 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t da = MD::kAMn ? desc_mnmajor(sa + k * 2048) : desc_kmajor(sa + k * 32);
             const uint64_t db = MD::kBMn ? desc_mnmajor(sb + k * 2048) : desc_kmajor(sb + k * 32);
-            if (CG == 2) mma_bf16_pair(dcol, da, db, IDESC, (kb > 0 || k > 0) ? 1u : 0u);
-            else mma_bf16(dcol, da, db, IDESC, (kb > 0 || k > 0) ? 1u : 0u);
+            if (CG == 2) mma_bf16_pair(dcol, da, db, IDESC, (kb > t.kb0 || k > 0) ? 1u : 0u);
+            else mma_bf16(dcol, da, db, IDESC, (kb > t.kb0 || k > 0) ? 1u : 0u);
           }
           if (CG == 2) mma_commit_pair_mc(empty0 + 8 * s, 0x3);
           else mma_commit(empty0 + 8 * s);
@@ -536,7 +544,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else if (EPI == EPI_F32) {
-        float* orow = (float*)p.out + (size_t)row * p.ldo + t.n * BN;
+        float* obase = p.ksplit > 1 ? p.part + (size_t)t.ks * p.dense_rows * p.ldo : (float*)p.out;
+        float* orow = obase + (size_t)row * p.ldo + t.n * BN;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
           uint32_t a[32];
@@ -771,7 +780,35 @@ cudaError_t tc_init(Layer& L) {
   return cudaSuccess;
 }
 
-cudaError_t launch_tc_router_logits(const Layer& L, const void* x, int T, float* logits, cudaStream_t s) {
+// K splits of the router GEMM: with few row tiles (small T) about one CTA per SM gets work (at
+// least 4 K blocks per split, at most 16 splits). A function of the shapes only, so that every
+// routing call (route, forward, the no-allocation route) sums the logits in the same order; the
+// partials must fit kRouterPartBytes and the forward scratch o (R x d x 2 bytes).
+int tc_router_splits(const Layer& L, int T) {
+  const int tiles = (T + BM - 1) / BM;
+  const int nk = L.d / BK;
+  int ks = L.num_sms / (tiles > 0 ? tiles : 1);
+  if (ks > nk / 4) ks = nk / 4;
+  if (ks > 16) ks = 16;
+  const size_t o_bytes = (size_t)T * (L.k + L.S) * L.d * 2;
+  while (ks > 1 && ((size_t)ks * T * L.E * sizeof(float) > kRouterPartBytes ||
+                    (size_t)ks * T * L.E * sizeof(float) > o_bytes))
+    --ks;
+  return ks > 1 ? ks : 1;
+}
+
+// logits = sum of the K splits' partials, in split order.
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ part, long n, int ksplit,
+                                                            float* __restrict__ out) {
+  const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float sum = 0.f;
+  for (int q = 0; q < ksplit; ++q) sum += part[q * n + i];
+  out[i] = sum;
+}
+
+cudaError_t launch_tc_router_logits(const Layer& L, const void* x, int T, float* logits, cudaStream_t s,
+                                    float* part, size_t part_bytes) {
   CUtensorMap tx, tw;
   if (!make_tmap(&tx, x, L.d, T, BK, BM) || !make_tmap(&tw, L.Wr, L.d, L.E, BK, kBNrouter))
     return cudaErrorInvalidValue;
@@ -784,8 +821,16 @@ cudaError_t launch_tc_router_logits(const Layer& L, const void* x, int T, float*
   p.n_valid = L.E;
   p.status = L.status;
   const int tiles = (T + BM - 1) / BM;
-  return launch<kBNrouter, A_TMA_K, B_TMA_K, SCHED_DENSE, EPI_F32>(tx, tw, p, tiles < L.num_sms ? tiles : L.num_sms,
-                                                                   s);
+  p.ksplit = tc_router_splits(L, T);
+  if (p.ksplit > 1 && (!part || (size_t)p.ksplit * T * L.E * sizeof(float) > part_bytes)) return cudaErrorInvalidValue;
+  p.part = part;
+  const int total = tiles * p.ksplit;
+  cudaError_t e = launch<kBNrouter, A_TMA_K, B_TMA_K, SCHED_DENSE, EPI_F32>(tx, tw, p, total < L.num_sms ? total
+                                                                                                    : L.num_sms, s);
+  if (e != cudaSuccess || p.ksplit == 1) return e;
+  const long n = (long)T * L.E;
+  splitk_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(part, n, p.ksplit, logits);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_tc_gateup(const Layer& L, const Bufs& B, const void* x, cudaStream_t s) {
