@@ -224,7 +224,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 2-D tensor map over [rows][cols] (cols contiguous) of bf16 (elem_bytes 2) or bytes (1),
 // box box_cols x box_rows, 128-byte swizzle.
 bool make_tmap(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-               uint32_t box_rows, int elem_bytes = 2) {
+               uint32_t box_rows, int elem_bytes = 2, bool swizzle = true) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -233,7 +233,8 @@ bool make_tmap(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, 
   cuuint32_t estr[2] = {1, 1};
   return fn(tm, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
             const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
