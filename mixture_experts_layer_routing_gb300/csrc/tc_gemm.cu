@@ -542,16 +542,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else if (EPI == EPI_DH) {
-        // r = dy_t Wd[e] for 128 features n*128..: SwiGLU backward with the saved u, v;
-        // dg partials over each 64-feature half.
-        static_assert(EPI != EPI_DH || BN == 128, "EPI_DH works on one 128-feature block");
+        // r = dy_t Wd[e] for the BN features n*BN..: SwiGLU backward with the saved u, v, which
+        // (like du, dv) sit in 128-feature blocks [u of block b | v of block b]; dg partials over
+        // each 64-feature quarter. The last tile may run past f (its B columns were zero-filled):
+        // blocks at or beyond f are skipped.
+        static_assert(EPI != EPI_DH || BN % 128 == 0, "EPI_DH works on whole 128-feature blocks");
         const float g = valid ? p.row_gate[row] : 0.f;
-        const bf16* urow = p.uv + (size_t)row * p.ld_uv + t.n * 256;
-        bf16* durow = (bf16*)p.out + (size_t)row * p.ld_uv + t.n * 256;
-        bf16* hgrow = (bf16*)p.out2 + (size_t)row * p.ldo + t.n * 128;
+        const bf16* uvrow = p.uv + (size_t)row * p.ld_uv;
+        bf16* dudvrow = (bf16*)p.out + (size_t)row * p.ld_uv;
+        bf16* hgrow = (bf16*)p.out2 + (size_t)row * p.ldo + t.n * BN;
         float dgp = 0.f;
 #pragma unroll 1
-        for (int c0 = 0; c0 < 128; c0 += 32) {
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          const int feat = t.n * BN + c0;   // first feature of this chunk
+          if (feat >= p.ldo) break;
+          const int blk = (feat >> 7) * 256 + (c0 & 127);   // column of u (v: + 128) in uv / dudv
           uint32_t a[32];
           tmem_ld32(tbase + c0, a);
           tmem_ld_wait();
@@ -559,8 +564,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             float uf[32], vf[32], du[32], dv[32], hg[32];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              unpack8_to(urow + c0 + q * 8, uf + q * 8);
-              unpack8_to(urow + 128 + c0 + q * 8, vf + q * 8);
+              unpack8_to(uvrow + blk + q * 8, uf + q * 8);
+              unpack8_to(uvrow + blk + 128 + q * 8, vf + q * 8);
             }
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -576,12 +581,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              *reinterpret_cast<uint4*>(durow + c0 + q * 8) = pack8(du + q * 8);
-              *reinterpret_cast<uint4*>(durow + 128 + c0 + q * 8) = pack8(dv + q * 8);
+              *reinterpret_cast<uint4*>(dudvrow + blk + q * 8) = pack8(du + q * 8);
+              *reinterpret_cast<uint4*>(dudvrow + blk + 128 + q * 8) = pack8(dv + q * 8);
               *reinterpret_cast<uint4*>(hgrow + c0 + q * 8) = pack8(hg + q * 8);
             }
             if ((c0 & 63) == 32) {
-              if (row < p.A_rows) p.dg_part[(size_t)row * p.dg_slots + (t.n * 128 + c0 - 32) / 64] = dgp;
+              if (row < p.A_rows) p.dg_part[(size_t)row * p.dg_slots + (feat - 32) / 64] = dgp;
               dgp = 0.f;
             }
           }
@@ -778,7 +783,7 @@ cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcParam
 constexpr int kBNup = 256;     // gate/up: 128 gate + 128 up columns
 constexpr int kBNdown = 256;
 constexpr int kBNrouter = 256;
-constexpr int kBNdh = 128;     // one 128-feature block per tile
+constexpr int kBNdh = 256;     // two 128-feature blocks per tile (the last may hold one)
 constexpr int kBNdx = 256;
 constexpr int kBNdw13 = 256;
 constexpr int kBNdwd = 256;
@@ -912,7 +917,7 @@ cudaError_t launch_tc_bwd_dh(const Layer& L, const Bufs& B, const void* dy, cuda
   p.A = (const bf16*)dy;
   p.lda = L.d;
   p.K = L.d;
-  p.n_tiles = L.f / kBNdh;
+  p.n_tiles = (L.f + kBNdh - 1) / kBNdh;
   p.b_rows_per_seg = L.d;
   p.out = B.dudv;
   p.out2 = B.hg;
