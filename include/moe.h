@@ -174,6 +174,23 @@ moe_status moe_decode(moe_handle h, const void* x, int B, void* y, void* workspa
  * MOE_ERR_INVALID_ARG. */
 moe_status moe_set_pairs(moe_handle h, int mode);
 
+/* Forward of a bf16 tensor-core layer with its two expert GEMMs in one kernel
+ * (on = 1): the gate/up GEMM (A5) and the down GEMM (A6) run as one
+ * persistent cooperative launch over a single tile order, a down tile starting
+ * as soon as the gate/up tiles of its 128 rows have stored h (per-row-block
+ * arrival counters held by the handle, waits bounded by the device timeout),
+ * so no SM idles through the gate/up tail and the kernel boundary. This
+ * follows the one-call design of "Cursor открыл код ядра Mixture of
+ * Experts..." (section "Три решения, которые дали результат"), on one GPU.
+ * Routing (A1-A4) and the combine (A7) stay separate launches: on GB300 the
+ * combine as a phase of the persistent kernel (8 warps per SM) measured
+ * slower than its own high-occupancy launch at every size tried. Results are
+ * bit-identical to on = 0 (the default). Host-only. on = 1 for a layer without
+ * the bf16 tensor-core path returns MOE_ERR_UNSUPPORTED; other values
+ * MOE_ERR_INVALID_ARG. While on = 1, calls on one handle must not run
+ * concurrently on two streams (the counters are per handle). */
+moe_status moe_set_fused(moe_handle h, int on);
+
 /* Wait for the handle's queued work on `stream`, then read and clear the
  * device status word into *device_status (MOE_OK if no device error). */
 moe_status moe_get_status(moe_handle h, void* stream, int* device_status);

@@ -16,11 +16,12 @@ using namespace moe;
 // Kernel groups reported by moe_profile_read.
 enum Group {
   G_ROUTER_LOGITS, G_TOPK, G_SCAN_PERMUTE, G_GATEUP, G_DOWN, G_COMBINE, G_BWD_DH, G_BWD_DX, G_ROUTER_BWD,
-  G_DX_GATHER, G_BWD_DW13, G_BWD_DWD, G_DECODE_ROUTE, G_DECODE_GATEUP, G_DECODE_DOWN, G_PACK, G_MX_QUANT, G_COUNT
+  G_DX_GATHER, G_BWD_DW13, G_BWD_DWD, G_DECODE_ROUTE, G_DECODE_GATEUP, G_DECODE_DOWN, G_PACK, G_MX_QUANT, G_FUSED, G_COUNT
 };
 static const char* kGroupNames[G_COUNT] = {
     "router_logits", "topk", "scan_permute", "gateup", "down", "combine", "bwd_dh", "bwd_dx", "router_bwd",
-    "dx_gather", "bwd_dw13", "bwd_dwd", "decode_route", "decode_gateup", "decode_down", "pack_weights", "mx_quant"};
+    "dx_gather", "bwd_dw13", "bwd_dwd", "decode_route", "decode_gateup", "decode_down", "pack_weights", "mx_quant",
+    "experts_fused"};
 
 namespace {
 
@@ -221,6 +222,8 @@ moe_status forward_body(moe_handle_s* h, const void* x, int T, void* y, void* ct
     CK(run(h, s, G_MX_QUANT, 1, [&] { return launch_mx_quant_rows(x, T, L.d, B.xq, B.xs, s); }));
     CK(run(h, s, G_GATEUP, 1, [&] { return launch_mx_gateup(L, B, s); }));
     CK(run(h, s, G_DOWN, 1, [&] { return launch_mx_down(L, B, s); }));
+  } else if (h->tc && L.fused) {
+    CK(run(h, s, G_FUSED, 1, [&] { return launch_tc_fused_experts(L, B, x, s); }));
   } else if (h->tc) {
     CK(run(h, s, G_GATEUP, 1, [&] { return launch_tc_gateup(L, B, x, s); }));
     CK(run(h, s, G_DOWN, 1, [&] { return launch_tc_down(L, B, s); }));
@@ -343,20 +346,26 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
   L.router = c.router; L.renorm = c.renorm ? 1 : 0; L.prec = c.prec; L.scale = c.route_scale;
   L.G = (c.f % kGate == 0) ? kGate : 64;
   L.pairs = 0;
+  L.fused = 0;
   L.has_weights = false;
   if (cudaGetDevice(&h->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&L.num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
     delete h;
     return MOE_ERR_CUDA;
   }
+  // status word, decode counter, and the fused expert kernel's counters (4 + one per m-tile)
+  const size_t max_mtiles = ((size_t)c.T_max * (c.k + c.n_shared) + 127) / 128 + c.E + c.n_shared;
+  const size_t word_bytes = 256 + 4 * (4 + max_mtiles);
   int* words = nullptr;
-  if (cudaMalloc(&words, 256) != cudaSuccess || cudaMemset(words, 0, 256) != cudaSuccess) {
+  if (cudaMalloc(&words, word_bytes) != cudaSuccess || cudaMemset(words, 0, word_bytes) != cudaSuccess) {
     if (words) cudaFree(words);
     delete h;
     return MOE_ERR_CUDA;
   }
   L.status = words;
   L.decode_counter = words + 32;
+  L.dep_done = (unsigned*)(words + 64);
+  L.dep = (unsigned*)(words + 68);
   if (c.prec == MOE_MXFP8) L.G = kGateMx;
   h->tc = (c.prec == MOE_BF16) && tc_supported(L);
   h->mx = (c.prec == MOE_MXFP8) && mx_supported(L);
@@ -649,6 +658,13 @@ moe_status moe_profile_read(moe_handle h, int max_groups, char* names, long long
 moe_status moe_launch_count(moe_handle h, long long* launches) {
   if (!h || !launches) return MOE_ERR_INVALID_ARG;
   *launches = h->launches;
+  return MOE_OK;
+}
+
+moe_status moe_set_fused(moe_handle h, int on) {
+  if (!h || on < 0 || on > 1) return MOE_ERR_INVALID_ARG;
+  if (on && !h->tc) return MOE_ERR_UNSUPPORTED;
+  h->L.fused = on;
   return MOE_OK;
 }
 

@@ -214,7 +214,7 @@ struct Modes {
 // With CTA pairs (CG = 2) this CTA loads B columns rank*BN/2 .. of the n-tile, and every TMA load
 // of either CTA completes on rank 0's full barrier (lead_full), which rank 0 arms with the bytes of
 // both CTAs.
-template <int BN, int AMODE, int BMODE, int SCHED, int CG>
+template <int BN, int AMODE, int BMODE, int SCHED, int CG, bool kCounted = Modes<AMODE, BMODE>::kCpAsync>
 __device__ __forceinline__ void load_stage(const TcParams& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
                                            const Tile& t, int kb, uint32_t sa, uint32_t sb, uint32_t full_bar,
                                            const bf16* const (&gsrc)[8], const uint32_t (&gbytes)[8], int ktok,
@@ -226,7 +226,7 @@ __device__ __forceinline__ void load_stage(const TcParams& p, const CUtensorMap*
   const int ptid = threadIdx.x;
   if (ptid == 0 && tma_bytes) {
     if (rank == 0) {
-      if (Modes<AMODE, BMODE>::kCpAsync) mbar_expect_tx(full_bar, CG * tma_bytes);
+      if (kCounted) mbar_expect_tx(full_bar, CG * tma_bytes);
       else mbar_arrive_expect_tx(full_bar, CG * tma_bytes);
     }
     auto load = [&](uint32_t dst, const CUtensorMap* tm, int c0, int c1) {
@@ -270,6 +270,61 @@ __device__ __forceinline__ void load_stage(const TcParams& p, const CUtensorMap*
       const int j = (lane >> 3) % LPR, q = lane & 7;
       const bf16* src = p.Bsrc + (size_t)tok * p.ldb + t.n * BN + j * 64 + q * 8;
       cp_async16(sb + j * kChunkBytes + kk * 128 + ((q ^ (kk & 7)) << 4), src, v ? 16u : 0u);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- epilogues
+// Gate/up: u = columns 0..BN/2 of the tile, v = BN/2..BN (one 128-feature block of each);
+// h = silu(u) v stored to out, and u, v to the saved pre-activations when kept.
+template <int BN>
+__device__ __forceinline__ void epi_swiglu(const TcParams& p, const Tile& t, uint32_t tbase, int row, bool valid) {
+  bf16* hrow = (bf16*)p.out + (size_t)row * p.ldo + t.n * (BN / 2);
+  bf16* uvrow = p.uv ? p.uv + (size_t)row * p.ld_uv + t.n * BN : nullptr;
+#pragma unroll 1
+  for (int c0 = 0; c0 < BN / 2; c0 += 32) {
+    uint32_t u[32], v[32];
+    tmem_ld32(tbase + c0, u);
+    tmem_ld32(tbase + BN / 2 + c0, v);
+    tmem_ld_wait();
+    if (valid) {
+      float hf[32], uf[32], vf[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        uf[i] = __uint_as_float(u[i]);
+        vf[i] = __uint_as_float(v[i]);
+        hf[i] = silu_f(uf[i]) * vf[i];
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(hrow + c0 + q * 8) = pack8(hf + q * 8);
+      if (uvrow) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          *reinterpret_cast<uint4*>(uvrow + c0 + q * 8) = pack8(uf + q * 8);
+          *reinterpret_cast<uint4*>(uvrow + BN / 2 + c0 + q * 8) = pack8(vf + q * 8);
+        }
+      }
+    }
+  }
+}
+
+// Down (kGate: scaled by the row's gate) and dx rows: the tile's BN columns stored as bf16.
+template <int BN, bool kGate>
+__device__ __forceinline__ void epi_scale_store(const TcParams& p, const Tile& t, uint32_t tbase, int row,
+                                                bool valid) {
+  const float g = (kGate && valid) ? p.row_gate[row] : 1.f;
+  bf16* orow = (bf16*)p.out + (size_t)row * p.ldo + t.n * BN;
+#pragma unroll 1
+  for (int c0 = 0; c0 < BN; c0 += 32) {
+    uint32_t a[32];
+    tmem_ld32(tbase + c0, a);
+    tmem_ld_wait();
+    if (valid) {
+      float of[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) of[i] = g * __uint_as_float(a[i]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(orow + c0 + q * 8) = pack8(of + q * 8);
     }
   }
 }
@@ -484,49 +539,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = t.row0 + r;   // SEG_M / DENSE output row
       const bool valid = row < t.row_end;
       if (EPI == EPI_SWIGLU) {
-        bf16* hrow = (bf16*)p.out + (size_t)row * p.ldo + t.n * (BN / 2);
-        bf16* uvrow = p.uv ? p.uv + (size_t)row * p.ld_uv + t.n * BN : nullptr;
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN / 2; c0 += 32) {
-          uint32_t u[32], v[32];
-          tmem_ld32(tbase + c0, u);
-          tmem_ld32(tbase + BN / 2 + c0, v);
-          tmem_ld_wait();
-          if (valid) {
-            float hf[32], uf[32], vf[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              uf[i] = __uint_as_float(u[i]);
-              vf[i] = __uint_as_float(v[i]);
-              hf[i] = silu_f(uf[i]) * vf[i];
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(hrow + c0 + q * 8) = pack8(hf + q * 8);
-            if (uvrow) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                *reinterpret_cast<uint4*>(uvrow + c0 + q * 8) = pack8(uf + q * 8);
-                *reinterpret_cast<uint4*>(uvrow + BN / 2 + c0 + q * 8) = pack8(vf + q * 8);
-              }
-            }
-          }
-        }
+        epi_swiglu<BN>(p, t, tbase, row, valid);
       } else if (EPI == EPI_GATE || EPI == EPI_STORE) {
-        const float g = (EPI == EPI_GATE && valid) ? p.row_gate[row] : 1.f;
-        bf16* orow = (bf16*)p.out + (size_t)row * p.ldo + t.n * BN;
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-          uint32_t a[32];
-          tmem_ld32(tbase + c0, a);
-          tmem_ld_wait();
-          if (valid) {
-            float of[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) of[i] = g * __uint_as_float(a[i]);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(orow + c0 + q * 8) = pack8(of + q * 8);
-          }
-        }
+        epi_scale_store<BN, EPI == EPI_GATE>(p, t, tbase, row, valid);
       } else if (EPI == EPI_F32) {
         float* obase = p.ksplit > 1 ? p.part + (size_t)t.ks * p.dense_rows * p.ldo : (float*)p.out;
         float* orow = obase + (size_t)row * p.ldo + t.n * BN;
@@ -739,6 +754,247 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------------------- fused expert kernel
+// The forward's two expert GEMMs in one persistent launch: the gate/up tiles, then the down tiles,
+// taken from one static order (CTA b takes entries b, b + grid, ...), so a CTA that runs out of
+// gate/up tiles goes straight on to down tiles instead of idling through the gate/up tail and a
+// kernel boundary. A down tile of (segment e, m-tile m) needs the h rows that all gate/up tiles of
+// (e, m) write: each epilogue warp of a gate/up tile adds 1 to dep[mt_off[e] + m] once its rows
+// are stored (and to done[2]), and the producer issuing the down tile's loads waits (acquire,
+// bounded) for kEpiWarps x gate/up n-tiles arrivals, or sees done[2] complete. Every dependency
+// points to an earlier entry of the order and every CTA walks its entries in increasing order, so
+// with all CTAs resident (cooperative launch) the waits end. The last CTA to finish (ticket
+// done[1]) zeroes the counters for the next call. Every wait gives up after kWaitLimitNs with
+// MOE_ERR_TIMEOUT.
+struct FusedParams {
+  TcParams gu, dn;       // gate/up and down GEMMs, as for the separate kernels
+  unsigned* dep;         // per m-tile of the segment schedule
+  unsigned* done;        // [1]: CTAs finished; [2]: gate/up-tile epilogue warps finished
+};
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Waits until *p >= need; false (status set) after kWaitLimitNs or once this CTA aborted.
+__device__ __noinline__ bool wait_count(const unsigned* p, unsigned need, volatile int* abort_flag, int* status) {
+  if (ld_acquire_u32(p) >= need) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    __nanosleep(128);
+    if (ld_acquire_u32(p) >= need) return true;
+    if ((i & 15) == 0) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > kWaitLimitNs) {
+        set_error(status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// One warp's arrival on a counter after its global stores (read by other CTAs' TMA loads).
+__device__ __forceinline__ void signal_count(unsigned* p, int lane) {
+  fence_proxy_async_global();
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence();
+    atomicAdd(p, 1u);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    fused_experts_kernel(const __grid_constant__ CUtensorMap tmW13, const __grid_constant__ CUtensorMap tmH,
+                         const __grid_constant__ CUtensorMap tmWd, const __grid_constant__ FusedParams q) {
+  constexpr int BN = 256;
+  using SM = Smem<BN, SCHED_SEG_M, 1>;
+  constexpr int NS = SM::NS;
+  constexpr uint32_t TMEM_COLS = 512;
+  constexpr uint32_t IDESC = idesc_bf16(BM, BN, 0, 0);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* stage_base = smem;
+  uint64_t* bars = (uint64_t*)(smem + NS * SM::STAGE);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + NS);
+  const uint32_t tfull0 = smem_u32(bars + 2 * NS), tempty0 = smem_u32(bars + 2 * NS + 2);
+  const uint32_t drain = smem_u32(bars + 2 * NS + 4);
+  volatile int* abort_flag = (volatile int*)(bars + 2 * NS + 5);
+  uint32_t* tmem_slot = (uint32_t*)(bars + 2 * NS + 6);
+  int* ticket = (int*)(bars + 2 * NS + 7);
+  int* status = q.gu.status;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full0 + 8 * s, kProducerWarps * 32);   // every producer thread arrives on every stage
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, kEpiWarps * 32);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int n_gu = total_tiles<SCHED_SEG_M, 1>(q.gu);
+  const int n_all = n_gu + total_tiles<SCHED_SEG_M, 1>(q.dn);
+  const unsigned gu_arrivals = kEpiWarps * q.gu.n_tiles;   // per m-tile
+
+  if (warp < kProducerWarps) {
+    // ------------------------------------------------------------ producers
+    int it = 0;
+    bool ok = true;
+    bool all_up = false;   // every gate/up tile finished: no down tile needs to wait any more
+    for (int G = blockIdx.x; G < n_all && ok; G += gridDim.x) {
+      const bool up = G < n_gu;
+      const Tile t = up ? map_tile<SCHED_SEG_M, 1>(q.gu, G, 0) : map_tile<SCHED_SEG_M, 1>(q.dn, G - n_gu, 0);
+      const bf16* gsrc[8];
+      uint32_t gbytes[8];
+      if (up) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int r = warp * 32 + j * 4 + (lane >> 3);
+          const int row = t.row0 + r;
+          const bool v = row < t.row_end;
+          const int tok = v ? q.gu.row_token[row] : 0;
+          gsrc[j] = q.gu.A + (size_t)tok * q.gu.lda + (lane & 7) * 8;
+          gbytes[j] = v ? 16u : 0u;
+        }
+      } else if (threadIdx.x == 0 && !all_up) {
+        // the h rows of this m-tile: every gate/up tile of (e, m) finished by all its epilogue warps
+        if (ld_acquire_u32(q.done + 2) >= kEpiWarps * (unsigned)n_gu) all_up = true;
+        else if (!wait_count(q.dep + q.gu.mt_off[t.e] + t.m, gu_arrivals, abort_flag, status)) ok = false;
+        fence_proxy_async_global();
+      }
+      for (int kb = 0; kb < t.nkb && ok; ++kb, ++it) {
+        const int s = it % NS;
+        const uint32_t ph = (it / NS) & 1;
+        if (!mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sa = smem_u32(stage_base + s * SM::STAGE);
+        const uint32_t sb = sa + SM::A_BYTES;
+        if (up)
+          load_stage<BN, A_GATHER_K, B_TMA_K, SCHED_SEG_M, 1, true>(q.gu, &tmW13, &tmW13, t, kb, sa, sb,
+                                                                     full0 + 8 * s, gsrc, gbytes, 0, 0, 0);
+        else
+          load_stage<BN, A_TMA_K, B_TMA_K, SCHED_SEG_M, 1, true>(q.dn, &tmH, &tmWd, t, kb, sa, sb, full0 + 8 * s,
+                                                                  gsrc, gbytes, 0, 0, 0);
+        cp_async_mbar_arrive_noinc(full0 + 8 * s);
+      }
+    }
+    cp_async_wait<0>();
+  } else if (warp == kMmaWarp) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      int it = 0, tcount = 0;
+      bool ok = true;
+      for (int G = blockIdx.x; G < n_all && ok; G += gridDim.x, ++tcount) {
+        const bool up = G < n_gu;
+        const Tile t = up ? map_tile<SCHED_SEG_M, 1>(q.gu, G, 0) : map_tile<SCHED_SEG_M, 1>(q.dn, G - n_gu, 0);
+        const int acc = tcount & 1;
+        if (!mbar_wait(tempty0 + 8 * acc, ((tcount >> 1) & 1) ^ 1, abort_flag, status)) break;
+        tc_fence_after();
+        const uint32_t dcol = tmem_base + acc * BN;
+        for (int kb = 0; kb < t.nkb; ++kb, ++it) {
+          const int s = it % NS;
+          if (!mbar_wait(full0 + 8 * s, (it / NS) & 1, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (up) fence_proxy_async();   // gathered rows (cp.async, generic proxy) seen by the MMA
+          const uint32_t sa = smem_u32(stage_base + s * SM::STAGE);
+          const uint32_t sb = sa + SM::A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_bf16(dcol, desc_kmajor(sa + k * 32), desc_kmajor(sb + k * 32), IDESC, (kb > 0 || k > 0) ? 1u : 0u);
+          mma_commit(empty0 + 8 * s);
+        }
+        if (!ok) break;
+        mma_commit(tfull0 + 8 * acc);
+      }
+      mma_commit(drain);
+      const uint64_t t0 = global_ns();
+      while (!mbar_try_wait(drain, 0)) {
+        if (global_ns() - t0 > kWaitLimitNs) {
+          set_error(status, MOE_ERR_TIMEOUT);
+          break;
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - kProducerWarps;
+    const int r = ew * 32 + lane;
+    int tcount = 0;
+    for (int G = blockIdx.x; G < n_all; G += gridDim.x, ++tcount) {
+      const bool up = G < n_gu;
+      const Tile t = up ? map_tile<SCHED_SEG_M, 1>(q.gu, G, 0) : map_tile<SCHED_SEG_M, 1>(q.dn, G - n_gu, 0);
+      const int acc = tcount & 1;
+      if (!mbar_wait(tfull0 + 8 * acc, (tcount >> 1) & 1, abort_flag, status)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(ew * 32) << 16);
+      const int row = t.row0 + r;
+      const bool valid = row < t.row_end;
+      if (up) {
+        epi_swiglu<BN>(q.gu, t, tbase, row, valid);
+        signal_count(q.dep + q.gu.mt_off[t.e] + t.m, lane);
+        if (lane == 0) atomicAdd(q.done + 2, 1u);
+      } else {
+        epi_scale_store<BN, true>(q.dn, t, tbase, row, valid);
+      }
+      tc_fence_before();
+      mbar_arrive(tempty0 + 8 * acc);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                 : "memory");
+  }
+  // the last CTA to finish zeroes the counters for the next call
+  if (threadIdx.x == 0) {
+    __threadfence();
+    *ticket = (int)atomicAdd(q.done + 1, 1u);
+  }
+  __syncthreads();
+  if (*ticket == (int)gridDim.x - 1) {
+    __threadfence();
+    const int nm = q.gu.mt_off[q.gu.nseg];
+    for (int i = threadIdx.x; i < nm; i += blockDim.x) q.dep[i] = 0;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      q.done[1] = 0;
+      q.done[2] = 0;
+      __threadfence();
+    }
+  }
+}
+
 // -------------------------------------------------------------- host side
 template <int BN, int AMODE, int BMODE, int SCHED, int EPI, int CG = 1>
 cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcParams& p, int grid, cudaStream_t s,
@@ -880,7 +1136,7 @@ cudaError_t launch_tc_router_logits(const Layer& L, const void* x, int T, float*
   return cudaGetLastError();
 }
 
-cudaError_t launch_tc_gateup(const Layer& L, const Bufs& B, const void* x, cudaStream_t s) {
+TcParams gateup_params(const Layer& L, const Bufs& B, const void* x) {
   TcParams p = base_params(L, B);
   p.A = (const bf16*)x;
   p.lda = L.d;
@@ -891,6 +1147,22 @@ cudaError_t launch_tc_gateup(const Layer& L, const Bufs& B, const void* x, cudaS
   p.ldo = L.f;
   p.uv = (bf16*)B.uv;
   p.ld_uv = 2 * L.f;
+  return p;
+}
+
+TcParams down_params(const Layer& L, const Bufs& B) {
+  TcParams p = base_params(L, B);
+  p.K = L.f;
+  p.n_tiles = L.d / kBNdown;
+  p.b_rows_per_seg = L.d;
+  p.out = B.o;
+  p.ldo = L.d;
+  p.row_gate = B.row_gate;
+  return p;
+}
+
+cudaError_t launch_tc_gateup(const Layer& L, const Bufs& B, const void* x, cudaStream_t s) {
+  const TcParams p = gateup_params(L, B, x);
   if (use_pairs(L, B))
     return launch<kBNup, A_GATHER_K, B_TMA_K, SCHED_SEG_M, EPI_SWIGLU, 2>(L.tm_W13_h /*unused*/, L.tm_W13_h, p,
                                                                           L.num_sms, s);
@@ -900,15 +1172,39 @@ cudaError_t launch_tc_gateup(const Layer& L, const Bufs& B, const void* x, cudaS
 cudaError_t launch_tc_down(const Layer& L, const Bufs& B, cudaStream_t s) {
   CUtensorMap th;
   if (!make_tmap(&th, B.h, L.f, B.R, BK, BM)) return cudaErrorInvalidValue;
-  TcParams p = base_params(L, B);
-  p.K = L.f;
-  p.n_tiles = L.d / kBNdown;
-  p.b_rows_per_seg = L.d;
-  p.out = B.o;
-  p.ldo = L.d;
-  p.row_gate = B.row_gate;
+  const TcParams p = down_params(L, B);
   if (use_pairs(L, B)) return launch<kBNdown, A_TMA_K, B_TMA_K, SCHED_SEG_M, EPI_GATE, 2>(th, L.tm_Wd_h, p, L.num_sms, s);
   return launch<kBNdown, A_TMA_K, B_TMA_K, SCHED_SEG_M, EPI_GATE>(th, L.tm_Wd, p, L.num_sms, s);
+}
+
+// A5 + A6 in one persistent cooperative launch (fused_experts_kernel).
+cudaError_t launch_tc_fused_experts(const Layer& L, const Bufs& B, const void* x, cudaStream_t s) {
+  static_assert(kBNup == 256 && kBNdown == 256, "the fused kernel runs 128 x 256 tiles");
+  CUtensorMap th;
+  if (!make_tmap(&th, B.h, L.f, B.R, BK, BM)) return cudaErrorInvalidValue;
+  FusedParams q = {};
+  q.gu = gateup_params(L, B, x);
+  q.dn = down_params(L, B);
+  q.dep = L.dep;
+  q.done = L.dep_done;
+  const int smem = Smem<256, SCHED_SEG_M, 1>::TOTAL;
+  static bool attr = false;
+  if (!attr) {
+    const cudaError_t e = cudaFuncSetAttribute(fused_experts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeCooperative;   // every CTA resident: the dependency waits can end
+  at[0].val.cooperative = 1;
+  cfg.gridDim = dim3(L.num_sms);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fused_experts_kernel, L.tm_W13, th, L.tm_Wd, q);
 }
 
 // B1: r = dy_t Wd[e] (K = d; Wd read MN-major), SwiGLU backward, g*h, gate-gradient partials.

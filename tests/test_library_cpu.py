@@ -65,4 +65,5 @@ def test_null_arguments_rejected(lib):
     assert lib.moe_route(None, None, 1, *([None] * 10)) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_decode(None, None, 1, None, None, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_set_pairs(None, 1) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_set_fused(None, 1) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_status_string(3) == b"workspace or context too small or misaligned"
