@@ -670,11 +670,12 @@ PROFILE_CASES = {
     "dsv3_e32_bf16_fwd_t4096": (moe_synth.DSV3_UNIFORM.with_(name="dsv3_e32_bf16", E=32, T=4096, seed=9), "fwd", 4096),
     "dsv3_e32_mxfp8_chunked_t4096": (moe_synth.DSV3_MXFP8.with_(name="dsv3_e32_mxfp8", E=32, T=4096, chunk=2048,
                                                                 seed=11), "chunked", 4096),
+    "bf16_t2048_fused_fwd": (moe_synth.BF16_T2048, "fwd_fused", 2048),
 }
 
 
 def run_profile_case(args):
-    from mixture_experts_layer_routing_gb300 import MoeLayer, moe_decode
+    from mixture_experts_layer_routing_gb300 import MoeLayer, moe_decode, moe_set_fused
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     import __graft_entry__
@@ -692,7 +693,8 @@ def run_profile_case(args):
         def fn():
             moe_decode(layer.h, xs[it[0] % 8], n, y, ws)
             it[0] += 1
-    elif kind == "fwd":
+    elif kind in ("fwd", "fwd_fused"):
+        moe_set_fused(layer.h, 1 if kind == "fwd_fused" else 0)
         fn = lambda: layer.forward(inp["x"])  # noqa: E731
     else:
         fn = lambda: layer.train_chunked(inp["x"], inp["dy"], slots=1)  # noqa: E731
