@@ -7,7 +7,9 @@
 // kernels, without multi-step staging, cross-warp synchronisation or extra
 // buffers, and the output sits closer to an FP32 reference.
 // Here:
-//   route     warp per (token, expert) router logit; the last block to finish
+//   route     one to eight warps per (token, expert) router logit (split along d
+//             when B x E is small, so that every SM streams part of Wr; the
+//             partial sums are added in warp order); the last block to finish
 //             selects the top-k of every token and lists the used experts U
 //             (ascending, the shared expert last) with their tokens.
 //   gate/up   warp per (expert in U, row i): streams Wg[e][i,:] and Wu[e][i,:]
@@ -77,21 +79,24 @@ constexpr int kBatch = 7;   // 16-byte chunks per lane loaded before they are us
 
 __global__ void __launch_bounds__(kRouteWarps * 32) decode_route_kernel(
     const bf16* __restrict__ x, const bf16* __restrict__ Wr, const float* __restrict__ bias, int B, int d, int E,
-    int k, int S, int router, int renorm, float scale, DecodeWs w, int* counter) {
+    int k, int S, int router, int renorm, float scale, int parts, DecodeWs w, int* counter) {
   griddep_launch();
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-  const int item = blockIdx.x * kRouteWarps + wib;   // (t, e)
+  // `parts` consecutive warps of a block share one (t, e); warp `part` takes the 16-byte chunks
+  // part*32 + lane, + 32*parts, ...
+  const int item = blockIdx.x * (kRouteWarps / parts) + wib / parts, part = wib % parts;
+  __shared__ float red[kRouteWarps];
+  float acc = 0.f;
   if (item < B * E) {
     const int t = item / E, e = item % E;
     const bf16* xr = x + (size_t)t * d;
     const bf16* wr = Wr + (size_t)e * d;
-    const int nchunk = d / 8;
-    float acc = 0.f;
-    for (int cb = lane; cb < nchunk; cb += 32 * kBatch) {
+    const int nchunk = d / 8, step = 32 * parts;
+    for (int cb = part * 32 + lane; cb < nchunk; cb += step * kBatch) {
       uint4 wv[kBatch], xv[kBatch];
 #pragma unroll
       for (int q = 0; q < kBatch; ++q) {
-        const int c = cb + q * 32;
+        const int c = cb + q * step;
         if (c < nchunk) {
           wv[q] = ld_stream(wr + c * 8);
           xv[q] = *reinterpret_cast<const uint4*>(xr + c * 8);
@@ -99,7 +104,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) decode_route_kernel(
       }
 #pragma unroll
       for (int q = 0; q < kBatch; ++q) {
-        if (cb + q * 32 < nchunk) {
+        if (cb + q * step < nchunk) {
           float a[8], b[8];
           unpack8(xv[q], a);
           unpack8(wv[q], b);
@@ -109,7 +114,13 @@ __global__ void __launch_bounds__(kRouteWarps * 32) decode_route_kernel(
       }
     }
     acc = warp_sum(acc);
-    if (lane == 0) w.logits[item] = acc;
+  }
+  if (lane == 0) red[wib] = acc;
+  __syncthreads();
+  if (item < B * E && part == 0 && lane == 0) {
+    float sum = red[wib];
+    for (int q = 1; q < parts; ++q) sum += red[wib + q];
+    w.logits[item] = sum;
   }
   // last block to finish selects experts for every token
   __shared__ int last;
@@ -712,9 +723,13 @@ size_t decode_workspace_bytes(const Layer& L, int B) {
 
 cudaError_t launch_decode_route(const Layer& L, const void* x, int B, void* ws, cudaStream_t s) {
   DecodeWs w = carve(L, B, ws);
-  const int route_blocks = (B * L.E + kRouteWarps - 1) / kRouteWarps;
+  // warps per logit: enough for about eight warps per SM, at most one block's eight
+  int parts = 1;
+  while (parts < kRouteWarps && (long)B * L.E * parts * 2 <= (long)L.num_sms * kRouteWarps) parts *= 2;
+  const int items_per_block = kRouteWarps / parts;
+  const int route_blocks = (B * L.E + items_per_block - 1) / items_per_block;
   decode_route_kernel<<<route_blocks, kRouteWarps * 32, 0, s>>>((const bf16*)x, (const bf16*)L.Wr, L.bias, B, L.d,
-                                                                L.E, L.k, L.S, L.router, L.renorm, L.scale, w,
+                                                                L.E, L.k, L.S, L.router, L.renorm, L.scale, parts, w,
                                                                 L.decode_counter);
   return cudaGetLastError();
 }
