@@ -130,7 +130,11 @@ moe_status moe_forward(moe_handle h, const void* x, int T, void* y, void* ctx, v
 /* Backward of the forward that filled ctx with the same x and T. dy [T, d] is
  * dL/dy. Writes (not accumulates) dx [T, d], dWr [E, d] fp32, and dWg, dWu
  * [E+S, f, d], dWd [E+S, d, f] in the storage type (fp32 for MOE_FP32, else
- * bf16). The selection bias gets no gradient. */
+ * bf16). The selection bias gets no gradient. On the bf16 tensor-core path the
+ * router backward and the dx gather-sum run on a stream of the handle's own,
+ * forked from and joined back into `stream` with events (so the call stays
+ * asynchronous on `stream` and capturable in a CUDA graph); calls on one
+ * handle must therefore come from one host thread at a time. */
 moe_status moe_backward(moe_handle h, const void* x, const void* dy, int T, const void* ctx,
                         void* dx, float* dWr, void* dWg, void* dWu, void* dWd, void* workspace,
                         void* stream);
@@ -232,7 +236,9 @@ moe_status moe_selftest_timeout(moe_handle h, int limit_ms, void* stream);
  * each kernel group that ran (at most max_groups), its name (NUL-terminated,
  * at most 31 characters, in names[32*i]), its kernel launches and the summed
  * milliseconds between its events; then it forgets the records. *n_groups
- * receives the number of groups written. */
+ * receives the number of groups written. While enabled, every kernel runs on
+ * the call's stream (no side-stream overlap in moe_backward), so that each
+ * group's events bracket its own kernels. */
 moe_status moe_profile_enable(moe_handle h, int enable);
 moe_status moe_profile_read(moe_handle h, int max_groups, char* names, long long* launches, double* total_ms,
                             int* n_groups);

@@ -178,6 +178,15 @@ cudaError_t run(moe_handle_s* h, cudaStream_t s, int group, int nk, F&& f) {
   return e;
 }
 
+void destroy_side(moe_handle_s* h) {
+  if (h->ev_dh) cudaEventDestroy(h->ev_dh);
+  if (h->ev_dx) cudaEventDestroy(h->ev_dx);
+  if (h->ev_join) cudaEventDestroy(h->ev_join);
+  if (h->side) cudaStreamDestroy(h->side);
+  h->side = nullptr;
+  h->ev_dh = h->ev_dx = h->ev_join = nullptr;
+}
+
 moe_status check_T(const moe_handle_s* h, int T) {
   if (T < 0 || T > h->cfg.T_max) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
@@ -248,6 +257,27 @@ moe_status backward_body(moe_handle_s* h, const void* x, const void* dy, int T, 
     CK(run(h, s, G_BWD_DX, 1, [&] { return launch_mx_bwd_dx(L, B, s); }));
   } else if (h->tc) {
     CK(run(h, s, G_BWD_DH, 1, [&] { return launch_tc_bwd_dh(L, B, dy, s); }));
+    if (h->side && !h->prof) {
+      // (with per-group profiling on, everything stays on s so that each group's events bracket
+      // its own kernels)
+      // the router backward needs only dY.Wd's gate-gradient partials: it runs on the side stream
+      // beside the dx GEMM (whose CTAs leave an SM's threads, registers and ~35 KB of shared memory
+      // free); the dx gather-sum follows dx there, beside the weight-gradient GEMMs
+      CK(cudaEventRecord(h->ev_dh, s));
+      CK(cudaStreamWaitEvent(h->side, h->ev_dh, 0));
+      const int router_kernels = (L.router == MOE_ROUTER_SOFTMAX && !L.renorm) ? 2 : 3;
+      CK(run(h, h->side, G_ROUTER_BWD, router_kernels,
+             [&] { return launch_router_bwd(L, B, x, dWr, acc, h->side); }));
+      CK(run(h, s, G_BWD_DX, 1, [&] { return launch_tc_bwd_dx(L, B, s); }));
+      CK(cudaEventRecord(h->ev_dx, s));
+      CK(cudaStreamWaitEvent(h->side, h->ev_dx, 0));
+      CK(run(h, h->side, G_DX_GATHER, 1, [&] { return launch_dx_gather(L, B, dx, h->side); }));
+      CK(cudaEventRecord(h->ev_join, h->side));
+      CK(run(h, s, G_BWD_DW13, 1, [&] { return launch_tc_bwd_dw13(L, B, x, dWg, dWu, acc, s); }));
+      CK(run(h, s, G_BWD_DWD, 1, [&] { return launch_tc_bwd_dwd(L, B, dy, dWd, acc, s); }));
+      CK(cudaStreamWaitEvent(s, h->ev_join, 0));
+      return MOE_OK;
+    }
     CK(run(h, s, G_BWD_DX, 1, [&] { return launch_tc_bwd_dx(L, B, s); }));
   } else {
     CK(run(h, s, G_BWD_DH, 1, [&] { return launch_simt_bwd_dh(L, B, dy, s); }));
@@ -368,6 +398,19 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
   L.dep = (unsigned*)(words + 68);
   if (c.prec == MOE_MXFP8) L.G = kGateMx;
   h->tc = (c.prec == MOE_BF16) && tc_supported(L);
+  if (h->tc) {
+    int lo = 0, hi = 0;
+    if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&h->side, cudaStreamNonBlocking, hi) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_dh, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_dx, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess) {
+      destroy_side(h);
+      cudaFree(words);
+      delete h;
+      return MOE_ERR_CUDA;
+    }
+  }
   h->mx = (c.prec == MOE_MXFP8) && mx_supported(L);
   h->tc_router = h->tc || h->mx;
   if (c.prec == MOE_MXFP8 && !h->mx) {
@@ -387,6 +430,7 @@ moe_status moe_destroy(moe_handle h) {
     cudaEventDestroy(r.b);
   }
   for (auto e : h->pool) cudaEventDestroy(e);
+  destroy_side(h);
   cudaFree(h->L.status);
   delete h;
   return MOE_OK;

@@ -20,4 +20,8 @@ struct moe_handle_s {
   long long launches = 0;
   std::vector<ProfRec> recs;
   std::vector<cudaEvent_t> pool;
+  // Backward side stream: the router backward and the dx gather-sum run beside the dx and
+  // weight-gradient GEMMs (fork / join with these events; capturable in a CUDA graph).
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_dh = nullptr, ev_dx = nullptr, ev_join = nullptr;
 };
