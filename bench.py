@@ -718,6 +718,7 @@ def run_extra_mxfp8(dev, pk):
         "groups_ms": {k: v[1] / 2 for k, v in prof.items()}}}
     # decode on the E4M3 weights: per expert W13 and Wd codes plus one scale byte per 32
     out.update(decode_lines(layer, spec, dev, pk, "dsv3_mxfp8", 3 * f * d * (1 + 1 / 32)))
+    out["dsv3_mxfp8_decode_vs_grouped_gemm"] = decode_crossover(layer, spec, dev)
     layer.close()
     del layer, inp, g, y
     torch.cuda.empty_cache()
