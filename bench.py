@@ -588,6 +588,7 @@ def decode_lines(layer, spec, dev, pk, tag, expert_bytes, n_batches=16):
         nbytes = float(np.mean(nact)) * expert_bytes + spec.E * spec.d * 2
         t_roof = nbytes / (pk["hbm_gbs"] * 1e9)
         out[f"{tag}_decode_B{B}"] = {
+            "path": "warp-per-output kernels" if B < 8 else "grouped-GEMM forward (from the crossover batch)",
             "tokens_per_s": B / (msb * 1e-3), "ms": msb, "weight_gbs": nbytes / (msb * 1e-3) / 1e9,
             "roofline_ms": t_roof * 1e3, "frac_of_roofline": t_roof * 1e3 / msb,
             "experts_read_mean": float(np.mean(nact)), "batches": n_batches,
@@ -656,7 +657,8 @@ def fused_vs_separate(dev, steps=30):
 def decode_crossover(layer, spec, dev, n_batches=8):
     """Milliseconds per step of the warp-per-output decode kernels and of the grouped-GEMM forward on
     the same B tokens (independent batches in turn), and the smallest B where the GEMM path wins."""
-    from mixture_experts_layer_routing_gb300 import moe_decode, moe_forward
+    from mixture_experts_layer_routing_gb300 import moe_decode, moe_forward, moe_set_decode_crossover
+    moe_set_decode_crossover(layer.h, 65)   # every batch on the warp kernels for this comparison
     rows = {}
     cross = None
     for B in (1, 2, 4, 8, 16, 32, 64):
@@ -678,7 +680,9 @@ def decode_crossover(layer, spec, dev, n_batches=8):
         rows[str(B)] = {"decode_ms": md, "grouped_gemm_ms": mg}
         if cross is None and mg < md:
             cross = B
-    return {"ms": rows, "gemm_faster_from_B": cross}
+    moe_set_decode_crossover(layer.h, 8)
+    return {"ms": rows, "gemm_faster_from_B": cross,
+            "note": "decode_ms: warp-per-output kernels forced; moe_decode itself switches to the GEMMs from B = 8"}
 
 
 def run_extra_mxfp8(dev, pk):

@@ -24,7 +24,8 @@ MOE_FP32, MOE_BF16, MOE_MXFP8 = 0, 1, 2
 EXPORTED = ("moe_create", "moe_destroy", "moe_workspace_size", "moe_set_weights", "moe_route", "moe_forward",
             "moe_backward", "moe_decode", "moe_get_status", "moe_profile_enable", "moe_profile_read",
             "moe_launch_count", "moe_route_noalloc", "moe_train_chunked_sizes", "moe_train_chunked",
-            "moe_selftest_timeout", "moe_set_pairs", "moe_set_fused", "moe_status_string")
+            "moe_selftest_timeout", "moe_set_pairs", "moe_set_fused", "moe_set_decode_crossover",
+            "moe_status_string")
 
 
 class MoeError(RuntimeError):
@@ -71,6 +72,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_train_chunked.argtypes = [vp, vp, vp, i32] + [vp] * 7 + [sz, vp, P(i32), vp]
     lib.moe_set_pairs.argtypes = [vp, i32]
     lib.moe_set_fused.argtypes = [vp, i32]
+    lib.moe_set_decode_crossover.argtypes = [vp, i32]
     lib.moe_status_string.argtypes = [i32]
     lib.moe_status_string.restype = ctypes.c_char_p
     for name in EXPORTED[:-1]:
@@ -184,6 +186,11 @@ def moe_set_pairs(h, mode: int):
 def moe_set_fused(h, on: int):
     """Forward expert part (gate/up, down, combine) as one persistent kernel (1) or three launches (0)."""
     _check(load_library().moe_set_fused(h, on), "moe_set_fused")
+
+
+def moe_set_decode_crossover(h, b_min: int):
+    """Batch size from which moe_decode takes the grouped-GEMM forward (default 8; 65: never)."""
+    _check(load_library().moe_set_decode_crossover(h, b_min), "moe_set_decode_crossover")
 
 
 def moe_get_status(h, stream=None) -> int:

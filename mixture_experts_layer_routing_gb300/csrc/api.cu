@@ -648,6 +648,9 @@ moe_status moe_decode(moe_handle h, const void* x, int B, void* y, void* workspa
   if (!aligned16(x) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   const Layer& L = h->L;
+  // from the crossover batch on, the tensor-core grouped GEMMs beat the warp-per-output kernels
+  // (their per-token FMA work grows with B; the GEMMs read each expert's weights once)
+  if (B >= h->decode_gemm_from && (h->tc || h->mx)) return forward_body(h, x, B, y, nullptr, workspace, s);
   CK(run(h, s, G_DECODE_ROUTE, 1, [&] { return launch_decode_route(L, x, B, workspace, s); }));
   if (L.prec == MOE_MXFP8) {
     CK(run(h, s, G_MX_QUANT, 1, [&] { return launch_decode_quant_x_mx(L, x, B, workspace, s); }));
@@ -658,6 +661,12 @@ moe_status moe_decode(moe_handle h, const void* x, int B, void* y, void* workspa
   }
   CK(run(h, s, G_DECODE_GATEUP, 1, [&] { return launch_decode_gateup(L, x, B, workspace, s); }));
   CK(run(h, s, G_DECODE_DOWN, 1, [&] { return launch_decode_down(L, B, y, workspace, s); }));
+  return MOE_OK;
+}
+
+moe_status moe_set_decode_crossover(moe_handle h, int b_min) {
+  if (!h || b_min < 1 || b_min > kMaxDecodeB + 1) return MOE_ERR_INVALID_ARG;
+  h->decode_gemm_from = b_min;
   return MOE_OK;
 }
 

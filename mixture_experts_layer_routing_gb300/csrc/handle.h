@@ -22,6 +22,8 @@ struct moe_handle_s {
   std::vector<cudaEvent_t> pool;
   // Backward side stream: the router backward and the dx gather-sum run beside the dx and
   // weight-gradient GEMMs (fork / join with these events; capturable in a CUDA graph).
+  // moe_decode runs the grouped-GEMM forward for B >= decode_gemm_from (the measured crossover)
+  int decode_gemm_from = moe::kDecodeGemmFrom;
   cudaStream_t side = nullptr;
   cudaEvent_t ev_dh = nullptr, ev_dx = nullptr, ev_join = nullptr;
 };

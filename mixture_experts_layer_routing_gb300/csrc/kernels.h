@@ -19,6 +19,7 @@ constexpr int kDenseTiles = 8;    // segments with this many M-tiles or more are
 constexpr int kGate = 128;        // gate/up interleave block of the packed bf16 W13 (rows)
 constexpr int kGateMx = 64;       // gate/up interleave block of the MXFP8 W13 (rows)
 constexpr int kMaxDecodeB = 64;
+constexpr int kDecodeGemmFrom = 8;   // batch size from which moe_decode takes the grouped-GEMM forward
 
 // Shape of one layer and the pointers that stay fixed after moe_set_weights.
 struct Layer {

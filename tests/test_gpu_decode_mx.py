@@ -1,4 +1,5 @@
-"""Small-batch decode of an MXFP8 layer (warp-per-output kernels on E4M3 weights).
+"""Small-batch decode of an MXFP8 layer (warp-per-output kernels on E4M3 weights, and from the
+crossover batch the grouped-GEMM forward).
 
 Decode is the MXFP8 layer forward on B tokens: x quantised along d, the
 weights along each product's K, h along f. Checked against the oracle's
@@ -37,11 +38,18 @@ def layer_and_inputs():
     layer.close()
 
 
+@pytest.mark.parametrize("path", ["warp", "crossover"])
 @pytest.mark.parametrize("B", [1, 3, 16, 64])
-def test_mx_decode_parity(layer_and_inputs, B):
+def test_mx_decode_parity(layer_and_inputs, B, path):
+    """path "warp": the warp-per-output kernels at every B; "crossover": the default, where
+    moe_decode takes the grouped-GEMM forward from B = 8 (then equal to moe_forward bit for bit)."""
+    from mixture_experts_layer_routing_gb300 import moe_set_decode_crossover
     layer, g, n = layer_and_inputs
+    moe_set_decode_crossover(layer.h, 65 if path == "warp" else 8)
     x = g["x"][:B].contiguous()
     y = layer.decode(x)
+    if path == "crossover" and B >= 8:
+        assert torch.equal(y, layer.forward(x))
     y2 = layer.decode(x)
     logits = layer.route(x)["logits"].cpu().numpy()
     torch.cuda.synchronize()

@@ -66,4 +66,5 @@ def test_null_arguments_rejected(lib):
     assert lib.moe_decode(None, None, 1, None, None, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_set_pairs(None, 1) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_set_fused(None, 1) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_set_decode_crossover(None, 8) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_status_string(3) == b"workspace or context too small or misaligned"
