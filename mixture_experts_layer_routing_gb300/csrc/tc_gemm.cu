@@ -42,7 +42,7 @@ constexpr int kProducerWarps = 4, kEpiWarps = 4;
 constexpr int kThreads = (kProducerWarps + kEpiWarps + 1) * 32;   // 288
 constexpr int kMmaWarp = kProducerWarps + kEpiWarps;               // warp 8
 
-enum { A_GATHER_K = 0, A_TMA_K = 1, A_TMA_MN = 2 };
+enum { A_GATHER_K = 0, A_TMA_K = 1, A_TMA_MN = 2, A_GATHER_MN = 3 };
 enum { B_TMA_K = 0, B_TMA_MN = 1, B_GATHER_MN = 2 };
 enum { SCHED_SEG_M = 0, SCHED_DENSE = 1, SCHED_SEG_K = 2 };
 enum { EPI_SWIGLU = 0, EPI_GATE = 1, EPI_F32 = 2, EPI_DH = 3, EPI_STORE = 4, EPI_DW13 = 5, EPI_DWD = 6 };
@@ -64,7 +64,7 @@ struct TcParams {
   int b_rows_per_seg;     // B by TMA: first row of segment e is e * b_rows_per_seg (SEG_M / DENSE)
   void* out;              // primary output (see the epilogues)
   int ldo;
-  int n_valid;            // EPI_F32: columns to store
+  int n_valid;            // EPI_F32, EPI_DWD: columns to store
   void* out2;             // EPI_DH: g*h [R, f]; EPI_DW13: dWu
   const float* row_gate;  // EPI_GATE, EPI_DH
   bf16* uv;               // EPI_SWIGLU: saved pre-activations (nullable); EPI_DH: read
@@ -205,8 +205,8 @@ struct Smem {
 
 template <int AMODE, int BMODE>
 struct Modes {
-  static constexpr bool kCpAsync = AMODE == A_GATHER_K || BMODE == B_GATHER_MN;
-  static constexpr int kAMn = AMODE == A_TMA_MN ? 1 : 0;
+  static constexpr bool kCpAsync = AMODE == A_GATHER_K || AMODE == A_GATHER_MN || BMODE == B_GATHER_MN;
+  static constexpr int kAMn = (AMODE == A_TMA_MN || AMODE == A_GATHER_MN) ? 1 : 0;
   static constexpr int kBMn = (BMODE == B_TMA_MN || BMODE == B_GATHER_MN) ? 1 : 0;
 };
 
@@ -252,6 +252,20 @@ __device__ __forceinline__ void load_stage(const TcParams& p, const CUtensorMap*
       const int r = warp * 32 + j * 4 + (lane >> 3);
       const int c = lane & 7;
       cp_async16(sa + r * 128 + ((c ^ (r & 7)) << 4), gsrc[j] + kb * BK, gbytes[j]);
+    }
+  }
+  if (AMODE == A_GATHER_MN) {
+    // 128 M columns of K row 16w + rr (token ktok of lane rr) = 2 lines: two rows per instruction
+    const int warp = ptid >> 5, lane = ptid & 31;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rr = 2 * i + (lane >> 4);
+      const int kk = 16 * warp + rr;
+      const int tok = __shfl_sync(0xffffffffu, ktok, rr);
+      const bool v = t.row0 + kb * BK + kk < t.row_end;
+      const int j = (lane >> 3) & 1, q = lane & 7;
+      const bf16* src = p.A + (size_t)tok * p.lda + t.m * BM + j * 64 + q * 8;
+      cp_async16(sa + j * kChunkBytes + kk * 128 + ((q ^ (kk & 7)) << 4), src, v ? 16u : 0u);
     }
   }
   if (BMODE == B_GATHER_MN) {
@@ -421,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // GATHER_MN: the token index of each gathered K row is loaded two blocks ahead so the L2
       // round trip overlaps the pipeline.
-      constexpr bool kTokRing = BMODE == B_GATHER_MN;
+      constexpr bool kTokRing = AMODE == A_GATHER_MN || BMODE == B_GATHER_MN;
       int tk0 = 0, tk1 = 0, tk2 = 0;
       auto tok_at = [&](int kb) {
         // lane l < 16 of warp w: token of K row 16w + l of block kb
@@ -606,82 +620,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-      } else if (EPI == EPI_DWD) {
-        // dWd[e] computed transposed: TMEM lane = feature (this warp: features f0 .. f0+31),
-        // column = model dimension. Each 64-column sub-tile leaves through a 64 x 32 staging buffer
-        // (a row per model dimension, 64 bytes of features), stored by TMA into dWd[e][d][f].
-        // Lane pairs swap values so that each lane writes whole 32-bit words (two features): for
-        // column pair (2i, 2i+1) the even lane keeps column 2i and the odd lane column 2i+1.
-        const bool empty = t.nkb == 0;
-        const int f0 = t.m * BM + ew * 32;
-        const int odd = lane & 1;
-        const int drow0 = t.e * p.ldb + t.n * BN;   // dWd row of the tile's first model dimension
-        const uint32_t wbuf = smem_u32(out_stage) + ew * 2 * 4096;
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 64) {
-          const int sub = c0 >> 6;
-          const uint32_t buf = wbuf + (sub & 1) * 4096;
-          float of[64];
-          if (!empty) {
-            uint32_t a[32], b[32];
-            tmem_ld32(tbase + c0, a);
-            tmem_ld32(tbase + c0 + 32, b);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              of[i] = __uint_as_float(a[i]);
-              of[32 + i] = __uint_as_float(b[i]);
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 64; ++i) of[i] = 0.f;
-          }
-          uint32_t old[32];
-          if (p.accumulate) {
-            const bf16* base = (const bf16*)p.out + (size_t)(drow0 + c0 + odd) * p.ldo + f0 + (lane & ~1);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) old[i] = *reinterpret_cast<const uint32_t*>(base + (size_t)(2 * i) * p.ldo);
-          }
-          uint32_t w[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float send = odd ? of[2 * i] : of[2 * i + 1];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-            float lo = odd ? recv : of[2 * i];       // feature f0 + (lane & ~1)
-            float hi = odd ? of[2 * i + 1] : recv;   // the next feature
-            if (p.accumulate) {
-              lo += __uint_as_float(old[i] << 16);
-              hi += __uint_as_float(old[i] & 0xffff0000u);
-            }
-            w[i] = pack2(lo, hi);
-          }
-          // the store that last read this buffer (two sub-tiles ago) must have finished reading it
-          if (lane == 0) bulk_wait_read<1>();
-          __syncwarp();
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            asm volatile("st.shared.b32 [%0], %1;" ::"r"(buf + (2 * i + odd) * 64 + (lane >> 1) * 4), "r"(w[i])
-                         : "memory");
-          fence_proxy_async();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmC, f0, drow0 + c0, buf);
-            bulk_commit();
-          }
-        }
       } else {
-        // dW13: each warp writes its 32 rows of the tile as 32x64 sub-tiles through a
-        // double-buffered 128-byte-swizzled staging buffer, stored by TMA.
+        // Weight gradients (dW13, dWd): each warp writes its 32 rows of the tile as 32x64 sub-tiles
+        // through a double-buffered 128-byte-swizzled staging buffer, stored by TMA.
         const bool empty = t.nkb == 0;
         const CUtensorMap* tmo = &tmC;
-        // an M tile of 128 packed rows is all gate rows (m even, dWg) or all up rows (m odd, dWu)
-        if (t.m & 1) tmo = &tmC2;
-        const int orow0 = t.e * (p.m_tiles / 2) * BM + (t.m >> 1) * BM + ew * 32;
+        // dW13: an M tile of 128 packed rows is all gate rows (m even, dWg) or all up rows (m odd,
+        // dWu); dWd: one plane, and a last n-tile may run past the n_valid columns (its B columns
+        // were zero-filled): sub-tiles at or beyond them are not stored
+        if (EPI == EPI_DW13 && (t.m & 1)) tmo = &tmC2;
+        const int orow0 = EPI == EPI_DW13 ? t.e * (p.m_tiles / 2) * BM + (t.m >> 1) * BM + ew * 32
+                                          : (t.e * p.m_tiles + t.m) * BM + ew * 32;
         const uint32_t wbuf = smem_u32(out_stage) + ew * 2 * 4096;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 64) {
           const int sub = c0 >> 6;
           const uint32_t buf = wbuf + (sub & 1) * 4096;
+          if (EPI == EPI_DWD && t.n * BN + c0 >= p.n_valid) break;
           float of[64];
           if (!empty) {
             uint32_t a[32], b[32];
@@ -698,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 64; ++i) of[i] = 0.f;
           }
           if (p.accumulate) {
-            const bf16* base = (t.m & 1) ? (const bf16*)p.out2 : (const bf16*)p.out;
+            const bf16* base = (EPI == EPI_DW13 && (t.m & 1)) ? (const bf16*)p.out2 : (const bf16*)p.out;
             const bf16* old = base + (size_t)(orow0 + lane) * p.ldo + t.n * BN + c0;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -1266,23 +1221,23 @@ cudaError_t launch_tc_bwd_dw13(const Layer& L, const Bufs& B, const void* x, voi
                                                                        &tu);
 }
 
-// B3: dWd[e] = dy_seg^T (g h)_seg, K over the expert's sorted rows. Computed as its transpose,
-// (g h)_seg^T dy_seg: 128 features by 256 model dimensions per tile (the dW13 kernel's shape, half
-// the tiles of 128 x 128 ones), transposed on the way out.
+// B3: dWd[e] = dy_seg^T (g h)_seg, K over the expert's sorted rows: 128 model dimensions (dY rows
+// gathered by token, MN-major) by 256 features (g h by TMA) per tile, the dW13 kernel's shape; the
+// last feature tile of an odd number of 128-feature blocks runs half empty.
 cudaError_t launch_tc_bwd_dwd(const Layer& L, const Bufs& B, const void* dy, void* dWd, bool acc, cudaStream_t s) {
   CUtensorMap thg, td;
   if (!make_tmap(&thg, B.hg, L.f, B.R, 64, BK)) return cudaErrorInvalidValue;
-  if (!make_tmap(&td, dWd, L.f, (uint64_t)(L.E + L.S) * L.d, 32, 64, 2, /*swizzle=*/false))
-    return cudaErrorInvalidValue;
+  if (!make_tmap(&td, dWd, L.f, (uint64_t)(L.E + L.S) * L.d, 64, 32)) return cudaErrorInvalidValue;
   TcParams q = base_params(L, B);
-  q.Bsrc = (const bf16*)dy;
-  q.ldb = L.d;
-  q.m_tiles = L.f / BM;
-  q.n_tiles = L.d / kBNdwd;
+  q.A = (const bf16*)dy;
+  q.lda = L.d;
+  q.m_tiles = L.d / BM;
+  q.n_tiles = (L.f + kBNdwd - 1) / kBNdwd;
+  q.n_valid = L.f;
   q.out = dWd;
   q.ldo = L.f;
   q.accumulate = acc ? 1 : 0;
-  return launch<kBNdwd, A_TMA_MN, B_GATHER_MN, SCHED_SEG_K, EPI_DWD>(thg, thg /*unused*/, q, L.num_sms, s, &td);
+  return launch<kBNdwd, A_GATHER_MN, B_TMA_MN, SCHED_SEG_K, EPI_DWD>(thg /*unused*/, thg, q, L.num_sms, s, &td);
 }
 
 }  // namespace moe
