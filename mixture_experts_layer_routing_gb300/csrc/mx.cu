@@ -635,7 +635,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           fence_proxy_async();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(tmo, t.n * MBN + c0, orow0, buf);
+            tma_store_2d_hint(tmo, t.n * MBN + c0, orow0, buf, policy_evict_first());
             bulk_commit();
           }
         }
