@@ -2,7 +2,8 @@
 //
 // One persistent kernel template serves every GEMM of the layer: the router
 // logits, both expert projections of the forward pass, and the four grouped
-// products of the backward pass. Per CTA (one per SM):
+// products of the backward pass (fused_experts_kernel, further down, runs the
+// forward's two expert GEMMs in one launch). Per CTA (one per SM):
 //   warps 0-3  producers: operands pulled by token index with 16-byte cp.async
 //              into the 128-byte-swizzled layout the MMA reads (the dispatch
 //              never materialises a permuted copy of x or dy), or loaded by TMA
@@ -15,10 +16,12 @@
 // along M or N, K the row index): the backward reads the weights transposed
 // and reduces the weight gradients over each expert's token segment without
 // any transposed copy.
-// Schedules: SEG_M, tiles (segment, n-tile, m-tile) over the sorted rows of
-// each expert with m fastest, so CTAs running together share an expert's
-// weight tile through L2; DENSE, one segment; SEG_K, tiles (segment, n, m) of
-// a per-expert weight gradient whose K runs over that expert's sorted rows.
+// Schedules: SEG_M, tiles over the sorted rows of each expert in groups of 16
+// m-tiles (every n-tile of a group before the next), so CTAs running together
+// share an expert's weight and row tiles through L2, experts with many and few
+// tiles interleaved when both are numerous; DENSE, one segment, optionally
+// split over K; SEG_K, tiles (segment, n, m) of a per-expert weight gradient
+// whose K runs over that expert's sorted rows.
 //
 // Pull dispatch and one fused, deterministic call per step follow "Cursor
 // открыл код ядра Mixture of Experts ..." (dzen.guru), section "Три решения,

@@ -69,12 +69,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(cluster_bar)
       : "memory");
 }
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, int c0, int c1, uint32_t src) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                   reinterpret_cast<uint64_t>(tm)),
-               "r"(c0), "r"(c1), "r"(src)
-               : "memory");
-}
 // L2 policy for data that is written once and not read again in the step (the weight gradients):
 // evicted first, so that it does not push reused operand tiles out of L2.
 __device__ __forceinline__ uint64_t policy_evict_first() {
@@ -82,7 +76,7 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
-// tma_store_2d with an L2 cache policy.
+// TMA store of a 2-D box from shared memory (bulk group), with an L2 cache policy.
 __device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* tm, int c0, int c1, uint32_t src, uint64_t pol) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;" ::"l"(
                    reinterpret_cast<uint64_t>(tm)),
