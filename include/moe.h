@@ -26,11 +26,13 @@
  *
  * Conventions for every call:
  *  - Pointers named "device" must be device memory; the caller owns all of it.
- *    The library never allocates device memory except the small status word in
- *    moe_create. Scratch comes from the caller's `workspace` (sizes from
- *    moe_workspace_size), 256-byte aligned.
+ *    The library never allocates device memory except one small array in
+ *    moe_create (the status word and a few counters). Scratch comes from the
+ *    caller's `workspace` (sizes from moe_workspace_size), 256-byte aligned.
  *  - Every compute call only enqueues work on `stream` (a cudaStream_t passed
- *    as void*; NULL = legacy default stream) and never synchronises the host.
+ *    as void*; NULL = legacy default stream) and never synchronises the host
+ *    (moe_backward forks part of its work to a stream of the handle and joins
+ *    it back into `stream` with events).
  *  - Arguments are validated on the host first; a bad argument returns an
  *    error code and launches nothing. Launch failures return MOE_ERR_CUDA.
  *    Errors detected on the device (an index out of range, a pipeline wait
@@ -84,8 +86,11 @@ typedef struct {
 } moe_config;
 
 /* Create a handle for one layer shape on the current CUDA device. Validates
- * the config (MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED) and allocates the
- * device status word (the library's only allocation). */
+ * the config (MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED) and allocates one
+ * small device array (the status word, the decode router's counter and the
+ * fused kernel's per-row-block counters: 4 x (T_max (k+S) / 128 + E + S + 68)
+ * bytes, the library's only allocation); on the bf16 tensor-core path it also
+ * creates one stream and three events for moe_backward's side work. */
 moe_status moe_create(const moe_config* cfg, moe_handle* out);
 moe_status moe_destroy(moe_handle h);
 
