@@ -517,11 +517,16 @@ def run_ours(args):
         out["extra"] = run_extra(args, dev, pk)
     if rank == 0 and not args.no_cpu_baseline:
         n = oracle_inputs(moe_synth.make_inputs(spec, "cpu", grad=True))
-        ntok = args.cpu_tokens
-        dt = cpu_baseline(spec, n, ntok)
+        ntok = min(args.cpu_tokens, spec.T)
+        # whole passes over the sample until at least --cpu-seconds of host time have gone by
+        times = []
+        while not times or (sum(times) < args.cpu_seconds and len(times) < 16):
+            times.append(cpu_baseline(spec, n, ntok))
+        dt = float(np.mean(times))
+        what = f"the whole {spec.T}-token" if ntok == spec.T else f"the first {ntok} of {spec.T} tokens'"
         out["cpu_baseline"] = {"value": ntok / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
-                               "sample": f"fwd+bwd of the first {ntok} of {spec.T} tokens (all experts' weights), "
-                                         f"{dt:.1f} s"}
+                               "sample": f"{what} fwd+bwd (all experts' weights), {len(times)} passes of "
+                                         f"{dt:.1f} s each, mean"}
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -821,7 +826,7 @@ def run_reference(args):
         return
     spec = moe_synth.BF16_T2048
     n = oracle_inputs(moe_synth.make_inputs(spec, "cpu", grad=True))
-    ntok = args.ref_tokens
+    ntok = min(args.ref_tokens, spec.T)
     for _ in range(args.warmup):
         cpu_baseline(spec, n, ntok)
     times = [cpu_baseline(spec, n, ntok) for _ in range(args.steps)]
@@ -833,7 +838,8 @@ def run_reference(args):
            "config": {"workload": spec.name + " fwd+bwd", "T": spec.T, "d": spec.d, "E": spec.E, "f": spec.f,
                       "k": spec.k, "sample_tokens_per_step": ntok},
            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
-                            "sample": f"fwd+bwd of the first {ntok} of {spec.T} tokens per step"},
+                            "sample": (f"the whole {spec.T}-token fwd+bwd per step" if ntok == spec.T else
+                                       f"fwd+bwd of the first {ntok} of {spec.T} tokens per step")},
            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
 
@@ -846,8 +852,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-tokens", type=int, default=128, help="oracle sample for cpu_baseline")
-    ap.add_argument("--ref-tokens", type=int, default=16, help="oracle sample per reference-arm step")
+    ap.add_argument("--cpu-tokens", type=int, default=2048,
+                    help="tokens of the workload the oracle runs for cpu_baseline (default: all of them)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="cpu_baseline repeats whole oracle passes until this much host time has gone by")
+    ap.add_argument("--ref-tokens", type=int, default=2048,
+                    help="tokens of the workload the oracle runs per reference-arm step (default: all of them)")
     ap.add_argument("--chunk-sweep", action="store_true",
                     help="instead of the bench line: the DeepSeek-V3 MXFP8 fwd+bwd over chunk sizes 1024..8192")
     ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES),
