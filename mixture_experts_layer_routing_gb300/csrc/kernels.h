@@ -15,7 +15,9 @@ constexpr int kChunk = 1024;      // assignments per block of the histogram / pe
 constexpr int kBM = 128;          // rows per M-tile of the grouped GEMMs (segment padding unit)
 constexpr int kRouterSplit = 8;   // most row splits of an expert segment in the router weight gradient
 constexpr int kRouterSplitRows = 256;   // rows per split
-constexpr int kDenseTiles = 4;    // segments with this many M-tiles or more are scheduled as "dense"
+// Segments with kDenseTiles M-tiles or more reuse each weight byte for >= 384 rows, above the
+// bf16 ridge of about 280 flop/byte: candidates for the "dense" tile stream (see scan_kernel).
+constexpr int kDenseTiles = 3;
 constexpr int kGate = 128;        // gate/up interleave block of the packed bf16 W13 (rows)
 constexpr int kGateMx = 64;       // gate/up interleave block of the MXFP8 W13 (rows)
 constexpr int kMaxDecodeB = 64;

@@ -96,19 +96,35 @@ __global__ void __launch_bounds__(512) scan_kernel(const int* __restrict__ chunk
                                                    int* __restrict__ off, int* __restrict__ mt_off) {
   __shared__ int c_s[kMaxE + 1];
   __shared__ int warp_tot[16][5];
+  __shared__ int tot[4];   // all tiles, candidate dense tiles, other tiles, other non-empty segments
   const int tid = threadIdx.x;
   const int nseg = E + S;
+  if (tid < 4) tot[tid] = 0;
   int c = 0;
   if (tid < E) {
     for (int ch = 0; ch < nch; ++ch) c += chunk_hist[(size_t)ch * E + tid];
   } else if (tid == E && S) {
     c = T;
   }
-  // exclusive scans over the 512 threads of: c, ceil(c / kBM) (tiles), ceil(tiles / 2) (pairs),
-  // and the tiles of "dense" segments (>= kDenseTiles tiles) and of the others
   const int lane = tid & 31, w = tid >> 5;
   const int tiles = (c + kBM - 1) / kBM, pairs = (tiles + 1) / 2;
-  const int dense = tiles >= kDenseTiles ? tiles : 0, sparse = tiles - dense;
+  // The GEMM schedule interleaves the tiles of "dense" segments (tensor-bound) with the others
+  // (HBM-bound) only when that mixes two kinds of work: the candidates (>= kDenseTiles tiles) hold
+  // at least a quarter of the tiles and the other non-empty segments average under 1.5 tiles
+  // (<= 192 rows per weight byte pair). Otherwise no segment is dense and the order stays
+  // segment-major; e.g. uniform routing with 2-3 tiles per expert has both kinds near the ridge.
+  const bool cand = tiles >= kDenseTiles;
+  __syncthreads();
+  if (tiles) {
+    atomicAdd(&tot[0], tiles);
+    atomicAdd(&tot[cand ? 1 : 2], tiles);
+    if (!cand) atomicAdd(&tot[3], 1);
+  }
+  __syncthreads();
+  const bool mix = 4 * tot[1] >= tot[0] && 2 * tot[2] < 3 * tot[3];
+  // exclusive scans over the 512 threads of: c, ceil(c / kBM) (tiles), ceil(tiles / 2) (pairs),
+  // and the tiles of dense segments and of the others
+  const int dense = mix && cand ? tiles : 0, sparse = tiles - dense;
   int v[5] = {c, tiles, pairs, dense, sparse};
   const int own[5] = {c, tiles, pairs, dense, sparse};
 #pragma unroll

@@ -152,12 +152,13 @@ __device__ __forceinline__ Tile map_tile(const TcParams& p, int L, int rank) {
     t.nkb = (t.row_end - t.row0 + BK - 1) / BK;
     return t;
   }
-  // Segments with kDenseTiles or more m-tiles ("dense": each weight tile serves many row tiles,
-  // tensor-bound) and the others (each weight tile streamed for a few rows, HBM-bound) form two
-  // tile streams, interleaved in proportion: tile L is dense iff floor((L+1) Nd / N) steps, so
-  // CTAs running at the same time mix both kinds and keep the tensor pipe and HBM busy together.
-  // A dense stream under a quarter of the tiles (uniform routing: only the shared expert) stays in
-  // segment order at the end: spread thin, its weight and row tiles would leave L2 between uses.
+  // Segments marked dense by scan_kernel (each weight tile serves several row tiles: tensor-bound)
+  // and the others (each weight tile streamed for a tile or two of rows: HBM-bound) form two tile
+  // streams, interleaved in proportion: tile L is dense iff floor((L+1) Nd / N) steps, so CTAs
+  // running at the same time mix both kinds and keep the tensor pipe and HBM busy together.
+  // scan_kernel marks none when the mix would not pay (dense under a quarter of the tiles, or the
+  // others near the ridge): then the order is segment-major, which keeps each segment's weight and
+  // row tiles in L2 between uses.
   const int* dn = p.mt_off + 2 * (p.nseg + 1);
   const int* sp = p.mt_off + 3 * (p.nseg + 1);
   const long N = (long)p.mt_off[p.nseg] * p.n_tiles, Nd = (long)dn[p.nseg] * p.n_tiles;
