@@ -2,7 +2,8 @@
 
 * bf16 T=2048, d=2048, E=64, f=1408, top-6, Zipf(1.0) load: forward + backward, every output
   element against the oracle (relative Frobenius error <= 5e-3), routing bit-exact given the
-  GPU's logits, reruns bit-identical.
+  GPU's logits, reruns bit-identical; the step captured in a CUDA graph (as bench.py times it)
+  and replayed on new inputs gives the eager calls' results bit for bit.
 * DeepSeek-V3 shapes (T=8192, d=7168, 256 + 1 experts, f=2048, top-8 sigmoid x 2.5), uniform
   and Zipf(1.2): forward on a sample of tokens. Tokens are independent in the forward, so the
   oracle evaluates only the sampled rows (with the GPU's fp32 logits for those rows, so both
@@ -14,7 +15,7 @@ import pytest
 import torch
 
 import moe_synth
-from mixture_experts_layer_routing_gb300 import MoeLayer
+from mixture_experts_layer_routing_gb300 import MoeLayer, moe_backward, moe_forward
 from oracle import moe_oracle as oracle
 
 pytestmark = pytest.mark.gpu
@@ -79,6 +80,47 @@ def test_bf16_T2048_fwd_bwd_full():
     assert torch.equal(y, y2)
     for name in g:
         assert torch.equal(g[name], g2[name]), name
+    layer.close()
+
+
+def test_bf16_T2048_graph_replay_full():
+    spec = moe_synth.BF16_T2048
+    inp = moe_synth.make_inputs(spec, DEV, grad=True)
+    layer = MoeLayer.from_spec(spec, device=DEV)
+    layer.set_weights(inp["Wr"], inp["b"], inp["Wg"], inp["Wu"], inp["Wd"])
+    T = spec.T
+    x, dy = inp["x"].clone(), inp["dy"].clone()
+    y = torch.empty_like(x)
+    ctx = layer.new_ctx(T)
+    g = layer.grads_like(x)
+    sz = layer.sizes(T)
+    ws, bws = layer.buffer("fwd", sz["fwd_ws"]), layer.buffer("bwd", sz["bwd_ws"])
+
+    def step():
+        moe_forward(layer.h, x, T, y, ctx, ws)
+        moe_backward(layer.h, x, dy, T, ctx, g["dx"], g["dWr"], g["dWg"], g["dWu"], g["dWd"], bws)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for seed_offset in (11, 12):
+        new = moe_synth.make_tokens(spec, 2, DEV, seed_offset=seed_offset)
+        x.copy_(new[0])
+        dy.copy_(new[1])
+        graph.replay()
+        torch.cuda.synchronize()
+        got = {"y": y.clone(), **{k: v.clone() for k, v in g.items()}}
+        step()
+        torch.cuda.synchronize()
+        assert layer.status() == 0
+        assert torch.equal(got["y"], y)
+        for k, v in g.items():
+            assert torch.equal(got[k], v), k
     layer.close()
 
 
