@@ -242,6 +242,26 @@ def test_token_permutation_equivariance_and_duplicates():
     np.testing.assert_allclose(y2, y[p], rtol=1e-13, atol=1e-14)
 
 
+@pytest.mark.parametrize("mx", [False, True])
+def test_token_subset_rows_equal_full_batch(mx):
+    """y and dx rows of a few tokens, evaluated alone (only the experts they reach), match the rows
+    of the whole batch: every operand of a token's y and dx (x, dY, h, du, dv; MXFP8 blocks along
+    each row) belongs to that token. Full-size GPU checks sample tokens on this basis."""
+    L = _layer(12, T=96, d=64, E=6, f=64, S=1, wr=0.5)
+    kw = dict(k=2, router="sigmoid", renorm=True, scale=2.5, n_shared=1, mx=mx)
+    dy = np.random.default_rng(13).standard_normal(L["x"].shape)
+    args = (L["Wr"], L["b"], L["Wg"], L["Wu"], L["Wd"])
+    full_y = oracle.forward(L["x"], *args, **kw)["y"]
+    full = oracle.backward(L["x"], *args, dy, **kw)
+    toks = np.array([3, 50, 95])
+    reached = sorted(set(full["idx"][toks].ravel().tolist()) | {6})
+    sub_y = oracle.forward(L["x"][toks], *args, **kw)["y"]
+    sub = oracle.backward(L["x"][toks], *args, dy[toks], experts=reached, **kw)
+    # equal up to the summation order of the library matmul over a different number of rows
+    np.testing.assert_allclose(sub_y, full_y[toks], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(sub["dx"], full["dx"][toks], rtol=1e-12, atol=1e-13)
+
+
 # ------------------------------------------------------------- backward
 
 def _selection_margin(x, Wr, b, k):
