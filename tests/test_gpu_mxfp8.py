@@ -125,8 +125,9 @@ class DeviceExperts:
 
 
 def test_dsv3_mxfp8_chunked_fullsize_sampled_experts():
-    """DeepSeek-V3 shapes, T=8192 in 2368-token chunks, 512 MB ring: properties at full size and the
-    weight gradients of sampled experts against the oracle (per chunk, summed in backward order)."""
+    """DeepSeek-V3 shapes, T=8192 in 2368-token chunks, 512 MB ring: properties at full size, the
+    weight gradients of sampled experts against the oracle (per chunk, summed in backward order),
+    and the y and dx rows of sampled tokens."""
     spec = moe_synth.DSV3_MXFP8
     inp = moe_synth.make_inputs(spec, DEV, grad=True)
     layer = MoeLayer.from_spec(spec, device=DEV)
@@ -163,4 +164,17 @@ def test_dsv3_mxfp8_chunked_fullsize_sampled_experts():
         for k in ("dWg", "dWu", "dWd"):
             err = oracle.rel_frobenius(np64(keep[k][e]), acc[k][e])
             assert err <= TOL_MX, (e, k, err)
+    # y and dx rows of two tokens, one in the first chunk (recomputed in the backward: the ring holds
+    # fewer slots than there are chunks) and one in the last; every quantised operand of a token's
+    # y and dx is quantised along that token's own row, so the oracle can take the tokens alone
+    bounds = oracle.chunk_bounds(spec.T, spec.chunk)
+    toks = np.array([int(rng.integers(bounds[0][0], bounds[0][1])), int(rng.integers(bounds[-1][0], bounds[-1][1]))])
+    ti = torch.as_tensor(toks, device=DEV)
+    touched = sorted(set(r["idx"][ti].cpu().numpy().ravel().tolist()) | {spec.E})
+    ref = oracle.backward(n["x"][toks], n["Wr"], n["b"], W["Wg"], W["Wu"], W["Wd"], n["dy"][toks],
+                          logits32=logits[toks], mx=True, experts=touched, **kw(spec))
+    y_ref = oracle.forward(n["x"][toks], n["Wr"], n["b"], W["Wg"], W["Wu"], W["Wd"], logits32=logits[toks],
+                           mx=True, **kw(spec))["y"]
+    assert oracle.rel_frobenius(np64(keep["y"][ti]), y_ref) <= TOL_MX
+    assert oracle.rel_frobenius(np64(keep["dx"][ti]), ref["dx"]) <= TOL_MX
     layer.close()
