@@ -55,9 +55,28 @@ def _create(**over):
     (dict(f=96), moe.MOE_ERR_UNSUPPORTED),             # f not a multiple of 64
     (dict(d=100), moe.MOE_ERR_UNSUPPORTED),            # d not a multiple of 8
     (dict(E=300), moe.MOE_ERR_UNSUPPORTED),            # above the routing kernels' expert limit
+    (dict(k=0), moe.MOE_ERR_INVALID_ARG),
+    (dict(d=0), moe.MOE_ERR_INVALID_ARG),
+    (dict(E=0), moe.MOE_ERR_INVALID_ARG),
+    (dict(f=0), moe.MOE_ERR_INVALID_ARG),
+    (dict(prec=7), moe.MOE_ERR_INVALID_ARG),           # unknown precision
+    (dict(route_scale=0.0), moe.MOE_ERR_INVALID_ARG),
+    (dict(route_scale=float("nan")), moe.MOE_ERR_INVALID_ARG),
+    (dict(route_scale=float("inf")), moe.MOE_ERR_INVALID_ARG),
+    (dict(chunk_tokens=-1), moe.MOE_ERR_INVALID_ARG),
+    (dict(prec=2, d=192), moe.MOE_ERR_UNSUPPORTED),     # MXFP8: d not a multiple of 128
+    (dict(prec=2, f=192), moe.MOE_ERR_UNSUPPORTED),     # MXFP8: f not a multiple of 128
+    (dict(T_max=1 << 28, k=4, E=8), moe.MOE_ERR_UNSUPPORTED),   # T*k assignments past 2^30
 ])
 def test_create_rejects_bad_config_on_host(lib, over, code):
     assert _create(**over) == code
+
+
+def test_create_null_pointers_rejected(lib):
+    cfg = moe.moe_config(16, 256, 8, 0, 128, 2, 0, 1, 1.0, 1, 0, 0)
+    h = ctypes.c_void_p()
+    assert lib.moe_create(None, ctypes.byref(h)) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_create(ctypes.byref(cfg), None) == moe.MOE_ERR_INVALID_ARG
 
 
 def test_null_arguments_rejected(lib):
