@@ -59,7 +59,7 @@ typedef struct moe_handle_s* moe_handle;
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1,   /* null pointer, size out of range, k > E, ... */
-  MOE_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement (shape multiple, precision) */
+  MOE_ERR_UNSUPPORTED = 2,   /* valid request the library does not implement (shape multiple, precision) */
   MOE_ERR_WORKSPACE = 3,     /* workspace or context smaller than required / misaligned */
   MOE_ERR_CUDA = 4,          /* a CUDA runtime call failed */
   MOE_ERR_TIMEOUT = 5,       /* device status: a pipeline wait exceeded its limit */
