@@ -233,7 +233,12 @@ moe_status moe_get_status(moe_handle h, void* stream, int* device_status);
  * pad() rounding up to 256; larger T returns MOE_ERR_WORKSPACE before any
  * launch (E = 256, k = 8, S = 1 allows T up to 47,573 tokens).
  * The first call on a device looks up the array's address there; make that
- * first call before any stream capture. Every call on a device shares the one
+ * first call before any stream capture. The address is kept for the life of
+ * the process: after a cudaDeviceReset of that device (which tears down the
+ * context the address belongs to) do not call this entry point there again.
+ * The steps, launch counting and profiling records are moe_route's own: the
+ * same router path (tensor cores for bf16 and MXFP8 layers, CUDA cores for
+ * fp32) and the same split-K order, so every output equals moe_route's. Every call on a device shares the one
  * array and it keeps the last call's contents (each call writes every entry
  * it reads, so none needs clearing); calls whose GPU work overlaps (other
  * streams, other handles) race and must be serialised by the caller. The

@@ -184,7 +184,9 @@ def moe_set_pairs(h, mode: int):
 
 
 def moe_set_fused(h, on: int):
-    """Forward expert part (gate/up, down, combine) as one persistent kernel (1) or three launches (0)."""
+    """Forward expert GEMMs (gate/up and down) as one persistent kernel (1) or two launches (0).
+
+    The combine stays its own launch either way."""
     _check(load_library().moe_set_fused(h, on), "moe_set_fused")
 
 

@@ -192,19 +192,22 @@ moe_status check_T(const moe_handle_s* h, int T) {
   return MOE_OK;
 }
 
-// router logits, top-k, counts, offsets, permutation
+// router logits, top-k, counts, offsets, permutation. part (nullable): where the router GEMM's
+// split-K partials go; by default the forward scratch o, which is not yet written at this point.
 moe_status run_route(moe_handle_s* h, const Bufs& B, const void* x, const float* logits_override,
-                     cudaStream_t s) {
+                     cudaStream_t s, float* part = nullptr, size_t part_bytes = 0) {
   const Layer& L = h->L;
   const float* lg = B.logits;
   if (logits_override) {
     lg = logits_override;
   } else if (h->tc_router) {
-    // the forward scratch o (not yet written) holds the split-K partials of the router GEMM
-    const size_t part_bytes = B.o ? (size_t)B.R * L.d * elem_bytes(L.prec) : 0;
+    if (!part) {
+      part = (float*)B.o;
+      part_bytes = B.o ? (size_t)B.R * L.d * elem_bytes(L.prec) : 0;
+    }
     const int nk = tc_router_splits(L, B.T) > 1 ? 2 : 1;
     CK(run(h, s, G_ROUTER_LOGITS, nk,
-           [&] { return launch_tc_router_logits(L, x, B.T, B.logits, s, (float*)B.o, part_bytes); }));
+           [&] { return launch_tc_router_logits(L, x, B.T, B.logits, s, part, part_bytes); }));
   } else {
     CK(run(h, s, G_ROUTER_LOGITS, 1, [&] { return launch_router_logits(L, x, B.T, B.logits, s); }));
   }
@@ -339,6 +342,13 @@ ChunkPlan chunk_plan(const moe_handle_s* h, int T) {
 }
 
 }  // namespace
+
+// The routing steps of moe_route (same kernels, launch counts and profiling records) with the
+// router's split-K partials in a buffer the caller names: moe_route_noalloc.
+moe_status route_steps(moe_handle_s* h, const Bufs& B, const void* x, float* part, size_t part_bytes,
+                       cudaStream_t s) {
+  return run_route(h, B, x, nullptr, s, part, part_bytes);
+}
 
 extern "C" {
 

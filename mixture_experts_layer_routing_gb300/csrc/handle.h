@@ -27,3 +27,9 @@ struct moe_handle_s {
   cudaStream_t side = nullptr;
   cudaEvent_t ev_dh = nullptr, ev_dx = nullptr, ev_join = nullptr;
 };
+
+// api.cu: the routing steps of moe_route (router logits, top-k, counts, offsets, permutation) into
+// the arrays of B, with the router GEMM's split-K partials in part (part_bytes); the no-allocation
+// entry point runs exactly these steps.
+moe_status route_steps(moe_handle_s* h, const moe::Bufs& B, const void* x, float* part, size_t part_bytes,
+                       cudaStream_t s);

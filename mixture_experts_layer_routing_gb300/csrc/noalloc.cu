@@ -46,7 +46,10 @@ size_t scratch_bytes(const Layer& L, int T) {
 }
 
 // Device addresses of the arrays on device `dev` (the current device): out[0] the routing scratch,
-// out[1] the router partials. Looked up on the first call for that device and remembered.
+// out[1] the router partials. Looked up on the first call for that device and remembered for the
+// life of the process: a cudaDeviceReset (or any teardown of the device's primary context) makes
+// the remembered addresses stale, so a process that resets a device must not call this entry
+// point on that device afterwards.
 cudaError_t scratch_address(int dev, void** out) {
   std::lock_guard<std::mutex> lock(g_mu);
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
@@ -105,12 +108,12 @@ extern "C" moe_status moe_route_noalloc(moe_handle h, const void* x, int T, floa
 
   cudaStream_t s = (cudaStream_t)stream;
   // Every scratch entry the kernels read is written earlier in the same call,
-  // so nothing needs clearing between calls.
-  cudaError_t e = h->tc ? launch_tc_router_logits(L, x, T, logits, s, (float*)addr[1], kRouterPartBytes) : launch_router_logits(L, x, T, logits, s);
-  if (e == cudaSuccess) e = launch_topk(L, logits, T, idx, gate, s);
-  if (e == cudaSuccess) e = launch_scan_permute(L, B, s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(cnt, B.cnt, 4 * (size_t)L.E, cudaMemcpyDeviceToDevice, s);
+  // so nothing needs clearing between calls. The steps are moe_route's own
+  // (same router path for every precision, same split-K order, same launch
+  // counting and profiling records).
+  const moe_status st = route_steps(h, B, x, (float*)addr[1], kRouterPartBytes, s);
+  if (st != MOE_OK) return st;
+  cudaError_t e = cudaMemcpyAsync(cnt, B.cnt, 4 * (size_t)L.E, cudaMemcpyDeviceToDevice, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(off, B.off, 4 * (size_t)(L.E + 1), cudaMemcpyDeviceToDevice, s);
-  h->launches += 2 + (L.S ? 4 : 3);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -20,6 +20,12 @@ pytestmark = pytest.mark.gpu
 
 SPEC = moe_synth.LayerSpec("bf16_T300_d512_E16+1_f256_top4_sigmoid", 300, 512, 16, 1, 256, 4, "sigmoid", True,
                            2.5, "bf16", None, 21)
+# one handle per router path: tensor-core router (bf16, MXFP8 layers) and CUDA-core router (fp32);
+# d and f suit every precision's expert path (multiples of 256 and 128)
+SPECS = {"bf16": SPEC,
+         "mxfp8": SPEC.with_(name="mxfp8_T300_d512_E16+1_f256_top4_sigmoid", dtype="mxfp8", seed=22),
+         "fp32": SPEC.with_(name="fp32_T300_d512_E16+1_f256_top4_softmax", dtype="fp32", router="softmax",
+                            route_scale=1.0, seed=23)}
 
 
 def _outputs(T, E, k, dev):
@@ -32,25 +38,32 @@ def _outputs(T, E, k, dev):
                 inv=torch.full((T * k,), -1, dtype=torch.int32, device=dev))
 
 
-def test_route_noalloc_matches_route_on_two_calls():
+@pytest.mark.parametrize("prec", list(SPECS))
+def test_route_noalloc_matches_route_on_two_calls(prec):
     __graft_entry__.build()
     import mixture_experts_layer_routing_gb300 as moe
+    spec = SPECS[prec]
     dev = torch.device("cuda:0")
-    inp = moe_synth.make_inputs(SPEC, "cpu")
+    inp = moe_synth.make_inputs(spec, "cpu")
     g = {n: v.to(dev) for n, v in inp.items()}
-    layer = moe.MoeLayer.from_spec(SPEC, device=dev)
+    layer = moe.MoeLayer.from_spec(spec, device=dev)
     layer.set_weights(g["Wr"], g["b"], g["Wg"], g["Wu"], g["Wd"])
     for call in range(2):
-        x = moe_synth.make_tokens(SPEC, 1, "cpu", seed_offset=100 + call)[0].to(dev)
+        x = moe_synth.make_tokens(spec, 1, "cpu", seed_offset=100 + call)[0].to(dev)
+        n0 = moe.moe_launch_count(layer.h)
         want = layer.route(x)
-        got = _outputs(SPEC.T, SPEC.E, SPEC.k, dev)
-        moe.moe_route_noalloc(layer.h, x, SPEC.T, got["logits"], got["idx"], got["gate"], got["cnt"],
+        n1 = moe.moe_launch_count(layer.h)
+        got = _outputs(spec.T, spec.E, spec.k, dev)
+        moe.moe_route_noalloc(layer.h, x, spec.T, got["logits"], got["idx"], got["gate"], got["cnt"],
                               got["off"], got["perm"], got["inv"])
+        n2 = moe.moe_launch_count(layer.h)
         torch.cuda.synchronize()
         assert layer.status() == 0
+        # the same kernels as moe_route, counted the same way
+        assert n2 - n1 == n1 - n0, (prec, call, n1 - n0, n2 - n1)
         for name in want:
-            assert torch.equal(got[name], want[name]), (call, name)
-        assert int(got["cnt"].sum()) == SPEC.T * SPEC.k
+            assert torch.equal(got[name], want[name]), (prec, call, name)
+        assert int(got["cnt"].sum()) == spec.T * spec.k
     layer.close()
 
 
