@@ -202,6 +202,65 @@ def work_per_group(spec, cnt, training=True):
     return g
 
 
+def layer_work(spec, cnt, kind="fwd"):
+    """Algorithmic (flops, bytes) of one whole call, from the method's definition.
+
+    FLOPs: the routed expert products (shared expert included; never the dense E-expert FFN that
+    routing avoids) and the router GEMM. Bytes that must move at least once: the weights of the
+    experts that received tokens, the router weight, the activations in and out. What an
+    implementation writes and reads back between its kernels (h, the gated expert outputs before
+    the combine) is not algorithmic work; it shows in the ncu traffic instead.
+    kind "fwd" (also decode: the forward of B tokens) or "fwd+bwd": the backward reads the used
+    experts' weights once more, writes every expert's weight gradients once, reads x and dy, writes
+    dx, and reads the u, v pre-activations the forward saved (written once by the forward).
+    """
+    T, d, E, S, f, k = spec.T, spec.d, spec.E, spec.S, spec.f, spec.k
+    eb = 4 if spec.dtype == "fp32" else 2
+    R = T * k + S * T
+    active = int(np.count_nonzero(np.asarray(cnt)[:E])) + S
+    w_used = active * 3 * f * d * eb
+    fl = 2 * R * 3 * f * d + 2 * T * E * d
+    by = w_used + E * d * eb + 2 * T * d * eb
+    if kind == "fwd":
+        return fl, by
+    fl += 2 * (2 * R * 3 * f * d) + 2 * (2 * T * E * d)
+    by += w_used + (E + S) * 3 * f * d * eb + 3 * T * d * eb + 2 * R * 2 * f * eb
+    return fl, by
+
+
+def roof_line(ms, flops, nbytes, pk, tensor_peak=None):
+    """Whole-call roofline: t_roof = max(flops / tensor peak, bytes / HBM bandwidth), and ms's fraction."""
+    tp = tensor_peak or pk["bf16_tflops"]
+    t_t, t_h = flops / (tp * 1e12), nbytes / (pk["hbm_gbs"] * 1e9)
+    t_roof = max(t_t, t_h)
+    return {"GB": nbytes / 1e9, "TFLOP": flops / 1e12, "roofline_ms": t_roof * 1e3,
+            "bound": "tensor" if t_t >= t_h else "hbm", "frac_of_roofline": t_roof * 1e3 / ms}
+
+
+def host_cpu():
+    """Host CPU model and online core count (the oracle's machine)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as fh:
+                for line in fh:
+                    if line.lower().startswith("model name"):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    import platform
+    return {"model": model or platform.machine(), "nproc": os.cpu_count()}
+
+
 def roofline_entry(group, ms_per_launch, flops, nbytes, pk, traffic=None):
     t_tensor = flops / (pk["bf16_tflops"] * 1e12)
     t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
@@ -357,23 +416,29 @@ class PipelinedE2E:
             comp.wait_event(e)
 
 
-def time_steps(fn, steps, warmup, world):
+def time_steps(fn, steps, warmup, world, stats=None):
+    """Mean milliseconds per step over `steps` timed steps (CUDA events on the current stream, after
+    `warmup` untimed steps, synchronised and barriered on both sides; max over ranks). With a dict
+    `stats`, also fills in the median and the min of the per-step times (an event between steps)."""
     for _ in range(warmup):
         fn()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(steps):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record()
+    for i in range(steps):
         fn()
-    b.record()
+        ev[i + 1].record()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    ms = a.elapsed_time(b) / steps
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    ms = ev[0].elapsed_time(ev[steps]) / steps
     if world > 1:
         ms = reduce_max(ms, "cuda")
+    if stats is not None:
+        stats.update(ms_mean=ms, ms_median=float(np.median(per)), ms_min=float(min(per)), steps=steps)
     return ms
 
 
@@ -423,6 +488,41 @@ def blas_threads():
     return os.cpu_count() or 1
 
 
+def bench_config(spec, world):
+    """The bench line's "config" (the same dict on both arms)."""
+    return {"workload": spec.name + " fwd+bwd", "T": spec.T, "d": spec.d, "E": spec.E, "f": spec.f, "k": spec.k,
+            "router": "softmax top-6 renorm, Zipf(1.0) load bias", "global_batch": spec.T * world,
+            "parallelism": f"replicas x{world}",
+            "l2": "no flush: expert weights (1.11 GB) exceed L2 and stream from HBM every step"}
+
+
+def capture(fn):
+    """fn's launches captured once in a CUDA graph (fn only enqueues work)."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        fn()
+    return graph
+
+
+def r4(v):
+    """v rounded to 4 significant digits (the summary is read from the tail of the output)."""
+    return float(f"{v:.4g}") if isinstance(v, float) else v
+
+
+def summary_row(st, tokens, rl):
+    """One line of the per-workload summary: mean / median / min ms per call, tokens/s from the mean,
+    the algorithmic work (GB, TFLOP), the whole-call roofline and the mean's fraction of it."""
+    row = {"ms": st["ms_mean"], "med": st["ms_median"], "min": st["ms_min"], "tok_s": tokens / (st["ms_mean"] * 1e-3),
+           "GB": rl["GB"], "TF": rl["TFLOP"], "roof_ms": rl["roofline_ms"], "bound": rl["bound"],
+           "frac": rl["frac_of_roofline"]}
+    return {k: r4(v) for k, v in row.items()}
+
+
 def run_ours(args):
     world, rank, local = dist_env()
     if world > 1:
@@ -431,7 +531,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     import __graft_entry__
     __graft_entry__.build()
-    from mixture_experts_layer_routing_gb300 import moe_launch_count
+    from mixture_experts_layer_routing_gb300 import moe_forward, moe_launch_count
     pk = peaks()
     spec = moe_synth.BF16_T2048
     step = TrainStep(spec, dev)
@@ -443,14 +543,11 @@ def run_ours(args):
         step()
     torch.cuda.synchronize()
     n0 = moe_launch_count(step.layer.h)
-    side = torch.cuda.Stream()
-    side.wait_stream(torch.cuda.current_stream())
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=side):
-        step()
-    launches_per_step = moe_launch_count(step.layer.h) - n0
+    graph = capture(step)
+    launches_per_step = (moe_launch_count(step.layer.h) - n0) // 2
+    st = {}
     with ClockSampler(local) as clk:
-        ms = time_steps(graph.replay, args.steps, args.warmup, world)
+        ms = time_steps(graph.replay, args.steps, args.warmup, world, st)
     launches = launches_per_step * args.steps
     ms_eager = time_steps(step, args.steps, args.warmup, world)
     value = world * spec.T / (ms * 1e-3)
@@ -500,21 +597,32 @@ def run_ours(args):
                                "frac": wbytes / (dom_ms * 1e-3) / 1e9 / wpk,
                                "peak_source": "fill of a 1 GiB buffer, CUDA events, this run"}
 
+    # the per-workload summary (last key of the line): the step above, its forward alone, the tiny fp32
+    # layer, and (rank 0) the DeepSeek-V3-shaped workloads
+    summary = {}
+    if rank == 0:
+        fst = {}
+        fwd_graph = capture(lambda: moe_forward(step.layer.h, step.inp["x"], spec.T, step.y, None, step.ws))
+        time_steps(fwd_graph.replay, args.steps, args.warmup, 1, fst)
+        del fwd_graph
+        summary["c0 fp32 T64 fwd"] = tiny_forward_line(dev, pk, args)
+        summary["c1 bf16 T2048 fwd"] = summary_row(fst, spec.T, roof_line(fst["ms_mean"], *layer_work(spec, cnt), pk))
+    summary["c1 bf16 T2048 fwd+bwd (headline)"] = summary_row(st, spec.T, roof_line(
+        ms, *layer_work(spec, cnt, "fwd+bwd"), pk))
+
     out = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-           "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+           "warmup": args.warmup, "ms_per_step": ms, "ms_median": st["ms_median"], "ms_min": st["ms_min"],
+           "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, moe_synth)",
-           "config": {"workload": spec.name + " fwd+bwd", "T": spec.T, "d": spec.d, "E": spec.E, "f": spec.f,
-                      "k": spec.k, "router": "softmax top-6 renorm, Zipf(1.0) load bias", "global_batch": spec.T * world,
-                      "parallelism": f"replicas x{world}",
-                      "l2": "no flush: expert weights (1.11 GB) exceed L2 and stream from HBM every step",
-                      "active_experts": int(np.count_nonzero(cnt)), "max_expert_load": int(cnt.max())},
+           "config": bench_config(spec, world),
+           "routing": {"active_experts": int(np.count_nonzero(cnt)), "max_expert_load": int(cnt.max())},
            "launch": "CUDA graph of the step's C-ABI calls, replayed", "eager_ms_per_step": ms_eager,
-           "e2e": e2e, "gpu_launches": int(launches), "roofline": roof, "kernel_groups": groups,
+           "e2e": e2e, "gpu_launches": int(launches), "kernel_groups": groups,
            "pages_context": PAGES_CONTEXT}
     out["clocks"] = clk.summary()
 
     if rank == 0 and not args.no_extra:
-        out["extra"] = run_extra(args, dev, pk)
+        out["extra"] = run_extra(args, dev, pk, summary)
     if rank == 0 and not args.no_cpu_baseline:
         n = oracle_inputs(moe_synth.make_inputs(spec, "cpu", grad=True))
         ntok = min(args.cpu_tokens, spec.T)
@@ -525,19 +633,48 @@ def run_ours(args):
         dt = float(np.mean(times))
         what = f"the whole {spec.T}-token" if ntok == spec.T else f"the first {ntok} of {spec.T} tokens'"
         out["cpu_baseline"] = {"value": ntok / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                               "host": host_cpu(),
                                "sample": f"{what} fwd+bwd (all experts' weights), {len(times)} passes of "
                                          f"{dt:.1f} s each, mean"}
+    out["roofline"] = roof
+    out["configs"] = summary
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
 
 
-def run_extra(args, dev, pk):
-    """DeepSeek-V3-shaped forward (uniform, Zipf 1.2) and decode B=1/4/16."""
+def tiny_forward_line(dev, pk, args):
+    """The tiny fp32 layer's forward (launch-bound; reported without a target): one C-ABI forward per
+    step, replayed from a CUDA graph, and the eager calls' time beside it."""
+    from mixture_experts_layer_routing_gb300 import MoeLayer, moe_forward
+    spec = moe_synth.TINY_FP32
+    inp = moe_synth.make_inputs(spec, dev)
+    layer = MoeLayer.from_spec(spec, device=dev)
+    layer.set_weights(inp["Wr"], inp["b"], inp["Wg"], inp["Wu"], inp["Wd"])
+    cnt = layer.route(inp["x"])["cnt"].cpu().numpy()
+    y = torch.empty_like(inp["x"])
+    ws = layer.buffer("fwd", layer.sizes(spec.T)["fwd_ws"])
+    fn = lambda: moe_forward(layer.h, inp["x"], spec.T, y, None, ws)  # noqa: E731
+    eager = {}
+    time_steps(fn, args.steps, args.warmup, 1, eager)
+    g = capture(fn)
+    st = {}
+    time_steps(g.replay, args.steps, args.warmup, 1, st)
+    row = summary_row(st, spec.T, roof_line(st["ms_mean"], *layer_work(spec, cnt), pk))
+    row["eager_ms"] = r4(eager["ms_mean"])
+    row["note"] = "launch-bound; no target"
+    del g
+    layer.close()
+    return row
+
+
+def run_extra(args, dev, pk, summary):
+    """DeepSeek-V3-shaped forward (uniform, Zipf 1.2), decode B=1/4/16, the MXFP8 chunked step;
+    their summary rows go into `summary`."""
     from mixture_experts_layer_routing_gb300 import MoeLayer, moe_decode, moe_forward
     extra = {}
-    steps, warm = max(3, args.steps // 2), 3
+    steps, warm = args.steps, 5
     for spec in (moe_synth.DSV3_UNIFORM, moe_synth.DSV3_ZIPF):
         inp = moe_synth.make_inputs(spec, dev)
         layer = MoeLayer.from_spec(spec, device=dev)
@@ -548,31 +685,51 @@ def run_extra(args, dev, pk):
         y = torch.empty_like(inp["x"])
         ws = layer.buffer("fwd", layer.sizes(spec.T)["fwd_ws"])
         fn = lambda: moe_forward(layer.h, inp["x"], spec.T, y, None, ws)  # noqa: E731
+        # the forward's C-ABI call replayed from a CUDA graph, as the headline step; eager beside it
+        graph = capture(fn)
         for _ in range(warm):
-            fn()
+            graph.replay()
+        st = {}
         with ClockSampler(dev.index or 0) as clk:
-            ms = time_steps(fn, steps, 0, 1)
+            ms = time_steps(graph.replay, steps, 0, 1, st)
+        del graph
+        eager = {}
+        time_steps(fn, steps, warm, 1, eager)
         prof = profile_groups(layer.h, fn, steps)
+        fl, by = layer_work(spec, cnt)
+        rl = roof_line(ms, fl, by, pk)
+        # a loop of these 6 ms steps can draw ~1.4 kW and meet the power cap: the sustained bf16 peak
+        # is the denominator for a kernel timed inside such a loop when the clocks show the cap
+        rl_s = roof_line(ms, fl, by, dict(pk, bf16_tflops=pk["bf16_tflops_sustained"]))
+        groups_ms = {g: v[1] / steps for g, v in prof.items()}
         work = work_per_group(spec, cnt, training=False)
-        fl = sum(work[g][0] for g in ("router_logits", "gateup", "down", "combine"))
-        by = sum(work[g][1] for g in ("router_logits", "gateup", "down", "combine"))
-        t_roof = max(fl / (pk["bf16_tflops"] * 1e12), by / (pk["hbm_gbs"] * 1e9))
-        # a loop of these 6 ms steps draws ~1.4 kW and meets the power cap: the sustained bf16 peak
-        # is the denominator for a kernel timed inside such a loop
-        t_roof_s = max(fl / (pk["bf16_tflops_sustained"] * 1e12), by / (pk["hbm_gbs"] * 1e9))
+        dom = max((g for g in groups_ms if g in work), key=lambda g: groups_ms[g])
+        row = summary_row(st, spec.T, rl)
+        dent = roofline_entry(dom, groups_ms[dom], *work[dom], pk, stored_traffic("dsv3_" + dom))
+        cl = clk.summary()
+        row["frac_sustained_peak"] = r4(rl_s["frac_of_roofline"])
+        row["sm_mhz"] = cl["sm_mhz"]
+        row["clock_reasons"] = cl["reasons"]
+        row["dominant"] = {"kernel": dom, "bound": dent["bound"], "frac": r4(dent["frac"])}
+        row["eager_ms"] = r4(eager["ms_mean"])
+        summary["c2 bf16 " + ("uniform" if spec.zipf_s is None else f"zipf{spec.zipf_s}") + " fwd"] = row
         extra[spec.name + " fwd"] = {
-            "tokens_per_s": spec.T / (ms * 1e-3), "ms": ms, "steps": steps, "roofline_ms": t_roof * 1e3,
-            "frac_of_roofline": t_roof * 1e3 / ms, "frac_of_roofline_sustained_peak": t_roof_s * 1e3 / ms,
+            "tokens_per_s": spec.T / (ms * 1e-3), **st, **rl, "eager_ms": eager["ms_mean"],
+            "launch": "CUDA graph of the forward's C-ABI call, replayed",
+            "frac_of_roofline_sustained_peak": rl_s["frac_of_roofline"],
             "clocks": clk.summary(), "active_experts": int(np.count_nonzero(cnt)) + spec.S,
-            "groups_ms": {g: v[1] / steps for g, v in prof.items()}}
+            "groups_ms": groups_ms}
         # decode on the same weights
         if spec is moe_synth.DSV3_UNIFORM:
-            extra.update(decode_lines(layer, spec, dev, pk, "dsv3_bf16", 3 * spec.f * spec.d * 2))
+            dl = decode_lines(layer, spec, dev, pk, "dsv3_bf16", 3 * spec.f * spec.d * 2)
+            extra.update(dl)
+            for key, v in dl.items():
+                summary["c4 bf16 decode B" + key.rsplit("B", 1)[1]] = decode_row(v)
             extra["dsv3_bf16_decode_vs_grouped_gemm"] = decode_crossover(layer, spec, dev)
         layer.close()
         del layer, inp
         torch.cuda.empty_cache()
-    extra.update(run_extra_mxfp8(dev, pk))
+    extra.update(run_extra_mxfp8(dev, pk, summary))
     extra["bf16_T128_d2048_E64_f1408_top6 fwd+bwd, eager vs CUDA graph"] = graph_vs_eager(dev)
     extra["forward, gate/up + down as one persistent kernel vs two launches"] = fused_vs_separate(dev)
     return extra
@@ -594,18 +751,27 @@ def decode_lines(layer, spec, dev, pk, tag, expert_bytes, n_batches=16):
             moe_decode(layer.h, xs[it[0] % n_batches], B, yb, wsb)
             it[0] += 1
 
-        msb = time_steps(fnb, 64, 8, 1)
+        stb = {}
+        msb = time_steps(fnb, 64, 8, 1, stb)
         profb = profile_groups(layer.h, fnb, 32)
         nact = [int(np.count_nonzero(layer.route(x)["cnt"].cpu().numpy())) + spec.S for x in xs]
         nbytes = float(np.mean(nact)) * expert_bytes + spec.E * spec.d * 2
         t_roof = nbytes / (pk["hbm_gbs"] * 1e9)
         out[f"{tag}_decode_B{B}"] = {
             "path": "warp-per-output kernels" if B < 8 else "grouped-GEMM forward (from the crossover batch)",
-            "tokens_per_s": B / (msb * 1e-3), "ms": msb, "weight_gbs": nbytes / (msb * 1e-3) / 1e9,
+            "tokens_per_s": B / (msb * 1e-3), "ms": msb, "ms_median": stb["ms_median"], "ms_min": stb["ms_min"],
+            "weight_gbs": nbytes / (msb * 1e-3) / 1e9,
             "roofline_ms": t_roof * 1e3, "frac_of_roofline": t_roof * 1e3 / msb,
             "experts_read_mean": float(np.mean(nact)), "batches": n_batches,
             "groups_ms": {g: v[1] / 32 for g, v in profb.items()}}
     return out
+
+
+def decode_row(v):
+    """Summary line of a decode workload (bytes: the router weight and the used experts' weights)."""
+    return {"ms": r4(v["ms"]), "med": r4(v["ms_median"]), "min": r4(v["ms_min"]), "tok_s": r4(v["tokens_per_s"]),
+            "weight_GBs": r4(v["weight_gbs"]), "roof_ms": r4(v["roofline_ms"]), "frac": r4(v["frac_of_roofline"]),
+            "path": "warp" if v["path"].startswith("warp") else "grouped GEMM"}
 
 
 def graph_vs_eager(dev, T=128, steps=50):
@@ -697,7 +863,24 @@ def decode_crossover(layer, spec, dev, n_batches=8):
             "note": "decode_ms: warp-per-output kernels forced; moe_decode itself switches to the GEMMs from B = 8"}
 
 
-def run_extra_mxfp8(dev, pk):
+def mx_step_work(spec, n_chunks, slots, fl_fwd, fl_bwd):
+    """Algorithmic (flops, bytes) of the chunked MXFP8 step: "ideal once" (each quantised weight copy
+    read once, E4M3 codes + one E8M0 byte per 32; bf16 weight gradients written once; activations in
+    and out once) and "per chunk" (the chunked method's own cost: every chunk's forward, and the
+    recomputed forwards of the chunks the ring does not hold, read the forward weight copies; every
+    chunk's backward reads the backward copies)."""
+    nseg, d, f = spec.E + spec.S, spec.d, spec.f
+    w_axis = 3 * nseg * f * d * (1 + 1 / 32)          # W13 + Wd, one quantisation axis
+    grads = 3 * nseg * f * d * 2
+    acts = 4 * spec.T * spec.d * 2                     # x, dy in; y, dx out
+    recompute = max(0, n_chunks - slots)
+    ideal = (fl_fwd + fl_bwd, 2 * w_axis + grads + acts)
+    per_chunk = (fl_fwd * (1 + recompute / n_chunks) + fl_bwd,
+                 (n_chunks + recompute) * w_axis + n_chunks * w_axis + grads + acts)
+    return ideal, per_chunk
+
+
+def run_extra_mxfp8(dev, pk, summary):
     """DeepSeek-V3-shaped MXFP8 forward + backward, T=8192 in 2368-token chunks over a 512 MB ring."""
     from mixture_experts_layer_routing_gb300 import MoeLayer, moe_train_chunked, moe_train_chunked_sizes
     spec = moe_synth.DSV3_MXFP8
@@ -717,23 +900,32 @@ def run_extra_mxfp8(dev, pk):
     rec = []
     fn = lambda: rec.append(moe_train_chunked(layer.h, inp["x"], inp["dy"], spec.T, y, g["dx"], g["dWr"],  # noqa: E731
                                               g["dWg"], g["dWu"], g["dWd"], ring, ring_bytes, ws))
-    ms = time_steps(fn, 3, 3, 1)
+    st = {}
+    ms = time_steps(fn, 5, 3, 1, st)
     prof = profile_groups(layer.h, fn, 2)
-    work_f = work_per_group(spec, cnt, training=True)
-    fl = sum(work_f[k][0] for k in ("router_logits", "gateup", "down", "bwd_dh", "bwd_dx", "bwd_dw13", "bwd_dwd"))
-    nseg, d, f = spec.E + spec.S, spec.d, spec.f
-    # ideal bytes: each weight once per quantisation axis (E4M3 + E8M0), weight gradients written once (bf16),
-    # activations in and out once
-    by = 2 * (3 * nseg * f * d) * (1 + 1 / 32) + 3 * nseg * f * d * 2 + 4 * spec.T * d * 2
+    fl_fwd, _ = layer_work(spec, cnt, "fwd")
+    fl_all, _ = layer_work(spec, cnt, "fwd+bwd")
+    slots = ring_bytes // z["slot"]
+    (fi, bi), (fc, bc) = mx_step_work(spec, z["n_chunks"], slots, fl_fwd, fl_all - fl_fwd)
     mx_peak = 2 * pk["bf16_tflops"]          # MXFP8 dense = 2x bf16 (nominal ratio) of the measured bf16 peak
-    t_roof = max(fl / (mx_peak * 1e12), by / (pk["hbm_gbs"] * 1e9))
-    out = {spec.name + " fwd+bwd": {
-        "tokens_per_s": spec.T / (ms * 1e-3), "ms": ms, "roofline_ms": t_roof * 1e3,
-        "frac_of_roofline": t_roof * 1e3 / ms, "chunks": z["n_chunks"], "ring_slots": ring_bytes // z["slot"],
+    once = roof_line(ms, fi, bi, pk, mx_peak)
+    chunked = roof_line(ms, fc, bc, pk, mx_peak)
+    key = spec.name + " fwd+bwd"
+    out = {key: {
+        "tokens_per_s": spec.T / (ms * 1e-3), **st, "roofline_ms": once["roofline_ms"],
+        "frac_of_roofline": once["frac_of_roofline"], "ideal_once": once, "per_chunk": chunked,
+        "chunks": z["n_chunks"], "ring_slots": slots,
         "recomputed_chunks": rec[-1] if rec else None, "peak_mxfp8_tflops": mx_peak,
         "groups_ms": {k: v[1] / 2 for k, v in prof.items()}}}
+    row = summary_row(st, spec.T, once)
+    row["frac_per_chunk"] = r4(chunked["frac_of_roofline"])
+    row["roof_ms_per_chunk"] = r4(chunked["roofline_ms"])
+    summary["c3 mxfp8 T8192 chunked fwd+bwd (frac: ideal once)"] = row
     # decode on the E4M3 weights: per expert W13 and Wd codes plus one scale byte per 32
-    out.update(decode_lines(layer, spec, dev, pk, "dsv3_mxfp8", 3 * f * d * (1 + 1 / 32)))
+    dl = decode_lines(layer, spec, dev, pk, "dsv3_mxfp8", 3 * spec.f * spec.d * (1 + 1 / 32))
+    out.update(dl)
+    for k, v in dl.items():
+        summary["c4 mxfp8 decode B" + k.rsplit("B", 1)[1]] = decode_row(v)
     out["dsv3_mxfp8_decode_vs_grouped_gemm"] = decode_crossover(layer, spec, dev)
     layer.close()
     del layer, inp, g, y
@@ -835,9 +1027,9 @@ def run_reference(args):
     out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, moe_synth)",
-           "config": {"workload": spec.name + " fwd+bwd", "T": spec.T, "d": spec.d, "E": spec.E, "f": spec.f,
-                      "k": spec.k, "sample_tokens_per_step": ntok},
+           "config": bench_config(spec, world),
            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                            "host": host_cpu(),
                             "sample": (f"the whole {spec.T}-token fwd+bwd per step" if ntok == spec.T else
                                        f"fwd+bwd of the first {ntok} of {spec.T} tokens per step")},
            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

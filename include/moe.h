@@ -190,11 +190,14 @@ moe_status moe_set_decode_crossover(moe_handle h, int b_min);
 /* Tensor-core scheduling of the bf16 expert GEMMs (gate/up, down, dY.Wd, dx).
  * mode 1 runs them on pairs of SMs: 2-CTA clusters, one
  * tcgen05.mma.cta_group::2 per K step over a 256-row tile, each CTA holding
- * its own 128 rows and half of the weight tile. mode 0 (the default) runs one
- * CTA per 128-row tile. The modes agree up to fp32 summation order and each is
- * deterministic; on GB300 the pairs measured no faster for this layer's
- * shapes, so they are opt-in. Host-only; another mode returns
- * MOE_ERR_INVALID_ARG. */
+ * its own 128 rows and half of the weight tile. mode 0 runs one CTA per
+ * 128-row tile. mode 2 runs one CTA per two 128-row tiles of an expert's
+ * rows on one SM: two M = 128 MMAs per K step share each staged weight tile
+ * (an expert's last, odd tile runs alone), so a pipeline stage carries twice
+ * the MMA work. Modes 0 and 2 accumulate every output element with the same
+ * instructions in the same K order, so their results are bit-identical; mode 1
+ * agrees with them up to fp32 summation order. Each mode is deterministic.
+ * Host-only; another mode returns MOE_ERR_INVALID_ARG. */
 moe_status moe_set_pairs(moe_handle h, int mode);
 
 /* Forward of a bf16 tensor-core layer with its two expert GEMMs in one kernel
@@ -225,13 +228,13 @@ moe_status moe_get_status(moe_handle h, void* stream, int* device_status);
  * such as a plugin inside a host program that owns all device memory, or a
  * serving loop that bans cudaMalloc/cudaFree after start-up because they can
  * block and synchronise the device.
- * Its scratch is one fixed 4 MiB array inside the library, plus an 8 MiB one
+ * Its scratch is one fixed 4 MiB array inside the library, plus a 24 MiB one
  * for the split-K partials of the router GEMM (both held on every GPU that
  * loads the library until the process exits). A call needs
- *   2*pad(4*ceil(T*k/1024)*E) + 2*pad(4*(E+S+1)) + pad(16*(E+S+1))
+ *   2*pad(4*ceil(T*k/1024)*E) + 2*pad(4*(E+S+1)) + pad(24*(E+S+1))
  *   + 2*pad(4*T*(k+S)) bytes of the 4 MiB,
  * pad() rounding up to 256; larger T returns MOE_ERR_WORKSPACE before any
- * launch (E = 256, k = 8, S = 1 allows T up to 47,573 tokens).
+ * launch (E = 256, k = 8, S = 1 allows T up to 47,544 tokens).
  * The first call on a device looks up the array's address there; make that
  * first call before any stream capture. The address is kept for the life of
  * the process: after a cudaDeviceReset of that device (which tears down the

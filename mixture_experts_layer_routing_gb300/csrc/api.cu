@@ -42,7 +42,7 @@ Sizes sizes_for(const Layer& L, int T) {
   const size_t eb = elem_bytes(L.prec);
   const size_t nch = (A + kChunk - 1) / kChunk;
   Sizes z;
-  z.route = al(4 * T * (size_t)L.E) + 2 * al(4 * A) + 2 * al(4 * (nseg + 1)) + al(16 * (nseg + 1)) + 2 * al(4 * A) +
+  z.route = al(4 * T * (size_t)L.E) + 2 * al(4 * A) + 2 * al(4 * (nseg + 1)) + al(4 * kPrefixArrays * (nseg + 1)) + 2 * al(4 * A) +
             2 * al(4 * R);
   z.uv = al(eb * R * 2 * L.f);
   z.fwd_scratch = 2 * al(4 * nch * L.E) + al(eb * R * L.f) + al(eb * R * L.d);
@@ -74,7 +74,7 @@ char* carve_route(Bufs& B, const Layer& L, char* p) {
   B.gate = (float*)p; p += al(4 * (size_t)B.A);
   B.cnt = (int*)p; p += al(4 * (nseg + 1));
   B.off = (int*)p; p += al(4 * (nseg + 1));
-  B.mt_off = (int*)p; p += al(16 * (nseg + 1));   // mt_off, then the pair / dense / sparse prefixes
+  B.mt_off = (int*)p; p += al(4 * kPrefixArrays * (nseg + 1));   // mt_off, then the other tile prefixes
   B.perm = (int*)p; p += al(4 * (size_t)B.A);
   B.inv = (int*)p; p += al(4 * (size_t)B.A);
   B.row_token = (int*)p; p += al(4 * (size_t)B.R);
@@ -387,6 +387,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
   L.G = (c.f % kGate == 0) ? kGate : 64;
   L.pairs = 0;
   L.fused = 0;
+  L.row_tiles = 1;
   L.has_weights = false;
   if (cudaGetDevice(&h->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&L.num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
@@ -732,8 +733,9 @@ moe_status moe_set_fused(moe_handle h, int on) {
 }
 
 moe_status moe_set_pairs(moe_handle h, int mode) {
-  if (!h || mode < 0 || mode > 1) return MOE_ERR_INVALID_ARG;
-  h->L.pairs = mode;
+  if (!h || mode < 0 || mode > 2) return MOE_ERR_INVALID_ARG;
+  h->L.pairs = mode == 1 ? 1 : 0;
+  h->L.row_tiles = mode == 2 ? 2 : 1;
   return MOE_OK;
 }
 

@@ -45,10 +45,12 @@ struct DecodeWs {
   int* a_tok;      // [B*k + B] (t << 8) | slot
   float* a_gate;   // [B*k + B]
   float* h;        // [B, k+1, f]
-  // MXFP8 layers only. E4M3 x E8M0 values are exact in bf16 (4 significant bits, exponents within
-  // bf16's range), so the quantised activations are held as bf16.
-  bf16* xd;        // [B, d]      x quantised along d
-  bf16* hd;        // [B, k+1, f] h quantised along f
+  // MXFP8 layers only: the quantised activations as their E4M3 codes held in fp16 (every E4M3
+  // value is exact in fp16) and one E8M0 byte per 32 values; value = code * 2^(scale - 127).
+  uint16_t* xc;    // [B, d]      x quantised along d: codes
+  uint8_t* xs;     // [B, d/32]   and scales
+  uint16_t* hc;    // [B, k+1, f] h quantised along f: codes
+  uint8_t* hs;     // [B, k+1, f/32]
 };
 
 inline size_t al(size_t v) { return (v + 255) & ~size_t(255); }
@@ -66,10 +68,13 @@ DecodeWs carve(const Layer& L, int B, void* ws) {
   w.a_tok = (int*)p; p += al(sizeof(int) * na);
   w.a_gate = (float*)p; p += al(sizeof(float) * na);
   w.h = (float*)p; p += al(sizeof(float) * B * (L.k + 1) * L.f);
-  w.xd = w.hd = nullptr;
+  w.xc = w.hc = nullptr;
+  w.xs = w.hs = nullptr;
   if (L.prec == MOE_MXFP8) {
-    w.xd = (bf16*)p; p += al(sizeof(bf16) * B * L.d);
-    w.hd = (bf16*)p; p += al(sizeof(bf16) * B * (L.k + 1) * L.f);
+    w.xc = (uint16_t*)p; p += al(2 * (size_t)B * L.d);
+    w.xs = (uint8_t*)p; p += al((size_t)B * L.d / 32);
+    w.hc = (uint16_t*)p; p += al(2 * (size_t)B * (L.k + 1) * L.f);
+    w.hs = (uint8_t*)p; p += al((size_t)B * (L.k + 1) * L.f / 32);
   }
   return w;
 }
@@ -377,50 +382,67 @@ __global__ void __launch_bounds__(kDownWarps * 32) decode_down_kernel(const bf16
 }
 
 // ------------------------------------------------------------------ MXFP8
-// 16 E4M3 codes -> floats (exact).
-__device__ __forceinline__ void fp8x16(const uint4& v, float (&o)[16]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[q] & 0xffffu), __NV_E4M3);
-    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[q] >> 16), __NV_E4M3);
-    const float2 a = __half22float2(__half2(lo)), b = __half22float2(__half2(hi));
-    o[4 * q] = a.x;
-    o[4 * q + 1] = a.y;
-    o[4 * q + 2] = b.x;
-    o[4 * q + 3] = b.y;
-  }
-}
 // 2^(s - 127) for an E8M0 byte s (s = 0 is the subnormal 2^-127).
 __device__ __forceinline__ float e8m0(uint32_t s) {
   return s ? __uint_as_float(s << 23) : __uint_as_float(0x00400000u);
 }
 
-// In place: 32 fp32 values -> their MX quantisation (E4M3 codes times the block's E8M0 scale),
-// held as the exact fp32 values.
-__device__ __forceinline__ void fake_quant32(float (&v)[32]) {
-  uint4 lo, hi;
-  const float s = e8m0(quant32(v, lo, hi));
-  float c[16];
-  fp8x16(lo, c);
+// 32 fp32 values -> their MX quantisation: 32 E4M3 codes written as fp16 values (64 bytes at
+// codes), the E8M0 byte at *scale.
+__device__ __forceinline__ void quant32_to_f16(const float (&v)[32], uint16_t* codes, uint8_t* scale) {
+  uint4 q[2];
+  *scale = quant32(v, q[0], q[1]);
+  uint4* dst = reinterpret_cast<uint4*>(codes);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = c[i] * s;
-  fp8x16(hi, c);
+  for (int hlf = 0; hlf < 2; ++hlf) {
+    const uint32_t w[4] = {q[hlf].x, q[hlf].y, q[hlf].z, q[hlf].w};
+    uint32_t o[8];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[16 + i] = c[i] * s;
+    for (int i = 0; i < 4; ++i) {
+      const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] & 0xffffu), __NV_E4M3);
+      const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] >> 16), __NV_E4M3);
+      o[2 * i] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
+      o[2 * i + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
+    }
+    dst[2 * hlf] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[2 * hlf + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
 }
 
-// x [B, d] bf16 -> xd: one thread per 32-value block.
+// acc + a * b for fp16 a, b (exact products) with fp32 accumulation, one rounding per step.
+__device__ __forceinline__ float fma_h(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"((unsigned short)a), "h"((unsigned short)b), "f"(c));
+  return d;
+}
+
+// sum_{i < 16} w[i] * a[i] in order i = 0..15, fp32 accumulation: w = 16 E4M3 codes (one 16-byte
+// chunk), a = 16 fp16 codes (two 16-byte chunks). The codes are exact in fp16, so every product is
+// exact and only the running sum rounds.
+__device__ __forceinline__ float dot16_codes(const uint4& w, const uint4& a0, const uint4& a1) {
+  const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+  const uint32_t aa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+  float acc = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(ww[q] & 0xffffu), __NV_E4M3);
+    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(ww[q] >> 16), __NV_E4M3);
+    acc = fma_h(lo.x, aa[2 * q], acc);
+    acc = fma_h(lo.y, aa[2 * q] >> 16, acc);
+    acc = fma_h(hi.x, aa[2 * q + 1], acc);
+    acc = fma_h(hi.y, aa[2 * q + 1] >> 16, acc);
+  }
+  return acc;
+}
+
+// x [B, d] bf16 -> xc, xs: one thread per 32-value block.
 __global__ void __launch_bounds__(256) decode_quant_x_kernel(const bf16* __restrict__ x, int nblocks, DecodeWs w) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= nblocks) return;
   float v[32];
 #pragma unroll
   for (int q = 0; q < 4; ++q) unpack8(*reinterpret_cast<const uint4*>(x + (size_t)b * 32 + 8 * q), v + 8 * q);
-  fake_quant32(v);
-  uint4* dst = reinterpret_cast<uint4*>(w.xd + (size_t)b * 32);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) dst[q] = pack8(v + 8 * q);   // exact
+  quant32_to_f16(v, w.xc + (size_t)b * 32, w.xs + b);
 }
 
 constexpr int kBatchMx = 4;   // 16-byte chunks per lane per row in flight (two blocks per SM fit)
@@ -462,9 +484,14 @@ __global__ void __launch_bounds__(256, 2) decode_gateup_mx_kernel(const uint8_t*
     const uint8_t* su = W13s + ru * nb;
     for (int g0 = a0; g0 < a1; g0 += kTokGroup) {
       const int nt = min(kTokGroup, a1 - g0);
-      const bf16* xr[kTokGroup];
+      const uint16_t* xr[kTokGroup];
+      const uint8_t* xsr[kTokGroup];
 #pragma unroll
-      for (int q = 0; q < kTokGroup; ++q) xr[q] = w.xd + (size_t)(q < nt ? (w.a_tok[g0 + q] >> 8) : 0) * d;
+      for (int q = 0; q < kTokGroup; ++q) {
+        const size_t t = q < nt ? (w.a_tok[g0 + q] >> 8) : 0;
+        xr[q] = w.xc + t * d;
+        xsr[q] = w.xs + t * nb;
+      }
       float au[kTokGroup], av[kTokGroup];
 #pragma unroll
       for (int q = 0; q < kTokGroup; ++q) au[q] = av[q] = 0.f;
@@ -485,27 +512,16 @@ __global__ void __launch_bounds__(256, 2) decode_gateup_mx_kernel(const uint8_t*
         for (int q = 0; q < kBatchMx; ++q) {
           const int c = cb + q * 32;
           if (c < nchunk) {
-            float fg[16], fu[16];
-            fp8x16(gv[q], fg);
-            fp8x16(uvv[q], fu);
             const float s_g = e8m0(sgv[q]), s_u = e8m0(suv[q]);
 #pragma unroll
             for (int tt = 0; tt < kTokGroup; ++tt) {
               if (tt < nt) {
+                // weight codes times x codes, then the x block scale and the weight block scale
                 const uint4* xv8 = reinterpret_cast<const uint4*>(xr[tt] + (size_t)c * 16);
-                float pg = 0.f, pu = 0.f;
-#pragma unroll
-                for (int h8 = 0; h8 < 2; ++h8) {
-                  float xv[8];
-                  unpack8(xv8[h8], xv);
-#pragma unroll
-                  for (int r = 0; r < 8; ++r) {
-                    pg = fmaf(xv[r], fg[8 * h8 + r], pg);
-                    pu = fmaf(xv[r], fu[8 * h8 + r], pu);
-                  }
-                }
-                au[tt] = fmaf(pg, s_g, au[tt]);
-                av[tt] = fmaf(pu, s_u, av[tt]);
+                const uint4 xa = xv8[0], xb = xv8[1];
+                const float s_x = e8m0(xsr[tt][c >> 1]);
+                au[tt] = fmaf(dot16_codes(gv[q], xa, xb) * s_x, s_g, au[tt]);
+                av[tt] = fmaf(dot16_codes(uvv[q], xa, xb) * s_x, s_u, av[tt]);
               }
             }
           }
@@ -527,7 +543,7 @@ __global__ void __launch_bounds__(256, 2) decode_gateup_mx_kernel(const uint8_t*
   }
 }
 
-// h [B, k+1, f] fp32 -> its MX quantisation along f (hd, bf16); one thread per 32-value block.
+// h [B, k+1, f] fp32 -> its MX quantisation along f (hc, hs); one thread per 32-value block.
 __global__ void __launch_bounds__(256) decode_quant_h_kernel(int nblocks, DecodeWs w) {
   griddep_launch();
   griddep_wait();
@@ -543,10 +559,7 @@ __global__ void __launch_bounds__(256) decode_quant_h_kernel(int nblocks, Decode
     v[4 * q + 2] = t.z;
     v[4 * q + 3] = t.w;
   }
-  fake_quant32(v);
-  uint4* dst = reinterpret_cast<uint4*>(w.hd + (size_t)b * 32);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) dst[q] = pack8(v + 8 * q);   // exact
+  quant32_to_f16(v, w.hc + (size_t)b * 32, w.hs + b);
 }
 
 constexpr int kFChunksMx = 4;   // 16-byte chunks (16 values) of a Wd row per lane (f <= 2048 per pass)
@@ -606,24 +619,19 @@ __global__ void __launch_bounds__(kDownWarps * 32) decode_down_mx_kernel(const u
         const int code = w.a_tok[a0];
         const int t = code >> 8, slot = code & 255;
         const float g = w.a_gate[a0];
-        const bf16* hr = w.hd + ((size_t)t * (k + 1) + slot) * f;
+        const size_t hrow = (size_t)t * (k + 1) + slot;
+        const uint16_t* hr = w.hc + hrow * f;
+        const uint8_t* hsr = w.hs + hrow * nb;
         float s[kCols] = {};
 #pragma unroll
         for (int q = 0; q < kFChunksMx; ++q) {
           const int c = f0 + (lane + 32 * q) * 16;
           if (c < f) {
-            float hv[16];
-            unpack8(*reinterpret_cast<const uint4*>(hr + c), hv);
-            unpack8(*reinterpret_cast<const uint4*>(hr + c + 8), hv + 8);
+            const uint4 ha = *reinterpret_cast<const uint4*>(hr + c), hb = *reinterpret_cast<const uint4*>(hr + c + 8);
+            const float s_h = e8m0(hsr[c >> 5]);
 #pragma unroll
-            for (int cc = 0; cc < kCols; ++cc) {
-              float wf[16];
-              fp8x16(wcur[cc][q], wf);
-              float pr = 0.f;
-#pragma unroll
-              for (int r = 0; r < 16; ++r) pr = fmaf(hv[r], wf[r], pr);
-              s[cc] = fmaf(pr, e8m0(scur[cc][q]), s[cc]);
-            }
+            for (int cc = 0; cc < kCols; ++cc)
+              s[cc] = fmaf(dot16_codes(wcur[cc][q], ha, hb) * s_h, e8m0(scur[cc][q]), s[cc]);
           }
         }
 #pragma unroll
@@ -637,11 +645,14 @@ __global__ void __launch_bounds__(kDownWarps * 32) decode_down_mx_kernel(const u
       // several tokens: in groups of kTokGroup, each chunk decoded and scaled once per group
       for (int g0 = a0; g0 < a1; g0 += kTokGroup) {
         const int nt = min(kTokGroup, a1 - g0);
-        const bf16* hr[kTokGroup];
+        const uint16_t* hr[kTokGroup];
+        const uint8_t* hsr[kTokGroup];
 #pragma unroll
         for (int tt = 0; tt < kTokGroup; ++tt) {
           const int code = w.a_tok[g0 + (tt < nt ? tt : 0)];
-          hr[tt] = w.hd + ((size_t)(code >> 8) * (k + 1) + (code & 255)) * f;
+          const size_t hrow = (size_t)(code >> 8) * (k + 1) + (code & 255);
+          hr[tt] = w.hc + hrow * f;
+          hsr[tt] = w.hs + hrow * nb;
         }
         float s[kTokGroup][kCols] = {};
 #pragma unroll
@@ -649,21 +660,14 @@ __global__ void __launch_bounds__(kDownWarps * 32) decode_down_mx_kernel(const u
           const int c = f0 + (lane + 32 * q) * 16;
           if (c < f) {
 #pragma unroll
-            for (int cc = 0; cc < kCols; ++cc) {
-              float wf[16];
-              fp8x16(wcur[cc][q], wf);
-              const float sw = e8m0(scur[cc][q]);
+            for (int tt = 0; tt < kTokGroup; ++tt) {
+              if (tt < nt) {
+                const uint4 ha = *reinterpret_cast<const uint4*>(hr[tt] + c);
+                const uint4 hb = *reinterpret_cast<const uint4*>(hr[tt] + c + 8);
+                const float s_h = e8m0(hsr[tt][c >> 5]);
 #pragma unroll
-              for (int tt = 0; tt < kTokGroup; ++tt) {
-                if (tt < nt) {
-                  float hv[16];
-                  unpack8(*reinterpret_cast<const uint4*>(hr[tt] + c), hv);
-                  unpack8(*reinterpret_cast<const uint4*>(hr[tt] + c + 8), hv + 8);
-                  float pr = 0.f;
-#pragma unroll
-                  for (int r = 0; r < 16; ++r) pr = fmaf(hv[r], wf[r], pr);
-                  s[tt][cc] = fmaf(pr, sw, s[tt][cc]);
-                }
+                for (int cc = 0; cc < kCols; ++cc)
+                  s[tt][cc] = fmaf(dot16_codes(wcur[cc][q], ha, hb) * s_h, e8m0(scur[cc][q]), s[tt][cc]);
               }
             }
           }
@@ -717,7 +721,9 @@ size_t decode_workspace_bytes(const Layer& L, int B) {
   size_t z = al(sizeof(float) * B * L.E) + al(sizeof(int) * B * L.k) + al(sizeof(float) * B * L.k) + al(sizeof(int)) +
              al(sizeof(int) * (L.E + 1)) + al(sizeof(int) * (L.E + 2)) + al(sizeof(int) * na) +
              al(sizeof(float) * na) + al(sizeof(float) * B * (L.k + 1) * L.f);
-  if (L.prec == MOE_MXFP8) z += al(sizeof(bf16) * B * L.d) + al(sizeof(bf16) * B * (L.k + 1) * L.f);
+  if (L.prec == MOE_MXFP8)
+    z += al(2 * (size_t)B * L.d) + al((size_t)B * L.d / 32) + al(2 * (size_t)B * (L.k + 1) * L.f) +
+         al((size_t)B * (L.k + 1) * L.f / 32);
   return z;
 }
 

@@ -18,6 +18,7 @@ constexpr int kRouterSplitRows = 256;   // rows per split
 // Segments with kDenseTiles M-tiles or more reuse each weight byte for >= 384 rows, above the
 // bf16 ridge of about 280 flop/byte: candidates for the "dense" tile stream (see scan_kernel).
 constexpr int kDenseTiles = 3;
+constexpr int kPrefixArrays = 6;   // tile-schedule prefix arrays of nseg + 1 ints each (Bufs::mt_off)
 constexpr int kGate = 128;        // gate/up interleave block of the packed bf16 W13 (rows)
 constexpr int kGateMx = 64;       // gate/up interleave block of the MXFP8 W13 (rows)
 constexpr int kMaxDecodeB = 64;
@@ -46,6 +47,7 @@ struct Layer {
   CUtensorMap tm_Wd_h;      // K-major rows of Wd, box 64 x 128
   int pairs;                // 1: expert GEMMs on 2-SM CTA pairs; 0 (default): one CTA per tile
   int fused;                // 1: forward gate/up and down GEMMs as one persistent kernel
+  int row_tiles;            // 128-row tiles per CTA of the bf16 segment GEMMs over token rows (1 or 2)
   unsigned* dep;            // fused kernel: per-m-tile arrival counters (zero between calls)
   unsigned* dep_done;       // fused kernel: [1] CTAs finished, [2] gate/up tiles finished ([0] unused)
   // MXFP8 packed weights: E4M3 codes and E8M0 scales (one per 32 along the named axis)
@@ -69,7 +71,8 @@ struct Bufs {
   int* cnt;              // [E+S]
   int* off;              // [E+S+1]
   int* mt_off;           // [E+S+1] prefix of ceil(cnt / kBM), then [E+S+1] each: prefixes of
-                         // pairs of tiles, of the tiles of dense segments and of the others
+                         // pairs of tiles, of the tiles of dense segments and of the others, of
+                         // the pairs of dense segments and of the others (kPrefixArrays in all)
   int* perm;             // [A]
   int* inv;              // [A]
   int* row_token;        // [R]
@@ -130,7 +133,7 @@ cudaError_t launch_decode_down_mx(const Layer& L, int B, void* y, void* ws, cuda
 bool tc_supported(const Layer& L);
 cudaError_t tc_init(Layer& L);   // encodes the weight tensor maps, sets kernel attributes
 // part (nullable, part_bytes): scratch for split-K partials when T gives few row tiles
-constexpr size_t kRouterPartBytes = 8u << 20;   // router split-K partials, at most
+constexpr size_t kRouterPartBytes = 24u << 20;   // router split-K partials, at most (2 splits of T = 12288, E = 256)
 int tc_router_splits(const Layer& L, int T);
 cudaError_t launch_tc_router_logits(const Layer& L, const void* x, int T, float* logits, cudaStream_t s,
                                     float* part, size_t part_bytes);

@@ -42,7 +42,8 @@ inline size_t al(size_t v) { return (v + 255) & ~size_t(255); }
 size_t scratch_bytes(const Layer& L, int T) {
   const size_t A = (size_t)T * L.k, R = A + (size_t)L.S * T, nseg = L.E + L.S;
   const size_t nch = (A + kChunk - 1) / kChunk;
-  return 2 * al(4 * nch * L.E) + 2 * al(4 * (nseg + 1)) + al(16 * (nseg + 1)) + al(4 * R) + al(4 * R);
+  return 2 * al(4 * nch * L.E) + 2 * al(4 * (nseg + 1)) + al(4 * kPrefixArrays * (nseg + 1)) + al(4 * R) +
+         al(4 * R);
 }
 
 // Device addresses of the arrays on device `dev` (the current device): out[0] the routing scratch,
@@ -97,7 +98,7 @@ extern "C" moe_status moe_route_noalloc(moe_handle h, const void* x, int T, floa
   B.chunk_base = (int*)p; p += al(4 * (size_t)B.nch * L.E);
   B.cnt = (int*)p; p += al(4 * (nseg + 1));
   B.off = (int*)p; p += al(4 * (nseg + 1));
-  B.mt_off = (int*)p; p += al(16 * (nseg + 1));   // mt_off, then the pair / dense / sparse prefixes
+  B.mt_off = (int*)p; p += al(4 * kPrefixArrays * (nseg + 1));   // mt_off, then the other tile prefixes
   B.row_token = (int*)p; p += al(4 * (size_t)B.R);
   B.row_gate = (float*)p;
   B.logits = logits;

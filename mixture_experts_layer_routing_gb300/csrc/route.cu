@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(512) scan_kernel(const int* __restrict__ chunk
                                                    int* __restrict__ chunk_base, int* __restrict__ cnt,
                                                    int* __restrict__ off, int* __restrict__ mt_off) {
   __shared__ int c_s[kMaxE + 1];
-  __shared__ int warp_tot[16][5];
+  __shared__ int warp_tot[16][7];
   __shared__ int tot[4];   // all tiles, candidate dense tiles, other tiles, other non-empty segments
   const int tid = threadIdx.x;
   const int nseg = E + S;
@@ -123,49 +123,46 @@ __global__ void __launch_bounds__(512) scan_kernel(const int* __restrict__ chunk
   __syncthreads();
   const bool mix = 4 * tot[1] >= tot[0] && 2 * tot[2] < 3 * tot[3];
   // exclusive scans over the 512 threads of: c, ceil(c / kBM) (tiles), ceil(tiles / 2) (pairs),
-  // and the tiles of dense segments and of the others
+  // the tiles of dense segments and of the others, and the same split of the pairs (the GEMMs
+  // whose CTAs take two 128-row tiles of a segment at once)
   const int dense = mix && cand ? tiles : 0, sparse = tiles - dense;
-  int v[5] = {c, tiles, pairs, dense, sparse};
-  const int own[5] = {c, tiles, pairs, dense, sparse};
+  const int dense_p = mix && cand ? pairs : 0, sparse_p = pairs - dense_p;
+  constexpr int NQ = 7;
+  int v[NQ] = {c, tiles, pairs, dense, sparse, dense_p, sparse_p};
+  const int own[NQ] = {c, tiles, pairs, dense, sparse, dense_p, sparse_p};
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
 #pragma unroll
-    for (int q = 0; q < 5; ++q) {
+    for (int q = 0; q < NQ; ++q) {
       const int n = __shfl_up_sync(0xffffffffu, v[q], o);
       if (lane >= o) v[q] += n;
     }
   }
   if (lane == 31) {
 #pragma unroll
-    for (int q = 0; q < 5; ++q) warp_tot[w][q] = v[q];
+    for (int q = 0; q < NQ; ++q) warp_tot[w][q] = v[q];
   }
   __syncthreads();
-  int ex[5];
+  int ex[NQ];
 #pragma unroll
-  for (int q = 0; q < 5; ++q) {
+  for (int q = 0; q < NQ; ++q) {
     int b = 0;
     for (int u = 0; u < w; ++u) b += warp_tot[u][q];
     ex[q] = b + v[q] - own[q];
   }
-  // after mt_off: the pair prefix, then the dense-tile and sparse-tile prefixes
-  int* mp_off = mt_off + (nseg + 1);
-  int* dn_off = mt_off + 2 * (nseg + 1);
-  int* sp_off = mt_off + 3 * (nseg + 1);
+  // mt_off, then (kPrefixArrays arrays of nseg + 1 each) the pair prefix, the dense-tile and
+  // sparse-tile prefixes, the dense-pair and sparse-pair prefixes
   if (tid < nseg) {
     cnt[tid] = c;
     off[tid] = ex[0];
-    mt_off[tid] = ex[1];
-    mp_off[tid] = ex[2];
-    dn_off[tid] = ex[3];
-    sp_off[tid] = ex[4];
+#pragma unroll
+    for (int q = 1; q < NQ; ++q) mt_off[(q - 1) * (nseg + 1) + tid] = ex[q];
     c_s[tid] = ex[0];
   }
   if (tid == nseg - 1) {
     off[nseg] = ex[0] + c;
-    mt_off[nseg] = ex[1] + tiles;
-    mp_off[nseg] = ex[2] + pairs;
-    dn_off[nseg] = ex[3] + dense;
-    sp_off[nseg] = ex[4] + sparse;
+#pragma unroll
+    for (int q = 1; q < NQ; ++q) mt_off[(q - 1) * (nseg + 1) + nseg] = ex[q] + own[q];
   }
   __syncthreads();
   if (tid < E) {

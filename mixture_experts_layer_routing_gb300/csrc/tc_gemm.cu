@@ -44,6 +44,9 @@ constexpr int kSmemMax = 227 * 1024;   // dynamic shared memory per CTA
 constexpr int kProducerWarps = 4, kEpiWarps = 4;
 constexpr int kThreads = (kProducerWarps + kEpiWarps + 1) * 32;   // 288
 constexpr int kMmaWarp = kProducerWarps + kEpiWarps;               // warp 8
+// Two row tiles per CTA (MT = 2): a second group of four epilogue warps (9-12) drains the second
+// 128-row accumulator while warps 4-7 drain the first.
+constexpr int threads_for(int MT) { return MT == 2 ? kThreads + kEpiWarps * 32 : kThreads; }   // 288 / 416
 
 enum { A_GATHER_K = 0, A_TMA_K = 1, A_TMA_MN = 2, A_GATHER_MN = 3 };
 enum { B_TMA_K = 0, B_TMA_MN = 1, B_GATHER_MN = 2 };
@@ -59,7 +62,8 @@ struct TcParams {
   const int* off;         // [nseg+1] segment row offsets
   const int* mt_off;      // [nseg+1] prefix of 128-row tiles (SEG_M)
   const int* mp_off;      // [nseg+1] prefix of pairs of 128-row tiles (SEG_M over CTA pairs)
-  int nseg;
+  int nseg;               // segments scheduled (SEG_M: the first nseg segments)
+  int pstride;            // entries per tile-prefix array (all segments + 1)
   int dense_rows;         // DENSE: rows of the single segment
   int K;                  // reduction length for SEG_M / DENSE (multiple of 64)
   int m_tiles;            // SEG_K: M / 128
@@ -87,16 +91,18 @@ __device__ __forceinline__ void unpack8_to(const bf16* p, float* f) { unpack8(*r
 struct Tile {
   int e, m, n;
   int row0, row_end;   // SEG_M / DENSE: output rows; SEG_K: the segment's sorted rows (the K range)
+  int arow0;           // first row of the A operand loaded by TMA (SEG_M: row0)
   int nkb;             // end of the K-block range (blocks of 64)
   int kb0 = 0;         // first K block (DENSE split-K; 0 otherwise)
   int ks = 0;          // K split index (DENSE split-K)
+  bool two = false;    // MT = 2: the second 128-row tile (rows row0 + 128 ..) holds rows of the segment
 };
 
-template <int SCHED, int CG>
+template <int SCHED, int CG, int MT = 1>
 __device__ __forceinline__ int total_tiles(const TcParams& p) {
   if (SCHED == SCHED_DENSE) return ((p.dense_rows + BM - 1) / BM) * p.n_tiles * p.ksplit;
   if (SCHED == SCHED_SEG_K) return p.nseg * p.m_tiles * p.n_tiles;
-  return (CG == 2 ? p.mp_off[p.nseg] : p.mt_off[p.nseg]) * p.n_tiles;
+  return (CG == 2 || MT == 2 ? p.mp_off[p.nseg] : p.mt_off[p.nseg]) * p.n_tiles;
 }
 
 // CTA pairs: tile L is (segment, pair of m-tiles 2j and 2j+1, n); the CTA of cluster rank r takes
@@ -120,11 +126,12 @@ __device__ __forceinline__ Tile map_tile_pair(const TcParams& p, int L, int rank
   t.m = 2 * (g * kRasterP + within % gp) + rank;
   t.row0 = p.off[lo] + t.m * BM;
   t.row_end = p.off[lo + 1];
+  t.arow0 = t.row0;
   t.nkb = p.K / BK;
   return t;
 }
 
-template <int SCHED, int CG>
+template <int SCHED, int CG, int MT = 1>
 __device__ __forceinline__ Tile map_tile(const TcParams& p, int L, int rank) {
   if (CG == 2) return map_tile_pair(p, L, rank);
   Tile t;
@@ -137,6 +144,7 @@ __device__ __forceinline__ Tile map_tile(const TcParams& p, int L, int rank) {
     t.m = rest / p.n_tiles;
     t.row0 = t.m * BM;
     t.row_end = p.dense_rows;
+    t.arow0 = t.row0;
     t.kb0 = t.ks * nk / p.ksplit;
     t.nkb = (t.ks + 1) * nk / p.ksplit;
     return t;
@@ -149,6 +157,7 @@ __device__ __forceinline__ Tile map_tile(const TcParams& p, int L, int rank) {
     t.m = rem % p.m_tiles;
     t.row0 = p.off[t.e];
     t.row_end = p.off[t.e + 1];
+    t.arow0 = t.row0;
     t.nkb = (t.row_end - t.row0 + BK - 1) / BK;
     return t;
   }
@@ -159,13 +168,15 @@ __device__ __forceinline__ Tile map_tile(const TcParams& p, int L, int rank) {
   // scan_kernel marks none when the mix would not pay (dense under a quarter of the tiles, or the
   // others near the ridge): then the order is segment-major, which keeps each segment's weight and
   // row tiles in L2 between uses.
-  const int* dn = p.mt_off + 2 * (p.nseg + 1);
-  const int* sp = p.mt_off + 3 * (p.nseg + 1);
-  const long N = (long)p.mt_off[p.nseg] * p.n_tiles, Nd = (long)dn[p.nseg] * p.n_tiles;
-  const bool mix = 4 * Nd >= N;
+  // MT = 2: the units are pairs of 128-row tiles of a segment (prefixes of pairs), one per CTA.
+  const int* all = MT == 2 ? p.mt_off + p.pstride : p.mt_off;
+  const int* dn = p.mt_off + (MT == 2 ? 4 : 2) * p.pstride;
+  const int* sp = p.mt_off + (MT == 2 ? 5 : 3) * p.pstride;
+  const long N = (long)all[p.nseg] * p.n_tiles, Nd = (long)dn[p.nseg] * p.n_tiles;
+  const bool mix = Nd > 0;   // scan_kernel marks dense segments only when it chose to interleave
   const long cd = mix ? (long)L * Nd / N : 0;
   const bool is_dense = mix && (long)(L + 1) * Nd / N > cd;
-  const int* pre = !mix ? p.mt_off : (is_dense ? dn : sp);
+  const int* pre = !mix ? all : (is_dense ? dn : sp);
   const int Lc = (int)(is_dense ? cd : L - cd);   // index within the stream
   int lo = 0, hi = p.nseg;
   while (hi - lo > 1) {
@@ -174,17 +185,21 @@ __device__ __forceinline__ Tile map_tile(const TcParams& p, int L, int rank) {
   }
   const int Me = pre[lo + 1] - pre[lo];
   const int local = Lc - pre[lo] * p.n_tiles;
-  // m-tiles in groups of kRasterM, every n-tile of a group before the next group: CTAs running
-  // together share the group's token rows and the expert's weight tiles in L2
-  const int g = local / (kRasterM * p.n_tiles);
-  const int gm = min(kRasterM, Me - g * kRasterM);
-  const int within = local - g * kRasterM * p.n_tiles;
+  // units in groups of kRasterM / MT (kRasterM 128-row tiles), every n-tile of a group before the
+  // next group: CTAs running together share the group's token rows and the expert's weight tiles
+  // in L2
+  constexpr int RG = kRasterM / MT;
+  const int g = local / (RG * p.n_tiles);
+  const int gm = min(RG, Me - g * RG);
+  const int within = local - g * RG * p.n_tiles;
   t.e = lo;
   t.n = within / gm;
-  t.m = g * kRasterM + within % gm;
+  t.m = MT * (g * RG + within % gm);
   t.row0 = p.off[lo] + t.m * BM;
   t.row_end = p.off[lo + 1];
+  t.arow0 = t.row0;
   t.nkb = p.K / BK;
+  t.two = MT == 2 && t.row0 + BM < t.row_end;
   return t;
 }
 
@@ -195,9 +210,9 @@ constexpr int kStageOutBytes = kEpiWarps * 2 * 32 * 128;
 // when a CTA pair shares the B tile), then staging and barriers. Single CTAs keep 4 stages (deeper
 // rings measured no faster and leave no L1 for the epilogue's loads); pairs take as many as fit,
 // up to 8.
-template <int BN, int SCHED, int CG>
+template <int BN, int SCHED, int CG, int MT = 1>
 struct Smem {
-  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int A_BYTES = MT * BM * BK * 2;
   static constexpr int B_BYTES = (BN / CG) * BK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int OUT = SCHED == SCHED_SEG_K ? kStageOutBytes : 0;
@@ -218,15 +233,18 @@ struct Modes {
 // With CTA pairs (CG = 2) this CTA loads B columns rank*BN/2 .. of the n-tile, and every TMA load
 // of either CTA completes on rank 0's full barrier (lead_full), which rank 0 arms with the bytes of
 // both CTAs.
-template <int BN, int AMODE, int BMODE, int SCHED, int CG, bool kCounted = Modes<AMODE, BMODE>::kCpAsync>
+// MT = 2: the A tile holds two 128-row tiles (the second at sa + BM * 128 bytes); the second is
+// loaded only when it holds rows of the segment (t.two), and the MMA reads it only then.
+template <int BN, int AMODE, int BMODE, int SCHED, int CG, bool kCounted = Modes<AMODE, BMODE>::kCpAsync, int MT = 1>
 __device__ __forceinline__ void load_stage(const TcParams& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
                                            const Tile& t, int kb, uint32_t sa, uint32_t sb, uint32_t full_bar,
-                                           const bf16* const (&gsrc)[8], const uint32_t (&gbytes)[8], int ktok,
-                                           int rank, uint32_t lead_full) {
-  using SM = Smem<BN, SCHED, CG>;
+                                           const bf16* const (&gsrc)[8 * MT], const uint32_t (&gbytes)[8 * MT],
+                                           int ktok, int rank, uint32_t lead_full) {
+  using SM = Smem<BN, SCHED, CG, MT>;
   constexpr int BNC = BN / CG;   // B columns held by this CTA
-  constexpr uint32_t tma_bytes = (AMODE == A_TMA_K || AMODE == A_TMA_MN ? SM::A_BYTES : 0) +
-                                 (BMODE == B_TMA_K || BMODE == B_TMA_MN ? SM::B_BYTES : 0);
+  constexpr int kHalfA = BM * BK * 2;   // bytes of one 128-row A tile
+  const uint32_t tma_bytes = (AMODE == A_TMA_K || AMODE == A_TMA_MN ? (MT == 2 && !t.two ? kHalfA : SM::A_BYTES) : 0) +
+                             (BMODE == B_TMA_K || BMODE == B_TMA_MN ? SM::B_BYTES : 0);
   const int ptid = threadIdx.x;
   if (ptid == 0 && tma_bytes) {
     if (rank == 0) {
@@ -237,7 +255,10 @@ __device__ __forceinline__ void load_stage(const TcParams& p, const CUtensorMap*
       if (CG == 2) tma_load_2d_pair(dst, tm, c0, c1, lead_full);
       else tma_load_2d(dst, tm, c0, c1, full_bar);
     };
-    if (AMODE == A_TMA_K) load(sa, tmA, kb * BK, t.row0);
+    if (AMODE == A_TMA_K) {
+      load(sa, tmA, kb * BK, t.arow0);
+      if (MT == 2 && t.two) load(sa + kHalfA, tmA, kb * BK, t.arow0 + BM);
+    }
     if (AMODE == A_TMA_MN) {
 #pragma unroll
       for (int j = 0; j < BM / 64; ++j) load(sa + j * kChunkBytes, tmA, t.m * BM + j * 64, t.row0 + kb * BK);
@@ -252,10 +273,14 @@ __device__ __forceinline__ void load_stage(const TcParams& p, const CUtensorMap*
   if (AMODE == A_GATHER_K) {
     const int warp = ptid >> 5, lane = ptid & 31;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int r = warp * 32 + j * 4 + (lane >> 3);
-      const int c = lane & 7;
-      cp_async16(sa + r * 128 + ((c ^ (r & 7)) << 4), gsrc[j] + kb * BK, gbytes[j]);
+    for (int h = 0; h < MT; ++h) {
+      if (h == 1 && !t.two) break;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int r = warp * 32 + j * 4 + (lane >> 3);
+        const int c = lane & 7;
+        cp_async16(sa + h * kHalfA + r * 128 + ((c ^ (r & 7)) << 4), gsrc[h * 8 + j] + kb * BK, gbytes[h * 8 + j]);
+      }
     }
   }
   if (AMODE == A_GATHER_MN) {
@@ -354,17 +379,24 @@ __device__ __forceinline__ void epi_scale_store(const TcParams& p, const Tile& t
 // per MAC and the ring is deeper. Rank 1's MMA-warp lane relays "stage s of this CTA is full" to
 // rank 0's full barrier; rank 0's commits are multicast to both CTAs' empty / accumulator-full
 // barriers; both epilogues report "accumulator drained" to rank 0.
-template <int BN, int AMODE, int BMODE, int SCHED, int EPI, int CG>
-__global__ void __launch_bounds__(kThreads, 1)
+// MT = 2: each CTA computes two 128-row tiles of a segment (256 x BN) with two M = 128 MMAs per
+// K step that share the stage's B tile, so a stage carries twice the MMA work for 4/3 of the
+// bytes; the two accumulators fill TMEM (no double buffering) and eight epilogue warps drain them.
+template <int BN, int AMODE, int BMODE, int SCHED, int EPI, int CG, int MT>
+__global__ void __launch_bounds__(threads_for(MT), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2, TcParams p) {
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(CG == 1 || (CG == 2 && SCHED == SCHED_SEG_M && (AMODE == A_GATHER_K || AMODE == A_TMA_K) &&
                             (BMODE == B_TMA_K || BMODE == B_TMA_MN) && BN >= 128),
                 "CTA pairs: segment-M schedule, K-major A, B by TMA");
+  static_assert(MT == 1 || (MT == 2 && CG == 1 && SCHED == SCHED_SEG_M && (AMODE == A_GATHER_K || AMODE == A_TMA_K) &&
+                            BN == 256),
+                "two row tiles per CTA: segment-M schedule, K-major A, 256-column tiles");
   using MD = Modes<AMODE, BMODE>;
-  using SM = Smem<BN, SCHED, CG>;
+  using SM = Smem<BN, SCHED, CG, MT>;
   constexpr int NS = SM::NS;
+  constexpr int NACC = MT == 2 ? 1 : 2;   // accumulator buffers in TMEM
   constexpr uint32_t TMEM_COLS = 2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512);
   constexpr uint32_t IDESC = idesc_bf16(BM * CG, BN, MD::kAMn, MD::kBMn);
   extern __shared__ uint8_t smem_raw[];
@@ -390,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, CG == 2 ? 2 * kEpiWarps : kEpiWarps * 32);
+      mbar_init(tempty0 + 8 * a, CG == 2 ? 2 * kEpiWarps : MT * kEpiWarps * 32);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -414,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (CG == 2) cluster_sync();   // the peer's barriers are initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int ntiles = total_tiles<SCHED, CG>(p);
+  const int ntiles = total_tiles<SCHED, CG, MT>(p);
   const int tile0 = blockIdx.x / CG, tstep = gridDim.x / CG;
   const uint32_t lead_full0 = CG == 2 ? mapa_shared(full0, 0) : full0;   // rank 0's full barriers
 
@@ -423,13 +455,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0;
     bool ok = true;
     for (int L = tile0; L < ntiles && ok; L += tstep) {
-      const Tile t = map_tile<SCHED, CG>(p, L, rank);
-      const bf16* gsrc[8];
-      uint32_t gbytes[8];
+      const Tile t = map_tile<SCHED, CG, MT>(p, L, rank);
+      const bf16* gsrc[8 * MT];
+      uint32_t gbytes[8 * MT];
       if (AMODE == A_GATHER_K) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int r = warp * 32 + j * 4 + (lane >> 3);
+        for (int j = 0; j < 8 * MT; ++j) {
+          const int r = (j >> 3) * BM + warp * 32 + (j & 7) * 4 + (lane >> 3);
           const int row = t.row0 + r;
           const bool v = row < t.row_end;
           const int tok = v ? p.row_token[row] : 0;
@@ -464,8 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t sa = smem_u32(stage_base + s * SM::STAGE);
         const uint32_t sb = sa + SM::A_BYTES;
-        load_stage<BN, AMODE, BMODE, SCHED, CG>(p, &tmA, &tmB, t, kb, sa, sb, full0 + 8 * s, gsrc, gbytes, tk0,
-                                                rank, lead_full0 + 8 * s);
+        load_stage<BN, AMODE, BMODE, SCHED, CG, MD::kCpAsync, MT>(p, &tmA, &tmB, t, kb, sa, sb, full0 + 8 * s, gsrc,
+                                                                  gbytes, tk0, rank, lead_full0 + 8 * s);
         // the stage's full barrier counts this thread's arrival once all of its copies so far have
         // landed; the producer goes straight on to the next stage
         if (MD::kCpAsync) cp_async_mbar_arrive_noinc(full0 + 8 * s);
@@ -494,9 +526,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0, tcount = 0;
       bool ok = true;
       for (int L = tile0; L < ntiles && ok; L += tstep, ++tcount) {
-        const Tile t = map_tile<SCHED, CG>(p, L, rank);
-        const int acc = tcount & 1;
-        const uint32_t aph = (tcount >> 1) & 1;
+        const Tile t = map_tile<SCHED, CG, MT>(p, L, rank);
+        const int acc = tcount % NACC;
+        const uint32_t aph = (tcount / NACC) & 1;
         if (!(CG == 2 ? mbar_wait_cluster(tempty0 + 8 * acc, aph ^ 1, abort_flag, p.status)
                       : mbar_wait(tempty0 + 8 * acc, aph ^ 1, abort_flag, p.status)))
           break;
@@ -520,6 +552,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t db = MD::kBMn ? desc_mnmajor(sb + k * 2048) : desc_kmajor(sb + k * 32);
             if (CG == 2) mma_bf16_pair(dcol, da, db, IDESC, (kb > t.kb0 || k > 0) ? 1u : 0u);
             else mma_bf16(dcol, da, db, IDESC, (kb > t.kb0 || k > 0) ? 1u : 0u);
+            if (MT == 2 && t.two)   // second 128-row tile: its own accumulator, the same B tile
+              mma_bf16(dcol + BN, desc_kmajor(sa + BM * 128 + k * 32), db, IDESC, (kb > t.kb0 || k > 0) ? 1u : 0u);
           }
           if (CG == 2) mma_commit_pair_mc(empty0 + 8 * s, 0x3);
           else mma_commit(empty0 + 8 * s);
@@ -542,21 +576,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int ew = warp - kProducerWarps;     // 0..3 == warp % 4: TMEM lanes 32*ew..
-    const int r = ew * 32 + lane;             // tile row
+    const int ew = warp & 3;                  // TMEM lane quadrant of this warp: lanes 32*ew..
+    const int half = MT == 2 && warp > kMmaWarp ? 1 : 0;   // MT = 2: which 128-row tile it drains
+    const int r = half * BM + ew * 32 + lane;   // tile row
     int tcount = 0;
     for (int L = tile0; L < ntiles; L += tstep, ++tcount) {
-      const Tile t = map_tile<SCHED, CG>(p, L, rank);
-      const int acc = tcount & 1;
-      const uint32_t aph = (tcount >> 1) & 1;
+      const Tile t = map_tile<SCHED, CG, MT>(p, L, rank);
+      const int acc = tcount % NACC;
+      const uint32_t aph = (tcount / NACC) & 1;
       if (!(CG == 2 ? mbar_wait_cluster(tfull0 + 8 * acc, aph, abort_flag, p.status)
                     : mbar_wait(tfull0 + 8 * acc, aph, abort_flag, p.status)))
         break;
       tc_fence_after();
-      const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(ew * 32) << 16);
+      const uint32_t tbase = tmem_base + (acc + half) * BN + ((uint32_t)(ew * 32) << 16);
       const int row = t.row0 + r;   // SEG_M / DENSE output row
       const bool valid = row < t.row_end;
-      if (EPI == EPI_SWIGLU) {
+      if (MT == 2 && half && !t.two) {
+        // the second tile holds no rows of the segment: nothing was accumulated for it
+      } else if (EPI == EPI_SWIGLU) {
         epi_swiglu<BN>(p, t, tbase, row, valid);
       } else if (EPI == EPI_GATE || EPI == EPI_STORE) {
         epi_scale_store<BN, EPI == EPI_GATE>(p, t, tbase, row, valid);
@@ -955,11 +992,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // -------------------------------------------------------------- host side
-template <int BN, int AMODE, int BMODE, int SCHED, int EPI, int CG = 1>
+template <int BN, int AMODE, int BMODE, int SCHED, int EPI, int CG = 1, int MT = 1>
 cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcParams& p, int grid, cudaStream_t s,
                    const CUtensorMap* tmC = nullptr, const CUtensorMap* tmC2 = nullptr) {
-  auto kern = tc_gemm_kernel<BN, AMODE, BMODE, SCHED, EPI, CG>;
-  const int smem = Smem<BN, SCHED, CG>::TOTAL;
+  auto kern = tc_gemm_kernel<BN, AMODE, BMODE, SCHED, EPI, CG, MT>;
+  const int smem = Smem<BN, SCHED, CG, MT>::TOTAL;
   static bool attr = false;
   static int pair_grid = 0;   // CTAs of as many 2-CTA clusters as fit on the GPU at once
   if (!attr) {
@@ -968,7 +1005,7 @@ cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcParam
     attr = true;
   }
   if (CG == 1) {
-    kern<<<grid, kThreads, smem, s>>>(tmA, tmB, tmC ? *tmC : tmA, tmC2 ? *tmC2 : tmA, p);
+    kern<<<grid, threads_for(MT), smem, s>>>(tmA, tmB, tmC ? *tmC : tmA, tmC2 ? *tmC2 : tmA, p);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -1007,7 +1044,8 @@ constexpr int kBNdwd = 256;
 // segment with an odd tile count also computes an empty second tile), and the relay of gathered
 // rows to rank 0 costs a cluster-scope release per stage.
 bool use_pairs(const Layer& L, const Bufs&) { return L.pairs == 1; }
-
+// Two 128-row tiles per CTA for the segment GEMMs over token rows (gate/up, down, dY.Wd, dx).
+bool use_mt2(const Layer& L) { return L.row_tiles == 2 && L.pairs != 1; }
 TcParams base_params(const Layer& L, const Bufs& B) {
   TcParams p = {};
   p.row_token = B.row_token;
@@ -1015,6 +1053,7 @@ TcParams base_params(const Layer& L, const Bufs& B) {
   p.mt_off = B.mt_off;
   p.mp_off = B.mt_off + (L.E + L.S + 1);   // the routing scan stores the pair prefix after mt_off
   p.nseg = L.E + L.S;
+  p.pstride = L.E + L.S + 1;
   p.A_rows = B.A;
   p.status = L.status;
   return p;
@@ -1125,6 +1164,9 @@ cudaError_t launch_tc_gateup(const Layer& L, const Bufs& B, const void* x, cudaS
   if (use_pairs(L, B))
     return launch<kBNup, A_GATHER_K, B_TMA_K, SCHED_SEG_M, EPI_SWIGLU, 2>(L.tm_W13_h /*unused*/, L.tm_W13_h, p,
                                                                           L.num_sms, s);
+  if (use_mt2(L))
+    return launch<kBNup, A_GATHER_K, B_TMA_K, SCHED_SEG_M, EPI_SWIGLU, 1, 2>(L.tm_W13 /*unused*/, L.tm_W13, p,
+                                                                             L.num_sms, s);
   return launch<kBNup, A_GATHER_K, B_TMA_K, SCHED_SEG_M, EPI_SWIGLU>(L.tm_W13 /*unused*/, L.tm_W13, p, L.num_sms, s);
 }
 
@@ -1133,6 +1175,7 @@ cudaError_t launch_tc_down(const Layer& L, const Bufs& B, cudaStream_t s) {
   if (!make_tmap(&th, B.h, L.f, B.R, BK, BM)) return cudaErrorInvalidValue;
   const TcParams p = down_params(L, B);
   if (use_pairs(L, B)) return launch<kBNdown, A_TMA_K, B_TMA_K, SCHED_SEG_M, EPI_GATE, 2>(th, L.tm_Wd_h, p, L.num_sms, s);
+  if (use_mt2(L)) return launch<kBNdown, A_TMA_K, B_TMA_K, SCHED_SEG_M, EPI_GATE, 1, 2>(th, L.tm_Wd, p, L.num_sms, s);
   return launch<kBNdown, A_TMA_K, B_TMA_K, SCHED_SEG_M, EPI_GATE>(th, L.tm_Wd, p, L.num_sms, s);
 }
 
@@ -1185,6 +1228,9 @@ cudaError_t launch_tc_bwd_dh(const Layer& L, const Bufs& B, const void* dy, cuda
   if (use_pairs(L, B))
     return launch<kBNdh, A_GATHER_K, B_TMA_MN, SCHED_SEG_M, EPI_DH, 2>(L.tm_Wd_mn /*unused*/, L.tm_Wd_mn, p,
                                                                        L.num_sms, s);
+  if (use_mt2(L))
+    return launch<kBNdh, A_GATHER_K, B_TMA_MN, SCHED_SEG_M, EPI_DH, 1, 2>(L.tm_Wd_mn /*unused*/, L.tm_Wd_mn, p,
+                                                                          L.num_sms, s);
   return launch<kBNdh, A_GATHER_K, B_TMA_MN, SCHED_SEG_M, EPI_DH>(L.tm_Wd_mn /*unused*/, L.tm_Wd_mn, p, L.num_sms,
                                                                   s);
 }
@@ -1200,6 +1246,7 @@ cudaError_t launch_tc_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s) {
   p.out = B.dx_rows;
   p.ldo = L.d;
   if (use_pairs(L, B)) return launch<kBNdx, A_TMA_K, B_TMA_MN, SCHED_SEG_M, EPI_STORE, 2>(ta, L.tm_W13_mn, p, L.num_sms, s);
+  if (use_mt2(L)) return launch<kBNdx, A_TMA_K, B_TMA_MN, SCHED_SEG_M, EPI_STORE, 1, 2>(ta, L.tm_W13_mn, p, L.num_sms, s);
   return launch<kBNdx, A_TMA_K, B_TMA_MN, SCHED_SEG_M, EPI_STORE>(ta, L.tm_W13_mn, p, L.num_sms, s);
 }
 

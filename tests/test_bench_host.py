@@ -83,3 +83,77 @@ def test_committed_traffic_entries_name_their_captures():
         for s in ent["sources"]:
             assert os.path.exists(os.path.join(ROOT, s)), (group, s)
         assert ent["dram_bytes_per_launch"] > 0
+
+
+def test_layer_work_deepseek_v3_forward_matches_the_survey_figures():
+    # every routed expert used, plus the shared one: 22.64 GB of bf16 expert weights, 3.7 MB of router
+    # weight and 235 MB of x and y; 6.49 TFLOP of expert products plus 0.03 of router GEMM
+    spec = moe_synth.DSV3_UNIFORM
+    cnt = np.full(spec.E, spec.T * spec.k // spec.E)
+    fl, by = bench.layer_work(spec, cnt)
+    assert abs(by - (257 * 3 * 2048 * 7168 * 2 + 256 * 7168 * 2 + 2 * 8192 * 7168 * 2)) == 0
+    assert np.isclose(by / 1e9, 22.88, atol=0.01)
+    assert np.isclose(fl / 1e12, 6.49 + 0.03, atol=0.01)
+    # an expert without tokens moves no weights
+    cnt[:16] = 0
+    _, by16 = bench.layer_work(spec, cnt)
+    assert by - by16 == 16 * 3 * 2048 * 7168 * 2
+    # the h and o round trips are not algorithmic work: the whole-call bytes stay well under the
+    # per-kernel sum that counts them
+    w = bench.work_per_group(spec, np.full(spec.E, 256), training=False)
+    assert sum(w[g][1] for g in ("router_logits", "gateup", "down", "combine")) > by + 2.5e9
+
+
+def test_layer_work_training_step_matches_the_survey_figures():
+    # fwd: weights 1.107 GB + x, y 17 MB; bwd: weights read again 1.107 GB, weight gradients of every expert
+    # 1.107 GB, x, dy, dx 25 MB, saved u, v 69 MB (written by the forward, read by the backward)
+    spec = moe_synth.BF16_T2048
+    cnt = np.full(spec.E, spec.T * spec.k // spec.E)
+    fl_f, by_f = bench.layer_work(spec, cnt, "fwd")
+    fl, by = bench.layer_work(spec, cnt, "fwd+bwd")
+    W = 64 * 3 * 1408 * 2048 * 2
+    assert np.isclose(W / 1e9, 1.107, atol=1e-3)
+    assert by_f == W + 64 * 2048 * 2 + 2 * 2048 * 2048 * 2
+    uv = 12288 * 2 * 1408 * 2
+    assert by - by_f == W + W + 3 * 2048 * 2048 * 2 + 2 * uv
+    assert np.isclose(fl_f / 1e9, 213, atol=1) and np.isclose((fl - fl_f) / 1e9, 426, atol=2)
+    # fp32 storage doubles the bytes of the same shapes
+    tiny = moe_synth.TINY_FP32
+    _, by32 = bench.layer_work(tiny, np.full(tiny.E, 16))
+    assert by32 == 8 * 3 * 128 * 256 * 4 + 8 * 256 * 4 + 2 * 64 * 256 * 4
+
+
+def test_roof_line_bound_and_fraction():
+    r = bench.roof_line(2.0, 2e12, 8e9, PK)                 # 1 ms of tensor work, 1 ms of HBM at 8 TB/s
+    assert np.isclose(r["roofline_ms"], 1.0) and np.isclose(r["frac_of_roofline"], 0.5)
+    r = bench.roof_line(2.0, 1e12, 8e9, PK)
+    assert r["bound"] == "hbm" and np.isclose(r["roofline_ms"], 1.0)
+    r = bench.roof_line(2.0, 8e12, 4e9, PK, tensor_peak=4000.0)   # a tensor peak other than bf16's
+    assert r["bound"] == "tensor" and np.isclose(r["roofline_ms"], 2.0) and np.isclose(r["frac_of_roofline"], 1.0)
+
+
+def test_mxfp8_step_work_ideal_once_and_per_chunk():
+    spec = moe_synth.DSV3_MXFP8
+    w_axis = 3 * 257 * 2048 * 7168 * (1 + 1 / 32)
+    grads = 3 * 257 * 2048 * 7168 * 2
+    acts = 4 * 8192 * 7168 * 2
+    (fi, bi), (fc, bc) = bench.mx_step_work(spec, 4, 3, 6.5e12, 13e12)
+    assert np.isclose(bi, 2 * w_axis + grads + acts)
+    # 4 chunk forwards + 1 recomputed (3 ring slots), 4 chunk backwards: 9 weight streams
+    assert np.isclose(bc, 9 * w_axis + grads + acts)
+    assert np.isclose(bc / 1e9, 128.0, atol=1.5)
+    assert np.isclose(fc, 6.5e12 * 1.25 + 13e12) and fi == 6.5e12 + 13e12
+    # a ring that holds every chunk recomputes nothing
+    _, (fc4, bc4) = bench.mx_step_work(spec, 4, 4, 6.5e12, 13e12)
+    assert np.isclose(bc4, 8 * w_axis + grads + acts) and fc4 == fi
+
+
+def test_both_arms_report_the_same_config():
+    spec = moe_synth.BF16_T2048
+    assert bench.bench_config(spec, 1) == bench.bench_config(spec, 1)
+    assert bench.bench_config(spec, 2)["global_batch"] == 2 * spec.T
+
+
+def test_host_cpu_reports_model_and_cores():
+    h = bench.host_cpu()
+    assert h["nproc"] == os.cpu_count() and isinstance(h["model"], str) and h["model"]

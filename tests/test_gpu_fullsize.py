@@ -5,10 +5,15 @@
   GPU's logits, reruns bit-identical; the step captured in a CUDA graph (as bench.py times it)
   and replayed on new inputs gives the eager calls' results bit for bit.
 * DeepSeek-V3 shapes (T=8192, d=7168, 256 + 1 experts, f=2048, top-8 sigmoid x 2.5), uniform
-  and Zipf(1.2): forward on a sample of tokens. Tokens are independent in the forward, so the
+  and Zipf(1.2): forward on 512 sampled tokens. Tokens are independent in the forward, so the
   oracle evaluates only the sampled rows (with the GPU's fp32 logits for those rows, so both
   sides route identically), fetching each expert's weights from the device as it needs them.
-* decode B = 1, 4, 16 on the DeepSeek-V3 weights against the oracle.
+  The GPU's router logits of the sampled rows are compared with the oracle's own.
+* decode B = 1, 4, 16 on the DeepSeek-V3 weights against the oracle, and the decode path's own
+  router end to end (its output against the oracle routed on the oracle's logits).
+* End-to-end routing (every workload above, all tokens): the GPU's indices agree with the
+  oracle's own selection wherever the top-k key gaps exceed 4x the measured logit error; the
+  count of such index exceptions must be 0 and is reported with the near-tie count.
 """
 import numpy as np
 import pytest
@@ -17,6 +22,7 @@ import torch
 import moe_synth
 from mixture_experts_layer_routing_gb300 import MoeLayer, moe_backward, moe_forward
 from oracle import moe_oracle as oracle
+from routing_checks import report, routing_exceptions
 
 pytestmark = pytest.mark.gpu
 
@@ -71,8 +77,12 @@ def test_bf16_T2048_fwd_bwd_full():
         errs[name] = oracle.rel_frobenius(np64(g[name]), ref[name])
     assert all(v <= TOL_BF16 for v in errs.values()), errs
     # end to end the GPU and oracle logits agree closely, and the selection agrees off near-ties
-    l_ref = oracle.router_logits(n["x"], n["Wr"])
-    assert np.max(np.abs(logits - l_ref)) < 1e-3
+    o4 = routing_exceptions(r["idx"].cpu().numpy(), logits, n["x"], n["Wr"], n["b"], spec.k)
+    report("routing end to end, bf16 T=2048 E=64 top-6", tokens=o4["tokens"], logit_err=o4["logit_err"],
+           index_exceptions=o4["exceptions"], near_ties=o4["near_ties"],
+           near_tie_disagreements=o4["near_tie_disagreements"])
+    assert o4["logit_err"] < 1e-3
+    assert o4["exceptions"] == 0, o4["exceptions"]
     # rerun: bit-identical
     y2 = layer.forward(inp["x"], ctx=ctx)
     g2 = layer.backward(inp["x"], inp["dy"], ctx)
@@ -147,14 +157,27 @@ def test_dsv3_forward_sampled_tokens(dsv3):
     assert torch.equal(y, y_again)
     cnt = r["cnt"].cpu().numpy()
     assert cnt.sum() == spec.T * spec.k
+    Wr, b = np64(inp["Wr"]), np64(inp["b"])
+    # the router GEMM at this shape (E = 256, d = 7168) against the oracle's logits, and the
+    # selection end to end, over all T tokens
+    logits = r["logits"].cpu().numpy()
+    o4 = routing_exceptions(r["idx"].cpu().numpy(), logits, np64(inp["x"]), Wr, b, spec.k)
+    report(f"routing end to end, {spec.name}", tokens=o4["tokens"], logit_err=o4["logit_err"],
+           index_exceptions=o4["exceptions"], near_ties=o4["near_ties"],
+           near_tie_disagreements=o4["near_tie_disagreements"])
+    assert o4["logit_err"] < 1e-3, o4["logit_err"]
+    assert o4["exceptions"] == 0, o4["exceptions"]
     rng = np.random.default_rng(0)
-    sample = np.sort(rng.choice(spec.T, size=96, replace=False))
+    sample = np.sort(rng.choice(spec.T, size=512, replace=False))
     xs = np64(inp["x"][sample])
-    ls = r["logits"][sample].cpu().numpy()
-    ys = oracle.forward(xs, np64(inp["Wr"]), np64(inp["b"]), DeviceExperts(inp["Wg"]), DeviceExperts(inp["Wu"]),
-                        DeviceExperts(inp["Wd"]), logits32=ls, **kw(spec))
+    ls = logits[sample]
+    # element by element on the sampled rows (the rows the expert check below uses)
+    assert np.max(np.abs(ls - oracle.router_logits(xs, Wr))) < 1e-3
+    ys = oracle.forward(xs, Wr, b, DeviceExperts(inp["Wg"]), DeviceExperts(inp["Wu"]), DeviceExperts(inp["Wd"]),
+                        logits32=ls, **kw(spec))
     assert np.array_equal(r["idx"][sample].cpu().numpy(), ys["idx"])
     err = oracle.rel_frobenius(np64(y[sample]), ys["y"])
+    report(f"forward on 512 sampled tokens, {spec.name}", rel_frobenius=err)
     assert err <= TOL_BF16, err
 
 
@@ -175,3 +198,20 @@ def test_dsv3_decode(dsv3, B):
     yd2 = layer.decode(x)
     torch.cuda.synchronize()
     assert torch.equal(yd, yd2)
+    # the decode path routes with its own kernel, whose indices it does not return: check it end to end
+    # through its output, against the oracle routed on the oracle's own logits. A token off the
+    # near-ties (gaps above 4x the logit error, at least 1e-4) whose output is far from that
+    # reference (a wrong expert moves a token's output by tens of percent) is an index exception.
+    o4 = routing_exceptions(r["idx"].cpu().numpy(), r["logits"].cpu().numpy(), np64(x), np64(inp["Wr"]),
+                            np64(inp["b"]), spec.k, err_floor=1e-4)
+    own = oracle.decode(np64(x), np64(inp["Wr"]), np64(inp["b"]), DeviceExperts(inp["Wg"]), DeviceExperts(inp["Wu"]),
+                        DeviceExperts(inp["Wd"]), **kw(spec))
+    yd64 = np64(yd)
+    per_token = np.array([oracle.rel_frobenius(yd64[t], own["y"][t]) for t in range(B)])
+    sure = o4["sure"]
+    exceptions = int(np.count_nonzero(sure & (per_token > 2e-2)))
+    report(f"decode router end to end, B={B}", tokens=B, near_ties=int(np.count_nonzero(~sure)),
+           index_exceptions=exceptions, max_token_rel_err=float(per_token[sure].max()) if sure.any() else 0.0)
+    assert exceptions == 0, per_token
+    if sure.any():
+        assert oracle.rel_frobenius(yd64[sure], own["y"][sure]) <= TOL_BF16

@@ -14,6 +14,7 @@ import torch
 import moe_synth
 from mixture_experts_layer_routing_gb300 import MoeLayer
 from oracle import moe_oracle as oracle
+from routing_checks import report, routing_exceptions
 
 pytestmark = pytest.mark.gpu
 
@@ -149,6 +150,13 @@ def test_dsv3_mxfp8_chunked_fullsize_sampled_experts():
     cnt = r["cnt"].cpu().numpy()
     assert cnt.sum() == spec.T * spec.k                    # dropless
     logits = r["logits"].cpu().numpy()
+    # the MXFP8 layer's router (bf16 tensor-core GEMM) against the oracle's logits, and its selection
+    # end to end, over all T tokens
+    o4 = routing_exceptions(r["idx"].cpu().numpy(), logits, np64(inp["x"]), np64(inp["Wr"]), np64(inp["b"]),
+                            spec.k)
+    report(f"routing end to end, {spec.name}", tokens=o4["tokens"], logit_err=o4["logit_err"],
+           index_exceptions=o4["exceptions"], near_ties=o4["near_ties"])
+    assert o4["logit_err"] < 1e-3 and o4["exceptions"] == 0, (o4["logit_err"], o4["exceptions"])
     rng = np.random.default_rng(1)
     sample = sorted({int(np.argmax(cnt)), spec.E, int(rng.integers(spec.E))})   # hottest, shared, random
     n = {k: np64(inp[k]) for k in ("x", "dy", "Wr", "b")}

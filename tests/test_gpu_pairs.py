@@ -81,3 +81,38 @@ def test_pairs_parity(spec, bias):
     if bias is not None:
         assert (tiles == 0).any()
     layer.close()
+
+
+def interleaved(cnt_with_shared):
+    """Whether the routing scan interleaves dense and sparse experts for these counts (its rule:
+    experts with >= 3 row tiles hold a quarter of the tiles and the others average under 1.5)."""
+    tiles = (np.asarray(cnt_with_shared) + 127) // 128
+    cand = tiles >= 3
+    return 4 * tiles[cand].sum() >= tiles.sum() and 2 * tiles[~cand].sum() < 3 * np.count_nonzero(~cand & (tiles > 0))
+
+
+@pytest.mark.parametrize("spec,bias", CASES, ids=[c[0].name for c in CASES])
+def test_two_row_tiles_per_cta_bit_identical(spec, bias):
+    """Mode 2 (one CTA per two 128-row tiles of an expert, two M = 128 MMAs per K step sharing the
+    staged weight tile) computes every output element with the same instructions in the same K order
+    as mode 0: results must be bit-identical, forward and backward, and rerun bit-identically. The
+    cases give experts odd tile counts (a lone last tile), single partial tiles and no tiles, in the
+    segment-major order (uniform case) and the dense/sparse interleave (skewed case)."""
+    inp = moe_synth.make_inputs(spec, DEV, grad=True)
+    if bias is not None:
+        inp["b"] = torch.as_tensor(bias, dtype=torch.float32, device=DEV)
+    layer = MoeLayer.from_spec(spec, device=DEV)
+    layer.set_weights(inp["Wr"], inp["b"], inp["Wg"], inp["Wu"], inp["Wd"])
+    two = run(layer, inp, 2)
+    two2 = run(layer, inp, 2)
+    one = run(layer, inp, 0)
+    for k in one:
+        assert torch.equal(two[k], two2[k]), k
+        assert torch.equal(two[k], one[k]), k
+    cnt = layer.route(inp["x"])["cnt"].cpu().numpy()
+    full = np.concatenate([cnt, [spec.T] * spec.S])
+    tiles = (full + 127) // 128
+    assert (tiles % 2 == 1).any() and (tiles >= 2).any()
+    assert interleaved(full) == (bias is not None)
+    moe_set_pairs(layer.h, 0)
+    layer.close()

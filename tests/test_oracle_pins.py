@@ -520,3 +520,39 @@ def test_backward_expert_filter_matches_full_backward():
         for e in (1, 3):
             for n in ("dWg", "dWu", "dWd"):
                 np.testing.assert_array_equal(part[n][e], full[n][e])
+
+
+# ------------------------------------------------------------ the checkers
+
+def test_rel_frobenius_hand_cases():
+    # ||(0, 1)|| / ||(3, 4)|| = 1 / 5
+    assert oracle.rel_frobenius([[3.0, 5.0]], [[3.0, 4.0]]) == pytest.approx(0.2, abs=1e-15)
+    # every element counts, squared: diff (-3, 0, 0, 1) against ref norm 5 -> sqrt(10) / 5
+    assert oracle.rel_frobenius([[0.0, 0.0], [0.0, 5.0]], [[3.0, 0.0], [0.0, 4.0]]) == \
+        pytest.approx(math.sqrt(10) / 5, abs=1e-15)
+    # relative to the reference, not to the argument: swapping them changes the value
+    assert oracle.rel_frobenius([[3.0, 4.0]], [[3.0, 5.0]]) == pytest.approx(1 / math.sqrt(34), abs=1e-15)
+    # a sign flip is an error of twice the norm
+    assert oracle.rel_frobenius([[-1.0, -2.0]], [[1.0, 2.0]]) == pytest.approx(2.0, abs=1e-15)
+    assert oracle.rel_frobenius(np.zeros((2, 3)), np.zeros((2, 3))) == 0.0
+
+
+def test_routing_check_margins_and_exceptions():
+    from routing_checks import key_margins, routing_exceptions
+    # keys of token 0: 3, 2, 1.5, 0 (k = 2: gaps among the 3 largest are 1 and 0.5); token 1 has a tie
+    logits = np.array([[3.0, 2.0, 1.5, 0.0], [1.0, 1.0, 0.0, -1.0]], np.float32)
+    bias = np.zeros(4, np.float32)
+    assert key_margins(logits, bias, 2).tolist() == [0.5, 0.0]
+    # the bias enters the keys: +1 on expert 3 makes token 0's keys 3, 2, 1.5, 1 -> gaps 1, 0.5
+    assert key_margins(logits, np.array([0, 0, 0, 1], np.float32), 2).tolist() == [0.5, 0.0]
+    # routing_exceptions computes the oracle's logits from x and Wr: with Wr = I the logits are x
+    x = logits.astype(np.float64)
+    Wr = np.eye(4)
+    ok = routing_exceptions(np.array([[0, 1], [0, 1]]), logits, x, Wr, bias, 2)
+    assert ok["exceptions"] == 0 and ok["near_ties"] == 1 and ok["logit_err"] == 0.0
+    # a wrong expert on the well-separated token is an exception; on the tied token it is not
+    bad = routing_exceptions(np.array([[0, 2], [1, 0]]), logits, x, Wr, bias, 2)
+    assert bad["exceptions"] == 1 and bad["near_tie_disagreements"] == 1
+    # a large measured logit error turns token 0 into a near-tie as well (4 x 0.2 > 0.5)
+    noisy = routing_exceptions(np.array([[0, 2], [0, 1]]), logits + np.float32(0.2), x, Wr, bias, 2)
+    assert noisy["near_ties"] == 2 and noisy["exceptions"] == 0
