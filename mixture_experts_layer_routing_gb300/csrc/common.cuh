@@ -74,7 +74,10 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
-__device__ __forceinline__ float sigmoid_f(float z) { return 1.0f / (1.0f + __expf(-z)); }
+// silu(z) = z / (1 + e^-z) and sigmoid(z) = 1 / (1 + e^-z) with the fast reciprocal-based divide
+// (a few ulp; the slow IEEE divide made the SwiGLU backward epilogue the bound of its GEMM). For
+// z -> -inf the denominator overflows to inf and both return 0, the limits.
+__device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+__device__ __forceinline__ float sigmoid_f(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
 
 }  // namespace moe
