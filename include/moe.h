@@ -89,8 +89,9 @@ typedef struct {
  * the config (MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED) and allocates one
  * small device array (the status word, the decode router's counter and the
  * fused kernel's per-row-block counters: 4 x (T_max (k+S) / 128 + E + S + 68)
- * bytes, the library's only allocation); on the bf16 tensor-core path it also
- * creates one stream and three events for moe_backward's side work. */
+ * bytes, the library's only allocation); on the tensor-core paths (bf16 and
+ * MXFP8) it also creates one stream and three events for side work
+ * (moe_backward's router backward, moe_train_chunked's next-chunk routing). */
 moe_status moe_create(const moe_config* cfg, moe_handle* out);
 moe_status moe_destroy(moe_handle h);
 
@@ -158,8 +159,13 @@ moe_status moe_backward(moe_handle h, const void* x, const void* dy, int T, cons
  * order (fp32 within a chunk, one bf16 rounding per chunk; dWr in fp32).
  * ring (device, >= slot_bytes, 256-byte aligned) and workspace (device,
  * workspace_bytes) come from moe_train_chunked_sizes. *recomputed (nullable,
- * host) receives the number of recomputed chunk forwards. Asynchronous on
- * `stream` like every compute call. */
+ * host) receives the number of recomputed chunk forwards. With at least two
+ * ring slots, the routing of chunk c + 1 (router GEMM, top-k, counts,
+ * offsets, permutation) runs on the handle's own stream while chunk c's
+ * expert GEMMs run (the page's "medium granularity" overlap, on one GPU),
+ * forked from and joined back into `stream` with events, so the call stays
+ * asynchronous on `stream` and capturable in a CUDA graph; results do not
+ * depend on it. Asynchronous on `stream` like every compute call. */
 moe_status moe_train_chunked_sizes(moe_handle h, int T, size_t* slot_bytes, size_t* workspace_bytes,
                                    int* n_chunks);
 moe_status moe_train_chunked(moe_handle h, const void* x, const void* dy, int T, void* y, void* dx, float* dWr,

@@ -224,12 +224,11 @@ struct MxDefer {
   const int* base;  // [nseg] row where each expert's rows of the current chunk start
 };
 
-// Forward of T >= 1 tokens (arguments already validated).
-moe_status forward_body(moe_handle_s* h, const void* x, int T, void* y, void* ctx, void* workspace, cudaStream_t s) {
+// The expert part of a forward of T >= 1 tokens whose routing is in ctx (or the workspace).
+moe_status forward_experts(moe_handle_s* h, const void* x, int T, void* y, void* ctx, void* workspace,
+                           cudaStream_t s) {
   const Layer& L = h->L;
   Bufs B = carve(L, T, workspace, ctx, nullptr);
-  moe_status st = run_route(h, B, x, nullptr, s);
-  if (st != MOE_OK) return st;
   if (h->mx) {
     CK(run(h, s, G_MX_QUANT, 1, [&] { return launch_mx_quant_rows(x, T, L.d, B.xq, B.xs, s); }));
     CK(run(h, s, G_GATEUP, 1, [&] { return launch_mx_gateup(L, B, s); }));
@@ -245,6 +244,14 @@ moe_status forward_body(moe_handle_s* h, const void* x, int T, void* y, void* ct
   }
   CK(run(h, s, G_COMBINE, 1, [&] { return launch_combine(L, B, y, s); }));
   return MOE_OK;
+}
+
+// Forward of T >= 1 tokens (arguments already validated).
+moe_status forward_body(moe_handle_s* h, const void* x, int T, void* y, void* ctx, void* workspace, cudaStream_t s) {
+  const Bufs B = carve(h->L, T, workspace, ctx, nullptr);
+  const moe_status st = run_route(h, B, x, nullptr, s);
+  if (st != MOE_OK) return st;
+  return forward_experts(h, x, T, y, ctx, workspace, s);
 }
 
 // Backward of T >= 1 tokens with the forward's ctx (arguments already validated). acc: add the
@@ -320,6 +327,7 @@ struct ChunkPlan {
   int chunk, n;
   size_t slot, fwd_ws, bwd_ws, comb;   // comb: MXFP8 combined weight-gradient operands (0 otherwise)
   size_t rc;                           // rows of the combined operands
+  size_t part;                         // router split-K partials of the side-stream routing (0: none)
 };
 ChunkPlan chunk_plan(const moe_handle_s* h, int T) {
   ChunkPlan c;
@@ -332,6 +340,7 @@ ChunkPlan chunk_plan(const moe_handle_s* h, int T) {
   c.bwd_ws = al(z.bwd_ws);
   c.comb = 0;
   c.rc = 0;
+  c.part = (h->side && c.n > 1) ? al(kRouterPartBytes) : 0;
   if (h->mx) {
     const size_t nseg = L.E + L.S, d = L.d, f = L.f;
     c.rc = ((size_t)T * L.k + (size_t)L.S * T + 127) / 128 * 128 + 128 * nseg * (size_t)c.n;
@@ -409,7 +418,8 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
   L.dep = (unsigned*)(words + 68);
   if (c.prec == MOE_MXFP8) L.G = kGateMx;
   h->tc = (c.prec == MOE_BF16) && tc_supported(L);
-  if (h->tc) {
+  h->mx = (c.prec == MOE_MXFP8) && mx_supported(L);
+  if (h->tc || h->mx) {
     int lo = 0, hi = 0;
     if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess ||
         cudaStreamCreateWithPriority(&h->side, cudaStreamNonBlocking, hi) != cudaSuccess ||
@@ -422,9 +432,9 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
       return MOE_ERR_CUDA;
     }
   }
-  h->mx = (c.prec == MOE_MXFP8) && mx_supported(L);
   h->tc_router = h->tc || h->mx;
   if (c.prec == MOE_MXFP8 && !h->mx) {
+    destroy_side(h);
     cudaFree(words);
     delete h;
     *out = nullptr;
@@ -550,7 +560,7 @@ moe_status moe_train_chunked_sizes(moe_handle h, int T, size_t* slot_bytes, size
   if (!h || T < 1 || T > h->cfg.T_max) return MOE_ERR_INVALID_ARG;
   const ChunkPlan c = chunk_plan(h, T);
   if (slot_bytes) *slot_bytes = c.slot;
-  if (workspace_bytes) *workspace_bytes = c.fwd_ws + c.bwd_ws + c.comb;
+  if (workspace_bytes) *workspace_bytes = c.fwd_ws + c.bwd_ws + c.comb + c.part;
   if (n_chunks) *n_chunks = c.n;
   return MOE_OK;
 }
@@ -597,13 +607,41 @@ moe_status moe_train_chunked(moe_handle h, const void* x, const void* dy, int T,
     t0 = ch * c.chunk;
     Tc = (T - t0) < c.chunk ? (T - t0) : c.chunk;
   };
-  // forward: chunk ch saves its routing and pre-activations into slot ch mod R
+  // forward: chunk ch saves its routing and pre-activations into slot ch mod R. With a side stream
+  // and at least two slots, chunk ch + 1's routing (router GEMM, top-k, counts, permutation, into its
+  // own slot; split-K partials in a buffer of its own) runs on the side stream while chunk ch's expert
+  // GEMMs run, forked once chunk ch's routing is done (the chunk histograms are free then) and joined
+  // before chunk ch + 1's expert GEMMs. One slot would be shared by both chunks' routing arrays.
+  const bool overlap = c.part && !h->prof && R >= 2;
+  auto route_chunk = [&](int ch, cudaStream_t st_, float* part) {
+    int t0, Tc;
+    span(ch, t0, Tc);
+    const Bufs Bc = carve(L, Tc, ws_f, slot_of(ch), nullptr);
+    return run_route(h, Bc, (const char*)x + t0 * row_bytes, nullptr, st_, part, part ? kRouterPartBytes : 0);
+  };
+  float* side_part = (float*)(ws_b + c.bwd_ws + c.comb);
+  if (overlap) {
+    const moe_status st = route_chunk(0, s, nullptr);
+    if (st != MOE_OK) return st;
+  }
   for (int ch = 0; ch < c.n; ++ch) {
     int t0, Tc;
     span(ch, t0, Tc);
-    const moe_status st = forward_body(h, (const char*)x + t0 * row_bytes, Tc, (char*)y + t0 * row_bytes,
-                                       slot_of(ch), ws_f, s);
+    const bool fork = overlap && ch + 1 < c.n;
+    if (fork) {
+      CK(cudaEventRecord(h->ev_dh, s));
+      CK(cudaStreamWaitEvent(h->side, h->ev_dh, 0));
+      const moe_status st = route_chunk(ch + 1, h->side, side_part);
+      if (st != MOE_OK) return st;
+      CK(cudaEventRecord(h->ev_join, h->side));
+    }
+    const moe_status st =
+        overlap ? forward_experts(h, (const char*)x + t0 * row_bytes, Tc, (char*)y + t0 * row_bytes, slot_of(ch),
+                                  ws_f, s)
+                : forward_body(h, (const char*)x + t0 * row_bytes, Tc, (char*)y + t0 * row_bytes, slot_of(ch),
+                               ws_f, s);
     if (st != MOE_OK) return st;
+    if (fork) CK(cudaStreamWaitEvent(s, h->ev_join, 0));
     if (h->mx) {
       const Bufs Bc = carve(L, Tc, nullptr, slot_of(ch), nullptr);
       CK(cudaMemcpyAsync(chunk_mt + (size_t)ch * (L.E + L.S + 1), Bc.mt_off, 4 * (size_t)(L.E + L.S + 1),

@@ -20,8 +20,9 @@ struct moe_handle_s {
   long long launches = 0;
   std::vector<ProfRec> recs;
   std::vector<cudaEvent_t> pool;
-  // Backward side stream: the router backward and the dx gather-sum run beside the dx and
-  // weight-gradient GEMMs (fork / join with these events; capturable in a CUDA graph).
+  // Side stream: the router backward and the dx gather-sum run beside the dx and weight-gradient
+  // GEMMs, and in a chunked step the next chunk's routing beside this chunk's expert GEMMs (fork /
+  // join with these events; capturable in a CUDA graph).
   // moe_decode runs the grouped-GEMM forward for B >= decode_gemm_from (the measured crossover)
   int decode_gemm_from = moe::kDecodeGemmFrom;
   cudaStream_t side = nullptr;

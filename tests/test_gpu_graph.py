@@ -84,3 +84,49 @@ def test_decode_graph_replay_matches_eager():
     assert layer.status() == 0
     assert torch.equal(got, y)
     layer.close()
+
+
+@pytest.mark.parametrize("prec", ["bf16", "mxfp8"])
+def test_chunked_step_graph_replay_matches_eager(prec):
+    """The chunked training step forks the next chunk's routing onto the handle's side stream and
+    joins it back with events (three chunks over two ring slots, so the fork is taken): captured in
+    a graph and replayed on new inputs it must give the eager call's results bit for bit."""
+    from mixture_experts_layer_routing_gb300 import moe_train_chunked, moe_train_chunked_sizes
+    spec = SPEC.with_(name=f"{prec}_T600_d512_E16+1_f256_top4_chunk256", T=600, dtype=prec, chunk=256, seed=82)
+    inp = moe_synth.make_inputs(spec, DEV, grad=True)
+    layer = MoeLayer.from_spec(spec, device=DEV)
+    layer.set_weights(inp["Wr"], inp["b"], inp["Wg"], inp["Wu"], inp["Wd"])
+    T = spec.T
+    z = moe_train_chunked_sizes(layer.h, T)
+    assert z["n_chunks"] == 3
+    ring = layer.buffer("ring", 2 * z["slot"])
+    ws = layer.buffer("chunk_ws", z["workspace"])
+    x, dy = inp["x"].clone(), inp["dy"].clone()
+    y = torch.empty_like(x)
+    g = layer.grads_like(x)
+
+    def step():
+        moe_train_chunked(layer.h, x, dy, T, y, g["dx"], g["dWr"], g["dWg"], g["dWu"], g["dWd"], ring, 2 * z["slot"],
+                          ws)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    new = moe_synth.make_tokens(spec, 2, DEV, seed_offset=6)
+    x.copy_(new[0])
+    dy.copy_(new[1])
+    graph.replay()
+    torch.cuda.synchronize()
+    got = {"y": y.clone(), **{k: v.clone() for k, v in g.items()}}
+    step()
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert torch.equal(got["y"], y)
+    for k, v in g.items():
+        assert torch.equal(got[k], v), k
+    layer.close()
