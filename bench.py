@@ -731,7 +731,7 @@ def run_extra(args, dev, pk, summary):
         torch.cuda.empty_cache()
     extra.update(run_extra_mxfp8(dev, pk, summary))
     extra["bf16_T128_d2048_E64_f1408_top6 fwd+bwd, eager vs CUDA graph"] = graph_vs_eager(dev)
-    extra["forward, gate/up + down as one persistent kernel vs two launches"] = fused_vs_separate(dev)
+    extra["forward as one persistent kernel (expert GEMMs / whole forward) vs separate launches"] = fused_vs_separate(dev)
     return extra
 
 
@@ -798,8 +798,9 @@ def graph_vs_eager(dev, T=128, steps=50):
 
 def fused_vs_separate(dev, steps=30):
     """Forward milliseconds (CUDA-graph replay, so launch gaps are the graph's) with the gate/up and
-    down GEMMs as one persistent kernel (moe_set_fused 1) and as two launches (0), on the 2048-token
-    bench layer at several T and on the DeepSeek-V3-shaped layer (uniform routing) at T=8192."""
+    down GEMMs as one persistent kernel (moe_set_fused 1), the whole forward as one persistent kernel
+    (2), and separate launches (0), on the 2048-token bench layer at several T and on the
+    DeepSeek-V3-shaped layer (uniform routing) at T=8192."""
     from mixture_experts_layer_routing_gb300 import MoeLayer, moe_forward, moe_set_fused
     out = {}
     for spec, Ts in ((moe_synth.BF16_T2048, (64, 256, 2048)), (moe_synth.DSV3_UNIFORM, (8192,))):
@@ -811,7 +812,7 @@ def fused_vs_separate(dev, steps=30):
             y = torch.empty_like(x)
             ws = layer.buffer("fwd", layer.sizes(T)["fwd_ws"])
             row = {}
-            for fused in (0, 1):
+            for fused in (0, 1, 2):
                 moe_set_fused(layer.h, fused)
                 s = torch.cuda.Stream()
                 s.wait_stream(torch.cuda.current_stream())
@@ -821,9 +822,10 @@ def fused_vs_separate(dev, steps=30):
                 graph = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(graph):
                     moe_forward(layer.h, x, T, y, None, ws)
-                row["fused_ms" if fused else "separate_ms"] = time_steps(graph.replay, steps, 5, 1)
+                row[("separate_ms", "fused_experts_ms", "fused_forward_ms")[fused]] = time_steps(graph.replay, steps, 5, 1)
                 del graph
-            row["speedup"] = row["separate_ms"] / row["fused_ms"]
+            row["speedup_experts"] = row["separate_ms"] / row["fused_experts_ms"]
+            row["speedup_forward"] = row["separate_ms"] / row["fused_forward_ms"]
             out[f"{spec.name.split('_')[0]}_d{spec.d}_E{spec.E}_T{T}"] = row
         moe_set_fused(layer.h, 0)
         layer.close()

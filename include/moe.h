@@ -88,7 +88,7 @@ typedef struct {
 /* Create a handle for one layer shape on the current CUDA device. Validates
  * the config (MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED) and allocates one
  * small device array (the status word, the decode router's counter and the
- * fused kernel's per-row-block counters: 4 x (T_max (k+S) / 128 + E + S + 68)
+ * fused kernels' counters: 4 x (T_max (k+S) / 128 + E + S + 72)
  * bytes, the library's only allocation); on the tensor-core paths (bf16 and
  * MXFP8) it also creates one stream and three events for side work
  * (moe_backward's router backward, moe_train_chunked's next-chunk routing). */
@@ -206,20 +206,28 @@ moe_status moe_set_decode_crossover(moe_handle h, int b_min);
  * Host-only; another mode returns MOE_ERR_INVALID_ARG. */
 moe_status moe_set_pairs(moe_handle h, int mode);
 
-/* Forward of a bf16 tensor-core layer with its two expert GEMMs in one kernel
- * (on = 1): the gate/up GEMM (A5) and the down GEMM (A6) run as one
- * persistent cooperative launch over a single tile order, a down tile starting
- * as soon as the gate/up tiles of its 128 rows have stored h (per-row-block
- * arrival counters held by the handle, waits bounded by the device timeout),
- * so no SM idles through the gate/up tail and the kernel boundary. This
- * follows the one-call design of "Cursor открыл код ядра Mixture of
- * Experts..." (section "Три решения, которые дали результат"), on one GPU.
- * Routing (A1-A4) and the combine (A7) stay separate launches: on GB300 the
- * combine as a phase of the persistent kernel (8 warps per SM) measured
- * slower than its own high-occupancy launch at every size tried. Results are
- * bit-identical to on = 0 (the default). Host-only. on = 1 for a layer without
- * the bf16 tensor-core path returns MOE_ERR_UNSUPPORTED; other values
- * MOE_ERR_INVALID_ARG. While on = 1, calls on one handle must not run
+/* Forward of a bf16 tensor-core layer as one persistent kernel, following the
+ * one-call design of "Cursor открыл код ядра Mixture of Experts..." (section
+ * "Три решения, которые дали результат"), on one GPU.
+ * on = 1: the two expert GEMMs in one kernel: the gate/up GEMM (A5) and the
+ * down GEMM (A6) run as one cooperative launch over a single tile order, a
+ * down tile starting as soon as the gate/up tiles of its 128 rows have stored
+ * h (per-row-block arrival counters held by the handle, waits bounded by the
+ * device timeout), so no SM idles through the gate/up tail and the kernel
+ * boundary; routing (A1-A4) and the combine (A7) stay separate launches.
+ * on = 2: the whole forward in one cooperative launch: the router GEMM (the
+ * same K splits as the separate launch, partials added in split order), top-k
+ * and gates, chunk histograms, scan, permutation, the expert tiles taken from
+ * a device tile queue (an atomic head; the dependency counters of on = 1),
+ * and the combine, phases separated by grid-wide barriers; every wait is
+ * bounded and past its limit records MOE_ERR_TIMEOUT and ends the call's work.
+ * Results of both modes are bit-identical to on = 0 (the default, separate
+ * launches). On GB300 mode 1 is 4-8% faster than separate launches on the
+ * 2048-token layer at T <= 2048 and slower on the DeepSeek-V3 shape; mode 2
+ * is faster than separate launches only at small T (T = 64), its routing and
+ * combine phases running at one CTA per SM. Host-only. A nonzero value for a
+ * layer without the bf16 tensor-core path returns MOE_ERR_UNSUPPORTED; other
+ * values MOE_ERR_INVALID_ARG. While on != 0, calls on one handle must not run
  * concurrently on two streams (the counters are per handle). */
 moe_status moe_set_fused(moe_handle h, int on);
 

@@ -184,9 +184,8 @@ def moe_set_pairs(h, mode: int):
 
 
 def moe_set_fused(h, on: int):
-    """Forward expert GEMMs (gate/up and down) as one persistent kernel (1) or two launches (0).
-
-    The combine stays its own launch either way."""
+    """Forward as one persistent kernel: 1 the two expert GEMMs, 2 the whole forward (routing, both
+    expert GEMMs, combine); 0 separate launches (the default). Results are bit-identical."""
     _check(load_library().moe_set_fused(h, on), "moe_set_fused")
 
 

@@ -249,6 +249,10 @@ moe_status forward_experts(moe_handle_s* h, const void* x, int T, void* y, void*
 // Forward of T >= 1 tokens (arguments already validated).
 moe_status forward_body(moe_handle_s* h, const void* x, int T, void* y, void* ctx, void* workspace, cudaStream_t s) {
   const Bufs B = carve(h->L, T, workspace, ctx, nullptr);
+  if (h->tc && h->L.fused == 2) {
+    CK(run(h, s, G_FUSED, 1, [&] { return launch_tc_fused_forward(h->L, B, x, y, s); }));
+    return MOE_OK;
+  }
   const moe_status st = run_route(h, B, x, nullptr, s);
   if (st != MOE_OK) return st;
   return forward_experts(h, x, T, y, ctx, workspace, s);
@@ -403,9 +407,9 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
     delete h;
     return MOE_ERR_CUDA;
   }
-  // status word, decode counter, and the fused expert kernel's counters (4 + one per m-tile)
+  // status word, decode counter, and the fused kernels' counters (8 + one per m-tile)
   const size_t max_mtiles = ((size_t)c.T_max * (c.k + c.n_shared) + 127) / 128 + c.E + c.n_shared;
-  const size_t word_bytes = 256 + 4 * (4 + max_mtiles);
+  const size_t word_bytes = 256 + 4 * (8 + max_mtiles);
   int* words = nullptr;
   if (cudaMalloc(&words, word_bytes) != cudaSuccess || cudaMemset(words, 0, word_bytes) != cudaSuccess) {
     if (words) cudaFree(words);
@@ -414,8 +418,9 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
   }
   L.status = words;
   L.decode_counter = words + 32;
-  L.dep_done = (unsigned*)(words + 64);
-  L.dep = (unsigned*)(words + 68);
+  L.dep_done = (unsigned*)(words + 64);   // 8 words: see Layer::dep_done
+  L.dep = (unsigned*)(words + 72);
+  L.dep_len = (int)max_mtiles;
   if (c.prec == MOE_MXFP8) L.G = kGateMx;
   h->tc = (c.prec == MOE_BF16) && tc_supported(L);
   h->mx = (c.prec == MOE_MXFP8) && mx_supported(L);
@@ -764,7 +769,7 @@ moe_status moe_launch_count(moe_handle h, long long* launches) {
 }
 
 moe_status moe_set_fused(moe_handle h, int on) {
-  if (!h || on < 0 || on > 1) return MOE_ERR_INVALID_ARG;
+  if (!h || on < 0 || on > 2) return MOE_ERR_INVALID_ARG;
   if (on && !h->tc) return MOE_ERR_UNSUPPORTED;
   h->L.fused = on;
   return MOE_OK;

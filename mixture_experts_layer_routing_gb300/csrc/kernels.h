@@ -46,10 +46,12 @@ struct Layer {
   CUtensorMap tm_W13_h;     // K-major rows of W13, box 64 x 128 (half an n-tile: one CTA of a pair)
   CUtensorMap tm_Wd_h;      // K-major rows of Wd, box 64 x 128
   int pairs;                // 1: expert GEMMs on 2-SM CTA pairs; 0 (default): one CTA per tile
-  int fused;                // 1: forward gate/up and down GEMMs as one persistent kernel
+  int fused;                // 1: forward gate/up and down GEMMs as one persistent kernel; 2: the whole forward
   int row_tiles;            // 128-row tiles per CTA of the bf16 segment GEMMs over token rows (1 or 2)
-  unsigned* dep;            // fused kernel: per-m-tile arrival counters (zero between calls)
-  unsigned* dep_done;       // fused kernel: [1] CTAs finished, [2] gate/up tiles finished ([0] unused)
+  unsigned* dep;            // fused kernels: per-m-tile arrival counters (zero between calls)
+  int dep_len;              // their number
+  unsigned* dep_done;       // fused kernels: [0] tile queue head, [1] CTAs finished, [2] gate/up epilogue warps
+                            // finished, [3] grid-barrier arrivals, [4] abort (zero between calls)
   // MXFP8 packed weights: E4M3 codes and E8M0 scales (one per 32 along the named axis)
   // MXFP8 scales: K-major arrays row-major (rows, K/32); MN-major arrays (Krows/32, W) stored
   // as [Krows/128][W][4] (the four scales of a column's 128-row K block in one word).
@@ -140,6 +142,7 @@ cudaError_t launch_tc_router_logits(const Layer& L, const void* x, int T, float*
 cudaError_t launch_tc_gateup(const Layer& L, const Bufs& B, const void* x, cudaStream_t s);
 cudaError_t launch_tc_down(const Layer& L, const Bufs& B, cudaStream_t s);
 cudaError_t launch_tc_fused_experts(const Layer& L, const Bufs& B, const void* x, cudaStream_t s);
+cudaError_t launch_tc_fused_forward(const Layer& L, const Bufs& B, const void* x, void* y, cudaStream_t s);
 cudaError_t launch_tc_bwd_dh(const Layer& L, const Bufs& B, const void* dy, cudaStream_t s);
 cudaError_t launch_tc_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s);
 cudaError_t launch_tc_bwd_dw13(const Layer& L, const Bufs& B, const void* x, void* dWg, void* dWu, bool acc,

@@ -33,7 +33,9 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "route_phases.cuh"
 #include "tc_ptx.cuh"
+#include "topk.cuh"
 
 namespace moe {
 
@@ -991,6 +993,466 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------------------ whole-forward kernel
+// The whole forward in one cooperative persistent launch: router logits (tcgen05 tiles, the same
+// K splits as the separate router launch, partials added in split order), top-k and gates, the
+// chunk histograms, the scan (one CTA), the stable permutation, the gate/up and down GEMM tiles,
+// and the combine. Phases are separated by grid-wide barriers; every wait (barrier, dependency
+// counter, mbarrier) is bounded and past its limit records MOE_ERR_TIMEOUT, raises a global abort
+// word that every CTA's later waits see, and the kernel runs to its end without further work.
+// The expert tiles come from a device tile queue (an atomic head, gate/up tiles first): the
+// producer's first thread takes the next tile and publishes it in a small shared-memory ring that
+// the producer warps, the MMA thread and the epilogue warps read in order; a down tile's loads
+// wait for the h rows of its row block (per-row-block counters, as in fused_experts_kernel).
+// Dependencies point only to tiles taken earlier, and every CTA finishes its tiles in the order it
+// took them, so with all CTAs resident (cooperative launch) every wait ends. Each output element
+// is computed with the same instructions in the same order as the separate launches: results are
+// bit-identical to them. The last CTA to finish zeroes the counters for the next call.
+struct FwdParams {
+  TcParams rt, gu, dn;   // router (DENSE, EPI_F32: partials in rt.part when rt.ksplit > 1), gate/up, down
+  const float* bias;
+  float* logits;         // [T, E]
+  int* idx;              // [T, k]
+  float* gate;           // [T, k]
+  int* chunk_hist;
+  int* chunk_base;
+  int* cnt;
+  int* off;
+  int* mt_off;
+  int* perm;
+  int* inv;
+  int* row_token;
+  float* row_gate;
+  const bf16* o;         // gated expert outputs [R, d] (written by the down tiles)
+  bf16* y;               // [T, d]
+  int T, E, S, k, d, router, renorm, A, nch;
+  float scale;
+  unsigned* dep;         // per m-tile arrival counters
+  int dep_len;           // their number (cleared in full after every call)
+  unsigned* ctr;         // [0] tile queue head, [1] CTAs finished, [2] gate/up epilogue warps finished,
+                         // [3] grid-barrier arrivals, [4] abort
+};
+
+constexpr int kTq = 32;   // entries of the shared tile-queue ring
+constexpr int kFwdScratch = permute_smem(kThreads / 32) > kScanSmem ? permute_smem(kThreads / 32) : kScanSmem;
+// ring, then the SIMT scratch and the queue ring, then the barriers (aligned to 8) and two ints
+constexpr int kFwdSmem = Smem<256, SCHED_SEG_M, 1>::NS * Smem<256, SCHED_SEG_M, 1>::STAGE + 4 * (kFwdScratch + 2 * kTq) +
+                         8 + 8 * (2 * Smem<256, SCHED_SEG_M, 1>::NS + 8) + 1024;
+static_assert(kFwdSmem <= kSmemMax, "whole-forward kernel shared memory");
+
+// Grid-wide barrier number gen (1, 2, ...): every CTA adds one to ctr[3] and waits until it reaches
+// gen * gridDim.x. False (for the whole CTA) if the global abort word is raised or the wait passes
+// kWaitLimitNs (then MOE_ERR_TIMEOUT is recorded and the abort word raised).
+__device__ __noinline__ bool grid_barrier(unsigned* ctr, unsigned gen, int* status, int* ok_s) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(ctr + 3, 1u);
+    const unsigned need = gen * gridDim.x;
+    int ok = 1;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0; ld_acquire_u32(ctr + 3) < need; ++i) {
+      __nanosleep(64);
+      if ((i & 15) == 15) {
+        if (ld_acquire_u32(ctr + 4)) {
+          ok = 0;
+          break;
+        }
+        if (global_ns() - t0 > kWaitLimitNs) {
+          set_error(status, MOE_ERR_TIMEOUT);
+          atomicExch(ctr + 4, 1u);
+          ok = 0;
+          break;
+        }
+      }
+    }
+    if (ok && ld_acquire_u32(ctr + 4)) ok = 0;
+    __threadfence();
+    *ok_s = ok;
+  }
+  __syncthreads();
+  return *ok_s != 0;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    fused_forward_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmWr,
+                         const __grid_constant__ CUtensorMap tmW13, const __grid_constant__ CUtensorMap tmH,
+                         const __grid_constant__ CUtensorMap tmWd, const __grid_constant__ FwdParams q) {
+  constexpr int BN = 256;
+  using SM = Smem<BN, SCHED_SEG_M, 1>;
+  constexpr int NS = SM::NS;
+  constexpr uint32_t TMEM_COLS = 512;
+  constexpr uint32_t IDESC = idesc_bf16(BM, BN, 0, 0);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* stage_base = smem;
+  int* scratch = (int*)(smem + NS * SM::STAGE);                     // SIMT phases
+  volatile int* tq_tile = (volatile int*)(scratch + kFwdScratch);   // [kTq] tile of queue entry i
+  volatile int* tq_seq = tq_tile + kTq;                              // [kTq] entry number held
+  uint64_t* bars = (uint64_t*)(((uintptr_t)(scratch + kFwdScratch + 2 * kTq) + 7) & ~(uintptr_t)7);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + NS);
+  const uint32_t tfull0 = smem_u32(bars + 2 * NS), tempty0 = smem_u32(bars + 2 * NS + 2);
+  const uint32_t drain = smem_u32(bars + 2 * NS + 4);
+  volatile int* abort_flag = (volatile int*)(bars + 2 * NS + 5);
+  uint32_t* tmem_slot = (uint32_t*)(bars + 2 * NS + 6);
+  int* ticket = (int*)(bars + 2 * NS + 7);
+  int* ok_s = ticket + 1;
+  int* status = q.gu.status;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full0 + 8 * s, kProducerWarps * 32);   // every producer thread arrives on every stage
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, kEpiWarps * 32);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  for (int i = threadIdx.x; i < kTq; i += blockDim.x) tq_seq[i] = -1;
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // pipeline positions, kept by each role across the two GEMM phases
+  int it = 0, tcount = 0;
+  bool ok = true;   // this thread's role has seen no failed wait
+
+  // ------------------------------------------------------------- phase 1: router logit tiles
+  const int n_rt = total_tiles<SCHED_DENSE, 1>(q.rt);
+  if (warp < kProducerWarps) {
+    const bf16* gsrc[8] = {};
+    uint32_t gbytes[8] = {};
+    for (int L = blockIdx.x; L < n_rt && ok; L += gridDim.x) {
+      const Tile t = map_tile<SCHED_DENSE, 1>(q.rt, L, 0);
+      for (int kb = t.kb0; kb < t.nkb; ++kb, ++it) {
+        const int s = it % NS;
+        if (!mbar_wait(empty0 + 8 * s, ((it / NS) & 1) ^ 1, abort_flag, status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sa = smem_u32(stage_base + s * SM::STAGE);
+        load_stage<BN, A_TMA_K, B_TMA_K, SCHED_DENSE, 1, true>(q.rt, &tmX, &tmWr, t, kb, sa, sa + SM::A_BYTES,
+                                                              full0 + 8 * s, gsrc, gbytes, 0, 0, 0);
+        cp_async_mbar_arrive_noinc(full0 + 8 * s);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      for (int L = blockIdx.x; L < n_rt && ok; L += gridDim.x, ++tcount) {
+        const Tile t = map_tile<SCHED_DENSE, 1>(q.rt, L, 0);
+        const int acc = tcount & 1;
+        if (!mbar_wait(tempty0 + 8 * acc, ((tcount >> 1) & 1) ^ 1, abort_flag, status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t dcol = tmem_base + acc * BN;
+        for (int kb = t.kb0; kb < t.nkb; ++kb, ++it) {
+          const int s = it % NS;
+          if (!mbar_wait(full0 + 8 * s, (it / NS) & 1, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(stage_base + s * SM::STAGE);
+          const uint32_t sb = sa + SM::A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_bf16(dcol, desc_kmajor(sa + k * 32), desc_kmajor(sb + k * 32), IDESC,
+                     (kb > t.kb0 || k > 0) ? 1u : 0u);
+          mma_commit(empty0 + 8 * s);
+        }
+        if (!ok) break;
+        mma_commit(tfull0 + 8 * acc);
+      }
+    }
+    __syncwarp();
+  } else {
+    const int ew = warp - kProducerWarps;
+    const int r = ew * 32 + lane;
+    for (int L = blockIdx.x; L < n_rt && ok; L += gridDim.x, ++tcount) {
+      const Tile t = map_tile<SCHED_DENSE, 1>(q.rt, L, 0);
+      const int acc = tcount & 1;
+      if (!mbar_wait(tfull0 + 8 * acc, (tcount >> 1) & 1, abort_flag, status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(ew * 32) << 16);
+      const int row = t.row0 + r;
+      const bool valid = row < t.row_end;
+      float* obase = q.rt.ksplit > 1 ? q.rt.part + (size_t)t.ks * q.rt.dense_rows * q.rt.ldo : (float*)q.rt.out;
+      float* orow = obase + (size_t)row * q.rt.ldo + t.n * BN;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t a[32];
+        tmem_ld32(tbase + c0, a);
+        tmem_ld_wait();
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (t.n * BN + c0 + i < q.rt.n_valid) orow[c0 + i] = __uint_as_float(a[i]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty0 + 8 * acc);
+    }
+  }
+  if (!ok) {
+    *abort_flag = 1;
+    atomicExch(q.ctr + 4, 1u);
+  }
+
+  // --------------------------------------------- phases 2-6: the routing, CTA- or warp-parallel
+  const int gwarp = blockIdx.x * (kThreads / 32) + warp, nwarps = gridDim.x * (kThreads / 32);
+  bool live = grid_barrier(q.ctr, 1, status, ok_s);
+  if (live && q.rt.ksplit > 1) {
+    // logits = the K splits' partials added in split order
+    const long n = (long)q.T * q.E;
+    for (long i = (long)blockIdx.x * kThreads + threadIdx.x; i < n; i += (long)gridDim.x * kThreads) {
+      float sum = 0.f;
+      for (int ks = 0; ks < q.rt.ksplit; ++ks) sum += __ldcg(q.rt.part + ks * n + i);
+      q.logits[i] = sum;
+    }
+  }
+  live = grid_barrier(q.ctr, 2, status, ok_s) && live;
+  if (live)
+    for (int t = gwarp; t < q.T; t += nwarps)
+      warp_topk_gates(q.logits + (size_t)t * q.E, q.bias, q.E, q.k, q.router, q.renorm, q.scale,
+                      q.idx + (size_t)t * q.k, q.gate + (size_t)t * q.k);
+  live = grid_barrier(q.ctr, 3, status, ok_s) && live;
+  if (live)
+    for (int ch = blockIdx.x; ch < q.nch; ch += gridDim.x) hist_chunk(q.idx, q.A, q.E, ch, q.chunk_hist, status, scratch);
+  live = grid_barrier(q.ctr, 4, status, ok_s) && live;
+  if (live && blockIdx.x == 0)
+    scan_segments(q.chunk_hist, q.nch, q.E, q.S, q.T, q.chunk_base, q.cnt, q.off, q.mt_off, scratch);
+  live = grid_barrier(q.ctr, 5, status, ok_s) && live;
+  if (live) {
+    for (int ch = blockIdx.x; ch < q.nch; ch += gridDim.x)
+      permute_chunk(q.idx, q.gate, q.A, q.E, q.k, ch, q.chunk_base, q.perm, q.inv, q.row_token, q.row_gate, scratch);
+    if (q.S)
+      for (int t = blockIdx.x * kThreads + threadIdx.x; t < q.T; t += gridDim.x * kThreads) {
+        q.row_token[q.A + t] = t;
+        q.row_gate[q.A + t] = 1.0f;
+      }
+  }
+  live = grid_barrier(q.ctr, 6, status, ok_s) && live;
+  if (!live) *abort_flag = 1;
+
+  // -------------------------------------------------- phase 7: expert tiles from the tile queue
+  const int n_gu = live ? total_tiles<SCHED_SEG_M, 1>(q.gu) : 0;
+  const int n_all = live ? n_gu + total_tiles<SCHED_SEG_M, 1>(q.dn) : 0;
+  const unsigned gu_arrivals = kEpiWarps * q.gu.n_tiles;   // per m-tile
+  // queue entry i of this CTA: waits until published (bounded), -1 past the last tile or on abort.
+  // The publishing thread is at most a few tiles ahead of any reader (its loads wait for stages the
+  // MMA freed, the MMA waits for accumulators the epilogue freed), far less than kTq.
+  auto entry = [&](int i) -> int {
+    const int slot = i % kTq;
+    const uint64_t t0 = global_ns();
+    for (uint32_t n = 0; tq_seq[slot] != i; ++n) {
+      if ((n & 63) == 63) {
+        if (*abort_flag) return -1;
+        if (global_ns() - t0 > kWaitLimitNs) {
+          set_error(status, MOE_ERR_TIMEOUT);
+          *abort_flag = 1;
+          return -1;
+        }
+      }
+    }
+    __threadfence_block();
+    return tq_tile[slot];
+  };
+  if (warp < kProducerWarps) {
+    bool all_up = false;   // every gate/up tile finished: no down tile needs to wait any more
+    for (int i = 0; live && ok; ++i) {
+      int G;
+      if (threadIdx.x == 0) {
+        const int G0 = *abort_flag ? n_all : (int)atomicAdd(q.ctr + 0, 1u);
+        G = G0 < n_all ? G0 : -1;
+        tq_tile[i % kTq] = G;
+        __threadfence_block();
+        tq_seq[i % kTq] = i;
+      } else {
+        G = entry(i);
+      }
+      if (G < 0) break;
+      const bool up = G < n_gu;
+      const Tile t = up ? map_tile<SCHED_SEG_M, 1>(q.gu, G, 0) : map_tile<SCHED_SEG_M, 1>(q.dn, G - n_gu, 0);
+      const bf16* gsrc[8];
+      uint32_t gbytes[8];
+      if (up) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int rr = warp * 32 + j * 4 + (lane >> 3);
+          const int row = t.row0 + rr;
+          const bool v = row < t.row_end;
+          const int tok = v ? q.gu.row_token[row] : 0;
+          gsrc[j] = q.gu.A + (size_t)tok * q.gu.lda + (lane & 7) * 8;
+          gbytes[j] = v ? 16u : 0u;
+        }
+      } else if (threadIdx.x == 0 && !all_up) {
+        // the h rows of this m-tile: every gate/up tile of (e, m) finished by all its epilogue warps
+        if (ld_acquire_u32(q.ctr + 2) >= kEpiWarps * (unsigned)n_gu) all_up = true;
+        else if (!wait_count(q.dep + q.gu.mt_off[t.e] + t.m, gu_arrivals, abort_flag, status)) ok = false;
+        fence_proxy_async_global();
+      }
+      for (int kb = 0; kb < t.nkb && ok; ++kb, ++it) {
+        const int s = it % NS;
+        if (!mbar_wait(empty0 + 8 * s, ((it / NS) & 1) ^ 1, abort_flag, status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sa = smem_u32(stage_base + s * SM::STAGE);
+        const uint32_t sb = sa + SM::A_BYTES;
+        if (up)
+          load_stage<BN, A_GATHER_K, B_TMA_K, SCHED_SEG_M, 1, true>(q.gu, &tmW13, &tmW13, t, kb, sa, sb,
+                                                                     full0 + 8 * s, gsrc, gbytes, 0, 0, 0);
+        else
+          load_stage<BN, A_TMA_K, B_TMA_K, SCHED_SEG_M, 1, true>(q.dn, &tmH, &tmWd, t, kb, sa, sb, full0 + 8 * s,
+                                                                  gsrc, gbytes, 0, 0, 0);
+        cp_async_mbar_arrive_noinc(full0 + 8 * s);
+      }
+    }
+    cp_async_wait<0>();
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      for (int i = 0; live && ok; ++i, ++tcount) {
+        const int G = entry(i);
+        if (G < 0) break;
+        const bool up = G < n_gu;
+        const Tile t = up ? map_tile<SCHED_SEG_M, 1>(q.gu, G, 0) : map_tile<SCHED_SEG_M, 1>(q.dn, G - n_gu, 0);
+        const int acc = tcount & 1;
+        if (!mbar_wait(tempty0 + 8 * acc, ((tcount >> 1) & 1) ^ 1, abort_flag, status)) break;
+        tc_fence_after();
+        const uint32_t dcol = tmem_base + acc * BN;
+        for (int kb = 0; kb < t.nkb; ++kb, ++it) {
+          const int s = it % NS;
+          if (!mbar_wait(full0 + 8 * s, (it / NS) & 1, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (up) fence_proxy_async();   // gathered rows (cp.async, generic proxy) seen by the MMA
+          const uint32_t sa = smem_u32(stage_base + s * SM::STAGE);
+          const uint32_t sb = sa + SM::A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_bf16(dcol, desc_kmajor(sa + k * 32), desc_kmajor(sb + k * 32), IDESC, (kb > 0 || k > 0) ? 1u : 0u);
+          mma_commit(empty0 + 8 * s);
+        }
+        if (!ok) break;
+        mma_commit(tfull0 + 8 * acc);
+      }
+      // drain: wait until every issued MMA has completed before TMEM is freed
+      mma_commit(drain);
+      const uint64_t t0 = global_ns();
+      while (!mbar_try_wait(drain, 0)) {
+        if (global_ns() - t0 > kWaitLimitNs) {
+          set_error(status, MOE_ERR_TIMEOUT);
+          break;
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    const int ew = warp - kProducerWarps;
+    const int r = ew * 32 + lane;
+    for (int i = 0; live; ++i, ++tcount) {
+      const int G = entry(i);
+      if (G < 0) break;
+      const bool up = G < n_gu;
+      const Tile t = up ? map_tile<SCHED_SEG_M, 1>(q.gu, G, 0) : map_tile<SCHED_SEG_M, 1>(q.dn, G - n_gu, 0);
+      const int acc = tcount & 1;
+      if (!mbar_wait(tfull0 + 8 * acc, (tcount >> 1) & 1, abort_flag, status)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(ew * 32) << 16);
+      const int row = t.row0 + r;
+      const bool valid = row < t.row_end;
+      if (up) {
+        epi_swiglu<BN>(q.gu, t, tbase, row, valid);
+        signal_count(q.dep + q.gu.mt_off[t.e] + t.m, lane);
+        if (lane == 0) atomicAdd(q.ctr + 2, 1u);
+      } else {
+        epi_scale_store<BN, true>(q.dn, t, tbase, row, valid);
+      }
+      tc_fence_before();
+      mbar_arrive(tempty0 + 8 * acc);
+    }
+  }
+  if (*abort_flag) atomicExch(q.ctr + 4, 1u);
+
+  // ------------------------------------------------------------------- phase 8: the combine
+  // y[t] = o[A + t] (shared) + sum_j o[inv[t k + j]], fp32 in that order, one rounding
+  live = grid_barrier(q.ctr, 7, status, ok_s) && live;
+  if (live) {
+    const int vecs = q.d / 8;
+    const long n = (long)q.T * vecs;
+    for (long v = (long)blockIdx.x * kThreads + threadIdx.x; v < n; v += (long)gridDim.x * kThreads) {
+      const int t = (int)(v / vecs), c = (int)(v % vecs) * 8;
+      // all k + 1 rows in flight before the sum (nine warps per SM: the loads' latency must overlap)
+      int rj[kMaxK];
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) rj[j] = j < q.k ? q.inv[(long)t * q.k + j] : 0;
+      const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+      const uint4 us = q.S ? __ldcg(reinterpret_cast<const uint4*>(q.o + (long)(q.A + t) * q.d + c)) : zero;
+      uint4 uj[kMaxK];
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        uj[j] = j < q.k ? __ldcg(reinterpret_cast<const uint4*>(q.o + (long)rj[j] * q.d + c)) : zero;
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      auto add = [&](const uint4& u) {
+        float f[8];
+        unpack8(u, f);
+#pragma unroll
+        for (int w = 0; w < 8; ++w) acc[w] += f[w];
+      };
+      if (q.S) add(us);
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        if (j < q.k) add(uj[j]);
+      *reinterpret_cast<uint4*>(q.y + (long)t * q.d + c) = pack8(acc);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                 : "memory");
+  }
+  // the last CTA to finish zeroes the counters for the next call
+  if (threadIdx.x == 0) {
+    __threadfence();
+    *ticket = (int)atomicAdd(q.ctr + 1, 1u);
+  }
+  __syncthreads();
+  if (*ticket == (int)gridDim.x - 1) {
+    __threadfence();
+    for (int i = threadIdx.x; i < q.dep_len; i += blockDim.x) q.dep[i] = 0;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      q.ctr[0] = 0;
+      q.ctr[1] = 0;
+      q.ctr[2] = 0;
+      q.ctr[3] = 0;
+      q.ctr[4] = 0;
+      __threadfence();
+    }
+  }
+}
+
 // -------------------------------------------------------------- host side
 template <int BN, int AMODE, int BMODE, int SCHED, int EPI, int CG = 1, int MT = 1>
 cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcParams& p, int grid, cudaStream_t s,
@@ -1207,6 +1669,80 @@ cudaError_t launch_tc_fused_experts(const Layer& L, const Bufs& B, const void* x
   cfg.attrs = at;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, fused_experts_kernel, L.tm_W13, th, L.tm_Wd, q);
+}
+
+// The whole forward (routing A1-A4, A5, A6, combine A7) in one cooperative launch
+// (fused_forward_kernel). The router splits K exactly as launch_tc_router_logits does, its partials
+// in the forward scratch o (which the down tiles write only later).
+cudaError_t launch_tc_fused_forward(const Layer& L, const Bufs& B, const void* x, void* y, cudaStream_t s) {
+  static_assert(kBNup == 256 && kBNdown == 256 && kBNrouter == 256, "the fused kernels run 128 x 256 tiles");
+  if (L.E + L.S > kThreads) return cudaErrorInvalidValue;   // the scan runs on one CTA
+  CUtensorMap tx, twr, th;
+  if (!make_tmap(&tx, x, L.d, B.T, BK, BM) || !make_tmap(&twr, L.Wr, L.d, L.E, BK, kBNrouter) ||
+      !make_tmap(&th, B.h, L.f, B.R, BK, BM))
+    return cudaErrorInvalidValue;
+  FwdParams q = {};
+  TcParams rt = {};
+  rt.dense_rows = B.T;
+  rt.K = L.d;
+  rt.n_tiles = 1;
+  rt.out = B.logits;
+  rt.ldo = L.E;
+  rt.n_valid = L.E;
+  rt.status = L.status;
+  rt.ksplit = tc_router_splits(L, B.T);
+  rt.part = (float*)B.o;
+  if (rt.ksplit > 1 && (size_t)rt.ksplit * B.T * L.E * sizeof(float) > (size_t)B.R * L.d * 2)
+    return cudaErrorInvalidValue;
+  q.rt = rt;
+  q.gu = gateup_params(L, B, x);
+  q.dn = down_params(L, B);
+  q.bias = L.bias;
+  q.logits = B.logits;
+  q.idx = B.idx;
+  q.gate = B.gate;
+  q.chunk_hist = B.chunk_hist;
+  q.chunk_base = B.chunk_base;
+  q.cnt = B.cnt;
+  q.off = B.off;
+  q.mt_off = B.mt_off;
+  q.perm = B.perm;
+  q.inv = B.inv;
+  q.row_token = B.row_token;
+  q.row_gate = B.row_gate;
+  q.o = (const bf16*)B.o;
+  q.y = (bf16*)y;
+  q.T = B.T;
+  q.E = L.E;
+  q.S = L.S;
+  q.k = L.k;
+  q.d = L.d;
+  q.router = L.router;
+  q.renorm = L.renorm;
+  q.scale = L.scale;
+  q.A = B.A;
+  q.nch = B.nch;
+  q.dep = L.dep;
+  q.dep_len = L.dep_len;
+  q.ctr = L.dep_done;
+  static bool attr = false;
+  if (!attr) {
+    const cudaError_t e = cudaFuncSetAttribute(fused_forward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               kFwdSmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeCooperative;   // every CTA resident: the grid barriers and waits can end
+  at[0].val.cooperative = 1;
+  cfg.gridDim = dim3(L.num_sms);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kFwdSmem;
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fused_forward_kernel, tx, twr, L.tm_W13, th, L.tm_Wd, q);
 }
 
 // B1: r = dy_t Wd[e] (K = d; Wd read MN-major), SwiGLU backward, g*h, gate-gradient partials.

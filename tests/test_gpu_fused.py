@@ -1,9 +1,14 @@
-"""The forward's two expert GEMMs as one persistent kernel
-(moe_set_fused(h, 1)): gate/up and down tiles in a single cooperative launch,
-down tiles released by per-row-block arrival counters.
+"""The forward as one persistent kernel.
 
-The fused kernel runs the same tiles with the same K order as the two
-separate launches, so:
+moe_set_fused(h, 1): the two expert GEMMs (gate/up and down tiles) in a single
+cooperative launch, down tiles released by per-row-block arrival counters.
+moe_set_fused(h, 2): the whole forward in one cooperative launch: the router
+GEMM (the same K splits), top-k, histogram, scan, permutation, the expert
+tiles taken from a device tile queue, and the combine, separated by bounded
+grid-wide barriers.
+
+The fused kernels run the same tiles with the same K order as the separate
+launches, so:
 
 * y is bit-identical to the unfused forward, and so are the saved activations
   (checked through the backward, whose dx and weight gradients must match
@@ -59,17 +64,18 @@ def step(layer, inp, fused):
     return {"y": y.clone(), **{k: v.clone() for k, v in grads.items()}}
 
 
+@pytest.mark.parametrize("mode", [1, 2], ids=["experts", "whole_forward"])
 @pytest.mark.parametrize("spec,bias", CASES, ids=[c[0].name for c in CASES])
-def test_fused_matches_separate_launches(spec, bias):
+def test_fused_matches_separate_launches(spec, bias, mode):
     inp, layer = make(spec, bias)
     sep = step(layer, inp, 0)
-    fus = step(layer, inp, 1)
-    fus2 = step(layer, inp, 1)
+    fus = step(layer, inp, mode)
+    fus2 = step(layer, inp, mode)
     for k in sep:
         assert torch.equal(fus[k], sep[k]), k
         assert torch.equal(fus2[k], sep[k]), k
     # inference forward (no saved activations) as well
-    moe_set_fused(layer.h, 1)
+    moe_set_fused(layer.h, mode)
     y_inf = layer.forward(inp["x"])
     torch.cuda.synchronize()
     assert layer.status() == 0
@@ -86,7 +92,8 @@ def test_fused_matches_separate_launches(spec, bias):
     layer.close()
 
 
-def test_fused_many_calls_and_graph_replay():
+@pytest.mark.parametrize("mode", [1, 2], ids=["experts", "whole_forward"])
+def test_fused_many_calls_and_graph_replay(mode):
     spec, bias = CASES[0]
     inp, layer = make(spec, bias)
     T = spec.T
@@ -98,7 +105,7 @@ def test_fused_many_calls_and_graph_replay():
     toks = [moe_synth.make_tokens(spec, 1, DEV, seed_offset=20 + i)[0] for i in range(4)]
     for t in toks:
         refs.append(layer.forward(t).clone())
-    moe_set_fused(layer.h, 1)
+    moe_set_fused(layer.h, mode)
     for _ in range(2):
         for t, ref in zip(toks, refs):
             assert torch.equal(layer.forward(t), ref)
