@@ -945,11 +945,15 @@ PROFILE_CASES = {
     "dsv3_e32_mxfp8_chunked_t4096": (moe_synth.DSV3_MXFP8.with_(name="dsv3_e32_mxfp8", E=32, T=4096, chunk=2048,
                                                                 seed=11), "chunked", 4096),
     "bf16_t2048_fused_fwd": (moe_synth.BF16_T2048, "fwd_fused", 2048),
+    # ~256 rows per routed expert (2-3 row tiles), as in the 256-expert, 8192-token forward; 2.9 GB of weights
+    "dsv3_e32_bf16_fwd_t1024": (moe_synth.DSV3_UNIFORM.with_(name="dsv3_e32_T1024", E=32, T=1024, seed=9), "fwd", 1024),
+    "dsv3_e32_bf16_fwd_t1024_rowtiles2": (moe_synth.DSV3_UNIFORM.with_(name="dsv3_e32_T1024", E=32, T=1024, seed=9),
+                                          "fwd_rowtiles2", 1024),
 }
 
 
 def run_profile_case(args):
-    from mixture_experts_layer_routing_gb300 import MoeLayer, moe_decode, moe_set_fused
+    from mixture_experts_layer_routing_gb300 import MoeLayer, moe_decode, moe_set_fused, moe_set_pairs
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     import __graft_entry__
@@ -967,8 +971,9 @@ def run_profile_case(args):
         def fn():
             moe_decode(layer.h, xs[it[0] % 8], n, y, ws)
             it[0] += 1
-    elif kind in ("fwd", "fwd_fused"):
+    elif kind in ("fwd", "fwd_fused", "fwd_rowtiles2"):
         moe_set_fused(layer.h, 1 if kind == "fwd_fused" else 0)
+        moe_set_pairs(layer.h, 2 if kind == "fwd_rowtiles2" else 0)
         fn = lambda: layer.forward(inp["x"])  # noqa: E731
     else:
         fn = lambda: layer.train_chunked(inp["x"], inp["dy"], slots=1)  # noqa: E731
