@@ -18,6 +18,9 @@
 // Gate/up rows of the MXFP8 W13 are interleaved in blocks of 64 so that one
 // 128-column tile holds 64 gate and the matching 64 up features.
 //
+// The products over token rows (gate/up, down, dY.Wd, dx) run one CTA per 128-row tile and pair of
+// 128-column tiles (NB = 2): the staged A tile feeds two MMAs, so a 48 KB stage carries 512 MMA
+// cycles (a 32 KB stage of one column tile carries 256, too few for the loads to keep up).
 // Scale factors reach TMEM through tcgen05.st from the producer warps. For a
 // 128-row operand tile the MMA reads row r's four k-block scales (one per 32
 // elements of a 128-element stage, selected by the instruction's scale id)
@@ -49,9 +52,15 @@ enum { ME_SWIGLU_Q = 0, ME_GATE = 1, ME_DH_Q = 2, ME_STORE = 3, ME_DW13 = 4, ME_
 
 // Weight-gradient epilogue staging: per epilogue warp two 32-row x 64-column bf16 sub-tiles.
 constexpr int kMxOut = kEpi * 2 * 32 * 128;
-template <int SCHED>
+// NB: 128-column B tiles per CTA (1, or 2 for the segment-M products: one staged A tile feeds two
+// MMAs, so a 48 KB stage carries 512 MMA cycles where a 32 KB one carries 256). Stages, stage bytes
+// and the block-scale TMEM columns per stage (A, then each B tile).
+template <int NB> constexpr int mx_stages() { return NB == 2 ? 4 : MSTAGES; }
+template <int NB> constexpr int mx_stage_bytes() { return MBM * MBK + NB * MBN * MBK; }
+template <int NB> constexpr int mx_scale_cols() { return 4 + 4 * NB; }
+template <int SCHED, int NB = 1>
 constexpr int mx_smem() {
-  return MSTAGES * kStageBytes + (SCHED == MS_SEG_K ? kMxOut : 0) + 1024 + 256;
+  return mx_stages<NB>() * mx_stage_bytes<NB>() + (SCHED == MS_SEG_K ? kMxOut : 0) + 1024 + 256;
 }
 
 struct MxParams {
@@ -213,16 +222,18 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 
 struct MTile {
   int e, m, n, row0, row_end, nkb;
+  int nb;   // B tiles of this unit (n, n+1, ..): 1 or 2
 };
 
-template <int SCHED>
+template <int SCHED, int NB = 1>
 __device__ __forceinline__ int mx_total(const MxParams& p) {
-  return SCHED == MS_SEG_K ? p.nseg * p.m_tiles * p.n_tiles : p.mt_off[p.nseg] * p.n_tiles;
+  return SCHED == MS_SEG_K ? p.nseg * p.m_tiles * p.n_tiles : p.mt_off[p.nseg] * ((p.n_tiles + NB - 1) / NB);
 }
 
-template <int SCHED>
+template <int SCHED, int NB = 1>
 __device__ __forceinline__ MTile mx_map(const MxParams& p, int L) {
   MTile t;
+  t.nb = 1;
   if (SCHED == MS_SEG_K) {
     const int per = p.m_tiles * p.n_tiles;
     t.e = L / per;
@@ -234,19 +245,21 @@ __device__ __forceinline__ MTile mx_map(const MxParams& p, int L) {
     t.nkb = p.mt_off[t.e + 1] - p.mt_off[t.e];
     return t;
   }
+  const int nu = (p.n_tiles + NB - 1) / NB;   // units of NB column tiles
   int lo = 0, hi = p.nseg;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (p.mt_off[mid] * p.n_tiles <= L) lo = mid; else hi = mid;
+    if (p.mt_off[mid] * nu <= L) lo = mid; else hi = mid;
   }
   const int Me = p.mt_off[lo + 1] - p.mt_off[lo];
-  const int local = L - p.mt_off[lo] * p.n_tiles;
-  // m-tiles in groups of kRasterM, every n-tile of a group before the next group (L2 reuse)
-  const int g = local / (kRasterM * p.n_tiles);
+  const int local = L - p.mt_off[lo] * nu;
+  // m-tiles in groups of kRasterM, every column unit of a group before the next group (L2 reuse)
+  const int g = local / (kRasterM * nu);
   const int gm = min(kRasterM, Me - g * kRasterM);
-  const int within = local - g * kRasterM * p.n_tiles;
+  const int within = local - g * kRasterM * nu;
   t.e = lo;
-  t.n = within / gm;
+  t.n = NB * (within / gm);
+  t.nb = min(NB, p.n_tiles - t.n);
   t.m = g * kRasterM + within % gm;
   t.row0 = p.off[lo] + t.m * MBM;
   t.row_end = p.off[lo + 1];
@@ -261,10 +274,18 @@ __device__ __forceinline__ uint32_t scale_word_mn(const uint8_t* s, long krow0, 
   return *reinterpret_cast<const uint32_t*>(s + ((krow0 >> 7) * (long)W + col) * 4);   // krow0: multiple of 128
 }
 
-template <int AMODE, int BMODE, int SCHED, int EPI>
+// NB = 2 (segment-M products): each CTA unit is one 128-row tile by two 128-column tiles; the two
+// accumulators fill the TMEM columns that NB = 1 uses for double buffering, so a unit's epilogue is
+// not overlapped with the next unit's MMAs.
+template <int AMODE, int BMODE, int SCHED, int EPI, int NB>
 __global__ void __launch_bounds__(kMxThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2, MxParams p) {
+  static_assert(NB == 1 || (NB == 2 && SCHED == MS_SEG_M), "two B tiles per CTA: segment-M products");
+  constexpr int MSTAGES = mx_stages<NB>();
+  constexpr int kStageBytes = mx_stage_bytes<NB>();
+  constexpr int SCOLS = mx_scale_cols<NB>();
+  constexpr int NACC = NB == 2 ? 1 : 2;   // accumulator buffers
   constexpr int A_MN = AMODE == MA_TMA_MN ? 1 : 0;
   constexpr int B_MN = BMODE == MB_TMA_MN ? 1 : 0;
   constexpr bool kGather = AMODE == MA_GATHER_K;
@@ -300,7 +321,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int ntiles = mx_total<SCHED>(p);
+  const int ntiles = mx_total<SCHED, NB>(p);
 
   if (warp < kProd) {
     // ------------------------------------------------------------ producers
@@ -309,7 +330,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     int it = 0;
     bool ok = true;
     for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
-      const MTile t = mx_map<SCHED>(p, L);
+      const MTile t = mx_map<SCHED, NB>(p, L);
       const uint8_t* gsrc[8];
       uint32_t gbytes[8];
       long arow[4];        // K-major A: source row (token for gathers) of MMA rows lane + 32c
@@ -341,10 +362,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       // E4M3 stage is 256 MMA cycles; dW13 and dWd 15-17% faster than with two blocks ahead); the
       // forward products and dY.Wd read them at the stage (measured 3-7% faster there).
       constexpr bool kScaleRing = SCHED == MS_SEG_K || (AMODE == MA_TMA_K && BMODE == MB_TMA_MN);
-      auto scale_words = [&](int kb, uint32_t (&wa)[4], uint32_t (&wb)[4]) {
+      auto scale_words = [&](int kb, uint32_t (&wa)[4], uint32_t (&wb)[4], uint32_t (&wb2)[4]) {
         const long krowB = (SCHED == MS_SEG_K ? (long)t.row0 : (long)t.e * p.b_rows_per_seg) + (long)kb * MBK;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
+          wb2[c] = 0u;
           if (kb >= t.nkb) {
             wa[c] = wb[c] = 0u;
             continue;
@@ -358,23 +380,27 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           }
           if (BMODE == MB_TMA_MN) {
             wb[c] = scale_word_mn(p.Bs, krowB, p.b_w, t.n * MBN + lane + 32 * c);
+            if (NB == 2 && t.nb == 2) wb2[c] = scale_word_mn(p.Bs, krowB, p.b_w, (t.n + 1) * MBN + lane + 32 * c);
           } else {
             wb[c] = scale_word_k(p.Bs, (long)t.e * p.b_rows_per_seg + t.n * MBN + lane + 32 * c, p.K, kb);
+            if (NB == 2 && t.nb == 2)
+              wb2[c] = scale_word_k(p.Bs, (long)t.e * p.b_rows_per_seg + (t.n + 1) * MBN + lane + 32 * c, p.K, kb);
           }
         }
       };
-      uint32_t ra[kScaleAhead][4], rb[kScaleAhead][4];   // ring[j]: the words of K block kb + j
+      uint32_t ra[kScaleAhead][4], rb[kScaleAhead][4], rc[kScaleAhead][4];   // ring[j]: K block kb + j
       if (kScaleRing) {
 #pragma unroll
-        for (int j = 0; j < kScaleAhead; ++j) scale_words(j, ra[j], rb[j]);
+        for (int j = 0; j < kScaleAhead; ++j) scale_words(j, ra[j], rb[j], rc[j]);
       }
       for (int kb = 0; kb < t.nkb; ++kb, ++it) {
-        uint32_t wa[4], wb[4];
+        uint32_t wa[4], wb[4], wb2[4];
         if (kScaleRing) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             wa[c] = ra[0][c];
             wb[c] = rb[0][c];
+            wb2[c] = rc[0][c];
           }
 #pragma unroll
           for (int j = 0; j + 1 < kScaleAhead; ++j)
@@ -382,8 +408,9 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             for (int c = 0; c < 4; ++c) {
               ra[j][c] = ra[j + 1][c];
               rb[j][c] = rb[j + 1][c];
+              rc[j][c] = rc[j + 1][c];
             }
-          scale_words(kb + kScaleAhead, ra[kScaleAhead - 1], rb[kScaleAhead - 1]);
+          scale_words(kb + kScaleAhead, ra[kScaleAhead - 1], rb[kScaleAhead - 1], rc[kScaleAhead - 1]);
         }
         const int s = it % MSTAGES;
         const uint32_t ph = (it / MSTAGES) & 1;
@@ -396,11 +423,14 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         const uint32_t fb = full0 + 8 * s;
         const long krowB = (SCHED == MS_SEG_K ? (long)t.row0 : (long)t.e * p.b_rows_per_seg) + (long)kb * MBK;
         if (ptid == 0) {
-          mbar_expect_tx(fb, (kGather ? 0 : MBM * MBK) + MBN * MBK);
+          mbar_expect_tx(fb, (kGather ? 0 : MBM * MBK) + t.nb * MBN * MBK);
           if (AMODE == MA_TMA_K) tma_load_2d(sa, &tmA, kb * MBK, t.row0, fb);
           if (AMODE == MA_TMA_MN) tma_load_2d(sa, &tmA, t.m * MBM, t.row0 + kb * MBK, fb);
-          if (BMODE == MB_TMA_K) tma_load_2d(sb, &tmB, kb * MBK, t.e * p.b_rows_per_seg + t.n * MBN, fb);
-          if (BMODE == MB_TMA_MN) tma_load_2d(sb, &tmB, t.n * MBN, (int)krowB, fb);
+          for (int j = 0; j < t.nb; ++j) {   // the unit's B tiles, MBN * MBK bytes apart
+            if (BMODE == MB_TMA_K)
+              tma_load_2d(sb + j * MBN * MBK, &tmB, kb * MBK, t.e * p.b_rows_per_seg + (t.n + j) * MBN, fb);
+            if (BMODE == MB_TMA_MN) tma_load_2d(sb + j * MBN * MBK, &tmB, (t.n + j) * MBN, (int)krowB, fb);
+          }
         }
         if (kGather) {
 #pragma unroll
@@ -411,10 +441,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           }
         }
         // block scales of this stage into TMEM (replicated layout, see the file header)
-        if (!kScaleRing) scale_words(kb, wa, wb);
-        const uint32_t scol = tmem_base + kScaleCol0 + s * 8;
+        if (!kScaleRing) scale_words(kb, wa, wb, wb2);
+        const uint32_t scol = tmem_base + kScaleCol0 + s * SCOLS;
         tmem_st4(scol + lanebits, wa[0], wa[1], wa[2], wa[3]);
         tmem_st4(scol + 4 + lanebits, wb[0], wb[1], wb[2], wb[3]);
+        if (NB == 2) tmem_st4(scol + 8 + lanebits, wb2[0], wb2[1], wb2[2], wb2[3]);
         tmem_st_wait();
         tc_fence_before();
         // gathered rows: the arrival is counted once this thread's copies have landed
@@ -429,9 +460,9 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       int it = 0, tcount = 0;
       bool ok = true;
       for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x, ++tcount) {
-        const MTile t = mx_map<SCHED>(p, L);
-        const int acc = tcount & 1;
-        const uint32_t aph = (tcount >> 1) & 1;
+        const MTile t = mx_map<SCHED, NB>(p, L);
+        const int acc = tcount % NACC;
+        const uint32_t aph = (tcount / NACC) & 1;
         if (!mbar_wait(tempty0 + 8 * acc, aph ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t dcol = tmem_base + acc * MBN;
@@ -446,12 +477,17 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           if (kGather) fence_proxy_async();   // cp.async (generic proxy) writes seen by the MMA
           const uint32_t sa = smem_u32(smem + s * kStageBytes);
           const uint32_t sb = sa + MBM * MBK;
-          const uint32_t scol = tmem_base + kScaleCol0 + s * 8;
+          const uint32_t scol = tmem_base + kScaleCol0 + s * SCOLS;
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint64_t da = A_MN ? desc_mnmajor(sa + k * 4096) : desc_kmajor(sa + k * 32);
             const uint64_t db = B_MN ? desc_mnmajor(sb + k * 4096) : desc_kmajor(sb + k * 32);
             mma_mx(dcol, da, db, idesc_mx(A_MN, B_MN, k), scol, scol + 4, (kb > 0 || k > 0) ? 1u : 0u);
+            if (NB == 2 && t.nb == 2) {   // the second B tile: its own accumulator, the same A tile
+              const uint32_t sb1 = sb + MBN * MBK;
+              const uint64_t db1 = B_MN ? desc_mnmajor(sb1 + k * 4096) : desc_kmajor(sb1 + k * 32);
+              mma_mx(dcol + MBN, da, db1, idesc_mx(A_MN, B_MN, k), scol, scol + 8, (kb > 0 || k > 0) ? 1u : 0u);
+            }
           }
           mma_commit(empty0 + 8 * s);
         }
@@ -474,12 +510,17 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     const int r = ew * 32 + lane;
     int tcount = 0;
     for (int L = blockIdx.x; L < ntiles; L += gridDim.x, ++tcount) {
-      const MTile t = mx_map<SCHED>(p, L);
-      const int acc = tcount & 1;
-      const uint32_t aph = (tcount >> 1) & 1;
+      const MTile t0 = mx_map<SCHED, NB>(p, L);
+      const int acc = tcount % NACC;
+      const uint32_t aph = (tcount / NACC) & 1;
       if (!mbar_wait(tfull0 + 8 * acc, aph, abort_flag, p.status)) break;
       tc_fence_after();
-      const uint32_t tbase = tmem_base + acc * MBN + ((uint32_t)(ew * 32) << 16);
+      // the unit's column tiles (NB = 2: accumulator jb holds column tile t0.n + jb)
+#pragma unroll 1
+      for (int jb = 0; jb < t0.nb; ++jb) {
+      MTile t = t0;
+      t.n = t0.n + jb;
+      const uint32_t tbase = tmem_base + (NB == 2 ? jb : acc) * MBN + ((uint32_t)(ew * 32) << 16);
       const int row = t.row0 + r;
       const bool valid = row < t.row_end;
       if (EPI == ME_SWIGLU_Q) {
@@ -647,6 +688,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           }
         }
       }
+      }   // column tiles of the unit
       tc_fence_before();
       mbar_arrive(tempty0 + 8 * acc);
     }
@@ -661,11 +703,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   }
 }
 
-template <int AMODE, int BMODE, int SCHED, int EPI>
+template <int AMODE, int BMODE, int SCHED, int EPI, int NB = 1>
 cudaError_t mx_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const MxParams& p, int grid, cudaStream_t s,
                       const CUtensorMap* tmC = nullptr, const CUtensorMap* tmC2 = nullptr) {
-  auto kern = mx_gemm_kernel<AMODE, BMODE, SCHED, EPI>;
-  constexpr int smem = mx_smem<SCHED>();
+  auto kern = mx_gemm_kernel<AMODE, BMODE, SCHED, EPI, NB>;
+  constexpr int smem = mx_smem<SCHED, NB>();
   static bool attr = false;
   if (!attr) {
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -805,7 +847,7 @@ cudaError_t launch_mx_gateup(const Layer& L, const Bufs& B, cudaStream_t s) {
   p.os = B.hs;
   p.uv = (bf16*)B.uv;
   p.ld_uv = 2 * L.f;
-  return mx_launch<MA_GATHER_K, MB_TMA_K, MS_SEG_M, ME_SWIGLU_Q>(L.tm_W13q /*unused*/, L.tm_W13q, p, L.num_sms, s);
+  return mx_launch<MA_GATHER_K, MB_TMA_K, MS_SEG_M, ME_SWIGLU_Q, 2>(L.tm_W13q /*unused*/, L.tm_W13q, p, L.num_sms, s);
 }
 
 cudaError_t launch_mx_down(const Layer& L, const Bufs& B, cudaStream_t s) {
@@ -821,7 +863,7 @@ cudaError_t launch_mx_down(const Layer& L, const Bufs& B, cudaStream_t s) {
   p.out = B.o;
   p.ldo = L.d;
   p.row_gate = B.row_gate;
-  return mx_launch<MA_TMA_K, MB_TMA_K, MS_SEG_M, ME_GATE>(th, L.tm_Wdq, p, L.num_sms, s);
+  return mx_launch<MA_TMA_K, MB_TMA_K, MS_SEG_M, ME_GATE, 2>(th, L.tm_Wdq, p, L.num_sms, s);
 }
 
 cudaError_t launch_mx_bwd_dh(const Layer& L, const Bufs& B, cudaStream_t s) {
@@ -843,7 +885,7 @@ cudaError_t launch_mx_bwd_dh(const Layer& L, const Bufs& B, cudaStream_t s) {
   p.ld_uv = 2 * L.f;
   p.dg_part = B.dg_part;
   p.dg_slots = L.f / 64;
-  return mx_launch<MA_GATHER_K, MB_TMA_MN, MS_SEG_M, ME_DH_Q>(L.tm_Wdc /*unused*/, L.tm_Wdc, p, L.num_sms, s);
+  return mx_launch<MA_GATHER_K, MB_TMA_MN, MS_SEG_M, ME_DH_Q, 2>(L.tm_Wdc /*unused*/, L.tm_Wdc, p, L.num_sms, s);
 }
 
 cudaError_t launch_mx_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s) {
@@ -860,7 +902,7 @@ cudaError_t launch_mx_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s) {
   p.b_rows_per_seg = 2 * L.f;
   p.out = B.dx_rows;
   p.ldo = L.d;
-  return mx_launch<MA_TMA_K, MB_TMA_MN, MS_SEG_M, ME_STORE>(ta, L.tm_W13c, p, L.num_sms, s);
+  return mx_launch<MA_TMA_K, MB_TMA_MN, MS_SEG_M, ME_STORE, 2>(ta, L.tm_W13c, p, L.num_sms, s);
 }
 
 cudaError_t launch_mx_bwd_dw13(const Layer& L, const Bufs& B, void* dWg, void* dWu, bool acc, cudaStream_t s) {
