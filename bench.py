@@ -945,6 +945,7 @@ PROFILE_CASES = {
     "dsv3_e32_mxfp8_chunked_t4096": (moe_synth.DSV3_MXFP8.with_(name="dsv3_e32_mxfp8", E=32, T=4096, chunk=2048,
                                                                 seed=11), "chunked", 4096),
     "bf16_t2048_fused_fwd": (moe_synth.BF16_T2048, "fwd_fused", 2048),
+    "bf16_t2048_fused_whole_fwd": (moe_synth.BF16_T2048, "fwd_fused_whole", 2048),
     # ~256 rows per routed expert (2-3 row tiles), as in the 256-expert, 8192-token forward; 2.9 GB of weights
     "dsv3_e32_bf16_fwd_t1024": (moe_synth.DSV3_UNIFORM.with_(name="dsv3_e32_T1024", E=32, T=1024, seed=9), "fwd", 1024),
     "dsv3_e32_bf16_fwd_t1024_rowtiles2": (moe_synth.DSV3_UNIFORM.with_(name="dsv3_e32_T1024", E=32, T=1024, seed=9),
@@ -971,8 +972,8 @@ def run_profile_case(args):
         def fn():
             moe_decode(layer.h, xs[it[0] % 8], n, y, ws)
             it[0] += 1
-    elif kind in ("fwd", "fwd_fused", "fwd_rowtiles2"):
-        moe_set_fused(layer.h, 1 if kind == "fwd_fused" else 0)
+    elif kind in ("fwd", "fwd_fused", "fwd_fused_whole", "fwd_rowtiles2"):
+        moe_set_fused(layer.h, {"fwd_fused": 1, "fwd_fused_whole": 2}.get(kind, 0))
         moe_set_pairs(layer.h, 2 if kind == "fwd_rowtiles2" else 0)
         fn = lambda: layer.forward(inp["x"])  # noqa: E731
     else:
