@@ -53,9 +53,10 @@ Sizes sizes_for(const Layer& L, int T) {
   z.packed = al(eb * nseg * 2 * L.f * L.d) + al(eb * nseg * L.d * L.f) + al(eb * L.E * L.d) + al(4 * L.E);
   if (L.prec == MOE_MXFP8) {
     const size_t d = L.d, f = L.f, Rp = rp_max(L, T);
-    z.fwd_scratch = 2 * al(4 * nch * L.E) + al(T * d) + al(T * d / 32) + al(R * f) + al(R * f / 32) + al(2 * R * d);
+    // activations: codes in expert-sorted row order [R], scale atoms per 128-row tile (Rp rows)
+    z.fwd_scratch = 2 * al(4 * nch * L.E) + al(R * d) + al(Rp * d / 32) + al(R * f) + al(Rp * f / 32) + al(2 * R * d);
     z.fwd_ws = z.route + z.fwd_scratch;
-    z.bwd_ws += al(T * d) + al(T * d / 32) + al(R * 2 * f) + al(R * 2 * f / 32) + al(Rp * 2 * f) +
+    z.bwd_ws += al(R * d) + al(Rp * d / 32) + al(R * 2 * f) + al(Rp * 2 * f / 32) + al(Rp * 2 * f) +
                 al(Rp * 2 * f / 32) + 2 * (al(Rp * d) + al(Rp * d / 32)) + al(Rp * f) + al(Rp * f / 32);
     z.packed = mx_packed_bytes(L) + al(2 * L.E * d) + al(4 * L.E);
   }
@@ -98,15 +99,16 @@ Bufs carve(const Layer& L, int T, void* ws, const void* ctx, void* bws) {
     w = carve_route(B, L, w);
   }
   const bool mx = L.prec == MOE_MXFP8;
-  const size_t d = L.d, f = L.f, R = B.R, Tt = T;
+  const size_t d = L.d, f = L.f, R = B.R;
   if (w) {
     B.chunk_hist = (int*)w; w += al(4 * (size_t)B.nch * L.E);
     B.chunk_base = (int*)w; w += al(4 * (size_t)B.nch * L.E);
     if (mx) {
-      B.xq = (uint8_t*)w; w += al(Tt * d);
-      B.xs = (uint8_t*)w; w += al(Tt * d / 32);
+      const size_t Rp = rp_max(L, T);
+      B.xq = (uint8_t*)w; w += al(R * d);
+      B.xs = (uint8_t*)w; w += al(Rp * d / 32);
       B.hq = (uint8_t*)w; w += al(R * f);
-      B.hs = (uint8_t*)w; w += al(R * f / 32);
+      B.hs = (uint8_t*)w; w += al(Rp * f / 32);
     } else {
       B.h = w; w += al(eb * B.R * L.f);
     }
@@ -124,10 +126,10 @@ Bufs carve(const Layer& L, int T, void* ws, const void* ctx, void* bws) {
     if (mx) {
       const size_t Rp = rp_max(L, T);
       B.Rp_max = (int)Rp;
-      B.dyq = (uint8_t*)b; b += al(Tt * d);
-      B.dys = (uint8_t*)b; b += al(Tt * d / 32);
+      B.dyq = (uint8_t*)b; b += al(R * d);
+      B.dys = (uint8_t*)b; b += al(Rp * d / 32);
       B.dudvq = (uint8_t*)b; b += al(R * 2 * f);
-      B.dudvs = (uint8_t*)b; b += al(R * 2 * f / 32);
+      B.dudvs = (uint8_t*)b; b += al(Rp * 2 * f / 32);
       B.dudv_t = (uint8_t*)b; b += al(Rp * 2 * f);
       B.dudv_ts = (uint8_t*)b; b += al(Rp * 2 * f / 32);
       B.x_t = (uint8_t*)b; b += al(Rp * d);
@@ -230,7 +232,7 @@ moe_status forward_experts(moe_handle_s* h, const void* x, int T, void* y, void*
   const Layer& L = h->L;
   Bufs B = carve(L, T, workspace, ctx, nullptr);
   if (h->mx) {
-    CK(run(h, s, G_MX_QUANT, 1, [&] { return launch_mx_quant_rows(x, T, L.d, B.xq, B.xs, s); }));
+    CK(run(h, s, G_MX_QUANT, 1, [&] { return launch_mx_quant_sorted(L, B, x, L.d, B.xq, B.xs, s); }));
     CK(run(h, s, G_GATEUP, 1, [&] { return launch_mx_gateup(L, B, s); }));
     CK(run(h, s, G_DOWN, 1, [&] { return launch_mx_down(L, B, s); }));
   } else if (h->tc && L.fused) {
@@ -266,7 +268,7 @@ moe_status backward_body(moe_handle_s* h, const void* x, const void* dy, int T, 
   const Layer& L = h->L;
   Bufs B = carve(L, T, nullptr, ctx, workspace);
   if (h->mx) {
-    CK(run(h, s, G_MX_QUANT, 1, [&] { return launch_mx_quant_rows(dy, T, L.d, B.dyq, B.dys, s); }));
+    CK(run(h, s, G_MX_QUANT, 1, [&] { return launch_mx_quant_sorted(L, B, dy, L.d, B.dyq, B.dys, s); }));
     CK(run(h, s, G_BWD_DH, 1, [&] { return launch_mx_bwd_dh(L, B, s); }));
     CK(run(h, s, G_BWD_DX, 1, [&] { return launch_mx_bwd_dx(L, B, s); }));
   } else if (h->tc) {

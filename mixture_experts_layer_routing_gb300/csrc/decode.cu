@@ -480,8 +480,6 @@ __global__ void __launch_bounds__(256, 2) decode_gateup_mx_kernel(const uint8_t*
     const size_t rg = (size_t)e * 2 * f + (i / G) * 2 * G + (i % G), ru = rg + G;
     const uint8_t* wg = W13q + rg * d;
     const uint8_t* wu = W13q + ru * d;
-    const uint8_t* sg = W13s + rg * nb;
-    const uint8_t* su = W13s + ru * nb;
     for (int g0 = a0; g0 < a1; g0 += kTokGroup) {
       const int nt = min(kTokGroup, a1 - g0);
       const uint16_t* xr[kTokGroup];
@@ -504,8 +502,8 @@ __global__ void __launch_bounds__(256, 2) decode_gateup_mx_kernel(const uint8_t*
           if (c < nchunk) {
             gv[q] = ld_stream(reinterpret_cast<const bf16*>(wg + (size_t)c * 16));
             uvv[q] = ld_stream(reinterpret_cast<const bf16*>(wu + (size_t)c * 16));
-            sgv[q] = sg[c >> 1];
-            suv[q] = su[c >> 1];
+            sgv[q] = W13s[atom_k(rg, c >> 1, d)];
+            suv[q] = W13s[atom_k(ru, c >> 1, d)];
           }
         }
 #pragma unroll
@@ -576,7 +574,7 @@ __device__ __forceinline__ void load_wd_mx(const uint8_t* Wdq, const uint8_t* Wd
       const int c = (lane + 32 * q) * 16;
       if (f0 + c < f) {
         wv[cc][q] = ld_stream(reinterpret_cast<const bf16*>(row + c));
-        sv[cc][q] = Wds[r * (f / 32) + ((f0 + c) >> 5)];
+        sv[cc][q] = Wds[atom_k(r, (f0 + c) >> 5, f)];
       }
     }
   }
@@ -604,7 +602,6 @@ __global__ void __launch_bounds__(kDownWarps * 32) decode_down_mx_kernel(const u
     uint32_t scur[kCols][kFChunksMx], snext[kCols][kFChunksMx];
     load_wd_mx(Wdq, Wds, w.U[0], d, f, c0, f0, lane, wnext, snext);
     for (int ui = 0; ui < nU; ++ui) {
-      const int e = w.U[ui];
 #pragma unroll
       for (int cc = 0; cc < kCols; ++cc)
 #pragma unroll

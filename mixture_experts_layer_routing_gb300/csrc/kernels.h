@@ -55,10 +55,11 @@ struct Layer {
   // MXFP8 packed weights: E4M3 codes and E8M0 scales (one per 32 along the named axis)
   // MXFP8 scales: K-major arrays row-major (rows, K/32); MN-major arrays (Krows/32, W) stored
   // as [Krows/128][W][4] (the four scales of a column's 128-row K block in one word).
-  uint8_t *W13q, *W13s;     // [E+S][2f][d] along d (gate/up interleaved in blocks of kGateMx rows); [..][d/32]
-  uint8_t *W13c, *W13cs;    // same rows quantised along the packed 2f rows; scales [(E+S)*2f/32][d]
-  uint8_t *Wdq, *Wds;       // [E+S][d][f] along f; [..][f/32]
-  uint8_t *Wdc, *Wdcs;      // same rows quantised along d; scales [(E+S)*d/32][f]
+  // scales in 512-byte atoms (mx_quant.cuh: atom_k for the K-major copies, atom_mn for the others)
+  uint8_t *W13q, *W13s;     // [E+S][2f][d] along d (gate/up interleaved in blocks of kGateMx rows)
+  uint8_t *W13c, *W13cs;    // same rows quantised along the packed 2f rows
+  uint8_t *Wdq, *Wds;       // [E+S][d][f] along f
+  uint8_t *Wdc, *Wdcs;      // same rows quantised along d
   CUtensorMap tm_W13q, tm_Wdq, tm_W13c, tm_Wdc;
 };
 
@@ -94,12 +95,13 @@ struct Bufs {
   float* dwr_part;       // [kRouterSplit, E, d] router weight-gradient partials
   float* dgate;          // [T, k]
   // MXFP8 operands (codes, scales)
-  uint8_t *xq, *xs;      // [T, d], [T, d/32]
-  uint8_t *hq, *hs;      // [R, f], [R, f/32]
-  uint8_t *dyq, *dys;    // [T, d], [T, d/32]
-  uint8_t *dudvq, *dudvs;  // [R, 2f], [R, 2f/32]
+  // codes in expert-sorted row order, scale atoms by row tile (atom_tile, Rp rows)
+  uint8_t *xq, *xs;      // [R, d]: x of each sorted row
+  uint8_t *hq, *hs;      // [R, f]
+  uint8_t *dyq, *dys;    // [R, d]: dy of each sorted row
+  uint8_t *dudvq, *dudvs;  // [R, 2f]
   int Rp_max;            // rows of the token-axis operands: each segment padded to 128 (upper bound)
-  uint8_t *dudv_t, *dudv_ts, *x_t, *x_ts, *dy_t, *dy_ts, *hg_t, *hg_ts;  // [Rp, W], [Rp/32, W]
+  uint8_t *dudv_t, *dudv_ts, *x_t, *x_ts, *dy_t, *dy_ts, *hg_t, *hg_ts;  // [Rp, W], atom_mn scales
 };
 
 // ----------------------------------------------------------- launchers
@@ -153,7 +155,8 @@ cudaError_t launch_tc_bwd_dwd(const Layer& L, const Bufs& B, const void* dy, voi
 bool mx_supported(const Layer& L);
 size_t mx_packed_bytes(const Layer& L);
 cudaError_t mx_pack_weights(Layer& L, const void* Wg, const void* Wu, const void* Wd, void* base, cudaStream_t s);
-cudaError_t launch_mx_quant_rows(const void* src, int rows, int K, uint8_t* q, uint8_t* s, cudaStream_t st);
+cudaError_t launch_mx_quant_sorted(const Layer& L, const Bufs& B, const void* src, int K, uint8_t* q, uint8_t* s,
+                                   cudaStream_t st);
 cudaError_t launch_mx_quant_tokens(const Layer& L, const Bufs& B, const void* src, bool gather, int W, uint8_t* q,
                                    uint8_t* s, cudaStream_t st, const int* out_base = nullptr);
 cudaError_t launch_mx_chunk_layout(const Layer& L, const int* chunk_mt, int n, int* comb_base, int* comb_mt,

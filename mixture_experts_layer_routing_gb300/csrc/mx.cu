@@ -21,11 +21,17 @@
 // The products over token rows (gate/up, down, dY.Wd, dx) run one CTA per 128-row tile and pair of
 // 128-column tiles (NB = 2): the staged A tile feeds two MMAs, so a 48 KB stage carries 512 MMA
 // cycles (a 32 KB stage of one column tile carries 256, too few for the loads to keep up).
-// Scale factors reach TMEM through tcgen05.st from the producer warps. For a
-// 128-row operand tile the MMA reads row r's four k-block scales (one per 32
-// elements of a 128-element stage, selected by the instruction's scale id)
-// from column r/32 of lane 32q + (r mod 32) of the lane quadrant q serving the
-// output row, so every quadrant holds all four columns.
+// Every operand reaches shared memory through the async proxy, issued by one producer thread per
+// stage: TMA tiles for the codes (the token-row activations are quantised in expert-sorted row order,
+// so the A tile of a row tile is one rectangular load) and one 512-byte bulk copy per operand for
+// the block scales, which every quantiser and epilogue writes in the MMA's atom order (see
+// mx_quant.cuh). The MMA thread moves the scales to TMEM with tcgen05.cp.32x128b.warpx4 ahead of the
+// stage's MMAs: for a 128-row operand tile the MMA reads row r's four k-block scales (one per 32
+// elements of a 128-element stage, selected by the instruction's scale id) from column r/32 of lane
+// 32q + (r mod 32) of the lane quadrant q serving the output row, and the warpx4 copy writes the
+// atom's 32 x 4 words to all four quadrants. (Per-thread cp.async row gathers and scale loads kept
+// the producers issue-bound at ~1,200 cycles per stage, and the MMA thread then needed a proxy
+// fence per stage that drained the tensor pipe.)
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -37,15 +43,20 @@ namespace moe {
 
 namespace {
 
-constexpr int MBM = 128, MBN = 128, MBK = 128, MSTAGES = 6;
-constexpr int kProd = 4, kEpi = 4;
+constexpr int MBM = 128, MBN = 128, MBK = 128;
+// Warps: 0 the producer (one thread issues every copy), 1-4 the epilogue (warp w reads TMEM lane
+// quadrant w mod 4), 5 the MMA issuer.
+constexpr int kProd = 1, kEpi = 4;
 constexpr int kMxThreads = (kProd + kEpi + 1) * 32;
 constexpr int kMxMmaWarp = kProd + kEpi;
-constexpr int kStageBytes = MBM * MBK + MBN * MBK;                 // 32 KB
 constexpr int kScaleCol0 = 2 * MBN;                                 // TMEM columns after the two accumulators
-constexpr int kScaleAhead = 4;   // K blocks between a stage's scale-word loads and their use
+constexpr int kScaleAtom = 512;   // one 128-row operand's scale words for one K block (32 rows x 16 bytes)
+// off[] and the tile prefix mt_off[] (nseg + 1 each), copied to shared memory at kernel start: every
+// role maps each unit through them, and a binary search over global memory is ~9 dependent L2
+// round trips at the start of every unit, during which the producers issue no loads.
+constexpr int kSegCache = 2 * (kMaxE + 2) * 4;
 
-enum { MA_GATHER_K = 0, MA_TMA_K = 1, MA_TMA_MN = 2 };
+enum { MA_TMA_K = 1, MA_TMA_MN = 2 };
 enum { MB_TMA_K = 0, MB_TMA_MN = 1 };
 enum { MS_SEG_M = 0, MS_SEG_K = 1 };
 enum { ME_SWIGLU_Q = 0, ME_GATE = 1, ME_DH_Q = 2, ME_STORE = 3, ME_DW13 = 4, ME_DWD = 5 };
@@ -53,23 +64,26 @@ enum { ME_SWIGLU_Q = 0, ME_GATE = 1, ME_DH_Q = 2, ME_STORE = 3, ME_DW13 = 4, ME_
 // Weight-gradient epilogue staging: per epilogue warp two 32-row x 64-column bf16 sub-tiles.
 constexpr int kMxOut = kEpi * 2 * 32 * 128;
 // NB: 128-column B tiles per CTA (1, or 2 for the segment-M products: one staged A tile feeds two
-// MMAs, so a 48 KB stage carries 512 MMA cycles where a 32 KB one carries 256). Stages, stage bytes
-// and the block-scale TMEM columns per stage (A, then each B tile).
-template <int NB> constexpr int mx_stages() { return NB == 2 ? 4 : MSTAGES; }
+// MMAs, so a 48 KB stage carries 512 MMA cycles where a 32 KB one carries 256). Stages, stage bytes,
+// the block-scale TMEM columns per stage (A, then each B tile) and the staged scale bytes per stage.
+// Shared memory: [scale atoms of every stage][stage ring][SEG_K epilogue staging][barriers].
+template <int SCHED, int NB> constexpr int mx_stages() { return NB == 2 ? 4 : SCHED == MS_SEG_K ? 5 : 6; }
 template <int NB> constexpr int mx_stage_bytes() { return MBM * MBK + NB * MBN * MBK; }
 template <int NB> constexpr int mx_scale_cols() { return 4 + 4 * NB; }
+template <int NB> constexpr int mx_scale_bytes() { return (1 + NB) * kScaleAtom; }
+template <int SCHED, int NB> constexpr int mx_scale_region() {
+  return (mx_stages<SCHED, NB>() * mx_scale_bytes<NB>() + 1023) / 1024 * 1024;
+}
 template <int SCHED, int NB = 1>
 constexpr int mx_smem() {
-  return mx_stages<NB>() * mx_stage_bytes<NB>() + (SCHED == MS_SEG_K ? kMxOut : 0) + 1024 + 256;
+  return mx_scale_region<SCHED, NB>() + mx_stages<SCHED, NB>() * mx_stage_bytes<NB>() +
+         (SCHED == MS_SEG_K ? kMxOut : 0) + 1024 + 256 + kSegCache;
 }
 
 struct MxParams {
-  const uint8_t* Ag;      // gathered A codes [*, K] (MA_GATHER_K)
-  const uint8_t* As;      // A scales: [rows][K/32] (K-major) or [Krows/32][W] (MN-major)
+  const uint8_t* As;      // A scale atoms: by row tile (K-major, atom_tile) or 128-row K group (atom_mn)
   int a_w;                // MN-major A: row width W of the code / scale arrays
-  int a_rows;             // rows of a K-major TMA A operand (guards scale reads)
-  long a_kb_rows;         // > 0: A's K-major scales are k-block-major with this many rows
-  const uint8_t* Bs;      // B scales
+  const uint8_t* Bs;      // B scale atoms (K-major weights: atom_k; MN-major: atom_mn)
   int b_w;                // MN-major B: row width W
   int b_rows_per_seg;     // B rows (K-major) or K rows (MN-major) per segment
   const int* row_token;
@@ -95,23 +109,10 @@ struct MxParams {
 };
 
 // ------------------------------------------------------------- quantise (mx_quant.cuh)
-// Scale layouts.
-//  K-major operands: row-major [rows][K/32], byte (row, j = k/32) at row * K/32 + j; the four
-//  bytes of one 128-element K block of a row are one aligned 32-bit word.
-//  The du/dv scales (K-major, read by dx) are instead k-block-major [2f/128][R][4], byte (row, j)
-//  at ((j/4) * R + row) * 4 + j%4: one stage's words of 32 consecutive rows are one request
-//  (measured faster for dx; for the weights' K-major scales the row-major layout, whose
-//  sectors are reused by eight consecutive K blocks, measured faster).
-//  MN-major operands: [Krows/128][W][4], byte (krow/32 = j, col) at ((j/4) * W + col) * 4 + j%4:
-//  the four bytes of one K block of a column are one 32-bit word and the words of consecutive
-//  columns are adjacent, so a warp reads one stage's words of 32 columns in one coalesced request
-//  (the row-major [Krows/32][W] layout took four byte loads per column).
-__host__ __device__ __forceinline__ long sc_index_k(long row, long j, long K) { return row * (K / 32) + j; }
-__host__ __device__ __forceinline__ long sc_index_kb(long row, long j, long rows) {
-  return ((j >> 2) * rows + row) * 4 + (j & 3);
-}
-__host__ __device__ __forceinline__ long sc_index_mn(long j, long col, long W) { return ((j >> 2) * W + col) * 4 + (j & 3); }
-enum { SRC_PLAIN = 0, SRC_GATHER = 1, SRC_W13 = 2 };
+// Scale layouts (all in 512-byte atoms, mx_quant.cuh): the packed weights along K by row (atom_k),
+// the expert-sorted activations along K by row tile (atom_tile), the MN-major operands (weights
+// quantised along their other axis, token-axis operands) by 128-row K group and column (atom_mn).
+enum { SRC_PLAIN = 0, SRC_W13 = 2 };
 
 // Source row of packed W13 row `row` (gate/up interleaved in blocks of G rows).
 __device__ __forceinline__ const bf16* w13_src(const bf16* Wg, const bf16* Wu, long row, int f, int G, int K) {
@@ -125,14 +126,12 @@ __device__ __forceinline__ const bf16* w13_src(const bf16* Wg, const bf16* Wu, l
 // Along K: one warp per row, one lane per 32-element block.
 template <int SRC>
 __global__ void __launch_bounds__(256) mx_quant_rows_kernel(const bf16* __restrict__ src, const bf16* __restrict__ src2,
-                                                            const int* __restrict__ map, long rows, int K, int f, int G,
+                                                            long rows, int K, int f, int G,
                                                             uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
   const long row = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
-  const bf16* sr = SRC == SRC_PLAIN ? src + row * K
-                 : SRC == SRC_GATHER ? src + (long)map[row] * K
-                                     : w13_src(src, src2, row, f, G, K);
+  const bf16* sr = SRC == SRC_PLAIN ? src + row * K : w13_src(src, src2, row, f, G, K);
   for (int b = lane; b < K / 32; b += 32) {
     float v[32];
 #pragma unroll
@@ -141,7 +140,56 @@ __global__ void __launch_bounds__(256) mx_quant_rows_kernel(const bf16* __restri
     const uint8_t sc = quant32(v, lo, hi);
     *reinterpret_cast<uint4*>(q + row * K + b * 32) = lo;
     *reinterpret_cast<uint4*>(q + row * K + b * 32 + 16) = hi;
-    s[sc_index_k(row, b, K)] = sc;
+    s[atom_k(row, b, K)] = sc;
+  }
+}
+
+// Expert-sorted activation rows: CTA per 128-row tile mt of the routing's tile prefix (mt_off), one
+// warp per row, one lane per 32-element block. Row r of tile mt of segment e is sorted row
+// off[e] + (mt - mt_off[e]) * 128 + r, the token row_token[...] of src (src_rows = T) or, with
+// row_token null, that row of src itself; its codes go to q[sorted row] and its scales to the tile's
+// atoms. Tile rows past the segment get zero scales (their codes belong to the next segment).
+__global__ void __launch_bounds__(256) mx_quant_sorted_kernel(const bf16* __restrict__ src,
+                                                              const int* __restrict__ row_token,
+                                                              const int* __restrict__ off,
+                                                              const int* __restrict__ mt_off, int nseg, int K,
+                                                              uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
+  __shared__ int seg[3];
+  const int mt = blockIdx.x;
+  if (threadIdx.x == 0) {
+    int lo = -1;
+    if (mt < mt_off[nseg]) {
+      int l = 0, h = nseg;
+      while (h - l > 1) {
+        const int mid = (l + h) >> 1;
+        if (mt_off[mid] <= mt) l = mid; else h = mid;
+      }
+      lo = l;
+    }
+    seg[0] = lo;
+    seg[1] = lo >= 0 ? off[lo] + (mt - mt_off[lo]) * 128 : 0;
+    seg[2] = lo >= 0 ? off[lo + 1] : 0;
+  }
+  __syncthreads();
+  if (seg[0] < 0) return;
+  const int lane = threadIdx.x & 31;
+  for (int r = threadIdx.x >> 5; r < 128; r += blockDim.x >> 5) {
+    const long p = (long)seg[1] + r;
+    const bool valid = p < seg[2];
+    const bf16* sr = valid ? src + (row_token ? (long)row_token[p] : p) * K : nullptr;
+    for (int b = lane; b < K / 32; b += 32) {
+      uint8_t sc = 0;
+      if (valid) {
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) unpack8(*reinterpret_cast<const uint4*>(sr + b * 32 + 8 * i), v + 8 * i);
+        uint4 lo, hi;
+        sc = quant32(v, lo, hi);
+        *reinterpret_cast<uint4*>(q + p * K + b * 32) = lo;
+        *reinterpret_cast<uint4*>(q + p * K + b * 32 + 16) = hi;
+      }
+      s[atom_tile(mt, r, b, K)] = sc;
+    }
   }
 }
 
@@ -197,7 +245,7 @@ __global__ void __launch_bounds__(256) mx_quant_cols_kernel(const bf16* __restri
   rb += out_shift / 32;                    // segment bases are multiples of 128 rows
 #pragma unroll
   for (int i = 0; i < 32; ++i) q[(rb * 32 + i) * W + c] = (uint8_t)(w[i >> 2] >> (8 * (i & 3)));
-  s[sc_index_mn(rb, c, W)] = sc;
+  s[atom_mn(rb, c, W)] = sc;
 }
 
 // ---------------------------------------------------------------- GEMM
@@ -213,25 +261,38 @@ __device__ __forceinline__ void mma_mx(uint32_t d, uint64_t a, uint64_t b, uint3
       "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
       : "memory");
 }
-__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
+// Shared-memory descriptor of one scale atom for tcgen05.cp: no swizzle, 8-row core matrices of
+// 16-byte rows 128 bytes apart (the atom's 32 rows contiguous).
+__device__ __forceinline__ uint64_t desc_scale_atom(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)(16 >> 4) << 16) | ((uint64_t)(128 >> 4) << 32) |
+         ((uint64_t)1 << 46);
+}
+// 32 rows x 128 bits from shared memory to TMEM columns taddr .. taddr + 3 of every lane quadrant.
+// Ordered before the tcgen05.mma issued after it by the same thread.
+__device__ __forceinline__ void tmem_cp_scales(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+// Contiguous bytes (16-byte aligned, a multiple of 16) into shared memory, counted on an mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
                : "memory");
 }
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 struct MTile {
   int e, m, n, row0, row_end, nkb;
   int nb;   // B tiles of this unit (n, n+1, ..): 1 or 2
+  int mt;   // segment-M: the row tile's index in the tile prefix (its activation scale atoms)
 };
 
+// off / mt_off: the shared-memory copies of p.off and p.mt_off
 template <int SCHED, int NB = 1>
-__device__ __forceinline__ int mx_total(const MxParams& p) {
-  return SCHED == MS_SEG_K ? p.nseg * p.m_tiles * p.n_tiles : p.mt_off[p.nseg] * ((p.n_tiles + NB - 1) / NB);
+__device__ __forceinline__ int mx_total(const MxParams& p, const int* mt_off) {
+  return SCHED == MS_SEG_K ? p.nseg * p.m_tiles * p.n_tiles : mt_off[p.nseg] * ((p.n_tiles + NB - 1) / NB);
 }
 
 template <int SCHED, int NB = 1>
-__device__ __forceinline__ MTile mx_map(const MxParams& p, int L) {
+__device__ __forceinline__ MTile mx_map(const MxParams& p, int L, const int* off, const int* mt_off) {
   MTile t;
   t.nb = 1;
   if (SCHED == MS_SEG_K) {
@@ -240,19 +301,19 @@ __device__ __forceinline__ MTile mx_map(const MxParams& p, int L) {
     const int rem = L % per;
     t.n = rem / p.m_tiles;
     t.m = rem % p.m_tiles;
-    t.row0 = p.mt_off[t.e] * MBK;                  // padded token rows of the segment
-    t.row_end = t.row0 + (p.off[t.e + 1] - p.off[t.e]);
-    t.nkb = p.mt_off[t.e + 1] - p.mt_off[t.e];
+    t.row0 = mt_off[t.e] * MBK;                  // padded token rows of the segment
+    t.row_end = t.row0 + (off[t.e + 1] - off[t.e]);
+    t.nkb = mt_off[t.e + 1] - mt_off[t.e];
     return t;
   }
   const int nu = (p.n_tiles + NB - 1) / NB;   // units of NB column tiles
   int lo = 0, hi = p.nseg;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (p.mt_off[mid] * nu <= L) lo = mid; else hi = mid;
+    if (mt_off[mid] * nu <= L) lo = mid; else hi = mid;
   }
-  const int Me = p.mt_off[lo + 1] - p.mt_off[lo];
-  const int local = L - p.mt_off[lo] * nu;
+  const int Me = mt_off[lo + 1] - mt_off[lo];
+  const int local = L - mt_off[lo] * nu;
   // m-tiles in groups of kRasterM, every column unit of a group before the next group (L2 reuse)
   const int g = local / (kRasterM * nu);
   const int gm = min(kRasterM, Me - g * kRasterM);
@@ -261,17 +322,11 @@ __device__ __forceinline__ MTile mx_map(const MxParams& p, int L) {
   t.n = NB * (within / gm);
   t.nb = min(NB, p.n_tiles - t.n);
   t.m = g * kRasterM + within % gm;
-  t.row0 = p.off[lo] + t.m * MBM;
-  t.row_end = p.off[lo + 1];
+  t.row0 = off[lo] + t.m * MBM;
+  t.row_end = off[lo + 1];
+  t.mt = mt_off[lo] + t.m;
   t.nkb = p.K / MBK;
   return t;
-}
-
-__device__ __forceinline__ uint32_t scale_word_k(const uint8_t* s, long row, int K, int kb) {
-  return *reinterpret_cast<const uint32_t*>(s + row * (K / 32) + kb * 4);
-}
-__device__ __forceinline__ uint32_t scale_word_mn(const uint8_t* s, long krow0, int W, int col) {
-  return *reinterpret_cast<const uint32_t*>(s + ((krow0 >> 7) * (long)W + col) * 4);   // krow0: multiple of 128
 }
 
 // NB = 2 (segment-M products): each CTA unit is one 128-row tile by two 128-column tiles; the two
@@ -282,15 +337,17 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2, MxParams p) {
   static_assert(NB == 1 || (NB == 2 && SCHED == MS_SEG_M), "two B tiles per CTA: segment-M products");
-  constexpr int MSTAGES = mx_stages<NB>();
+  static_assert(mx_smem<SCHED, NB>() <= 227 * 1024, "shared memory per CTA");
+  constexpr int MSTAGES = mx_stages<SCHED, NB>();
   constexpr int kStageBytes = mx_stage_bytes<NB>();
+  constexpr int kScaleBytes = mx_scale_bytes<NB>();
   constexpr int SCOLS = mx_scale_cols<NB>();
   constexpr int NACC = NB == 2 ? 1 : 2;   // accumulator buffers
   constexpr int A_MN = AMODE == MA_TMA_MN ? 1 : 0;
   constexpr int B_MN = BMODE == MB_TMA_MN ? 1 : 0;
-  constexpr bool kGather = AMODE == MA_GATHER_K;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* scales = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);   // per stage: A, B (, B2) atoms
+  uint8_t* smem = scales + mx_scale_region<SCHED, NB>();                             // stage ring (1024-aligned)
   uint8_t* out_stage = smem + MSTAGES * kStageBytes;   // SEG_K epilogue staging (1024-aligned)
   uint64_t* bars = (uint64_t*)(out_stage + (SCHED == MS_SEG_K ? kMxOut : 0));
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + MSTAGES);
@@ -298,10 +355,16 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   const uint32_t drain = smem_u32(bars + 2 * MSTAGES + 4);
   volatile int* abort_flag = (volatile int*)(bars + 2 * MSTAGES + 5);
   uint32_t* tmem_slot = (uint32_t*)(bars + 2 * MSTAGES + 6);
+  int* s_off = (int*)(smem_raw + mx_smem<SCHED, NB>() - kSegCache);   // [kMaxE + 2]
+  int* s_mt = s_off + kMaxE + 2;                                       // [kMaxE + 2]
+  for (int i = threadIdx.x; i <= p.nseg; i += blockDim.x) {
+    s_off[i] = p.off[i];
+    s_mt[i] = p.mt_off[i];
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < MSTAGES; ++s) {
-      mbar_init(full0 + 8 * s, kProd * 32);
+      mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -321,146 +384,55 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int ntiles = mx_total<SCHED, NB>(p);
+  const int ntiles = mx_total<SCHED, NB>(p, s_mt);
 
-  if (warp < kProd) {
-    // ------------------------------------------------------------ producers
-    const int ptid = threadIdx.x;
-    const uint32_t lanebits = (uint32_t)(warp * 32) << 16;
-    int it = 0;
-    bool ok = true;
-    for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
-      const MTile t = mx_map<SCHED, NB>(p, L);
-      const uint8_t* gsrc[8];
-      uint32_t gbytes[8];
-      long arow[4];        // K-major A: source row (token for gathers) of MMA rows lane + 32c
-      if (kGather) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int r = warp * 32 + j * 4 + (lane >> 3);
-          const int row = t.row0 + r;
-          const bool v = row < t.row_end;
-          const int tok = v ? p.row_token[row] : 0;
-          gsrc[j] = p.Ag + (size_t)tok * p.K + (lane & 7) * 16;
-          gbytes[j] = v ? 16u : 0u;
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int row = t.row0 + lane + 32 * c;
-          arow[c] = row < t.row_end ? p.row_token[row] : -1;
-        }
-      } else if (AMODE == MA_TMA_K) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const long row = t.row0 + lane + 32 * c;
-          arow[c] = row < p.a_rows ? row : -1;
-        }
-      }
-      // Block-scale words of K block kb for MMA rows / columns lane + 32c. For the weight gradients
-      // and dx they are read kScaleAhead blocks ahead of their stage into a register ring, so the L2
-      // round trip overlaps the pipeline instead of delaying each stage's full barrier (a 128-deep
-      // E4M3 stage is 256 MMA cycles; dW13 and dWd 15-17% faster than with two blocks ahead); the
-      // forward products and dY.Wd read them at the stage (measured 3-7% faster there).
-      constexpr bool kScaleRing = SCHED == MS_SEG_K || (AMODE == MA_TMA_K && BMODE == MB_TMA_MN);
-      auto scale_words = [&](int kb, uint32_t (&wa)[4], uint32_t (&wb)[4], uint32_t (&wb2)[4]) {
-        const long krowB = (SCHED == MS_SEG_K ? (long)t.row0 : (long)t.e * p.b_rows_per_seg) + (long)kb * MBK;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          wb2[c] = 0u;
-          if (kb >= t.nkb) {
-            wa[c] = wb[c] = 0u;
-            continue;
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (one thread)
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
+        const MTile t = mx_map<SCHED, NB>(p, L, s_off, s_mt);
+        for (int kb = 0; kb < t.nkb; ++kb, ++it) {
+          const int s = it % MSTAGES;
+          const uint32_t ph = (it / MSTAGES) & 1;
+          if (!mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, p.status)) {
+            ok = false;
+            break;
           }
-          if (AMODE == MA_TMA_MN) {
-            wa[c] = scale_word_mn(p.As, (long)t.row0 + (long)kb * MBK, p.a_w, t.m * MBM + lane + 32 * c);
-          } else {
-            wa[c] = arow[c] < 0 ? 0u
-                    : p.a_kb_rows ? *reinterpret_cast<const uint32_t*>(p.As + ((long)kb * p.a_kb_rows + arow[c]) * 4)
-                                  : scale_word_k(p.As, arow[c], p.K, kb);
-          }
-          if (BMODE == MB_TMA_MN) {
-            wb[c] = scale_word_mn(p.Bs, krowB, p.b_w, t.n * MBN + lane + 32 * c);
-            if (NB == 2 && t.nb == 2) wb2[c] = scale_word_mn(p.Bs, krowB, p.b_w, (t.n + 1) * MBN + lane + 32 * c);
-          } else {
-            wb[c] = scale_word_k(p.Bs, (long)t.e * p.b_rows_per_seg + t.n * MBN + lane + 32 * c, p.K, kb);
-            if (NB == 2 && t.nb == 2)
-              wb2[c] = scale_word_k(p.Bs, (long)t.e * p.b_rows_per_seg + (t.n + 1) * MBN + lane + 32 * c, p.K, kb);
-          }
-        }
-      };
-      uint32_t ra[kScaleAhead][4], rb[kScaleAhead][4], rc[kScaleAhead][4];   // ring[j]: K block kb + j
-      if (kScaleRing) {
-#pragma unroll
-        for (int j = 0; j < kScaleAhead; ++j) scale_words(j, ra[j], rb[j], rc[j]);
-      }
-      for (int kb = 0; kb < t.nkb; ++kb, ++it) {
-        uint32_t wa[4], wb[4], wb2[4];
-        if (kScaleRing) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            wa[c] = ra[0][c];
-            wb[c] = rb[0][c];
-            wb2[c] = rc[0][c];
-          }
-#pragma unroll
-          for (int j = 0; j + 1 < kScaleAhead; ++j)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              ra[j][c] = ra[j + 1][c];
-              rb[j][c] = rb[j + 1][c];
-              rc[j][c] = rc[j + 1][c];
-            }
-          scale_words(kb + kScaleAhead, ra[kScaleAhead - 1], rb[kScaleAhead - 1], rc[kScaleAhead - 1]);
-        }
-        const int s = it % MSTAGES;
-        const uint32_t ph = (it / MSTAGES) & 1;
-        if (!mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, p.status)) {
-          ok = false;
-          break;
-        }
-        const uint32_t sa = smem_u32(smem + s * kStageBytes);
-        const uint32_t sb = sa + MBM * MBK;
-        const uint32_t fb = full0 + 8 * s;
-        const long krowB = (SCHED == MS_SEG_K ? (long)t.row0 : (long)t.e * p.b_rows_per_seg) + (long)kb * MBK;
-        if (ptid == 0) {
-          mbar_expect_tx(fb, (kGather ? 0 : MBM * MBK) + t.nb * MBN * MBK);
+          const uint32_t sa = smem_u32(smem + s * kStageBytes);
+          const uint32_t sb = sa + MBM * MBK;
+          const uint32_t ssc = smem_u32(scales + s * kScaleBytes);
+          const uint32_t fb = full0 + 8 * s;
+          const long krowB = (SCHED == MS_SEG_K ? (long)t.row0 : (long)t.e * p.b_rows_per_seg) + (long)kb * MBK;
+          mbar_arrive_expect_tx(fb, (MBM * MBK + kScaleAtom) * (1 + t.nb));
+          // codes: A (sorted token rows, K-major; or a token-axis operand, MN-major), the unit's B tiles
           if (AMODE == MA_TMA_K) tma_load_2d(sa, &tmA, kb * MBK, t.row0, fb);
           if (AMODE == MA_TMA_MN) tma_load_2d(sa, &tmA, t.m * MBM, t.row0 + kb * MBK, fb);
-          for (int j = 0; j < t.nb; ++j) {   // the unit's B tiles, MBN * MBK bytes apart
+          for (int j = 0; j < t.nb; ++j) {   // MBN * MBK bytes apart
             if (BMODE == MB_TMA_K)
               tma_load_2d(sb + j * MBN * MBK, &tmB, kb * MBK, t.e * p.b_rows_per_seg + (t.n + j) * MBN, fb);
             if (BMODE == MB_TMA_MN) tma_load_2d(sb + j * MBN * MBK, &tmB, (t.n + j) * MBN, (int)krowB, fb);
           }
-        }
-        if (kGather) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int r = warp * 32 + j * 4 + (lane >> 3);
-            const int c = lane & 7;
-            cp_async16(sa + r * 128 + ((c ^ (r & 7)) << 4), gsrc[j] + kb * MBK, gbytes[j]);
+          // block scales: one atom per operand tile
+          const long a_atom = A_MN ? ((long)t.row0 / MBK + kb) * (p.a_w / MBM) + t.m : (long)t.mt * (p.K / MBK) + kb;
+          bulk_load(ssc, p.As + a_atom * kScaleAtom, kScaleAtom, fb);
+          for (int j = 0; j < t.nb; ++j) {
+            const long b_atom = B_MN ? krowB / MBK * (p.b_w / MBN) + t.n + j
+                                     : ((long)t.e * p.b_rows_per_seg / MBN + t.n + j) * (p.K / MBK) + kb;
+            bulk_load(ssc + (1 + j) * kScaleAtom, p.Bs + b_atom * kScaleAtom, kScaleAtom, fb);
           }
         }
-        // block scales of this stage into TMEM (replicated layout, see the file header)
-        if (!kScaleRing) scale_words(kb, wa, wb, wb2);
-        const uint32_t scol = tmem_base + kScaleCol0 + s * SCOLS;
-        tmem_st4(scol + lanebits, wa[0], wa[1], wa[2], wa[3]);
-        tmem_st4(scol + 4 + lanebits, wb[0], wb[1], wb[2], wb[3]);
-        if (NB == 2) tmem_st4(scol + 8 + lanebits, wb2[0], wb2[1], wb2[2], wb2[3]);
-        tmem_st_wait();
-        tc_fence_before();
-        // gathered rows: the arrival is counted once this thread's copies have landed
-        if (kGather) cp_async_mbar_arrive_noinc(fb);
-        else mbar_arrive(fb);
       }
     }
-    if (kGather) cp_async_wait<0>();
+    __syncwarp();
   } else if (warp == kMxMmaWarp) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
       int it = 0, tcount = 0;
       bool ok = true;
       for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x, ++tcount) {
-        const MTile t = mx_map<SCHED, NB>(p, L);
+        const MTile t = mx_map<SCHED, NB>(p, L, s_off, s_mt);
         const int acc = tcount % NACC;
         const uint32_t aph = (tcount / NACC) & 1;
         if (!mbar_wait(tempty0 + 8 * acc, aph ^ 1, abort_flag, p.status)) break;
@@ -474,10 +446,15 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             break;
           }
           tc_fence_after();
-          if (kGather) fence_proxy_async();   // cp.async (generic proxy) writes seen by the MMA
           const uint32_t sa = smem_u32(smem + s * kStageBytes);
           const uint32_t sb = sa + MBM * MBK;
           const uint32_t scol = tmem_base + kScaleCol0 + s * SCOLS;
+          const uint32_t ssc = smem_u32(scales + s * kScaleBytes);
+          // the stage's scales into TMEM; the previous use of these columns (stage s, MSTAGES K blocks
+          // ago) finished before the producers could refill the stage
+          tmem_cp_scales(scol, desc_scale_atom(ssc));
+          tmem_cp_scales(scol + 4, desc_scale_atom(ssc + kScaleAtom));
+          if (NB == 2 && t.nb == 2) tmem_cp_scales(scol + 8, desc_scale_atom(ssc + 2 * kScaleAtom));
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint64_t da = A_MN ? desc_mnmajor(sa + k * 4096) : desc_kmajor(sa + k * 32);
@@ -506,11 +483,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int ew = warp - kProd;
+    const int ew = warp & 3;   // TMEM lane quadrant of this warp
     const int r = ew * 32 + lane;
     int tcount = 0;
     for (int L = blockIdx.x; L < ntiles; L += gridDim.x, ++tcount) {
-      const MTile t0 = mx_map<SCHED, NB>(p, L);
+      const MTile t0 = mx_map<SCHED, NB>(p, L, s_off, s_mt);
       const int acc = tcount % NACC;
       const uint32_t aph = (tcount / NACC) & 1;
       if (!mbar_wait(tfull0 + 8 * acc, aph, abort_flag, p.status)) break;
@@ -544,7 +521,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             const uint8_t sc = quant32(hf, lo, hi);
             *reinterpret_cast<uint4*>(p.oq + (size_t)row * p.f + col) = lo;
             *reinterpret_cast<uint4*>(p.oq + (size_t)row * p.f + col + 16) = hi;
-            p.os[sc_index_k(row, col / 32, p.f)] = sc;
+            p.os[atom_tile(t.mt, r, col / 32, p.f)] = sc;
             if (p.uv) {
               bf16* uvrow = p.uv + (size_t)row * p.ld_uv + t.n * 128;
 #pragma unroll
@@ -615,11 +592,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             uint8_t* qrow = p.oq + (size_t)row * p.ld_uv;
             *reinterpret_cast<uint4*>(qrow + ucol) = lo;
             *reinterpret_cast<uint4*>(qrow + ucol + 16) = hi;
-            p.os[sc_index_kb(row, ucol / 32, p.a_rows)] = sc;
+            p.os[atom_tile(t.mt, r, ucol / 32, 2 * (long)p.f)] = sc;
             sc = quant32(dv, lo, hi);
             *reinterpret_cast<uint4*>(qrow + ucol + 64) = lo;
             *reinterpret_cast<uint4*>(qrow + ucol + 80) = hi;
-            p.os[sc_index_kb(row, (ucol + 64) / 32, p.a_rows)] = sc;
+            p.os[atom_tile(t.mt, r, (ucol + 64) / 32, 2 * (long)p.f)] = sc;
             if ((c0 & 63) == 32) {
               if (row < p.A_rows) p.dg_part[(size_t)row * p.dg_slots + (t.n * 128 + c0 - 32) / 64] = dgp;
               dgp = 0.f;
@@ -760,9 +737,9 @@ cudaError_t mx_pack_weights(Layer& L, const void* Wg, const void* Wu, const void
   L.Wdcs = p; p += al(wd / 32);
   const bf16 *g = (const bf16*)Wg, *u = (const bf16*)Wu, *dw = (const bf16*)Wd;
   const long r13 = (long)nseg * 2 * f, rd = (long)nseg * d;
-  mx_quant_rows_kernel<SRC_W13><<<blocks_for(r13, 8), 256, 0, s>>>(g, u, nullptr, r13, L.d, L.f, kGateMx, L.W13q,
+  mx_quant_rows_kernel<SRC_W13><<<blocks_for(r13, 8), 256, 0, s>>>(g, u, r13, L.d, L.f, kGateMx, L.W13q,
                                                                      L.W13s);
-  mx_quant_rows_kernel<SRC_PLAIN><<<blocks_for(rd, 8), 256, 0, s>>>(dw, nullptr, nullptr, rd, L.f, L.f, 0, L.Wdq,
+  mx_quant_rows_kernel<SRC_PLAIN><<<blocks_for(rd, 8), 256, 0, s>>>(dw, nullptr, rd, L.f, L.f, 0, L.Wdq,
                                                                      L.Wds);
   mx_quant_cols_kernel<CSRC_W13><<<dim3(blocks_for(d, 256), (unsigned)(r13 / 32)), 256, 0, s>>>(
       g, u, nullptr, nullptr, nullptr, 0, L.d, L.f, kGateMx, L.W13c, L.W13cs, nullptr);
@@ -776,9 +753,13 @@ cudaError_t mx_pack_weights(Layer& L, const void* Wg, const void* Wu, const void
   return cudaSuccess;
 }
 
-cudaError_t launch_mx_quant_rows(const void* src, int rows, int K, uint8_t* q, uint8_t* s, cudaStream_t st) {
-  mx_quant_rows_kernel<SRC_PLAIN><<<blocks_for(rows, 8), 256, 0, st>>>((const bf16*)src, nullptr, nullptr, rows, K, 0,
-                                                                        0, q, s);
+// Token rows of src [T, K] in expert-sorted order (row_token) with their scale atoms by row tile.
+cudaError_t launch_mx_quant_sorted(const Layer& L, const Bufs& B, const void* src, int K, uint8_t* q, uint8_t* s,
+                                   cudaStream_t st) {
+  const int nseg = L.E + L.S;
+  const long tiles = ((long)B.R + 127L * nseg) / 128 + 1;   // at least the routing's tile count
+  mx_quant_sorted_kernel<<<(unsigned)tiles, 256, 0, st>>>((const bf16*)src, B.row_token, B.off, B.mt_off, nseg, K, q,
+                                                          s);
   return cudaGetLastError();
 }
 
@@ -836,8 +817,9 @@ cudaError_t launch_mx_chunk_layout(const Layer& L, const int* chunk_mt, int n, i
 }
 
 cudaError_t launch_mx_gateup(const Layer& L, const Bufs& B, cudaStream_t s) {
+  CUtensorMap ta;
+  if (!make_tmap(&ta, B.xq, L.d, B.R, MBK, MBM, 1)) return cudaErrorInvalidValue;
   MxParams p = mx_base(L, B);
-  p.Ag = B.xq;
   p.As = B.xs;
   p.Bs = L.W13s;
   p.K = L.d;
@@ -847,7 +829,7 @@ cudaError_t launch_mx_gateup(const Layer& L, const Bufs& B, cudaStream_t s) {
   p.os = B.hs;
   p.uv = (bf16*)B.uv;
   p.ld_uv = 2 * L.f;
-  return mx_launch<MA_GATHER_K, MB_TMA_K, MS_SEG_M, ME_SWIGLU_Q, 2>(L.tm_W13q /*unused*/, L.tm_W13q, p, L.num_sms, s);
+  return mx_launch<MA_TMA_K, MB_TMA_K, MS_SEG_M, ME_SWIGLU_Q, 2>(ta, L.tm_W13q, p, L.num_sms, s);
 }
 
 cudaError_t launch_mx_down(const Layer& L, const Bufs& B, cudaStream_t s) {
@@ -855,7 +837,6 @@ cudaError_t launch_mx_down(const Layer& L, const Bufs& B, cudaStream_t s) {
   if (!make_tmap(&th, B.hq, L.f, B.R, MBK, MBM, 1)) return cudaErrorInvalidValue;
   MxParams p = mx_base(L, B);
   p.As = B.hs;
-  p.a_rows = B.R;
   p.Bs = L.Wds;
   p.K = L.f;
   p.n_tiles = L.d / MBN;
@@ -867,8 +848,9 @@ cudaError_t launch_mx_down(const Layer& L, const Bufs& B, cudaStream_t s) {
 }
 
 cudaError_t launch_mx_bwd_dh(const Layer& L, const Bufs& B, cudaStream_t s) {
+  CUtensorMap ta;
+  if (!make_tmap(&ta, B.dyq, L.d, B.R, MBK, MBM, 1)) return cudaErrorInvalidValue;
   MxParams p = mx_base(L, B);
-  p.Ag = B.dyq;
   p.As = B.dys;
   p.Bs = L.Wdcs;
   p.b_w = L.f;
@@ -879,13 +861,12 @@ cudaError_t launch_mx_bwd_dh(const Layer& L, const Bufs& B, cudaStream_t s) {
   p.out2 = B.hg;
   p.oq = B.dudvq;
   p.os = B.dudvs;
-  p.a_rows = B.R;   // rows of the du/dv scale array written k-block-major (A is gathered: no guard)
   p.row_gate = B.row_gate;
   p.uv = (bf16*)B.uv;
   p.ld_uv = 2 * L.f;
   p.dg_part = B.dg_part;
   p.dg_slots = L.f / 64;
-  return mx_launch<MA_GATHER_K, MB_TMA_MN, MS_SEG_M, ME_DH_Q, 2>(L.tm_Wdc /*unused*/, L.tm_Wdc, p, L.num_sms, s);
+  return mx_launch<MA_TMA_K, MB_TMA_MN, MS_SEG_M, ME_DH_Q, 2>(ta, L.tm_Wdc, p, L.num_sms, s);
 }
 
 cudaError_t launch_mx_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s) {
@@ -893,8 +874,6 @@ cudaError_t launch_mx_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s) {
   if (!make_tmap(&ta, B.dudvq, 2 * L.f, B.R, MBK, MBM, 1)) return cudaErrorInvalidValue;
   MxParams p = mx_base(L, B);
   p.As = B.dudvs;
-  p.a_rows = B.R;
-  p.a_kb_rows = B.R;
   p.Bs = L.W13cs;
   p.b_w = L.d;
   p.K = 2 * L.f;

@@ -17,6 +17,26 @@ __device__ __forceinline__ int mx_exponent(float amax) {
   const int X = e - 127 - 8;
   return X < -127 ? -127 : (X > 127 ? 127 : X);
 }
+// Block-scale layout of every MXFP8 operand: "atoms" of 512 bytes, one per 128 operand rows (or
+// columns, MN-major) and 128-element K block, each in the order in which tcgen05.cp.32x128b.warpx4
+// moves it to TMEM for the MMA (row r of the 128 at byte 16 (r mod 32) + 4 (r / 32), the four
+// 32-element sub-blocks of the K block in its four bytes). A GEMM stage then loads each operand's
+// scales with one 512-byte bulk copy.
+// K-major operand whose 128-row tiles start at multiples of 128 (the packed weights): byte of
+// (row, 32-block b) for reduction length K.
+__host__ __device__ __forceinline__ long atom_k(long row, long b, long K) {
+  return (((row >> 7) * (K >> 7) + (b >> 2)) << 9) + ((row & 31) << 4) + (((row >> 5) & 3) << 2) + (b & 3);
+}
+// K-major operand in 128-row tiles numbered mt (the expert-sorted activations: tile mt of expert e
+// covers its rows m*128 .. m*128+127, mt = tile prefix of e + m): byte of (tile mt, row r < 128, b).
+__host__ __device__ __forceinline__ long atom_tile(long mt, int r, long b, long K) {
+  return ((mt * (K >> 7) + (b >> 2)) << 9) + ((r & 31) << 4) + (((r >> 5) & 3) << 2) + (b & 3);
+}
+// MN-major operand [Krows][W] quantised along Krows in 32-row blocks rb: byte of (rb, column c).
+__host__ __device__ __forceinline__ long atom_mn(long rb, long c, long W) {
+  return (((rb >> 2) * (W >> 7) + (c >> 7)) << 9) + ((c & 31) << 4) + (((c >> 5) & 3) << 2) + (rb & 3);
+}
+
 // 32 values -> 32 E4M3 codes (two uint4) and the E8M0 byte.
 __device__ __forceinline__ uint8_t quant32(const float* v, uint4& lo, uint4& hi) {
   float amax = 0.f;

@@ -53,9 +53,19 @@ def packed_w13(Wg, Wu, G):
     return out
 
 
+def scales_k(raw, rows, K):
+    """Scale bytes of a K-major operand as [rows][K/32]. Stored in 512-byte atoms, one per 128 rows and
+    128-element K block, in the order the MMA's scale copy takes them: row r of the 128 at byte
+    16 (r mod 32) + 4 (r / 32), the four 32-element blocks of the K block in its four bytes."""
+    a = raw.reshape(rows // 128, K // 128, 32, 4, 4)          # (row tile, K block, r mod 32, r / 32, block)
+    return a.transpose(0, 3, 2, 1, 4).reshape(rows, K // 32)
+
+
 def scales_mn(raw, Krows, W):
-    """Scale bytes of an MN-major operand, stored [Krows/128][W][4], as [Krows/32][W]."""
-    return raw.reshape(Krows // 128, W, 4).transpose(0, 2, 1).reshape(Krows // 32, W)
+    """Scale bytes of an MN-major operand as [Krows/32][W]: atoms of 128 K rows by 128 columns, column c
+    of the 128 at byte 16 (c mod 32) + 4 (c / 32), the four 32-row blocks in its four bytes."""
+    a = raw.reshape(Krows // 128, W // 128, 32, 4, 4)        # (K group, column tile, c mod 32, c / 32, block)
+    return a.transpose(0, 4, 1, 3, 2).reshape(Krows // 32, W)
 
 
 def test_mx_weight_quantisation_byte_exact():
@@ -74,10 +84,10 @@ def test_mx_weight_quantisation_byte_exact():
     W13 = packed_w13(n["Wg"], n["Wu"], G_MX)
     c, s = oracle.mx_quantize(W13, axis=2)
     assert np.array_equal(parts["W13q"].reshape(c.shape), c)
-    assert np.array_equal(parts["W13s"].reshape(s.shape), s)
+    assert np.array_equal(scales_k(parts["W13s"], nseg * 2 * f, d).reshape(s.shape), s)
     c, s = oracle.mx_quantize(n["Wd"], axis=2)
     assert np.array_equal(parts["Wdq"].reshape(c.shape), c)
-    assert np.array_equal(parts["Wds"].reshape(s.shape), s)
+    assert np.array_equal(scales_k(parts["Wds"], nseg * d, f).reshape(s.shape), s)
     c, s = oracle.mx_quantize(W13, axis=1)                 # along the packed 2f rows
     assert np.array_equal(parts["W13c"].reshape(c.shape), c)
     assert np.array_equal(scales_mn(parts["W13cs"], nseg * 2 * f, d).reshape(s.shape), s)
