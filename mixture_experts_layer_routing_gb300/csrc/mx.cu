@@ -18,9 +18,10 @@
 // Gate/up rows of the MXFP8 W13 are interleaved in blocks of 64 so that one
 // 128-column tile holds 64 gate and the matching 64 up features.
 //
-// The products over token rows (gate/up, down, dY.Wd, dx) run one CTA per 128-row tile and pair of
-// 128-column tiles (NB = 2): the staged A tile feeds two MMAs, so a 48 KB stage carries 512 MMA
-// cycles (a 32 KB stage of one column tile carries 256, too few for the loads to keep up).
+// The products over token rows gate/up, down and dx run one CTA per 128-row tile and pair of
+// 128-column tiles (NB = 2): the staged A tile feeds two MMAs (a 48 KB stage carries 512 MMA cycles)
+// and is read from shared memory once per pair. dY.Wd runs one column tile per CTA (NB = 1), whose
+// double-buffered accumulators let its heavy epilogue overlap the next tile's MMAs.
 // Every operand reaches shared memory through the async proxy, issued by one producer thread per
 // stage: TMA tiles for the codes (the token-row activations are quantised in expert-sorted row order,
 // so the A tile of a row tile is one rectangular load) and one 512-byte bulk copy per operand for
@@ -56,28 +57,23 @@ constexpr int kScaleAtom = 512;   // one 128-row operand's scale words for one K
 // round trips at the start of every unit, during which the producers issue no loads.
 constexpr int kSegCache = 2 * (kMaxE + 2) * 4;
 
-enum { MA_TMA_K = 1, MA_TMA_MN = 2 };
 enum { MB_TMA_K = 0, MB_TMA_MN = 1 };
-enum { MS_SEG_M = 0, MS_SEG_K = 1 };
 enum { ME_SWIGLU_Q = 0, ME_GATE = 1, ME_DH_Q = 2, ME_STORE = 3, ME_DW13 = 4, ME_DWD = 5 };
 
-// Weight-gradient epilogue staging: per epilogue warp two 32-row x 64-column bf16 sub-tiles.
-constexpr int kMxOut = kEpi * 2 * 32 * 128;
 // NB: 128-column B tiles per CTA (1, or 2 for the segment-M products: one staged A tile feeds two
 // MMAs, so a 48 KB stage carries 512 MMA cycles where a 32 KB one carries 256). Stages, stage bytes,
 // the block-scale TMEM columns per stage (A, then each B tile) and the staged scale bytes per stage.
 // Shared memory: [scale atoms of every stage][stage ring][SEG_K epilogue staging][barriers].
-template <int SCHED, int NB> constexpr int mx_stages() { return NB == 2 ? 4 : SCHED == MS_SEG_K ? 5 : 6; }
+template <int NB> constexpr int mx_stages() { return NB == 2 ? 4 : 6; }
 template <int NB> constexpr int mx_stage_bytes() { return MBM * MBK + NB * MBN * MBK; }
 template <int NB> constexpr int mx_scale_cols() { return 4 + 4 * NB; }
 template <int NB> constexpr int mx_scale_bytes() { return (1 + NB) * kScaleAtom; }
-template <int SCHED, int NB> constexpr int mx_scale_region() {
-  return (mx_stages<SCHED, NB>() * mx_scale_bytes<NB>() + 1023) / 1024 * 1024;
+template <int NB> constexpr int mx_scale_region() {
+  return (mx_stages<NB>() * mx_scale_bytes<NB>() + 1023) / 1024 * 1024;
 }
-template <int SCHED, int NB = 1>
+template <int NB>
 constexpr int mx_smem() {
-  return mx_scale_region<SCHED, NB>() + mx_stages<SCHED, NB>() * mx_stage_bytes<NB>() +
-         (SCHED == MS_SEG_K ? kMxOut : 0) + 1024 + 256 + kSegCache;
+  return mx_scale_region<NB>() + mx_stages<NB>() * mx_stage_bytes<NB>() + 1024 + 256 + kSegCache;
 }
 
 struct MxParams {
@@ -286,26 +282,14 @@ struct MTile {
 };
 
 // off / mt_off: the shared-memory copies of p.off and p.mt_off
-template <int SCHED, int NB = 1>
+template <int NB>
 __device__ __forceinline__ int mx_total(const MxParams& p, const int* mt_off) {
-  return SCHED == MS_SEG_K ? p.nseg * p.m_tiles * p.n_tiles : mt_off[p.nseg] * ((p.n_tiles + NB - 1) / NB);
+  return mt_off[p.nseg] * ((p.n_tiles + NB - 1) / NB);
 }
 
-template <int SCHED, int NB = 1>
+template <int NB>
 __device__ __forceinline__ MTile mx_map(const MxParams& p, int L, const int* off, const int* mt_off) {
   MTile t;
-  t.nb = 1;
-  if (SCHED == MS_SEG_K) {
-    const int per = p.m_tiles * p.n_tiles;
-    t.e = L / per;
-    const int rem = L % per;
-    t.n = rem / p.m_tiles;
-    t.m = rem % p.m_tiles;
-    t.row0 = mt_off[t.e] * MBK;                  // padded token rows of the segment
-    t.row_end = t.row0 + (off[t.e + 1] - off[t.e]);
-    t.nkb = mt_off[t.e + 1] - mt_off[t.e];
-    return t;
-  }
   const int nu = (p.n_tiles + NB - 1) / NB;   // units of NB column tiles
   int lo = 0, hi = p.nseg;
   while (hi - lo > 1) {
@@ -329,33 +313,30 @@ __device__ __forceinline__ MTile mx_map(const MxParams& p, int L, const int* off
   return t;
 }
 
-// NB = 2 (segment-M products): each CTA unit is one 128-row tile by two 128-column tiles; the two
-// accumulators fill the TMEM columns that NB = 1 uses for double buffering, so a unit's epilogue is
-// not overlapped with the next unit's MMAs.
-template <int AMODE, int BMODE, int SCHED, int EPI, int NB>
+// Products over the expert-sorted token rows: A = activation rows [R, K] (K-major), B = the expert's
+// weight rows (K-major) or columns (MN-major); units of one 128-row tile and NB 128-column tiles.
+// NB = 2: the two accumulators fill the TMEM columns that NB = 1 uses for double buffering, so a
+// unit's epilogue is not overlapped with the next unit's MMAs.
+template <int BMODE, int EPI, int NB>
 __global__ void __launch_bounds__(kMxThreads, 1)
-    mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2, MxParams p) {
-  static_assert(NB == 1 || (NB == 2 && SCHED == MS_SEG_M), "two B tiles per CTA: segment-M products");
-  static_assert(mx_smem<SCHED, NB>() <= 227 * 1024, "shared memory per CTA");
-  constexpr int MSTAGES = mx_stages<SCHED, NB>();
+    mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, MxParams p) {
+  static_assert(mx_smem<NB>() <= 227 * 1024, "shared memory per CTA");
+  constexpr int MSTAGES = mx_stages<NB>();
   constexpr int kStageBytes = mx_stage_bytes<NB>();
   constexpr int kScaleBytes = mx_scale_bytes<NB>();
   constexpr int SCOLS = mx_scale_cols<NB>();
   constexpr int NACC = NB == 2 ? 1 : 2;   // accumulator buffers
-  constexpr int A_MN = AMODE == MA_TMA_MN ? 1 : 0;
   constexpr int B_MN = BMODE == MB_TMA_MN ? 1 : 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* scales = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);   // per stage: A, B (, B2) atoms
-  uint8_t* smem = scales + mx_scale_region<SCHED, NB>();                             // stage ring (1024-aligned)
-  uint8_t* out_stage = smem + MSTAGES * kStageBytes;   // SEG_K epilogue staging (1024-aligned)
-  uint64_t* bars = (uint64_t*)(out_stage + (SCHED == MS_SEG_K ? kMxOut : 0));
+  uint8_t* smem = scales + mx_scale_region<NB>();                                    // stage ring (1024-aligned)
+  uint64_t* bars = (uint64_t*)(smem + MSTAGES * kStageBytes);
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + MSTAGES);
   const uint32_t tfull0 = smem_u32(bars + 2 * MSTAGES), tempty0 = smem_u32(bars + 2 * MSTAGES + 2);
   const uint32_t drain = smem_u32(bars + 2 * MSTAGES + 4);
   volatile int* abort_flag = (volatile int*)(bars + 2 * MSTAGES + 5);
   uint32_t* tmem_slot = (uint32_t*)(bars + 2 * MSTAGES + 6);
-  int* s_off = (int*)(smem_raw + mx_smem<SCHED, NB>() - kSegCache);   // [kMaxE + 2]
+  int* s_off = (int*)(smem_raw + mx_smem<NB>() - kSegCache);   // [kMaxE + 2]
   int* s_mt = s_off + kMaxE + 2;                                       // [kMaxE + 2]
   for (int i = threadIdx.x; i <= p.nseg; i += blockDim.x) {
     s_off[i] = p.off[i];
@@ -384,7 +365,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int ntiles = mx_total<SCHED, NB>(p, s_mt);
+  const int ntiles = mx_total<NB>(p, s_mt);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (one thread)
@@ -392,7 +373,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       int it = 0;
       bool ok = true;
       for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x) {
-        const MTile t = mx_map<SCHED, NB>(p, L, s_off, s_mt);
+        const MTile t = mx_map<NB>(p, L, s_off, s_mt);
         for (int kb = 0; kb < t.nkb; ++kb, ++it) {
           const int s = it % MSTAGES;
           const uint32_t ph = (it / MSTAGES) & 1;
@@ -404,18 +385,17 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           const uint32_t sb = sa + MBM * MBK;
           const uint32_t ssc = smem_u32(scales + s * kScaleBytes);
           const uint32_t fb = full0 + 8 * s;
-          const long krowB = (SCHED == MS_SEG_K ? (long)t.row0 : (long)t.e * p.b_rows_per_seg) + (long)kb * MBK;
+          const long krowB = (long)t.e * p.b_rows_per_seg + (long)kb * MBK;
           mbar_arrive_expect_tx(fb, (MBM * MBK + kScaleAtom) * (1 + t.nb));
-          // codes: A (sorted token rows, K-major; or a token-axis operand, MN-major), the unit's B tiles
-          if (AMODE == MA_TMA_K) tma_load_2d(sa, &tmA, kb * MBK, t.row0, fb);
-          if (AMODE == MA_TMA_MN) tma_load_2d(sa, &tmA, t.m * MBM, t.row0 + kb * MBK, fb);
+          // codes: A (sorted token rows), the unit's B tiles
+          tma_load_2d(sa, &tmA, kb * MBK, t.row0, fb);
           for (int j = 0; j < t.nb; ++j) {   // MBN * MBK bytes apart
             if (BMODE == MB_TMA_K)
               tma_load_2d(sb + j * MBN * MBK, &tmB, kb * MBK, t.e * p.b_rows_per_seg + (t.n + j) * MBN, fb);
             if (BMODE == MB_TMA_MN) tma_load_2d(sb + j * MBN * MBK, &tmB, (t.n + j) * MBN, (int)krowB, fb);
           }
           // block scales: one atom per operand tile
-          const long a_atom = A_MN ? ((long)t.row0 / MBK + kb) * (p.a_w / MBM) + t.m : (long)t.mt * (p.K / MBK) + kb;
+          const long a_atom = (long)t.mt * (p.K / MBK) + kb;
           bulk_load(ssc, p.As + a_atom * kScaleAtom, kScaleAtom, fb);
           for (int j = 0; j < t.nb; ++j) {
             const long b_atom = B_MN ? krowB / MBK * (p.b_w / MBN) + t.n + j
@@ -432,7 +412,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       int it = 0, tcount = 0;
       bool ok = true;
       for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x, ++tcount) {
-        const MTile t = mx_map<SCHED, NB>(p, L, s_off, s_mt);
+        const MTile t = mx_map<NB>(p, L, s_off, s_mt);
         const int acc = tcount % NACC;
         const uint32_t aph = (tcount / NACC) & 1;
         if (!mbar_wait(tempty0 + 8 * acc, aph ^ 1, abort_flag, p.status)) break;
@@ -457,13 +437,13 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           if (NB == 2 && t.nb == 2) tmem_cp_scales(scol + 8, desc_scale_atom(ssc + 2 * kScaleAtom));
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint64_t da = A_MN ? desc_mnmajor(sa + k * 4096) : desc_kmajor(sa + k * 32);
+            const uint64_t da = desc_kmajor(sa + k * 32);
             const uint64_t db = B_MN ? desc_mnmajor(sb + k * 4096) : desc_kmajor(sb + k * 32);
-            mma_mx(dcol, da, db, idesc_mx(A_MN, B_MN, k), scol, scol + 4, (kb > 0 || k > 0) ? 1u : 0u);
+            mma_mx(dcol, da, db, idesc_mx(0, B_MN, k), scol, scol + 4, (kb > 0 || k > 0) ? 1u : 0u);
             if (NB == 2 && t.nb == 2) {   // the second B tile: its own accumulator, the same A tile
               const uint32_t sb1 = sb + MBN * MBK;
               const uint64_t db1 = B_MN ? desc_mnmajor(sb1 + k * 4096) : desc_kmajor(sb1 + k * 32);
-              mma_mx(dcol + MBN, da, db1, idesc_mx(A_MN, B_MN, k), scol, scol + 8, (kb > 0 || k > 0) ? 1u : 0u);
+              mma_mx(dcol + MBN, da, db1, idesc_mx(0, B_MN, k), scol, scol + 8, (kb > 0 || k > 0) ? 1u : 0u);
             }
           }
           mma_commit(empty0 + 8 * s);
@@ -487,7 +467,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     const int r = ew * 32 + lane;
     int tcount = 0;
     for (int L = blockIdx.x; L < ntiles; L += gridDim.x, ++tcount) {
-      const MTile t0 = mx_map<SCHED, NB>(p, L, s_off, s_mt);
+      const MTile t0 = mx_map<NB>(p, L, s_off, s_mt);
       const int acc = tcount % NACC;
       const uint32_t aph = (tcount / NACC) & 1;
       if (!mbar_wait(tfull0 + 8 * acc, aph, abort_flag, p.status)) break;
@@ -603,75 +583,12 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             }
           }
         }
-      } else {
-        // Weight gradients (SEG_K). Tile rows are packed dW13 rows (blocks of 64 gate then 64 up
-        // features: warps 0-1 write dWg rows, warps 2-3 dWu rows) or dWd rows. Each warp writes its
-        // 32 rows as 32 x 64 sub-tiles through a double-buffered 128-byte-swizzled staging buffer,
-        // stored by TMA (whole lines, no partial-sector writes).
-        const bool empty = t.nkb == 0;
-        const CUtensorMap* tmo = &tmC;
-        int orow0;
-        if (EPI == ME_DW13) {
-          if (ew >= 2) tmo = &tmC2;
-          orow0 = t.e * p.f + t.m * 64 + (ew & 1) * 32;
-        } else {
-          orow0 = (t.e * p.m_tiles + t.m) * MBM + ew * 32;
-        }
-        const uint32_t wbuf = smem_u32(out_stage) + ew * 2 * 4096;
-#pragma unroll 1
-        for (int c0 = 0; c0 < MBN; c0 += 64) {
-          const uint32_t buf = wbuf + ((c0 >> 6) & 1) * 4096;
-          float of[64];
-          if (!empty) {
-            uint32_t a[32], b[32];
-            tmem_ld32(tbase + c0, a);
-            tmem_ld32(tbase + c0 + 32, b);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              of[i] = __uint_as_float(a[i]);
-              of[32 + i] = __uint_as_float(b[i]);
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 64; ++i) of[i] = 0.f;
-          }
-          if (p.accumulate) {
-            const bf16* base = (EPI == ME_DW13 && ew >= 2) ? (const bf16*)p.out2 : (const bf16*)p.out;
-            const bf16* old = base + (size_t)(orow0 + lane) * p.ldo + t.n * MBN + c0;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              float o8[8];
-              unpack8(*reinterpret_cast<const uint4*>(old + q * 8), o8);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) of[q * 8 + i] += o8[i];
-            }
-          }
-          // the store that last read this buffer (two sub-tiles ago) must have finished reading it
-          if (lane == 0) bulk_wait_read<1>();
-          __syncwarp();
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint4 v = pack8(of + q * 8);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf + lane * 128 + ((q ^ (lane & 7)) << 4)),
-                         "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                         : "memory");
-          }
-          fence_proxy_async();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d_hint(tmo, t.n * MBN + c0, orow0, buf, policy_evict_first());
-            bulk_commit();
-          }
-        }
       }
       }   // column tiles of the unit
       tc_fence_before();
       mbar_arrive(tempty0 + 8 * acc);
     }
   }
-  // the weight-gradient stores must have read their staging before the CTA exits
-  if (SCHED == MS_SEG_K && warp >= kProd && warp < kMxMmaWarp && lane == 0) bulk_wait<0>();
   tc_fence_before();
   __syncthreads();
   if (warp == kMxMmaWarp) {
@@ -680,18 +597,324 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   }
 }
 
-template <int AMODE, int BMODE, int SCHED, int EPI, int NB = 1>
-cudaError_t mx_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const MxParams& p, int grid, cudaStream_t s,
-                      const CUtensorMap* tmC = nullptr, const CUtensorMap* tmC2 = nullptr) {
-  auto kern = mx_gemm_kernel<AMODE, BMODE, SCHED, EPI, NB>;
-  constexpr int smem = mx_smem<SCHED, NB>();
+// One 128 x 128 weight-gradient tile (expert e, row tile m, column tile n) from TMEM to the output,
+// by the four epilogue warps (warp ew: rows 32 ew .. 32 ew + 31), each through its two 4 KB staging
+// buffers (128-byte swizzled, stored by TMA: whole lines). nkb == 0: the expert had no token rows; the
+// tile is zero (or left as it was, accumulating).
+template <int EPI>
+__device__ __forceinline__ void wgrad_tile_store(const MxParams& p, const CUtensorMap* tmC, const CUtensorMap* tmC2,
+                                                 uint32_t wbuf, uint32_t tbase, int e, int m, int n, int nkb, int ew,
+                                                 int lane) {
+  // Tile rows are packed dW13 rows (blocks of 64 gate then 64 up features: warps 0-1 write dWg rows,
+  // warps 2-3 dWu rows) or dWd rows; each warp writes its 32 rows as two 32 x 64 sub-tiles.
+  const bool empty = nkb == 0;
+  const CUtensorMap* tmo = tmC;
+  int orow0;
+  if (EPI == ME_DW13) {
+    if (ew >= 2) tmo = tmC2;
+    orow0 = e * p.f + m * 64 + (ew & 1) * 32;
+  } else {
+    orow0 = (e * p.m_tiles + m) * MBM + ew * 32;
+  }
+#pragma unroll 1
+  for (int c0 = 0; c0 < MBN; c0 += 64) {
+    const uint32_t buf = wbuf + ((c0 >> 6) & 1) * 4096;
+    float of[64];
+    if (!empty) {
+      uint32_t a[32], b[32];
+      tmem_ld32(tbase + c0, a);
+      tmem_ld32(tbase + c0 + 32, b);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        of[i] = __uint_as_float(a[i]);
+        of[32 + i] = __uint_as_float(b[i]);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 64; ++i) of[i] = 0.f;
+    }
+    if (p.accumulate) {
+      const bf16* base = (EPI == ME_DW13 && ew >= 2) ? (const bf16*)p.out2 : (const bf16*)p.out;
+      const bf16* old = base + (size_t)(orow0 + lane) * p.ldo + n * MBN + c0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float o8[8];
+        unpack8(*reinterpret_cast<const uint4*>(old + q * 8), o8);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) of[q * 8 + i] += o8[i];
+      }
+    }
+    // the store that last read this buffer (two sub-tiles ago) must have finished reading it
+    if (lane == 0) bulk_wait_read<1>();
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const uint4 v = pack8(of + q * 8);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf + lane * 128 + ((q ^ (lane & 7)) << 4)),
+                   "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                   : "memory");
+    }
+    fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d_hint(tmo, n * MBN + c0, orow0, buf, policy_evict_first());
+      bulk_commit();
+    }
+  }
+}
+
+// ------------------------------------------------------------------ weight gradients
+// dW[e] (rows: the 2f packed gate/up features or d; columns: d or f) = A^T B over the expert's
+// sorted token rows; A and B are token-axis operands [Rp, W] (MN-major, 32-row scale blocks; each
+// expert's rows start at a multiple of 128 and are zero past its tokens). A unit is (expert e,
+// 128-row output tile m): the CTA keeps the unit's A K groups resident in shared memory (when there
+// are at most kWgA * kWgKG of them) and streams the B groups of every column tile n through a ring,
+// so A is read once per unit instead of once per output tile; an expert with more K groups streams
+// A with B. A stage holds two 128-row K groups (eight MMAs per B stage): the MMA thread's per-stage
+// work (waits, fences, scale copies, commits) leaves the tensor pipe idle, since it queues little
+// more than one MMA ahead, and at four MMAs per stage that overhead doubled the stage time. The
+// CTAs of one expert start their column sweep at different tiles (row tile m at
+// m * n_tiles / m_tiles), spreading their B requests over the expert's tiles.
+constexpr int kWgKG = 2;            // 128-row K groups per stage (8 MMAs per B stage)
+constexpr int kWgA = 2, kWgB = 3;   // resident A stages (up to kWgA * kWgKG K groups), B ring stages
+constexpr int kWgStage = kWgKG * MBM * MBK;              // bytes of one operand stage
+constexpr int kWgAtoms = kWgKG * kScaleAtom;             // scale bytes of one operand stage
+constexpr int kWgOut = kEpi * 2 * 32 * 128;              // epilogue staging: two 32 x 64 bf16 sub-tiles per warp
+constexpr int kWgScaleRegion = ((kWgA + kWgB) * kWgAtoms + 1023) / 1024 * 1024;
+constexpr int kWgSmem = kWgScaleRegion + (kWgA + kWgB) * kWgStage + kWgOut + 1024 + 256 + kSegCache;
+static_assert(kWgSmem <= 227 * 1024, "shared memory per CTA");
+constexpr int kWgScaleColA = 2 * MBN, kWgScaleColB = kWgScaleColA + 4 * kWgKG * kWgA;   // TMEM scale columns
+
+template <int EPI>
+__global__ void __launch_bounds__(kMxThreads, 1)
+    mx_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2, MxParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* scales = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);   // A stages' atoms, then B's
+  uint8_t* sA = scales + kWgScaleRegion;            // kWgA stages (1024-aligned)
+  uint8_t* sB = sA + kWgA * kWgStage;               // kWgB stages
+  uint8_t* out_stage = sB + kWgB * kWgStage;        // epilogue staging (1024-aligned)
+  uint64_t* bars = (uint64_t*)(out_stage + kWgOut);
+  const uint32_t afull0 = smem_u32(bars), aempty0 = smem_u32(bars + kWgA);
+  const uint32_t bfull0 = smem_u32(bars + 2 * kWgA), bempty0 = smem_u32(bars + 2 * kWgA + kWgB);
+  const uint32_t tfull0 = smem_u32(bars + 2 * kWgA + 2 * kWgB), tempty0 = tfull0 + 16;
+  const uint32_t drain = tfull0 + 32;
+  volatile int* abort_flag = (volatile int*)(bars + 2 * kWgA + 2 * kWgB + 5);
+  uint32_t* tmem_slot = (uint32_t*)(bars + 2 * kWgA + 2 * kWgB + 6);
+  int* s_mt = (int*)(smem_raw + kWgSmem - kSegCache);   // [kMaxE + 2]: the 128-row block prefix
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i <= p.nseg; i += blockDim.x) s_mt[i] = p.mt_off[i];
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kWgA; ++i) {
+      mbar_init(afull0 + 8 * i, 1);
+      mbar_init(aempty0 + 8 * i, 1);
+    }
+    for (int i = 0; i < kWgB; ++i) {
+      mbar_init(bfull0 + 8 * i, 1);
+      mbar_init(bempty0 + 8 * i, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, kEpi * 32);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kMxMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_slot))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int units = p.nseg * p.m_tiles;
+  const int nt = p.n_tiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (one thread)
+    if (lane == 0) {
+      int ait = 0, bit = 0;
+      bool ok = true;
+      // K groups g0 .. g0 + ng - 1 of the stage (tile, 128-row scale atom each) into stage memory dst
+      auto load_stage = [&](uint32_t dst, uint32_t sc, const CUtensorMap* tm, const uint8_t* atoms, int w, int col,
+                            int row0, int g0, int ng, uint32_t fb) {
+        mbar_arrive_expect_tx(fb, ng * (MBM * MBK + kScaleAtom));
+        for (int g = 0; g < ng; ++g) {
+          const long kg = row0 / MBK + g0 + g;
+          tma_load_2d(dst + g * MBM * MBK, tm, col * MBM, row0 + (g0 + g) * MBK, fb);
+          bulk_load(sc + g * kScaleAtom, atoms + (kg * (w / MBM) + col) * kScaleAtom, kScaleAtom, fb);
+        }
+      };
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const int e = u / p.m_tiles, m = u % p.m_tiles;
+        const int row0 = s_mt[e] * MBK, nkb = s_mt[e + 1] - s_mt[e];
+        const int nst = (nkb + kWgKG - 1) / kWgKG;
+        const bool resident = nst <= kWgA;
+        const int n0 = m * nt / p.m_tiles;
+        for (int i = 0; i < nt && ok; ++i) {
+          const int n = (n0 + i) % nt;
+          for (int st = 0; st < nst; ++st) {
+            const int g0 = st * kWgKG, ng = min(kWgKG, nkb - g0);
+            if (!resident || i == 0) {
+              const int as = ait % kWgA;
+              if (!mbar_wait(aempty0 + 8 * as, ((ait / kWgA) & 1) ^ 1, abort_flag, p.status)) {
+                ok = false;
+                break;
+              }
+              load_stage(smem_u32(sA + as * kWgStage), smem_u32(scales + as * kWgAtoms), &tmA, p.As, p.a_w, m, row0,
+                         g0, ng, afull0 + 8 * as);
+              ++ait;
+            }
+            const int bs = bit % kWgB;
+            if (!mbar_wait(bempty0 + 8 * bs, ((bit / kWgB) & 1) ^ 1, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            load_stage(smem_u32(sB + bs * kWgStage), smem_u32(scales + (kWgA + bs) * kWgAtoms), &tmB, p.Bs, p.b_w, n,
+                       row0, g0, ng, bfull0 + 8 * bs);
+            ++bit;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMxMmaWarp) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      int ait = 0, bit = 0, tcount = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const int e = u / p.m_tiles;
+        const int nkb = s_mt[e + 1] - s_mt[e];
+        const int nst = (nkb + kWgKG - 1) / kWgKG;
+        const bool resident = nst <= kWgA;
+        const int ait0 = ait;
+        for (int i = 0; i < nt && ok; ++i, ++tcount) {
+          const int acc = tcount & 1;
+          if (!mbar_wait(tempty0 + 8 * acc, ((tcount >> 1) & 1) ^ 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t dcol = tmem_base + acc * MBN;
+          for (int st = 0; st < nst; ++st) {
+            const int ng = min(kWgKG, nkb - st * kWgKG);
+            int as;
+            if (!resident || i == 0) {
+              as = ait % kWgA;
+              if (!mbar_wait(afull0 + 8 * as, (ait / kWgA) & 1, abort_flag, p.status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              // the stage's A scales stay in these TMEM columns for every column tile of the unit
+              for (int g = 0; g < ng; ++g)
+                tmem_cp_scales(tmem_base + kWgScaleColA + 4 * (as * kWgKG + g),
+                               desc_scale_atom(smem_u32(scales + as * kWgAtoms + g * kScaleAtom)));
+              ++ait;
+            } else {
+              as = (ait0 + st) % kWgA;
+            }
+            const int bs = bit % kWgB;
+            if (!mbar_wait(bfull0 + 8 * bs, (bit / kWgB) & 1, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            for (int g = 0; g < ng; ++g)
+              tmem_cp_scales(tmem_base + kWgScaleColB + 4 * (bs * kWgKG + g),
+                             desc_scale_atom(smem_u32(scales + (kWgA + bs) * kWgAtoms + g * kScaleAtom)));
+            const uint32_t sa = smem_u32(sA + as * kWgStage), sb = smem_u32(sB + bs * kWgStage);
+            for (int g = 0; g < ng; ++g) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_mx(dcol, desc_mnmajor(sa + g * MBM * MBK + k * 4096), desc_mnmajor(sb + g * MBN * MBK + k * 4096),
+                       idesc_mx(1, 1, k), tmem_base + kWgScaleColA + 4 * (as * kWgKG + g),
+                       tmem_base + kWgScaleColB + 4 * (bs * kWgKG + g), (st > 0 || g > 0 || k > 0) ? 1u : 0u);
+            }
+            mma_commit(bempty0 + 8 * bs);
+            ++bit;
+            // an A stage is released after its last use: the unit's last column tile (resident) or this one
+            if (!resident || i == nt - 1) mma_commit(aempty0 + 8 * as);
+          }
+          if (!ok) break;
+          mma_commit(tfull0 + 8 * acc);
+        }
+      }
+      mma_commit(drain);
+      const uint64_t t0 = global_ns();
+      while (!mbar_try_wait(drain, 0)) {
+        if (global_ns() - t0 > kWaitLimitNs) {
+          set_error(p.status, MOE_ERR_TIMEOUT);
+          break;
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp & 3;   // TMEM lane quadrant of this warp
+    const uint32_t wbuf = smem_u32(out_stage) + ew * 2 * 4096;
+    int tcount = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const int e = u / p.m_tiles, m = u % p.m_tiles;
+      const int nkb = s_mt[e + 1] - s_mt[e];
+      const int n0 = m * nt / p.m_tiles;
+      for (int i = 0; i < nt; ++i, ++tcount) {
+        const int n = (n0 + i) % nt;
+        const int acc = tcount & 1;
+        if (!mbar_wait(tfull0 + 8 * acc, (tcount >> 1) & 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        wgrad_tile_store<EPI>(p, &tmC, &tmC2, wbuf, tmem_base + acc * MBN + ((uint32_t)(ew * 32) << 16), e, m, n,
+                              nkb, ew, lane);
+        tc_fence_before();
+        mbar_arrive(tempty0 + 8 * acc);
+      }
+    }
+    // the stores must have read their staging before the CTA exits
+    if (lane == 0) bulk_wait<0>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMxMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base) : "memory");
+  }
+}
+
+template <int EPI>
+cudaError_t wg_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const MxParams& p, int grid, cudaStream_t s,
+                      const CUtensorMap& tmC, const CUtensorMap& tmC2) {
+  auto kern = mx_wgrad_kernel<EPI>;
+  static bool attr = false;
+  if (!attr) {
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kWgSmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  kern<<<grid, kMxThreads, kWgSmem, s>>>(tmA, tmB, tmC, tmC2, p);
+  return cudaGetLastError();
+}
+
+template <int BMODE, int EPI, int NB>
+cudaError_t mx_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const MxParams& p, int grid, cudaStream_t s) {
+  auto kern = mx_gemm_kernel<BMODE, EPI, NB>;
+  constexpr int smem = mx_smem<NB>();
   static bool attr = false;
   if (!attr) {
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  kern<<<grid, kMxThreads, smem, s>>>(tmA, tmB, tmC ? *tmC : tmA, tmC2 ? *tmC2 : tmA, p);
+  kern<<<grid, kMxThreads, smem, s>>>(tmA, tmB, p);
   return cudaGetLastError();
 }
 
@@ -829,7 +1052,7 @@ cudaError_t launch_mx_gateup(const Layer& L, const Bufs& B, cudaStream_t s) {
   p.os = B.hs;
   p.uv = (bf16*)B.uv;
   p.ld_uv = 2 * L.f;
-  return mx_launch<MA_TMA_K, MB_TMA_K, MS_SEG_M, ME_SWIGLU_Q, 2>(ta, L.tm_W13q, p, L.num_sms, s);
+  return mx_launch<MB_TMA_K, ME_SWIGLU_Q, 2>(ta, L.tm_W13q, p, L.num_sms, s);
 }
 
 cudaError_t launch_mx_down(const Layer& L, const Bufs& B, cudaStream_t s) {
@@ -844,7 +1067,7 @@ cudaError_t launch_mx_down(const Layer& L, const Bufs& B, cudaStream_t s) {
   p.out = B.o;
   p.ldo = L.d;
   p.row_gate = B.row_gate;
-  return mx_launch<MA_TMA_K, MB_TMA_K, MS_SEG_M, ME_GATE, 2>(th, L.tm_Wdq, p, L.num_sms, s);
+  return mx_launch<MB_TMA_K, ME_GATE, 2>(th, L.tm_Wdq, p, L.num_sms, s);
 }
 
 cudaError_t launch_mx_bwd_dh(const Layer& L, const Bufs& B, cudaStream_t s) {
@@ -866,7 +1089,9 @@ cudaError_t launch_mx_bwd_dh(const Layer& L, const Bufs& B, cudaStream_t s) {
   p.ld_uv = 2 * L.f;
   p.dg_part = B.dg_part;
   p.dg_slots = L.f / 64;
-  return mx_launch<MA_TMA_K, MB_TMA_MN, MS_SEG_M, ME_DH_Q, 2>(ta, L.tm_Wdc, p, L.num_sms, s);
+  // one column tile per CTA: its accumulators double-buffer, so the SwiGLU-backward epilogue of a tile
+  // overlaps the next tile's MMAs (measured faster here; the other products keep two column tiles)
+  return mx_launch<MB_TMA_MN, ME_DH_Q, 1>(ta, L.tm_Wdc, p, L.num_sms, s);
 }
 
 cudaError_t launch_mx_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s) {
@@ -881,7 +1106,7 @@ cudaError_t launch_mx_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s) {
   p.b_rows_per_seg = 2 * L.f;
   p.out = B.dx_rows;
   p.ldo = L.d;
-  return mx_launch<MA_TMA_K, MB_TMA_MN, MS_SEG_M, ME_STORE, 2>(ta, L.tm_W13c, p, L.num_sms, s);
+  return mx_launch<MB_TMA_MN, ME_STORE, 2>(ta, L.tm_W13c, p, L.num_sms, s);
 }
 
 cudaError_t launch_mx_bwd_dw13(const Layer& L, const Bufs& B, void* dWg, void* dWu, bool acc, cudaStream_t s) {
@@ -903,7 +1128,7 @@ cudaError_t launch_mx_bwd_dw13(const Layer& L, const Bufs& B, void* dWg, void* d
   CUtensorMap tg, tu;
   if (!make_tmap(&tg, dWg, L.d, nseg * L.f, 64, 32) || !make_tmap(&tu, dWu, L.d, nseg * L.f, 64, 32))
     return cudaErrorInvalidValue;
-  return mx_launch<MA_TMA_MN, MB_TMA_MN, MS_SEG_K, ME_DW13>(ta, tb, p, L.num_sms, s, &tg, &tu);
+  return wg_launch<ME_DW13>(ta, tb, p, L.num_sms, s, tg, tu);
 }
 
 cudaError_t launch_mx_bwd_dwd(const Layer& L, const Bufs& B, void* dWd, bool acc, cudaStream_t s) {
@@ -922,7 +1147,7 @@ cudaError_t launch_mx_bwd_dwd(const Layer& L, const Bufs& B, void* dWd, bool acc
   p.accumulate = acc ? 1 : 0;
   CUtensorMap td;
   if (!make_tmap(&td, dWd, L.f, (uint64_t)(L.E + L.S) * L.d, 64, 32)) return cudaErrorInvalidValue;
-  return mx_launch<MA_TMA_MN, MB_TMA_MN, MS_SEG_K, ME_DWD>(ta, tb, p, L.num_sms, s, &td);
+  return wg_launch<ME_DWD>(ta, tb, p, L.num_sms, s, td, td);
 }
 
 }  // namespace moe
