@@ -191,19 +191,20 @@ __global__ void __launch_bounds__(256) mx_quant_sorted_kernel(const bf16* __rest
 
 enum { CSRC_PLAIN = 0, CSRC_W13 = 1, CSRC_SEG_GATHER = 2, CSRC_SEG_DIRECT = 3 };
 
-// Along rows, in blocks of 32 rows: one thread per column, one block of 256
-// columns x 32 rows per CTA. Segment modes write each expert's sorted rows at
-// mt_off[e] * 128 (segments padded to 128 rows with zero codes).
+// Along rows, in blocks of 32 rows: one warp per 32-row block and 128 columns (4 columns per lane,
+// 8-byte loads of each row and one 4-byte store of its codes), 4 warps per CTA. Segment modes write
+// each expert's sorted rows at mt_off[e] * 128 (segments padded to 128 rows with zero codes).
 template <int SRC>
-__global__ void __launch_bounds__(256) mx_quant_cols_kernel(const bf16* __restrict__ src, const bf16* __restrict__ src2,
+__global__ void __launch_bounds__(128) mx_quant_cols_kernel(const bf16* __restrict__ src, const bf16* __restrict__ src2,
                                                             const int* __restrict__ row_token,
                                                             const int* __restrict__ off,
                                                             const int* __restrict__ mt_off, int nseg, int W, int f,
                                                             int G, uint8_t* __restrict__ q, uint8_t* __restrict__ s,
                                                             const int* __restrict__ out_base) {
-  const int c = blockIdx.x * 256 + threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int c = (blockIdx.x * 4 + (threadIdx.x >> 5)) * 128 + lane * 4;   // this lane's 4 columns
   long rb = blockIdx.y;                    // 32-row block (of the chunk's padded segment layout)
-  if (c >= W) return;
+  if (c >= W) return;                      // W is a multiple of 128: whole warps
   long seg_first = 0, seg_len = 0, seg_src0 = 0, out_shift = 0;
   if (SRC == CSRC_SEG_GATHER || SRC == CSRC_SEG_DIRECT) {
     const int pr = (int)(rb * 32);
@@ -219,29 +220,55 @@ __global__ void __launch_bounds__(256) mx_quant_cols_kernel(const bf16* __restri
     // out_base (optional): segment lo's rows go to out_base[lo] onwards instead of seg_first
     if (out_base) out_shift = (long)out_base[lo] - seg_first;
   }
-  float v[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const long orow = rb * 32 + i;
-    const bf16* row = nullptr;
-    if (SRC == CSRC_PLAIN) row = src + orow * W;
-    if (SRC == CSRC_W13) row = w13_src(src, src2, orow, f, G, W);
+  // source row of row `lane` of the block (null: a zero padding row), then each row's 4 values
+  const bf16* my_row = nullptr;
+  {
+    const long orow = rb * 32 + lane;
+    if (SRC == CSRC_PLAIN) my_row = src + orow * W;
+    if (SRC == CSRC_W13) my_row = w13_src(src, src2, orow, f, G, W);
     if (SRC == CSRC_SEG_GATHER || SRC == CSRC_SEG_DIRECT) {
       const long local = orow - seg_first;
       if (local < seg_len) {
         const long p = seg_src0 + local;
-        row = src + (SRC == CSRC_SEG_GATHER ? (long)row_token[p] : p) * W;
+        my_row = src + (SRC == CSRC_SEG_GATHER ? (long)row_token[p] : p) * W;
       }
     }
-    v[i] = row ? __bfloat162float(row[c]) : 0.f;
   }
-  uint4 lo, hi;
-  const uint8_t sc = quant32(v, lo, hi);
-  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  uint2 raw[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const bf16* r = reinterpret_cast<const bf16*>(__shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(my_row), i));
+    raw[i] = r ? *reinterpret_cast<const uint2*>(r + c) : make_uint2(0u, 0u);
+  }
+  // per column: amax over the 32 rows, the block exponent, then the codes (as quant32 does)
+  float amax[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    amax[0] = fmaxf(amax[0], fabsf(__uint_as_float(raw[i].x << 16)));
+    amax[1] = fmaxf(amax[1], fabsf(__uint_as_float(raw[i].x & 0xffff0000u)));
+    amax[2] = fmaxf(amax[2], fabsf(__uint_as_float(raw[i].y << 16)));
+    amax[3] = fmaxf(amax[3], fabsf(__uint_as_float(raw[i].y & 0xffff0000u)));
+  }
+  int X[4];
+  float inv[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    X[j] = mx_exponent(amax[j]);
+    inv[j] = __uint_as_float((uint32_t)(127 - X[j]) << 23);
+  }
   rb += out_shift / 32;                    // segment bases are multiples of 128 rows
 #pragma unroll
-  for (int i = 0; i < 32; ++i) q[(rb * 32 + i) * W + c] = (uint8_t)(w[i >> 2] >> (8 * (i & 3)));
-  s[atom_mn(rb, c, W)] = sc;
+  for (int i = 0; i < 32; ++i) {
+    const uint32_t a = __nv_cvt_float2_to_fp8x2(make_float2(__uint_as_float(raw[i].x << 16) * inv[0],
+                                                             __uint_as_float(raw[i].x & 0xffff0000u) * inv[1]),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    const uint32_t b = __nv_cvt_float2_to_fp8x2(make_float2(__uint_as_float(raw[i].y << 16) * inv[2],
+                                                             __uint_as_float(raw[i].y & 0xffff0000u) * inv[3]),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    *reinterpret_cast<uint32_t*>(q + (rb * 32 + i) * W + c) = a | (b << 16);
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) s[atom_mn(rb, c + j, W)] = (uint8_t)(X[j] + 127);
 }
 
 // ---------------------------------------------------------------- GEMM
@@ -964,9 +991,9 @@ cudaError_t mx_pack_weights(Layer& L, const void* Wg, const void* Wu, const void
                                                                      L.W13s);
   mx_quant_rows_kernel<SRC_PLAIN><<<blocks_for(rd, 8), 256, 0, s>>>(dw, nullptr, rd, L.f, L.f, 0, L.Wdq,
                                                                      L.Wds);
-  mx_quant_cols_kernel<CSRC_W13><<<dim3(blocks_for(d, 256), (unsigned)(r13 / 32)), 256, 0, s>>>(
+  mx_quant_cols_kernel<CSRC_W13><<<dim3(blocks_for(d, 512), (unsigned)(r13 / 32)), 128, 0, s>>>(
       g, u, nullptr, nullptr, nullptr, 0, L.d, L.f, kGateMx, L.W13c, L.W13cs, nullptr);
-  mx_quant_cols_kernel<CSRC_PLAIN><<<dim3(blocks_for(f, 256), (unsigned)(rd / 32)), 256, 0, s>>>(
+  mx_quant_cols_kernel<CSRC_PLAIN><<<dim3(blocks_for(f, 512), (unsigned)(rd / 32)), 128, 0, s>>>(
       dw, nullptr, nullptr, nullptr, nullptr, 0, L.f, L.f, 0, L.Wdc, L.Wdcs, nullptr);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -990,12 +1017,12 @@ cudaError_t launch_mx_quant_sorted(const Layer& L, const Bufs& B, const void* sr
 // out_base (nullable, device [nseg]): row where each segment's rows start in q (default mt_off[e] * 128).
 cudaError_t launch_mx_quant_tokens(const Layer& L, const Bufs& B, const void* src, bool gather, int W, uint8_t* q,
                                    uint8_t* s, cudaStream_t st, const int* out_base) {
-  const dim3 grid(blocks_for(W, 256), (unsigned)(B.Rp_max / 32));
+  const dim3 grid(blocks_for(W, 512), (unsigned)(B.Rp_max / 32));
   if (gather)
-    mx_quant_cols_kernel<CSRC_SEG_GATHER><<<grid, 256, 0, st>>>((const bf16*)src, nullptr, B.row_token, B.off,
+    mx_quant_cols_kernel<CSRC_SEG_GATHER><<<grid, 128, 0, st>>>((const bf16*)src, nullptr, B.row_token, B.off,
                                                                 B.mt_off, L.E + L.S, W, 0, 0, q, s, out_base);
   else
-    mx_quant_cols_kernel<CSRC_SEG_DIRECT><<<grid, 256, 0, st>>>((const bf16*)src, nullptr, B.row_token, B.off,
+    mx_quant_cols_kernel<CSRC_SEG_DIRECT><<<grid, 128, 0, st>>>((const bf16*)src, nullptr, B.row_token, B.off,
                                                                 B.mt_off, L.E + L.S, W, 0, 0, q, s, out_base);
   return cudaGetLastError();
 }
