@@ -50,6 +50,7 @@ Sizes sizes_for(const Layer& L, int T) {
   z.fwd_ws = z.route + z.fwd_scratch;
   z.bwd_ws = al(eb * R * 2 * L.f) + al(eb * R * L.f) + al(4 * A * (L.f / 64)) + al(eb * R * L.d) +
              al(4 * T * (size_t)L.E) + al(4 * A) + al(4 * (size_t)kRouterSplit * L.E * L.d);
+  if (L.prec == MOE_MXFP8) z.bwd_ws -= al(eb * R * 2 * L.f) + al(eb * R * L.f);   // no bf16 du/dv, g * h
   z.packed = al(eb * nseg * 2 * L.f * L.d) + al(eb * nseg * L.d * L.f) + al(eb * L.E * L.d) + al(4 * L.E);
   if (L.prec == MOE_MXFP8) {
     const size_t d = L.d, f = L.f, Rp = rp_max(L, T);
@@ -116,8 +117,10 @@ Bufs carve(const Layer& L, int T, void* ws, const void* ctx, void* bws) {
   }
   if (bws) {
     char* b = (char*)bws;
-    B.dudv = b; b += al(eb * B.R * 2 * L.f);
-    B.hg = b; b += al(eb * B.R * L.f);
+    if (!mx) {   // (MXFP8 quantises du/dv and g * h in the dY.Wd epilogue)
+      B.dudv = b; b += al(eb * B.R * 2 * L.f);
+      B.hg = b; b += al(eb * B.R * L.f);
+    }
     B.dg_part = (float*)b; b += al(4 * (size_t)B.A * (L.f / 64));
     B.dx_rows = b; b += al(eb * B.R * L.d);
     B.dl = (float*)b; b += al(4 * (size_t)B.T * L.E);
@@ -267,9 +270,13 @@ moe_status backward_body(moe_handle_s* h, const void* x, const void* dy, int T, 
                          const MxDefer* defer = nullptr) {
   const Layer& L = h->L;
   Bufs B = carve(L, T, nullptr, ctx, workspace);
+  // MXFP8: the token-axis operands of the weight gradients go into this call's buffers, or (chunked
+  // step) into the step's combined buffers, whose single weight-gradient pass runs after the last chunk
+  const Bufs& O = defer ? defer->comb : B;
+  const int* base = defer ? defer->base : nullptr;
   if (h->mx) {
     CK(run(h, s, G_MX_QUANT, 1, [&] { return launch_mx_quant_sorted(L, B, dy, L.d, B.dyq, B.dys, s); }));
-    CK(run(h, s, G_BWD_DH, 1, [&] { return launch_mx_bwd_dh(L, B, s); }));
+    CK(run(h, s, G_BWD_DH, 1, [&] { return launch_mx_bwd_dh(L, B, O, base, s); }));
     CK(run(h, s, G_BWD_DX, 1, [&] { return launch_mx_bwd_dx(L, B, s); }));
   } else if (h->tc) {
     CK(run(h, s, G_BWD_DH, 1, [&] { return launch_tc_bwd_dh(L, B, dy, s); }));
@@ -303,15 +310,10 @@ moe_status backward_body(moe_handle_s* h, const void* x, const void* dy, int T, 
   CK(run(h, s, G_ROUTER_BWD, router_kernels, [&] { return launch_router_bwd(L, B, x, dWr, acc, s); }));
   CK(run(h, s, G_DX_GATHER, 1, [&] { return launch_dx_gather(L, B, dx, s); }));
   if (h->mx) {
-    // token-axis operands of the weight gradients: into this call's buffers, or (chunked step)
-    // into the step's combined buffers, whose single weight-gradient pass runs after the last chunk
-    const Bufs& O = defer ? defer->comb : B;
-    const int* base = defer ? defer->base : nullptr;
-    CK(run(h, s, G_MX_QUANT, 4, [&] {
-      cudaError_t e = launch_mx_quant_tokens(L, B, B.dudv, false, 2 * L.f, O.dudv_t, O.dudv_ts, s, base);
-      if (e == cudaSuccess) e = launch_mx_quant_tokens(L, B, x, true, L.d, O.x_t, O.x_ts, s, base);
-      if (e == cudaSuccess) e = launch_mx_quant_tokens(L, B, dy, true, L.d, O.dy_t, O.dy_ts, s, base);
-      if (e == cudaSuccess) e = launch_mx_quant_tokens(L, B, B.hg, false, L.f, O.hg_t, O.hg_ts, s, base);
+    // x and dy along the token axis (du/dv and g * h came from the dY.Wd epilogue)
+    CK(run(h, s, G_MX_QUANT, 2, [&] {
+      cudaError_t e = launch_mx_quant_tokens(L, B, x, L.d, O.x_t, O.x_ts, s, base);
+      if (e == cudaSuccess) e = launch_mx_quant_tokens(L, B, dy, L.d, O.dy_t, O.dy_ts, s, base);
       return e;
     }));
     if (!defer) {

@@ -157,13 +157,15 @@ size_t mx_packed_bytes(const Layer& L);
 cudaError_t mx_pack_weights(Layer& L, const void* Wg, const void* Wu, const void* Wd, void* base, cudaStream_t s);
 cudaError_t launch_mx_quant_sorted(const Layer& L, const Bufs& B, const void* src, int K, uint8_t* q, uint8_t* s,
                                    cudaStream_t st);
-cudaError_t launch_mx_quant_tokens(const Layer& L, const Bufs& B, const void* src, bool gather, int W, uint8_t* q,
-                                   uint8_t* s, cudaStream_t st, const int* out_base = nullptr);
+cudaError_t launch_mx_quant_tokens(const Layer& L, const Bufs& B, const void* src, int W, uint8_t* q, uint8_t* s,
+                                   cudaStream_t st, const int* out_base = nullptr);
 cudaError_t launch_mx_chunk_layout(const Layer& L, const int* chunk_mt, int n, int* comb_base, int* comb_mt,
                                    cudaStream_t st);
 cudaError_t launch_mx_gateup(const Layer& L, const Bufs& B, cudaStream_t s);
 cudaError_t launch_mx_down(const Layer& L, const Bufs& B, cudaStream_t s);
-cudaError_t launch_mx_bwd_dh(const Layer& L, const Bufs& B, cudaStream_t s);
+// dY.Wd with the SwiGLU backward: du/dv quantised along 2f into B (dx's operand) and, with g * h,
+// along the token axis into O's token-axis buffers (rows from tok_base[e], or mt_off[e] * 128 when null)
+cudaError_t launch_mx_bwd_dh(const Layer& L, const Bufs& B, const Bufs& O, const int* tok_base, cudaStream_t s);
 cudaError_t launch_mx_bwd_dx(const Layer& L, const Bufs& B, cudaStream_t s);
 cudaError_t launch_mx_bwd_dw13(const Layer& L, const Bufs& B, void* dWg, void* dWu, bool acc, cudaStream_t s);
 cudaError_t launch_mx_bwd_dwd(const Layer& L, const Bufs& B, void* dWd, bool acc, cudaStream_t s);

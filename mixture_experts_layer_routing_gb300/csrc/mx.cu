@@ -93,6 +93,9 @@ struct MxParams {
   void* out2;
   uint8_t* oq;            // quantised output codes (ME_SWIGLU_Q: h, ME_DH_Q: dudv)
   uint8_t* os;            // and their scales
+  uint8_t *tq, *ts;       // ME_DH_Q: du/dv along the token axis (token-axis operand of dW13), codes and scales
+  uint8_t *tq2, *ts2;     // ME_DH_Q: g * h along the token axis (operand of dWd)
+  const int* tok_base;    // ME_DH_Q (nullable): row where each segment's token-axis rows start (default mt_off * 128)
   const float* row_gate;
   bf16* uv;
   int ld_uv;
@@ -189,7 +192,7 @@ __global__ void __launch_bounds__(256) mx_quant_sorted_kernel(const bf16* __rest
   }
 }
 
-enum { CSRC_PLAIN = 0, CSRC_W13 = 1, CSRC_SEG_GATHER = 2, CSRC_SEG_DIRECT = 3 };
+enum { CSRC_PLAIN = 0, CSRC_W13 = 1, CSRC_SEG_GATHER = 2 };
 
 // Along rows, in blocks of 32 rows: one warp per 32-row block and 128 columns (4 columns per lane,
 // 8-byte loads of each row and one 4-byte store of its codes), 4 warps per CTA. Segment modes write
@@ -206,7 +209,7 @@ __global__ void __launch_bounds__(128) mx_quant_cols_kernel(const bf16* __restri
   long rb = blockIdx.y;                    // 32-row block (of the chunk's padded segment layout)
   if (c >= W) return;                      // W is a multiple of 128: whole warps
   long seg_first = 0, seg_len = 0, seg_src0 = 0, out_shift = 0;
-  if (SRC == CSRC_SEG_GATHER || SRC == CSRC_SEG_DIRECT) {
+  if (SRC == CSRC_SEG_GATHER) {
     const int pr = (int)(rb * 32);
     if (pr >= mt_off[nseg] * 128) return;
     int lo = 0, hi = nseg;
@@ -226,11 +229,11 @@ __global__ void __launch_bounds__(128) mx_quant_cols_kernel(const bf16* __restri
     const long orow = rb * 32 + lane;
     if (SRC == CSRC_PLAIN) my_row = src + orow * W;
     if (SRC == CSRC_W13) my_row = w13_src(src, src2, orow, f, G, W);
-    if (SRC == CSRC_SEG_GATHER || SRC == CSRC_SEG_DIRECT) {
+    if (SRC == CSRC_SEG_GATHER) {
       const long local = orow - seg_first;
       if (local < seg_len) {
         const long p = seg_src0 + local;
-        my_row = src + (SRC == CSRC_SEG_GATHER ? (long)row_token[p] : p) * W;
+        my_row = src + (long)row_token[p] * W;
       }
     }
   }
@@ -269,6 +272,32 @@ __global__ void __launch_bounds__(128) mx_quant_cols_kernel(const bf16* __restri
   }
 #pragma unroll
   for (int j = 0; j < 4; ++j) s[atom_mn(rb, c + j, W)] = (uint8_t)(X[j] + 127);
+}
+
+// Token-axis quantisation inside an epilogue: each lane holds 32 values (columns col0 .. col0 + 31) of
+// one row, and the warp's 32 lanes are the 32 consecutive rows of one 32-row block (lanes past the
+// segment hold zeros). Column j's block exponent comes from the amax over the lanes (as quant32
+// does for one block); the lane's 32 codes go to its row, column col0 + lane's scale to its atom.
+__device__ __forceinline__ void quant_tokens32(const float* v, long row, int col0, long W, int lane, uint8_t* q,
+                                               uint8_t* s) {
+  uint32_t w[8];
+  int mine = 0;
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    const float a0 = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v[j]))));
+    const float a1 = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v[j + 1]))));
+    const int X0 = mx_exponent(a0), X1 = mx_exponent(a1);
+    const float i0 = __uint_as_float((uint32_t)(127 - X0) << 23), i1 = __uint_as_float((uint32_t)(127 - X1) << 23);
+    const uint32_t c = __nv_cvt_float2_to_fp8x2(make_float2(v[j] * i0, v[j + 1] * i1), __NV_SATFINITE, __NV_E4M3);
+    if (j & 2) w[j >> 2] |= c << 16;
+    else w[j >> 2] = c;
+    if (lane == j) mine = X0 + 127;
+    if (lane == j + 1) mine = X1 + 127;
+  }
+  uint4* dst = reinterpret_cast<uint4*>(q + row * W + col0);
+  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  s[atom_mn(row >> 5, col0 + lane, W)] = (uint8_t)mine;
 }
 
 // ---------------------------------------------------------------- GEMM
@@ -556,19 +585,24 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           }
         }
       } else if (EPI == ME_DH_Q) {
-        // r for features n*128 .. n*128+127 = gate/up blocks 2n, 2n+1 (64 features each)
+        // r for features n*128 .. n*128+127 = gate/up blocks 2n, 2n+1 (64 features each). du and dv
+        // go out quantised along 2f (dx's A operand) and, with g * h, along the token axis (the
+        // weight gradients' operands): this warp's 32 rows are one 32-row block of the expert's
+        // token-axis rows, which start at tok_base[e] (or mt_off[e] * 128).
         const float g = valid ? p.row_gate[row] : 0.f;
+        const long trow = (p.tok_base ? (long)p.tok_base[t.e] : (long)s_mt[t.e] * MBM) + (long)t.m * MBM + r;
         float dgp = 0.f;
 #pragma unroll 1
         for (int c0 = 0; c0 < 128; c0 += 32) {
           uint32_t a[32];
           tmem_ld32(tbase + c0, a);
           tmem_ld_wait();
+          const int blk = 2 * t.n + (c0 >> 6), within = c0 & 63;
+          const int ucol = blk * 128 + within;          // packed column of u; v at + 64
+          float du[32], dv[32], hg[32];
           if (valid) {
-            const int blk = 2 * t.n + (c0 >> 6), within = c0 & 63;
-            const size_t ucol = (size_t)blk * 128 + within;          // packed column of u; v at + 64
             const bf16* urow = p.uv + (size_t)row * p.ld_uv;
-            float uf[32], vf[32], du[32], dv[32], hg[32];
+            float uf[32], vf[32];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               unpack8(*reinterpret_cast<const uint4*>(urow + ucol + q * 8), uf + q * 8);
@@ -586,14 +620,6 @@ __global__ void __launch_bounds__(kMxThreads, 1)
               dv[i] = dh * sl;
               hg[i] = g * hv;
             }
-            bf16* drow = (bf16*)p.out + (size_t)row * p.ld_uv;
-            bf16* hgrow = (bf16*)p.out2 + (size_t)row * p.f + t.n * 128 + c0;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              *reinterpret_cast<uint4*>(drow + ucol + q * 8) = pack8(du + q * 8);
-              *reinterpret_cast<uint4*>(drow + ucol + 64 + q * 8) = pack8(dv + q * 8);
-              *reinterpret_cast<uint4*>(hgrow + q * 8) = pack8(hg + q * 8);
-            }
             uint4 lo, hi;
             uint8_t sc = quant32(du, lo, hi);
             uint8_t* qrow = p.oq + (size_t)row * p.ld_uv;
@@ -608,7 +634,13 @@ __global__ void __launch_bounds__(kMxThreads, 1)
               if (row < p.A_rows) p.dg_part[(size_t)row * p.dg_slots + (t.n * 128 + c0 - 32) / 64] = dgp;
               dgp = 0.f;
             }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) du[i] = dv[i] = hg[i] = 0.f;
           }
+          quant_tokens32(du, trow, ucol, 2 * (long)p.f, lane, p.tq, p.ts);
+          quant_tokens32(dv, trow, ucol + 64, 2 * (long)p.f, lane, p.tq, p.ts);
+          quant_tokens32(hg, trow, t.n * 128 + c0, p.f, lane, p.tq2, p.ts2);
         }
       }
       }   // column tiles of the unit
@@ -1013,17 +1045,14 @@ cudaError_t launch_mx_quant_sorted(const Layer& L, const Bufs& B, const void* sr
   return cudaGetLastError();
 }
 
-// Token-axis operands of the weight gradients: [Rp, W] codes, [Rp/32, W] scales, Rp = mt_off[nseg] * 128.
+// Token rows of src [T, W] (x or dY) along the token axis, the operands of the weight gradients: [Rp, W]
+// codes (each segment's rows in sorted order, zero-padded to 128) and atom_mn scales, Rp = mt_off[nseg] * 128.
 // out_base (nullable, device [nseg]): row where each segment's rows start in q (default mt_off[e] * 128).
-cudaError_t launch_mx_quant_tokens(const Layer& L, const Bufs& B, const void* src, bool gather, int W, uint8_t* q,
-                                   uint8_t* s, cudaStream_t st, const int* out_base) {
+cudaError_t launch_mx_quant_tokens(const Layer& L, const Bufs& B, const void* src, int W, uint8_t* q, uint8_t* s,
+                                   cudaStream_t st, const int* out_base) {
   const dim3 grid(blocks_for(W, 512), (unsigned)(B.Rp_max / 32));
-  if (gather)
-    mx_quant_cols_kernel<CSRC_SEG_GATHER><<<grid, 128, 0, st>>>((const bf16*)src, nullptr, B.row_token, B.off,
-                                                                B.mt_off, L.E + L.S, W, 0, 0, q, s, out_base);
-  else
-    mx_quant_cols_kernel<CSRC_SEG_DIRECT><<<grid, 128, 0, st>>>((const bf16*)src, nullptr, B.row_token, B.off,
-                                                                B.mt_off, L.E + L.S, W, 0, 0, q, s, out_base);
+  mx_quant_cols_kernel<CSRC_SEG_GATHER><<<grid, 128, 0, st>>>((const bf16*)src, nullptr, B.row_token, B.off, B.mt_off,
+                                                              L.E + L.S, W, 0, 0, q, s, out_base);
   return cudaGetLastError();
 }
 
@@ -1097,7 +1126,7 @@ cudaError_t launch_mx_down(const Layer& L, const Bufs& B, cudaStream_t s) {
   return mx_launch<MB_TMA_K, ME_GATE, 2>(th, L.tm_Wdq, p, L.num_sms, s);
 }
 
-cudaError_t launch_mx_bwd_dh(const Layer& L, const Bufs& B, cudaStream_t s) {
+cudaError_t launch_mx_bwd_dh(const Layer& L, const Bufs& B, const Bufs& O, const int* tok_base, cudaStream_t s) {
   CUtensorMap ta;
   if (!make_tmap(&ta, B.dyq, L.d, B.R, MBK, MBM, 1)) return cudaErrorInvalidValue;
   MxParams p = mx_base(L, B);
@@ -1107,10 +1136,13 @@ cudaError_t launch_mx_bwd_dh(const Layer& L, const Bufs& B, cudaStream_t s) {
   p.K = L.d;
   p.n_tiles = L.f / MBN;
   p.b_rows_per_seg = L.d;
-  p.out = B.dudv;
-  p.out2 = B.hg;
   p.oq = B.dudvq;
   p.os = B.dudvs;
+  p.tq = O.dudv_t;
+  p.ts = O.dudv_ts;
+  p.tq2 = O.hg_t;
+  p.ts2 = O.hg_ts;
+  p.tok_base = tok_base;
   p.row_gate = B.row_gate;
   p.uv = (bf16*)B.uv;
   p.ld_uv = 2 * L.f;
