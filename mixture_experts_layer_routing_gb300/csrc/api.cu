@@ -398,6 +398,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
   moe_handle_s* h = new (std::nothrow) moe_handle_s();
   if (!h) return MOE_ERR_INVALID_ARG;
   h->cfg = c;
+  h->decode_gemm_from = c.prec == MOE_MXFP8 ? kDecodeGemmFromMx : kDecodeGemmFrom;
   Layer& L = h->L;
   L.d = c.d; L.E = c.E; L.S = c.n_shared; L.f = c.f; L.k = c.k;
   L.router = c.router; L.renorm = c.renorm ? 1 : 0; L.prec = c.prec; L.scale = c.route_scale;
@@ -711,7 +712,6 @@ moe_status moe_decode(moe_handle h, const void* x, int B, void* y, void* workspa
   if (B >= h->decode_gemm_from && (h->tc || h->mx)) return forward_body(h, x, B, y, nullptr, workspace, s);
   CK(run(h, s, G_DECODE_ROUTE, 1, [&] { return launch_decode_route(L, x, B, workspace, s); }));
   if (L.prec == MOE_MXFP8) {
-    CK(run(h, s, G_MX_QUANT, 1, [&] { return launch_decode_quant_x_mx(L, x, B, workspace, s); }));
     CK(run(h, s, G_DECODE_GATEUP, 1, [&] { return launch_decode_gateup_mx(L, B, workspace, s); }));
     CK(run(h, s, G_MX_QUANT, 1, [&] { return launch_decode_quant_h_mx(L, B, workspace, s); }));
     CK(run(h, s, G_DECODE_DOWN, 1, [&] { return launch_decode_down_mx(L, B, y, workspace, s); }));

@@ -7,6 +7,7 @@
 // slots j = 0..k-1), with no floating-point atomics.
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace moe {
 
@@ -17,6 +18,8 @@ namespace {
 template <typename T>
 __global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ o, const int* __restrict__ inv, int Tn,
                                                       int d, int k, int A, int S, T* __restrict__ y) {
+  griddep_wait();    // after the predecessor grid (launch.cuh)
+  griddep_launch();
   constexpr int V = 16 / sizeof(T);
   const int vecs = d / V;
   const long q = (long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -60,6 +63,8 @@ __global__ void __launch_bounds__(256) router_dl_kernel(const float* __restrict_
                                                         const float* __restrict__ dg_part, int nslots, int Tn, int E,
                                                         int k, int router, int renorm, float scale,
                                                         float* __restrict__ dgate, float* __restrict__ dl) {
+  griddep_wait();    // after the predecessor grid (launch.cuh)
+  griddep_launch();
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= Tn) return;
@@ -140,6 +145,8 @@ __global__ void __launch_bounds__(256) router_dw_seg_kernel(const float* __restr
                                                             const int* __restrict__ off, const int* __restrict__ perm,
                                                             int d, int E, int k, int accumulate,
                                                             float* __restrict__ dWr, float* __restrict__ part) {
+  griddep_wait();    // after the predecessor grid (launch.cuh)
+  griddep_launch();
   constexpr int V = 16 / sizeof(T);
   __shared__ float red[8][32 * V];
   const int e = blockIdx.y, sp = blockIdx.z, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -187,6 +194,8 @@ __global__ void __launch_bounds__(256) router_dw_seg_kernel(const float* __restr
 __global__ void __launch_bounds__(256) router_dw_reduce_kernel(const float* __restrict__ part,
                                                                const int* __restrict__ off, int E, int d,
                                                                int accumulate, float* __restrict__ dWr) {
+  griddep_wait();    // after the predecessor grid (launch.cuh)
+  griddep_launch();
   const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
   const long n = (long)E * d;
   if (i >= n) return;
@@ -203,6 +212,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) router_dw_dense_kernel(const float* __restrict__ dl, const T* __restrict__ x,
                                                               int Tn, int d, int E, int accumulate,
                                                               float* __restrict__ dWr) {
+  griddep_wait();    // after the predecessor grid (launch.cuh)
+  griddep_launch();
   const int e = blockIdx.y;
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= d) return;
@@ -219,6 +230,8 @@ __global__ void __launch_bounds__(256) dx_gather_kernel(const T* __restrict__ dx
                                                         const int* __restrict__ idx, const float* __restrict__ dl,
                                                         const T* __restrict__ Wr, int Tn, int d, int E, int k, int A,
                                                         int S, int dense, T* __restrict__ dx) {
+  griddep_wait();    // after the predecessor grid (launch.cuh)
+  griddep_launch();
   constexpr int V = 16 / sizeof(T);
   const int vecs = d / V;
   const long q = (long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -281,33 +294,38 @@ cudaError_t launch_combine(const Layer& L, const Bufs& B, void* y, cudaStream_t 
   const long n = (long)B.T * (L.d / V);
   const int blocks = (int)((n + 255) / 256);
   if (L.prec == MOE_FP32)
-    combine_kernel<float><<<blocks, 256, 0, s>>>((const float*)B.o, B.inv, B.T, L.d, L.k, B.A, L.S, (float*)y);
+    MOE_TRY(launch_pdl(combine_kernel<float>, dim3(blocks), dim3(256), 0, s, (const float*)B.o, B.inv, B.T, L.d, L.k,
+        B.A, L.S, (float*)y));
   else
-    combine_kernel<bf16><<<blocks, 256, 0, s>>>((const bf16*)B.o, B.inv, B.T, L.d, L.k, B.A, L.S, (bf16*)y);
+    MOE_TRY(launch_pdl(combine_kernel<bf16>, dim3(blocks), dim3(256), 0, s, (const bf16*)B.o, B.inv, B.T, L.d, L.k,
+        B.A, L.S, (bf16*)y));
   return cudaGetLastError();
 }
 
 cudaError_t launch_router_bwd(const Layer& L, const Bufs& B, const void* x, float* dWr, bool acc, cudaStream_t s) {
   const int dense = (L.router == MOE_ROUTER_SOFTMAX && !L.renorm) ? 1 : 0;
-  router_dl_kernel<<<(B.T * 32 + 255) / 256, 256, 0, s>>>(B.logits, B.idx, B.gate, B.inv, B.dg_part, L.f / 64, B.T,
-                                                          L.E, L.k, L.router, L.renorm, L.scale, B.dgate, B.dl);
+  MOE_TRY(launch_pdl(router_dl_kernel, dim3((B.T * 32 + 255) / 256), dim3(256), 0, s, B.logits, B.idx, B.gate, B.inv,
+      B.dg_part, L.f / 64, B.T, L.E, L.k, L.router, L.renorm, L.scale, B.dgate, B.dl));
   if (dense) {
     dim3 grid((L.d + 255) / 256, L.E);
     if (L.prec == MOE_FP32)
-      router_dw_dense_kernel<float><<<grid, 256, 0, s>>>(B.dl, (const float*)x, B.T, L.d, L.E, acc, dWr);
+      MOE_TRY(launch_pdl(router_dw_dense_kernel<float>, dim3(grid), dim3(256), 0, s, B.dl, (const float*)x, B.T, L.d,
+          L.E, acc, dWr));
     else
-      router_dw_dense_kernel<bf16><<<grid, 256, 0, s>>>(B.dl, (const bf16*)x, B.T, L.d, L.E, acc, dWr);
+      MOE_TRY(launch_pdl(router_dw_dense_kernel<bf16>, dim3(grid), dim3(256), 0, s, B.dl, (const bf16*)x, B.T, L.d,
+          L.E, acc, dWr));
   } else {
     const int cols = 32 * 16 / (int)elem_bytes(L.prec);
     dim3 grid((L.d + cols - 1) / cols, L.E, kRouterSplit);
     if (L.prec == MOE_FP32)
-      router_dw_seg_kernel<float><<<grid, 256, 0, s>>>(B.dl, (const float*)x, B.off, B.perm, L.d, L.E, L.k, acc,
-                                                              dWr, B.dwr_part);
+      MOE_TRY(launch_pdl(router_dw_seg_kernel<float>, dim3(grid), dim3(256), 0, s, B.dl, (const float*)x, B.off,
+          B.perm, L.d, L.E, L.k, acc, dWr, B.dwr_part));
     else
-      router_dw_seg_kernel<bf16><<<grid, 256, 0, s>>>(B.dl, (const bf16*)x, B.off, B.perm, L.d, L.E, L.k, acc,
-                                                             dWr, B.dwr_part);
+      MOE_TRY(launch_pdl(router_dw_seg_kernel<bf16>, dim3(grid), dim3(256), 0, s, B.dl, (const bf16*)x, B.off, B.perm,
+          L.d, L.E, L.k, acc, dWr, B.dwr_part));
     const long n = (long)L.E * L.d;
-    router_dw_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(B.dwr_part, B.off, L.E, L.d, acc, dWr);
+    MOE_TRY(launch_pdl(router_dw_reduce_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, B.dwr_part, B.off,
+        L.E, L.d, acc, dWr));
   }
   return cudaGetLastError();
 }
@@ -318,11 +336,11 @@ cudaError_t launch_dx_gather(const Layer& L, const Bufs& B, void* dx, cudaStream
   const long n = (long)B.T * (L.d / V);
   const int blocks = (int)((n + 255) / 256);
   if (L.prec == MOE_FP32)
-    dx_gather_kernel<float><<<blocks, 256, 0, s>>>((const float*)B.dx_rows, B.inv, B.idx, B.dl, (const float*)L.Wr,
-                                                   B.T, L.d, L.E, L.k, B.A, L.S, dense, (float*)dx);
+    MOE_TRY(launch_pdl(dx_gather_kernel<float>, dim3(blocks), dim3(256), 0, s, (const float*)B.dx_rows, B.inv, B.idx,
+        B.dl, (const float*)L.Wr, B.T, L.d, L.E, L.k, B.A, L.S, dense, (float*)dx));
   else
-    dx_gather_kernel<bf16><<<blocks, 256, 0, s>>>((const bf16*)B.dx_rows, B.inv, B.idx, B.dl, (const bf16*)L.Wr,
-                                                  B.T, L.d, L.E, L.k, B.A, L.S, dense, (bf16*)dx);
+    MOE_TRY(launch_pdl(dx_gather_kernel<bf16>, dim3(blocks), dim3(256), 0, s, (const bf16*)B.dx_rows, B.inv, B.idx,
+        B.dl, (const bf16*)L.Wr, B.T, L.d, L.E, L.k, B.A, L.S, dense, (bf16*)dx));
   return cudaGetLastError();
 }
 

@@ -30,6 +30,7 @@
 #include "kernels.h"
 #include "mx_quant.cuh"
 #include "topk.cuh"
+#include "launch.cuh"
 
 namespace moe {
 
@@ -79,13 +80,46 @@ DecodeWs carve(const Layer& L, int B, void* ws) {
   return w;
 }
 
+// 32 fp32 values -> their MX quantisation: 32 E4M3 codes written as fp16 values (64 bytes at
+// codes), the E8M0 byte at *scale.
+__device__ __forceinline__ void quant32_to_f16(const float (&v)[32], uint16_t* codes, uint8_t* scale) {
+  uint4 q[2];
+  *scale = quant32(v, q[0], q[1]);
+  uint4* dst = reinterpret_cast<uint4*>(codes);
+#pragma unroll
+  for (int hlf = 0; hlf < 2; ++hlf) {
+    const uint32_t w[4] = {q[hlf].x, q[hlf].y, q[hlf].z, q[hlf].w};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] & 0xffffu), __NV_E4M3);
+      const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] >> 16), __NV_E4M3);
+      o[2 * i] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
+      o[2 * i + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
+    }
+    dst[2 * hlf] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[2 * hlf + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+// x [B, d] bf16 -> xc, xs (MXFP8 layers), 32-value block b.
+__device__ __forceinline__ void quant_x_block(const bf16* __restrict__ x, int b, const DecodeWs& w) {
+  float v[32];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) unpack8(*reinterpret_cast<const uint4*>(x + (size_t)b * 32 + 8 * q), v + 8 * q);
+  quant32_to_f16(v, w.xc + (size_t)b * 32, w.xs + b);
+}
+
 constexpr int kRouteWarps = 8;
 constexpr int kBatch = 7;   // 16-byte chunks per lane loaded before they are used
 
 __global__ void __launch_bounds__(kRouteWarps * 32) decode_route_kernel(
     const bf16* __restrict__ x, const bf16* __restrict__ Wr, const float* __restrict__ bias, int B, int d, int E,
-    int k, int S, int router, int renorm, float scale, int parts, DecodeWs w, int* counter) {
+    int k, int S, int router, int renorm, float scale, int parts, DecodeWs w, int* counter, int quant_x) {
   griddep_launch();
+  // MXFP8 layers: the blocks also quantise x along d for the gate/up kernel (one launch fewer)
+  if (quant_x)
+    for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < B * d / 32; b += gridDim.x * blockDim.x) quant_x_block(x, b, w);
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   // `parts` consecutive warps of a block share one (t, e); warp `part` takes the 16-byte chunks
   // part*32 + lane, + 32*parts, ...
@@ -387,27 +421,6 @@ __device__ __forceinline__ float e8m0(uint32_t s) {
   return s ? __uint_as_float(s << 23) : __uint_as_float(0x00400000u);
 }
 
-// 32 fp32 values -> their MX quantisation: 32 E4M3 codes written as fp16 values (64 bytes at
-// codes), the E8M0 byte at *scale.
-__device__ __forceinline__ void quant32_to_f16(const float (&v)[32], uint16_t* codes, uint8_t* scale) {
-  uint4 q[2];
-  *scale = quant32(v, q[0], q[1]);
-  uint4* dst = reinterpret_cast<uint4*>(codes);
-#pragma unroll
-  for (int hlf = 0; hlf < 2; ++hlf) {
-    const uint32_t w[4] = {q[hlf].x, q[hlf].y, q[hlf].z, q[hlf].w};
-    uint32_t o[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] & 0xffffu), __NV_E4M3);
-      const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] >> 16), __NV_E4M3);
-      o[2 * i] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
-      o[2 * i + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
-    }
-    dst[2 * hlf] = make_uint4(o[0], o[1], o[2], o[3]);
-    dst[2 * hlf + 1] = make_uint4(o[4], o[5], o[6], o[7]);
-  }
-}
 
 // acc + a * b for fp16 a, b (exact products) with fp32 accumulation, one rounding per step.
 __device__ __forceinline__ float fma_h(uint32_t a, uint32_t b, float c) {
@@ -433,16 +446,6 @@ __device__ __forceinline__ float dot16_codes(const uint4& w, const uint4& a0, co
     acc = fma_h(hi.y, aa[2 * q + 1] >> 16, acc);
   }
   return acc;
-}
-
-// x [B, d] bf16 -> xc, xs: one thread per 32-value block.
-__global__ void __launch_bounds__(256) decode_quant_x_kernel(const bf16* __restrict__ x, int nblocks, DecodeWs w) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= nblocks) return;
-  float v[32];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) unpack8(*reinterpret_cast<const uint4*>(x + (size_t)b * 32 + 8 * q), v + 8 * q);
-  quant32_to_f16(v, w.xc + (size_t)b * 32, w.xs + b);
 }
 
 constexpr int kBatchMx = 4;   // 16-byte chunks per lane per row in flight (two blocks per SM fit)
@@ -696,20 +699,6 @@ __global__ void __launch_bounds__(kDownWarps * 32) decode_down_mx_kernel(const u
 // Launch with programmatic stream serialisation: the kernel may start while
 // its predecessor finishes; it waits (griddepcontrol.wait) before reading the
 // predecessor's results.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), int grid, int block, size_t smem, cudaStream_t s, Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(block);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
-}
 
 }  // namespace
 
@@ -733,7 +722,7 @@ cudaError_t launch_decode_route(const Layer& L, const void* x, int B, void* ws, 
   const int route_blocks = (B * L.E + items_per_block - 1) / items_per_block;
   decode_route_kernel<<<route_blocks, kRouteWarps * 32, 0, s>>>((const bf16*)x, (const bf16*)L.Wr, L.bias, B, L.d,
                                                                 L.E, L.k, L.S, L.router, L.renorm, L.scale, parts, w,
-                                                                L.decode_counter);
+                                                                L.decode_counter, L.prec == MOE_MXFP8 ? 1 : 0);
   return cudaGetLastError();
 }
 
@@ -741,13 +730,6 @@ cudaError_t launch_decode_gateup(const Layer& L, const void* x, int B, void* ws,
   DecodeWs w = carve(L, B, ws);
   return launch_pdl(decode_gateup_kernel, L.num_sms * 4, 256, 0, s, (const bf16*)x, (const bf16*)L.W13, L.d, L.f, L.G,
                     L.k, L.E, L.S, w);
-}
-
-cudaError_t launch_decode_quant_x_mx(const Layer& L, const void* x, int B, void* ws, cudaStream_t s) {
-  DecodeWs w = carve(L, B, ws);
-  const int nblocks = B * L.d / 32;
-  decode_quant_x_kernel<<<(nblocks + 255) / 256, 256, 0, s>>>((const bf16*)x, nblocks, w);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_decode_gateup_mx(const Layer& L, int B, void* ws, cudaStream_t s) {

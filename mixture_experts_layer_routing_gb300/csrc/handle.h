@@ -24,7 +24,7 @@ struct moe_handle_s {
   // GEMMs, and in a chunked step the next chunk's routing beside this chunk's expert GEMMs (fork /
   // join with these events; capturable in a CUDA graph).
   // moe_decode runs the grouped-GEMM forward for B >= decode_gemm_from (the measured crossover)
-  int decode_gemm_from = moe::kDecodeGemmFrom;
+  int decode_gemm_from = moe::kDecodeGemmFrom;   // (MXFP8 layers: kDecodeGemmFromMx)
   cudaStream_t side = nullptr;
   cudaEvent_t ev_dh = nullptr, ev_dx = nullptr, ev_join = nullptr;
 };

@@ -22,7 +22,8 @@ constexpr int kPrefixArrays = 6;   // tile-schedule prefix arrays of nseg + 1 in
 constexpr int kGate = 128;        // gate/up interleave block of the packed bf16 W13 (rows)
 constexpr int kGateMx = 64;       // gate/up interleave block of the MXFP8 W13 (rows)
 constexpr int kMaxDecodeB = 64;
-constexpr int kDecodeGemmFrom = 8;   // batch size from which moe_decode takes the grouped-GEMM forward
+constexpr int kDecodeGemmFrom = 8;     // batch size from which moe_decode takes the grouped-GEMM forward (bf16)
+constexpr int kDecodeGemmFromMx = 4;   // (MXFP8)
 
 // Shape of one layer and the pointers that stay fixed after moe_set_weights.
 struct Layer {
@@ -129,7 +130,6 @@ cudaError_t launch_decode_route(const Layer& L, const void* x, int B, void* ws, 
 cudaError_t launch_decode_gateup(const Layer& L, const void* x, int B, void* ws, cudaStream_t s);
 cudaError_t launch_decode_down(const Layer& L, int B, void* y, void* ws, cudaStream_t s);
 // MXFP8 layers: x quantised along d, gate/up on E4M3 W13, h quantised along f, down on E4M3 Wd.
-cudaError_t launch_decode_quant_x_mx(const Layer& L, const void* x, int B, void* ws, cudaStream_t s);
 cudaError_t launch_decode_gateup_mx(const Layer& L, int B, void* ws, cudaStream_t s);
 cudaError_t launch_decode_quant_h_mx(const Layer& L, int B, void* ws, cudaStream_t s);
 cudaError_t launch_decode_down_mx(const Layer& L, int B, void* y, void* ws, cudaStream_t s);

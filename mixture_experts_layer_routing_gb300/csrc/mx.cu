@@ -39,6 +39,7 @@
 #include "kernels.h"
 #include "tc_ptx.cuh"
 #include "mx_quant.cuh"
+#include "launch.cuh"
 
 namespace moe {
 
@@ -153,6 +154,8 @@ __global__ void __launch_bounds__(256) mx_quant_sorted_kernel(const bf16* __rest
                                                               const int* __restrict__ off,
                                                               const int* __restrict__ mt_off, int nseg, int K,
                                                               uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
+  griddep_wait();    // after the predecessor grid (launch.cuh)
+  griddep_launch();
   __shared__ int seg[3];
   const int mt = blockIdx.x;
   if (threadIdx.x == 0) {
@@ -204,6 +207,8 @@ __global__ void __launch_bounds__(128) mx_quant_cols_kernel(const bf16* __restri
                                                             const int* __restrict__ mt_off, int nseg, int W, int f,
                                                             int G, uint8_t* __restrict__ q, uint8_t* __restrict__ s,
                                                             const int* __restrict__ out_base) {
+  griddep_wait();    // after the predecessor grid (launch.cuh)
+  griddep_launch();
   const int lane = threadIdx.x & 31;
   const int c = (blockIdx.x * 4 + (threadIdx.x >> 5)) * 128 + lane * 4;   // this lane's 4 columns
   long rb = blockIdx.y;                    // 32-row block (of the chunk's padded segment layout)
@@ -376,6 +381,8 @@ __device__ __forceinline__ MTile mx_map(const MxParams& p, int L, const int* off
 template <int BMODE, int EPI, int NB>
 __global__ void __launch_bounds__(kMxThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, MxParams p) {
+  griddep_wait();    // after the predecessor grid (launch.cuh)
+  griddep_launch();
   static_assert(mx_smem<NB>() <= 227 * 1024, "shared memory per CTA");
   constexpr int MSTAGES = mx_stages<NB>();
   constexpr int kStageBytes = mx_stage_bytes<NB>();
@@ -749,6 +756,8 @@ template <int EPI>
 __global__ void __launch_bounds__(kMxThreads, 1)
     mx_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2, MxParams p) {
+  griddep_wait();    // after the predecessor grid (launch.cuh)
+  griddep_launch();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* scales = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);   // A stages' atoms, then B's
   uint8_t* sA = scales + kWgScaleRegion;            // kWgA stages (1024-aligned)
@@ -959,7 +968,7 @@ cudaError_t wg_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const MxPa
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  kern<<<grid, kMxThreads, kWgSmem, s>>>(tmA, tmB, tmC, tmC2, p);
+  MOE_TRY(launch_pdl(kern, dim3(grid), dim3(kMxThreads), kWgSmem, s, tmA, tmB, tmC, tmC2, p));
   return cudaGetLastError();
 }
 
@@ -973,7 +982,7 @@ cudaError_t mx_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const MxPa
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  kern<<<grid, kMxThreads, smem, s>>>(tmA, tmB, p);
+  MOE_TRY(launch_pdl(kern, dim3(grid), dim3(kMxThreads), smem, s, tmA, tmB, p));
   return cudaGetLastError();
 }
 
@@ -1023,10 +1032,10 @@ cudaError_t mx_pack_weights(Layer& L, const void* Wg, const void* Wu, const void
                                                                      L.W13s);
   mx_quant_rows_kernel<SRC_PLAIN><<<blocks_for(rd, 8), 256, 0, s>>>(dw, nullptr, rd, L.f, L.f, 0, L.Wdq,
                                                                      L.Wds);
-  mx_quant_cols_kernel<CSRC_W13><<<dim3(blocks_for(d, 512), (unsigned)(r13 / 32)), 128, 0, s>>>(
-      g, u, nullptr, nullptr, nullptr, 0, L.d, L.f, kGateMx, L.W13c, L.W13cs, nullptr);
-  mx_quant_cols_kernel<CSRC_PLAIN><<<dim3(blocks_for(f, 512), (unsigned)(rd / 32)), 128, 0, s>>>(
-      dw, nullptr, nullptr, nullptr, nullptr, 0, L.f, L.f, 0, L.Wdc, L.Wdcs, nullptr);
+  MOE_TRY(launch_pdl(mx_quant_cols_kernel<CSRC_W13>, dim3(dim3(blocks_for(d, 512), (unsigned)(r13 / 32))), dim3(128),
+      0, s, g, u, nullptr, nullptr, nullptr, 0, L.d, L.f, kGateMx, L.W13c, L.W13cs, nullptr));
+  MOE_TRY(launch_pdl(mx_quant_cols_kernel<CSRC_PLAIN>, dim3(dim3(blocks_for(f, 512), (unsigned)(rd / 32))), dim3(128),
+      0, s, dw, nullptr, nullptr, nullptr, nullptr, 0, L.f, L.f, 0, L.Wdc, L.Wdcs, nullptr));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (!make_tmap(&L.tm_W13q, L.W13q, d, r13, MBK, MBN, 1) || !make_tmap(&L.tm_Wdq, L.Wdq, f, rd, MBK, MBN, 1) ||
@@ -1040,8 +1049,8 @@ cudaError_t launch_mx_quant_sorted(const Layer& L, const Bufs& B, const void* sr
                                    cudaStream_t st) {
   const int nseg = L.E + L.S;
   const long tiles = ((long)B.R + 127L * nseg) / 128 + 1;   // at least the routing's tile count
-  mx_quant_sorted_kernel<<<(unsigned)tiles, 256, 0, st>>>((const bf16*)src, B.row_token, B.off, B.mt_off, nseg, K, q,
-                                                          s);
+  MOE_TRY(launch_pdl(mx_quant_sorted_kernel, dim3((unsigned)tiles), dim3(256), 0, st, (const bf16*)src, B.row_token,
+      B.off, B.mt_off, nseg, K, q, s));
   return cudaGetLastError();
 }
 
@@ -1051,8 +1060,8 @@ cudaError_t launch_mx_quant_sorted(const Layer& L, const Bufs& B, const void* sr
 cudaError_t launch_mx_quant_tokens(const Layer& L, const Bufs& B, const void* src, int W, uint8_t* q, uint8_t* s,
                                    cudaStream_t st, const int* out_base) {
   const dim3 grid(blocks_for(W, 512), (unsigned)(B.Rp_max / 32));
-  mx_quant_cols_kernel<CSRC_SEG_GATHER><<<grid, 128, 0, st>>>((const bf16*)src, nullptr, B.row_token, B.off, B.mt_off,
-                                                              L.E + L.S, W, 0, 0, q, s, out_base);
+  MOE_TRY(launch_pdl(mx_quant_cols_kernel<CSRC_SEG_GATHER>, dim3(grid), dim3(128), 0, st, (const bf16*)src, nullptr,
+      B.row_token, B.off, B.mt_off, L.E + L.S, W, 0, 0, q, s, out_base));
   return cudaGetLastError();
 }
 
@@ -1062,6 +1071,8 @@ cudaError_t launch_mx_quant_tokens(const Layer& L, const Bufs& B, const void* sr
 // One block; thread e per expert (nseg <= 1024).
 __global__ void __launch_bounds__(1024) mx_chunk_layout_kernel(const int* __restrict__ chunk_mt, int n, int nseg,
                                                                 int* __restrict__ comb_base, int* __restrict__ comb_mt) {
+  griddep_wait();    // after the predecessor grid (launch.cuh)
+  griddep_launch();
   __shared__ int wsum[32];
   const int e = threadIdx.x, lane = e & 31, w = e >> 5;
   int tot = 0;
@@ -1091,7 +1102,7 @@ __global__ void __launch_bounds__(1024) mx_chunk_layout_kernel(const int* __rest
 
 cudaError_t launch_mx_chunk_layout(const Layer& L, const int* chunk_mt, int n, int* comb_base, int* comb_mt,
                                    cudaStream_t st) {
-  mx_chunk_layout_kernel<<<1, 1024, 0, st>>>(chunk_mt, n, L.E + L.S, comb_base, comb_mt);
+  MOE_TRY(launch_pdl(mx_chunk_layout_kernel, dim3(1), dim3(1024), 0, st, chunk_mt, n, L.E + L.S, comb_base, comb_mt));
   return cudaGetLastError();
 }
 

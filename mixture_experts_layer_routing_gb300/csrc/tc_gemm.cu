@@ -36,6 +36,7 @@
 #include "route_phases.cuh"
 #include "tc_ptx.cuh"
 #include "topk.cuh"
+#include "launch.cuh"
 
 namespace moe {
 
@@ -388,6 +389,8 @@ template <int BN, int AMODE, int BMODE, int SCHED, int EPI, int CG, int MT>
 __global__ void __launch_bounds__(threads_for(MT), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2, TcParams p) {
+  griddep_wait();    // after the predecessor grid (launch.cuh)
+  griddep_launch();
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(CG == 1 || (CG == 2 && SCHED == SCHED_SEG_M && (AMODE == A_GATHER_K || AMODE == A_TMA_K) &&
                             (BMODE == B_TMA_K || BMODE == B_TMA_MN) && BN >= 128),
@@ -1467,7 +1470,8 @@ cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcParam
     attr = true;
   }
   if (CG == 1) {
-    kern<<<grid, threads_for(MT), smem, s>>>(tmA, tmB, tmC ? *tmC : tmA, tmC2 ? *tmC2 : tmA, p);
+    MOE_TRY(launch_pdl(kern, dim3(grid), dim3(threads_for(MT)), smem, s, tmA, tmB, tmC ? *tmC : tmA,
+        tmC2 ? *tmC2 : tmA, p));
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -1563,6 +1567,8 @@ int tc_router_splits(const Layer& L, int T) {
 // logits = sum of the K splits' partials, in split order.
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ part, long n, int ksplit,
                                                             float* __restrict__ out) {
+  griddep_wait();    // after the predecessor grid (launch.cuh)
+  griddep_launch();
   const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   float sum = 0.f;
@@ -1592,7 +1598,8 @@ cudaError_t launch_tc_router_logits(const Layer& L, const void* x, int T, float*
                                                                                                     : L.num_sms, s);
   if (e != cudaSuccess || p.ksplit == 1) return e;
   const long n = (long)T * L.E;
-  splitk_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(part, n, p.ksplit, logits);
+  MOE_TRY(launch_pdl(splitk_reduce_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, part, n, p.ksplit,
+      logits));
   return cudaGetLastError();
 }
 

@@ -41,14 +41,14 @@ def layer_and_inputs():
 @pytest.mark.parametrize("path", ["warp", "crossover"])
 @pytest.mark.parametrize("B", [1, 3, 16, 64])
 def test_mx_decode_parity(layer_and_inputs, B, path):
-    """path "warp": the warp-per-output kernels at every B; "crossover": the default, where
-    moe_decode takes the grouped-GEMM forward from B = 8 (then equal to moe_forward bit for bit)."""
+    """path "warp": the warp-per-output kernels at every B; "crossover": the MXFP8 default, where
+    moe_decode takes the grouped-GEMM forward from B = 4 (then equal to moe_forward bit for bit)."""
     from mixture_experts_layer_routing_gb300 import moe_set_decode_crossover
     layer, g, n = layer_and_inputs
-    moe_set_decode_crossover(layer.h, 65 if path == "warp" else 8)
+    moe_set_decode_crossover(layer.h, 65 if path == "warp" else 4)
     x = g["x"][:B].contiguous()
     y = layer.decode(x)
-    if path == "crossover" and B >= 8:
+    if path == "crossover" and B >= 4:
         assert torch.equal(y, layer.forward(x))
     y2 = layer.decode(x)
     logits = layer.route(x)["logits"].cpu().numpy()
