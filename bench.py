@@ -952,6 +952,14 @@ PROFILE_CASES = {
     "dsv3_e32_bf16_fwd_t1024": (moe_synth.DSV3_UNIFORM.with_(name="dsv3_e32_T1024", E=32, T=1024, seed=9), "fwd", 1024),
     "dsv3_e32_bf16_fwd_t1024_rowtiles2": (moe_synth.DSV3_UNIFORM.with_(name="dsv3_e32_T1024", E=32, T=1024, seed=9),
                                           "fwd_rowtiles2", 1024),
+    # MXFP8 decode at B = 1 (the warp-per-output kernels; from B = 4 moe_decode takes the grouped GEMMs)
+    "dsv3_e32_mxfp8_decode_b1": (moe_synth.DSV3_MXFP8.with_(name="dsv3_e32_mxfp8", E=32, T=64, chunk=0, seed=12),
+                                 "decode", 1),
+    # 256 + 1 experts and four 1024-token chunks: ~4 token-axis K groups per expert in the weight gradients, as in
+    # the 8192-token DeepSeek-V3 step, at d = 1024, f = 512 (~4 GB on the device)
+    "mxfp8_e256_d1024_chunked_t4096": (moe_synth.LayerSpec("mxfp8_T4096_d1024_E256+1_f512_top8_chunk1024", 4096, 1024,
+                                                           256, 1, 512, 8, "sigmoid", True, 2.5, "mxfp8", None, 81,
+                                                           1024), "chunked", 4096),
 }
 
 
