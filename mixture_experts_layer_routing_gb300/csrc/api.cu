@@ -353,7 +353,7 @@ ChunkPlan chunk_plan(const moe_handle_s* h, int T) {
     const size_t nseg = L.E + L.S, d = L.d, f = L.f;
     c.rc = ((size_t)T * L.k + (size_t)L.S * T + 127) / 128 * 128 + 128 * nseg * (size_t)c.n;
     c.comb = al(c.rc * 2 * f) + al(c.rc * 2 * f / 32) + 2 * (al(c.rc * d) + al(c.rc * d / 32)) + al(c.rc * f) +
-             al(c.rc * f / 32) + al(4 * (size_t)c.n * (nseg + 1)) + al(4 * (size_t)c.n * nseg) + al(4 * (nseg + 1));
+             al(c.rc * f / 32) + al(4 * (size_t)c.n * (nseg + 1)) + al(4 * (size_t)c.n * nseg) + 2 * al(4 * (nseg + 1));
   }
   return c;
 }
@@ -594,7 +594,7 @@ moe_status moe_train_chunked(moe_handle h, const void* x, const void* dy, int T,
   auto slot_of = [&](int ch) { return (char*)ring + (size_t)(ch % R) * c.slot; };
   // MXFP8: weight-gradient operands of every chunk go to combined buffers (one gradient pass at the end)
   MxDefer defer;
-  int* chunk_mt = nullptr;
+  int* chunk_off = nullptr;
   if (h->mx) {
     const size_t nseg = L.E + L.S, d = L.d, f = L.f, rc = c.rc;
     char* q = ws_b + c.bwd_ws;
@@ -607,8 +607,9 @@ moe_status moe_train_chunked(moe_handle h, const void* x, const void* dy, int T,
     defer.comb.dy_ts = (uint8_t*)q; q += al(rc * d / 32);
     defer.comb.hg_t = (uint8_t*)q; q += al(rc * f);
     defer.comb.hg_ts = (uint8_t*)q; q += al(rc * f / 32);
-    chunk_mt = (int*)q; q += al(4 * (size_t)c.n * (nseg + 1));
+    chunk_off = (int*)q; q += al(4 * (size_t)c.n * (nseg + 1));
     int* comb_base = (int*)q; q += al(4 * (size_t)c.n * nseg);
+    defer.comb.tok_k32 = (int*)q; q += al(4 * (nseg + 1));
     defer.comb.mt_off = (int*)q;
     defer.comb.Rp_max = (int)rc;
     defer.base = comb_base;
@@ -654,11 +655,12 @@ moe_status moe_train_chunked(moe_handle h, const void* x, const void* dy, int T,
     if (fork) CK(cudaStreamWaitEvent(s, h->ev_join, 0));
     if (h->mx) {
       const Bufs Bc = carve(L, Tc, nullptr, slot_of(ch), nullptr);
-      CK(cudaMemcpyAsync(chunk_mt + (size_t)ch * (L.E + L.S + 1), Bc.mt_off, 4 * (size_t)(L.E + L.S + 1),
+      CK(cudaMemcpyAsync(chunk_off + (size_t)ch * (L.E + L.S + 1), Bc.off, 4 * (size_t)(L.E + L.S + 1),
                          cudaMemcpyDeviceToDevice, s));
     }
   }
-  if (h->mx) CK(launch_mx_chunk_layout(L, chunk_mt, c.n, (int*)defer.base, defer.comb.mt_off, s));
+  if (h->mx)
+    CK(launch_mx_chunk_layout(L, chunk_off, c.n, (int*)defer.base, defer.comb.mt_off, (int*)defer.comb.tok_k32, s));
   // backward, last chunk first: a chunk whose slot a later chunk overwrote is recomputed
   int rec = 0;
   for (int ch = c.n - 1; ch >= 0; --ch) {
@@ -691,6 +693,7 @@ moe_status moe_train_chunked(moe_handle h, const void* x, const void* dy, int T,
     Bw.dy_ts = defer.comb.dy_ts;
     Bw.hg_t = defer.comb.hg_t;
     Bw.hg_ts = defer.comb.hg_ts;
+    Bw.tok_k32 = defer.comb.tok_k32;
     CK(run(h, s, G_BWD_DW13, 1, [&] { return launch_mx_bwd_dw13(L, Bw, dWg, dWu, false, s); }));
     CK(run(h, s, G_BWD_DWD, 1, [&] { return launch_mx_bwd_dwd(L, Bw, dWd, false, s); }));
   }

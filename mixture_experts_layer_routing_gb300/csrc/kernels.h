@@ -102,6 +102,8 @@ struct Bufs {
   uint8_t *dyq, *dys;    // [R, d]: dy of each sorted row
   uint8_t *dudvq, *dudvs;  // [R, 2f]
   int Rp_max;            // rows of the token-axis operands: each segment padded to 128 (upper bound)
+  const int* tok_k32;    // chunked step (nullable): 32-row blocks of each segment's token-axis rows, whose
+                         // chunks are packed at 32 rows (the rest of its last 128-row group is unused)
   uint8_t *dudv_t, *dudv_ts, *x_t, *x_ts, *dy_t, *dy_ts, *hg_t, *hg_ts;  // [Rp, W], atom_mn scales
 };
 
@@ -159,8 +161,8 @@ cudaError_t launch_mx_quant_sorted(const Layer& L, const Bufs& B, const void* sr
                                    cudaStream_t st);
 cudaError_t launch_mx_quant_tokens(const Layer& L, const Bufs& B, const void* src, int W, uint8_t* q, uint8_t* s,
                                    cudaStream_t st, const int* out_base = nullptr);
-cudaError_t launch_mx_chunk_layout(const Layer& L, const int* chunk_mt, int n, int* comb_base, int* comb_mt,
-                                   cudaStream_t st);
+cudaError_t launch_mx_chunk_layout(const Layer& L, const int* chunk_off, int n, int* comb_base, int* comb_mt,
+                                   int* comb_k32, cudaStream_t st);
 cudaError_t launch_mx_gateup(const Layer& L, const Bufs& B, cudaStream_t s);
 cudaError_t launch_mx_down(const Layer& L, const Bufs& B, cudaStream_t s);
 // dY.Wd with the SwiGLU backward: du/dv quantised along 2f into B (dx's operand) and, with g * h,

@@ -97,6 +97,7 @@ struct MxParams {
   uint8_t *tq, *ts;       // ME_DH_Q: du/dv along the token axis (token-axis operand of dW13), codes and scales
   uint8_t *tq2, *ts2;     // ME_DH_Q: g * h along the token axis (operand of dWd)
   const int* tok_base;    // ME_DH_Q (nullable): row where each segment's token-axis rows start (default mt_off * 128)
+  const int* k32;         // weight gradients (nullable): each segment's 32-row K blocks (packed chunk layout)
   const float* row_gate;
   bf16* uv;
   int ld_uv;
@@ -225,8 +226,12 @@ __global__ void __launch_bounds__(128) mx_quant_cols_kernel(const bf16* __restri
     seg_first = (long)mt_off[lo] * 128;
     seg_len = off[lo + 1] - off[lo];
     seg_src0 = off[lo];
-    // out_base (optional): segment lo's rows go to out_base[lo] onwards instead of seg_first
-    if (out_base) out_shift = (long)out_base[lo] - seg_first;
+    // out_base (optional): segment lo's rows go to out_base[lo] onwards instead of seg_first, packed at
+    // 32 rows: the blocks past the segment's last 32-row block belong to the next chunk's rows there
+    if (out_base) {
+      if (rb * 32 - seg_first >= ((seg_len + 31) & ~31L)) return;
+      out_shift = (long)out_base[lo] - seg_first;
+    }
   }
   // source row of row `lane` of the block (null: a zero padding row), then each row's 4 values
   const bf16* my_row = nullptr;
@@ -264,7 +269,7 @@ __global__ void __launch_bounds__(128) mx_quant_cols_kernel(const bf16* __restri
     X[j] = mx_exponent(amax[j]);
     inv[j] = __uint_as_float((uint32_t)(127 - X[j]) << 23);
   }
-  rb += out_shift / 32;                    // segment bases are multiples of 128 rows
+  rb += out_shift / 32;                    // segment bases are multiples of 32 rows
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
     const uint32_t a = __nv_cvt_float2_to_fp8x2(make_float2(__uint_as_float(raw[i].x << 16) * inv[0],
@@ -598,6 +603,9 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         // token-axis rows, which start at tok_base[e] (or mt_off[e] * 128).
         const float g = valid ? p.row_gate[row] : 0.f;
         const long trow = (p.tok_base ? (long)p.tok_base[t.e] : (long)s_mt[t.e] * MBM) + (long)t.m * MBM + r;
+        // packed chunk layout (tok_base): a warp block past the segment's last 32-row block is the next chunk's
+        const bool tok_block =
+            !p.tok_base || t.m * MBM + ew * 32 < ((s_off[t.e + 1] - s_off[t.e] + 31) & ~31);
         float dgp = 0.f;
 #pragma unroll 1
         for (int c0 = 0; c0 < 128; c0 += 32) {
@@ -645,9 +653,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) du[i] = dv[i] = hg[i] = 0.f;
           }
-          quant_tokens32(du, trow, ucol, 2 * (long)p.f, lane, p.tq, p.ts);
-          quant_tokens32(dv, trow, ucol + 64, 2 * (long)p.f, lane, p.tq, p.ts);
-          quant_tokens32(hg, trow, t.n * 128 + c0, p.f, lane, p.tq2, p.ts2);
+          if (tok_block) {
+            quant_tokens32(du, trow, ucol, 2 * (long)p.f, lane, p.tq, p.ts);
+            quant_tokens32(dv, trow, ucol + 64, 2 * (long)p.f, lane, p.tq, p.ts);
+            quant_tokens32(hg, trow, t.n * 128 + c0, p.f, lane, p.tq2, p.ts2);
+          }
         }
       }
       }   // column tiles of the unit
@@ -860,6 +870,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         const int nkb = s_mt[e + 1] - s_mt[e];
         const int nst = (nkb + kWgKG - 1) / kWgKG;
         const bool resident = nst <= kWgA;
+        const int k32 = p.k32 ? p.k32[e] : 4 * nkb;   // 32-row K blocks that hold rows
         const int ait0 = ait;
         for (int i = 0; i < nt && ok; ++i, ++tcount) {
           const int acc = tcount & 1;
@@ -898,11 +909,14 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                              desc_scale_atom(smem_u32(scales + (kWgA + bs) * kWgAtoms + g * kScaleAtom)));
             const uint32_t sa = smem_u32(sA + as * kWgStage), sb = smem_u32(sB + bs * kWgStage);
             for (int g = 0; g < ng; ++g) {
+              const int kmax = min(4, k32 - 4 * (st * kWgKG + g));
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                mma_mx(dcol, desc_mnmajor(sa + g * MBM * MBK + k * 4096), desc_mnmajor(sb + g * MBN * MBK + k * 4096),
-                       idesc_mx(1, 1, k), tmem_base + kWgScaleColA + 4 * (as * kWgKG + g),
-                       tmem_base + kWgScaleColB + 4 * (bs * kWgKG + g), (st > 0 || g > 0 || k > 0) ? 1u : 0u);
+                if (k < kmax)
+                  mma_mx(dcol, desc_mnmajor(sa + g * MBM * MBK + k * 4096),
+                         desc_mnmajor(sb + g * MBN * MBK + k * 4096), idesc_mx(1, 1, k),
+                         tmem_base + kWgScaleColA + 4 * (as * kWgKG + g), tmem_base + kWgScaleColB + 4 * (bs * kWgKG + g),
+                         (st > 0 || g > 0 || k > 0) ? 1u : 0u);
             }
             mma_commit(bempty0 + 8 * bs);
             ++bit;
@@ -1065,19 +1079,22 @@ cudaError_t launch_mx_quant_tokens(const Layer& L, const Bufs& B, const void* sr
   return cudaGetLastError();
 }
 
-// Layout of the combined token-axis operands of a chunked step: chunk_mt [n][nseg+1] holds each chunk's
-// 128-row tile prefix. Expert e's rows of chunk c start at comb_base[c][e] (all chunks of expert e
-// contiguous, in chunk order); comb_mt [nseg+1] is the prefix of 128-row blocks per expert.
-// One block; thread e per expert (nseg <= 1024).
-__global__ void __launch_bounds__(1024) mx_chunk_layout_kernel(const int* __restrict__ chunk_mt, int n, int nseg,
-                                                                int* __restrict__ comb_base, int* __restrict__ comb_mt) {
+// Layout of the combined token-axis operands of a chunked step: chunk_off [n][nseg+1] holds each chunk's row
+// offsets (off). Expert e's rows of chunk c start at comb_base[c][e]: all chunks of expert e contiguous, in
+// chunk order, each padded to a multiple of 32 rows (the token-axis scale block); comb_mt [nseg+1] is the
+// prefix of each expert's 128-row groups and comb_k32[e] its 32-row blocks (the weight gradients' MMAs stop
+// there; the rest of the last group is never read). One block; thread e per expert (nseg <= 1024).
+__global__ void __launch_bounds__(1024) mx_chunk_layout_kernel(const int* __restrict__ chunk_off, int n, int nseg,
+                                                                int* __restrict__ comb_base, int* __restrict__ comb_mt,
+                                                                int* __restrict__ comb_k32) {
   griddep_wait();    // after the predecessor grid (launch.cuh)
   griddep_launch();
   __shared__ int wsum[32];
   const int e = threadIdx.x, lane = e & 31, w = e >> 5;
-  int tot = 0;
+  int rows32 = 0;   // this expert's rows over all chunks, each chunk rounded up to 32
   if (e < nseg)
-    for (int c = 0; c < n; ++c) tot += chunk_mt[c * (nseg + 1) + e + 1] - chunk_mt[c * (nseg + 1) + e];
+    for (int c = 0; c < n; ++c) rows32 += (chunk_off[c * (nseg + 1) + e + 1] - chunk_off[c * (nseg + 1) + e] + 31) & ~31;
+  const int tot = (rows32 + 127) / 128;   // 128-row groups
   int incl = tot;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -1091,18 +1108,20 @@ __global__ void __launch_bounds__(1024) mx_chunk_layout_kernel(const int* __rest
   const int excl = base + incl - tot;
   if (e < nseg) {
     comb_mt[e] = excl;
-    int run = excl;
+    comb_k32[e] = rows32 / 32;
+    int run = excl * 128;
     for (int c = 0; c < n; ++c) {
-      comb_base[c * nseg + e] = run * 128;
-      run += chunk_mt[c * (nseg + 1) + e + 1] - chunk_mt[c * (nseg + 1) + e];
+      comb_base[c * nseg + e] = run;
+      run += (chunk_off[c * (nseg + 1) + e + 1] - chunk_off[c * (nseg + 1) + e] + 31) & ~31;
     }
     if (e == nseg - 1) comb_mt[nseg] = excl + tot;
   }
 }
 
-cudaError_t launch_mx_chunk_layout(const Layer& L, const int* chunk_mt, int n, int* comb_base, int* comb_mt,
-                                   cudaStream_t st) {
-  MOE_TRY(launch_pdl(mx_chunk_layout_kernel, dim3(1), dim3(1024), 0, st, chunk_mt, n, L.E + L.S, comb_base, comb_mt));
+cudaError_t launch_mx_chunk_layout(const Layer& L, const int* chunk_off, int n, int* comb_base, int* comb_mt,
+                                   int* comb_k32, cudaStream_t st) {
+  MOE_TRY(launch_pdl(mx_chunk_layout_kernel, dim3(1), dim3(1024), 0, st, chunk_off, n, L.E + L.S, comb_base, comb_mt,
+                     comb_k32));
   return cudaGetLastError();
 }
 
@@ -1192,6 +1211,7 @@ cudaError_t launch_mx_bwd_dw13(const Layer& L, const Bufs& B, void* dWg, void* d
   p.n_tiles = L.d / MBN;
   p.out = dWg;
   p.out2 = dWu;
+  p.k32 = B.tok_k32;
   p.ldo = L.d;
   p.accumulate = acc ? 1 : 0;
   const uint64_t nseg = L.E + L.S;
@@ -1214,6 +1234,7 @@ cudaError_t launch_mx_bwd_dwd(const Layer& L, const Bufs& B, void* dWd, bool acc
   p.n_tiles = L.f / MBN;
   p.out = dWd;
   p.ldo = L.f;
+  p.k32 = B.tok_k32;
   p.accumulate = acc ? 1 : 0;
   CUtensorMap td;
   if (!make_tmap(&td, dWd, L.f, (uint64_t)(L.E + L.S) * L.d, 64, 32)) return cudaErrorInvalidValue;
