@@ -14,7 +14,8 @@
 //   dy.Wd     dy rows (along d)         x  Wd read MN-major, quantised along d
 //   dx        [du dv] rows (along 2f)   x  W13 read MN-major, quantised along 2f
 //   dW13      [du dv] and x, both along the expert's sorted tokens (32-token
-//   dWd       dy and g*h                 blocks, each segment zero-padded to 128)
+//   dWd       dy and g*h                 blocks, each segment zero-padded to 128;
+//                                        chunked step: each chunk's rows at 32)
 // Gate/up rows of the MXFP8 W13 are interleaved in blocks of 64 so that one
 // 128-column tile holds 64 gate and the matching 64 up features.
 //
@@ -54,17 +55,16 @@ constexpr int kMxMmaWarp = kProd + kEpi;
 constexpr int kScaleCol0 = 2 * MBN;                                 // TMEM columns after the two accumulators
 constexpr int kScaleAtom = 512;   // one 128-row operand's scale words for one K block (32 rows x 16 bytes)
 // off[] and the tile prefix mt_off[] (nseg + 1 each), copied to shared memory at kernel start: every
-// role maps each unit through them, and a binary search over global memory is ~9 dependent L2
-// round trips at the start of every unit, during which the producers issue no loads.
+// role maps each unit through them with a shared-memory search.
 constexpr int kSegCache = 2 * (kMaxE + 2) * 4;
 
 enum { MB_TMA_K = 0, MB_TMA_MN = 1 };
 enum { ME_SWIGLU_Q = 0, ME_GATE = 1, ME_DH_Q = 2, ME_STORE = 3, ME_DW13 = 4, ME_DWD = 5 };
 
-// NB: 128-column B tiles per CTA (1, or 2 for the segment-M products: one staged A tile feeds two
+// NB: 128-column B tiles per CTA of the token-row products (1 or 2: with 2, one staged A tile feeds two
 // MMAs, so a 48 KB stage carries 512 MMA cycles where a 32 KB one carries 256). Stages, stage bytes,
 // the block-scale TMEM columns per stage (A, then each B tile) and the staged scale bytes per stage.
-// Shared memory: [scale atoms of every stage][stage ring][SEG_K epilogue staging][barriers].
+// Shared memory: [scale atoms of every stage][stage ring][barriers][segment cache].
 template <int NB> constexpr int mx_stages() { return NB == 2 ? 4 : 6; }
 template <int NB> constexpr int mx_stage_bytes() { return MBM * MBK + NB * MBN * MBK; }
 template <int NB> constexpr int mx_scale_cols() { return 4 + 4 * NB; }
@@ -87,7 +87,7 @@ struct MxParams {
   const int* off;
   const int* mt_off;
   int nseg;
-  int K;                  // SEG_M reduction length (multiple of 128)
+  int K;                  // token-row products: reduction length (multiple of 128)
   int m_tiles, n_tiles;
   void* out;
   int ldo;
