@@ -758,7 +758,7 @@ def decode_lines(layer, spec, dev, pk, tag, expert_bytes, n_batches=16):
         nbytes = float(np.mean(nact)) * expert_bytes + spec.E * spec.d * 2
         t_roof = nbytes / (pk["hbm_gbs"] * 1e9)
         out[f"{tag}_decode_B{B}"] = {
-            "path": ("warp-per-output kernels" if B < (4 if tag == "mx" else 8)
+            "path": ("warp-per-output kernels" if B < (4 if "mxfp8" in tag else 8)
                      else "grouped-GEMM forward (from the crossover batch)"),
             "tokens_per_s": B / (msb * 1e-3), "ms": msb, "ms_median": stb["ms_median"], "ms_min": stb["ms_min"],
             "weight_gbs": nbytes / (msb * 1e-3) / 1e9,
