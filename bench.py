@@ -758,7 +758,7 @@ def decode_lines(layer, spec, dev, pk, tag, expert_bytes, n_batches=16):
         nbytes = float(np.mean(nact)) * expert_bytes + spec.E * spec.d * 2
         t_roof = nbytes / (pk["hbm_gbs"] * 1e9)
         out[f"{tag}_decode_B{B}"] = {
-            "path": ("warp-per-output kernels" if B < (4 if "mxfp8" in tag else 8)
+            "path": ("warp-per-output kernels" if B < 4
                      else "grouped-GEMM forward (from the crossover batch)"),
             "tokens_per_s": B / (msb * 1e-3), "ms": msb, "ms_median": stb["ms_median"], "ms_min": stb["ms_min"],
             "weight_gbs": nbytes / (msb * 1e-3) / 1e9,
@@ -861,7 +861,7 @@ def decode_crossover(layer, spec, dev, n_batches=8):
         rows[str(B)] = {"decode_ms": md, "grouped_gemm_ms": mg}
         if cross is None and mg < md:
             cross = B
-    default = 4 if spec.dtype == "mxfp8" else 8
+    default = 4
     moe_set_decode_crossover(layer.h, default)
     return {"ms": rows, "gemm_faster_from_B": cross,
             "note": f"decode_ms: warp-per-output kernels forced; moe_decode itself switches to the GEMMs from B = {default}"}

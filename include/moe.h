@@ -174,7 +174,7 @@ moe_status moe_train_chunked(moe_handle h, const void* x, const void* dy, int T,
 
 /* Small-batch decode: y [B, d] bf16 = layer(x [B, d] bf16), 1 <= B <= 64,
  * cfg.prec MOE_BF16 or MOE_MXFP8 (MOE_FP32: MOE_ERR_UNSUPPORTED). Below the
- * crossover batch (moe_set_decode_crossover; default 8, MXFP8 4): warp-per-output
+ * crossover batch (moe_set_decode_crossover; default 4): warp-per-output
  * kernels with fp32 intermediates ("Cursor a réécrit le décodage de MoE",
  * toolnavs.com); from it, the grouped-GEMM forward. An MXFP8 layer decodes on
  * its E4M3 weights and computes its MXFP8 forward on the B tokens: x quantised
@@ -184,11 +184,10 @@ moe_status moe_decode(moe_handle h, const void* x, int B, void* y, void* workspa
 /* Batch size from which moe_decode runs the tensor-core grouped-GEMM forward
  * (moe_forward on the B tokens, inference) instead of the warp-per-output
  * kernels, on layers that have the tensor-core path (bf16 and MXFP8). On GB300
- * at DeepSeek-V3 shapes the bf16 warp kernels win up to B = 4 and the grouped
- * GEMMs from B = 8 (their per-token FMA work grows with B while the GEMMs read
- * each used expert's weights once), so the bf16 default is 8; on E4M3 weights
- * the grouped GEMMs win from B = 4 (the warp kernels decode each weight byte on
- * the CUDA cores), so the MXFP8 default is 4. b_min = 65 keeps every
+ * at DeepSeek-V3 shapes the warp kernels win at B = 1 and 2 and the grouped
+ * GEMMs from B = 4 in both precisions (the warp kernels' per-token work grows
+ * with B while the GEMMs read each used expert's weights once), so the default
+ * is 4. b_min = 65 keeps every
  * batch on the warp kernels. Both paths compute the layer within the
  * precision's tolerance (the warp kernels keep h in fp32, the GEMM path rounds
  * it to the storage type, as moe_forward does). Host-only; b_min outside

@@ -250,7 +250,10 @@ constexpr int kTokGroup = 4;
 
 // One warp per (U entry, row i) item, grid-stride over items. Each lane loads
 // kBatch 16-byte chunks of both weight rows before using any of them.
-__global__ void __launch_bounds__(256) decode_gateup_kernel(const bf16* __restrict__ x, const bf16* __restrict__ W13,
+// TG tokens of an expert per pass, NB 16-byte chunks per lane per row in flight: (4, NB) in
+// general, (1, 10) for single tokens, where the registers of the token group go to a deeper batch.
+template <int TG, int NB>
+__global__ void __launch_bounds__(256, 2) decode_gateup_kernel(const bf16* __restrict__ x, const bf16* __restrict__ W13,
                                                             int d, int f, int G, int k, int E, int S, DecodeWs w) {
   griddep_launch();
   // The shared expert is used by every token whatever the routing: while the
@@ -281,18 +284,18 @@ __global__ void __launch_bounds__(256) decode_gateup_kernel(const bf16* __restri
     const int a0 = w.u_off[ui], a1 = w.u_off[ui + 1];
     const bf16* wg = W13 + ((size_t)e * 2 * f + (i / G) * 2 * G + (i % G)) * d;
     const bf16* wu = wg + (size_t)G * d;
-    for (int g0 = a0; g0 < a1; g0 += kTokGroup) {
-      const int nt = min(kTokGroup, a1 - g0);
-      const bf16* xr[kTokGroup];
+    for (int g0 = a0; g0 < a1; g0 += TG) {
+      const int nt = min(TG, a1 - g0);
+      const bf16* xr[TG];
 #pragma unroll
-      for (int q = 0; q < kTokGroup; ++q) xr[q] = x + (size_t)(q < nt ? (w.a_tok[g0 + q] >> 8) : 0) * d;
-      float au[kTokGroup], av[kTokGroup];
+      for (int q = 0; q < TG; ++q) xr[q] = x + (size_t)(q < nt ? (w.a_tok[g0 + q] >> 8) : 0) * d;
+      float au[TG], av[TG];
 #pragma unroll
-      for (int q = 0; q < kTokGroup; ++q) au[q] = av[q] = 0.f;
-      for (int cb = lane; cb < nchunk; cb += 32 * kBatch) {
-        uint4 gv[kBatch], uvv[kBatch];
+      for (int q = 0; q < TG; ++q) au[q] = av[q] = 0.f;
+      for (int cb = lane; cb < nchunk; cb += 32 * NB) {
+        uint4 gv[NB], uvv[NB];
 #pragma unroll
-        for (int q = 0; q < kBatch; ++q) {
+        for (int q = 0; q < NB; ++q) {
           const int c = cb + q * 32;
           if (c < nchunk) {
             gv[q] = ld_stream(wg + c * 8);
@@ -300,14 +303,14 @@ __global__ void __launch_bounds__(256) decode_gateup_kernel(const bf16* __restri
           }
         }
 #pragma unroll
-        for (int q = 0; q < kBatch; ++q) {
+        for (int q = 0; q < NB; ++q) {
           const int c = cb + q * 32;
           if (c < nchunk) {
             float fg[8], fu[8];
             unpack8(gv[q], fg);
             unpack8(uvv[q], fu);
 #pragma unroll
-            for (int tt = 0; tt < kTokGroup; ++tt) {
+            for (int tt = 0; tt < TG; ++tt) {
               if (tt < nt) {
                 float xv[8];
                 unpack8(*reinterpret_cast<const uint4*>(xr[tt] + c * 8), xv);
@@ -322,7 +325,7 @@ __global__ void __launch_bounds__(256) decode_gateup_kernel(const bf16* __restri
         }
       }
 #pragma unroll
-      for (int tt = 0; tt < kTokGroup; ++tt) {
+      for (int tt = 0; tt < TG; ++tt) {
         if (tt < nt) {
           const float u = warp_sum(au[tt]);
           const float v = warp_sum(av[tt]);
@@ -448,11 +451,14 @@ __device__ __forceinline__ float dot16_codes(const uint4& w, const uint4& a0, co
   return acc;
 }
 
-constexpr int kBatchMx = 4;   // 16-byte chunks per lane per row in flight (two blocks per SM fit)
 
 // Gate/up on E4M3 weights: one warp per (U entry, row i); each lane takes 16-byte chunks (16
 // values, half of a 32-value scale block) of the gate and up rows, decodes them once and applies
 // the block scale to each token's partial dot product.
+// TG tokens of an expert per pass, NB 16-byte chunks per lane per row in flight; launched as (1, 7):
+// one token per pass leaves the registers for seven chunks per row in flight at two blocks per SM
+// (with four tokens per pass only four fit, and every B measured ran slower).
+template <int TG, int NB>
 __global__ void __launch_bounds__(256, 2) decode_gateup_mx_kernel(const uint8_t* __restrict__ W13q,
                                                                const uint8_t* __restrict__ W13s, int d, int f, int G,
                                                                int k, int E, int S, DecodeWs w) {
@@ -483,24 +489,24 @@ __global__ void __launch_bounds__(256, 2) decode_gateup_mx_kernel(const uint8_t*
     const size_t rg = (size_t)e * 2 * f + (i / G) * 2 * G + (i % G), ru = rg + G;
     const uint8_t* wg = W13q + rg * d;
     const uint8_t* wu = W13q + ru * d;
-    for (int g0 = a0; g0 < a1; g0 += kTokGroup) {
-      const int nt = min(kTokGroup, a1 - g0);
-      const uint16_t* xr[kTokGroup];
-      const uint8_t* xsr[kTokGroup];
+    for (int g0 = a0; g0 < a1; g0 += TG) {
+      const int nt = min(TG, a1 - g0);
+      const uint16_t* xr[TG];
+      const uint8_t* xsr[TG];
 #pragma unroll
-      for (int q = 0; q < kTokGroup; ++q) {
+      for (int q = 0; q < TG; ++q) {
         const size_t t = q < nt ? (w.a_tok[g0 + q] >> 8) : 0;
         xr[q] = w.xc + t * d;
         xsr[q] = w.xs + t * nb;
       }
-      float au[kTokGroup], av[kTokGroup];
+      float au[TG], av[TG];
 #pragma unroll
-      for (int q = 0; q < kTokGroup; ++q) au[q] = av[q] = 0.f;
-      for (int cb = lane; cb < nchunk; cb += 32 * kBatchMx) {
-        uint4 gv[kBatchMx], uvv[kBatchMx];
-        uint32_t sgv[kBatchMx], suv[kBatchMx];
+      for (int q = 0; q < TG; ++q) au[q] = av[q] = 0.f;
+      for (int cb = lane; cb < nchunk; cb += 32 * NB) {
+        uint4 gv[NB], uvv[NB];
+        uint32_t sgv[NB], suv[NB];
 #pragma unroll
-        for (int q = 0; q < kBatchMx; ++q) {
+        for (int q = 0; q < NB; ++q) {
           const int c = cb + q * 32;
           if (c < nchunk) {
             gv[q] = ld_stream(reinterpret_cast<const bf16*>(wg + (size_t)c * 16));
@@ -510,12 +516,12 @@ __global__ void __launch_bounds__(256, 2) decode_gateup_mx_kernel(const uint8_t*
           }
         }
 #pragma unroll
-        for (int q = 0; q < kBatchMx; ++q) {
+        for (int q = 0; q < NB; ++q) {
           const int c = cb + q * 32;
           if (c < nchunk) {
             const float s_g = e8m0(sgv[q]), s_u = e8m0(suv[q]);
 #pragma unroll
-            for (int tt = 0; tt < kTokGroup; ++tt) {
+            for (int tt = 0; tt < TG; ++tt) {
               if (tt < nt) {
                 // weight codes times x codes, then the x block scale and the weight block scale
                 const uint4* xv8 = reinterpret_cast<const uint4*>(xr[tt] + (size_t)c * 16);
@@ -529,7 +535,7 @@ __global__ void __launch_bounds__(256, 2) decode_gateup_mx_kernel(const uint8_t*
         }
       }
 #pragma unroll
-      for (int tt = 0; tt < kTokGroup; ++tt) {
+      for (int tt = 0; tt < TG; ++tt) {
         if (tt < nt) {
           const float u = warp_sum(au[tt]);
           const float v = warp_sum(av[tt]);
@@ -563,17 +569,17 @@ __global__ void __launch_bounds__(256) decode_quant_h_kernel(int nblocks, Decode
   quant32_to_f16(v, w.hc + (size_t)b * 32, w.hs + b);
 }
 
-constexpr int kFChunksMx = 4;   // 16-byte chunks (16 values) of a Wd row per lane (f <= 2048 per pass)
 
 // The Wd rows c0.. of expert e, features [f0, f0 + 2048), and their block scales (as 2^(s-127)).
+template <int NC, int FC>
 __device__ __forceinline__ void load_wd_mx(const uint8_t* Wdq, const uint8_t* Wds, int e, int d, int f, int c0, int f0,
-                                           int lane, uint4 (&wv)[kCols][kFChunksMx], uint32_t (&sv)[kCols][kFChunksMx]) {
+                                           int lane, uint4 (&wv)[NC][FC], uint32_t (&sv)[NC][FC]) {
 #pragma unroll
-  for (int cc = 0; cc < kCols; ++cc) {
-    const size_t r = (size_t)e * d + c0 + cc;
+  for (int cc = 0; cc < NC; ++cc) {
+    const size_t r = (size_t)e * d + min(c0 + cc, d - 1);   // columns past d: any row (not stored)
     const uint8_t* row = Wdq + r * f + f0;
 #pragma unroll
-    for (int q = 0; q < kFChunksMx; ++q) {
+    for (int q = 0; q < FC; ++q) {
       const int c = (lane + 32 * q) * 16;
       if (f0 + c < f) {
         wv[cc][q] = ld_stream(reinterpret_cast<const bf16*>(row + c));
@@ -585,34 +591,38 @@ __device__ __forceinline__ void load_wd_mx(const uint8_t* Wdq, const uint8_t* Wd
 
 // Down on E4M3 weights: warp per pair of output columns, as the bf16 kernel; h comes quantised
 // (as exact fp32 values); each Wd chunk is decoded and scaled once per expert.
+// NC output columns per warp, FC 16-byte chunks of a Wd row per lane per pass over f; launched as
+// (3, 2): three columns per warp fit the whole projection in one wave of blocks (two columns took
+// 1.5 waves), and two chunks keep the registers of both experts' rows in flight.
+template <int NC, int FC>
 __global__ void __launch_bounds__(kDownWarps * 32) decode_down_mx_kernel(const uint8_t* __restrict__ Wdq,
                                                                          const uint8_t* __restrict__ Wds, int B, int d,
                                                                          int f, int k, DecodeWs w,
                                                                          bf16* __restrict__ y) {
-  extern __shared__ float acc_s[];   // [kDownWarps][B][kCols]
+  extern __shared__ float acc_s[];   // [kDownWarps][B][NC]
   griddep_launch();
   griddep_wait();
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-  float* acc = acc_s + (size_t)wib * B * kCols;
+  float* acc = acc_s + (size_t)wib * B * NC;
   const int nU = *w.nU;
-  const int c0 = (blockIdx.x * kDownWarps + wib) * kCols;
+  const int c0 = (blockIdx.x * kDownWarps + wib) * NC;
   if (c0 >= d) return;
   const int nb = f / 32;
-  for (int q = lane; q < B * kCols; q += 32) acc[q] = 0.f;
+  for (int q = lane; q < B * NC; q += 32) acc[q] = 0.f;
   __syncwarp();
-  for (int f0 = 0; f0 < f; f0 += 32 * kFChunksMx * 16) {
-    uint4 wcur[kCols][kFChunksMx], wnext[kCols][kFChunksMx];
-    uint32_t scur[kCols][kFChunksMx], snext[kCols][kFChunksMx];
-    load_wd_mx(Wdq, Wds, w.U[0], d, f, c0, f0, lane, wnext, snext);
+  for (int f0 = 0; f0 < f; f0 += 32 * FC * 16) {
+    uint4 wcur[NC][FC], wnext[NC][FC];
+    uint32_t scur[NC][FC], snext[NC][FC];
+    load_wd_mx<NC, FC>(Wdq, Wds, w.U[0], d, f, c0, f0, lane, wnext, snext);
     for (int ui = 0; ui < nU; ++ui) {
 #pragma unroll
-      for (int cc = 0; cc < kCols; ++cc)
+      for (int cc = 0; cc < NC; ++cc)
 #pragma unroll
-        for (int q = 0; q < kFChunksMx; ++q) {
+        for (int q = 0; q < FC; ++q) {
           wcur[cc][q] = wnext[cc][q];
           scur[cc][q] = snext[cc][q];
         }
-      if (ui + 1 < nU) load_wd_mx(Wdq, Wds, w.U[ui + 1], d, f, c0, f0, lane, wnext, snext);   // next expert in flight
+      if (ui + 1 < nU) load_wd_mx<NC, FC>(Wdq, Wds, w.U[ui + 1], d, f, c0, f0, lane, wnext, snext);   // next expert in flight
       const int a0 = w.u_off[ui], a1 = w.u_off[ui + 1];
       if (a1 - a0 == 1) {
         // one token (the common case at small B): no decoded copy of the chunk is kept
@@ -622,22 +632,22 @@ __global__ void __launch_bounds__(kDownWarps * 32) decode_down_mx_kernel(const u
         const size_t hrow = (size_t)t * (k + 1) + slot;
         const uint16_t* hr = w.hc + hrow * f;
         const uint8_t* hsr = w.hs + hrow * nb;
-        float s[kCols] = {};
+        float s[NC] = {};
 #pragma unroll
-        for (int q = 0; q < kFChunksMx; ++q) {
+        for (int q = 0; q < FC; ++q) {
           const int c = f0 + (lane + 32 * q) * 16;
           if (c < f) {
             const uint4 ha = *reinterpret_cast<const uint4*>(hr + c), hb = *reinterpret_cast<const uint4*>(hr + c + 8);
             const float s_h = e8m0(hsr[c >> 5]);
 #pragma unroll
-            for (int cc = 0; cc < kCols; ++cc)
+            for (int cc = 0; cc < NC; ++cc)
               s[cc] = fmaf(dot16_codes(wcur[cc][q], ha, hb) * s_h, e8m0(scur[cc][q]), s[cc]);
           }
         }
 #pragma unroll
-        for (int cc = 0; cc < kCols; ++cc) {
+        for (int cc = 0; cc < NC; ++cc) {
           const float tot = warp_sum(s[cc]);
-          if (lane == 0) acc[t * kCols + cc] = fmaf(g, tot, acc[t * kCols + cc]);
+          if (lane == 0) acc[t * NC + cc] = fmaf(g, tot, acc[t * NC + cc]);
         }
         __syncwarp();
         continue;
@@ -654,9 +664,9 @@ __global__ void __launch_bounds__(kDownWarps * 32) decode_down_mx_kernel(const u
           hr[tt] = w.hc + hrow * f;
           hsr[tt] = w.hs + hrow * nb;
         }
-        float s[kTokGroup][kCols] = {};
+        float s[kTokGroup][NC] = {};
 #pragma unroll
-        for (int q = 0; q < kFChunksMx; ++q) {
+        for (int q = 0; q < FC; ++q) {
           const int c = f0 + (lane + 32 * q) * 16;
           if (c < f) {
 #pragma unroll
@@ -666,7 +676,7 @@ __global__ void __launch_bounds__(kDownWarps * 32) decode_down_mx_kernel(const u
                 const uint4 hb = *reinterpret_cast<const uint4*>(hr[tt] + c + 8);
                 const float s_h = e8m0(hsr[tt][c >> 5]);
 #pragma unroll
-                for (int cc = 0; cc < kCols; ++cc)
+                for (int cc = 0; cc < NC; ++cc)
                   s[tt][cc] = fmaf(dot16_codes(wcur[cc][q], ha, hb) * s_h, e8m0(scur[cc][q]), s[tt][cc]);
               }
             }
@@ -679,9 +689,9 @@ __global__ void __launch_bounds__(kDownWarps * 32) decode_down_mx_kernel(const u
             const int t = code >> 8;
             const float g = w.a_gate[g0 + tt];
 #pragma unroll
-            for (int cc = 0; cc < kCols; ++cc) {
+            for (int cc = 0; cc < NC; ++cc) {
               const float tot = warp_sum(s[tt][cc]);
-              if (lane == 0) acc[t * kCols + cc] = fmaf(g, tot, acc[t * kCols + cc]);
+              if (lane == 0) acc[t * NC + cc] = fmaf(g, tot, acc[t * NC + cc]);
             }
           }
         }
@@ -690,8 +700,8 @@ __global__ void __launch_bounds__(kDownWarps * 32) decode_down_mx_kernel(const u
     }
   }
   __syncwarp();
-  for (int q = lane; q < B * kCols; q += 32) {
-    const int t = q / kCols, cc = q % kCols;
+  for (int q = lane; q < B * NC; q += 32) {
+    const int t = q / NC, cc = q % NC;
     if (c0 + cc < d) y[(size_t)t * d + c0 + cc] = __float2bfloat16_rn(acc[q]);
   }
 }
@@ -728,14 +738,19 @@ cudaError_t launch_decode_route(const Layer& L, const void* x, int B, void* ws, 
 
 cudaError_t launch_decode_gateup(const Layer& L, const void* x, int B, void* ws, cudaStream_t s) {
   DecodeWs w = carve(L, B, ws);
-  return launch_pdl(decode_gateup_kernel, L.num_sms * 4, 256, 0, s, (const bf16*)x, (const bf16*)L.W13, L.d, L.f, L.G,
-                    L.k, L.E, L.S, w);
+  if (B == 1)   // one token per expert
+    return launch_pdl(decode_gateup_kernel<1, 10>, L.num_sms * 4, 256, 0, s, (const bf16*)x, (const bf16*)L.W13, L.d,
+                      L.f, L.G, L.k, L.E, L.S, w);
+  return launch_pdl(decode_gateup_kernel<kTokGroup, kBatch>, L.num_sms * 4, 256, 0, s, (const bf16*)x,
+                    (const bf16*)L.W13, L.d, L.f, L.G, L.k, L.E, L.S, w);
 }
 
 cudaError_t launch_decode_gateup_mx(const Layer& L, int B, void* ws, cudaStream_t s) {
   DecodeWs w = carve(L, B, ws);
-  return launch_pdl(decode_gateup_mx_kernel, L.num_sms * 4, 256, 0, s, (const uint8_t*)L.W13q, (const uint8_t*)L.W13s,
-                    L.d, L.f, L.G, L.k, L.E, L.S, w);
+  // one token per pass over a row (an expert with several tokens re-reads its rows, from L2): the
+  // registers go to a deeper load batch, faster at every B measured (1-64)
+  return launch_pdl(decode_gateup_mx_kernel<1, 7>, L.num_sms * 4, 256, 0, s, (const uint8_t*)L.W13q,
+                    (const uint8_t*)L.W13s, L.d, L.f, L.G, L.k, L.E, L.S, w);
 }
 
 cudaError_t launch_decode_quant_h_mx(const Layer& L, int B, void* ws, cudaStream_t s) {
@@ -746,10 +761,11 @@ cudaError_t launch_decode_quant_h_mx(const Layer& L, int B, void* ws, cudaStream
 
 cudaError_t launch_decode_down_mx(const Layer& L, int B, void* y, void* ws, cudaStream_t s) {
   DecodeWs w = carve(L, B, ws);
-  const int down_blocks = (L.d + kDownWarps * kCols - 1) / (kDownWarps * kCols);
-  const size_t smem = sizeof(float) * kDownWarps * B * kCols;
-  return launch_pdl(decode_down_mx_kernel, down_blocks, kDownWarps * 32, smem, s, (const uint8_t*)L.Wdq,
-                    (const uint8_t*)L.Wds, B, L.d, L.f, L.k, w, (bf16*)y);
+  // three columns per warp: the d / 24 blocks fit one wave at two blocks per SM
+  constexpr int NC = 3;
+  const int blocks = (L.d + kDownWarps * NC - 1) / (kDownWarps * NC);
+  return launch_pdl(decode_down_mx_kernel<NC, 2>, blocks, kDownWarps * 32, sizeof(float) * kDownWarps * B * NC, s,
+                    (const uint8_t*)L.Wdq, (const uint8_t*)L.Wds, B, L.d, L.f, L.k, w, (bf16*)y);
 }
 
 cudaError_t launch_decode_down(const Layer& L, int B, void* y, void* ws, cudaStream_t s) {

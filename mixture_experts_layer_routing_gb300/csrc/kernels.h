@@ -22,7 +22,7 @@ constexpr int kPrefixArrays = 6;   // tile-schedule prefix arrays of nseg + 1 in
 constexpr int kGate = 128;        // gate/up interleave block of the packed bf16 W13 (rows)
 constexpr int kGateMx = 64;       // gate/up interleave block of the MXFP8 W13 (rows)
 constexpr int kMaxDecodeB = 64;
-constexpr int kDecodeGemmFrom = 8;     // batch size from which moe_decode takes the grouped-GEMM forward (bf16)
+constexpr int kDecodeGemmFrom = 4;     // batch size from which moe_decode takes the grouped-GEMM forward (bf16)
 constexpr int kDecodeGemmFromMx = 4;   // (MXFP8)
 
 // Shape of one layer and the pointers that stay fixed after moe_set_weights.
