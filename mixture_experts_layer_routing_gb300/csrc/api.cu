@@ -716,7 +716,9 @@ moe_status moe_decode(moe_handle h, const void* x, int B, void* y, void* workspa
   CK(run(h, s, G_DECODE_ROUTE, 1, [&] { return launch_decode_route(L, x, B, workspace, s); }));
   if (L.prec == MOE_MXFP8) {
     CK(run(h, s, G_DECODE_GATEUP, 1, [&] { return launch_decode_gateup_mx(L, B, workspace, s); }));
-    CK(run(h, s, G_MX_QUANT, 1, [&] { return launch_decode_quant_h_mx(L, B, workspace, s); }));
+    // at small B the down kernel quantises h itself (into shared memory)
+    if (!decode_down_mx_stages_h(L, B))
+      CK(run(h, s, G_MX_QUANT, 1, [&] { return launch_decode_quant_h_mx(L, B, workspace, s); }));
     CK(run(h, s, G_DECODE_DOWN, 1, [&] { return launch_decode_down_mx(L, B, y, workspace, s); }));
     return MOE_OK;
   }

@@ -594,26 +594,55 @@ __device__ __forceinline__ void load_wd_mx(const uint8_t* Wdq, const uint8_t* Wd
 // NC output columns per warp, FC 16-byte chunks of a Wd row per lane per pass over f; launched as
 // (3, 2): three columns per warp fit the whole projection in one wave of blocks (two columns took
 // 1.5 waves), and two chunks keep the registers of both experts' rows in flight.
-template <int NC, int FC>
+// STAGE: the block first quantises h [B, k+1, f] along f itself, into shared memory (codes held in
+// fp16 and the scale bytes, exactly as the h quantiser kernel would store them), so that kernel is
+// not launched and the per-expert reads of h come from shared memory; taken while the staged h
+// leaves two blocks per SM (B <= 3 at DeepSeek-V3 shapes). The first expert's weight rows are
+// already in flight meanwhile.
+template <int NC, int FC, bool STAGE>
 __global__ void __launch_bounds__(kDownWarps * 32) decode_down_mx_kernel(const uint8_t* __restrict__ Wdq,
                                                                          const uint8_t* __restrict__ Wds, int B, int d,
                                                                          int f, int k, DecodeWs w,
                                                                          bf16* __restrict__ y) {
-  extern __shared__ float acc_s[];   // [kDownWarps][B][NC]
+  extern __shared__ __align__(16) float acc_s[];   // [kDownWarps][B][NC], then (STAGE) h codes and scales
   griddep_launch();
   griddep_wait();
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   float* acc = acc_s + (size_t)wib * B * NC;
   const int nU = *w.nU;
   const int c0 = (blockIdx.x * kDownWarps + wib) * NC;
-  if (c0 >= d) return;
   const int nb = f / 32;
+  uint4 wcur[NC][FC], wnext[NC][FC];
+  uint32_t scur[NC][FC], snext[NC][FC];
+  if (c0 < d) load_wd_mx<NC, FC>(Wdq, Wds, w.U[0], d, f, c0, 0, lane, wnext, snext);
+  const uint16_t* hc = w.hc;
+  const uint8_t* hs = w.hs;
+  if (STAGE) {
+    const int na = B * (k + 1);
+    uint16_t* shc = reinterpret_cast<uint16_t*>(acc_s + ((kDownWarps * B * NC + 3) & ~3));   // 16-byte aligned
+    uint8_t* shs = reinterpret_cast<uint8_t*>(shc + (size_t)na * f);
+    for (int b = threadIdx.x; b < na * nb; b += blockDim.x) {
+      float v[32];
+      const float4* src = reinterpret_cast<const float4*>(w.h + (size_t)b * 32);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 t4 = src[q];
+        v[4 * q] = t4.x;
+        v[4 * q + 1] = t4.y;
+        v[4 * q + 2] = t4.z;
+        v[4 * q + 3] = t4.w;
+      }
+      quant32_to_f16(v, shc + (size_t)b * 32, shs + b);
+    }
+    __syncthreads();
+    hc = shc;
+    hs = shs;
+  }
+  if (c0 >= d) return;
   for (int q = lane; q < B * NC; q += 32) acc[q] = 0.f;
   __syncwarp();
   for (int f0 = 0; f0 < f; f0 += 32 * FC * 16) {
-    uint4 wcur[NC][FC], wnext[NC][FC];
-    uint32_t scur[NC][FC], snext[NC][FC];
-    load_wd_mx<NC, FC>(Wdq, Wds, w.U[0], d, f, c0, f0, lane, wnext, snext);
+    if (f0 > 0) load_wd_mx<NC, FC>(Wdq, Wds, w.U[0], d, f, c0, f0, lane, wnext, snext);
     for (int ui = 0; ui < nU; ++ui) {
 #pragma unroll
       for (int cc = 0; cc < NC; ++cc)
@@ -630,8 +659,8 @@ __global__ void __launch_bounds__(kDownWarps * 32) decode_down_mx_kernel(const u
         const int t = code >> 8, slot = code & 255;
         const float g = w.a_gate[a0];
         const size_t hrow = (size_t)t * (k + 1) + slot;
-        const uint16_t* hr = w.hc + hrow * f;
-        const uint8_t* hsr = w.hs + hrow * nb;
+        const uint16_t* hr = hc + hrow * f;
+        const uint8_t* hsr = hs + hrow * nb;
         float s[NC] = {};
 #pragma unroll
         for (int q = 0; q < FC; ++q) {
@@ -661,8 +690,8 @@ __global__ void __launch_bounds__(kDownWarps * 32) decode_down_mx_kernel(const u
         for (int tt = 0; tt < kTokGroup; ++tt) {
           const int code = w.a_tok[g0 + (tt < nt ? tt : 0)];
           const size_t hrow = (size_t)(code >> 8) * (k + 1) + (code & 255);
-          hr[tt] = w.hc + hrow * f;
-          hsr[tt] = w.hs + hrow * nb;
+          hr[tt] = hc + hrow * f;
+          hsr[tt] = hs + hrow * nb;
         }
         float s[kTokGroup][NC] = {};
 #pragma unroll
@@ -759,13 +788,32 @@ cudaError_t launch_decode_quant_h_mx(const Layer& L, int B, void* ws, cudaStream
   return launch_pdl(decode_quant_h_kernel, (nblocks + 255) / 256, 256, 0, s, nblocks, w);
 }
 
+// Shared memory of the MXFP8 down kernel that stages h, in bytes.
+size_t down_mx_stage_bytes(const Layer& L, int B) {
+  constexpr int NC = 3;
+  const size_t na = (size_t)B * (L.k + 1);
+  return (((size_t)kDownWarps * B * NC + 3) & ~(size_t)3) * sizeof(float) + na * L.f * 2 + na * (L.f / 32);
+}
+
+bool decode_down_mx_stages_h(const Layer& L, int B) { return down_mx_stage_bytes(L, B) <= 112 * 1024; }
+
 cudaError_t launch_decode_down_mx(const Layer& L, int B, void* y, void* ws, cudaStream_t s) {
   DecodeWs w = carve(L, B, ws);
   // three columns per warp: the d / 24 blocks fit one wave at two blocks per SM
   constexpr int NC = 3;
   const int blocks = (L.d + kDownWarps * NC - 1) / (kDownWarps * NC);
-  return launch_pdl(decode_down_mx_kernel<NC, 2>, blocks, kDownWarps * 32, sizeof(float) * kDownWarps * B * NC, s,
-                    (const uint8_t*)L.Wdq, (const uint8_t*)L.Wds, B, L.d, L.f, L.k, w, (bf16*)y);
+  if (decode_down_mx_stages_h(L, B)) {
+    static bool attr = false;
+    if (!attr) {
+      MOE_TRY(cudaFuncSetAttribute(decode_down_mx_kernel<NC, 2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   112 * 1024));
+      attr = true;
+    }
+    return launch_pdl(decode_down_mx_kernel<NC, 2, true>, blocks, kDownWarps * 32, down_mx_stage_bytes(L, B), s,
+                      (const uint8_t*)L.Wdq, (const uint8_t*)L.Wds, B, L.d, L.f, L.k, w, (bf16*)y);
+  }
+  return launch_pdl(decode_down_mx_kernel<NC, 2, false>, blocks, kDownWarps * 32, sizeof(float) * kDownWarps * B * NC,
+                    s, (const uint8_t*)L.Wdq, (const uint8_t*)L.Wds, B, L.d, L.f, L.k, w, (bf16*)y);
 }
 
 cudaError_t launch_decode_down(const Layer& L, int B, void* y, void* ws, cudaStream_t s) {

@@ -135,6 +135,7 @@ cudaError_t launch_decode_down(const Layer& L, int B, void* y, void* ws, cudaStr
 cudaError_t launch_decode_gateup_mx(const Layer& L, int B, void* ws, cudaStream_t s);
 cudaError_t launch_decode_quant_h_mx(const Layer& L, int B, void* ws, cudaStream_t s);
 cudaError_t launch_decode_down_mx(const Layer& L, int B, void* y, void* ws, cudaStream_t s);
+bool decode_down_mx_stages_h(const Layer& L, int B);   // the down kernel quantises h itself (no h quantiser)
 // tc_gemm.cu (bf16 tcgen05 path)
 bool tc_supported(const Layer& L);
 cudaError_t tc_init(Layer& L);   // encodes the weight tensor maps, sets kernel attributes
