@@ -28,8 +28,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ o, c
   float acc[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) acc[i] = 0.f;
-  auto add_row = [&](long row) {
-    const uint4 u = *reinterpret_cast<const uint4*>(o + row * d + c);
+  auto add_row = [&](const uint4& u) {
     if constexpr (sizeof(T) == 2) {
       float f[8];
       unpack8(u, f);
@@ -42,8 +41,19 @@ __global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ o, c
       acc[3] += __uint_as_float(u.w);
     }
   };
-  if (S) add_row(A + t);
-  for (int j = 0; j < k; ++j) add_row(inv[(long)t * k + j]);
+  // every row's load goes out before the first add (the sum keeps its order: shared, then j)
+  int rows[kMaxK];
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) rows[j] = j < k ? inv[(long)t * k + j] : 0;
+  uint4 v[kMaxK + 1];
+  if (S) v[kMaxK] = *reinterpret_cast<const uint4*>(o + (long)(A + t) * d + c);
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j)
+    if (j < k) v[j] = *reinterpret_cast<const uint4*>(o + (long)rows[j] * d + c);
+  if (S) add_row(v[kMaxK]);
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j)
+    if (j < k) add_row(v[j]);
   uint4 out;
   if constexpr (sizeof(T) == 2) {
     out = pack8(acc);
