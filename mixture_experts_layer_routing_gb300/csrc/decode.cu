@@ -38,8 +38,6 @@ namespace {
 
 struct DecodeWs {
   float* logits;   // [B, E]
-  int* idx;        // [B, k]
-  float* gate;     // [B, k]
   int* nU;         // [1]
   int* U;          // [E + 1]   experts in use, ascending, shared expert (E) last
   int* u_off;      // [E + 2]   token-list offsets per U entry
@@ -61,8 +59,6 @@ DecodeWs carve(const Layer& L, int B, void* ws) {
   DecodeWs w;
   const int na = B * L.k + B;
   w.logits = (float*)p; p += al(sizeof(float) * B * L.E);
-  w.idx = (int*)p; p += al(sizeof(int) * B * L.k);
-  w.gate = (float*)p; p += al(sizeof(float) * B * L.k);
   w.nU = (int*)p; p += al(sizeof(int));
   w.U = (int*)p; p += al(sizeof(int) * (L.E + 1));
   w.u_off = (int*)p; p += al(sizeof(int) * (L.E + 2));
@@ -169,9 +165,11 @@ __global__ void __launch_bounds__(kRouteWarps * 32) decode_route_kernel(
   __syncthreads();
   if (!last) return;
   __threadfence();
+  // the selection stays in shared memory: only this block reads it
+  __shared__ int s_idx[kMaxDecodeB * kMaxK];
+  __shared__ float s_gate[kMaxDecodeB * kMaxK];
   for (int t = wib; t < B; t += kRouteWarps)
-    warp_topk_gates(w.logits + (size_t)t * E, bias, E, k, router, renorm, scale, w.idx + (size_t)t * k,
-                    w.gate + (size_t)t * k);
+    warp_topk_gates(w.logits + (size_t)t * E, bias, E, k, router, renorm, scale, s_idx + t * k, s_gate + t * k);
   __syncthreads();
   // experts in use and their token lists (stable: ascending assignment); thread e owns expert e
   __shared__ int cnt[kMaxE + 1];
@@ -180,7 +178,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) decode_route_kernel(
   for (int e = threadIdx.x; e <= E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
   const int A = B * k;
-  for (int a = threadIdx.x; a < A; a += blockDim.x) atomicAdd(&cnt[__ldcg(w.idx + a)], 1);
+  for (int a = threadIdx.x; a < A; a += blockDim.x) atomicAdd(&cnt[s_idx[a]], 1);
   __syncthreads();
   {
     // block-wide exclusive scans of (expert used, its count) over e = threadIdx.x < E
@@ -232,12 +230,12 @@ __global__ void __launch_bounds__(kRouteWarps * 32) decode_route_kernel(
   }
   __syncthreads();
   for (int a = threadIdx.x; a < A; a += blockDim.x) {
-    const int e = __ldcg(w.idx + a);
+    const int e = s_idx[a];
     int rank = 0;
-    for (int q = 0; q < a; ++q) rank += (__ldcg(w.idx + q) == e);
+    for (int q = 0; q < a; ++q) rank += (s_idx[q] == e);
     const int pos = start[e] + rank;
     w.a_tok[pos] = ((a / k) << 8) | (a % k);
-    w.a_gate[pos] = __ldcg(w.gate + a);
+    w.a_gate[pos] = s_gate[a];
   }
   if (S)
     for (int t = threadIdx.x; t < B; t += blockDim.x) {
@@ -743,7 +741,7 @@ __global__ void __launch_bounds__(kDownWarps * 32) decode_down_mx_kernel(const u
 
 size_t decode_workspace_bytes(const Layer& L, int B) {
   const int na = B * L.k + B;
-  size_t z = al(sizeof(float) * B * L.E) + al(sizeof(int) * B * L.k) + al(sizeof(float) * B * L.k) + al(sizeof(int)) +
+  size_t z = al(sizeof(float) * B * L.E) + al(sizeof(int)) +
              al(sizeof(int) * (L.E + 1)) + al(sizeof(int) * (L.E + 2)) + al(sizeof(int) * na) +
              al(sizeof(float) * na) + al(sizeof(float) * B * (L.k + 1) * L.f);
   if (L.prec == MOE_MXFP8)
