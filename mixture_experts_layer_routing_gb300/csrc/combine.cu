@@ -81,11 +81,15 @@ __global__ void __launch_bounds__(256) router_dl_kernel(const float* __restrict_
   float dg[kMaxK], g[kMaxK], l[kMaxK];
   int ex[kMaxK];
   float dot = 0.f;
+  // lane j sums slot j's partials (in order; their loads batched), then every lane takes all k
+  float own = 0.f;
+  if (lane < k) {
+    const float* dp = dg_part + (long)inv[(long)t * k + lane] * nslots;
+#pragma unroll 8
+    for (int q = 0; q < nslots; ++q) own += dp[q];
+  }
   for (int j = 0; j < k; ++j) {
-    const long p = inv[(long)t * k + j];
-    float s = 0.f;
-    for (int q = 0; q < nslots; ++q) s += dg_part[p * nslots + q];
-    dg[j] = s;
+    dg[j] = __shfl_sync(0xffffffffu, own, j);
     g[j] = gate[(long)t * k + j];
     ex[j] = idx[(long)t * k + j];
     l[j] = logits[(long)t * E + ex[j]];
@@ -168,7 +172,7 @@ __global__ void __launch_bounds__(256) router_dw_seg_kernel(const float* __restr
 #pragma unroll
   for (int i = 0; i < V; ++i) acc[i] = 0.f;
   if (c < d) {
-#pragma unroll 4
+#pragma unroll 8
     for (int p = p0 + sp + ns * w; p < p1; p += ns * 8) {
       const int t = perm[p] / k;
       const float g = dl[(long)t * E + e];
