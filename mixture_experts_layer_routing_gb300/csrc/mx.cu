@@ -674,9 +674,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
 }
 
 // One 128 x 128 weight-gradient tile (expert e, row tile m, column tile n) from TMEM to the output,
-// by the four epilogue warps (warp ew: rows 32 ew .. 32 ew + 31), each through its two 4 KB staging
-// buffers (128-byte swizzled, stored by TMA: whole lines). nkb == 0: the expert had no token rows; the
-// tile is zero (or left as it was, accumulating).
+// by the four epilogue warps (warp ew: rows 32 ew .. 32 ew + 31), each staging its two 32 x 64
+// sub-tiles (128-byte swizzled, 4 KB each, back to back) and storing both with one TMA operation (a
+// 64 x 32 x 2 box of the chunked view of the output; half the store operations of one per sub-tile).
+// nkb == 0: the expert had no token rows; the tile is zero (or left as it was, accumulating).
 template <int EPI>
 __device__ __forceinline__ void wgrad_tile_store(const MxParams& p, const CUtensorMap* tmC, const CUtensorMap* tmC2,
                                                  uint32_t wbuf, uint32_t tbase, int e, int m, int n, int nkb, int ew,
@@ -692,9 +693,12 @@ __device__ __forceinline__ void wgrad_tile_store(const MxParams& p, const CUtens
   } else {
     orow0 = (e * p.m_tiles + m) * MBM + ew * 32;
   }
+  // the warp's previous store must have finished reading the staging
+  if (lane == 0) bulk_wait_read<0>();
+  __syncwarp();
 #pragma unroll 1
   for (int c0 = 0; c0 < MBN; c0 += 64) {
-    const uint32_t buf = wbuf + ((c0 >> 6) & 1) * 4096;
+    const uint32_t buf = wbuf + (c0 >> 6) * 4096;
     float of[64];
     if (!empty) {
       uint32_t a[32], b[32];
@@ -721,9 +725,6 @@ __device__ __forceinline__ void wgrad_tile_store(const MxParams& p, const CUtens
         for (int i = 0; i < 8; ++i) of[q * 8 + i] += o8[i];
       }
     }
-    // the store that last read this buffer (two sub-tiles ago) must have finished reading it
-    if (lane == 0) bulk_wait_read<1>();
-    __syncwarp();
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const uint4 v = pack8(of + q * 8);
@@ -731,12 +732,12 @@ __device__ __forceinline__ void wgrad_tile_store(const MxParams& p, const CUtens
                    "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                    : "memory");
     }
-    fence_proxy_async();
-    __syncwarp();
-    if (lane == 0) {
-      tma_store_2d_hint(tmo, n * MBN + c0, orow0, buf, policy_evict_first());
-      bulk_commit();
-    }
+  }
+  fence_proxy_async();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_3d_hint(tmo, 0, orow0, n * (MBN / 64), wbuf, policy_evict_first());
+    bulk_commit();
   }
 }
 
@@ -1216,7 +1217,8 @@ cudaError_t launch_mx_bwd_dw13(const Layer& L, const Bufs& B, void* dWg, void* d
   p.accumulate = acc ? 1 : 0;
   const uint64_t nseg = L.E + L.S;
   CUtensorMap tg, tu;
-  if (!make_tmap(&tg, dWg, L.d, nseg * L.f, 64, 32) || !make_tmap(&tu, dWu, L.d, nseg * L.f, 64, 32))
+  if (!make_tmap_chunked(&tg, dWg, L.d, nseg * L.f, 32, MBN / 64) ||
+      !make_tmap_chunked(&tu, dWu, L.d, nseg * L.f, 32, MBN / 64))
     return cudaErrorInvalidValue;
   return wg_launch<ME_DW13>(ta, tb, p, L.num_sms, s, tg, tu);
 }
@@ -1237,7 +1239,7 @@ cudaError_t launch_mx_bwd_dwd(const Layer& L, const Bufs& B, void* dWd, bool acc
   p.k32 = B.tok_k32;
   p.accumulate = acc ? 1 : 0;
   CUtensorMap td;
-  if (!make_tmap(&td, dWd, L.f, (uint64_t)(L.E + L.S) * L.d, 64, 32)) return cudaErrorInvalidValue;
+  if (!make_tmap_chunked(&td, dWd, L.f, (uint64_t)(L.E + L.S) * L.d, 32, MBN / 64)) return cudaErrorInvalidValue;
   return wg_launch<ME_DWD>(ta, tb, p, L.num_sms, s, td, td);
 }
 

@@ -89,6 +89,14 @@ __device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* tm, int c0,
                "r"(c0), "r"(c1), "r"(src), "l"(pol)
                : "memory");
 }
+__device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap* tm, int c0, int c1, int c2, uint32_t src,
+                                                  uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2, %3}], [%4], %5;" ::"l"(
+          reinterpret_cast<uint64_t>(tm)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(src), "l"(pol)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() {
@@ -256,6 +264,22 @@ bool make_tmap(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+
+// bf16 [rows][W] (W contiguous) seen as [W / 64 chunks][rows][64]: box 64 columns x box_rows rows x
+// box_chunks chunks, 128-byte swizzle, so that a store covers several 64-column sub-tiles of the same
+// rows (staged as consecutive 128-byte-swizzled sub-tiles) in one operation.
+bool make_tmap_chunked(CUtensorMap* tm, const void* base, uint64_t W, uint64_t rows, uint32_t box_rows,
+                       uint32_t box_chunks) {
+  auto fn = encode_fn();
+  if (!fn || W % 64) return false;
+  cuuint64_t dims[3] = {64, rows, W / 64};
+  cuuint64_t strides[2] = {W * 2, 128};
+  cuuint32_t box[3] = {64, box_rows, box_chunks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 }  // namespace
 }  // namespace moe
