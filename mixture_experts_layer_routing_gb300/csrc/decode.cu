@@ -15,10 +15,13 @@
 //   gate/up   warp per (expert in U, row i): streams Wg[e][i,:] and Wu[e][i,:]
 //             once with 16-byte coalesced loads and produces h[t, slot, i] =
 //             silu(u) v in fp32 for every token routed to e.
-//   down      warp per pair of output columns c: for each e in U ascending,
-//             streams Wd[e][c,:] once and adds gate * (h . w) to each token's
-//             fp32 accumulator; y[:, c] is written once. No atomics.
-// Intermediates stay fp32 (h is never rounded to bf16).
+//   down      warp per two (bf16) or three (MXFP8) output columns c: for each
+//             e in U ascending, streams Wd[e][c,:] once and adds gate * (h . w)
+//             to each token's fp32 accumulator; y[:, c] is written once. No
+//             atomics.
+// Intermediates stay fp32 (h is never rounded to bf16). The kernels are bound
+// by the weight bytes each warp keeps in flight, so a single-token batch runs
+// shapes that spend the registers of a token group on deeper load batches.
 //
 // MXFP8 layers decode the same way on their E4M3 weights (one E8M0 scale per
 // 32 values along each product's K): x is quantised along d and h along f
