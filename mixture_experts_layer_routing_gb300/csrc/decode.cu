@@ -250,9 +250,9 @@ __global__ void __launch_bounds__(kRouteWarps * 32) decode_route_kernel(
 constexpr int kTokGroup = 4;
 
 // One warp per (U entry, row i) item, grid-stride over items. Each lane loads
-// kBatch 16-byte chunks of both weight rows before using any of them.
-// TG tokens of an expert per pass, NB 16-byte chunks per lane per row in flight: (4, NB) in
-// general, (1, 10) for single tokens, where the registers of the token group go to a deeper batch.
+// NB 16-byte chunks of both weight rows before using any of them; TG tokens of
+// the expert per pass. Launched as (kTokGroup, kBatch), and as (1, 10) for a
+// single token, where the registers of the token group go to a deeper batch.
 template <int TG, int NB>
 __global__ void __launch_bounds__(256, 2) decode_gateup_kernel(const bf16* __restrict__ x, const bf16* __restrict__ W13,
                                                             int d, int f, int G, int k, int E, int S, DecodeWs w) {
