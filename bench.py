@@ -952,7 +952,8 @@ PROFILE_CASES = {
     "dsv3_e32_bf16_fwd_t1024": (moe_synth.DSV3_UNIFORM.with_(name="dsv3_e32_T1024", E=32, T=1024, seed=9), "fwd", 1024),
     "dsv3_e32_bf16_fwd_t1024_rowtiles2": (moe_synth.DSV3_UNIFORM.with_(name="dsv3_e32_T1024", E=32, T=1024, seed=9),
                                           "fwd_rowtiles2", 1024),
-    # MXFP8 decode at B = 1 (the warp-per-output kernels; from B = 4 moe_decode takes the grouped GEMMs)
+    # decode at B = 1 (the warp-per-output kernels; from B = 4 moe_decode takes the grouped GEMMs)
+    "dsv3_e32_bf16_decode_b1": (moe_synth.DSV3_UNIFORM.with_(name="dsv3_e32_bf16", E=32, T=64, seed=12), "decode", 1),
     "dsv3_e32_mxfp8_decode_b1": (moe_synth.DSV3_MXFP8.with_(name="dsv3_e32_mxfp8", E=32, T=64, chunk=0, seed=12),
                                  "decode", 1),
     # 256 + 1 experts and four 1024-token chunks: ~4 token-axis K groups per expert in the weight gradients, as in
