@@ -422,7 +422,6 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
     return MOE_ERR_CUDA;
   }
   L.status = words;
-  L.decode_counter = words + 32;
   L.dep_done = (unsigned*)(words + 64);   // 8 words: see Layer::dep_done
   L.dep = (unsigned*)(words + 72);
   L.dep_len = (int)max_mtiles;
@@ -713,7 +712,7 @@ moe_status moe_decode(moe_handle h, const void* x, int B, void* y, void* workspa
   // from the crossover batch on, the tensor-core grouped GEMMs beat the warp-per-output kernels
   // (their per-token FMA work grows with B; the GEMMs read each expert's weights once)
   if (B >= h->decode_gemm_from && (h->tc || h->mx)) return forward_body(h, x, B, y, nullptr, workspace, s);
-  CK(run(h, s, G_DECODE_ROUTE, 1, [&] { return launch_decode_route(L, x, B, workspace, s); }));
+  CK(run(h, s, G_DECODE_ROUTE, 2, [&] { return launch_decode_route(L, x, B, workspace, s); }));
   if (L.prec == MOE_MXFP8) {
     CK(run(h, s, G_DECODE_GATEUP, 1, [&] { return launch_decode_gateup_mx(L, B, workspace, s); }));
     // at small B the down kernel quantises h itself (into shared memory)

@@ -9,9 +9,10 @@
 // Here:
 //   route     one to eight warps per (token, expert) router logit (split along d
 //             when B x E is small, so that every SM streams part of Wr; the
-//             partial sums are added in warp order); the last block to finish
-//             selects the top-k of every token and lists the used experts U
-//             (ascending, the shared expert last) with their tokens.
+//             partial sums are added in warp order); then one block (launched
+//             ahead, programmatic dependent launch) selects the top-k of every
+//             token and lists the used experts U (ascending, the shared expert
+//             last) with their tokens.
 //   gate/up   warp per (expert in U, row i): streams Wg[e][i,:] and Wu[e][i,:]
 //             once with 16-byte coalesced loads and produces h[t, slot, i] =
 //             silu(u) v in fp32 for every token routed to e.
@@ -112,9 +113,9 @@ __device__ __forceinline__ void quant_x_block(const bf16* __restrict__ x, int b,
 constexpr int kRouteWarps = 8;
 constexpr int kBatch = 7;   // 16-byte chunks per lane loaded before they are used
 
-__global__ void __launch_bounds__(kRouteWarps * 32) decode_route_kernel(
-    const bf16* __restrict__ x, const bf16* __restrict__ Wr, const float* __restrict__ bias, int B, int d, int E,
-    int k, int S, int router, int renorm, float scale, int parts, DecodeWs w, int* counter, int quant_x) {
+__global__ void __launch_bounds__(kRouteWarps * 32) decode_logits_kernel(const bf16* __restrict__ x,
+                                                                       const bf16* __restrict__ Wr, int B, int d,
+                                                                       int E, int parts, DecodeWs w, int quant_x) {
   griddep_launch();
   // MXFP8 layers: the blocks also quantise x along d for the gate/up kernel (one launch fewer)
   if (quant_x)
@@ -160,14 +161,18 @@ __global__ void __launch_bounds__(kRouteWarps * 32) decode_route_kernel(
     for (int q = 1; q < parts; ++q) sum += red[wib + q];
     w.logits[item] = sum;
   }
-  // last block to finish selects experts for every token
-  __shared__ int last;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) last = (atomicAdd(counter, 1) == (int)gridDim.x - 1);
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
+}
+
+// One block: selects the top-k of every token from the logits and lists the used experts U
+// (ascending, the shared expert last) with their tokens. Launched after decode_logits_kernel with
+// programmatic dependent launch, so it is resident before the logits are complete and starts when
+// they are.
+__global__ void __launch_bounds__(kRouteWarps * 32) decode_select_kernel(const float* __restrict__ bias, int B, int E,
+                                                                       int k, int S, int router, int renorm,
+                                                                       float scale, DecodeWs w) {
+  griddep_launch();
+  griddep_wait();
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   // the selection stays in shared memory: only this block reads it
   __shared__ int s_idx[kMaxDecodeB * kMaxK];
   __shared__ float s_gate[kMaxDecodeB * kMaxK];
@@ -228,7 +233,6 @@ __global__ void __launch_bounds__(kRouteWarps * 32) decode_route_kernel(
       }
       w.u_off[nU] = r0;
       *w.nU = nU;
-      *counter = 0;                         // ready for the next call
     }
   }
   __syncthreads();
@@ -246,6 +250,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) decode_route_kernel(
       w.a_gate[start[E] + t] = 1.0f;
     }
 }
+
 
 constexpr int kTokGroup = 4;
 
@@ -760,10 +765,11 @@ cudaError_t launch_decode_route(const Layer& L, const void* x, int B, void* ws, 
   while (parts < kRouteWarps && (long)B * L.E * parts * 2 <= (long)L.num_sms * kRouteWarps) parts *= 2;
   const int items_per_block = kRouteWarps / parts;
   const int route_blocks = (B * L.E + items_per_block - 1) / items_per_block;
-  decode_route_kernel<<<route_blocks, kRouteWarps * 32, 0, s>>>((const bf16*)x, (const bf16*)L.Wr, L.bias, B, L.d,
-                                                                L.E, L.k, L.S, L.router, L.renorm, L.scale, parts, w,
-                                                                L.decode_counter, L.prec == MOE_MXFP8 ? 1 : 0);
-  return cudaGetLastError();
+  decode_logits_kernel<<<route_blocks, kRouteWarps * 32, 0, s>>>((const bf16*)x, (const bf16*)L.Wr, B, L.d, L.E,
+                                                                 parts, w, L.prec == MOE_MXFP8 ? 1 : 0);
+  MOE_TRY(cudaGetLastError());
+  return launch_pdl(decode_select_kernel, 1, kRouteWarps * 32, 0, s, L.bias, B, L.E, L.k, L.S, L.router, L.renorm,
+                    L.scale, w);
 }
 
 cudaError_t launch_decode_gateup(const Layer& L, const void* x, int B, void* ws, cudaStream_t s) {

@@ -36,7 +36,6 @@ struct Layer {
   void* Wr;              // [E][d]
   float* bias;           // [E]
   int* status;           // device status word
-  int* decode_counter;   // device counter of the decode router's last-block election
   int num_sms;
   bool has_weights;
   // tensor maps of the packed weights (bf16 tcgen05 path)
