@@ -261,7 +261,6 @@ constexpr int kTokGroup = 4;
 template <int TG, int NB>
 __global__ void __launch_bounds__(256, 2) decode_gateup_kernel(const bf16* __restrict__ x, const bf16* __restrict__ W13,
                                                             int d, int f, int G, int k, int E, int S, DecodeWs w) {
-  griddep_launch();
   // The shared expert is used by every token whatever the routing: while the
   // router still runs, pull its gate/up rows into L2 (each block one slice).
   if (S && threadIdx.x == 0) {
@@ -278,6 +277,8 @@ __global__ void __launch_bounds__(256, 2) decode_gateup_kernel(const bf16* __res
     }
   }
   griddep_wait();
+  // the next kernel may launch once every block is past the routing (it reads the lists early)
+  griddep_launch();
   const int lane = threadIdx.x & 31;
   const int nU = *w.nU;
   const int items = nU * f;
@@ -368,17 +369,20 @@ __global__ void __launch_bounds__(kDownWarps * 32) decode_down_kernel(const bf16
                                                                       int k, DecodeWs w, bf16* __restrict__ y) {
   extern __shared__ float acc_s[];   // [kDownWarps][B][kCols]
   griddep_launch();
-  griddep_wait();
+  // The routing lists are complete once this grid runs (the gate/up kernel lets it launch only
+  // after its own wait on the routing), so the first expert's rows go out before waiting for h.
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   float* acc = acc_s + (size_t)wib * B * kCols;
-  const int nU = *w.nU;
+  const int nU = __ldcg(w.nU);
   const int c0 = (blockIdx.x * kDownWarps + wib) * kCols;
   if (c0 >= d) return;
+  uint4 wcur[kCols][kFChunks], wnext[kCols][kFChunks];
+  load_wd(Wd, __ldcg(w.U), d, f, c0, 0, lane, wnext);
+  griddep_wait();
   for (int q = lane; q < B * kCols; q += 32) acc[q] = 0.f;
   __syncwarp();
   for (int f0 = 0; f0 < f; f0 += 32 * kFChunks * 8) {
-    uint4 wcur[kCols][kFChunks], wnext[kCols][kFChunks];
-    load_wd(Wd, w.U[0], d, f, c0, f0, lane, wnext);
+    if (f0 > 0) load_wd(Wd, w.U[0], d, f, c0, f0, lane, wnext);
     for (int ui = 0; ui < nU; ++ui) {
 #pragma unroll
       for (int cc = 0; cc < kCols; ++cc)
@@ -468,7 +472,6 @@ template <int TG, int NB>
 __global__ void __launch_bounds__(256, 2) decode_gateup_mx_kernel(const uint8_t* __restrict__ W13q,
                                                                const uint8_t* __restrict__ W13s, int d, int f, int G,
                                                                int k, int E, int S, DecodeWs w) {
-  griddep_launch();
   if (S && threadIdx.x == 0) {   // the shared expert's rows into L2 while the router runs
     const size_t bytes = (size_t)2 * f * d;
     const size_t slice = ((bytes + gridDim.x - 1) / gridDim.x + 15) & ~(size_t)15;
@@ -483,6 +486,8 @@ __global__ void __launch_bounds__(256, 2) decode_gateup_mx_kernel(const uint8_t*
     }
   }
   griddep_wait();
+  // the next kernel may launch once every block is past the routing (it reads the lists early)
+  griddep_launch();
   const int lane = threadIdx.x & 31;
   const int nU = *w.nU;
   const int items = nU * f;
@@ -612,15 +617,17 @@ __global__ void __launch_bounds__(kDownWarps * 32) decode_down_mx_kernel(const u
                                                                          bf16* __restrict__ y) {
   extern __shared__ __align__(16) float acc_s[];   // [kDownWarps][B][NC], then (STAGE) h codes and scales
   griddep_launch();
-  griddep_wait();
+  // The routing lists are complete once this grid runs (its predecessors let it launch only after
+  // their own waits on the routing), so the first expert's rows go out before waiting for h.
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   float* acc = acc_s + (size_t)wib * B * NC;
-  const int nU = *w.nU;
+  const int nU = __ldcg(w.nU);
   const int c0 = (blockIdx.x * kDownWarps + wib) * NC;
   const int nb = f / 32;
   uint4 wcur[NC][FC], wnext[NC][FC];
   uint32_t scur[NC][FC], snext[NC][FC];
-  if (c0 < d) load_wd_mx<NC, FC>(Wdq, Wds, w.U[0], d, f, c0, 0, lane, wnext, snext);
+  if (c0 < d) load_wd_mx<NC, FC>(Wdq, Wds, __ldcg(w.U), d, f, c0, 0, lane, wnext, snext);
+  griddep_wait();
   const uint16_t* hc = w.hc;
   const uint8_t* hs = w.hs;
   if (STAGE) {
