@@ -763,8 +763,22 @@ constexpr int kWgSmem = kWgScaleRegion + (kWgA + kWgB) * kWgStage + kWgOut + 102
 static_assert(kWgSmem <= 227 * 1024, "shared memory per CTA");
 constexpr int kWgScaleColA = 2 * MBN, kWgScaleColB = kWgScaleColA + 4 * kWgKG * kWgA;   // TMEM scale columns
 
+// Roles: warp 0 issues the TMA loads, warps 1-4 are the epilogue, warp 5 issues the scale copies and
+// MMAs, warp 6 tests the ring's full barriers. A test of an mbarrier in the MMA-issuing thread while the
+// tensor pipe runs costs a few hundred cycles of idle pipe (the pipe queues only ~1.5 MMAs of work), so
+// that thread never tests one: the waiter warp tests the stage's barriers and hands the stage over on a
+// named barrier (ids 1-3, one per B slot), and the epilogue hands back each accumulator on another (ids
+// 4-5). Both hand-overs are rendezvous (bar.sync on both sides), so no side runs more than one use ahead;
+// after a failed wait a role stops waiting but still takes part in every rendezvous, so none is left
+// waiting on a named barrier.
+constexpr int kWgWaitWarp = kMxMmaWarp + 1;
+constexpr int kWgThreads = (kWgWaitWarp + 1) * 32;
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 template <int EPI>
-__global__ void __launch_bounds__(kMxThreads, 1)
+__global__ void __launch_bounds__(kWgThreads, 1)
     mx_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2, MxParams p) {
   griddep_wait();    // after the predecessor grid (launch.cuh)
@@ -777,8 +791,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   uint64_t* bars = (uint64_t*)(out_stage + kWgOut);
   const uint32_t afull0 = smem_u32(bars), aempty0 = smem_u32(bars + kWgA);
   const uint32_t bfull0 = smem_u32(bars + 2 * kWgA), bempty0 = smem_u32(bars + 2 * kWgA + kWgB);
-  const uint32_t tfull0 = smem_u32(bars + 2 * kWgA + 2 * kWgB), tempty0 = tfull0 + 16;
-  const uint32_t drain = tfull0 + 32;
+  const uint32_t tfull0 = smem_u32(bars + 2 * kWgA + 2 * kWgB);
+  const uint32_t drain = tfull0 + 16;
   volatile int* abort_flag = (volatile int*)(bars + 2 * kWgA + 2 * kWgB + 5);
   uint32_t* tmem_slot = (uint32_t*)(bars + 2 * kWgA + 2 * kWgB + 6);
   int* s_mt = (int*)(smem_raw + kWgSmem - kSegCache);   // [kMaxE + 2]: the 128-row block prefix
@@ -793,10 +807,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       mbar_init(bfull0 + 8 * i, 1);
       mbar_init(bempty0 + 8 * i, 1);
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, kEpi * 32);
-    }
+    for (int a = 0; a < 2; ++a) mbar_init(tfull0 + 8 * a, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -812,6 +823,9 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   const int units = p.nseg * p.m_tiles;
   const int nt = p.n_tiles;
+  // the column tiles this CTA computes (every role walks the same units, tiles and stages)
+  const int cta_tiles = (blockIdx.x < units ? (units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0) * nt;
+  constexpr int kEpiSync = kEpi * 32 + 32;   // the epilogue warps and the MMA warp
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (one thread)
@@ -861,50 +875,55 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == kMxMmaWarp) {
-    // ----------------------------------------------------------------- MMA
-    if (lane == 0) {
-      int ait = 0, bit = 0, tcount = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const int e = u / p.m_tiles;
-        const int nkb = s_mt[e + 1] - s_mt[e];
-        const int nst = (nkb + kWgKG - 1) / kWgKG;
-        const bool resident = nst <= kWgA;
-        const int k32 = p.k32 ? p.k32[e] : 4 * nkb;   // 32-row K blocks that hold rows
-        const int ait0 = ait;
-        for (int i = 0; i < nt && ok; ++i, ++tcount) {
-          const int acc = tcount & 1;
-          if (!mbar_wait(tempty0 + 8 * acc, ((tcount >> 1) & 1) ^ 1, abort_flag, p.status)) {
-            ok = false;
-            break;
+  } else if (warp == kWgWaitWarp) {
+    // ------------------------------------------------ waiter: a stage's operands landed -> the MMA warp
+    int ait = 0, bit = 0;
+    bool dead = false;   // after a failed wait: no more waiting, every rendezvous still made
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const int e = u / p.m_tiles;
+      const int nkb = s_mt[e + 1] - s_mt[e];
+      const int nst = (nkb + kWgKG - 1) / kWgKG;
+      const bool resident = nst <= kWgA;
+      for (int i = 0; i < nt; ++i) {
+        for (int st = 0; st < nst; ++st) {
+          if (lane == 0 && !dead) {
+            if (!resident || i == 0) dead = !mbar_wait(afull0 + 8 * (ait % kWgA), (ait / kWgA) & 1, abort_flag, p.status);
+            if (!dead) dead = !mbar_wait(bfull0 + 8 * (bit % kWgB), (bit / kWgB) & 1, abort_flag, p.status);
           }
-          tc_fence_after();
-          const uint32_t dcol = tmem_base + acc * MBN;
-          for (int st = 0; st < nst; ++st) {
-            const int ng = min(kWgKG, nkb - st * kWgKG);
-            int as;
-            if (!resident || i == 0) {
-              as = ait % kWgA;
-              if (!mbar_wait(afull0 + 8 * as, (ait / kWgA) & 1, abort_flag, p.status)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              // the stage's A scales stay in these TMEM columns for every column tile of the unit
+          if (!resident || i == 0) ++ait;
+          __syncwarp();
+          named_sync(1 + bit % kWgB, 64);
+          ++bit;
+        }
+      }
+    }
+  } else if (warp == kMxMmaWarp) {
+    // ----------------------------------------------------------------- MMA (lane 0 issues)
+    int ait = 0, bit = 0, tcount = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const int e = u / p.m_tiles;
+      const int nkb = s_mt[e + 1] - s_mt[e];
+      const int nst = (nkb + kWgKG - 1) / kWgKG;
+      const bool resident = nst <= kWgA;
+      const int k32 = p.k32 ? p.k32[e] : 4 * nkb;   // 32-row K blocks that hold rows
+      const int ait0 = ait;
+      for (int i = 0; i < nt; ++i, ++tcount) {
+        const int acc = tcount & 1;
+        if (tcount >= 2) named_sync(4 + acc, kEpiSync);   // the epilogue has read this accumulator
+        const uint32_t dcol = tmem_base + acc * MBN;
+        for (int st = 0; st < nst; ++st) {
+          const int ng = min(kWgKG, nkb - st * kWgKG);
+          const bool load_a = !resident || i == 0;
+          const int as = load_a ? ait % kWgA : (ait0 + st) % kWgA;
+          const int bs = bit % kWgB;
+          named_sync(1 + bs, 64);   // the waiter saw the stage's A (when loaded) and B land
+          if (lane == 0) {
+            tc_fence_after();
+            // the stage's A scales stay in these TMEM columns for every column tile of the unit
+            if (load_a)
               for (int g = 0; g < ng; ++g)
                 tmem_cp_scales(tmem_base + kWgScaleColA + 4 * (as * kWgKG + g),
                                desc_scale_atom(smem_u32(scales + as * kWgAtoms + g * kScaleAtom)));
-              ++ait;
-            } else {
-              as = (ait0 + st) % kWgA;
-            }
-            const int bs = bit % kWgB;
-            if (!mbar_wait(bfull0 + 8 * bs, (bit / kWgB) & 1, abort_flag, p.status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
             for (int g = 0; g < ng; ++g)
               tmem_cp_scales(tmem_base + kWgScaleColB + 4 * (bs * kWgKG + g),
                              desc_scale_atom(smem_u32(scales + (kWgA + bs) * kWgAtoms + g * kScaleAtom)));
@@ -920,14 +939,18 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                          (st > 0 || g > 0 || k > 0) ? 1u : 0u);
             }
             mma_commit(bempty0 + 8 * bs);
-            ++bit;
             // an A stage is released after its last use: the unit's last column tile (resident) or this one
             if (!resident || i == nt - 1) mma_commit(aempty0 + 8 * as);
           }
-          if (!ok) break;
-          mma_commit(tfull0 + 8 * acc);
+          __syncwarp();
+          if (load_a) ++ait;
+          ++bit;
         }
+        if (lane == 0) mma_commit(tfull0 + 8 * acc);
+        __syncwarp();
       }
+    }
+    if (lane == 0) {
       mma_commit(drain);
       const uint64_t t0 = global_ns();
       while (!mbar_try_wait(drain, 0)) {
@@ -943,23 +966,23 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     const int ew = warp & 3;   // TMEM lane quadrant of this warp
     const uint32_t wbuf = smem_u32(out_stage) + ew * 2 * 4096;
     int tcount = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+    bool dead = false;   // after a failed wait: no more waiting or storing, every rendezvous still made
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const int e = u / p.m_tiles, m = u % p.m_tiles;
       const int nkb = s_mt[e + 1] - s_mt[e];
       const int n0 = m * nt / p.m_tiles;
       for (int i = 0; i < nt; ++i, ++tcount) {
         const int n = (n0 + i) % nt;
         const int acc = tcount & 1;
-        if (!mbar_wait(tfull0 + 8 * acc, (tcount >> 1) & 1, abort_flag, p.status)) {
-          ok = false;
-          break;
+        if (!dead) dead = !mbar_wait(tfull0 + 8 * acc, (tcount >> 1) & 1, abort_flag, p.status);
+        if (!dead) {
+          tc_fence_after();
+          wgrad_tile_store<EPI>(p, &tmC, &tmC2, wbuf, tmem_base + acc * MBN + ((uint32_t)(ew * 32) << 16), e, m, n,
+                                nkb, ew, lane);
         }
-        tc_fence_after();
-        wgrad_tile_store<EPI>(p, &tmC, &tmC2, wbuf, tmem_base + acc * MBN + ((uint32_t)(ew * 32) << 16), e, m, n,
-                              nkb, ew, lane);
         tc_fence_before();
-        mbar_arrive(tempty0 + 8 * acc);
+        __syncwarp();
+        if (tcount + 2 < cta_tiles) named_sync(4 + acc, kEpiSync);   // the MMA warp's tile tcount + 2
       }
     }
     // the stores must have read their staging before the CTA exits
@@ -983,7 +1006,7 @@ cudaError_t wg_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const MxPa
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  MOE_TRY(launch_pdl(kern, dim3(grid), dim3(kMxThreads), kWgSmem, s, tmA, tmB, tmC, tmC2, p));
+  MOE_TRY(launch_pdl(kern, dim3(grid), dim3(kWgThreads), kWgSmem, s, tmA, tmB, tmC, tmC2, p));
   return cudaGetLastError();
 }
 
