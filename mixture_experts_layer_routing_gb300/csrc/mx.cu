@@ -50,8 +50,24 @@ constexpr int MBM = 128, MBN = 128, MBK = 128;
 // Warps: 0 the producer (one thread issues every copy), 1-4 the epilogue (warp w reads TMEM lane
 // quadrant w mod 4), 5 the MMA issuer.
 constexpr int kProd = 1, kEpi = 4;
-constexpr int kMxThreads = (kProd + kEpi + 1) * 32;
 constexpr int kMxMmaWarp = kProd + kEpi;
+// Warp 0 issues the TMA loads, warps 1-4 are the epilogue, warp 5 issues the scale copies and MMAs, warp 6
+// tests the ring's full barriers. A test of an mbarrier in the MMA-issuing thread while the tensor pipe runs
+// costs a few hundred cycles of idle pipe (the pipe queues only ~1.5 MMAs of work), so that thread never
+// tests one: the waiter warp tests each stage's barrier and hands the stage over on a named barrier (one id
+// per ring slot), and the epilogue hands back each accumulator on another. Both hand-overs are rendezvous
+// (bar.sync on both sides), so no side runs more than one use ahead; after a failed wait a role stops
+// waiting but still takes part in every rendezvous, so none is left waiting on a named barrier.
+constexpr int kMxWaitWarp = kMxMmaWarp + 1;
+constexpr int kMxThreads = (kMxWaitWarp + 1) * 32;
+constexpr int kEpiSync = kEpi * 32 + 32;   // a rendezvous of the epilogue warps and the MMA warp
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// the CTA's share of n units dealt round-robin over the grid
+__device__ __forceinline__ int cta_share(int n) {
+  return (int)blockIdx.x < n ? (n - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+}
 constexpr int kScaleCol0 = 2 * MBN;                                 // TMEM columns after the two accumulators
 constexpr int kScaleAtom = 512;   // one 128-row operand's scale words for one K block (32 rows x 16 bytes)
 // off[] and the tile prefix mt_off[] (nseg + 1 each), copied to shared memory at kernel start: every
@@ -400,7 +416,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   uint8_t* smem = scales + mx_scale_region<NB>();                                    // stage ring (1024-aligned)
   uint64_t* bars = (uint64_t*)(smem + MSTAGES * kStageBytes);
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + MSTAGES);
-  const uint32_t tfull0 = smem_u32(bars + 2 * MSTAGES), tempty0 = smem_u32(bars + 2 * MSTAGES + 2);
+  const uint32_t tfull0 = smem_u32(bars + 2 * MSTAGES);
   const uint32_t drain = smem_u32(bars + 2 * MSTAGES + 4);
   volatile int* abort_flag = (volatile int*)(bars + 2 * MSTAGES + 5);
   uint32_t* tmem_slot = (uint32_t*)(bars + 2 * MSTAGES + 6);
@@ -416,10 +432,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, kEpi * 32);
-    }
+    for (int a = 0; a < 2; ++a) mbar_init(tfull0 + 8 * a, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -434,6 +447,9 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int ntiles = mx_total<NB>(p, s_mt);
+  const int cta_tiles = cta_share(ntiles);
+  // named barriers: 1 .. MSTAGES hand over the ring's slots, kAccId + acc the accumulators
+  constexpr int kAccId = 1 + MSTAGES;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (one thread)
@@ -474,25 +490,31 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       }
     }
     __syncwarp();
+  } else if (warp == kMxWaitWarp) {
+    // ------------------------------------------------ waiter: a stage's operands landed -> the MMA warp
+    int it = 0;
+    bool dead = false;   // after a failed wait: no more waiting, every rendezvous still made
+    for (int L = blockIdx.x; L < ntiles; L += gridDim.x) {
+      const MTile t = mx_map<NB>(p, L, s_off, s_mt);
+      for (int kb = 0; kb < t.nkb; ++kb, ++it) {
+        const int s = it % MSTAGES;
+        if (lane == 0 && !dead) dead = !mbar_wait(full0 + 8 * s, (it / MSTAGES) & 1, abort_flag, p.status);
+        __syncwarp();
+        named_sync(1 + s, 64);
+      }
+    }
   } else if (warp == kMxMmaWarp) {
-    // ----------------------------------------------------------------- MMA
-    if (lane == 0) {
-      int it = 0, tcount = 0;
-      bool ok = true;
-      for (int L = blockIdx.x; L < ntiles && ok; L += gridDim.x, ++tcount) {
-        const MTile t = mx_map<NB>(p, L, s_off, s_mt);
-        const int acc = tcount % NACC;
-        const uint32_t aph = (tcount / NACC) & 1;
-        if (!mbar_wait(tempty0 + 8 * acc, aph ^ 1, abort_flag, p.status)) break;
-        tc_fence_after();
-        const uint32_t dcol = tmem_base + acc * MBN;
-        for (int kb = 0; kb < t.nkb; ++kb, ++it) {
-          const int s = it % MSTAGES;
-          const uint32_t ph = (it / MSTAGES) & 1;
-          if (!mbar_wait(full0 + 8 * s, ph, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
+    // ----------------------------------------------------------------- MMA (lane 0 issues)
+    int it = 0, tcount = 0;
+    for (int L = blockIdx.x; L < ntiles; L += gridDim.x, ++tcount) {
+      const MTile t = mx_map<NB>(p, L, s_off, s_mt);
+      const int acc = tcount % NACC;
+      if (tcount >= NACC) named_sync(kAccId + acc, kEpiSync);   // the epilogue has read this accumulator
+      const uint32_t dcol = tmem_base + acc * MBN;
+      for (int kb = 0; kb < t.nkb; ++kb, ++it) {
+        const int s = it % MSTAGES;
+        named_sync(1 + s, 64);   // the waiter saw the stage land
+        if (lane == 0) {
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + s * kStageBytes);
           const uint32_t sb = sa + MBM * MBK;
@@ -516,9 +538,12 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           }
           mma_commit(empty0 + 8 * s);
         }
-        if (!ok) break;
-        mma_commit(tfull0 + 8 * acc);
+        __syncwarp();
       }
+      if (lane == 0) mma_commit(tfull0 + 8 * acc);
+      __syncwarp();
+    }
+    if (lane == 0) {
       mma_commit(drain);
       const uint64_t t0 = global_ns();
       while (!mbar_try_wait(drain, 0)) {
@@ -534,15 +559,16 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     const int ew = warp & 3;   // TMEM lane quadrant of this warp
     const int r = ew * 32 + lane;
     int tcount = 0;
+    bool dead = false;   // after a failed wait: no more waiting or storing, every rendezvous still made
     for (int L = blockIdx.x; L < ntiles; L += gridDim.x, ++tcount) {
       const MTile t0 = mx_map<NB>(p, L, s_off, s_mt);
       const int acc = tcount % NACC;
-      const uint32_t aph = (tcount / NACC) & 1;
-      if (!mbar_wait(tfull0 + 8 * acc, aph, abort_flag, p.status)) break;
+      if (!dead) dead = !mbar_wait(tfull0 + 8 * acc, (tcount / NACC) & 1, abort_flag, p.status);
+      dead = __any_sync(0xffffffffu, dead);   // the warp's lanes take the same path (warp-wide shuffles below)
       tc_fence_after();
       // the unit's column tiles (NB = 2: accumulator jb holds column tile t0.n + jb)
 #pragma unroll 1
-      for (int jb = 0; jb < t0.nb; ++jb) {
+      for (int jb = 0; jb < (dead ? 0 : t0.nb); ++jb) {
       MTile t = t0;
       t.n = t0.n + jb;
       const uint32_t tbase = tmem_base + (NB == 2 ? jb : acc) * MBN + ((uint32_t)(ew * 32) << 16);
@@ -662,7 +688,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       }
       }   // column tiles of the unit
       tc_fence_before();
-      mbar_arrive(tempty0 + 8 * acc);
+      __syncwarp();
+      if (tcount + NACC < cta_tiles) named_sync(kAccId + acc, kEpiSync);   // the MMA warp's tile tcount + NACC
     }
   }
   tc_fence_before();
@@ -763,22 +790,10 @@ constexpr int kWgSmem = kWgScaleRegion + (kWgA + kWgB) * kWgStage + kWgOut + 102
 static_assert(kWgSmem <= 227 * 1024, "shared memory per CTA");
 constexpr int kWgScaleColA = 2 * MBN, kWgScaleColB = kWgScaleColA + 4 * kWgKG * kWgA;   // TMEM scale columns
 
-// Roles: warp 0 issues the TMA loads, warps 1-4 are the epilogue, warp 5 issues the scale copies and
-// MMAs, warp 6 tests the ring's full barriers. A test of an mbarrier in the MMA-issuing thread while the
-// tensor pipe runs costs a few hundred cycles of idle pipe (the pipe queues only ~1.5 MMAs of work), so
-// that thread never tests one: the waiter warp tests the stage's barriers and hands the stage over on a
-// named barrier (ids 1-3, one per B slot), and the epilogue hands back each accumulator on another (ids
-// 4-5). Both hand-overs are rendezvous (bar.sync on both sides), so no side runs more than one use ahead;
-// after a failed wait a role stops waiting but still takes part in every rendezvous, so none is left
-// waiting on a named barrier.
-constexpr int kWgWaitWarp = kMxMmaWarp + 1;
-constexpr int kWgThreads = (kWgWaitWarp + 1) * 32;
-__device__ __forceinline__ void named_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
+// Roles as in mx_gemm_kernel; named barriers 1-3 hand over the B ring's slots (a stage's A, when it is
+// loaded, is tested with its B), 4-5 the accumulators.
 template <int EPI>
-__global__ void __launch_bounds__(kWgThreads, 1)
+__global__ void __launch_bounds__(kMxThreads, 1)
     mx_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2, MxParams p) {
   griddep_wait();    // after the predecessor grid (launch.cuh)
@@ -824,8 +839,7 @@ __global__ void __launch_bounds__(kWgThreads, 1)
   const int units = p.nseg * p.m_tiles;
   const int nt = p.n_tiles;
   // the column tiles this CTA computes (every role walks the same units, tiles and stages)
-  const int cta_tiles = (blockIdx.x < units ? (units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0) * nt;
-  constexpr int kEpiSync = kEpi * 32 + 32;   // the epilogue warps and the MMA warp
+  const int cta_tiles = cta_share(units) * nt;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (one thread)
@@ -875,7 +889,7 @@ __global__ void __launch_bounds__(kWgThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == kWgWaitWarp) {
+  } else if (warp == kMxWaitWarp) {
     // ------------------------------------------------ waiter: a stage's operands landed -> the MMA warp
     int ait = 0, bit = 0;
     bool dead = false;   // after a failed wait: no more waiting, every rendezvous still made
@@ -975,6 +989,7 @@ __global__ void __launch_bounds__(kWgThreads, 1)
         const int n = (n0 + i) % nt;
         const int acc = tcount & 1;
         if (!dead) dead = !mbar_wait(tfull0 + 8 * acc, (tcount >> 1) & 1, abort_flag, p.status);
+        dead = __any_sync(0xffffffffu, dead);   // the warp's lanes take the same path
         if (!dead) {
           tc_fence_after();
           wgrad_tile_store<EPI>(p, &tmC, &tmC2, wbuf, tmem_base + acc * MBN + ((uint32_t)(ew * 32) << 16), e, m, n,
@@ -1006,7 +1021,7 @@ cudaError_t wg_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const MxPa
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  MOE_TRY(launch_pdl(kern, dim3(grid), dim3(kWgThreads), kWgSmem, s, tmA, tmB, tmC, tmC2, p));
+  MOE_TRY(launch_pdl(kern, dim3(grid), dim3(kMxThreads), kWgSmem, s, tmA, tmB, tmC, tmC2, p));
   return cudaGetLastError();
 }
 
