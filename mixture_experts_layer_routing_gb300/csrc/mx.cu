@@ -811,8 +811,32 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   volatile int* abort_flag = (volatile int*)(bars + 2 * kWgA + 2 * kWgB + 5);
   uint32_t* tmem_slot = (uint32_t*)(bars + 2 * kWgA + 2 * kWgB + 6);
   int* s_mt = (int*)(smem_raw + kWgSmem - kSegCache);   // [kMaxE + 2]: the 128-row block prefix
+  int* s_uoff = s_mt + kMaxE + 2;                       // [kMaxE + 2]: the units' prefix over segments
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nt = p.n_tiles;
   for (int i = threadIdx.x; i <= p.nseg; i += blockDim.x) s_mt[i] = p.mt_off[i];
+  if (warp == 0) {
+    // units: an A-resident segment has one per row tile (it sweeps every column tile with A held); a
+    // streamed segment (A loaded again for every stage anyway) has one per output tile, so its work is
+    // dealt over all CTAs instead of landing, one row tile each, on m_tiles of them
+    int carry = 0;
+    for (int base = 0; base < p.nseg; base += 32) {
+      const int e = base + lane;
+      int c = 0;
+      if (e < p.nseg) {
+        const int nst = (p.mt_off[e + 1] - p.mt_off[e] + kWgKG - 1) / kWgKG;
+        c = nst <= kWgA ? p.m_tiles : p.m_tiles * nt;
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, c, o);
+        if (lane >= o) c += v;
+      }
+      if (e < p.nseg) s_uoff[e + 1] = carry + c;
+      carry += __shfl_sync(0xffffffffu, c, 31);
+    }
+    if (lane == 0) s_uoff[0] = 0;
+  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kWgA; ++i) {
       mbar_init(afull0 + 8 * i, 1);
@@ -836,10 +860,39 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int units = p.nseg * p.m_tiles;
-  const int nt = p.n_tiles;
+  const int units = s_uoff[p.nseg];
+  // unit u: segment e, row tile m, and its column tiles n0, n0 + 1, ... (mod n_tiles), ntl of them
+  struct Unit {
+    int e, m, nkb, nst, n0, ntl;
+    bool resident;
+  };
+  auto unit = [&](int u) {
+    int lo = 0, hi = p.nseg;   // the segment with s_uoff[e] <= u < s_uoff[e + 1]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_uoff[mid] <= u) lo = mid; else hi = mid;
+    }
+    Unit un;
+    un.e = lo;
+    un.nkb = s_mt[lo + 1] - s_mt[lo];
+    un.nst = (un.nkb + kWgKG - 1) / kWgKG;
+    un.resident = un.nst <= kWgA;
+    const int local = u - s_uoff[lo];
+    if (un.resident) {
+      // the row tiles of one expert start their column sweep at different tiles
+      un.m = local;
+      un.n0 = local * nt / p.m_tiles;
+      un.ntl = nt;
+    } else {
+      un.m = local / nt;
+      un.n0 = local % nt;
+      un.ntl = 1;
+    }
+    return un;
+  };
   // the column tiles this CTA computes (every role walks the same units, tiles and stages)
-  const int cta_tiles = cta_share(units) * nt;
+  int cta_tiles = 0;
+  for (int u = blockIdx.x; u < units; u += gridDim.x) cta_tiles += unit(u).ntl;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (one thread)
@@ -857,13 +910,12 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         }
       };
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const int e = u / p.m_tiles, m = u % p.m_tiles;
-        const int row0 = s_mt[e] * MBK, nkb = s_mt[e + 1] - s_mt[e];
-        const int nst = (nkb + kWgKG - 1) / kWgKG;
-        const bool resident = nst <= kWgA;
-        const int n0 = m * nt / p.m_tiles;
-        for (int i = 0; i < nt && ok; ++i) {
-          const int n = (n0 + i) % nt;
+        const Unit un = unit(u);
+        const int m = un.m, nkb = un.nkb, nst = un.nst;
+        const bool resident = un.resident;
+        const int row0 = s_mt[un.e] * MBK;
+        for (int i = 0; i < un.ntl && ok; ++i) {
+          const int n = (un.n0 + i) % nt;
           for (int st = 0; st < nst; ++st) {
             const int g0 = st * kWgKG, ng = min(kWgKG, nkb - g0);
             if (!resident || i == 0) {
@@ -894,11 +946,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     int ait = 0, bit = 0;
     bool dead = false;   // after a failed wait: no more waiting, every rendezvous still made
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      const int e = u / p.m_tiles;
-      const int nkb = s_mt[e + 1] - s_mt[e];
-      const int nst = (nkb + kWgKG - 1) / kWgKG;
-      const bool resident = nst <= kWgA;
-      for (int i = 0; i < nt; ++i) {
+      const Unit un = unit(u);
+      const int nst = un.nst;
+      const bool resident = un.resident;
+      for (int i = 0; i < un.ntl; ++i) {
         for (int st = 0; st < nst; ++st) {
           if (lane == 0 && !dead) {
             if (!resident || i == 0) dead = !mbar_wait(afull0 + 8 * (ait % kWgA), (ait / kWgA) & 1, abort_flag, p.status);
@@ -915,13 +966,12 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     // ----------------------------------------------------------------- MMA (lane 0 issues)
     int ait = 0, bit = 0, tcount = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      const int e = u / p.m_tiles;
-      const int nkb = s_mt[e + 1] - s_mt[e];
-      const int nst = (nkb + kWgKG - 1) / kWgKG;
-      const bool resident = nst <= kWgA;
-      const int k32 = p.k32 ? p.k32[e] : 4 * nkb;   // 32-row K blocks that hold rows
+      const Unit un = unit(u);
+      const int nkb = un.nkb, nst = un.nst;
+      const bool resident = un.resident;
+      const int k32 = p.k32 ? p.k32[un.e] : 4 * nkb;   // 32-row K blocks that hold rows
       const int ait0 = ait;
-      for (int i = 0; i < nt; ++i, ++tcount) {
+      for (int i = 0; i < un.ntl; ++i, ++tcount) {
         const int acc = tcount & 1;
         if (tcount >= 2) named_sync(4 + acc, kEpiSync);   // the epilogue has read this accumulator
         const uint32_t dcol = tmem_base + acc * MBN;
@@ -954,7 +1004,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             }
             mma_commit(bempty0 + 8 * bs);
             // an A stage is released after its last use: the unit's last column tile (resident) or this one
-            if (!resident || i == nt - 1) mma_commit(aempty0 + 8 * as);
+            if (!resident || i == un.ntl - 1) mma_commit(aempty0 + 8 * as);
           }
           __syncwarp();
           if (load_a) ++ait;
@@ -982,11 +1032,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     int tcount = 0;
     bool dead = false;   // after a failed wait: no more waiting or storing, every rendezvous still made
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      const int e = u / p.m_tiles, m = u % p.m_tiles;
-      const int nkb = s_mt[e + 1] - s_mt[e];
-      const int n0 = m * nt / p.m_tiles;
-      for (int i = 0; i < nt; ++i, ++tcount) {
-        const int n = (n0 + i) % nt;
+      const Unit un = unit(u);
+      const int e = un.e, m = un.m, nkb = un.nkb;
+      for (int i = 0; i < un.ntl; ++i, ++tcount) {
+        const int n = (un.n0 + i) % nt;
         const int acc = tcount & 1;
         if (!dead) dead = !mbar_wait(tfull0 + 8 * acc, (tcount >> 1) & 1, abort_flag, p.status);
         dead = __any_sync(0xffffffffu, dead);   // the warp's lanes take the same path
