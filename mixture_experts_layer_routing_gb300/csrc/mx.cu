@@ -161,8 +161,8 @@ __global__ void __launch_bounds__(256) mx_quant_rows_kernel(const bf16* __restri
   }
 }
 
-// Expert-sorted activation rows: CTA per 128-row tile mt of the routing's tile prefix (mt_off), one
-// warp per row, one lane per 32-element block. Row r of tile mt of segment e is sorted row
+// Expert-sorted activation rows: CTA per 32-row quarter (blockIdx.y) of a 128-row tile mt of the
+// routing's tile prefix (mt_off), one warp per row, one lane per 32-element block. Row r of tile mt of segment e is sorted row
 // off[e] + (mt - mt_off[e]) * 128 + r, the token row_token[...] of src (src_rows = T) or, with
 // row_token null, that row of src itself; its codes go to q[sorted row] and its scales to the tile's
 // atoms. Tile rows past the segment get zero scales (their codes belong to the next segment).
@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(256) mx_quant_sorted_kernel(const bf16* __rest
   __syncthreads();
   if (seg[0] < 0) return;
   const int lane = threadIdx.x & 31;
-  for (int r = threadIdx.x >> 5; r < 128; r += blockDim.x >> 5) {
+  for (int r = blockIdx.y * 32 + (threadIdx.x >> 5); r < (int)(blockIdx.y + 1) * 32; r += blockDim.x >> 5) {
     const long p = (long)seg[1] + r;
     const bool valid = p < seg[2];
     const bf16* sr = valid ? src + (row_token ? (long)row_token[p] : p) * K : nullptr;
@@ -1151,7 +1151,7 @@ cudaError_t launch_mx_quant_sorted(const Layer& L, const Bufs& B, const void* sr
                                    cudaStream_t st) {
   const int nseg = L.E + L.S;
   const long tiles = ((long)B.R + 127L * nseg) / 128 + 1;   // at least the routing's tile count
-  MOE_TRY(launch_pdl(mx_quant_sorted_kernel, dim3((unsigned)tiles), dim3(256), 0, st, (const bf16*)src, B.row_token,
+  MOE_TRY(launch_pdl(mx_quant_sorted_kernel, dim3((unsigned)tiles, 4), dim3(256), 0, st, (const bf16*)src, B.row_token,
       B.off, B.mt_off, nseg, K, q, s));
   return cudaGetLastError();
 }
