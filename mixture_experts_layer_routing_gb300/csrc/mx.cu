@@ -720,12 +720,9 @@ __device__ __forceinline__ void wgrad_tile_store(const MxParams& p, const CUtens
   } else {
     orow0 = (e * p.m_tiles + m) * MBM + ew * 32;
   }
-  // the warp's previous store must have finished reading the staging
-  if (lane == 0) bulk_wait_read<0>();
-  __syncwarp();
 #pragma unroll 1
   for (int c0 = 0; c0 < MBN; c0 += 64) {
-    const uint32_t buf = wbuf + (c0 >> 6) * 4096;
+    const uint32_t buf = wbuf;
     float of[64];
     if (!empty) {
       uint32_t a[32], b[32];
@@ -752,6 +749,9 @@ __device__ __forceinline__ void wgrad_tile_store(const MxParams& p, const CUtens
         for (int i = 0; i < 8; ++i) of[q * 8 + i] += o8[i];
       }
     }
+    // the warp's previous store must have finished reading the staging
+    if (lane == 0) bulk_wait_read<0>();
+    __syncwarp();
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const uint4 v = pack8(of + q * 8);
@@ -759,12 +759,12 @@ __device__ __forceinline__ void wgrad_tile_store(const MxParams& p, const CUtens
                    "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                    : "memory");
     }
-  }
-  fence_proxy_async();
-  __syncwarp();
-  if (lane == 0) {
-    tma_store_3d_hint(tmo, 0, orow0, n * (MBN / 64), wbuf, policy_evict_first());
-    bulk_commit();
+    fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d_hint(tmo, 0, orow0, n * (MBN / 64) + (c0 >> 6), wbuf, policy_evict_first());
+      bulk_commit();
+    }
   }
 }
 
@@ -781,10 +781,10 @@ __device__ __forceinline__ void wgrad_tile_store(const MxParams& p, const CUtens
 // CTAs of one expert start their column sweep at different tiles (row tile m at
 // m * n_tiles / m_tiles), spreading their B requests over the expert's tiles.
 constexpr int kWgKG = 2;            // 128-row K groups per stage (8 MMAs per B stage)
-constexpr int kWgA = 2, kWgB = 3;   // resident A stages (up to kWgA * kWgKG K groups), B ring stages
+constexpr int kWgA = 2, kWgB = 4;   // resident A stages (up to kWgA * kWgKG K groups), B ring stages
 constexpr int kWgStage = kWgKG * MBM * MBK;              // bytes of one operand stage
 constexpr int kWgAtoms = kWgKG * kScaleAtom;             // scale bytes of one operand stage
-constexpr int kWgOut = kEpi * 2 * 32 * 128;              // epilogue staging: two 32 x 64 bf16 sub-tiles per warp
+constexpr int kWgOut = kEpi * 32 * 128;                  // epilogue staging: one 32 x 64 bf16 sub-tile per warp
 constexpr int kWgScaleRegion = ((kWgA + kWgB) * kWgAtoms + 1023) / 1024 * 1024;
 constexpr int kWgSmem = kWgScaleRegion + (kWgA + kWgB) * kWgStage + kWgOut + 1024 + 256 + kSegCache;
 static_assert(kWgSmem <= 227 * 1024, "shared memory per CTA");
@@ -973,7 +973,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       const int ait0 = ait;
       for (int i = 0; i < un.ntl; ++i, ++tcount) {
         const int acc = tcount & 1;
-        if (tcount >= 2) named_sync(4 + acc, kEpiSync);   // the epilogue has read this accumulator
+        if (tcount >= 2) named_sync(1 + kWgB + acc, kEpiSync);   // the epilogue has read this accumulator
         const uint32_t dcol = tmem_base + acc * MBN;
         for (int st = 0; st < nst; ++st) {
           const int ng = min(kWgKG, nkb - st * kWgKG);
@@ -1028,7 +1028,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int ew = warp & 3;   // TMEM lane quadrant of this warp
-    const uint32_t wbuf = smem_u32(out_stage) + ew * 2 * 4096;
+    const uint32_t wbuf = smem_u32(out_stage) + ew * 4096;
     int tcount = 0;
     bool dead = false;   // after a failed wait: no more waiting or storing, every rendezvous still made
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
@@ -1046,7 +1046,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (tcount + 2 < cta_tiles) named_sync(4 + acc, kEpiSync);   // the MMA warp's tile tcount + 2
+        if (tcount + 2 < cta_tiles) named_sync(1 + kWgB + acc, kEpiSync);   // the MMA warp's tile tcount + 2
       }
     }
     // the stores must have read their staging before the CTA exits
@@ -1304,8 +1304,7 @@ cudaError_t launch_mx_bwd_dw13(const Layer& L, const Bufs& B, void* dWg, void* d
   p.accumulate = acc ? 1 : 0;
   const uint64_t nseg = L.E + L.S;
   CUtensorMap tg, tu;
-  if (!make_tmap_chunked(&tg, dWg, L.d, nseg * L.f, 32, MBN / 64) ||
-      !make_tmap_chunked(&tu, dWu, L.d, nseg * L.f, 32, MBN / 64))
+  if (!make_tmap_chunked(&tg, dWg, L.d, nseg * L.f, 32, 1) || !make_tmap_chunked(&tu, dWu, L.d, nseg * L.f, 32, 1))
     return cudaErrorInvalidValue;
   return wg_launch<ME_DW13>(ta, tb, p, L.num_sms, s, tg, tu);
 }
@@ -1326,7 +1325,7 @@ cudaError_t launch_mx_bwd_dwd(const Layer& L, const Bufs& B, void* dWd, bool acc
   p.k32 = B.tok_k32;
   p.accumulate = acc ? 1 : 0;
   CUtensorMap td;
-  if (!make_tmap_chunked(&td, dWd, L.f, (uint64_t)(L.E + L.S) * L.d, 32, MBN / 64)) return cudaErrorInvalidValue;
+  if (!make_tmap_chunked(&td, dWd, L.f, (uint64_t)(L.E + L.S) * L.d, 32, 1)) return cudaErrorInvalidValue;
   return wg_launch<ME_DWD>(ta, tb, p, L.num_sms, s, td, td);
 }
 
