@@ -702,8 +702,9 @@ __global__ void __launch_bounds__(kMxThreads, 1)
 
 // One 128 x 128 weight-gradient tile (expert e, row tile m, column tile n) from TMEM to the output,
 // by the four epilogue warps (warp ew: rows 32 ew .. 32 ew + 31), each staging its two 32 x 64
-// sub-tiles (128-byte swizzled, 4 KB each, back to back) and storing both with one TMA operation (a
-// 64 x 32 x 2 box of the chunked view of the output; half the store operations of one per sub-tile).
+// sub-tiles in turn through one 4 KB buffer (128-byte swizzled) and storing each with a TMA operation
+// (a 64 x 32 box of the chunked view of the output); the 16 KB this saves over a buffer per sub-tile
+// holds a fourth B stage.
 // nkb == 0: the expert had no token rows; the tile is zero (or left as it was, accumulating).
 template <int EPI>
 __device__ __forceinline__ void wgrad_tile_store(const MxParams& p, const CUtensorMap* tmC, const CUtensorMap* tmC2,
