@@ -47,12 +47,10 @@ namespace moe {
 namespace {
 
 constexpr int MBM = 128, MBN = 128, MBK = 128;
-// Warps: 0 the producer (one thread issues every copy), 1-4 the epilogue (warp w reads TMEM lane
-// quadrant w mod 4), 5 the MMA issuer.
 constexpr int kProd = 1, kEpi = 4;
 constexpr int kMxMmaWarp = kProd + kEpi;
-// Warp 0 issues the TMA loads, warps 1-4 are the epilogue, warp 5 issues the scale copies and MMAs, warp 6
-// tests the ring's full barriers. A test of an mbarrier in the MMA-issuing thread while the tensor pipe runs
+// Warp 0 is the producer (one thread issues every copy), warps 1-4 the epilogue (warp w reads TMEM lane
+// quadrant w mod 4), warp 5 issues the scale copies and MMAs, warp 6 tests the ring's full barriers. A test of an mbarrier in the MMA-issuing thread while the tensor pipe runs
 // costs a few hundred cycles of idle pipe (the pipe queues only ~1.5 MMAs of work), so that thread never
 // tests one: the waiter warp tests each stage's barrier and hands the stage over on a named barrier (one id
 // per ring slot), and the epilogue hands back each accumulator on another. Both hand-overs are rendezvous
