@@ -24,6 +24,11 @@ G_MX = 64      # gate/up interleave of the MXFP8 W13 rows
 
 SMALL_MX = moe_synth.LayerSpec("mxfp8_T300_d512_E16+1_f256_top4_sigmoid", 300, 512, 16, 1, 256, 4, "sigmoid", True,
                                2.5, "mxfp8", None, 31)
+# The shared expert's 640 token rows are five 128-row K groups: more than the weight-gradient kernel keeps
+# resident, so its A operand streams with B and its tiles are dealt one per unit; the routed experts'
+# ~160 rows stay resident.
+STREAMED_MX = moe_synth.LayerSpec("mxfp8_T640_d512_E8+1_f256_top2_softmax", 640, 512, 8, 1, 256, 2, "softmax", True,
+                                  1.0, "mxfp8", None, 33)
 
 
 def np64(t):
@@ -97,8 +102,8 @@ def test_mx_weight_quantisation_byte_exact():
     layer.close()
 
 
-def test_mx_forward_backward_parity_and_reruns():
-    spec = SMALL_MX
+@pytest.mark.parametrize("spec", [SMALL_MX, STREAMED_MX], ids=lambda sp: sp.name)
+def test_mx_forward_backward_parity_and_reruns(spec):
     layer, g, n = setup(spec)
     ctx = layer.new_ctx(spec.T)
     y = layer.forward(g["x"], ctx=ctx)
