@@ -216,7 +216,7 @@ enum { CSRC_PLAIN = 0, CSRC_W13 = 1, CSRC_SEG_GATHER = 2 };
 // 8-byte loads of each row and one 4-byte store of its codes), 4 warps per CTA. Segment modes write
 // each expert's sorted rows at mt_off[e] * 128 (segments padded to 128 rows with zero codes).
 template <int SRC>
-__global__ void __launch_bounds__(128) mx_quant_cols_kernel(const bf16* __restrict__ src, const bf16* __restrict__ src2,
+__global__ void __launch_bounds__(128, 4) mx_quant_cols_kernel(const bf16* __restrict__ src, const bf16* __restrict__ src2,
                                                             const int* __restrict__ row_token,
                                                             const int* __restrict__ off,
                                                             const int* __restrict__ mt_off, int nseg, int W, int f,
