@@ -770,15 +770,16 @@ __device__ __forceinline__ void wgrad_tile_store(const MxParams& p, const CUtens
 // ------------------------------------------------------------------ weight gradients
 // dW[e] (rows: the 2f packed gate/up features or d; columns: d or f) = A^T B over the expert's
 // sorted token rows; A and B are token-axis operands [Rp, W] (MN-major, 32-row scale blocks; each
-// expert's rows start at a multiple of 128 and are zero past its tokens). A unit is (expert e,
-// 128-row output tile m): the CTA keeps the unit's A K groups resident in shared memory (when there
-// are at most kWgA * kWgKG of them) and streams the B groups of every column tile n through a ring,
-// so A is read once per unit instead of once per output tile; an expert with more K groups streams
-// A with B. A stage holds two 128-row K groups (eight MMAs per B stage): the MMA thread's per-stage
-// work (waits, fences, scale copies, commits) leaves the tensor pipe idle, since it queues little
-// more than one MMA ahead, and at four MMAs per stage that overhead doubled the stage time. The
-// CTAs of one expert start their column sweep at different tiles (row tile m at
-// m * n_tiles / m_tiles), spreading their B requests over the expert's tiles.
+// expert's rows start at a multiple of 128 and are zero past its tokens). When an expert's A K groups
+// fit in shared memory (at most kWgA * kWgKG of them), a unit is (expert e, 128-row output tile m):
+// the CTA keeps them resident and streams the B groups of every column tile n through a ring, so A is
+// read once per unit instead of once per output tile; the CTAs of one expert start their column
+// sweep at different tiles (row tile m at m * n_tiles / m_tiles), spreading their B requests over the
+// expert's tiles. An expert with more K groups streams A with B, and its units are single output
+// tiles, dealt round-robin like the rest. A stage holds two 128-row K groups (eight MMAs per B
+// stage): the MMA thread's per-stage work (scale copies, commits, the hand-over) leaves the tensor
+// pipe idle, since it queues little more than one MMA ahead, and at four MMAs per stage that
+// overhead doubled the stage time.
 constexpr int kWgKG = 2;            // 128-row K groups per stage (8 MMAs per B stage)
 constexpr int kWgA = 2, kWgB = 4;   // resident A stages (up to kWgA * kWgKG K groups), B ring stages
 constexpr int kWgStage = kWgKG * MBM * MBK;              // bytes of one operand stage
@@ -789,8 +790,8 @@ constexpr int kWgSmem = kWgScaleRegion + (kWgA + kWgB) * kWgStage + kWgOut + 102
 static_assert(kWgSmem <= 227 * 1024, "shared memory per CTA");
 constexpr int kWgScaleColA = 2 * MBN, kWgScaleColB = kWgScaleColA + 4 * kWgKG * kWgA;   // TMEM scale columns
 
-// Roles as in mx_gemm_kernel; named barriers 1-3 hand over the B ring's slots (a stage's A, when it is
-// loaded, is tested with its B), 4-5 the accumulators.
+// Roles as in mx_gemm_kernel; named barriers 1 .. kWgB hand over the B ring's slots (a stage's A, when it
+// is loaded, is tested with its B), kWgB + 1 and kWgB + 2 the accumulators.
 template <int EPI>
 __global__ void __launch_bounds__(kMxThreads, 1)
     mx_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
