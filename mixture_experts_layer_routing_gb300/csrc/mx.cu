@@ -523,16 +523,18 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           tmem_cp_scales(scol, desc_scale_atom(ssc));
           tmem_cp_scales(scol + 4, desc_scale_atom(ssc + kScaleAtom));
           if (NB == 2 && t.nb == 2) tmem_cp_scales(scol + 8, desc_scale_atom(ssc + 2 * kScaleAtom));
+          // the stage's first descriptors; the others differ by constants (16-byte units inside the
+          // descriptors' 14-bit address field), so little scalar work sits between two MMA issues
+          const uint64_t da0 = desc_kmajor(sa), db0 = B_MN ? desc_mnmajor(sb) : desc_kmajor(sb);
+          const uint32_t acc0 = kb > 0 ? 1u : 0u;
+          const bool two = NB == 2 && t.nb == 2;
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint64_t da = desc_kmajor(sa + k * 32);
-            const uint64_t db = B_MN ? desc_mnmajor(sb + k * 4096) : desc_kmajor(sb + k * 32);
-            mma_mx(dcol, da, db, idesc_mx(0, B_MN, k), scol, scol + 4, (kb > 0 || k > 0) ? 1u : 0u);
-            if (NB == 2 && t.nb == 2) {   // the second B tile: its own accumulator, the same A tile
-              const uint32_t sb1 = sb + MBN * MBK;
-              const uint64_t db1 = B_MN ? desc_mnmajor(sb1 + k * 4096) : desc_kmajor(sb1 + k * 32);
-              mma_mx(dcol + MBN, da, db1, idesc_mx(0, B_MN, k), scol, scol + 8, (kb > 0 || k > 0) ? 1u : 0u);
-            }
+            const uint64_t db = db0 + (uint64_t)((B_MN ? k * 4096 : k * 32) >> 4);
+            mma_mx(dcol, da0 + (uint64_t)(k * 2), db, idesc_mx(0, B_MN, k), scol, scol + 4, k > 0 ? 1u : acc0);
+            if (two)   // the second B tile: its own accumulator, the same A tile
+              mma_mx(dcol + MBN, da0 + (uint64_t)(k * 2), db + (uint64_t)((MBN * MBK) >> 4), idesc_mx(0, B_MN, k), scol,
+                     scol + 8, k > 0 ? 1u : acc0);
           }
           mma_commit(empty0 + 8 * s);
         }
